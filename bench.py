@@ -1,0 +1,389 @@
+"""Benchmark: one decode step of paged attention on GB300 through the pa_v2 C ABI.
+
+A step is the whole hot path for one batch: the cache writer stores every sequence's newest
+token (pa_reshape_and_cache), then pa_v2_decode runs phase 1 (with the single-pass path for
+one-partition sequences) and phase 2.  The default workload is the Llama-style GQA decode
+batch (64 sequences, 32 query / 8 kv heads, head size 128, block size 16, lengths uniform in
+[1, 4096], fp16 query and cache); --workload picks another named workload.
+
+Printed (rank 0, one JSON line): achieved HBM GB/s over the step (value), microseconds per
+step, the phase-1 kernel's roofline fraction against the measured HBM copy bandwidth, an
+end-to-end number through host buffers, SM clocks sampled during the timed region, and the
+fp64 CPU oracle timed on a bounded sample of the same workload.
+
+--impl reference times that oracle alone (the reference arm: there is no reference GPU
+implementation of this path), on the host cores, for the same workload and metric.
+
+Multi-GPU (torchrun): every rank runs its own independent batch (sequences shard across GPUs
+with no data-path exchange); value = bytes of all ranks / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode attn µs/step and achieved HBM GB/s (fraction of GB300 peak), 1 GPU"
+DEFAULT_WORKLOAD = "llama_gqa_decode"
+L2_BYTES = 129 * 1024 * 1024
+KERNEL_SRC = os.path.join(ROOT, "paged_kv_cache_v2_gb300", "csrc", "pa_decode.cu")
+PROFILE_DIR = os.path.join(ROOT, "profiles")
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _kernel_hash() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def _profiled_traffic(workload: str):
+    """DRAM bytes per phase-1 launch from the committed ncu summary, if it was taken on the
+    current kernel source (else None)."""
+    path = os.path.join(PROFILE_DIR, f"pa_v2_phase1_{workload}.md")
+    try:
+        txt = open(path).read()
+    except OSError:
+        return None
+    h = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", txt)
+    b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    if not h or not b or h.group(1) != _kernel_hash():
+        return None
+    return float(b.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _cpu_baseline(wl, seconds: float, threads: int):
+    """Time the fp64 oracle on the first sequences of the workload (all heads) until about
+    `seconds` of work is done; returns (GB/s, description, threads)."""
+    import numpy as np
+
+    import oracle
+
+    lens = wl.seq_lens.numpy()
+    H = wl.num_heads
+    per_tok = wl.num_kv_heads * wl.head_size * wl.kv_elem_bytes * 2
+    qo = 2 * H * wl.head_size * wl.q_elem_bytes
+    done_bytes, done_seqs, t_total = 0, 0, 0.0
+    s = 0
+    while s < wl.num_seqs and t_total < seconds:
+        pairs = np.array([(s, h) for h in range(H)], dtype=np.int32)
+        t0 = time.perf_counter()
+        oracle.decode_workload(wl, pairs=pairs, threads=threads)
+        t_total += time.perf_counter() - t0
+        done_bytes += int(lens[s]) * per_tok + qo
+        done_seqs += 1
+        s += 1
+    gbs = done_bytes / t_total / 1e9 if t_total > 0 else None
+    desc = (f"oracle on sequences 0..{done_seqs - 1} of {wl.num_seqs} (all {H} heads, "
+            f"{int(lens[:done_seqs].sum())} tokens), {t_total:.1f} s")
+    return gbs, desc, done_bytes, t_total
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle, as it stands, on the host cores."""
+    ws, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    import workloads
+
+    threads = len(os.sched_getaffinity(0))
+    wl = workloads.make(args.workload, canaries=False)
+    per_step = []
+    budget = max(0.5, 150.0 / max(1, args.steps + args.warmup))
+    for i in range(args.warmup + args.steps):
+        gbs, desc, nbytes, t = _cpu_baseline(wl, budget, threads)
+        if i >= args.warmup:
+            per_step.append((gbs, nbytes, t, desc))
+    tot_b = sum(x[1] for x in per_step)
+    tot_t = sum(x[2] for x in per_step)
+    value = tot_b / tot_t / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(1e3 * tot_t / len(per_step), 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.q_dtype if wl.kv_cache_dtype == "auto" else "fp8_e4m3",
+        "data": "synthetic (seeded)",
+        "config": {"workload": args.workload, "num_seqs": wl.num_seqs, "num_heads": wl.num_heads,
+                   "num_kv_heads": wl.num_kv_heads, "head_size": wl.head_size,
+                   "block_size": wl.block_size, "kv_cache_dtype": wl.kv_cache_dtype,
+                   "l2": "n/a (host)"},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": per_step[-1][3] + " per step"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+
+    import paged_kv_cache_v2_gb300 as pa
+    import workloads
+
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    pa.load()
+
+    wl = workloads.shard(args.workload, rank, ws, canaries=False) if ws > 1 else \
+        workloads.make(args.workload, canaries=False)
+    S, H, d = wl.query.shape
+    nrot = 2  # rotate between cache copies so no step finds the previous step's pages in L2
+    kcs = [wl.key_cache.to(dev) for _ in range(nrot)]
+    vcs = [wl.value_cache.to(dev) for _ in range(nrot)]
+    q = wl.query.to(dev)
+    bt, sl = wl.block_tables.to(dev), wl.seq_lens.to(dev)
+    nk, nv, slots = wl.new_key.to(dev), wl.new_value.to(dev), wl.slot_mapping.to(dev)
+    slopes = None if wl.alibi_slopes is None else wl.alibi_slopes.to(dev)
+    out = torch.empty_like(q)
+    es, ml, tmp = pa.workspace(S, H, d, wl.max_seq_len, dev)
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        kc, vc = kcs[i % nrot], vcs[i % nrot]
+        pa.pa_reshape_and_cache(nk, nv, kc, vc, slots, wl.kv_cache_dtype, wl.k_scale, wl.v_scale)
+        pa.pa_v2_decode(out, es, ml, tmp, q, kc, vc, wl.num_kv_heads, wl.scale, bt, sl, wl.block_size,
+                        wl.max_seq_len, slopes, wl.kv_cache_dtype, wl.k_scale, wl.v_scale)
+
+    decode_bytes = wl.algorithmic_bytes()
+    step_bytes = decode_bytes + wl.writer_bytes()
+    kv_q_bytes = decode_bytes - S * H * d * wl.q_elem_bytes  # phase-1 share: K, V and Q
+    launches_per_step = 2 + (1 if wl.max_num_partitions > 1 else 0)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if ws > 1:
+            torch.distributed.barrier()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(dev.index) as clocks:
+        t_wall0 = time.perf_counter()
+        for i in range(args.steps):
+            pa.pa_v2_set_timing_events(kev[i][0], kev[i][1])
+            ev[i][0].record(stream)
+            step(args.warmup + i)
+            ev[i][1].record(stream)
+        pa.pa_v2_set_timing_events(None, None)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+    barrier()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    k_ms = [a.elapsed_time(b) for a, b in kev]
+    mean_ms = sum(step_ms) / len(step_ms)
+    if ws > 1:
+        tt = torch.tensor([mean_ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        mean_ms_max = float(tt.item())
+        bb = torch.tensor([float(step_bytes)], device=dev)
+        torch.distributed.all_reduce(bb)
+        all_bytes = float(bb.item())
+    else:
+        mean_ms_max, all_bytes = mean_ms, float(step_bytes)
+    value = all_bytes / (mean_ms_max * 1e-3) / 1e9
+
+    # ---- end to end through host buffers (pinned), same metric --------------------------
+    e2e = None
+    if not args.no_e2e:
+        hq = wl.query.pin_memory()
+        hbt, hsl = wl.block_tables.pin_memory(), wl.seq_lens.pin_memory()
+        hnk, hnv, hslots = wl.new_key.pin_memory(), wl.new_value.pin_memory(), wl.slot_mapping.pin_memory()
+        hout = torch.empty_like(wl.query).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hbt, hsl, hnk, hnv, hslots))
+        d2h = hout.numel() * hout.element_size()
+
+        def e2e_step(i):
+            q.copy_(hq, non_blocking=True)
+            bt.copy_(hbt, non_blocking=True)
+            sl.copy_(hsl, non_blocking=True)
+            nk.copy_(hnk, non_blocking=True)
+            nv.copy_(hnv, non_blocking=True)
+            slots.copy_(hslots, non_blocking=True)
+            step(i)
+            hout.copy_(out, non_blocking=True)
+
+        for i in range(max(1, args.warmup)):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.steps):
+            e2e_step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e_ms = e0.elapsed_time(e1) / args.steps
+        if ws > 1:
+            tt = torch.tensor([e_ms], device=dev)
+            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(tt.item())
+        e2e = {"value": round(all_bytes / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+               "us_per_step": round(e_ms * 1e3, 2), "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h)}
+
+    if rank != 0:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+
+    peak, peak_kind = _peaks()
+    k_mean = sum(k_ms) / len(k_ms)
+    achieved = kv_q_bytes / (k_mean * 1e-3) / 1e9
+    traffic = _profiled_traffic(args.workload)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "us_per_step": round(mean_ms_max * 1e3, 2),
+        "n_gpus": ws,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(mean_ms_max, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": wl.q_dtype if wl.kv_cache_dtype == "auto" else f"{wl.q_dtype}+fp8_e4m3",
+        "data": "synthetic (seeded N(0, sigma) values, random block tables)",
+        "config": {"workload": args.workload, "num_seqs": S, "num_heads": H, "num_kv_heads": wl.num_kv_heads,
+                   "head_size": d, "block_size": wl.block_size, "kv_cache_dtype": wl.kv_cache_dtype,
+                   "tokens": int(wl.seq_lens.sum()), "max_seq_len": wl.max_seq_len,
+                   "bytes_per_step": int(step_bytes), "fraction_of_peak": round(value / peak, 4),
+                   "l2": f"inputs larger than L2 ({decode_bytes / 2**20:.0f} MiB KV per step) and "
+                         f"{nrot} rotating cache copies", "parallelism": f"replicas x{ws} (sequence shards)"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "pa_v2_phase1_kernel", "kernel_us": round(k_mean * 1e3, 2),
+                     "bytes_per_launch": int(kv_q_bytes), "peak_source": f"{peak_kind} hbm_gbs (copy)"},
+        "cpu_baseline": None,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks.summary(),
+        "wall_s_timed_region": round(t_wall, 4),
+    }
+    if ws == 1 and not args.no_cpu_baseline:
+        threads = len(os.sched_getaffinity(0))
+        gbs, desc, _, _ = _cpu_baseline(wl, args.cpu_seconds, threads)
+        line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                                "sample": desc}
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

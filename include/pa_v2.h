@@ -1,0 +1,178 @@
+/*
+ * pa_v2.h -- C ABI of a GB300 (sm_103a) library for PagedAttention V2 single-query decode
+ * attention over a block-paged KV cache, plus the slot-mapping cache writer.
+ *
+ * Every entry point takes plain pointers, sizes and a CUDA stream; nothing here depends on
+ * any framework's tensor types.  Pointers named "device" must point to device memory (or
+ * memory the device can address).  All buffers are owned by the caller: these calls
+ * allocate nothing, never synchronise the stream, and return as soon as the work is
+ * enqueued.  Results are valid in stream order.
+ *
+ * Layouts are row-major C arrays:
+ *   query        [num_seqs][num_heads][head_size]                      q dtype
+ *   output       [num_seqs][num_heads][head_size]                      q dtype
+ *   key_cache    [num_blocks][num_kv_heads][head_size / x][block_size][x]
+ *   value_cache  [num_blocks][num_kv_heads][head_size][block_size]
+ *                x = 16 / (bytes per cache element): 8 for fp16/bf16, 16 for fp8 e4m3.
+ *   block_tables [num_seqs][max_blocks_per_seq]   int32, logical block -> physical block
+ *   seq_lens     [num_seqs]                       int32, tokens per sequence
+ *   exp_sums     [num_seqs][num_heads][max_num_partitions]             float32
+ *   max_logits   [num_seqs][num_heads][max_num_partitions]             float32
+ *   tmp_output   [num_seqs][num_heads][max_num_partitions][head_size]  float32
+ * These are the argument layouts of "paged_attention_v2_pytorch.py" (paged_attention_v2_pytorch)
+ * and the cache views of "paged_attn.py" (split_kv_cache).
+ */
+#ifndef PA_V2_H_
+#define PA_V2_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PA_DT_F16 = 0,
+    PA_DT_BF16 = 1,
+    PA_DT_F32 = 2,
+    PA_DT_FP8_E4M3 = 3
+} pa_dtype;
+
+/* "auto": the cache holds the query dtype; "fp8_e4m3": the cache holds OCP e4m3fn codes. */
+typedef enum {
+    PA_KV_AUTO = 0,
+    PA_KV_FP8_E4M3 = 1
+} pa_kv_cache_dtype;
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1, /* a pointer, size, ratio or scale breaks the contract below */
+    PA_ERR_UNSUPPORTED = 2, /* a valid combination this build does not implement          */
+    PA_ERR_CUDA = 3         /* the CUDA runtime reported an error while enqueueing          */
+} pa_status;
+
+/*
+ * pa_v2_decode -- one decode step of paged attention, two phases.
+ *
+ * Defines: "paged_attention_v2_pytorch.py", paged_attention_v2_pytorch (phase 1: per
+ * sequence s, query head h and 512-token partition p, the scores
+ *   s_t = scale * <q, k_t * k_scale> + (alibi ? alibi_slopes[h] * t : 0),  t = 0 .. L-1,
+ * the partition max m_p, exp-sum l_p = sum exp(s_t - m_p) and weighted V; phase 2: the
+ * log-sum-exp combine), and "paged_attention_v2_triton.py", _paged_attn_v2_reduce_kernel
+ * (out = sum_p exp(m_p - g) l_p tmp_p / sum_p exp(m_p - g) l_p, g = max_p m_p).
+ * Query head h reads kv head h / (num_heads / num_kv_heads) (the GQA view of the query).
+ *
+ * Writes, for every sequence with L = seq_lens[s] tokens and P = ceil(L / 512) partitions:
+ *   max_logits[s][h][p], exp_sums[s][h][p]  for p < P (m_p in natural-log units, absolute
+ *       ALiBi positions); max_logits = -inf and exp_sums = 0 for P <= p < max_num_partitions;
+ *   tmp_output[s][h][p][:] = sum_t exp(s_t - m_p) v_t / l_p  (partition-normalised) for
+ *       p < P when P > 1; left untouched otherwise;
+ *   output[s][h][:] = softmax(s) V in the query dtype; all zeros when L == 0.
+ * Sequences with P == 1 take a single pass: output is written directly, and the p = 0
+ * statistics are still written.
+ *
+ * Arguments:
+ *   output, exp_sums, max_logits, tmp_output   device, caller-owned, layouts above.
+ *   query, key_cache, value_cache               device; key_cache, value_cache and query
+ *                                               16-byte aligned.
+ *   num_seqs (0 .. 65535), num_heads, num_kv_heads (num_heads % num_kv_heads == 0),
+ *   head_size in {64, 80, 96, 112, 120, 128, 192, 256} (the supported sizes listed in
+ *       "paged_attn.py", get_supported_head_sizes); head_size % x == 0.
+ *   scale                 softmax scale (e.g. 1/sqrt(head_size)).
+ *   block_tables          device int32 [num_seqs][max_blocks_per_seq].
+ *   max_blocks_per_seq    >= ceil(max_seq_len / block_size).
+ *   num_blocks            physical blocks in each cache (ids must lie in [0, num_blocks)).
+ *   seq_lens              device int32 [num_seqs]; every entry in [0, max_seq_len].
+ *   block_size            8, 16 or 32 (512 % block_size == 0, "paged_attn.py" forward_decode).
+ *   max_seq_len           upper bound on every seq_lens entry.
+ *   max_num_partitions    >= ceil(max_seq_len / 512) and >= 1; the third extent of the
+ *                         workspace arrays.
+ *   alibi_slopes          device float32 [num_heads], or NULL for no ALiBi bias.
+ *   q_dtype               PA_DT_F16 or PA_DT_BF16 (query and output).
+ *   kv_cache_dtype        PA_KV_AUTO (cache in q_dtype) or PA_KV_FP8_E4M3.
+ *   tmp_dtype             PA_DT_F32 (the layout of tmp_output).
+ *   k_scale, v_scale      > 0, finite; multiply the decoded key and value elements.
+ *   stream                the CUDA stream the kernels are enqueued on.
+ *
+ * Errors: PA_ERR_INVALID_ARG / PA_ERR_UNSUPPORTED are returned before anything is
+ * enqueued.  Table contents are not read on the host: a block id outside [0, num_blocks),
+ * a sequence longer than its table row or than max_num_partitions * 512, or a negative
+ * length is skipped on the device (those tokens are masked out) and recorded in the flags
+ * pa_get_device_errors returns; with the environment variable PA_CHECK=1 the tables are
+ * instead copied to the host and checked first (this synchronises the stream) and a bad
+ * entry returns PA_ERR_INVALID_ARG.  PA_ERR_CUDA reports a launch error.
+ */
+PA_API pa_status pa_v2_decode(void* output, float* exp_sums, float* max_logits, void* tmp_output,
+                       const void* query, const void* key_cache, const void* value_cache,
+                       int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                       float scale, const int32_t* block_tables, int max_blocks_per_seq,
+                       int num_blocks, const int32_t* seq_lens, int block_size,
+                       int max_seq_len, int max_num_partitions, const float* alibi_slopes,
+                       pa_dtype q_dtype, pa_kv_cache_dtype kv_cache_dtype, pa_dtype tmp_dtype,
+                       float k_scale, float v_scale, cudaStream_t stream);
+
+/*
+ * pa_reshape_and_cache -- scatter new key/value rows into the paged caches by slot.
+ *
+ * Defines: "paged_attn.py", write_to_paged_cache (-> reshape_and_cache with the flattened
+ * slot_mapping) and split_kv_cache (the cache views).  For token t with
+ * slot = slot_mapping[t] >= 0, b = slot / block_size, o = slot % block_size:
+ *   key_cache[b][h][i / x][o][i % x] = enc(key[t][h][i]),
+ *   value_cache[b][h][i][o]         = enc(value[t][h][i]).
+ * enc is a bitwise copy when kv_cache_dtype == PA_KV_AUTO, and
+ * round-to-nearest-even-with-saturation to e4m3fn of (float)x / k_scale (resp. v_scale),
+ * the division in IEEE binary32, when kv_cache_dtype == PA_KV_FP8_E4M3.
+ * A negative slot skips the token.
+ *
+ * Arguments:
+ *   key, value            device [num_tokens][num_kv_heads][head_size] rows in src_dtype;
+ *                         consecutive tokens are key_stride_t / value_stride_t ELEMENTS
+ *                         apart (heads and head elements are contiguous inside a row).
+ *   key_cache, value_cache  device, layouts above, 16-byte aligned.
+ *   slot_mapping          device int64 [num_tokens].
+ *   num_tokens >= 0, num_kv_heads > 0, head_size as for pa_v2_decode, block_size 8/16/32,
+ *   num_blocks > 0; src_dtype PA_DT_F16 or PA_DT_BF16; k_scale, v_scale > 0 and finite.
+ * Errors: as for pa_v2_decode; a slot at or beyond num_blocks * block_size is skipped on
+ * the device and recorded in the device error flags.
+ */
+PA_API pa_status pa_reshape_and_cache(const void* key, const void* value, int64_t key_stride_t,
+                               int64_t value_stride_t, void* key_cache, void* value_cache,
+                               const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                               int head_size, int block_size, int num_blocks,
+                               pa_dtype src_dtype, pa_kv_cache_dtype kv_cache_dtype,
+                               float k_scale, float v_scale, cudaStream_t stream);
+
+/* Tokens per partition: 512 ("paged_attention_v2_pytorch.py", _PARTITION_SIZE). */
+PA_API int pa_v2_partition_size(void);
+
+/* A static, human-readable name for a status code. */
+PA_API const char* pa_status_string(pa_status status);
+
+/* Device-side error flags (bit 0: a block id outside [0, num_blocks) or a table row too
+ * short; bit 1: a sequence longer than max_num_partitions * 512 or a negative length;
+ * bit 2: a bounded wait for a shared-memory copy gave up; bit 3: a slot outside the
+ * cache).  Reads the flags of the current device (this synchronises the device) into
+ * *flags, and clears them when reset != 0.  Not part of the pages' interface: it reports
+ * what the kernels skipped instead of faulting. */
+PA_API pa_status pa_get_device_errors(uint32_t* flags, int reset);
+
+/* Timing hook (not part of the pages' interface): while begin and end are non-NULL, every
+ * pa_v2_decode call records `begin` on its stream just before the phase-1 kernel launch and
+ * `end` just after it, so a caller can time that kernel alone.  Pass NULL, NULL to stop.
+ * Process-wide and not thread-safe. */
+PA_API pa_status pa_v2_set_timing_events(cudaEvent_t begin, cudaEvent_t end);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_V2_H_ */

@@ -1,0 +1,199 @@
+"""paged_kv_cache_v2_gb300 -- Python binding of the pa_v2 C ABI (PagedAttention V2 decode on
+GB300).
+
+Argument marshalling only: every step of the computation runs in the CUDA kernels of
+``libpa_v2.so`` (built from ``csrc/``).  PyTorch supplies device memory and streams.  There
+is no fallback: if the library cannot be loaded, importing the binding functions fails.
+
+Entry points mirror ``include/pa_v2.h``:
+
+* ``pa_v2_decode(output, exp_sums, max_logits, tmp_output, query, key_cache, value_cache,
+  num_kv_heads, scale, block_tables, seq_lens, block_size, max_seq_len, alibi_slopes,
+  kv_cache_dtype, k_scale, v_scale)`` -- the op signature of "paged_attention_v2_pytorch.py"
+  (paged_attention_v2_pytorch) without its unused tensor-parallel / block-sparse arguments.
+* ``pa_reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, kv_cache_dtype,
+  k_scale, v_scale)`` -- "paged_attn.py" write_to_paged_cache.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+from . import _build
+
+PARTITION_SIZE = 512
+
+PA_DT_F16, PA_DT_BF16, PA_DT_F32, PA_DT_FP8_E4M3 = 0, 1, 2, 3
+PA_KV_AUTO, PA_KV_FP8_E4M3 = 0, 1
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported combination", 3: "CUDA error"}
+
+_lib = None
+
+
+class PagedAttentionError(RuntimeError):
+    def __init__(self, call: str, status: int):
+        super().__init__(f"{call} returned {status} ({STATUS.get(status, 'unknown')})")
+        self.status = status
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libpa_v2.so (building it first if it is missing or stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.build() if build_if_missing else _build.LIB
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library not built: {path}")
+    lib = ctypes.CDLL(path)
+    P, i32, i64, f32, u32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_uint32
+    lib.pa_v2_decode.restype = i32
+    lib.pa_v2_decode.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, f32, P, i32, i32, P, i32, i32,
+                                 i32, P, i32, i32, i32, f32, f32, P]
+    lib.pa_reshape_and_cache.restype = i32
+    lib.pa_reshape_and_cache.argtypes = [P, P, i64, i64, P, P, P, i32, i32, i32, i32, i32, i32, i32,
+                                         f32, f32, P]
+    lib.pa_v2_partition_size.restype = i32
+    lib.pa_v2_partition_size.argtypes = []
+    lib.pa_status_string.restype = ctypes.c_char_p
+    lib.pa_status_string.argtypes = [i32]
+    lib.pa_get_device_errors.restype = i32
+    lib.pa_get_device_errors.argtypes = [ctypes.POINTER(u32), i32]
+    lib.pa_v2_set_timing_events.restype = i32
+    lib.pa_v2_set_timing_events.argtypes = [P, P]
+    _lib = lib
+    return lib
+
+
+def _dt(t: torch.dtype) -> int:
+    if t == torch.float16:
+        return PA_DT_F16
+    if t == torch.bfloat16:
+        return PA_DT_BF16
+    raise TypeError(f"unsupported query dtype {t}")
+
+
+def _kv(kv_cache_dtype: str) -> int:
+    if kv_cache_dtype in ("auto", None):
+        return PA_KV_AUTO
+    if kv_cache_dtype in ("fp8", "fp8_e4m3"):
+        return PA_KV_FP8_E4M3
+    raise ValueError(f"unsupported kv_cache_dtype {kv_cache_dtype!r}")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(call: str, st: int) -> None:
+    if st != 0:
+        raise PagedAttentionError(call, st)
+
+
+def pa_v2_decode(output: torch.Tensor, exp_sums: torch.Tensor, max_logits: torch.Tensor,
+                 tmp_output: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                 value_cache: torch.Tensor, num_kv_heads: int, scale: float,
+                 block_tables: torch.Tensor, seq_lens: torch.Tensor, block_size: int,
+                 max_seq_len: int, alibi_slopes: Optional[torch.Tensor] = None,
+                 kv_cache_dtype: str = "auto", k_scale: float = 1.0, v_scale: float = 1.0,
+                 num_blocks: Optional[int] = None, stream=None) -> None:
+    """Enqueue one decode step (phase 1 + phase 2) on ``stream`` (default: current stream).
+
+    Shapes: query/output [S, H, d]; key_cache [NB, Hk, d/x, bs, x]; value_cache
+    [NB, Hk, d, bs]; block_tables int32 [S, W]; seq_lens int32 [S]; exp_sums/max_logits
+    fp32 [S, H, P]; tmp_output fp32 [S, H, P, d].  The fp8 cache may be passed as uint8
+    codes or as torch.float8_e4m3fn.
+    """
+    lib = load()
+    for name, t in (("output", output), ("exp_sums", exp_sums), ("max_logits", max_logits),
+                    ("tmp_output", tmp_output), ("query", query), ("key_cache", key_cache),
+                    ("value_cache", value_cache), ("block_tables", block_tables),
+                    ("seq_lens", seq_lens)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_tables and seq_lens must be int32")
+    if exp_sums.dtype != torch.float32 or max_logits.dtype != torch.float32:
+        raise TypeError("exp_sums and max_logits must be float32")
+    if tmp_output.dtype != torch.float32:
+        raise TypeError("tmp_output must be float32")
+    if output.dtype != query.dtype:
+        raise TypeError("output must have the query dtype")
+    if alibi_slopes is not None and (alibi_slopes.dtype != torch.float32 or not alibi_slopes.is_cuda):
+        raise TypeError("alibi_slopes must be a float32 CUDA tensor")
+    S, H, d = query.shape
+    if num_blocks is None:
+        num_blocks = key_cache.shape[0]
+    st = lib.pa_v2_decode(_ptr(output), _ptr(exp_sums), _ptr(max_logits), _ptr(tmp_output),
+                          _ptr(query), _ptr(key_cache), _ptr(value_cache), S, H, int(num_kv_heads),
+                          d, float(scale), _ptr(block_tables), int(block_tables.shape[1]),
+                          int(num_blocks), _ptr(seq_lens), int(block_size), int(max_seq_len),
+                          int(tmp_output.shape[2]), _ptr(alibi_slopes), _dt(query.dtype),
+                          _kv(kv_cache_dtype), PA_DT_F32, float(k_scale), float(v_scale),
+                          _stream(stream))
+    _check("pa_v2_decode", st)
+
+
+def pa_reshape_and_cache(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor,
+                         value_cache: torch.Tensor, slot_mapping: torch.Tensor,
+                         kv_cache_dtype: str = "auto", k_scale: float = 1.0, v_scale: float = 1.0,
+                         stream=None) -> None:
+    """Enqueue the slot-mapping cache writer: key/value [T, Hk, d] rows into the caches."""
+    lib = load()
+    if key.dim() != 3 or value.shape != key.shape:
+        raise ValueError("key and value must be [num_tokens, num_kv_heads, head_size]")
+    T, Hk, d = key.shape
+    if key.stride(2) != 1 or key.stride(1) != d or value.stride(2) != 1 or value.stride(1) != d:
+        raise ValueError("key/value rows must be contiguous [num_kv_heads, head_size]")
+    if slot_mapping.dtype != torch.int64 or not slot_mapping.is_contiguous():
+        raise TypeError("slot_mapping must be a contiguous int64 tensor")
+    bs = value_cache.shape[-1]
+    st = lib.pa_reshape_and_cache(_ptr(key), _ptr(value), key.stride(0), value.stride(0),
+                                  _ptr(key_cache), _ptr(value_cache), _ptr(slot_mapping), T, Hk, d,
+                                  int(bs), int(key_cache.shape[0]), _dt(key.dtype),
+                                  _kv(kv_cache_dtype), float(k_scale), float(v_scale),
+                                  _stream(stream))
+    _check("pa_reshape_and_cache", st)
+
+
+def pa_v2_partition_size() -> int:
+    return int(load().pa_v2_partition_size())
+
+
+def pa_status_string(status: int) -> str:
+    return load().pa_status_string(int(status)).decode()
+
+
+def pa_get_device_errors(reset: bool = True) -> int:
+    """Device-side error flags of the current device (synchronises the device)."""
+    v = ctypes.c_uint32(0)
+    _check("pa_get_device_errors", load().pa_get_device_errors(ctypes.byref(v), 1 if reset else 0))
+    return int(v.value)
+
+
+def pa_v2_set_timing_events(begin: Optional[torch.cuda.Event], end: Optional[torch.cuda.Event]) -> None:
+    """Record ``begin``/``end`` around every later phase-1 launch (None, None to stop)."""
+    b = None if begin is None else ctypes.c_void_p(begin.cuda_event)
+    e = None if end is None else ctypes.c_void_p(end.cuda_event)
+    _check("pa_v2_set_timing_events", load().pa_v2_set_timing_events(b, e))
+
+
+def workspace(num_seqs: int, num_heads: int, head_size: int, max_seq_len: int, device) -> tuple:
+    """Allocate (exp_sums, max_logits, tmp_output) for a decode step (caller-owned)."""
+    P = max(1, -(-max_seq_len // PARTITION_SIZE))
+    es = torch.empty((num_seqs, num_heads, P), dtype=torch.float32, device=device)
+    ml = torch.empty_like(es)
+    tmp = torch.empty((num_seqs, num_heads, P, head_size), dtype=torch.float32, device=device)
+    return es, ml, tmp

@@ -1,0 +1,944 @@
+// pa_decode.cu -- PagedAttention V2 single-query decode for sm_103a (GB300).
+//
+// What is computed ("paged_attention_v2_pytorch.py", paged_attention_v2_pytorch, and
+// "paged_attention_v2_triton.py", _paged_attn_v2_reduce_kernel): for every sequence s,
+// query head h and 512-token partition p, the scores s_t = scale * <q, k_t> * k_scale
+// (+ slope_h * t), the partition max m_p, exp-sum l_p and normalised weighted V; then the
+// log-sum-exp combine of the partitions into the output.
+//
+// How (GB300-first; the pages' PyTorch/Triton code is prior art, not the blueprint):
+//  * Phase 1, one CTA per (partition, kv head, <= 8 query heads of that kv head, sequence):
+//    every K and V byte of a partition is read from HBM once and serves all query heads
+//    of its GQA group.  Four warps each own a ring of shared-memory slots; a slot holds
+//    the K page and the V page of one (or two, for block size 8) cache block(s).  Each
+//    page is one contiguous span (head_size * block_size elements), so it moves with ONE
+//    1-D bulk copy (TMA engine, L2 evict-first) that completes on the slot's mbarrier; the
+//    warp refills a slot as soon as it has consumed it, keeping several pages in flight.
+//  * Scores and P.V run on the tensor cores with warp-level m16n8k16 MMA (fp32
+//    accumulate): 16 tokens x 8 query heads per MMA, K rows fed straight from the x-packed
+//    page with ldmatrix, V^T rows straight from the token-contiguous page, P moved from
+//    the score fragment into the P.V operand with movmatrix.  fp8 e4m3 pages are widened
+//    to f16/bf16 in registers (exact); k_scale and the softmax scale fold into one fp32
+//    multiplier on the scores, v_scale into the final normalisation.
+//  * The online softmax runs per warp in the base-2 domain; the warps' (m, l, acc) merge
+//    through shared memory at the end of the partition.  A one-partition sequence writes
+//    its normalised output directly (single pass); longer ones write tmp_output and the
+//    statistics for phase 2.
+//  * Phase 2, one CTA per (query head, sequence) with more than one partition: global max,
+//    weights exp(m_p - g) l_p, and the weighted sum of the tmp_output rows (float4 loads,
+//    eight warps over the partitions).  It is launched with programmatic dependent launch
+//    so its launch overlaps the tail of phase 1.
+//  * No spin-wait is unbounded: every mbarrier wait gives up after 2 s, records a device
+//    error flag and drains its own copies (again bounded) before the block exits.  Bad
+//    table entries are masked and flagged instead of being dereferenced.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "pa_v2.h"
+#include "pa_internal.h"
+#include "pa_ptx.cuh"
+
+namespace pa {
+
+static __device__ unsigned int g_device_errors = 0;
+
+constexpr int kPartition = 512;
+constexpr int kWarps = 4;              // phase-1 warps per CTA
+constexpr int kMaxHeadsPerCta = 8;     // the MMA N dimension
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct Phase1Params {
+    void* out;
+    float* exp_sums;
+    float* max_logits;
+    float* tmp_out;
+    const void* query;
+    const uint8_t* kcache;
+    const uint8_t* vcache;
+    const int32_t* block_tables;
+    const int32_t* seq_lens;
+    const float* alibi;
+    int H, Hk, G, ngroups, bs, mbps, num_blocks, Pmax, nstage;
+    uint32_t ring_bytes;  // kWarps * nstage * slot bytes
+    float qk_scale_log2;  // scale * k_scale * log2(e)
+    float v_scale;
+};
+
+struct Phase2Params {
+    void* out;
+    const float* exp_sums;
+    const float* max_logits;
+    const float* tmp_out;
+    const int32_t* seq_lens;
+    int H, D, Pmax;
+};
+
+__device__ __forceinline__ void flag_error(unsigned int bit) { atomicOr(&g_device_errors, bit); }
+
+// Token order of the 16 MMA rows for fp8 pages.  An fp8 V row hands each thread four
+// consecutive tokens, while the P operand (via movmatrix) hands thread t logical rows
+// {2t, 2t+1, 8+2t, 9+2t}; this order makes both agree (with the two halves swapped for
+// t >= 2) and keeps the K-row ldmatrix free of bank conflicts.
+__device__ __constant__ int8_t c_fp8_row_token[16] = {0, 1, 4, 5, 10, 11, 14, 15,
+                                                      2, 3, 6, 7, 8, 9, 12, 13};
+
+template <bool BF16>
+__device__ __forceinline__ void store_out(void* out, int64_t idx, float v) {
+    if constexpr (BF16)
+        reinterpret_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
+    else
+        reinterpret_cast<__half*>(out)[idx] = __float2half_rn(v);
+}
+
+// ---------------------------------------------------------------------------------------
+// Phase 1
+// ---------------------------------------------------------------------------------------
+template <bool BF16, int KVB, int D>
+__global__ void __launch_bounds__(kWarps * 32)
+pa_v2_phase1_kernel(const Phase1Params p) {
+    constexpr bool FP8 = (KVB == 1);
+    constexpr int NK = (D + 15) / 16;      // 16-wide steps over the head dimension
+    constexpr bool HALF_STEP = (D % 16) != 0;  // head_size 120: last step has 8 elements
+    static_assert(!(FP8 && HALF_STEP), "fp8 pages need head_size % 16 == 0");
+    extern __shared__ __align__(128) uint8_t smem[];
+
+    const int part = blockIdx.x;
+    const int kvh = blockIdx.y / p.ngroups;
+    const int grp = blockIdx.y - kvh * p.ngroups;
+    const int s = blockIdx.z;
+    const int h0 = kvh * p.G + grp * kMaxHeadsPerCta;
+    const int nh = min(kMaxHeadsPerCta, p.G - grp * kMaxHeadsPerCta);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int H = p.H;
+
+    griddep_wait();  // the cache writer (if it ran just before) must be visible
+
+    const int L = p.seq_lens[s];
+    const int P = L > 0 ? (L + kPartition - 1) / kPartition : 0;
+    if (threadIdx.x == 0 && part == 0 && (L < 0 || P > p.Pmax)) flag_error(2u);
+    if (part >= P) {
+        // Partition past the end of the sequence (or an empty sequence).
+        if (threadIdx.x < nh) {
+            const int64_t sidx = ((int64_t)s * H + h0 + threadIdx.x) * p.Pmax + part;
+            p.max_logits[sidx] = -INFINITY;
+            p.exp_sums[sidx] = 0.f;
+        }
+        if (part == 0) {
+            for (int i = threadIdx.x; i < nh * D; i += blockDim.x)
+                store_out<BF16>(p.out, ((int64_t)s * H + h0) * D + i, 0.f);
+        }
+        griddep_launch_dependents();
+        return;
+    }
+
+    const int bs = p.bs;
+    const int t0 = part * kPartition;
+    const int t1 = min(L, t0 + kPartition);
+    const int lb0 = t0 / bs;
+    const int npages = (t1 - 1) / bs - lb0 + 1;
+    const int pps = bs >= 16 ? 1 : 16 / bs;  // pages per slot
+    const int slot_tokens = pps * bs;
+    const int tiles_per_slot = slot_tokens / 16;
+    const int nslots = (npages + pps - 1) / pps;
+    const uint32_t page_bytes = (uint32_t)D * bs * KVB;
+    const uint32_t slot_bytes = 2u * pps * page_bytes;
+    const int nstage = p.nstage;
+
+    uint8_t* ring = smem + (size_t)warp * nstage * slot_bytes;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.ring_bytes) + warp * nstage;
+    float* red_m = reinterpret_cast<float*>(smem + p.ring_bytes + kWarps * nstage * sizeof(uint64_t));
+    float* red_l = red_m + kWarps * kMaxHeadsPerCta;
+    float* fin_m = red_l + kWarps * kMaxHeadsPerCta;  // [8] merged max (log2 units)
+    float* fin_l = fin_m + kMaxHeadsPerCta;           // [8] merged exp-sum
+
+    // Physical block ids of this partition: lane i holds pages i and 32 + i.
+    int bid0 = -1, bid1 = -1;
+    {
+        const int32_t* row = p.block_tables + (int64_t)s * p.mbps;
+        const int la = lb0 + lane, lbb = lb0 + 32 + lane;
+        if (lane < npages) {
+            if (la < p.mbps) {
+                const int b = row[la];
+                if (b >= 0 && b < p.num_blocks) bid0 = b; else flag_error(1u);
+            } else flag_error(1u);
+        }
+        if (32 + lane < npages) {
+            if (lbb < p.mbps) {
+                const int b = row[lbb];
+                if (b >= 0 && b < p.num_blocks) bid1 = b; else flag_error(1u);
+            } else flag_error(1u);
+        }
+    }
+
+    if (lane == 0) {
+        for (int k = 0; k < nstage; ++k) mbar_init(&bars[k], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+
+    const uint64_t policy = l2_policy_evict_first();
+    const uint8_t* kc_head = p.kcache + (size_t)kvh * page_bytes;
+    const uint8_t* vc_head = p.vcache + (size_t)kvh * page_bytes;
+    const size_t block_stride = (size_t)p.Hk * page_bytes;
+
+    // Fill ring position k % nstage with this warp's k-th slot (global slot warp + k*kWarps).
+    auto issue = [&](int k) {
+        const int j = warp + k * kWarps;
+        int b[2] = {-1, -1};
+        uint32_t bytes = 0;
+#pragma unroll
+        for (int pg = 0; pg < 2; ++pg) {
+            if (pg < pps) {
+                const int page = j * pps + pg;
+                const int v = __shfl_sync(0xffffffffu, page < 32 ? bid0 : bid1, page & 31);
+                b[pg] = page < npages ? v : -1;
+                if (b[pg] >= 0) bytes += 2u * page_bytes;
+            }
+        }
+        if (lane == 0) {
+            uint64_t* bar = &bars[k % nstage];
+            uint8_t* kdst = ring + (size_t)(k % nstage) * slot_bytes;
+            uint8_t* vdst = kdst + (size_t)pps * page_bytes;
+            mbar_arrive_expect_tx(bar, bytes);
+            for (int pg = 0; pg < pps; ++pg) {
+                if (b[pg] >= 0) {
+                    bulk_g2s(kdst + pg * page_bytes, kc_head + (size_t)b[pg] * block_stride, page_bytes, bar, policy);
+                    bulk_g2s(vdst + pg * page_bytes, vc_head + (size_t)b[pg] * block_stride, page_bytes, bar, policy);
+                }
+            }
+        }
+    };
+
+    const int my_slots = nslots > warp ? (nslots - warp + kWarps - 1) / kWarps : 0;
+    for (int k = 0; k < nstage && k < my_slots; ++k) issue(k);
+
+    // ---- query fragments (MMA B operand: k = head dim, n = query head g) -------------------
+    uint32_t qf[NK][2];
+    {
+        const bool live = g < nh;
+        const uint16_t* qrow = reinterpret_cast<const uint16_t*>(p.query) + ((int64_t)s * H + h0 + g) * D;
+#pragma unroll
+        for (int kk = 0; kk < NK; ++kk) {
+            uint32_t b0 = 0, b1 = 0;
+            if (live) {
+                if constexpr (FP8) {
+                    // fp8 rows deliver head-dim elements 4t..4t+3 of the 16-wide step.
+                    const uint2 v = *reinterpret_cast<const uint2*>(qrow + kk * 16 + 4 * t);
+                    b0 = v.x;
+                    b1 = v.y;
+                } else {
+                    b0 = *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 2 * t);
+                    if (!(HALF_STEP && kk == NK - 1))
+                        b1 = *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 8 + 2 * t);
+                }
+            }
+            qf[kk][0] = b0;
+            qf[kk][1] = b1;
+        }
+    }
+    // ALiBi slopes of this thread's two head columns (2t, 2t+1), base-2 units.
+    float sl0 = 0.f, sl1 = 0.f;
+    if (p.alibi != nullptr) {
+        if (2 * t < nh) sl0 = p.alibi[h0 + 2 * t] * kLog2e;
+        if (2 * t + 1 < nh) sl1 = p.alibi[h0 + 2 * t + 1] * kLog2e;
+    }
+    const int tref = t1 - 1;  // ALiBi positions are taken relative to the partition's last token
+
+    // Per-lane ldmatrix row offsets inside a slot (bytes), tile 0.
+    // K rows: lane -> (row within the 16-token tile, chunk offset).
+    int k_tok, k_chunk;
+    if constexpr (FP8) {
+        k_tok = c_fp8_row_token[(lane & 7) + 8 * ((lane >> 3) & 1)];
+        k_chunk = 0;
+    } else {
+        k_tok = (lane & 7) + 8 * ((lane >> 3) & 1);
+        k_chunk = lane >> 4;
+    }
+    // Physical tokens of this thread's two MMA rows (g, g + 8).
+    const int tokA = FP8 ? c_fp8_row_token[g] : g;
+    const int tokB = FP8 ? c_fp8_row_token[g + 8] : g + 8;
+
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float acc[NK][4];
+#pragma unroll
+    for (int i = 0; i < NK; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+
+    bool aborted = false;
+    int issued = min(nstage, my_slots);
+    for (int k = 0; k < my_slots; ++k) {
+        uint64_t* bar = &bars[k % nstage];
+        if (!mbar_wait_bounded(bar, (uint32_t)((k / nstage) & 1), kWaitLimitNs)) {
+            if (lane == 0) flag_error(4u);
+            aborted = true;
+            break;
+        }
+        const int j = warp + k * kWarps;
+        const uint8_t* kslot = ring + (size_t)(k % nstage) * slot_bytes;
+        const uint8_t* vslot = kslot + (size_t)pps * page_bytes;
+        const uint32_t kbase = smem_addr(kslot), vbase = smem_addr(vslot);
+        // page validity bits of this slot
+        uint32_t okmask = 0;
+#pragma unroll
+        for (int pg = 0; pg < 2; ++pg) {
+            if (pg < pps) {
+                const int page = j * pps + pg;
+                const int v = __shfl_sync(0xffffffffu, page < 32 ? bid0 : bid1, page & 31);
+                if (page < npages && v >= 0) okmask |= 1u << pg;
+            }
+        }
+        const int stok0 = t0 + j * slot_tokens;
+
+        for (int tile = 0; tile < tiles_per_slot; ++tile) {
+            const int ttok0 = stok0 + tile * 16;
+            const int lim = t1 - ttok0;  // tokens [0, lim) of the tile are in range
+            if (lim <= 0) break;
+            const bool full = lim >= 16 && okmask == (pps == 1 ? 1u : 3u);
+            // token validity inside the tile (tile-local index)
+            auto tok_ok = [&](int tok) -> bool {
+                const int pg = pps == 1 ? 0 : (tok >> 3);
+                return tok < lim && ((okmask >> pg) & 1u);
+            };
+
+            // ---- S^T = K . Q^T for 16 tokens x 8 heads ------------------------------------
+            uint32_t krow;
+            if (pps == 1)
+                krow = kbase + (uint32_t)(k_chunk * bs + tile * 16 + k_tok) * 16u;
+            else
+                krow = kbase + (uint32_t)(k_tok >> 3) * page_bytes + (uint32_t)(k_chunk * bs + (k_tok & 7)) * 16u;
+            float sc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kk = 0; kk < NK; ++kk) {
+                uint32_t a0, a1, a2, a3;
+                if constexpr (FP8) {
+                    uint32_t r0, r1;
+                    ldsm_x2(krow + (uint32_t)kk * 16u * bs, r0, r1);
+                    a0 = e4m3x2_to_mma<BF16>(lo16(r0));
+                    a2 = e4m3x2_to_mma<BF16>(hi16(r0));
+                    a1 = e4m3x2_to_mma<BF16>(lo16(r1));
+                    a3 = e4m3x2_to_mma<BF16>(hi16(r1));
+                } else {
+                    if (HALF_STEP && kk == NK - 1) {
+                        ldsm_x2(krow + (uint32_t)kk * 32u * bs, a0, a1);
+                        a2 = a3 = 0u;
+                    } else {
+                        ldsm_x4(krow + (uint32_t)kk * 32u * bs, a0, a1, a2, a3);
+                    }
+                }
+                mma16816<BF16>(sc, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+            }
+
+            // ---- scores in base-2 units, masking, online softmax ---------------------------
+            float s0 = sc[0] * p.qk_scale_log2, s1 = sc[1] * p.qk_scale_log2;
+            float s2 = sc[2] * p.qk_scale_log2, s3 = sc[3] * p.qk_scale_log2;
+            if (p.alibi != nullptr) {
+                const float ra = (float)(ttok0 + tokA - tref), rb = (float)(ttok0 + tokB - tref);
+                s0 = fmaf(sl0, ra, s0);
+                s1 = fmaf(sl1, ra, s1);
+                s2 = fmaf(sl0, rb, s2);
+                s3 = fmaf(sl1, rb, s3);
+            }
+            if (!full) {
+                if (!tok_ok(tokA)) s0 = s1 = -INFINITY;
+                if (!tok_ok(tokB)) s2 = s3 = -INFINITY;
+            }
+            float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+            }
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            const float base0 = mn0 == -INFINITY ? 0.f : mn0;
+            const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+            const float al0 = ex2(m0 - base0), al1 = ex2(m1 - base1);  // m = -inf -> 0
+            const float p0 = ex2(s0 - base0), p1 = ex2(s1 - base1);
+            const float p2 = ex2(s2 - base0), p3 = ex2(s3 - base1);
+            l0 = fmaf(l0, al0, p0 + p2);
+            l1 = fmaf(l1, al1, p1 + p3);
+            m0 = mn0;
+            m1 = mn1;
+#pragma unroll
+            for (int i = 0; i < NK; ++i) {
+                acc[i][0] *= al0;
+                acc[i][1] *= al1;
+                acc[i][2] *= al0;
+                acc[i][3] *= al1;
+            }
+
+            // ---- P into the B operand of O^T += V^T . P^T ----------------------------------
+            const uint32_t pb0 = movm_trans(pack2<BF16>(p0, p1));
+            const uint32_t pb1 = movm_trans(pack2<BF16>(p2, p3));
+            uint32_t pl0 = 0, pl1 = 0;
+            if constexpr (BF16) {
+                // bf16 keeps 8 significant bits; add the rounding residual as a second term
+                // so P enters the product with ~16 bits, as with fp16.
+                const float q0 = p0 - __bfloat162float(__float2bfloat16_rn(p0));
+                const float q1 = p1 - __bfloat162float(__float2bfloat16_rn(p1));
+                const float q2 = p2 - __bfloat162float(__float2bfloat16_rn(p2));
+                const float q3 = p3 - __bfloat162float(__float2bfloat16_rn(p3));
+                pl0 = movm_trans(pack2<true>(q0, q1));
+                pl1 = movm_trans(pack2<true>(q2, q3));
+            }
+
+            // ---- O^T += V^T . P^T over the head dimension ---------------------------------
+            if constexpr (!FP8) {
+                // lane -> (V row within the 16-row tile, token half)
+                const int vr = (lane & 7) + 8 * ((lane >> 3) & 1);
+                const int half = lane >> 4;
+                uint32_t vpage, vtok;
+                if (pps == 1) {
+                    vpage = vbase;
+                    vtok = (uint32_t)(tile * 16 + 8 * half);
+                } else {
+                    vpage = vbase + (uint32_t)half * page_bytes;
+                    vtok = 0;
+                }
+                // masks for this thread's token columns: a0/a1 tokens (2t, 2t+1), a2/a3 (8+2t, 9+2t)
+                uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+                if (!full) {
+                    mlo = (tok_ok(2 * t) ? 0x0000ffffu : 0u) | (tok_ok(2 * t + 1) ? 0xffff0000u : 0u);
+                    mhi = (tok_ok(8 + 2 * t) ? 0x0000ffffu : 0u) | (tok_ok(9 + 2 * t) ? 0xffff0000u : 0u);
+                }
+#pragma unroll
+                for (int mt = 0; mt < NK; ++mt) {
+                    int row = mt * 16 + vr;
+                    if (HALF_STEP && mt == NK - 1) row = min(row, D - 1);
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(vpage + ((uint32_t)row * bs + vtok) * 2u, a0, a1, a2, a3);
+                    a0 &= mlo;
+                    a1 &= mlo;
+                    a2 &= mhi;
+                    a3 &= mhi;
+                    mma16816<BF16>(acc[mt], a0, a1, a2, a3, pb0, pb1);
+                    if constexpr (BF16) mma16816<BF16>(acc[mt], a0, a1, a2, a3, pl0, pl1);
+                }
+            } else {
+                // thread holds tokens 4t..4t+3 of rows g and g+8 of each 16-row tile
+                uint32_t vpage, vtok;
+                if (pps == 1) {
+                    vpage = vbase;
+                    vtok = (uint32_t)(tile * 16 + 4 * t);
+                } else {
+                    vpage = vbase + (uint32_t)(t >> 1) * page_bytes;
+                    vtok = (uint32_t)((4 * t) & 7);
+                }
+                uint32_t bmask = 0xffffffffu;
+                if (!full) {
+                    bmask = 0;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if (tok_ok(4 * t + i)) bmask |= 0xffu << (8 * i);
+                }
+                const bool swap = t >= 2;
+#pragma unroll
+                for (int mt = 0; mt < NK; ++mt) {
+                    const uint32_t w0 = lds_u32(vpage + (uint32_t)(mt * 16 + g) * bs + vtok) & bmask;
+                    const uint32_t w1 = lds_u32(vpage + (uint32_t)(mt * 16 + g + 8) * bs + vtok) & bmask;
+                    const uint32_t a0 = e4m3x2_to_mma<BF16>(swap ? hi16(w0) : lo16(w0));
+                    const uint32_t a2 = e4m3x2_to_mma<BF16>(swap ? lo16(w0) : hi16(w0));
+                    const uint32_t a1 = e4m3x2_to_mma<BF16>(swap ? hi16(w1) : lo16(w1));
+                    const uint32_t a3 = e4m3x2_to_mma<BF16>(swap ? lo16(w1) : hi16(w1));
+                    mma16816<BF16>(acc[mt], a0, a1, a2, a3, pb0, pb1);
+                    if constexpr (BF16) mma16816<BF16>(acc[mt], a0, a1, a2, a3, pl0, pl1);
+                }
+            }
+        }
+
+        // Refill this ring position: order the generic-proxy reads above before the copy.
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (k + nstage < my_slots) {
+            issue(k + nstage);
+            issued = k + nstage + 1;
+        }
+    }
+
+    if (aborted) {
+        // Let every copy this warp started land before the block can exit.
+        for (int k = 0; k < issued; ++k) {
+            (void)mbar_wait_bounded(&bars[k % nstage], (uint32_t)((k / nstage) & 1), kWaitLimitNs);
+        }
+    }
+    griddep_launch_dependents();
+
+    // ---- merge the warps' (m, l, acc) ------------------------------------------------------
+#pragma unroll
+    for (int o = 4; o < 32; o <<= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+    }
+    if (g == 0) {
+        red_m[warp * kMaxHeadsPerCta + 2 * t] = m0;
+        red_m[warp * kMaxHeadsPerCta + 2 * t + 1] = m1;
+        red_l[warp * kMaxHeadsPerCta + 2 * t] = l0;
+        red_l[warp * kMaxHeadsPerCta + 2 * t + 1] = l1;
+    }
+    __syncthreads();
+    float M0 = -INFINITY, M1 = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        M0 = fmaxf(M0, red_m[w * kMaxHeadsPerCta + 2 * t]);
+        M1 = fmaxf(M1, red_m[w * kMaxHeadsPerCta + 2 * t + 1]);
+    }
+    const float f0 = m0 == -INFINITY ? 0.f : ex2(m0 - M0);
+    const float f1 = m1 == -INFINITY ? 0.f : ex2(m1 - M1);
+    if (warp == 0 && g == 0) {
+        float L0 = 0.f, L1 = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const float ma = red_m[w * kMaxHeadsPerCta + 2 * t], mb = red_m[w * kMaxHeadsPerCta + 2 * t + 1];
+            if (ma != -INFINITY) L0 += red_l[w * kMaxHeadsPerCta + 2 * t] * ex2(ma - M0);
+            if (mb != -INFINITY) L1 += red_l[w * kMaxHeadsPerCta + 2 * t + 1] * ex2(mb - M1);
+        }
+        fin_m[2 * t] = M0;
+        fin_m[2 * t + 1] = M1;
+        fin_l[2 * t] = L0;
+        fin_l[2 * t + 1] = L1;
+    }
+    // Scaled per-warp accumulators [warp][head][D + 4] reuse the (now idle) ring.
+    constexpr int RS = D + 4;
+    float* red_o = reinterpret_cast<float*>(smem);
+#pragma unroll
+    for (int mt = 0; mt < NK; ++mt) {
+        const int r0 = mt * 16 + g, r1 = r0 + 8;
+        float* base = red_o + (warp * kMaxHeadsPerCta + 2 * t) * RS;
+        if (r0 < D) {
+            base[r0] = acc[mt][0] * f0;
+            base[RS + r0] = acc[mt][1] * f1;
+        }
+        if (r1 < D) {
+            base[r1] = acc[mt][2] * f0;
+            base[RS + r1] = acc[mt][3] * f1;
+        }
+    }
+    __syncthreads();
+
+    const bool single = (P == 1);
+    for (int e = threadIdx.x; e < nh * D; e += blockDim.x) {
+        const int hh = e / D, i = e - hh * D;
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) v += red_o[(w * kMaxHeadsPerCta + hh) * RS + i];
+        const float lt = fin_l[hh];
+        v = lt > 0.f ? v * (p.v_scale / lt) : 0.f;
+        const int64_t row = (int64_t)s * H + h0 + hh;
+        if (single)
+            store_out<BF16>(p.out, row * D + i, v);
+        else
+            p.tmp_out[(row * p.Pmax + part) * D + i] = v;
+    }
+    if (threadIdx.x < nh) {
+        const int hh = threadIdx.x;
+        const int64_t sidx = ((int64_t)s * H + h0 + hh) * p.Pmax + part;
+        const float lt = fin_l[hh];
+        float mlog = -INFINITY;
+        if (lt > 0.f) {
+            mlog = fin_m[hh] * kLn2;
+            if (p.alibi != nullptr) mlog = fmaf(p.alibi[h0 + hh], (float)tref, mlog);
+        }
+        p.max_logits[sidx] = mlog;
+        p.exp_sums[sidx] = lt;
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// Phase 2: log-sum-exp combine across partitions
+// ---------------------------------------------------------------------------------------
+constexpr int kP2Threads = 256;
+constexpr int kP2Warps = kP2Threads / 32;
+
+template <bool BF16>
+__global__ void __launch_bounds__(kP2Threads)
+pa_v2_phase2_kernel(const Phase2Params p) {
+    extern __shared__ float sm2[];  // [Pmax] weights, then [kP2Warps][D] partial sums
+    __shared__ float red[kP2Warps];
+    __shared__ float bcast;
+    griddep_wait();
+    const int h = blockIdx.x, s = blockIdx.y;
+    const int L = p.seq_lens[s];
+    const int P = min(L > 0 ? (L + kPartition - 1) / kPartition : 0, p.Pmax);
+    if (P <= 1) return;  // written by phase 1 (single pass or empty)
+    const int D = p.D;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t row = (int64_t)s * p.H + h;
+    const float* ml = p.max_logits + row * p.Pmax;
+    const float* es = p.exp_sums + row * p.Pmax;
+    float* wts = sm2;
+    float* part = sm2 + p.Pmax;
+
+    float mx = -INFINITY;
+    for (int i = threadIdx.x; i < P; i += kP2Threads) mx = fmaxf(mx, ml[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    if (lane == 0) red[warp] = mx;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float m = red[0];
+        for (int w = 1; w < kP2Warps; ++w) m = fmaxf(m, red[w]);
+        bcast = m;
+    }
+    __syncthreads();
+    const float gmax = bcast;
+    float sum = 0.f;
+    for (int i = threadIdx.x; i < P; i += kP2Threads) {
+        const float m = ml[i];
+        const float w = (m == -INFINITY || gmax == -INFINITY) ? 0.f : ex2((m - gmax) * kLog2e) * es[i];
+        wts[i] = w;
+        sum += w;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+    __syncthreads();  // everyone has read bcast / red before they are reused
+    if (lane == 0) red[warp] = sum;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float tot = 0.f;
+        for (int w = 0; w < kP2Warps; ++w) tot += red[w];
+        bcast = tot;
+    }
+    __syncthreads();
+    const float inv = bcast > 0.f ? 1.f / bcast : 0.f;
+
+    // Each warp sums partitions p = warp, warp + 8, ...; lane covers float4 columns.
+    const int nq = D / 4;
+    const float4* tmp = reinterpret_cast<const float4*>(p.tmp_out + row * p.Pmax * D);
+    for (int c0 = 0; c0 < nq; c0 += 32) {
+        const int c = c0 + lane;
+        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (c < nq) {
+            int i = warp;
+            for (; i + 3 * kP2Warps < P; i += 4 * kP2Warps) {
+                const float4 x0 = tmp[(int64_t)i * nq + c];
+                const float4 x1 = tmp[(int64_t)(i + kP2Warps) * nq + c];
+                const float4 x2 = tmp[(int64_t)(i + 2 * kP2Warps) * nq + c];
+                const float4 x3 = tmp[(int64_t)(i + 3 * kP2Warps) * nq + c];
+                const float w0 = wts[i], w1 = wts[i + kP2Warps], w2 = wts[i + 2 * kP2Warps], w3 = wts[i + 3 * kP2Warps];
+                a.x += w0 * x0.x + w1 * x1.x + w2 * x2.x + w3 * x3.x;
+                a.y += w0 * x0.y + w1 * x1.y + w2 * x2.y + w3 * x3.y;
+                a.z += w0 * x0.z + w1 * x1.z + w2 * x2.z + w3 * x3.z;
+                a.w += w0 * x0.w + w1 * x1.w + w2 * x2.w + w3 * x3.w;
+            }
+            for (; i < P; i += kP2Warps) {
+                const float4 x = tmp[(int64_t)i * nq + c];
+                const float w = wts[i];
+                a.x += w * x.x;
+                a.y += w * x.y;
+                a.z += w * x.z;
+                a.w += w * x.w;
+            }
+            float* dst = part + warp * D + 4 * c;
+            dst[0] = a.x;
+            dst[1] = a.y;
+            dst[2] = a.z;
+            dst[3] = a.w;
+        }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < D; i += kP2Threads) {
+        float v = 0.f;
+#pragma unroll
+        for (int w = 0; w < kP2Warps; ++w) v += part[w * D + i];
+        store_out<BF16>(p.out, row * D + i, v * inv);
+    }
+}
+
+// ---------------------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------------------
+static cudaEvent_t g_t_begin = nullptr, g_t_end = nullptr;
+
+static bool supported_head_size(int d) {
+    switch (d) {
+        case 64: case 80: case 96: case 112: case 120: case 128: case 192: case 256: return true;
+        default: return false;
+    }
+}
+
+using Phase1Fn = void (*)(const Phase1Params);
+
+template <bool BF16, int KVB>
+static Phase1Fn pick_phase1(int d) {
+    switch (d) {
+        case 64: return pa_v2_phase1_kernel<BF16, KVB, 64>;
+        case 80: return pa_v2_phase1_kernel<BF16, KVB, 80>;
+        case 96: return pa_v2_phase1_kernel<BF16, KVB, 96>;
+        case 112: return pa_v2_phase1_kernel<BF16, KVB, 112>;
+        case 128: return pa_v2_phase1_kernel<BF16, KVB, 128>;
+        case 192: return pa_v2_phase1_kernel<BF16, KVB, 192>;
+        case 256: return pa_v2_phase1_kernel<BF16, KVB, 256>;
+        case 120:
+            if constexpr (KVB == 2) return pa_v2_phase1_kernel<BF16, KVB, 120>;
+            else return nullptr;
+        default: return nullptr;
+    }
+}
+
+static Phase1Fn phase1_for(bool bf16, bool fp8, int d) {
+    if (bf16) return fp8 ? pick_phase1<true, 1>(d) : pick_phase1<true, 2>(d);
+    return fp8 ? pick_phase1<false, 1>(d) : pick_phase1<false, 2>(d);
+}
+
+// Opt a kernel into `bytes` of dynamic shared memory once per (kernel, device).
+static cudaError_t ensure_smem(const void* fn, size_t bytes) {
+    struct Entry { const void* fn; int dev; size_t bytes; };
+    static Entry cache[256];
+    static int n = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    for (int i = 0; i < n; ++i)
+        if (cache[i].fn == fn && cache[i].dev == dev && cache[i].bytes >= bytes) return cudaSuccess;
+    e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e != cudaSuccess) return e;
+    if (n < 256) cache[n++] = Entry{fn, dev, bytes};
+    return cudaSuccess;
+}
+
+static bool aligned(const void* ptr, size_t a) { return (reinterpret_cast<uintptr_t>(ptr) % a) == 0; }
+
+// Optional host-side check of the table contents (PA_CHECK=1); synchronises the stream.
+static pa_status host_check_tables(const int32_t* block_tables, int mbps, int num_blocks,
+                                   const int32_t* seq_lens, int num_seqs, int block_size,
+                                   int max_seq_len, cudaStream_t stream) {
+    const char* env = getenv("PA_CHECK");
+    if (env == nullptr || env[0] != '1') return PA_OK;
+    if (num_seqs == 0) return PA_OK;
+    int32_t* lens = (int32_t*)malloc(sizeof(int32_t) * num_seqs);
+    int32_t* tab = (int32_t*)malloc(sizeof(int32_t) * (size_t)num_seqs * mbps);
+    if (!lens || !tab) { free(lens); free(tab); return PA_ERR_CUDA; }
+    pa_status st = PA_OK;
+    if (cudaMemcpyAsync(lens, seq_lens, sizeof(int32_t) * num_seqs, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaMemcpyAsync(tab, block_tables, sizeof(int32_t) * (size_t)num_seqs * mbps, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+        cudaStreamSynchronize(stream) != cudaSuccess) {
+        st = PA_ERR_CUDA;
+    } else {
+        for (int s = 0; s < num_seqs && st == PA_OK; ++s) {
+            const int L = lens[s];
+            if (L < 0 || L > max_seq_len) { st = PA_ERR_INVALID_ARG; break; }
+            const int nb = (L + block_size - 1) / block_size;
+            if (nb > mbps) { st = PA_ERR_INVALID_ARG; break; }
+            for (int b = 0; b < nb; ++b) {
+                const int id = tab[(size_t)s * mbps + b];
+                if (id < 0 || id >= num_blocks) { st = PA_ERR_INVALID_ARG; break; }
+            }
+        }
+    }
+    free(lens);
+    free(tab);
+    return st;
+}
+
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" int pa_v2_partition_size(void) { return kPartition; }
+
+extern "C" const char* pa_status_string(pa_status status) {
+    switch (status) {
+        case PA_OK: return "ok";
+        case PA_ERR_INVALID_ARG: return "invalid argument";
+        case PA_ERR_UNSUPPORTED: return "unsupported combination";
+        case PA_ERR_CUDA: return "CUDA error";
+    }
+    return "unknown status";
+}
+
+cudaError_t pa::read_decode_errors(unsigned int* v, bool reset) {
+    cudaError_t e = cudaMemcpyFromSymbol(v, g_device_errors, sizeof(*v));
+    if (e != cudaSuccess || !reset) return e;
+    const unsigned int z = 0;
+    return cudaMemcpyToSymbol(g_device_errors, &z, sizeof(z));
+}
+
+extern "C" pa_status pa_get_device_errors(uint32_t* flags, int reset) {
+    if (flags == nullptr) return PA_ERR_INVALID_ARG;
+    unsigned int a = 0, b = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return PA_ERR_CUDA;
+    if (read_decode_errors(&a, reset != 0) != cudaSuccess) return PA_ERR_CUDA;
+    if (read_cache_errors(&b, reset != 0) != cudaSuccess) return PA_ERR_CUDA;
+    *flags = a | b;
+    return PA_OK;
+}
+
+extern "C" pa_status pa_v2_set_timing_events(cudaEvent_t begin, cudaEvent_t end) {
+    if ((begin == nullptr) != (end == nullptr)) return PA_ERR_INVALID_ARG;
+    g_t_begin = begin;
+    g_t_end = end;
+    return PA_OK;
+}
+
+pa_status pa::validate_decode(const DecodeArgs& a) {
+    if (a.num_seqs < 0 || a.num_heads <= 0 || a.num_kv_heads <= 0) return PA_ERR_INVALID_ARG;
+    if (a.num_heads % a.num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    if (a.q_dtype != PA_DT_F16 && a.q_dtype != PA_DT_BF16) return PA_ERR_UNSUPPORTED;
+    if (a.kv_cache_dtype != PA_KV_AUTO && a.kv_cache_dtype != PA_KV_FP8_E4M3) return PA_ERR_INVALID_ARG;
+    if (a.tmp_dtype != PA_DT_F32) return PA_ERR_UNSUPPORTED;
+    if (!supported_head_size(a.head_size)) return PA_ERR_UNSUPPORTED;
+    const int x = a.kv_cache_dtype == PA_KV_FP8_E4M3 ? 16 : 8;
+    if (a.head_size % x != 0) return PA_ERR_INVALID_ARG;
+    if (a.block_size <= 0 || kPartition % a.block_size != 0) return PA_ERR_INVALID_ARG;
+    if (a.block_size != 8 && a.block_size != 16 && a.block_size != 32) return PA_ERR_UNSUPPORTED;
+    if (!(a.scale == a.scale) || !isfinite(a.scale)) return PA_ERR_INVALID_ARG;
+    if (!(a.k_scale > 0.f) || !isfinite(a.k_scale) || !(a.v_scale > 0.f) || !isfinite(a.v_scale))
+        return PA_ERR_INVALID_ARG;
+    if (a.max_seq_len < 0 || a.max_num_partitions < 1) return PA_ERR_INVALID_ARG;
+    if ((int64_t)a.max_num_partitions * kPartition < (int64_t)a.max_seq_len) return PA_ERR_INVALID_ARG;
+    if (a.max_blocks_per_seq < 0 ||
+        (int64_t)a.max_blocks_per_seq * a.block_size < (int64_t)a.max_seq_len)
+        return PA_ERR_INVALID_ARG;
+    if (a.num_blocks <= 0) return PA_ERR_INVALID_ARG;
+    if (a.num_seqs > 65535) return PA_ERR_UNSUPPORTED;
+    if ((int64_t)a.num_kv_heads * ((a.num_heads / a.num_kv_heads + kMaxHeadsPerCta - 1) / kMaxHeadsPerCta) > 65535)
+        return PA_ERR_UNSUPPORTED;
+    // Phase-2 weights live in shared memory.
+    if (a.max_num_partitions > 16384) return PA_ERR_UNSUPPORTED;
+    if (a.num_seqs == 0) return PA_OK;
+    if (!a.output || !a.exp_sums || !a.max_logits || !a.tmp_output || !a.query || !a.key_cache ||
+        !a.value_cache || !a.block_tables || !a.seq_lens)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned(a.key_cache, 16) || !aligned(a.value_cache, 16) || !aligned(a.query, 16) ||
+        !aligned(a.output, 4) || !aligned(a.tmp_output, 16) || !aligned(a.exp_sums, 4) ||
+        !aligned(a.max_logits, 4) || !aligned(a.block_tables, 4) || !aligned(a.seq_lens, 4))
+        return PA_ERR_INVALID_ARG;
+    return PA_OK;
+}
+
+pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_logits, float* tmp_out) {
+    const bool bf16 = a.q_dtype == PA_DT_BF16;
+    const bool fp8 = a.kv_cache_dtype == PA_KV_FP8_E4M3;
+    const int D = a.head_size, bs = a.block_size;
+    const int G = a.num_heads / a.num_kv_heads;
+    const int ngroups = (G + kMaxHeadsPerCta - 1) / kMaxHeadsPerCta;
+    const int kvb = fp8 ? 1 : 2;
+    const int pps = bs >= 16 ? 1 : 16 / bs;
+    const uint32_t page_bytes = (uint32_t)D * bs * kvb;
+    const uint32_t slot_bytes = 2u * pps * page_bytes;
+    int nstage = (int)((96u * 1024u) / (kWarps * slot_bytes));
+    nstage = nstage < 2 ? 2 : (nstage > 8 ? 8 : nstage);
+    uint32_t ring = (uint32_t)kWarps * nstage * slot_bytes;
+    const uint32_t red_o = (uint32_t)kWarps * kMaxHeadsPerCta * (D + 4) * 4u;
+    if (ring < red_o) ring = (red_o + 127u) & ~127u;
+    const size_t smem1 = ring + kWarps * nstage * sizeof(uint64_t) + (2 * kWarps + 2) * kMaxHeadsPerCta * sizeof(float);
+
+    Phase1Fn fn = phase1_for(bf16, fp8, D);
+    if (fn == nullptr) return PA_ERR_UNSUPPORTED;
+    if (ensure_smem((const void*)fn, smem1) != cudaSuccess) return PA_ERR_CUDA;
+
+    Phase1Params p1;
+    p1.out = a.output;
+    p1.exp_sums = exp_sums;
+    p1.max_logits = max_logits;
+    p1.tmp_out = tmp_out;
+    p1.query = a.query;
+    p1.kcache = (const uint8_t*)a.key_cache;
+    p1.vcache = (const uint8_t*)a.value_cache;
+    p1.block_tables = a.block_tables;
+    p1.seq_lens = a.seq_lens;
+    p1.alibi = a.alibi_slopes;
+    p1.H = a.num_heads;
+    p1.Hk = a.num_kv_heads;
+    p1.G = G;
+    p1.ngroups = ngroups;
+    p1.bs = bs;
+    p1.mbps = a.max_blocks_per_seq;
+    p1.num_blocks = a.num_blocks;
+    p1.Pmax = a.max_num_partitions;
+    p1.nstage = nstage;
+    p1.ring_bytes = ring;
+    p1.qk_scale_log2 = a.scale * a.k_scale * kLog2e;
+    p1.v_scale = a.v_scale;
+
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)a.max_num_partitions, (unsigned)(a.num_kv_heads * ngroups), (unsigned)a.num_seqs);
+    cfg.blockDim = dim3(kWarps * 32, 1, 1);
+    cfg.dynamicSmemBytes = smem1;
+    cfg.stream = a.stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (g_t_begin != nullptr) cudaEventRecord(g_t_begin, a.stream);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, fn, p1);
+    if (g_t_end != nullptr) cudaEventRecord(g_t_end, a.stream);
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+
+    if (a.max_num_partitions > 1) {
+        Phase2Params p2;
+        p2.out = a.output;
+        p2.exp_sums = exp_sums;
+        p2.max_logits = max_logits;
+        p2.tmp_out = tmp_out;
+        p2.seq_lens = a.seq_lens;
+        p2.H = a.num_heads;
+        p2.D = D;
+        p2.Pmax = a.max_num_partitions;
+        const size_t smem2 = ((size_t)a.max_num_partitions + (size_t)kP2Warps * D) * sizeof(float);
+        void (*fn2)(const Phase2Params) = bf16 ? pa_v2_phase2_kernel<true> : pa_v2_phase2_kernel<false>;
+        if (ensure_smem((const void*)fn2, smem2) != cudaSuccess) return PA_ERR_CUDA;
+        cudaLaunchConfig_t cfg2 = {};
+        cfg2.gridDim = dim3((unsigned)a.num_heads, (unsigned)a.num_seqs, 1);
+        cfg2.blockDim = dim3(kP2Threads, 1, 1);
+        cfg2.dynamicSmemBytes = smem2;
+        cfg2.stream = a.stream;
+        cfg2.attrs = attr;
+        cfg2.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg2, fn2, p2);
+        if (e != cudaSuccess) return PA_ERR_CUDA;
+    }
+    return PA_OK;
+}
+
+extern "C" pa_status pa_v2_decode(void* output, float* exp_sums, float* max_logits, void* tmp_output,
+                                  const void* query, const void* key_cache, const void* value_cache,
+                                  int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                                  float scale, const int32_t* block_tables, int max_blocks_per_seq,
+                                  int num_blocks, const int32_t* seq_lens, int block_size,
+                                  int max_seq_len, int max_num_partitions, const float* alibi_slopes,
+                                  pa_dtype q_dtype, pa_kv_cache_dtype kv_cache_dtype, pa_dtype tmp_dtype,
+                                  float k_scale, float v_scale, cudaStream_t stream) {
+    DecodeArgs a;
+    a.output = output;
+    a.exp_sums = exp_sums;
+    a.max_logits = max_logits;
+    a.tmp_output = tmp_output;
+    a.query = query;
+    a.key_cache = key_cache;
+    a.value_cache = value_cache;
+    a.num_seqs = num_seqs;
+    a.num_heads = num_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_size = head_size;
+    a.scale = scale;
+    a.block_tables = block_tables;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.seq_lens = seq_lens;
+    a.block_size = block_size;
+    a.max_seq_len = max_seq_len;
+    a.max_num_partitions = max_num_partitions;
+    a.alibi_slopes = alibi_slopes;
+    a.q_dtype = q_dtype;
+    a.kv_cache_dtype = kv_cache_dtype;
+    a.tmp_dtype = tmp_dtype;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.stream = stream;
+    pa_status st = validate_decode(a);
+    if (st != PA_OK || num_seqs == 0) return st;
+    st = host_check_tables(block_tables, max_blocks_per_seq, num_blocks, seq_lens, num_seqs, block_size,
+                           max_seq_len, stream);
+    if (st != PA_OK) return st;
+    return launch_decode(a, exp_sums, max_logits, (float*)tmp_output);
+}

@@ -1,0 +1,40 @@
+// pa_internal.h -- host-side plumbing shared by the library's translation units.
+#pragma once
+
+#include <stdint.h>
+
+#include "pa_v2.h"
+
+namespace pa {
+
+struct DecodeArgs {
+    void* output;
+    float* exp_sums;
+    float* max_logits;
+    void* tmp_output;
+    const void* query;
+    const void* key_cache;
+    const void* value_cache;
+    int num_seqs, num_heads, num_kv_heads, head_size;
+    float scale;
+    const int32_t* block_tables;
+    int max_blocks_per_seq, num_blocks;
+    const int32_t* seq_lens;
+    int block_size, max_seq_len, max_num_partitions;
+    const float* alibi_slopes;
+    pa_dtype q_dtype;
+    pa_kv_cache_dtype kv_cache_dtype;
+    pa_dtype tmp_dtype;
+    float k_scale, v_scale;
+    cudaStream_t stream;
+};
+
+// Argument checks shared by the decode entry points (no device access).
+pa_status validate_decode(const DecodeArgs& a);
+// Enqueue phase 1 (+ phase 2) with the given workspace.
+pa_status launch_decode(const DecodeArgs& a, float* exp_sums, float* max_logits, float* tmp_out);
+// Read (and optionally clear) each translation unit's device error word on the current device.
+cudaError_t read_decode_errors(unsigned int* v, bool reset);
+cudaError_t read_cache_errors(unsigned int* v, bool reset);
+
+}  // namespace pa

@@ -1,0 +1,122 @@
+"""Helpers for the GPU parity tests: run the CUDA path through the C ABI on a workload and
+compare it with the fp64 oracle under the stated tolerances.
+
+Tolerances (decode): output max-abs error <= 2e-3 for fp16/bf16 caches and <= 2e-2 for an
+fp8 cache, each plus half an ulp of the output dtype at the reference value (the kernel
+must round its fp32 result to fp16/bf16); max_logits within 1e-4 * max(|ref|, 1);
+exp_sums within relative 1e-4; unused partitions exactly -inf / 0.  Cache writes: bit-exact.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import oracle
+import paged_kv_cache_v2_gb300 as pa
+
+TOL_OUT = {"auto": 2e-3, "fp8_e4m3": 2e-2}
+TOL_STAT = 1e-4
+
+
+def half_ulp(ref: np.ndarray, dtype: str) -> np.ndarray:
+    """Half the spacing of the output format at |ref| (normal range; subnormals use the
+    smallest normal spacing)."""
+    mant = 10 if dtype == "f16" else 7
+    emin = -14 if dtype == "f16" else -126
+    a = np.abs(ref)
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** emin)))
+    return 0.5 * 2.0 ** (e - mant)
+
+
+def to_device(wl, device="cuda"):
+    return dict(
+        query=wl.query.to(device), key_cache=wl.key_cache.to(device),
+        value_cache=wl.value_cache.to(device), block_tables=wl.block_tables.to(device),
+        seq_lens=wl.seq_lens.to(device),
+        alibi=None if wl.alibi_slopes is None else wl.alibi_slopes.to(device),
+    )
+
+
+def run_decode(wl, dev=None, max_num_partitions=None, max_seq_len=None, poison=True):
+    """pa_v2_decode on a workload; returns CPU tensors (out, exp_sums, max_logits, tmp)."""
+    if dev is None:
+        dev = to_device(wl)
+    S, H, d = wl.query.shape
+    msl = wl.max_seq_len if max_seq_len is None else max_seq_len
+    P = max(1, -(-msl // 512)) if max_num_partitions is None else max_num_partitions
+    fill = float("nan") if poison else 0.0
+    out = torch.full((S, H, d), fill, dtype=wl.query.dtype, device="cuda")
+    es = torch.full((S, H, P), fill, dtype=torch.float32, device="cuda")
+    ml = torch.full((S, H, P), fill, dtype=torch.float32, device="cuda")
+    tmp = torch.full((S, H, P, d), fill, dtype=torch.float32, device="cuda")
+    pa.pa_v2_decode(out, es, ml, tmp, dev["query"], dev["key_cache"], dev["value_cache"],
+                    wl.num_kv_heads, wl.scale, dev["block_tables"], dev["seq_lens"], wl.block_size,
+                    msl, dev["alibi"], wl.kv_cache_dtype, wl.k_scale, wl.v_scale)
+    torch.cuda.synchronize()
+    return out.cpu(), es.cpu(), ml.cpu(), tmp.cpu()
+
+
+def out_f64(t: torch.Tensor) -> np.ndarray:
+    return t.to(torch.float64).numpy()
+
+
+def check_decode(wl, gpu, ref, pairs=None, label=""):
+    """Compare GPU results with oracle results (optionally only on (s, h) pairs).
+    Returns a dict of the worst errors seen."""
+    out, es, ml, tmp = gpu
+    H = wl.num_heads
+    P = es.shape[2]
+    if pairs is None:
+        pairs = ref["pairs"]
+    pairs = np.asarray(pairs).reshape(-1, 2)
+    lens = wl.seq_lens.numpy()
+    tol = TOL_OUT[wl.kv_cache_dtype]
+    worst = {"out": 0.0, "out_excess": -1.0, "ml": 0.0, "es": 0.0, "tmp": 0.0}
+    for n, (s, h) in enumerate(pairs):
+        L = int(lens[s])
+        Ps = -(-L // 512) if L > 0 else 0
+        r_out = ref["out"][n]
+        g_out = out_f64(out[s, h])
+        err = np.abs(g_out - r_out)
+        allow = tol + half_ulp(r_out, wl.q_dtype)
+        assert np.all(np.isfinite(g_out)), f"{label} non-finite output at s={s} h={h}"
+        bad = err > allow
+        assert not bad.any(), (f"{label} output mismatch s={s} h={h} L={L}: max err "
+                               f"{err.max():.3g} at i={int(err.argmax())} (allow {allow[err.argmax()]:.3g})")
+        worst["out"] = max(worst["out"], float(err.max()))
+        worst["out_excess"] = max(worst["out_excess"], float((err - tol).max()))
+        for p in range(P):
+            gm, ge = float(ml[s, h, p]), float(es[s, h, p])
+            if p < Ps:
+                rm, re_ = ref["max_logits"][n, p], ref["exp_sums"][n, p]
+                dm = abs(gm - rm)
+                assert dm <= TOL_STAT * max(abs(rm), 1.0), f"{label} max_logit s={s} h={h} p={p}: {gm} vs {rm}"
+                de = abs(ge - re_) / re_
+                assert de <= TOL_STAT, f"{label} exp_sum s={s} h={h} p={p}: {ge} vs {re_}"
+                worst["ml"] = max(worst["ml"], dm / max(abs(rm), 1.0))
+                worst["es"] = max(worst["es"], de)
+                if Ps > 1:
+                    te = np.abs(tmp[s, h, p].double().numpy() - ref["tmp_out"][n, p]).max()
+                    assert te <= tol, f"{label} tmp_output s={s} h={h} p={p}: err {te}"
+                    worst["tmp"] = max(worst["tmp"], float(te))
+            else:
+                assert gm == -math.inf and ge == 0.0, f"{label} unused partition s={s} h={h} p={p}: {gm}, {ge}"
+        if L == 0:
+            assert np.all(g_out == 0.0)
+    return worst
+
+
+def sample_pairs(wl, n=24, seed=0):
+    """A spread of (s, h) pairs: the longest and shortest sequences, every forced edge
+    length, then random ones."""
+    rng = np.random.default_rng(seed)
+    lens = wl.seq_lens.numpy()
+    S, H = wl.num_seqs, wl.num_heads
+    seqs = [int(lens.argmax()), int(lens.argmin())] + [int(i) for i in np.nonzero(lens <= 1)[0][:4]]
+    seqs += [int(x) for x in rng.integers(0, S, size=n)]
+    pairs = []
+    for i, s in enumerate(seqs[:n]):
+        pairs.append((s, int(rng.integers(0, H)) if i > 1 else (0 if i == 0 else H - 1)))
+    return np.array(pairs, dtype=np.int32)

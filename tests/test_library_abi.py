@@ -1,0 +1,124 @@
+"""CPU-only checks of the C-ABI library: it builds, loads, exports every function the
+header declares, and rejects invalid arguments on the host before touching a device."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import paged_kv_cache_v2_gb300 as pa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pa_v2.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"PA_API\s+[\w\s\*]+?\b(pa_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_entry_points():
+    names = _declared()
+    for must in ("pa_v2_decode", "pa_reshape_and_cache", "pa_v2_partition_size", "pa_status_string"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib_path = pa._build.build()
+    out = subprocess.run(["nm", "-D", "--defined-only", lib_path], capture_output=True, text=True,
+                         check=True).stdout
+    exported = set(re.findall(r"\sT\s(pa_\w+)$", out, flags=re.M))
+    assert set(_declared()) <= exported, set(_declared()) - exported
+    lib = ctypes.CDLL(lib_path)
+    for name in _declared():
+        assert hasattr(lib, name)
+
+
+def test_partition_size_and_status_strings():
+    assert pa.pa_v2_partition_size() == 512
+    assert pa.pa_status_string(0) == "ok"
+    assert pa.pa_status_string(1) == "invalid argument"
+    assert pa.pa_status_string(2) == "unsupported combination"
+
+
+def _decode_raw(**over):
+    """Call pa_v2_decode with fake (never dereferenced) pointers; returns the status."""
+    lib = pa.load()
+    P = 0x10000  # 16-byte aligned fake address: validation must fail before any use
+    a = dict(output=P, exp_sums=P, max_logits=P, tmp_output=P, query=P, key_cache=P, value_cache=P,
+             num_seqs=2, num_heads=8, num_kv_heads=2, head_size=128, scale=0.088,
+             block_tables=P, max_blocks_per_seq=64, num_blocks=100, seq_lens=P, block_size=16,
+             max_seq_len=1024, max_num_partitions=2, alibi_slopes=None, q_dtype=0, kv=0, tmp=2,
+             k_scale=1.0, v_scale=1.0)
+    a.update(over)
+    return lib.pa_v2_decode(a["output"], a["exp_sums"], a["max_logits"], a["tmp_output"], a["query"],
+                            a["key_cache"], a["value_cache"], a["num_seqs"], a["num_heads"],
+                            a["num_kv_heads"], a["head_size"], a["scale"], a["block_tables"],
+                            a["max_blocks_per_seq"], a["num_blocks"], a["seq_lens"], a["block_size"],
+                            a["max_seq_len"], a["max_num_partitions"], a["alibi_slopes"],
+                            a["q_dtype"], a["kv"], a["tmp"], a["k_scale"], a["v_scale"], None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(num_heads=6, num_kv_heads=4), 1),          # H % Hk != 0
+    (dict(block_size=24), 1),                        # 512 % bs != 0
+    (dict(block_size=64), 2),                        # valid but not built
+    (dict(head_size=100), 2),                        # not a supported head size
+    (dict(head_size=120, kv=1), 1),                  # fp8 needs head_size % 16 == 0
+    (dict(max_num_partitions=1), 1),                 # fewer partitions than max_seq_len needs
+    (dict(max_blocks_per_seq=10), 1),                # table narrower than max_seq_len needs
+    (dict(k_scale=0.0), 1),
+    (dict(v_scale=-1.0), 1),
+    (dict(k_scale=float("inf")), 1),
+    (dict(scale=float("nan")), 1),
+    (dict(output=None), 1),
+    (dict(query=None), 1),
+    (dict(tmp_output=None), 1),
+    (dict(key_cache=0x10008), 1),                    # bulk copies need 16-byte alignment
+    (dict(q_dtype=2), 2),                            # fp32 query not built
+    (dict(tmp=0), 2),                                # fp16 tmp_output not built
+    (dict(kv=7), 1),
+    (dict(num_blocks=0), 1),
+    (dict(num_seqs=-1), 1),
+    (dict(num_seqs=70000), 2),
+    (dict(max_num_partitions=20000, max_seq_len=20000 * 512, max_blocks_per_seq=20000 * 32), 2),
+])
+def test_decode_rejects_invalid_arguments_on_host(over, status):
+    assert _decode_raw(**over) == status
+
+
+def test_decode_with_zero_sequences_is_a_noop():
+    assert _decode_raw(num_seqs=0, output=None, query=None) == 0
+
+
+def _cache_raw(**over):
+    lib = pa.load()
+    P = 0x10000
+    a = dict(key=P, value=P, ks=256, vs=256, key_cache=P, value_cache=P, slots=P, T=4, Hk=2, d=128,
+             bs=16, nb=10, src=0, kv=0, k_scale=1.0, v_scale=1.0)
+    a.update(over)
+    return lib.pa_reshape_and_cache(a["key"], a["value"], a["ks"], a["vs"], a["key_cache"],
+                                    a["value_cache"], a["slots"], a["T"], a["Hk"], a["d"], a["bs"],
+                                    a["nb"], a["src"], a["kv"], a["k_scale"], a["v_scale"], None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(ks=100), 1),            # token stride shorter than a row
+    (dict(d=100), 2),
+    (dict(d=120, kv=1), 1),
+    (dict(bs=12), 2),
+    (dict(src=2), 2),
+    (dict(k_scale=0.0, kv=1), 1),
+    (dict(key=None), 1),
+    (dict(key_cache=0x10004), 1),
+    (dict(nb=0), 1),
+])
+def test_cache_writer_rejects_invalid_arguments_on_host(over, status):
+    assert _cache_raw(**over) == status
+
+
+def test_cache_writer_with_zero_tokens_is_a_noop():
+    assert _cache_raw(T=0, key=None) == 0
