@@ -135,6 +135,21 @@ def _dist():
     return ws, rank, local
 
 
+def combine_ranks(step_bytes: float, ms_per_step: float, device, world: int):
+    """Whole-job numbers of a multi-rank run: bytes summed over ranks, time of the slowest
+    rank (each rank processes its own sequences; nothing else is exchanged)."""
+    if world <= 1:
+        return step_bytes, ms_per_step
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([ms_per_step], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    b = torch.tensor([step_bytes], dtype=torch.float64, device=device)
+    dist.all_reduce(b, op=dist.ReduceOp.SUM)
+    return float(b.item()), float(t.item())
+
+
 def _cpu_baseline(wl, seconds: float, threads: int):
     """Time the fp64 oracle on the first sequences of the workload (all heads) until about
     `seconds` of work is done; returns (GB/s, description, threads)."""
@@ -250,6 +265,9 @@ def run_ours(args):
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in kev:  # create the CUDA events (torch creates them lazily on first record)
+        a.record(stream)
+        b.record(stream)
     barrier()
     torch.cuda.synchronize()
     with ClockSampler(dev.index) as clocks:
@@ -266,15 +284,7 @@ def run_ours(args):
     step_ms = [a.elapsed_time(b) for a, b in ev]
     k_ms = [a.elapsed_time(b) for a, b in kev]
     mean_ms = sum(step_ms) / len(step_ms)
-    if ws > 1:
-        tt = torch.tensor([mean_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        mean_ms_max = float(tt.item())
-        bb = torch.tensor([float(step_bytes)], device=dev)
-        torch.distributed.all_reduce(bb)
-        all_bytes = float(bb.item())
-    else:
-        mean_ms_max, all_bytes = mean_ms, float(step_bytes)
+    all_bytes, mean_ms_max = combine_ranks(float(step_bytes), mean_ms, dev, ws)
     value = all_bytes / (mean_ms_max * 1e-3) / 1e9
 
     # ---- end to end through host buffers (pinned), same metric --------------------------
@@ -309,10 +319,7 @@ def run_ours(args):
         torch.cuda.synchronize()
         barrier()
         e_ms = e0.elapsed_time(e1) / args.steps
-        if ws > 1:
-            tt = torch.tensor([e_ms], device=dev)
-            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(tt.item())
+        _, e_ms = combine_ranks(float(step_bytes), e_ms, dev, ws)
         e2e = {"value": round(all_bytes / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                "us_per_step": round(e_ms * 1e3, 2), "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h)}

@@ -168,6 +168,9 @@ extern "C" pa_status pa_reshape_and_cache(const void* key, const void* value, in
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, fn, p) != cudaSuccess) return PA_ERR_CUDA;
+    if (cudaLaunchKernelEx(&cfg, fn, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return PA_ERR_CUDA;
+    }
     return PA_OK;
 }

@@ -823,8 +823,10 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
     const int pps = bs >= 16 ? 1 : 16 / bs;
     const uint32_t page_bytes = (uint32_t)D * bs * kvb;
     const uint32_t slot_bytes = 2u * pps * page_bytes;
+    // Ring depth: about 96 KiB of pages per CTA (two CTAs per SM), at least one slot per warp.
     int nstage = (int)((96u * 1024u) / (kWarps * slot_bytes));
-    nstage = nstage < 2 ? 2 : (nstage > 8 ? 8 : nstage);
+    nstage = nstage < 1 ? 1 : (nstage > 8 ? 8 : nstage);
+    if (nstage == 1 && 2u * kWarps * slot_bytes <= 160u * 1024u) nstage = 2;
     uint32_t ring = (uint32_t)kWarps * nstage * slot_bytes;
     const uint32_t red_o = (uint32_t)kWarps * kMaxHeadsPerCta * (D + 4) * 4u;
     if (ring < red_o) ring = (red_o + 127u) & ~127u;
@@ -832,7 +834,17 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
 
     Phase1Fn fn = phase1_for(bf16, fp8, D);
     if (fn == nullptr) return PA_ERR_UNSUPPORTED;
-    if (ensure_smem((const void*)fn, smem1) != cudaSuccess) return PA_ERR_CUDA;
+    int dev = 0, optin = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return PA_ERR_CUDA;
+    }
+    if (smem1 > (size_t)optin) return PA_ERR_UNSUPPORTED;
+    if (ensure_smem((const void*)fn, smem1) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return PA_ERR_CUDA;
+    }
 
     Phase1Params p1;
     p1.out = a.output;
@@ -872,7 +884,10 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
     if (g_t_begin != nullptr) cudaEventRecord(g_t_begin, a.stream);
     cudaError_t e = cudaLaunchKernelEx(&cfg, fn, p1);
     if (g_t_end != nullptr) cudaEventRecord(g_t_end, a.stream);
-    if (e != cudaSuccess) return PA_ERR_CUDA;
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();  // leave no launch error behind for the caller's next call
+        return PA_ERR_CUDA;
+    }
 
     if (a.max_num_partitions > 1) {
         Phase2Params p2;
@@ -886,7 +901,10 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
         p2.Pmax = a.max_num_partitions;
         const size_t smem2 = ((size_t)a.max_num_partitions + (size_t)kP2Warps * D) * sizeof(float);
         void (*fn2)(const Phase2Params) = bf16 ? pa_v2_phase2_kernel<true> : pa_v2_phase2_kernel<false>;
-        if (ensure_smem((const void*)fn2, smem2) != cudaSuccess) return PA_ERR_CUDA;
+        if (ensure_smem((const void*)fn2, smem2) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return PA_ERR_CUDA;
+        }
         cudaLaunchConfig_t cfg2 = {};
         cfg2.gridDim = dim3((unsigned)a.num_heads, (unsigned)a.num_seqs, 1);
         cfg2.blockDim = dim3(kP2Threads, 1, 1);
@@ -895,7 +913,10 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
         cfg2.attrs = attr;
         cfg2.numAttrs = 1;
         e = cudaLaunchKernelEx(&cfg2, fn2, p2);
-        if (e != cudaSuccess) return PA_ERR_CUDA;
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            return PA_ERR_CUDA;
+        }
     }
     return PA_OK;
 }
