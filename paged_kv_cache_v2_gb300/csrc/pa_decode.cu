@@ -48,8 +48,16 @@ namespace pa {
 
 static __device__ unsigned int g_device_errors = 0;
 
+#ifndef PA_PHASE1_WARPS
+#define PA_PHASE1_WARPS 4
+#endif
+#ifndef PA_RING_KIB
+#define PA_RING_KIB 96
+#endif
+
 constexpr int kPartition = 512;
-constexpr int kWarps = 4;              // phase-1 warps per CTA
+constexpr int kWarps = PA_PHASE1_WARPS;  // phase-1 warps per CTA
+constexpr uint32_t kRingTarget = PA_RING_KIB * 1024u;  // shared-memory page ring per CTA
 constexpr int kMaxHeadsPerCta = 8;     // the MMA N dimension
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -120,9 +128,21 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     const int g = lane >> 2, t = lane & 3;
     const int H = p.H;
 
+    // Block ids of this partition's pages (lane i: pages i and 32 + i) and the sequence
+    // length load in parallel, before waiting on the previous kernel: a cache writer that
+    // ran just before changes neither.
+    const int bs = p.bs;
+    const int t0 = part * kPartition;
+    const int lb0 = t0 / bs;
+    int raw0 = -1, raw1 = -1;
+    {
+        const int32_t* row = p.block_tables + (int64_t)s * p.mbps;
+        if (lb0 + lane < p.mbps) raw0 = row[lb0 + lane];
+        if (bs == 8 && lb0 + 32 + lane < p.mbps) raw1 = row[lb0 + 32 + lane];
+    }
+    const int L = p.seq_lens[s];
     griddep_wait();  // the cache writer (if it ran just before) must be visible
 
-    const int L = p.seq_lens[s];
     const int P = L > 0 ? (L + kPartition - 1) / kPartition : 0;
     if (threadIdx.x == 0 && part == 0 && (L < 0 || P > p.Pmax)) flag_error(2u);
     if (part >= P) {
@@ -140,10 +160,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
         return;
     }
 
-    const int bs = p.bs;
-    const int t0 = part * kPartition;
     const int t1 = min(L, t0 + kPartition);
-    const int lb0 = t0 / bs;
     const int npages = (t1 - 1) / bs - lb0 + 1;
     const int pps = bs >= 16 ? 1 : 16 / bs;  // pages per slot
     const int slot_tokens = pps * bs;
@@ -160,23 +177,14 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     float* fin_m = red_l + kWarps * kMaxHeadsPerCta;  // [8] merged max (log2 units)
     float* fin_l = fin_m + kMaxHeadsPerCta;           // [8] merged exp-sum
 
-    // Physical block ids of this partition: lane i holds pages i and 32 + i.
+    // Keep the ids of pages that exist; mask (and flag) ids outside [0, num_blocks) or past
+    // the table row.
     int bid0 = -1, bid1 = -1;
-    {
-        const int32_t* row = p.block_tables + (int64_t)s * p.mbps;
-        const int la = lb0 + lane, lbb = lb0 + 32 + lane;
-        if (lane < npages) {
-            if (la < p.mbps) {
-                const int b = row[la];
-                if (b >= 0 && b < p.num_blocks) bid0 = b; else flag_error(1u);
-            } else flag_error(1u);
-        }
-        if (32 + lane < npages) {
-            if (lbb < p.mbps) {
-                const int b = row[lbb];
-                if (b >= 0 && b < p.num_blocks) bid1 = b; else flag_error(1u);
-            } else flag_error(1u);
-        }
+    if (lane < npages) {
+        if (raw0 >= 0 && raw0 < p.num_blocks && lb0 + lane < p.mbps) bid0 = raw0; else flag_error(1u);
+    }
+    if (32 + lane < npages) {
+        if (raw1 >= 0 && raw1 < p.num_blocks && lb0 + 32 + lane < p.mbps) bid1 = raw1; else flag_error(1u);
     }
 
     if (lane == 0) {
@@ -553,100 +561,84 @@ pa_v2_phase1_kernel(const Phase1Params p) {
 // ---------------------------------------------------------------------------------------
 // Phase 2: log-sum-exp combine across partitions
 // ---------------------------------------------------------------------------------------
-constexpr int kP2Threads = 256;
-constexpr int kP2Warps = kP2Threads / 32;
+// One CTA per (query head, sequence) with more than one partition; W warps (chosen from
+// max_num_partitions on the host).  Warp w folds partitions w, w + W, ... into a running
+// (m, l, acc) with the online rescaling, so its loads of max_logits, exp_sums and tmp rows
+// do not wait on one another; the W partial states merge through shared memory.
+// The combine is the pages' formula: g = max_p m_p, w_p = exp(m_p - g) l_p,
+// out = sum_p w_p tmp_p / sum_p w_p.
+constexpr int kP2MaxWarps = 16;
+constexpr int kP2MaxCols = 2;  // float4 columns per lane: head_size <= 256
 
 template <bool BF16>
-__global__ void __launch_bounds__(kP2Threads)
+__global__ void __launch_bounds__(kP2MaxWarps * 32)
 pa_v2_phase2_kernel(const Phase2Params p) {
-    extern __shared__ float sm2[];  // [Pmax] weights, then [kP2Warps][D] partial sums
-    __shared__ float red[kP2Warps];
-    __shared__ float bcast;
+    extern __shared__ float sm2[];  // [W][D] partial sums
+    __shared__ float wm[kP2MaxWarps], wl[kP2MaxWarps];
     griddep_wait();
     const int h = blockIdx.x, s = blockIdx.y;
     const int L = p.seq_lens[s];
     const int P = min(L > 0 ? (L + kPartition - 1) / kPartition : 0, p.Pmax);
     if (P <= 1) return;  // written by phase 1 (single pass or empty)
-    const int D = p.D;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int D = p.D, nq = D / 4;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, W = blockDim.x >> 5;
     const int64_t row = (int64_t)s * p.H + h;
     const float* ml = p.max_logits + row * p.Pmax;
     const float* es = p.exp_sums + row * p.Pmax;
-    float* wts = sm2;
-    float* part = sm2 + p.Pmax;
-
-    float mx = -INFINITY;
-    for (int i = threadIdx.x; i < P; i += kP2Threads) mx = fmaxf(mx, ml[i]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if (lane == 0) red[warp] = mx;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        float m = red[0];
-        for (int w = 1; w < kP2Warps; ++w) m = fmaxf(m, red[w]);
-        bcast = m;
-    }
-    __syncthreads();
-    const float gmax = bcast;
-    float sum = 0.f;
-    for (int i = threadIdx.x; i < P; i += kP2Threads) {
-        const float m = ml[i];
-        const float w = (m == -INFINITY || gmax == -INFINITY) ? 0.f : ex2((m - gmax) * kLog2e) * es[i];
-        wts[i] = w;
-        sum += w;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    __syncthreads();  // everyone has read bcast / red before they are reused
-    if (lane == 0) red[warp] = sum;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        float tot = 0.f;
-        for (int w = 0; w < kP2Warps; ++w) tot += red[w];
-        bcast = tot;
-    }
-    __syncthreads();
-    const float inv = bcast > 0.f ? 1.f / bcast : 0.f;
-
-    // Each warp sums partitions p = warp, warp + 8, ...; lane covers float4 columns.
-    const int nq = D / 4;
     const float4* tmp = reinterpret_cast<const float4*>(p.tmp_out + row * p.Pmax * D);
-    for (int c0 = 0; c0 < nq; c0 += 32) {
-        const int c = c0 + lane;
-        float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+
+    float m = -INFINITY, l = 0.f;
+    float4 acc[kP2MaxCols];
+#pragma unroll
+    for (int k = 0; k < kP2MaxCols; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = warp; i < P; i += W) {
+        const float mi = ml[i] * kLog2e, li = es[i];
+        float4 x[kP2MaxCols];
+#pragma unroll
+        for (int k = 0; k < kP2MaxCols; ++k) {
+            const int c = lane + 32 * k;
+            x[k] = c < nq ? tmp[(int64_t)i * nq + c] : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        if (mi == -INFINITY || !(li > 0.f)) continue;  // an all-masked partition adds nothing
+        const float mn = fmaxf(m, mi);
+        const float a = ex2(m - mn), wi = ex2(mi - mn) * li;  // m = -inf -> a = 0
+        l = l * a + wi;
+#pragma unroll
+        for (int k = 0; k < kP2MaxCols; ++k) {
+            acc[k].x = acc[k].x * a + wi * x[k].x;
+            acc[k].y = acc[k].y * a + wi * x[k].y;
+            acc[k].z = acc[k].z * a + wi * x[k].z;
+            acc[k].w = acc[k].w * a + wi * x[k].w;
+        }
+        m = mn;
+    }
+    if (lane == 0) {
+        wm[warp] = m;
+        wl[warp] = l;
+    }
+    __syncthreads();
+    float M = -INFINITY;
+    for (int w = 0; w < W; ++w) M = fmaxf(M, wm[w]);
+    float Lt = 0.f;
+    for (int w = 0; w < W; ++w)
+        if (wm[w] != -INFINITY) Lt += wl[w] * ex2(wm[w] - M);
+    const float f = (m == -INFINITY) ? 0.f : ex2(m - M);
+#pragma unroll
+    for (int k = 0; k < kP2MaxCols; ++k) {
+        const int c = lane + 32 * k;
         if (c < nq) {
-            int i = warp;
-            for (; i + 3 * kP2Warps < P; i += 4 * kP2Warps) {
-                const float4 x0 = tmp[(int64_t)i * nq + c];
-                const float4 x1 = tmp[(int64_t)(i + kP2Warps) * nq + c];
-                const float4 x2 = tmp[(int64_t)(i + 2 * kP2Warps) * nq + c];
-                const float4 x3 = tmp[(int64_t)(i + 3 * kP2Warps) * nq + c];
-                const float w0 = wts[i], w1 = wts[i + kP2Warps], w2 = wts[i + 2 * kP2Warps], w3 = wts[i + 3 * kP2Warps];
-                a.x += w0 * x0.x + w1 * x1.x + w2 * x2.x + w3 * x3.x;
-                a.y += w0 * x0.y + w1 * x1.y + w2 * x2.y + w3 * x3.y;
-                a.z += w0 * x0.z + w1 * x1.z + w2 * x2.z + w3 * x3.z;
-                a.w += w0 * x0.w + w1 * x1.w + w2 * x2.w + w3 * x3.w;
-            }
-            for (; i < P; i += kP2Warps) {
-                const float4 x = tmp[(int64_t)i * nq + c];
-                const float w = wts[i];
-                a.x += w * x.x;
-                a.y += w * x.y;
-                a.z += w * x.z;
-                a.w += w * x.w;
-            }
-            float* dst = part + warp * D + 4 * c;
-            dst[0] = a.x;
-            dst[1] = a.y;
-            dst[2] = a.z;
-            dst[3] = a.w;
+            float* dst = sm2 + warp * D + 4 * c;
+            dst[0] = acc[k].x * f;
+            dst[1] = acc[k].y * f;
+            dst[2] = acc[k].z * f;
+            dst[3] = acc[k].w * f;
         }
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < D; i += kP2Threads) {
+    const float inv = Lt > 0.f ? 1.f / Lt : 0.f;
+    for (int i = threadIdx.x; i < D; i += blockDim.x) {
         float v = 0.f;
-#pragma unroll
-        for (int w = 0; w < kP2Warps; ++w) v += part[w * D + i];
+        for (int w = 0; w < W; ++w) v += sm2[w * D + i];
         store_out<BF16>(p.out, row * D + i, v * inv);
     }
 }
@@ -800,8 +792,6 @@ pa_status pa::validate_decode(const DecodeArgs& a) {
     if (a.num_seqs > 65535) return PA_ERR_UNSUPPORTED;
     if ((int64_t)a.num_kv_heads * ((a.num_heads / a.num_kv_heads + kMaxHeadsPerCta - 1) / kMaxHeadsPerCta) > 65535)
         return PA_ERR_UNSUPPORTED;
-    // Phase-2 weights live in shared memory.
-    if (a.max_num_partitions > 16384) return PA_ERR_UNSUPPORTED;
     if (a.num_seqs == 0) return PA_OK;
     if (!a.output || !a.exp_sums || !a.max_logits || !a.tmp_output || !a.query || !a.key_cache ||
         !a.value_cache || !a.block_tables || !a.seq_lens)
@@ -823,8 +813,8 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
     const int pps = bs >= 16 ? 1 : 16 / bs;
     const uint32_t page_bytes = (uint32_t)D * bs * kvb;
     const uint32_t slot_bytes = 2u * pps * page_bytes;
-    // Ring depth: about 96 KiB of pages per CTA (two CTAs per SM), at least one slot per warp.
-    int nstage = (int)((96u * 1024u) / (kWarps * slot_bytes));
+    // Ring depth: about kRingTarget bytes of pages per CTA, at least one slot per warp.
+    int nstage = (int)(kRingTarget / (kWarps * slot_bytes));
     nstage = nstage < 1 ? 1 : (nstage > 8 ? 8 : nstage);
     if (nstage == 1 && 2u * kWarps * slot_bytes <= 160u * 1024u) nstage = 2;
     uint32_t ring = (uint32_t)kWarps * nstage * slot_bytes;
@@ -899,7 +889,10 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
         p2.H = a.num_heads;
         p2.D = D;
         p2.Pmax = a.max_num_partitions;
-        const size_t smem2 = ((size_t)a.max_num_partitions + (size_t)kP2Warps * D) * sizeof(float);
+        // Warps per combine: about 8 partitions per warp, 1 .. 16 warps.
+        int w2 = (a.max_num_partitions + 7) / 8;
+        w2 = w2 < 1 ? 1 : (w2 > kP2MaxWarps ? kP2MaxWarps : w2);
+        const size_t smem2 = (size_t)w2 * D * sizeof(float);
         void (*fn2)(const Phase2Params) = bf16 ? pa_v2_phase2_kernel<true> : pa_v2_phase2_kernel<false>;
         if (ensure_smem((const void*)fn2, smem2) != cudaSuccess) {
             (void)cudaGetLastError();
@@ -907,7 +900,7 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
         }
         cudaLaunchConfig_t cfg2 = {};
         cfg2.gridDim = dim3((unsigned)a.num_heads, (unsigned)a.num_seqs, 1);
-        cfg2.blockDim = dim3(kP2Threads, 1, 1);
+        cfg2.blockDim = dim3((unsigned)(32 * w2), 1, 1);
         cfg2.dynamicSmemBytes = smem2;
         cfg2.stream = a.stream;
         cfg2.attrs = attr;

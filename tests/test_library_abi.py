@@ -84,7 +84,7 @@ def _decode_raw(**over):
     (dict(num_blocks=0), 1),
     (dict(num_seqs=-1), 1),
     (dict(num_seqs=70000), 2),
-    (dict(max_num_partitions=20000, max_seq_len=20000 * 512, max_blocks_per_seq=20000 * 32), 2),
+    (dict(num_heads=8 * 70000, num_kv_heads=70000), 2),   # grid rows past 65535
 ])
 def test_decode_rejects_invalid_arguments_on_host(over, status):
     assert _decode_raw(**over) == status
