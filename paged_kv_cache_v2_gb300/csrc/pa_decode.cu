@@ -52,7 +52,13 @@ static __device__ unsigned int g_device_errors = 0;
 #define PA_PHASE1_WARPS 4
 #endif
 #ifndef PA_RING_KIB
-#define PA_RING_KIB 96
+#define PA_RING_KIB 64
+#endif
+#ifndef PA_MIN_STAGES
+#define PA_MIN_STAGES 1
+#endif
+#ifndef PA_GRID_WAVES
+#define PA_GRID_WAVES 64
 #endif
 
 constexpr int kPartition = 512;
@@ -113,12 +119,14 @@ template <bool BF16, int KVB, int D>
 __global__ void __launch_bounds__(kWarps * 32)
 pa_v2_phase1_kernel(const Phase1Params p) {
     constexpr bool FP8 = (KVB == 1);
-    constexpr int NK = (D + 15) / 16;      // 16-wide steps over the head dimension
+    constexpr int NK = (D + 15) / 16;          // 16-wide steps over the head dimension
     constexpr bool HALF_STEP = (D % 16) != 0;  // head_size 120: last step has 8 elements
     static_assert(!(FP8 && HALF_STEP), "fp8 pages need head_size % 16 == 0");
     extern __shared__ __align__(128) uint8_t smem[];
 
-    const int part = blockIdx.x;
+    // This CTA handles partitions px, px + PX, ... of one sequence for one group of <= 8
+    // query heads sharing a kv head.
+    const int px = blockIdx.x, PX = gridDim.x;
     const int kvh = blockIdx.y / p.ngroups;
     const int grp = blockIdx.y - kvh * p.ngroups;
     const int s = blockIdx.z;
@@ -126,49 +134,66 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     const int nh = min(kMaxHeadsPerCta, p.G - grp * kMaxHeadsPerCta);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t = lane & 3;
-    const int H = p.H;
+    const int H = p.H, bs = p.bs;
+    const int bs_log2 = bs == 8 ? 3 : (bs == 16 ? 4 : 5);
+    const int pps = bs >= 16 ? 1 : 16 / bs;  // pages per slot
+    const int slot_tokens = pps * bs;
+    const int tiles_per_slot = slot_tokens / 16;
+    const int ppart = kPartition / bs;  // pages in a full partition
+    const uint32_t page_bytes = (uint32_t)D * bs * KVB;
+    const uint32_t slot_bytes = 2u * pps * page_bytes;
+    const int nstage = p.nstage;
+    const int32_t* trow = p.block_tables + (int64_t)s * p.mbps;
 
-    // Block ids of this partition's pages (lane i: pages i and 32 + i) and the sequence
-    // length load in parallel, before waiting on the previous kernel: a cache writer that
-    // ran just before changes neither.
-    const int bs = p.bs;
-    const int t0 = part * kPartition;
-    const int lb0 = t0 / bs;
-    int raw0 = -1, raw1 = -1;
-    {
-        const int32_t* row = p.block_tables + (int64_t)s * p.mbps;
-        if (lb0 + lane < p.mbps) raw0 = row[lb0 + lane];
-        if (bs == 8 && lb0 + 32 + lane < p.mbps) raw1 = row[lb0 + 32 + lane];
-    }
+    // Raw table entries of partition q: lane i holds pages i and 32 + i.
+    auto load_ids = [&](int q, int& r0, int& r1) {
+        r0 = r1 = -1;
+        if (q < p.Pmax) {
+            const int lb = q * ppart;
+            if (lb + lane < p.mbps) r0 = trow[lb + lane];
+            if (ppart > 32 && lb + 32 + lane < p.mbps) r1 = trow[lb + 32 + lane];
+        }
+    };
+    // The ids of the first two partitions and the length load in parallel, before waiting on
+    // the previous kernel: a cache writer that ran just before changes none of them.
+    int c0, c1, n0, n1;
+    load_ids(px, c0, c1);
+    load_ids(px + PX, n0, n1);
     const int L = p.seq_lens[s];
     griddep_wait();  // the cache writer (if it ran just before) must be visible
 
     const int P = L > 0 ? (L + kPartition - 1) / kPartition : 0;
-    if (threadIdx.x == 0 && part == 0 && (L < 0 || P > p.Pmax)) flag_error(2u);
-    if (part >= P) {
-        // Partition past the end of the sequence (or an empty sequence).
-        if (threadIdx.x < nh) {
-            const int64_t sidx = ((int64_t)s * H + h0 + threadIdx.x) * p.Pmax + part;
+    if (threadIdx.x == 0 && px == 0 && (L < 0 || P > p.Pmax)) flag_error(2u);
+    const int Pl = min(P, p.Pmax);  // partitions with tokens that the grid covers
+    // This CTA's partitions past the end: max_logits = -inf, exp_sums = 0.
+    for (int q = px; q < p.Pmax; q += PX) {
+        if (q >= Pl && threadIdx.x < nh) {
+            const int64_t sidx = ((int64_t)s * H + h0 + threadIdx.x) * p.Pmax + q;
             p.max_logits[sidx] = -INFINITY;
             p.exp_sums[sidx] = 0.f;
         }
-        if (part == 0) {
-            for (int i = threadIdx.x; i < nh * D; i += blockDim.x)
-                store_out<BF16>(p.out, ((int64_t)s * H + h0) * D + i, 0.f);
-        }
+    }
+    if (px == 0 && L <= 0) {
+        for (int i = threadIdx.x; i < nh * D; i += blockDim.x)
+            store_out<BF16>(p.out, ((int64_t)s * H + h0) * D + i, 0.f);
+    }
+    if (px >= Pl) {
         griddep_launch_dependents();
         return;
     }
 
-    const int t1 = min(L, t0 + kPartition);
-    const int npages = (t1 - 1) / bs - lb0 + 1;
-    const int pps = bs >= 16 ? 1 : 16 / bs;  // pages per slot
-    const int slot_tokens = pps * bs;
-    const int tiles_per_slot = slot_tokens / 16;
-    const int nslots = (npages + pps - 1) / pps;
-    const uint32_t page_bytes = (uint32_t)D * bs * KVB;
-    const uint32_t slot_bytes = 2u * pps * page_bytes;
-    const int nstage = p.nstage;
+    auto npages_of = [&](int q) { return ((min(L, (q + 1) * kPartition) - 1) >> bs_log2) - q * ppart + 1; };
+    auto my_slots_of = [&](int np) {
+        const int ns = pps == 1 ? np : (np + 1) >> 1;
+        return ns > warp ? (ns - warp + kWarps - 1) / kWarps : 0;
+    };
+    // Physical id of page `pg` of partition q with np pages (all lanes): >= 0, -1 if the page
+    // does not exist, -2 if it exists but its table entry is out of range.
+    auto page_id = [&](int q, int np, int r0, int r1, int pg) -> int {
+        const int v = __shfl_sync(0xffffffffu, pg < 32 ? r0 : r1, pg & 31);
+        if (pg >= np) return -1;
+        return (v >= 0 && v < p.num_blocks && q * ppart + pg < p.mbps) ? v : -2;
+    };
 
     uint8_t* ring = smem + (size_t)warp * nstage * slot_bytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.ring_bytes) + warp * nstage;
@@ -176,16 +201,8 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     float* red_l = red_m + kWarps * kMaxHeadsPerCta;
     float* fin_m = red_l + kWarps * kMaxHeadsPerCta;  // [8] merged max (log2 units)
     float* fin_l = fin_m + kMaxHeadsPerCta;           // [8] merged exp-sum
-
-    // Keep the ids of pages that exist; mask (and flag) ids outside [0, num_blocks) or past
-    // the table row.
-    int bid0 = -1, bid1 = -1;
-    if (lane < npages) {
-        if (raw0 >= 0 && raw0 < p.num_blocks && lb0 + lane < p.mbps) bid0 = raw0; else flag_error(1u);
-    }
-    if (32 + lane < npages) {
-        if (raw1 >= 0 && raw1 < p.num_blocks && lb0 + 32 + lane < p.mbps) bid1 = raw1; else flag_error(1u);
-    }
+    float* red_o = fin_l + kMaxHeadsPerCta;           // [kWarps][nh][D + 4] scaled accumulators
+    constexpr int RS = D + 4;
 
     if (lane == 0) {
         for (int k = 0; k < nstage; ++k) mbar_init(&bars[k], 1);
@@ -198,36 +215,56 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     const uint8_t* vc_head = p.vcache + (size_t)kvh * page_bytes;
     const size_t block_stride = (size_t)p.Hk * page_bytes;
 
-    // Fill ring position k % nstage with this warp's k-th slot (global slot warp + k*kWarps).
-    auto issue = [&](int k) {
-        const int j = warp + k * kWarps;
-        int b[2] = {-1, -1};
-        uint32_t bytes = 0;
-#pragma unroll
-        for (int pg = 0; pg < 2; ++pg) {
-            if (pg < pps) {
-                const int page = j * pps + pg;
-                const int v = __shfl_sync(0xffffffffu, page < 32 ? bid0 : bid1, page & 31);
-                b[pg] = page < npages ? v : -1;
-                if (b[pg] >= 0) bytes += 2u * page_bytes;
+    // The warp's pages form one stream across its partitions: the issue cursor (iq, ii)
+    // runs up to nstage slots ahead of consumption and at most one partition ahead.
+    int cq = px;            // partition being consumed
+    int iq = px, ii = 0;    // issue cursor: partition, index among this warp's slots in it
+    int i_np = npages_of(iq), i_my = my_slots_of(i_np);
+    uint32_t nis = 0, ncons = 0;  // slots issued / consumed by this warp
+    bool aborted = false;
+    auto issue_more = [&]() {
+        while (!aborted && (int)(nis - ncons) < nstage) {
+            if (ii >= i_my) {
+                // move on (also past partitions where this warp has no slots), but never
+                // more than one partition ahead of the consumer
+                if (iq >= cq + PX || iq + PX >= Pl) break;
+                iq += PX;
+                ii = 0;
+                i_np = npages_of(iq);
+                i_my = my_slots_of(i_np);
+                continue;
             }
-        }
-        if (lane == 0) {
-            uint64_t* bar = &bars[k % nstage];
-            uint8_t* kdst = ring + (size_t)(k % nstage) * slot_bytes;
-            uint8_t* vdst = kdst + (size_t)pps * page_bytes;
-            mbar_arrive_expect_tx(bar, bytes);
-            for (int pg = 0; pg < pps; ++pg) {
-                if (b[pg] >= 0) {
-                    bulk_g2s(kdst + pg * page_bytes, kc_head + (size_t)b[pg] * block_stride, page_bytes, bar, policy);
-                    bulk_g2s(vdst + pg * page_bytes, vc_head + (size_t)b[pg] * block_stride, page_bytes, bar, policy);
+            const bool cur = iq == cq;
+            const int r0 = cur ? c0 : n0, r1 = cur ? c1 : n1;
+            const int j = warp + ii * kWarps;
+            int b[2] = {-1, -1};
+            uint32_t bytes = 0;
+#pragma unroll
+            for (int pg = 0; pg < 2; ++pg) {
+                if (pg < pps) {
+                    b[pg] = page_id(iq, i_np, r0, r1, j * pps + pg);
+                    if (b[pg] >= 0) bytes += 2u * page_bytes;
                 }
             }
+            if (lane == 0) {
+                const uint32_t pos = nis % nstage;
+                uint64_t* bar = &bars[pos];
+                uint8_t* kdst = ring + (size_t)pos * slot_bytes;
+                uint8_t* vdst = kdst + (size_t)pps * page_bytes;
+                mbar_arrive_expect_tx(bar, bytes);
+                for (int pg = 0; pg < pps; ++pg) {
+                    if (b[pg] >= 0) {
+                        bulk_g2s(kdst + pg * page_bytes, kc_head + (size_t)b[pg] * block_stride, page_bytes, bar, policy);
+                        bulk_g2s(vdst + pg * page_bytes, vc_head + (size_t)b[pg] * block_stride, page_bytes, bar, policy);
+                    } else if (b[pg] == -2) {
+                        flag_error(1u);
+                    }
+                }
+            }
+            ++nis;
+            ++ii;
         }
     };
-
-    const int my_slots = nslots > warp ? (nslots - warp + kWarps - 1) / kWarps : 0;
-    for (int k = 0; k < nstage && k < my_slots; ++k) issue(k);
 
     // ---- query fragments (MMA B operand: k = head dim, n = query head g) -------------------
     uint32_t qf[NK][2];
@@ -253,309 +290,331 @@ pa_v2_phase1_kernel(const Phase1Params p) {
             qf[kk][1] = b1;
         }
     }
+    issue_more();
+
     // ALiBi slopes of this thread's two head columns (2t, 2t+1), base-2 units.
     float sl0 = 0.f, sl1 = 0.f;
     if (p.alibi != nullptr) {
         if (2 * t < nh) sl0 = p.alibi[h0 + 2 * t] * kLog2e;
         if (2 * t + 1 < nh) sl1 = p.alibi[h0 + 2 * t + 1] * kLog2e;
     }
-    const int tref = t1 - 1;  // ALiBi positions are taken relative to the partition's last token
+    const float qk_mul = p.qk_scale_log2;
+    const float v_mul = p.v_scale;
 
-    // Per-lane ldmatrix row offsets inside a slot (bytes), tile 0.
-    // K rows: lane -> (row within the 16-token tile, chunk offset).
-    int k_tok, k_chunk;
-    if constexpr (FP8) {
-        k_tok = c_fp8_row_token[(lane & 7) + 8 * ((lane >> 3) & 1)];
-        k_chunk = 0;
-    } else {
-        k_tok = (lane & 7) + 8 * ((lane >> 3) & 1);
-        k_chunk = lane >> 4;
-    }
+    // Per-lane ldmatrix row of the K page: token within the 16-token tile, chunk offset.
+    const int k_tok = FP8 ? c_fp8_row_token[(lane & 7) + 8 * ((lane >> 3) & 1)] : (lane & 7) + 8 * ((lane >> 3) & 1);
+    const int k_chunk = lane >> 4;
     // Physical tokens of this thread's two MMA rows (g, g + 8).
     const int tokA = FP8 ? c_fp8_row_token[g] : g;
     const int tokB = FP8 ? c_fp8_row_token[g + 8] : g + 8;
+    const bool single = (P == 1);
+    uint32_t drain_from = 0;
 
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    float acc[NK][4];
-#pragma unroll
-    for (int i = 0; i < NK; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+    for (; cq < Pl; cq += PX) {
+        // ids of the partition after the next one (the issue cursor may need them soon)
+        int nn0 = -1, nn1 = -1;
+        if (cq + 2 * PX < Pl) load_ids(cq + 2 * PX, nn0, nn1);
+        const int t0 = cq * kPartition;
+        const int t1 = min(L, t0 + kPartition);
+        const int tref = t1 - 1;  // ALiBi positions relative to the partition's last token
+        const int c_np = npages_of(cq);
+        const int my = my_slots_of(c_np);
+        issue_more();  // in case the cursor is still behind this partition
 
-    bool aborted = false;
-    int issued = min(nstage, my_slots);
-    for (int k = 0; k < my_slots; ++k) {
-        uint64_t* bar = &bars[k % nstage];
-        if (!mbar_wait_bounded(bar, (uint32_t)((k / nstage) & 1), kWaitLimitNs)) {
-            if (lane == 0) flag_error(4u);
-            aborted = true;
-            break;
-        }
-        const int j = warp + k * kWarps;
-        const uint8_t* kslot = ring + (size_t)(k % nstage) * slot_bytes;
-        const uint8_t* vslot = kslot + (size_t)pps * page_bytes;
-        const uint32_t kbase = smem_addr(kslot), vbase = smem_addr(vslot);
-        // page validity bits of this slot
-        uint32_t okmask = 0;
+        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+        float acc[NK][4];
 #pragma unroll
-        for (int pg = 0; pg < 2; ++pg) {
-            if (pg < pps) {
-                const int page = j * pps + pg;
-                const int v = __shfl_sync(0xffffffffu, page < 32 ? bid0 : bid1, page & 31);
-                if (page < npages && v >= 0) okmask |= 1u << pg;
+        for (int i = 0; i < NK; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+
+        for (int k = 0; k < my && !aborted; ++k) {
+            const uint32_t pos = ncons % nstage;
+            if (!mbar_wait_bounded(&bars[pos], (ncons / nstage) & 1u, kWaitLimitNs)) {
+                if (lane == 0) flag_error(4u);
+                aborted = true;
+                drain_from = ncons;
+                break;
             }
-        }
-        const int stok0 = t0 + j * slot_tokens;
-
-        for (int tile = 0; tile < tiles_per_slot; ++tile) {
-            const int ttok0 = stok0 + tile * 16;
-            const int lim = t1 - ttok0;  // tokens [0, lim) of the tile are in range
-            if (lim <= 0) break;
-            const bool full = lim >= 16 && okmask == (pps == 1 ? 1u : 3u);
-            // token validity inside the tile (tile-local index)
-            auto tok_ok = [&](int tok) -> bool {
-                const int pg = pps == 1 ? 0 : (tok >> 3);
-                return tok < lim && ((okmask >> pg) & 1u);
-            };
-
-            // ---- S^T = K . Q^T for 16 tokens x 8 heads ------------------------------------
-            uint32_t krow;
-            if (pps == 1)
-                krow = kbase + (uint32_t)(k_chunk * bs + tile * 16 + k_tok) * 16u;
-            else
-                krow = kbase + (uint32_t)(k_tok >> 3) * page_bytes + (uint32_t)(k_chunk * bs + (k_tok & 7)) * 16u;
-            float sc[4] = {0.f, 0.f, 0.f, 0.f};
+            const int j = warp + k * kWarps;
+            const uint8_t* kslot = ring + (size_t)pos * slot_bytes;
+            const uint8_t* vslot = kslot + (size_t)pps * page_bytes;
+            const uint32_t kbase = smem_addr(kslot), vbase = smem_addr(vslot);
+            uint32_t okmask = 0;
 #pragma unroll
-            for (int kk = 0; kk < NK; ++kk) {
-                uint32_t a0, a1, a2, a3;
+            for (int pg = 0; pg < 2; ++pg)
+                if (pg < pps && page_id(cq, c_np, c0, c1, j * pps + pg) >= 0) okmask |= 1u << pg;
+            const int stok0 = t0 + j * slot_tokens;
+
+            for (int tile = 0; tile < tiles_per_slot; ++tile) {
+                const int ttok0 = stok0 + tile * 16;
+                const int lim = t1 - ttok0;  // tokens [0, lim) of the tile are in range
+                if (lim <= 0) break;
+                const bool full = lim >= 16 && okmask == (pps == 1 ? 1u : 3u);
+                auto tok_ok = [&](int tok) -> bool {
+                    const int pg = pps == 1 ? 0 : (tok >> 3);
+                    return tok < lim && ((okmask >> pg) & 1u);
+                };
+
+                // ---- S^T = K . Q^T for 16 tokens x 8 heads ------------------------------------
+                uint32_t krow;
+                if (pps == 1)
+                    krow = kbase + (uint32_t)(k_chunk * bs + tile * 16 + k_tok) * 16u;
+                else
+                    krow = kbase + (uint32_t)(k_tok >> 3) * page_bytes + (uint32_t)(k_chunk * bs + (k_tok & 7)) * 16u;
+                float sc[4] = {0.f, 0.f, 0.f, 0.f};
                 if constexpr (FP8) {
-                    uint32_t r0, r1;
-                    ldsm_x2(krow + (uint32_t)kk * 16u * bs, r0, r1);
-                    a0 = e4m3x2_to_mma<BF16>(lo16(r0));
-                    a2 = e4m3x2_to_mma<BF16>(hi16(r0));
-                    a1 = e4m3x2_to_mma<BF16>(lo16(r1));
-                    a3 = e4m3x2_to_mma<BF16>(hi16(r1));
+                    // one x4 load covers two 16-element steps (chunks kk, kk + 1)
+#pragma unroll
+                    for (int kk = 0; kk < NK; kk += 2) {
+                        uint32_t r[4];
+                        if (kk + 1 < NK) {
+                            ldsm_x4(krow + (uint32_t)kk * 16u * bs, r[0], r[1], r[2], r[3]);
+                        } else {
+                            ldsm_x2(krow + (uint32_t)kk * 16u * bs, r[0], r[1]);
+                            r[2] = r[3] = 0u;
+                        }
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            if (kk + h < NK) {
+                                const uint32_t a0 = e4m3x2_to_mma<BF16>(lo16(r[2 * h]));
+                                const uint32_t a2 = e4m3x2_to_mma<BF16>(hi16(r[2 * h]));
+                                const uint32_t a1 = e4m3x2_to_mma<BF16>(lo16(r[2 * h + 1]));
+                                const uint32_t a3 = e4m3x2_to_mma<BF16>(hi16(r[2 * h + 1]));
+                                mma16816<BF16>(sc, a0, a1, a2, a3, qf[kk + h][0], qf[kk + h][1]);
+                            }
+                        }
+                    }
                 } else {
-                    if (HALF_STEP && kk == NK - 1) {
-                        ldsm_x2(krow + (uint32_t)kk * 32u * bs, a0, a1);
-                        a2 = a3 = 0u;
-                    } else {
-                        ldsm_x4(krow + (uint32_t)kk * 32u * bs, a0, a1, a2, a3);
+#pragma unroll
+                    for (int kk = 0; kk < NK; ++kk) {
+                        uint32_t a0, a1, a2, a3;
+                        if (HALF_STEP && kk == NK - 1) {
+                            ldsm_x2(krow + (uint32_t)kk * 32u * bs, a0, a1);
+                            a2 = a3 = 0u;
+                        } else {
+                            ldsm_x4(krow + (uint32_t)kk * 32u * bs, a0, a1, a2, a3);
+                        }
+                        mma16816<BF16>(sc, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
                     }
                 }
-                mma16816<BF16>(sc, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
-            }
 
-            // ---- scores in base-2 units, masking, online softmax ---------------------------
-            float s0 = sc[0] * p.qk_scale_log2, s1 = sc[1] * p.qk_scale_log2;
-            float s2 = sc[2] * p.qk_scale_log2, s3 = sc[3] * p.qk_scale_log2;
-            if (p.alibi != nullptr) {
-                const float ra = (float)(ttok0 + tokA - tref), rb = (float)(ttok0 + tokB - tref);
-                s0 = fmaf(sl0, ra, s0);
-                s1 = fmaf(sl1, ra, s1);
-                s2 = fmaf(sl0, rb, s2);
-                s3 = fmaf(sl1, rb, s3);
-            }
-            if (!full) {
-                if (!tok_ok(tokA)) s0 = s1 = -INFINITY;
-                if (!tok_ok(tokB)) s2 = s3 = -INFINITY;
-            }
-            float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
-#pragma unroll
-            for (int o = 4; o < 32; o <<= 1) {
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-            }
-            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-            const float base0 = mn0 == -INFINITY ? 0.f : mn0;
-            const float base1 = mn1 == -INFINITY ? 0.f : mn1;
-            const float al0 = ex2(m0 - base0), al1 = ex2(m1 - base1);  // m = -inf -> 0
-            const float p0 = ex2(s0 - base0), p1 = ex2(s1 - base1);
-            const float p2 = ex2(s2 - base0), p3 = ex2(s3 - base1);
-            l0 = fmaf(l0, al0, p0 + p2);
-            l1 = fmaf(l1, al1, p1 + p3);
-            m0 = mn0;
-            m1 = mn1;
-#pragma unroll
-            for (int i = 0; i < NK; ++i) {
-                acc[i][0] *= al0;
-                acc[i][1] *= al1;
-                acc[i][2] *= al0;
-                acc[i][3] *= al1;
-            }
-
-            // ---- P into the B operand of O^T += V^T . P^T ----------------------------------
-            const uint32_t pb0 = movm_trans(pack2<BF16>(p0, p1));
-            const uint32_t pb1 = movm_trans(pack2<BF16>(p2, p3));
-            uint32_t pl0 = 0, pl1 = 0;
-            if constexpr (BF16) {
-                // bf16 keeps 8 significant bits; add the rounding residual as a second term
-                // so P enters the product with ~16 bits, as with fp16.
-                const float q0 = p0 - __bfloat162float(__float2bfloat16_rn(p0));
-                const float q1 = p1 - __bfloat162float(__float2bfloat16_rn(p1));
-                const float q2 = p2 - __bfloat162float(__float2bfloat16_rn(p2));
-                const float q3 = p3 - __bfloat162float(__float2bfloat16_rn(p3));
-                pl0 = movm_trans(pack2<true>(q0, q1));
-                pl1 = movm_trans(pack2<true>(q2, q3));
-            }
-
-            // ---- O^T += V^T . P^T over the head dimension ---------------------------------
-            if constexpr (!FP8) {
-                // lane -> (V row within the 16-row tile, token half)
-                const int vr = (lane & 7) + 8 * ((lane >> 3) & 1);
-                const int half = lane >> 4;
-                uint32_t vpage, vtok;
-                if (pps == 1) {
-                    vpage = vbase;
-                    vtok = (uint32_t)(tile * 16 + 8 * half);
-                } else {
-                    vpage = vbase + (uint32_t)half * page_bytes;
-                    vtok = 0;
+                // ---- scores in base-2 units, masking, online softmax ---------------------------
+                float s0 = sc[0] * qk_mul, s1 = sc[1] * qk_mul;
+                float s2 = sc[2] * qk_mul, s3 = sc[3] * qk_mul;
+                if (p.alibi != nullptr) {
+                    const float ra = (float)(ttok0 + tokA - tref), rb = (float)(ttok0 + tokB - tref);
+                    s0 = fmaf(sl0, ra, s0);
+                    s1 = fmaf(sl1, ra, s1);
+                    s2 = fmaf(sl0, rb, s2);
+                    s3 = fmaf(sl1, rb, s3);
                 }
-                // masks for this thread's token columns: a0/a1 tokens (2t, 2t+1), a2/a3 (8+2t, 9+2t)
-                uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
                 if (!full) {
-                    mlo = (tok_ok(2 * t) ? 0x0000ffffu : 0u) | (tok_ok(2 * t + 1) ? 0xffff0000u : 0u);
-                    mhi = (tok_ok(8 + 2 * t) ? 0x0000ffffu : 0u) | (tok_ok(9 + 2 * t) ? 0xffff0000u : 0u);
+                    if (!tok_ok(tokA)) s0 = s1 = -INFINITY;
+                    if (!tok_ok(tokB)) s2 = s3 = -INFINITY;
                 }
+                float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
 #pragma unroll
-                for (int mt = 0; mt < NK; ++mt) {
-                    int row = mt * 16 + vr;
-                    if (HALF_STEP && mt == NK - 1) row = min(row, D - 1);
-                    uint32_t a0, a1, a2, a3;
-                    ldsm_x4(vpage + ((uint32_t)row * bs + vtok) * 2u, a0, a1, a2, a3);
-                    a0 &= mlo;
-                    a1 &= mlo;
-                    a2 &= mhi;
-                    a3 &= mhi;
-                    mma16816<BF16>(acc[mt], a0, a1, a2, a3, pb0, pb1);
-                    if constexpr (BF16) mma16816<BF16>(acc[mt], a0, a1, a2, a3, pl0, pl1);
+                for (int o = 4; o < 32; o <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
                 }
-            } else {
-                // thread holds tokens 4t..4t+3 of rows g and g+8 of each 16-row tile
-                uint32_t vpage, vtok;
-                if (pps == 1) {
-                    vpage = vbase;
-                    vtok = (uint32_t)(tile * 16 + 4 * t);
+                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+                const float base0 = mn0 == -INFINITY ? 0.f : mn0;
+                const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+                const float al0 = ex2(m0 - base0), al1 = ex2(m1 - base1);  // m = -inf -> 0
+                const float p0 = ex2(s0 - base0), p1 = ex2(s1 - base1);
+                const float p2 = ex2(s2 - base0), p3 = ex2(s3 - base1);
+                l0 = fmaf(l0, al0, p0 + p2);
+                l1 = fmaf(l1, al1, p1 + p3);
+                m0 = mn0;
+                m1 = mn1;
+#pragma unroll
+                for (int i = 0; i < NK; ++i) {
+                    acc[i][0] *= al0;
+                    acc[i][1] *= al1;
+                    acc[i][2] *= al0;
+                    acc[i][3] *= al1;
+                }
+
+                // ---- P into the B operand of O^T += V^T . P^T ----------------------------------
+                const uint32_t pb0 = movm_trans(pack2<BF16>(p0, p1));
+                const uint32_t pb1 = movm_trans(pack2<BF16>(p2, p3));
+                uint32_t pl0 = 0, pl1 = 0;
+                if constexpr (BF16) {
+                    // bf16 keeps 8 significant bits; add the rounding residual as a second term
+                    // so P enters the product with ~16 bits, as with fp16.
+                    const float q0 = p0 - __bfloat162float(__float2bfloat16_rn(p0));
+                    const float q1 = p1 - __bfloat162float(__float2bfloat16_rn(p1));
+                    const float q2 = p2 - __bfloat162float(__float2bfloat16_rn(p2));
+                    const float q3 = p3 - __bfloat162float(__float2bfloat16_rn(p3));
+                    pl0 = movm_trans(pack2<true>(q0, q1));
+                    pl1 = movm_trans(pack2<true>(q2, q3));
+                }
+
+                // ---- O^T += V^T . P^T over the head dimension ---------------------------------
+                if constexpr (!FP8) {
+                    // lane -> (V row within the 16-row tile, token half)
+                    const int vr = (lane & 7) + 8 * ((lane >> 3) & 1);
+                    const int half = lane >> 4;
+                    uint32_t vpage, vtok;
+                    if (pps == 1) {
+                        vpage = vbase;
+                        vtok = (uint32_t)(tile * 16 + 8 * half);
+                    } else {
+                        vpage = vbase + (uint32_t)half * page_bytes;
+                        vtok = 0;
+                    }
+                    // masks for this thread's token columns: a0/a1 tokens (2t, 2t+1), a2/a3 (8+2t, 9+2t)
+                    uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+                    if (!full) {
+                        mlo = (tok_ok(2 * t) ? 0x0000ffffu : 0u) | (tok_ok(2 * t + 1) ? 0xffff0000u : 0u);
+                        mhi = (tok_ok(8 + 2 * t) ? 0x0000ffffu : 0u) | (tok_ok(9 + 2 * t) ? 0xffff0000u : 0u);
+                    }
+#pragma unroll
+                    for (int mt = 0; mt < NK; ++mt) {
+                        int row = mt * 16 + vr;
+                        if (HALF_STEP && mt == NK - 1) row = min(row, D - 1);
+                        uint32_t a0, a1, a2, a3;
+                        ldsm_x4(vpage + ((uint32_t)row * bs + vtok) * 2u, a0, a1, a2, a3);
+                        a0 &= mlo;
+                        a1 &= mlo;
+                        a2 &= mhi;
+                        a3 &= mhi;
+                        mma16816<BF16>(acc[mt], a0, a1, a2, a3, pb0, pb1);
+                        if constexpr (BF16) mma16816<BF16>(acc[mt], a0, a1, a2, a3, pl0, pl1);
+                    }
                 } else {
-                    vpage = vbase + (uint32_t)(t >> 1) * page_bytes;
-                    vtok = (uint32_t)((4 * t) & 7);
-                }
-                uint32_t bmask = 0xffffffffu;
-                if (!full) {
-                    bmask = 0;
+                    // thread holds tokens 4t..4t+3 of rows g and g+8 of each 16-row tile
+                    uint32_t vpage, vtok;
+                    if (pps == 1) {
+                        vpage = vbase;
+                        vtok = (uint32_t)(tile * 16 + 4 * t);
+                    } else {
+                        vpage = vbase + (uint32_t)(t >> 1) * page_bytes;
+                        vtok = (uint32_t)((4 * t) & 7);
+                    }
+                    uint32_t bmask = 0xffffffffu;
+                    if (!full) {
+                        bmask = 0;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        if (tok_ok(4 * t + i)) bmask |= 0xffu << (8 * i);
-                }
-                const bool swap = t >= 2;
+                        for (int i = 0; i < 4; ++i)
+                            if (tok_ok(4 * t + i)) bmask |= 0xffu << (8 * i);
+                    }
+                    const bool swap = t >= 2;
 #pragma unroll
-                for (int mt = 0; mt < NK; ++mt) {
-                    const uint32_t w0 = lds_u32(vpage + (uint32_t)(mt * 16 + g) * bs + vtok) & bmask;
-                    const uint32_t w1 = lds_u32(vpage + (uint32_t)(mt * 16 + g + 8) * bs + vtok) & bmask;
-                    const uint32_t a0 = e4m3x2_to_mma<BF16>(swap ? hi16(w0) : lo16(w0));
-                    const uint32_t a2 = e4m3x2_to_mma<BF16>(swap ? lo16(w0) : hi16(w0));
-                    const uint32_t a1 = e4m3x2_to_mma<BF16>(swap ? hi16(w1) : lo16(w1));
-                    const uint32_t a3 = e4m3x2_to_mma<BF16>(swap ? lo16(w1) : hi16(w1));
-                    mma16816<BF16>(acc[mt], a0, a1, a2, a3, pb0, pb1);
-                    if constexpr (BF16) mma16816<BF16>(acc[mt], a0, a1, a2, a3, pl0, pl1);
+                    for (int mt = 0; mt < NK; ++mt) {
+                        uint32_t w0 = lds_u32(vpage + (uint32_t)(mt * 16 + g) * bs + vtok) & bmask;
+                        uint32_t w1 = lds_u32(vpage + (uint32_t)(mt * 16 + g + 8) * bs + vtok) & bmask;
+                        if (swap) {
+                            w0 = __byte_perm(w0, 0, 0x1032);
+                            w1 = __byte_perm(w1, 0, 0x1032);
+                        }
+                        const uint32_t a0 = e4m3x2_to_mma<BF16>(lo16(w0));
+                        const uint32_t a2 = e4m3x2_to_mma<BF16>(hi16(w0));
+                        const uint32_t a1 = e4m3x2_to_mma<BF16>(lo16(w1));
+                        const uint32_t a3 = e4m3x2_to_mma<BF16>(hi16(w1));
+                        mma16816<BF16>(acc[mt], a0, a1, a2, a3, pb0, pb1);
+                        if constexpr (BF16) mma16816<BF16>(acc[mt], a0, a1, a2, a3, pl0, pl1);
+                    }
                 }
             }
+
+            // Order this slot's generic-proxy reads before the async copy that refills it.
+            ++ncons;
+            fence_proxy_async_smem();
+            __syncwarp();
+            issue_more();
         }
 
-        // Refill this ring position: order the generic-proxy reads above before the copy.
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (k + nstage < my_slots) {
-            issue(k + nstage);
-            issued = k + nstage + 1;
+        // ---- merge the warps' (m, l, acc) of this partition --------------------------------
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, o);
         }
+        if (g == 0) {
+            red_m[warp * kMaxHeadsPerCta + 2 * t] = m0;
+            red_m[warp * kMaxHeadsPerCta + 2 * t + 1] = m1;
+            red_l[warp * kMaxHeadsPerCta + 2 * t] = l0;
+            red_l[warp * kMaxHeadsPerCta + 2 * t + 1] = l1;
+        }
+        __syncthreads();
+        float M0 = -INFINITY, M1 = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            M0 = fmaxf(M0, red_m[w * kMaxHeadsPerCta + 2 * t]);
+            M1 = fmaxf(M1, red_m[w * kMaxHeadsPerCta + 2 * t + 1]);
+        }
+        const float f0 = m0 == -INFINITY ? 0.f : ex2(m0 - M0);
+        const float f1 = m1 == -INFINITY ? 0.f : ex2(m1 - M1);
+        if (warp == 0 && g == 0) {
+            float L0 = 0.f, L1 = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) {
+                const float ma = red_m[w * kMaxHeadsPerCta + 2 * t], mb = red_m[w * kMaxHeadsPerCta + 2 * t + 1];
+                if (ma != -INFINITY) L0 += red_l[w * kMaxHeadsPerCta + 2 * t] * ex2(ma - M0);
+                if (mb != -INFINITY) L1 += red_l[w * kMaxHeadsPerCta + 2 * t + 1] * ex2(mb - M1);
+            }
+            fin_m[2 * t] = M0;
+            fin_m[2 * t + 1] = M1;
+            fin_l[2 * t] = L0;
+            fin_l[2 * t + 1] = L1;
+        }
+#pragma unroll
+        for (int mt = 0; mt < NK; ++mt) {
+            const int r0 = mt * 16 + g, r1 = r0 + 8;
+            if (2 * t < nh) {
+                float* base = red_o + (warp * nh + 2 * t) * RS;
+                if (r0 < D) base[r0] = acc[mt][0] * f0;
+                if (r1 < D) base[r1] = acc[mt][2] * f0;
+            }
+            if (2 * t + 1 < nh) {
+                float* base = red_o + (warp * nh + 2 * t + 1) * RS;
+                if (r0 < D) base[r0] = acc[mt][1] * f1;
+                if (r1 < D) base[r1] = acc[mt][3] * f1;
+            }
+        }
+        __syncthreads();
+
+        for (int e = threadIdx.x; e < nh * D; e += blockDim.x) {
+            const int hh = e / D, i = e - hh * D;
+            float v = 0.f;
+#pragma unroll
+            for (int w = 0; w < kWarps; ++w) v += red_o[(w * nh + hh) * RS + i];
+            const float lt = fin_l[hh];
+            v = lt > 0.f ? v * (v_mul / lt) : 0.f;
+            const int64_t row = (int64_t)s * H + h0 + hh;
+            if (single)
+                store_out<BF16>(p.out, row * D + i, v);
+            else
+                p.tmp_out[(row * p.Pmax + cq) * D + i] = v;
+        }
+        if (threadIdx.x < nh) {
+            const int hh = threadIdx.x;
+            const int64_t sidx = ((int64_t)s * H + h0 + hh) * p.Pmax + cq;
+            const float lt = fin_l[hh];
+            float mlog = -INFINITY;
+            if (lt > 0.f) {
+                mlog = fin_m[hh] * kLn2;
+                if (p.alibi != nullptr) mlog = fmaf(p.alibi[h0 + hh], (float)tref, mlog);
+            }
+            p.max_logits[sidx] = mlog;
+            p.exp_sums[sidx] = lt;
+        }
+        __syncthreads();  // the merge buffers are reused by the next partition
+
+        // move the id buffers one partition on
+        c0 = n0;
+        c1 = n1;
+        n0 = nn0;
+        n1 = nn1;
     }
 
     if (aborted) {
         // Let every copy this warp started land before the block can exit.
-        for (int k = 0; k < issued; ++k) {
-            (void)mbar_wait_bounded(&bars[k % nstage], (uint32_t)((k / nstage) & 1), kWaitLimitNs);
-        }
+        for (uint32_t n = drain_from; n < nis; ++n)
+            (void)mbar_wait_bounded(&bars[n % nstage], (n / nstage) & 1u, kWaitLimitNs);
     }
     griddep_launch_dependents();
-
-    // ---- merge the warps' (m, l, acc) ------------------------------------------------------
-#pragma unroll
-    for (int o = 4; o < 32; o <<= 1) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, o);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, o);
-    }
-    if (g == 0) {
-        red_m[warp * kMaxHeadsPerCta + 2 * t] = m0;
-        red_m[warp * kMaxHeadsPerCta + 2 * t + 1] = m1;
-        red_l[warp * kMaxHeadsPerCta + 2 * t] = l0;
-        red_l[warp * kMaxHeadsPerCta + 2 * t + 1] = l1;
-    }
-    __syncthreads();
-    float M0 = -INFINITY, M1 = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-        M0 = fmaxf(M0, red_m[w * kMaxHeadsPerCta + 2 * t]);
-        M1 = fmaxf(M1, red_m[w * kMaxHeadsPerCta + 2 * t + 1]);
-    }
-    const float f0 = m0 == -INFINITY ? 0.f : ex2(m0 - M0);
-    const float f1 = m1 == -INFINITY ? 0.f : ex2(m1 - M1);
-    if (warp == 0 && g == 0) {
-        float L0 = 0.f, L1 = 0.f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            const float ma = red_m[w * kMaxHeadsPerCta + 2 * t], mb = red_m[w * kMaxHeadsPerCta + 2 * t + 1];
-            if (ma != -INFINITY) L0 += red_l[w * kMaxHeadsPerCta + 2 * t] * ex2(ma - M0);
-            if (mb != -INFINITY) L1 += red_l[w * kMaxHeadsPerCta + 2 * t + 1] * ex2(mb - M1);
-        }
-        fin_m[2 * t] = M0;
-        fin_m[2 * t + 1] = M1;
-        fin_l[2 * t] = L0;
-        fin_l[2 * t + 1] = L1;
-    }
-    // Scaled per-warp accumulators [warp][head][D + 4] reuse the (now idle) ring.
-    constexpr int RS = D + 4;
-    float* red_o = reinterpret_cast<float*>(smem);
-#pragma unroll
-    for (int mt = 0; mt < NK; ++mt) {
-        const int r0 = mt * 16 + g, r1 = r0 + 8;
-        float* base = red_o + (warp * kMaxHeadsPerCta + 2 * t) * RS;
-        if (r0 < D) {
-            base[r0] = acc[mt][0] * f0;
-            base[RS + r0] = acc[mt][1] * f1;
-        }
-        if (r1 < D) {
-            base[r1] = acc[mt][2] * f0;
-            base[RS + r1] = acc[mt][3] * f1;
-        }
-    }
-    __syncthreads();
-
-    const bool single = (P == 1);
-    for (int e = threadIdx.x; e < nh * D; e += blockDim.x) {
-        const int hh = e / D, i = e - hh * D;
-        float v = 0.f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) v += red_o[(w * kMaxHeadsPerCta + hh) * RS + i];
-        const float lt = fin_l[hh];
-        v = lt > 0.f ? v * (p.v_scale / lt) : 0.f;
-        const int64_t row = (int64_t)s * H + h0 + hh;
-        if (single)
-            store_out<BF16>(p.out, row * D + i, v);
-        else
-            p.tmp_out[(row * p.Pmax + part) * D + i] = v;
-    }
-    if (threadIdx.x < nh) {
-        const int hh = threadIdx.x;
-        const int64_t sidx = ((int64_t)s * H + h0 + hh) * p.Pmax + part;
-        const float lt = fin_l[hh];
-        float mlog = -INFINITY;
-        if (lt > 0.f) {
-            mlog = fin_m[hh] * kLn2;
-            if (p.alibi != nullptr) mlog = fmaf(p.alibi[h0 + hh], (float)tref, mlog);
-        }
-        p.max_logits[sidx] = mlog;
-        p.exp_sums[sidx] = lt;
-    }
 }
 
 // ---------------------------------------------------------------------------------------
@@ -816,11 +875,12 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
     // Ring depth: about kRingTarget bytes of pages per CTA, at least one slot per warp.
     int nstage = (int)(kRingTarget / (kWarps * slot_bytes));
     nstage = nstage < 1 ? 1 : (nstage > 8 ? 8 : nstage);
-    if (nstage == 1 && 2u * kWarps * slot_bytes <= 160u * 1024u) nstage = 2;
-    uint32_t ring = (uint32_t)kWarps * nstage * slot_bytes;
-    const uint32_t red_o = (uint32_t)kWarps * kMaxHeadsPerCta * (D + 4) * 4u;
-    if (ring < red_o) ring = (red_o + 127u) & ~127u;
-    const size_t smem1 = ring + kWarps * nstage * sizeof(uint64_t) + (2 * kWarps + 2) * kMaxHeadsPerCta * sizeof(float);
+    if (nstage < PA_MIN_STAGES && (uint32_t)PA_MIN_STAGES * kWarps * slot_bytes <= 160u * 1024u) nstage = PA_MIN_STAGES;
+    const uint32_t ring = (uint32_t)kWarps * nstage * slot_bytes;
+    const int red_heads = G < kMaxHeadsPerCta ? G : kMaxHeadsPerCta;
+    const size_t smem1 = ring + kWarps * nstage * sizeof(uint64_t) +
+                         (2 * kWarps + 2) * kMaxHeadsPerCta * sizeof(float) +
+                         (size_t)kWarps * red_heads * (D + 4) * sizeof(float);
 
     Phase1Fn fn = phase1_for(bf16, fp8, D);
     if (fn == nullptr) return PA_ERR_UNSUPPORTED;
@@ -864,8 +924,27 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
 
+    // Partition stride PX: each CTA takes partitions px, px + PX, ...  One partition per CTA
+    // (PX = max_num_partitions) schedules finest, but a ragged batch whose longest sequence
+    // is far above the typical one would then launch mostly empty CTAs, each holding a
+    // shared-memory slot while it starts.  So PX is capped to keep the grid within about
+    // PA_GRID_WAVES full waves, and each CTA takes at most 8 partitions.
+    int sms = 0, per_sm = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kWarps * 32, smem1) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return PA_ERR_CUDA;
+    }
+    const int64_t rows = (int64_t)a.num_kv_heads * ngroups * a.num_seqs;
+    const int64_t budget = (int64_t)PA_GRID_WAVES * sms * (per_sm > 0 ? per_sm : 1);
+    int64_t PX = budget / rows;
+    const int64_t px_min = (a.max_num_partitions + 7) / 8;
+    if (PX < px_min) PX = px_min;
+    if (PX > a.max_num_partitions) PX = a.max_num_partitions;
+    if (PX < 1) PX = 1;
+
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)a.max_num_partitions, (unsigned)(a.num_kv_heads * ngroups), (unsigned)a.num_seqs);
+    cfg.gridDim = dim3((unsigned)PX, (unsigned)(a.num_kv_heads * ngroups), (unsigned)a.num_seqs);
     cfg.blockDim = dim3(kWarps * 32, 1, 1);
     cfg.dynamicSmemBytes = smem1;
     cfg.stream = a.stream;

@@ -162,7 +162,6 @@ __device__ __forceinline__ uint32_t e4m3x2_to_mma(uint16_t v) {
     else
         return h;
 }
-// Four e4m3fn codes -> float32 x4 via f16 (exact).
 __device__ __forceinline__ uint16_t lo16(uint32_t v) { return static_cast<uint16_t>(v & 0xffffu); }
 __device__ __forceinline__ uint16_t hi16(uint32_t v) { return static_cast<uint16_t>(v >> 16); }
 
