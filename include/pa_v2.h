@@ -57,8 +57,13 @@ typedef enum {
     PA_OK = 0,
     PA_ERR_INVALID_ARG = 1, /* a pointer, size, ratio or scale breaks the contract below */
     PA_ERR_UNSUPPORTED = 2, /* a valid combination this build does not implement          */
-    PA_ERR_CUDA = 3         /* the CUDA runtime reported an error while enqueueing          */
+    PA_ERR_CUDA = 3,        /* the CUDA runtime reported an error while enqueueing          */
+    PA_ERR_SCRATCH_TOO_SMALL = 4 /* pa_v2_decode_noalloc: the step needs more than its fixed
+                                    device scratch (PA_NOALLOC_SCRATCH_BYTES)                 */
 } pa_status;
+
+/* Size of the fixed device scratch behind pa_v2_decode_noalloc (32 MiB per device). */
+#define PA_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 
 /*
  * pa_v2_decode -- one decode step of paged attention, two phases.
@@ -170,6 +175,49 @@ PA_API pa_status pa_get_device_errors(uint32_t* flags, int reset);
  * `end` just after it, so a caller can time that kernel alone.  Pass NULL, NULL to stop.
  * Process-wide and not thread-safe. */
 PA_API pa_status pa_v2_set_timing_events(cudaEvent_t begin, cudaEvent_t end);
+
+/*
+ * pa_v2_decode_noalloc -- pa_v2_decode for callers that cannot allocate device memory.
+ *
+ * Not part of the pages' interface (the paper has no counterpart); it exists for callers
+ * that are handed a stream but no allocator: an inference runtime that runs this library as
+ * a plugin with a device-memory budget fixed at start-up, code running while a stream is
+ * being captured into a CUDA graph (where a cudaMalloc would break the capture or stall on
+ * a device-wide synchronisation), or an embedded or real-time service that must not grow
+ * its footprint after initialisation.  Such a caller cannot provide the exp_sums,
+ * max_logits and tmp_output workspace that pa_v2_decode needs.
+ *
+ * Same computation and the same output as pa_v2_decode (argument meanings and layouts as
+ * there, with max_num_partitions = ceil(max_seq_len / 512) and tmp_dtype = PA_DT_F32).
+ * The workspace lives in a fixed array of PA_NOALLOC_SCRATCH_BYTES in device memory that
+ * the library defines at file scope: every GPU that loads the library holds it until the
+ * process exits.  This call allocates nothing (no cudaMalloc, cudaFree or allocating
+ * library routine).  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before any stream
+ * capture.  The partition statistics a caller of pa_v2_decode would receive are not
+ * returned.
+ *
+ * Errors: as pa_v2_decode, plus PA_ERR_SCRATCH_TOO_SMALL when
+ *   2 * align256(S*H*P*4) + S*H*P*head_size*4 > PA_NOALLOC_SCRATCH_BYTES,
+ *   P = ceil(max_seq_len / 512)
+ * (for example 64 sequences x 32 heads x head_size 128 up to 16K tokens, or 4 x 24 heads x
+ * 256 at 100K tokens, fit).  The PA_CHECK host check is not performed (it would allocate
+ * host memory).
+ *
+ * Concurrency: every call on a device shares the one array, which keeps whatever the last
+ * call left there (every entry a call reads is written by that same call first, so no
+ * clearing is needed).  Calls that can overlap on the GPU -- on different streams, or from
+ * different threads without ordering -- race on it and may return wrong results: order them
+ * on one stream or use pa_v2_decode with a workspace per stream.
+ */
+PA_API pa_status pa_v2_decode_noalloc(void* output, const void* query, const void* key_cache,
+                                      const void* value_cache, int num_seqs, int num_heads,
+                                      int num_kv_heads, int head_size, float scale,
+                                      const int32_t* block_tables, int max_blocks_per_seq,
+                                      int num_blocks, const int32_t* seq_lens, int block_size,
+                                      int max_seq_len, const float* alibi_slopes,
+                                      pa_dtype q_dtype, pa_kv_cache_dtype kv_cache_dtype,
+                                      float k_scale, float v_scale, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

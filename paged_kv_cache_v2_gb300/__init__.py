@@ -28,7 +28,9 @@ PARTITION_SIZE = 512
 
 PA_DT_F16, PA_DT_BF16, PA_DT_F32, PA_DT_FP8_E4M3 = 0, 1, 2, 3
 PA_KV_AUTO, PA_KV_FP8_E4M3 = 0, 1
-STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported combination", 3: "CUDA error"}
+STATUS = {0: "ok", 1: "invalid argument", 2: "unsupported combination", 3: "CUDA error",
+          4: "step needs more than the fixed no-allocation scratch"}
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 _lib = None
 
@@ -67,6 +69,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.pa_get_device_errors.argtypes = [ctypes.POINTER(u32), i32]
     lib.pa_v2_set_timing_events.restype = i32
     lib.pa_v2_set_timing_events.argtypes = [P, P]
+    lib.pa_v2_decode_noalloc.restype = i32
+    lib.pa_v2_decode_noalloc.argtypes = [P, P, P, P, i32, i32, i32, i32, f32, P, i32, i32, P, i32, i32,
+                                         P, i32, i32, f32, f32, P]
     _lib = lib
     return lib
 
@@ -166,6 +171,37 @@ def pa_reshape_and_cache(key: torch.Tensor, value: torch.Tensor, key_cache: torc
                                   _kv(kv_cache_dtype), float(k_scale), float(v_scale),
                                   _stream(stream))
     _check("pa_reshape_and_cache", st)
+
+
+def pa_v2_decode_noalloc(output: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
+                         value_cache: torch.Tensor, num_kv_heads: int, scale: float,
+                         block_tables: torch.Tensor, seq_lens: torch.Tensor, block_size: int,
+                         max_seq_len: int, alibi_slopes: Optional[torch.Tensor] = None,
+                         kv_cache_dtype: str = "auto", k_scale: float = 1.0, v_scale: float = 1.0,
+                         num_blocks: Optional[int] = None, stream=None) -> None:
+    """pa_v2_decode without a caller-provided workspace: for callers that cannot allocate
+    device memory (a plugin with a fixed memory budget, code running under stream capture).
+    The workspace is the library's fixed per-device scratch, shared by every call; calls that
+    can overlap on the GPU race on it."""
+    lib = load()
+    for name, t in (("output", output), ("query", query), ("key_cache", key_cache),
+                    ("value_cache", value_cache), ("block_tables", block_tables), ("seq_lens", seq_lens)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_tables and seq_lens must be int32")
+    if output.dtype != query.dtype:
+        raise TypeError("output must have the query dtype")
+    S, H, d = query.shape
+    if num_blocks is None:
+        num_blocks = key_cache.shape[0]
+    st = lib.pa_v2_decode_noalloc(_ptr(output), _ptr(query), _ptr(key_cache), _ptr(value_cache), S, H,
+                                  int(num_kv_heads), d, float(scale), _ptr(block_tables),
+                                  int(block_tables.shape[1]), int(num_blocks), _ptr(seq_lens),
+                                  int(block_size), int(max_seq_len), _ptr(alibi_slopes),
+                                  _dt(query.dtype), _kv(kv_cache_dtype), float(k_scale), float(v_scale),
+                                  _stream(stream))
+    _check("pa_v2_decode_noalloc", st)
 
 
 def pa_v2_partition_size() -> int:

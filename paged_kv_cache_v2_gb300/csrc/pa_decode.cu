@@ -40,6 +40,8 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <mutex>
+
 #include "pa_v2.h"
 #include "pa_internal.h"
 #include "pa_ptx.cuh"
@@ -800,6 +802,7 @@ extern "C" const char* pa_status_string(pa_status status) {
         case PA_ERR_INVALID_ARG: return "invalid argument";
         case PA_ERR_UNSUPPORTED: return "unsupported combination";
         case PA_ERR_CUDA: return "CUDA error";
+        case PA_ERR_SCRATCH_TOO_SMALL: return "step needs more than the fixed no-allocation scratch";
     }
     return "unknown status";
 }
@@ -1034,4 +1037,96 @@ extern "C" pa_status pa_v2_decode(void* output, float* exp_sums, float* max_logi
                            max_seq_len, stream);
     if (st != PA_OK) return st;
     return launch_decode(a, exp_sums, max_logits, (float*)tmp_output);
+}
+
+// ---------------------------------------------------------------------------------------
+// No-allocation entry point: the V2 workspace in a fixed file-scope device array
+// ---------------------------------------------------------------------------------------
+namespace pa {
+
+// Device scratch for pa_v2_decode_noalloc: exp_sums, max_logits and tmp_output of one call.
+// In host code this name is only a stand-in for the symbol; the device address comes from
+// cudaGetSymbolAddress (looked up once per device, with that device current).
+static __device__ __align__(256) unsigned char g_noalloc_scratch[PA_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+
+static pa_status noalloc_scratch(unsigned char** out) {
+    static std::mutex mu;
+    static unsigned char* addr[kMaxDevices] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        (void)cudaGetLastError();
+        return PA_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void* ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+            (void)cudaGetLastError();
+            return PA_ERR_CUDA;
+        }
+        addr[dev] = static_cast<unsigned char*>(ptr);
+    }
+    *out = addr[dev];
+    return PA_OK;
+}
+
+}  // namespace pa
+
+extern "C" pa_status pa_v2_decode_noalloc(void* output, const void* query, const void* key_cache,
+                                          const void* value_cache, int num_seqs, int num_heads,
+                                          int num_kv_heads, int head_size, float scale,
+                                          const int32_t* block_tables, int max_blocks_per_seq,
+                                          int num_blocks, const int32_t* seq_lens, int block_size,
+                                          int max_seq_len, const float* alibi_slopes,
+                                          pa_dtype q_dtype, pa_kv_cache_dtype kv_cache_dtype,
+                                          float k_scale, float v_scale, cudaStream_t stream) {
+    if (num_seqs < 0 || num_heads <= 0 || head_size <= 0 || max_seq_len < 0) return PA_ERR_INVALID_ARG;
+    const int P = max_seq_len > 0 ? (max_seq_len + kPartition - 1) / kPartition : 1;
+    const size_t rows = (size_t)num_seqs * (size_t)num_heads * (size_t)P;
+    const size_t stat_bytes = (rows * sizeof(float) + 255u) & ~(size_t)255u;
+    const size_t need = 2 * stat_bytes + rows * (size_t)head_size * sizeof(float);
+    if (need > (size_t)PA_NOALLOC_SCRATCH_BYTES) return PA_ERR_SCRATCH_TOO_SMALL;
+
+    DecodeArgs a;
+    a.output = output;
+    a.query = query;
+    a.key_cache = key_cache;
+    a.value_cache = value_cache;
+    a.num_seqs = num_seqs;
+    a.num_heads = num_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_size = head_size;
+    a.scale = scale;
+    a.block_tables = block_tables;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.seq_lens = seq_lens;
+    a.block_size = block_size;
+    a.max_seq_len = max_seq_len;
+    a.max_num_partitions = P;
+    a.alibi_slopes = alibi_slopes;
+    a.q_dtype = q_dtype;
+    a.kv_cache_dtype = kv_cache_dtype;
+    a.tmp_dtype = PA_DT_F32;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.stream = stream;
+    // placeholders so the shared argument check sees a workspace; replaced below
+    a.exp_sums = a.max_logits = reinterpret_cast<float*>(256);
+    a.tmp_output = reinterpret_cast<void*>(256);
+    pa_status st = validate_decode(a);
+    if (st != PA_OK || num_seqs == 0) return st;
+
+    unsigned char* base = nullptr;
+    st = noalloc_scratch(&base);
+    if (st != PA_OK) return st;
+    float* es = reinterpret_cast<float*>(base);
+    float* ml = reinterpret_cast<float*>(base + stat_bytes);
+    float* tmp = reinterpret_cast<float*>(base + 2 * stat_bytes);
+    a.exp_sums = es;
+    a.max_logits = ml;
+    a.tmp_output = tmp;
+    return launch_decode(a, es, ml, tmp);
 }

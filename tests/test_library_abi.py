@@ -122,3 +122,15 @@ def test_cache_writer_rejects_invalid_arguments_on_host(over, status):
 
 def test_cache_writer_with_zero_tokens_is_a_noop():
     assert _cache_raw(T=0, key=None) == 0
+
+
+def test_noalloc_entry_point_host_checks():
+    lib = pa.load()
+    P = 0x10000
+    # 64 x 32 heads x d128 at 64K tokens: ~256 MiB of workspace -> PA_ERR_SCRATCH_TOO_SMALL (4)
+    assert lib.pa_v2_decode_noalloc(P, P, P, P, 64, 32, 8, 128, 0.088, P, 4096, 100, P, 16, 65536,
+                                    None, 0, 0, 1.0, 1.0, None) == 4
+    # a null output is rejected before anything else happens
+    assert lib.pa_v2_decode_noalloc(None, P, P, P, 2, 8, 2, 128, 0.088, P, 64, 100, P, 16, 1024,
+                                    None, 0, 0, 1.0, 1.0, None) == 1
+    assert pa.pa_status_string(4).startswith("step needs more")
