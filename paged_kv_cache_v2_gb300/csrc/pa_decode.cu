@@ -117,8 +117,13 @@ __device__ __forceinline__ void store_out(void* out, int64_t idx, float v) {
 // ---------------------------------------------------------------------------------------
 // Phase 1
 // ---------------------------------------------------------------------------------------
+// Several CTAs per SM hide each other's partition boundaries; registers are capped so that
+// three (four for head sizes <= 96, whose rings are smaller) fit.
+#ifndef PA_FP8_MIN_CTAS
+#define PA_FP8_MIN_CTAS 3
+#endif
 template <bool BF16, int KVB, int D>
-__global__ void __launch_bounds__(kWarps * 32)
+__global__ void __launch_bounds__(kWarps * 32, KVB == 2 ? (D <= 96 ? 4 : 3) : ((BF16 && D >= 192) ? 2 : PA_FP8_MIN_CTAS))
 pa_v2_phase1_kernel(const Phase1Params p) {
     constexpr bool FP8 = (KVB == 1);
     constexpr int NK = (D + 15) / 16;          // 16-wide steps over the head dimension
@@ -138,7 +143,9 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     const int g = lane >> 2, t = lane & 3;
     const int H = p.H, bs = p.bs;
     const int bs_log2 = bs == 8 ? 3 : (bs == 16 ? 4 : 5);
-    const int pps = bs >= 16 ? 1 : 16 / bs;  // pages per slot
+    // A slot holds the K and V pages of 16 tokens (32 for fp8 caches: one k32 MMA step).
+    const int pps = FP8 ? 32 / bs : (bs >= 16 ? 1 : 16 / bs);  // pages per slot
+    const int pps_log2 = pps == 1 ? 0 : (pps == 2 ? 1 : 2);
     const int slot_tokens = pps * bs;
     const int tiles_per_slot = slot_tokens / 16;
     const int ppart = kPartition / bs;  // pages in a full partition
@@ -186,7 +193,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
 
     auto npages_of = [&](int q) { return ((min(L, (q + 1) * kPartition) - 1) >> bs_log2) - q * ppart + 1; };
     auto my_slots_of = [&](int np) {
-        const int ns = pps == 1 ? np : (np + 1) >> 1;
+        const int ns = (np + pps - 1) >> pps_log2;
         return ns > warp ? (ns - warp + kWarps - 1) / kWarps : 0;
     };
     // Physical id of page `pg` of partition q with np pages (all lanes): >= 0, -1 if the page
@@ -223,6 +230,10 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     int iq = px, ii = 0;    // issue cursor: partition, index among this warp's slots in it
     int i_np = npages_of(iq), i_my = my_slots_of(i_np);
     uint32_t nis = 0, ncons = 0;  // slots issued / consumed by this warp
+    // ring positions of the next slot to issue / consume, and the consumer's phase parity
+    // (kept incrementally: a runtime modulo per slot costs more than the rest of the bookkeeping)
+    int ipos = 0, cpos = 0;
+    uint32_t cphase = 0;
     bool aborted = false;
     auto issue_more = [&]() {
         while (!aborted && (int)(nis - ncons) < nstage) {
@@ -239,19 +250,18 @@ pa_v2_phase1_kernel(const Phase1Params p) {
             const bool cur = iq == cq;
             const int r0 = cur ? c0 : n0, r1 = cur ? c1 : n1;
             const int j = warp + ii * kWarps;
-            int b[2] = {-1, -1};
+            int b[4] = {-1, -1, -1, -1};
             uint32_t bytes = 0;
 #pragma unroll
-            for (int pg = 0; pg < 2; ++pg) {
+            for (int pg = 0; pg < 4; ++pg) {
                 if (pg < pps) {
                     b[pg] = page_id(iq, i_np, r0, r1, j * pps + pg);
                     if (b[pg] >= 0) bytes += 2u * page_bytes;
                 }
             }
             if (lane == 0) {
-                const uint32_t pos = nis % nstage;
-                uint64_t* bar = &bars[pos];
-                uint8_t* kdst = ring + (size_t)pos * slot_bytes;
+                uint64_t* bar = &bars[ipos];
+                uint8_t* kdst = ring + (size_t)ipos * slot_bytes;
                 uint8_t* vdst = kdst + (size_t)pps * page_bytes;
                 mbar_arrive_expect_tx(bar, bytes);
                 for (int pg = 0; pg < pps; ++pg) {
@@ -265,31 +275,105 @@ pa_v2_phase1_kernel(const Phase1Params p) {
             }
             ++nis;
             ++ii;
+            if (++ipos == nstage) ipos = 0;
         }
     };
 
     // ---- query fragments (MMA B operand: k = head dim, n = query head g) -------------------
-    uint32_t qf[NK][2];
+    // 16-bit caches: the query row as f16/bf16 pairs.  fp8 cache with an f16 query: f16 pairs
+    // in the order the widened fp8 K rows deliver the head dimension (4t..4t+3 of each 16).
+    // fp8 cache with a bf16 query: the row scaled by a power of two (per head, so the largest
+    // element lands near 224) and split into three e4m3 terms hi + mid + lo (at least 12
+    // significant bits, so every bf16 value is exact); the scale is undone on the scores.
+    constexpr int NS = (D + 31) / 32;  // k32 steps over the head dimension (fp8)
+    constexpr bool Q8 = FP8 && BF16;   // scores on the e4m3 tensor path
+    uint32_t qf[Q8 ? 1 : NK][2];
+    uint32_t qh[Q8 ? NS : 1][2], qm[Q8 ? NS : 1][2], ql[Q8 ? NS : 1][2];
+    float qs0 = 1.f, qs1 = 1.f;  // per-column score factor from the fp8 query scale
     {
         const bool live = g < nh;
         const uint16_t* qrow = reinterpret_cast<const uint16_t*>(p.query) + ((int64_t)s * H + h0 + g) * D;
+        if constexpr (!FP8) {
 #pragma unroll
-        for (int kk = 0; kk < NK; ++kk) {
-            uint32_t b0 = 0, b1 = 0;
-            if (live) {
-                if constexpr (FP8) {
-                    // fp8 rows deliver head-dim elements 4t..4t+3 of the 16-wide step.
-                    const uint2 v = *reinterpret_cast<const uint2*>(qrow + kk * 16 + 4 * t);
-                    b0 = v.x;
-                    b1 = v.y;
-                } else {
+            for (int kk = 0; kk < NK; ++kk) {
+                uint32_t b0 = 0, b1 = 0;
+                if (live) {
                     b0 = *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 2 * t);
                     if (!(HALF_STEP && kk == NK - 1))
                         b1 = *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 8 + 2 * t);
                 }
+                qf[kk][0] = b0;
+                qf[kk][1] = b1;
             }
-            qf[kk][0] = b0;
-            qf[kk][1] = b1;
+        } else if constexpr (!Q8) {
+#pragma unroll
+            for (int kk = 0; kk < NK; ++kk) {
+                uint2 v = make_uint2(0u, 0u);
+                if (live) v = *reinterpret_cast<const uint2*>(qrow + kk * 16 + 4 * t);
+                qf[kk][0] = v.x;
+                qf[kk][1] = v.y;
+            }
+        } else {
+            // thread holds elements 32 st + 16 hh + 4t + i of its head g; two passes over them
+            // (largest magnitude, then scale and split) keep few values live at once
+            auto load4 = [&](int idx, float (&f)[4]) {
+                uint2 w = make_uint2(0u, 0u);
+                if (live && idx < D) w = *reinterpret_cast<const uint2*>(qrow + idx);
+                const uint32_t ww[2] = {w.x, w.y};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint16_t bits = (uint16_t)(ww[i >> 1] >> (16 * (i & 1)));
+                    if constexpr (BF16)
+                        f[i] = __uint_as_float((uint32_t)bits << 16);
+                    else
+                        f[i] = __half2float(__ushort_as_half(bits));
+                }
+            };
+            float amax = 0.f;
+#pragma unroll
+            for (int st = 0; st < NS; ++st) {
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    float f[4];
+                    load4(32 * st + 16 * hh + 4 * t, f);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fabsf(f[i]));
+                }
+            }
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+            int e = 0;
+            if (amax > 0.f && amax < INFINITY) e = (int)floorf(__log2f(224.f / amax));
+            e = max(-100, min(100, e));
+            const float alpha = exp2f((float)e);  // exact power of two
+#pragma unroll
+            for (int st = 0; st < NS; ++st) {
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    float x[4];
+                    load4(32 * st + 16 * hh + 4 * t, x);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) x[i] *= alpha;
+                    // three successive e4m3 roundings of the remaining residual
+                    uint32_t term[3];
+#pragma unroll
+                    for (int k3 = 0; k3 < 3; ++k3) {
+                        const uint16_t c01 = f32x2_to_e4m3x2(x[0], x[1]), c23 = f32x2_to_e4m3x2(x[2], x[3]);
+                        const uint32_t d01 = e4m3x2_to_f16x2(c01), d23 = e4m3x2_to_f16x2(c23);
+                        x[0] -= f16_lo_to_f32(d01);
+                        x[1] -= f16_hi_to_f32(d01);
+                        x[2] -= f16_lo_to_f32(d23);
+                        x[3] -= f16_hi_to_f32(d23);
+                        term[k3] = (uint32_t)c01 | ((uint32_t)c23 << 16);
+                    }
+                    qh[st][hh] = term[0];
+                    qm[st][hh] = term[1];
+                    ql[st][hh] = term[2];
+                }
+            }
+            // columns 2t, 2t+1 of the score fragment belong to heads 2t, 2t+1
+            qs0 = 1.f / __shfl_sync(0xffffffffu, alpha, (2 * t) * 4);
+            qs1 = 1.f / __shfl_sync(0xffffffffu, alpha, (2 * t + 1) * 4);
         }
     }
     issue_more();
@@ -301,7 +385,9 @@ pa_v2_phase1_kernel(const Phase1Params p) {
         if (2 * t + 1 < nh) sl1 = p.alibi[h0 + 2 * t + 1] * kLog2e;
     }
     const float qk_mul = p.qk_scale_log2;
-    const float v_mul = p.v_scale;
+    const float qk_mul0 = qk_mul * qs0, qk_mul1 = qk_mul * qs1;  // fp8: per-column query scale
+    // fp8: P enters the P.V product as e4m3 of P * 256
+    const float v_mul = FP8 ? p.v_scale * (1.f / 256.f) : p.v_scale;
 
     // Per-lane ldmatrix row of the K page: token within the 16-token tile, chunk offset.
     const int k_tok = FP8 ? c_fp8_row_token[(lane & 7) + 8 * ((lane >> 3) & 1)] : (lane & 7) + 8 * ((lane >> 3) & 1);
@@ -329,8 +415,8 @@ pa_v2_phase1_kernel(const Phase1Params p) {
         for (int i = 0; i < NK; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
         for (int k = 0; k < my && !aborted; ++k) {
-            const uint32_t pos = ncons % nstage;
-            if (!mbar_wait_bounded(&bars[pos], (ncons / nstage) & 1u, kWaitLimitNs)) {
+            const int pos = cpos;
+            if (!mbar_wait_bounded(&bars[pos], cphase, kWaitLimitNs)) {
                 if (lane == 0) flag_error(4u);
                 aborted = true;
                 drain_from = ncons;
@@ -342,78 +428,71 @@ pa_v2_phase1_kernel(const Phase1Params p) {
             const uint32_t kbase = smem_addr(kslot), vbase = smem_addr(vslot);
             uint32_t okmask = 0;
 #pragma unroll
-            for (int pg = 0; pg < 2; ++pg)
+            for (int pg = 0; pg < 4; ++pg)
                 if (pg < pps && page_id(cq, c_np, c0, c1, j * pps + pg) >= 0) okmask |= 1u << pg;
             const int stok0 = t0 + j * slot_tokens;
 
-            for (int tile = 0; tile < tiles_per_slot; ++tile) {
-                const int ttok0 = stok0 + tile * 16;
-                const int lim = t1 - ttok0;  // tokens [0, lim) of the tile are in range
-                if (lim <= 0) break;
-                const bool full = lim >= 16 && okmask == (pps == 1 ? 1u : 3u);
+            if constexpr (FP8) {
+                // ---- one 32-token slot: two 16-token score tiles, one k32 P.V step ----------
+                const int lim = t1 - stok0;  // tokens [0, lim) of the slot are in range
+                const bool full = lim >= 32 && okmask == (1u << pps) - 1u;
                 auto tok_ok = [&](int tok) -> bool {
-                    const int pg = pps == 1 ? 0 : (tok >> 3);
-                    return tok < lim && ((okmask >> pg) & 1u);
+                    return tok < lim && ((okmask >> (tok >> bs_log2)) & 1u);
                 };
-
-                // ---- S^T = K . Q^T for 16 tokens x 8 heads ------------------------------------
-                uint32_t krow;
-                if (pps == 1)
-                    krow = kbase + (uint32_t)(k_chunk * bs + tile * 16 + k_tok) * 16u;
-                else
-                    krow = kbase + (uint32_t)(k_tok >> 3) * page_bytes + (uint32_t)(k_chunk * bs + (k_tok & 7)) * 16u;
-                float sc[4] = {0.f, 0.f, 0.f, 0.f};
-                if constexpr (FP8) {
-                    // one x4 load covers two 16-element steps (chunks kk, kk + 1)
+                float sv[2][4];
 #pragma unroll
-                    for (int kk = 0; kk < NK; kk += 2) {
-                        uint32_t r[4];
-                        if (kk + 1 < NK) {
-                            ldsm_x4(krow + (uint32_t)kk * 16u * bs, r[0], r[1], r[2], r[3]);
-                        } else {
-                            ldsm_x2(krow + (uint32_t)kk * 16u * bs, r[0], r[1]);
-                            r[2] = r[3] = 0u;
-                        }
+                for (int tile = 0; tile < 2; ++tile) {
+                    // S^T = K . Q^T on the e4m3 codes; rows are tokens in c_fp8_row_token order
+                    const int tt = tile * 16 + k_tok;
+                    const uint32_t krow = kbase + (uint32_t)(tt >> bs_log2) * page_bytes +
+                                          (uint32_t)(k_chunk * bs + (tt & (bs - 1))) * 16u;
+                    float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            if (kk + h < NK) {
-                                const uint32_t a0 = e4m3x2_to_mma<BF16>(lo16(r[2 * h]));
-                                const uint32_t a2 = e4m3x2_to_mma<BF16>(hi16(r[2 * h]));
-                                const uint32_t a1 = e4m3x2_to_mma<BF16>(lo16(r[2 * h + 1]));
-                                const uint32_t a3 = e4m3x2_to_mma<BF16>(hi16(r[2 * h + 1]));
-                                mma16816<BF16>(sc, a0, a1, a2, a3, qf[kk + h][0], qf[kk + h][1]);
-                            }
-                        }
-                    }
-                } else {
-#pragma unroll
-                    for (int kk = 0; kk < NK; ++kk) {
+                    for (int st = 0; st < NS; ++st) {
                         uint32_t a0, a1, a2, a3;
-                        if (HALF_STEP && kk == NK - 1) {
-                            ldsm_x2(krow + (uint32_t)kk * 32u * bs, a0, a1);
-                            a2 = a3 = 0u;
+                        if (2 * st + 1 < NK) {
+                            ldsm_x4(krow + (uint32_t)st * 32u * bs, a0, a1, a2, a3);
                         } else {
-                            ldsm_x4(krow + (uint32_t)kk * 32u * bs, a0, a1, a2, a3);
+                            ldsm_x2(krow + (uint32_t)st * 32u * bs, a0, a1);
+                            a2 = a3 = 0u;
                         }
-                        mma16816<BF16>(sc, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+                        if constexpr (Q8) {
+                            mma_e4m3_16832(sc, a0, a1, a2, a3, qh[st][0], qh[st][1]);
+                            mma_e4m3_16832(sc, a0, a1, a2, a3, qm[st][0], qm[st][1]);
+                            mma_e4m3_16832(sc, a0, a1, a2, a3, ql[st][0], ql[st][1]);
+                        } else {
+                            // widen the K codes to f16 (exact): chunk 2st in a0/a1, 2st+1 in a2/a3
+                            mma16816<false>(sc, e4m3x2_to_f16x2(lo16(a0)), e4m3x2_to_f16x2(lo16(a1)),
+                                            e4m3x2_to_f16x2(hi16(a0)), e4m3x2_to_f16x2(hi16(a1)),
+                                            qf[2 * st][0], qf[2 * st][1]);
+                            if (2 * st + 1 < NK)
+                                mma16816<false>(sc, e4m3x2_to_f16x2(lo16(a2)), e4m3x2_to_f16x2(lo16(a3)),
+                                                e4m3x2_to_f16x2(hi16(a2)), e4m3x2_to_f16x2(hi16(a3)),
+                                                qf[2 * st + 1][0], qf[2 * st + 1][1]);
+                        }
                     }
+                    const int ttok0 = stok0 + tile * 16;
+                    float s0 = sc[0] * qk_mul0, s1 = sc[1] * qk_mul1;
+                    float s2 = sc[2] * qk_mul0, s3 = sc[3] * qk_mul1;
+                    if (p.alibi != nullptr) {
+                        const float ra = (float)(ttok0 + tokA - tref), rb = (float)(ttok0 + tokB - tref);
+                        s0 = fmaf(sl0, ra, s0);
+                        s1 = fmaf(sl1, ra, s1);
+                        s2 = fmaf(sl0, rb, s2);
+                        s3 = fmaf(sl1, rb, s3);
+                    }
+                    if (!full) {
+                        if (!tok_ok(tile * 16 + tokA)) s0 = s1 = -INFINITY;
+                        if (!tok_ok(tile * 16 + tokB)) s2 = s3 = -INFINITY;
+                    }
+                    sv[tile][0] = s0;
+                    sv[tile][1] = s1;
+                    sv[tile][2] = s2;
+                    sv[tile][3] = s3;
                 }
-
-                // ---- scores in base-2 units, masking, online softmax ---------------------------
-                float s0 = sc[0] * qk_mul, s1 = sc[1] * qk_mul;
-                float s2 = sc[2] * qk_mul, s3 = sc[3] * qk_mul;
-                if (p.alibi != nullptr) {
-                    const float ra = (float)(ttok0 + tokA - tref), rb = (float)(ttok0 + tokB - tref);
-                    s0 = fmaf(sl0, ra, s0);
-                    s1 = fmaf(sl1, ra, s1);
-                    s2 = fmaf(sl0, rb, s2);
-                    s3 = fmaf(sl1, rb, s3);
-                }
-                if (!full) {
-                    if (!tok_ok(tokA)) s0 = s1 = -INFINITY;
-                    if (!tok_ok(tokB)) s2 = s3 = -INFINITY;
-                }
-                float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+                // online softmax over the slot's 32 tokens
+                float mx0 = fmaxf(fmaxf(sv[0][0], sv[0][2]), fmaxf(sv[1][0], sv[1][2]));
+                float mx1 = fmaxf(fmaxf(sv[0][1], sv[0][3]), fmaxf(sv[1][1], sv[1][3]));
 #pragma unroll
                 for (int o = 4; o < 32; o <<= 1) {
                     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
@@ -422,106 +501,223 @@ pa_v2_phase1_kernel(const Phase1Params p) {
                 const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
                 const float base0 = mn0 == -INFINITY ? 0.f : mn0;
                 const float base1 = mn1 == -INFINITY ? 0.f : mn1;
-                const float al0 = ex2(m0 - base0), al1 = ex2(m1 - base1);  // m = -inf -> 0
-                const float p0 = ex2(s0 - base0), p1 = ex2(s1 - base1);
-                const float p2 = ex2(s2 - base0), p3 = ex2(s3 - base1);
-                l0 = fmaf(l0, al0, p0 + p2);
-                l1 = fmaf(l1, al1, p1 + p3);
+                const float al0 = ex2(m0 - base0), al1 = ex2(m1 - base1);
+                float pv[2][4];
+#pragma unroll
+                for (int tile = 0; tile < 2; ++tile) {
+                    pv[tile][0] = ex2(sv[tile][0] - base0);
+                    pv[tile][1] = ex2(sv[tile][1] - base1);
+                    pv[tile][2] = ex2(sv[tile][2] - base0);
+                    pv[tile][3] = ex2(sv[tile][3] - base1);
+                }
+                l0 = fmaf(l0, al0, (pv[0][0] + pv[0][2]) + (pv[1][0] + pv[1][2]));
+                l1 = fmaf(l1, al1, (pv[0][1] + pv[0][3]) + (pv[1][1] + pv[1][3]));
+                if (__any_sync(0xffffffffu, mn0 != m0 || mn1 != m1)) {
+#pragma unroll
+                    for (int i = 0; i < NK; ++i) {
+                        acc[i][0] *= al0;
+                        acc[i][1] *= al1;
+                        acc[i][2] *= al0;
+                        acc[i][3] *= al1;
+                    }
+                }
                 m0 = mn0;
                 m1 = mn1;
+                // P^T operand: P * 256 as f16, transposed with movmatrix, split into e4m3 hi + lo.
+                // After the transpose thread t holds tokens {4t..4t+3} of head g (rows 2t, 2t+1
+                // and 8+2t, 9+2t in the token order above; the halves swap for t >= 2).
+                uint32_t bh[2], bl[2];
 #pragma unroll
-                for (int i = 0; i < NK; ++i) {
-                    acc[i][0] *= al0;
-                    acc[i][1] *= al1;
-                    acc[i][2] *= al0;
-                    acc[i][3] *= al1;
-                }
-
-                // ---- P into the B operand of O^T += V^T . P^T ----------------------------------
-                const uint32_t pb0 = movm_trans(pack2<BF16>(p0, p1));
-                const uint32_t pb1 = movm_trans(pack2<BF16>(p2, p3));
-                uint32_t pl0 = 0, pl1 = 0;
-                if constexpr (BF16) {
-                    // bf16 keeps 8 significant bits; add the rounding residual as a second term
-                    // so P enters the product with ~16 bits, as with fp16.
-                    const float q0 = p0 - __bfloat162float(__float2bfloat16_rn(p0));
-                    const float q1 = p1 - __bfloat162float(__float2bfloat16_rn(p1));
-                    const float q2 = p2 - __bfloat162float(__float2bfloat16_rn(p2));
-                    const float q3 = p3 - __bfloat162float(__float2bfloat16_rn(p3));
-                    pl0 = movm_trans(pack2<true>(q0, q1));
-                    pl1 = movm_trans(pack2<true>(q2, q3));
-                }
-
-                // ---- O^T += V^T . P^T over the head dimension ---------------------------------
-                if constexpr (!FP8) {
-                    // lane -> (V row within the 16-row tile, token half)
-                    const int vr = (lane & 7) + 8 * ((lane >> 3) & 1);
-                    const int half = lane >> 4;
-                    uint32_t vpage, vtok;
-                    if (pps == 1) {
-                        vpage = vbase;
-                        vtok = (uint32_t)(tile * 16 + 8 * half);
+                for (int tile = 0; tile < 2; ++tile) {
+                    const uint32_t x0 = movm_trans(pack2<false>(pv[tile][0] * 256.f, pv[tile][1] * 256.f));
+                    const uint32_t x1 = movm_trans(pack2<false>(pv[tile][2] * 256.f, pv[tile][3] * 256.f));
+                    uint16_t h0, l0b, h1, l1b;
+                    split_e4m3x2(x0, h0, l0b);
+                    split_e4m3x2(x1, h1, l1b);
+                    if (t < 2) {
+                        bh[tile] = (uint32_t)h0 | ((uint32_t)h1 << 16);
+                        bl[tile] = (uint32_t)l0b | ((uint32_t)l1b << 16);
                     } else {
-                        vpage = vbase + (uint32_t)half * page_bytes;
-                        vtok = 0;
+                        bh[tile] = (uint32_t)h1 | ((uint32_t)h0 << 16);
+                        bl[tile] = (uint32_t)l1b | ((uint32_t)l0b << 16);
                     }
-                    // masks for this thread's token columns: a0/a1 tokens (2t, 2t+1), a2/a3 (8+2t, 9+2t)
-                    uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
-                    if (!full) {
-                        mlo = (tok_ok(2 * t) ? 0x0000ffffu : 0u) | (tok_ok(2 * t + 1) ? 0xffff0000u : 0u);
-                        mhi = (tok_ok(8 + 2 * t) ? 0x0000ffffu : 0u) | (tok_ok(9 + 2 * t) ? 0xffff0000u : 0u);
+                }
+                // O^T += V^T . P^T: V rows straight from the page, 32 tokens per step
+                uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;  // bytes of masked tokens -> 0
+                if (!full) {
+                    mlo = 0u;
+                    mhi = 0u;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        if (tok_ok(4 * t + i)) mlo |= 0xffu << (8 * i);
+                        if (tok_ok(16 + 4 * t + i)) mhi |= 0xffu << (8 * i);
                     }
+                }
+                if (bs >= 16) {
+                    const int vr = (lane & 7) + 8 * ((lane >> 3) & 1);
+                    const int tk = 16 * (lane >> 4);  // token half of this lane's matrix row
+                    const uint32_t vrow = vbase + (uint32_t)(tk >> bs_log2) * page_bytes + (uint32_t)(vr * bs + (tk & (bs - 1)));
 #pragma unroll
                     for (int mt = 0; mt < NK; ++mt) {
-                        int row = mt * 16 + vr;
-                        if (HALF_STEP && mt == NK - 1) row = min(row, D - 1);
                         uint32_t a0, a1, a2, a3;
-                        ldsm_x4(vpage + ((uint32_t)row * bs + vtok) * 2u, a0, a1, a2, a3);
+                        ldsm_x4(vrow + (uint32_t)mt * 16u * bs, a0, a1, a2, a3);
                         a0 &= mlo;
                         a1 &= mlo;
                         a2 &= mhi;
                         a3 &= mhi;
-                        mma16816<BF16>(acc[mt], a0, a1, a2, a3, pb0, pb1);
-                        if constexpr (BF16) mma16816<BF16>(acc[mt], a0, a1, a2, a3, pl0, pl1);
+                        mma_e4m3_16832(acc[mt], a0, a1, a2, a3, bh[0], bh[1]);
+                        mma_e4m3_16832(acc[mt], a0, a1, a2, a3, bl[0], bl[1]);
                     }
                 } else {
-                    // thread holds tokens 4t..4t+3 of rows g and g+8 of each 16-row tile
-                    uint32_t vpage, vtok;
-                    if (pps == 1) {
-                        vpage = vbase;
-                        vtok = (uint32_t)(tile * 16 + 4 * t);
-                    } else {
-                        vpage = vbase + (uint32_t)(t >> 1) * page_bytes;
-                        vtok = (uint32_t)((4 * t) & 7);
-                    }
-                    uint32_t bmask = 0xffffffffu;
-                    if (!full) {
-                        bmask = 0;
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            if (tok_ok(4 * t + i)) bmask |= 0xffu << (8 * i);
-                    }
-                    const bool swap = t >= 2;
+                    // block size 8: a V row holds 8 tokens, so read each thread's 4 tokens
+                    const uint32_t va = vbase + (uint32_t)(t >> 1) * page_bytes + (uint32_t)((4 * t) & 7);
+                    const uint32_t vb = va + 2u * page_bytes;
 #pragma unroll
                     for (int mt = 0; mt < NK; ++mt) {
-                        uint32_t w0 = lds_u32(vpage + (uint32_t)(mt * 16 + g) * bs + vtok) & bmask;
-                        uint32_t w1 = lds_u32(vpage + (uint32_t)(mt * 16 + g + 8) * bs + vtok) & bmask;
-                        if (swap) {
-                            w0 = __byte_perm(w0, 0, 0x1032);
-                            w1 = __byte_perm(w1, 0, 0x1032);
-                        }
-                        const uint32_t a0 = e4m3x2_to_mma<BF16>(lo16(w0));
-                        const uint32_t a2 = e4m3x2_to_mma<BF16>(hi16(w0));
-                        const uint32_t a1 = e4m3x2_to_mma<BF16>(lo16(w1));
-                        const uint32_t a3 = e4m3x2_to_mma<BF16>(hi16(w1));
-                        mma16816<BF16>(acc[mt], a0, a1, a2, a3, pb0, pb1);
-                        if constexpr (BF16) mma16816<BF16>(acc[mt], a0, a1, a2, a3, pl0, pl1);
+                        const uint32_t r0 = (uint32_t)(mt * 16 + g) * bs, r1 = r0 + 8u * bs;
+                        const uint32_t a0 = lds_u32(va + r0) & mlo, a1 = lds_u32(va + r1) & mlo;
+                        const uint32_t a2 = lds_u32(vb + r0) & mhi, a3 = lds_u32(vb + r1) & mhi;
+                        mma_e4m3_16832(acc[mt], a0, a1, a2, a3, bh[0], bh[1]);
+                        mma_e4m3_16832(acc[mt], a0, a1, a2, a3, bl[0], bl[1]);
                     }
+                }
+            } else {
+                for (int tile = 0; tile < tiles_per_slot; ++tile) {
+                    const int ttok0 = stok0 + tile * 16;
+                    const int lim = t1 - ttok0;  // tokens [0, lim) of the tile are in range
+                    if (lim <= 0) break;
+                    const bool full = lim >= 16 && okmask == (pps == 1 ? 1u : 3u);
+                    auto tok_ok = [&](int tok) -> bool {
+                        const int pg = pps == 1 ? 0 : (tok >> 3);
+                        return tok < lim && ((okmask >> pg) & 1u);
+                    };
+
+                    // ---- S^T = K . Q^T for 16 tokens x 8 heads ------------------------------------
+                    uint32_t krow;
+                    if (pps == 1)
+                        krow = kbase + (uint32_t)(k_chunk * bs + tile * 16 + k_tok) * 16u;
+                    else
+                        krow = kbase + (uint32_t)(k_tok >> 3) * page_bytes + (uint32_t)(k_chunk * bs + (k_tok & 7)) * 16u;
+                    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+    #pragma unroll
+                        for (int kk = 0; kk < NK; ++kk) {
+                            uint32_t a0, a1, a2, a3;
+                            if (HALF_STEP && kk == NK - 1) {
+                                ldsm_x2(krow + (uint32_t)kk * 32u * bs, a0, a1);
+                                a2 = a3 = 0u;
+                            } else {
+                                ldsm_x4(krow + (uint32_t)kk * 32u * bs, a0, a1, a2, a3);
+                            }
+                            mma16816<BF16>(sc, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+                        }
+
+                    // ---- scores in base-2 units, masking, online softmax ---------------------------
+                    float s0 = sc[0] * qk_mul, s1 = sc[1] * qk_mul;
+                    float s2 = sc[2] * qk_mul, s3 = sc[3] * qk_mul;
+                    if (p.alibi != nullptr) {
+                        const float ra = (float)(ttok0 + tokA - tref), rb = (float)(ttok0 + tokB - tref);
+                        s0 = fmaf(sl0, ra, s0);
+                        s1 = fmaf(sl1, ra, s1);
+                        s2 = fmaf(sl0, rb, s2);
+                        s3 = fmaf(sl1, rb, s3);
+                    }
+                    if (!full) {
+                        if (!tok_ok(tokA)) s0 = s1 = -INFINITY;
+                        if (!tok_ok(tokB)) s2 = s3 = -INFINITY;
+                    }
+                    float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+    #pragma unroll
+                    for (int o = 4; o < 32; o <<= 1) {
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
+                    }
+                    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+                    const float base0 = mn0 == -INFINITY ? 0.f : mn0;
+                    const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+                    const float al0 = ex2(m0 - base0), al1 = ex2(m1 - base1);  // m = -inf -> 0
+                    const float p0 = ex2(s0 - base0), p1 = ex2(s1 - base1);
+                    const float p2 = ex2(s2 - base0), p3 = ex2(s3 - base1);
+                    l0 = fmaf(l0, al0, p0 + p2);
+                    l1 = fmaf(l1, al1, p1 + p3);
+                    // Rescale the accumulators only when some head's running max moved (after the
+                    // first tiles of a partition it rarely does); otherwise the factors are 1.
+                    if (__any_sync(0xffffffffu, mn0 != m0 || mn1 != m1)) {
+    #pragma unroll
+                        for (int i = 0; i < NK; ++i) {
+                            acc[i][0] *= al0;
+                            acc[i][1] *= al1;
+                            acc[i][2] *= al0;
+                            acc[i][3] *= al1;
+                        }
+                    }
+                    m0 = mn0;
+                    m1 = mn1;
+
+                    // ---- P into the B operand of O^T += V^T . P^T ----------------------------------
+                    const uint32_t pb0 = movm_trans(pack2<BF16>(p0, p1));
+                    const uint32_t pb1 = movm_trans(pack2<BF16>(p2, p3));
+                    uint32_t pl0 = 0, pl1 = 0;
+                    if constexpr (BF16) {
+                        // bf16 keeps 8 significant bits; add the rounding residual as a second term
+                        // so P enters the product with ~16 bits, as with fp16.
+                        const float q0 = p0 - __bfloat162float(__float2bfloat16_rn(p0));
+                        const float q1 = p1 - __bfloat162float(__float2bfloat16_rn(p1));
+                        const float q2 = p2 - __bfloat162float(__float2bfloat16_rn(p2));
+                        const float q3 = p3 - __bfloat162float(__float2bfloat16_rn(p3));
+                        pl0 = movm_trans(pack2<true>(q0, q1));
+                        pl1 = movm_trans(pack2<true>(q2, q3));
+                    }
+
+                    // ---- O^T += V^T . P^T over the head dimension ---------------------------------
+                        // lane -> (V row within the 16-row tile, token half)
+                        const int vr = (lane & 7) + 8 * ((lane >> 3) & 1);
+                        const int half = lane >> 4;
+                        uint32_t vpage, vtok;
+                        if (pps == 1) {
+                            vpage = vbase;
+                            vtok = (uint32_t)(tile * 16 + 8 * half);
+                        } else {
+                            vpage = vbase + (uint32_t)half * page_bytes;
+                            vtok = 0;
+                        }
+                        if (full) {
+    #pragma unroll
+                            for (int mt = 0; mt < NK; ++mt) {
+                                int row = mt * 16 + vr;
+                                if (HALF_STEP && mt == NK - 1) row = min(row, D - 1);
+                                uint32_t a0, a1, a2, a3;
+                                ldsm_x4(vpage + ((uint32_t)row * bs + vtok) * 2u, a0, a1, a2, a3);
+                                mma16816<BF16>(acc[mt], a0, a1, a2, a3, pb0, pb1);
+                                if constexpr (BF16) mma16816<BF16>(acc[mt], a0, a1, a2, a3, pl0, pl1);
+                            }
+                        } else {
+                            // zero the V columns of masked tokens (0 * NaN would poison every head):
+                            // a0/a1 hold tokens (2t, 2t+1), a2/a3 tokens (8+2t, 9+2t)
+                            const uint32_t mlo = (tok_ok(2 * t) ? 0x0000ffffu : 0u) | (tok_ok(2 * t + 1) ? 0xffff0000u : 0u);
+                            const uint32_t mhi = (tok_ok(8 + 2 * t) ? 0x0000ffffu : 0u) | (tok_ok(9 + 2 * t) ? 0xffff0000u : 0u);
+    #pragma unroll
+                            for (int mt = 0; mt < NK; ++mt) {
+                                int row = mt * 16 + vr;
+                                if (HALF_STEP && mt == NK - 1) row = min(row, D - 1);
+                                uint32_t a0, a1, a2, a3;
+                                ldsm_x4(vpage + ((uint32_t)row * bs + vtok) * 2u, a0, a1, a2, a3);
+                                a0 &= mlo;
+                                a1 &= mlo;
+                                a2 &= mhi;
+                                a3 &= mhi;
+                                mma16816<BF16>(acc[mt], a0, a1, a2, a3, pb0, pb1);
+                                if constexpr (BF16) mma16816<BF16>(acc[mt], a0, a1, a2, a3, pl0, pl1);
+                            }
+                        }
                 }
             }
 
             // Order this slot's generic-proxy reads before the async copy that refills it.
             ++ncons;
+            if (++cpos == nstage) {
+                cpos = 0;
+                cphase ^= 1u;
+            }
             fence_proxy_async_smem();
             __syncwarp();
             issue_more();
@@ -872,7 +1068,7 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
     const int G = a.num_heads / a.num_kv_heads;
     const int ngroups = (G + kMaxHeadsPerCta - 1) / kMaxHeadsPerCta;
     const int kvb = fp8 ? 1 : 2;
-    const int pps = bs >= 16 ? 1 : 16 / bs;
+    const int pps = fp8 ? 32 / bs : (bs >= 16 ? 1 : 16 / bs);  // pages per ring slot, as in the kernel
     const uint32_t page_bytes = (uint32_t)D * bs * kvb;
     const uint32_t slot_bytes = 2u * pps * page_bytes;
     // Ring depth: about kRingTarget bytes of pages per CTA, at least one slot per warp.

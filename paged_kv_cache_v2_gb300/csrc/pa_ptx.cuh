@@ -56,11 +56,27 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
+// try_wait with a suspend-time hint: the thread sleeps in hardware until the phase
+// completes or about `hint_ns` elapse, instead of spinning on issue slots.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+#ifndef PA_WAIT_HINT_NS
+#define PA_WAIT_HINT_NS 100000
+#endif
 // Wait for the barrier phase with the given parity; give up after `limit_ns` nanoseconds.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity)) {
+    while (!mbar_try_wait_hint(bar, parity, PA_WAIT_HINT_NS)) {
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
     return true;
@@ -126,6 +142,16 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
     }
 }
 
+// fp8 e4m3 x e4m3 -> fp32, m16n8k32: each 32-bit A/B register holds four consecutive k.
+__device__ __forceinline__ void mma_e4m3_16832(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, "
+        "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // ---- conversions ------------------------------------------------------------------------
 // Two floats -> packed 16-bit pair, `lo` in the low half.
 template <bool BF16>
@@ -172,9 +198,27 @@ __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
     return d;
 }
 
+// f16x2 -> two e4m3fn codes (RNE, saturating); the low half becomes the low byte.
+__device__ __forceinline__ uint16_t f16x2_to_e4m3x2(uint32_t v) {
+    uint16_t d;
+    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(d) : "r"(v));
+    return d;
+}
+__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+// A value split into two e4m3 terms, hi + lo: hi = e4m3(v), lo = e4m3(v - hi).  For the
+// f16x2 pair v the residual is exact in f16 (hi is within 2^-4 of v).
+__device__ __forceinline__ void split_e4m3x2(uint32_t v, uint16_t& hi, uint16_t& lo) {
+    hi = f16x2_to_e4m3x2(v);
+    lo = f16x2_to_e4m3x2(hsub2(v, e4m3x2_to_f16x2(hi)));
+}
+
 __device__ __forceinline__ float ex2(float x) {
     float y;
-    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));  // subnormal weights flush to 0
     return y;
 }
 
