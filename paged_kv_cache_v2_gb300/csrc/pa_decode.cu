@@ -60,7 +60,7 @@ static __device__ unsigned int g_device_errors = 0;
 #define PA_MIN_STAGES 1
 #endif
 #ifndef PA_GRID_WAVES
-#define PA_GRID_WAVES 64
+#define PA_GRID_WAVES 16
 #endif
 
 constexpr int kPartition = 512;
@@ -118,12 +118,13 @@ __device__ __forceinline__ void store_out(void* out, int64_t idx, float v) {
 // Phase 1
 // ---------------------------------------------------------------------------------------
 // Several CTAs per SM hide each other's partition boundaries; registers are capped so that
-// three (four for head sizes <= 96, whose rings are smaller) fit.
+// twelve warps (sixteen for head sizes <= 96, whose rings are smaller) fit on an SM.
 #ifndef PA_FP8_MIN_CTAS
 #define PA_FP8_MIN_CTAS 3
 #endif
 template <bool BF16, int KVB, int D>
-__global__ void __launch_bounds__(kWarps * 32, KVB == 2 ? (D <= 96 ? 4 : 3) : ((BF16 && D >= 192) ? 2 : PA_FP8_MIN_CTAS))
+__global__ void __launch_bounds__(kWarps * 32, KVB == 2 ? (D <= 96 ? 16 : 12) / kWarps
+                                                        : ((BF16 && D >= 192) ? 8 : 4 * PA_FP8_MIN_CTAS) / kWarps)
 pa_v2_phase1_kernel(const Phase1Params p) {
     constexpr bool FP8 = (KVB == 1);
     constexpr int NK = (D + 15) / 16;          // 16-wide steps over the head dimension
@@ -557,16 +558,26 @@ pa_v2_phase1_kernel(const Phase1Params p) {
                     const int vr = (lane & 7) + 8 * ((lane >> 3) & 1);
                     const int tk = 16 * (lane >> 4);  // token half of this lane's matrix row
                     const uint32_t vrow = vbase + (uint32_t)(tk >> bs_log2) * page_bytes + (uint32_t)(vr * bs + (tk & (bs - 1)));
+                    if (full) {
 #pragma unroll
-                    for (int mt = 0; mt < NK; ++mt) {
-                        uint32_t a0, a1, a2, a3;
-                        ldsm_x4(vrow + (uint32_t)mt * 16u * bs, a0, a1, a2, a3);
-                        a0 &= mlo;
-                        a1 &= mlo;
-                        a2 &= mhi;
-                        a3 &= mhi;
-                        mma_e4m3_16832(acc[mt], a0, a1, a2, a3, bh[0], bh[1]);
-                        mma_e4m3_16832(acc[mt], a0, a1, a2, a3, bl[0], bl[1]);
+                        for (int mt = 0; mt < NK; ++mt) {
+                            uint32_t a0, a1, a2, a3;
+                            ldsm_x4(vrow + (uint32_t)mt * 16u * bs, a0, a1, a2, a3);
+                            mma_e4m3_16832(acc[mt], a0, a1, a2, a3, bh[0], bh[1]);
+                            mma_e4m3_16832(acc[mt], a0, a1, a2, a3, bl[0], bl[1]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int mt = 0; mt < NK; ++mt) {
+                            uint32_t a0, a1, a2, a3;
+                            ldsm_x4(vrow + (uint32_t)mt * 16u * bs, a0, a1, a2, a3);
+                            a0 &= mlo;
+                            a1 &= mlo;
+                            a2 &= mhi;
+                            a3 &= mhi;
+                            mma_e4m3_16832(acc[mt], a0, a1, a2, a3, bh[0], bh[1]);
+                            mma_e4m3_16832(acc[mt], a0, a1, a2, a3, bl[0], bl[1]);
+                        }
                     }
                 } else {
                     // block size 8: a V row holds 8 tokens, so read each thread's 4 tokens
@@ -844,28 +855,59 @@ pa_v2_phase2_kernel(const Phase2Params p) {
     const float* es = p.exp_sums + row * p.Pmax;
     const float4* tmp = reinterpret_cast<const float4*>(p.tmp_out + row * p.Pmax * D);
 
+    // Warp w owns partitions w, w + W, ...  Their statistics load one per lane (32 at a
+    // time) and reduce with shuffles; the tmp rows then stream with independent loads.
     float m = -INFINITY, l = 0.f;
     float4 acc[kP2MaxCols];
 #pragma unroll
     for (int k = 0; k < kP2MaxCols; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i = warp; i < P; i += W) {
-        const float mi = ml[i] * kLog2e, li = es[i];
-        float4 x[kP2MaxCols];
-#pragma unroll
-        for (int k = 0; k < kP2MaxCols; ++k) {
-            const int c = lane + 32 * k;
-            x[k] = c < nq ? tmp[(int64_t)i * nq + c] : make_float4(0.f, 0.f, 0.f, 0.f);
+    const int mine = P > warp ? (P - warp + W - 1) / W : 0;  // partitions of this warp
+    for (int j0 = 0; j0 < mine; j0 += 32) {
+        const int nc = min(32, mine - j0);
+        float mj = -INFINITY, lj = 0.f;
+        if (lane < nc) {
+            const int i = warp + (j0 + lane) * W;
+            mj = ml[i] * kLog2e;
+            lj = es[i];
+            if (!(lj > 0.f)) mj = -INFINITY;  // an all-masked partition adds nothing
         }
-        if (mi == -INFINITY || !(li > 0.f)) continue;  // an all-masked partition adds nothing
-        const float mn = fmaxf(m, mi);
-        const float a = ex2(m - mn), wi = ex2(mi - mn) * li;  // m = -inf -> a = 0
-        l = l * a + wi;
+        float mc = mj;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, o));
+        if (mc == -INFINITY) continue;
+        const float wj = mj == -INFINITY ? 0.f : ex2(mj - mc) * lj;  // weight relative to mc
+        float lc = wj;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lc += __shfl_xor_sync(0xffffffffu, lc, o);
+        float4 ac[kP2MaxCols];
+#pragma unroll
+        for (int k = 0; k < kP2MaxCols; ++k) ac[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+        for (int jj = 0; jj < nc; ++jj) {
+            const float w = __shfl_sync(0xffffffffu, wj, jj);
+            const int64_t i = warp + (int64_t)(j0 + jj) * W;
+#pragma unroll
+            for (int k = 0; k < kP2MaxCols; ++k) {
+                const int c = lane + 32 * k;
+                if (c < nq) {
+                    const float4 x = tmp[i * nq + c];
+                    ac[k].x += w * x.x;
+                    ac[k].y += w * x.y;
+                    ac[k].z += w * x.z;
+                    ac[k].w += w * x.w;
+                }
+            }
+        }
+        // fold this chunk into the warp's running (m, l, acc)
+        const float mn = fmaxf(m, mc);
+        const float a = ex2(m - mn), b = ex2(mc - mn);  // m = -inf -> a = 0
+        l = l * a + lc * b;
 #pragma unroll
         for (int k = 0; k < kP2MaxCols; ++k) {
-            acc[k].x = acc[k].x * a + wi * x[k].x;
-            acc[k].y = acc[k].y * a + wi * x[k].y;
-            acc[k].z = acc[k].z * a + wi * x[k].z;
-            acc[k].w = acc[k].w * a + wi * x[k].w;
+            acc[k].x = acc[k].x * a + ac[k].x * b;
+            acc[k].y = acc[k].y * a + ac[k].y * b;
+            acc[k].z = acc[k].z * a + ac[k].z * b;
+            acc[k].w = acc[k].w * a + ac[k].w * b;
         }
         m = mn;
     }
