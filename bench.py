@@ -383,6 +383,51 @@ def run_ours(args):
     return 0
 
 
+def run_copy_blocks(args):
+    """Copy-on-write block copies ("paged_attn.py" copy_blocks): 32 layers of fp16 K/V caches
+    (8 kv heads x head size 128 x block size 16 = 32 KiB per block and cache), 512 random
+    (src, dst) pairs per step; bytes = read + write of every copied block."""
+    import torch
+
+    import paged_kv_cache_v2_gb300 as pa
+
+    torch.cuda.set_device(0)
+    pa.load()
+    L, NB, pairs = 32, 2048, 512
+    g = torch.Generator(device="cuda").manual_seed(11)
+    kcs = [torch.empty((NB, 8, 16, 16, 8), dtype=torch.float16, device="cuda").normal_(generator=g) for _ in range(L)]
+    vcs = [torch.empty((NB, 8, 128, 16), dtype=torch.float16, device="cuda").normal_(generator=g) for _ in range(L)]
+    perm = torch.randperm(NB, device="cuda", generator=g)
+    maps = [torch.stack([perm[:pairs], perm[pairs:2 * pairs]], 1).contiguous(),
+            torch.stack([perm[2 * pairs:3 * pairs], perm[3 * pairs:]], 1).contiguous()]
+    block = kcs[0][0].numel() * 2
+    step_bytes = L * pairs * 2 * block * 2
+    for i in range(args.warmup):
+        pa.pa_copy_blocks(kcs, vcs, maps[i % 2])
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(0) as clocks:
+        for i in range(args.steps):
+            ev[i][0].record()
+            pa.pa_copy_blocks(kcs, vcs, maps[i % 2])
+            ev[i][1].record()
+        torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in ev) / args.steps
+    peak, kind = _peaks()
+    gbs = step_bytes / (ms * 1e-3) / 1e9
+    print(json.dumps({
+        "metric": "copy_blocks achieved HBM GB/s (read + write of copied blocks), 1 GPU", "value": round(gbs, 1),
+        "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": "copy_blocks 32 layers x 512 pairs x 32 KiB blocks (K and V)",
+                   "bytes_per_step": step_bytes, "l2": f"{step_bytes / 2**20:.0f} MiB per step, > L2"},
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gbs / peak, 4), "traffic": None, "kernel": "pa_copy_blocks_kernel",
+                     "peak_source": f"{kind} hbm_gbs (copy)"},
+        "gpu_launches": args.steps, "clocks": clocks.summary()}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -393,11 +438,15 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--op", choices=["decode", "copy_blocks"], default="decode",
+                    help="decode: the decode step (default); copy_blocks: the block-copy kernel alone")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.op == "copy_blocks":
+        return run_copy_blocks(args)
     return run_ours(args)
 
 

@@ -18,7 +18,7 @@
  *   seq_lens     [num_seqs]                       int32, tokens per sequence
  *   exp_sums     [num_seqs][num_heads][max_num_partitions]             float32
  *   max_logits   [num_seqs][num_heads][max_num_partitions]             float32
- *   tmp_output   [num_seqs][num_heads][max_num_partitions][head_size]  float32
+ *   tmp_output   [num_seqs][num_heads][max_num_partitions][head_size]  float32 or q dtype
  * These are the argument layouts of "paged_attention_v2_pytorch.py" (paged_attention_v2_pytorch)
  * and the cache views of "paged_attn.py" (split_kv_cache).
  */
@@ -104,7 +104,10 @@ typedef enum {
  *   alibi_slopes          device float32 [num_heads], or NULL for no ALiBi bias.
  *   q_dtype               PA_DT_F16 or PA_DT_BF16 (query and output).
  *   kv_cache_dtype        PA_KV_AUTO (cache in q_dtype) or PA_KV_FP8_E4M3.
- *   tmp_dtype             PA_DT_F32 (the layout of tmp_output).
+ *   tmp_dtype             element type of tmp_output: PA_DT_F32, or q_dtype (as the pages'
+ *                         "paged_attn.py" forward_decode allocates it: half the workspace
+ *                         traffic, at the cost of one more rounding of each partition's
+ *                         output to the output dtype).
  *   k_scale, v_scale      > 0, finite; multiply the decoded key and value elements.
  *   stream                the CUDA stream the kernels are enqueued on.
  *
@@ -156,6 +159,48 @@ PA_API pa_status pa_reshape_and_cache(const void* key, const void* value, int64_
                                pa_dtype src_dtype, pa_kv_cache_dtype kv_cache_dtype,
                                float k_scale, float v_scale, cudaStream_t stream);
 
+/*
+ * pa_copy_blocks -- copy whole blocks inside every layer's K and V cache (copy-on-write of
+ * shared prefixes).
+ *
+ * Defines: "paged_attn.py", copy_blocks (-> ops.copy_blocks(key_caches, value_caches,
+ * src_to_dists)).  For every layer l < num_layers and pair i < num_pairs with
+ * (src, dst) = (block_mapping[2i], block_mapping[2i+1]):
+ *   key_caches[l][dst] = key_caches[l][src] and value_caches[l][dst] = value_caches[l][src],
+ * where a block is the block_bytes contiguous bytes of one physical block of one cache
+ * (num_kv_heads * head_size * block_size * element size).
+ *
+ * Arguments:
+ *   key_caches, value_caches  HOST arrays of num_layers device pointers, 16-byte aligned.
+ *   block_mapping             device int64 [num_pairs][2] (src, dst).
+ *   block_bytes               > 0, a multiple of 16.   num_blocks: blocks in each cache.
+ * Pairs run in parallel, so no dst may also be the src of another pair in the same call.
+ * Errors: PA_ERR_INVALID_ARG before anything is enqueued; an id outside [0, num_blocks) is
+ * skipped on the device and recorded in pa_get_device_errors (bit 4).
+ */
+PA_API pa_status pa_copy_blocks(void* const* key_caches, void* const* value_caches, int num_layers,
+                                const int64_t* block_mapping, int num_pairs, int64_t block_bytes,
+                                int num_blocks, cudaStream_t stream);
+
+/*
+ * pa_swap_blocks -- move whole blocks from one cache to another, typically between the
+ * GPU cache and a pinned host cache.
+ *
+ * Defines: "paged_attn.py", swap_blocks (-> ops.swap_blocks(src, dst, src_to_dst), called
+ * once for the K caches and once for the V caches).  For every pair (src, dst) of
+ * block_mapping: dst_cache[dst] = src_cache[src], block_bytes bytes each.
+ *
+ * Arguments:
+ *   src_cache, dst_cache  device or pinned host memory (any pair the runtime can copy).
+ *   block_mapping         HOST int64 [num_pairs][2] (src, dst), checked on the host.
+ *   block_bytes > 0; src_num_blocks / dst_num_blocks: blocks in each cache.
+ * One cudaMemcpyAsync per pair on `stream`.  Errors: PA_ERR_INVALID_ARG (nothing enqueued)
+ * for a bad size or an id out of range; PA_ERR_CUDA if a copy cannot be enqueued.
+ */
+PA_API pa_status pa_swap_blocks(const void* src_cache, void* dst_cache, const int64_t* block_mapping,
+                                int num_pairs, int64_t block_bytes, int src_num_blocks,
+                                int dst_num_blocks, cudaStream_t stream);
+
 /* Tokens per partition: 512 ("paged_attention_v2_pytorch.py", _PARTITION_SIZE). */
 PA_API int pa_v2_partition_size(void);
 
@@ -165,7 +210,7 @@ PA_API const char* pa_status_string(pa_status status);
 /* Device-side error flags (bit 0: a block id outside [0, num_blocks) or a table row too
  * short; bit 1: a sequence longer than max_num_partitions * 512 or a negative length;
  * bit 2: a bounded wait for a shared-memory copy gave up; bit 3: a slot outside the
- * cache).  Reads the flags of the current device (this synchronises the device) into
+ * cache; bit 4: a pa_copy_blocks id outside the cache).  Reads the flags of the current device (this synchronises the device) into
  * *flags, and clears them when reset != 0.  Not part of the pages' interface: it reports
  * what the kernels skipped instead of faulting. */
 PA_API pa_status pa_get_device_errors(uint32_t* flags, int reset);

@@ -59,6 +59,8 @@ def _load():
                                                         i32, i32, i32, f32, f32]
             lib.pa_oracle_decode_table.restype = i32
             lib.pa_oracle_decode_table.argtypes = [i32, P]
+            lib.pa_oracle_copy_blocks.restype = i32
+            lib.pa_oracle_copy_blocks.argtypes = [P, P, P, i32, i64, i32, i32]
             lib.pa_oracle_encode_e4m3.restype = None
             lib.pa_oracle_encode_e4m3.argtypes = [P, i64, P]
             _lib = lib
@@ -174,3 +176,17 @@ def encode_e4m3(x: np.ndarray) -> np.ndarray:
     out = np.zeros(a.shape, dtype=np.uint8)
     lib.pa_oracle_encode_e4m3(_ptr(a), a.size, _ptr(out))
     return out
+
+
+def copy_blocks(dst: np.ndarray, src: np.ndarray, mapping) -> None:
+    """Block moves in place: dst[d] = src[s] for each (s, d) pair of mapping, in order
+    (dst and src may be the same array, as in copy-on-write inside one cache)."""
+    lib = _load()
+    m = np.ascontiguousarray(_np(mapping), dtype=np.int64).reshape(-1, 2)
+    assert dst.flags.c_contiguous and src.flags.c_contiguous
+    block_bytes = dst[0].nbytes
+    assert src[0].nbytes == block_bytes
+    rc = lib.pa_oracle_copy_blocks(_ptr(dst), _ptr(src), _ptr(m), m.shape[0], block_bytes, src.shape[0],
+                                   dst.shape[0])
+    if rc != 0:
+        raise ValueError("oracle copy_blocks: id out of range")

@@ -333,3 +333,18 @@ int pa_oracle_decode_table(int fmt, double* out) {
 void pa_oracle_encode_e4m3(const float* x, int64_t n, uint8_t* out) {
     for (int64_t i = 0; i < n; ++i) out[i] = orc_enc_e4m3(x[i]);
 }
+
+/*
+ * Block moves ("paged_attn.py", copy_blocks / swap_blocks): for each pair n in order,
+ * dst block mapping[2n+1] receives src block mapping[2n] (block_bytes bytes each).
+ * Returns 0, or -1 for an id outside its cache.
+ */
+int pa_oracle_copy_blocks(void* dst, const void* src, const int64_t* mapping, int num_pairs,
+                          int64_t block_bytes, int src_num_blocks, int dst_num_blocks) {
+    for (int n = 0; n < num_pairs; ++n) {
+        int64_t s = mapping[2 * n], d = mapping[2 * n + 1];
+        if (s < 0 || s >= src_num_blocks || d < 0 || d >= dst_num_blocks) return -1;
+        memcpy((char*)dst + d * block_bytes, (const char*)src + s * block_bytes, (size_t)block_bytes);
+    }
+    return 0;
+}

@@ -69,6 +69,10 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.pa_get_device_errors.argtypes = [ctypes.POINTER(u32), i32]
     lib.pa_v2_set_timing_events.restype = i32
     lib.pa_v2_set_timing_events.argtypes = [P, P]
+    lib.pa_copy_blocks.restype = i32
+    lib.pa_copy_blocks.argtypes = [P, P, i32, P, i32, i64, i32, P]
+    lib.pa_swap_blocks.restype = i32
+    lib.pa_swap_blocks.argtypes = [P, P, P, i32, i64, i32, i32, P]
     lib.pa_v2_decode_noalloc.restype = i32
     lib.pa_v2_decode_noalloc.argtypes = [P, P, P, P, i32, i32, i32, i32, f32, P, i32, i32, P, i32, i32,
                                          P, i32, i32, f32, f32, P]
@@ -132,8 +136,12 @@ def pa_v2_decode(output: torch.Tensor, exp_sums: torch.Tensor, max_logits: torch
         raise TypeError("block_tables and seq_lens must be int32")
     if exp_sums.dtype != torch.float32 or max_logits.dtype != torch.float32:
         raise TypeError("exp_sums and max_logits must be float32")
-    if tmp_output.dtype != torch.float32:
-        raise TypeError("tmp_output must be float32")
+    if tmp_output.dtype == torch.float32:
+        tmp_dtype = PA_DT_F32
+    elif tmp_output.dtype == query.dtype:
+        tmp_dtype = _dt(query.dtype)
+    else:
+        raise TypeError("tmp_output must be float32 or the query dtype")
     if output.dtype != query.dtype:
         raise TypeError("output must have the query dtype")
     if alibi_slopes is not None and (alibi_slopes.dtype != torch.float32 or not alibi_slopes.is_cuda):
@@ -146,7 +154,7 @@ def pa_v2_decode(output: torch.Tensor, exp_sums: torch.Tensor, max_logits: torch
                           d, float(scale), _ptr(block_tables), int(block_tables.shape[1]),
                           int(num_blocks), _ptr(seq_lens), int(block_size), int(max_seq_len),
                           int(tmp_output.shape[2]), _ptr(alibi_slopes), _dt(query.dtype),
-                          _kv(kv_cache_dtype), PA_DT_F32, float(k_scale), float(v_scale),
+                          _kv(kv_cache_dtype), tmp_dtype, float(k_scale), float(v_scale),
                           _stream(stream))
     _check("pa_v2_decode", st)
 
@@ -204,6 +212,49 @@ def pa_v2_decode_noalloc(output: torch.Tensor, query: torch.Tensor, key_cache: t
     _check("pa_v2_decode_noalloc", st)
 
 
+def pa_copy_blocks(key_caches, value_caches, block_mapping: torch.Tensor, stream=None) -> None:
+    """Copy blocks inside each layer's caches ("paged_attn.py" copy_blocks): for every pair
+    (src, dst) of block_mapping (int64 [n, 2], on the GPU), cache[dst] = cache[src] in every
+    K and V cache of the lists.  No dst may be another pair's src."""
+    lib = load()
+    key_caches, value_caches = list(key_caches), list(value_caches)
+    if len(key_caches) != len(value_caches) or not key_caches:
+        raise ValueError("need one value cache per key cache")
+    nb = key_caches[0].shape[0]
+    block_bytes = key_caches[0][0].numel() * key_caches[0].element_size()
+    for t in key_caches + value_caches:
+        if not t.is_cuda or not t.is_contiguous() or t.shape[0] != nb or \
+                t[0].numel() * t.element_size() != block_bytes:
+            raise ValueError("caches must be contiguous CUDA tensors with equal block shapes")
+    m = block_mapping
+    if m.dtype != torch.int64 or not m.is_cuda or not m.is_contiguous() or m.dim() != 2 or m.shape[1] != 2:
+        raise TypeError("block_mapping must be a contiguous int64 CUDA tensor [n, 2]")
+    L = len(key_caches)
+    kp = (ctypes.c_void_p * L)(*[t.data_ptr() for t in key_caches])
+    vp = (ctypes.c_void_p * L)(*[t.data_ptr() for t in value_caches])
+    _check("pa_copy_blocks", lib.pa_copy_blocks(kp, vp, L, _ptr(m), m.shape[0], block_bytes, nb,
+                                                _stream(stream)))
+
+
+def pa_swap_blocks(src: torch.Tensor, dst: torch.Tensor, block_mapping: torch.Tensor, stream=None) -> None:
+    """Move blocks between two caches ("paged_attn.py" swap_blocks), e.g. GPU and pinned host:
+    dst[d] = src[s] for every pair (s, d) of block_mapping (int64 [n, 2], on the host)."""
+    lib = load()
+    if not src.is_contiguous() or not dst.is_contiguous():
+        raise ValueError("caches must be contiguous")
+    block_bytes = src[0].numel() * src.element_size()
+    if dst[0].numel() * dst.element_size() != block_bytes:
+        raise ValueError("blocks of src and dst differ in size")
+    m = block_mapping
+    if m.dtype != torch.int64 or m.is_cuda or m.dim() != 2 or m.shape[1] != 2:
+        raise TypeError("block_mapping must be an int64 CPU tensor [n, 2]")
+    m = m.contiguous()
+    if stream is None:
+        stream = torch.cuda.current_stream(dst.device if dst.is_cuda else src.device)
+    _check("pa_swap_blocks", lib.pa_swap_blocks(_ptr(src), _ptr(dst), _ptr(m), m.shape[0], block_bytes,
+                                                src.shape[0], dst.shape[0], _stream(stream)))
+
+
 def pa_v2_partition_size() -> int:
     return int(load().pa_v2_partition_size())
 
@@ -226,10 +277,12 @@ def pa_v2_set_timing_events(begin: Optional[torch.cuda.Event], end: Optional[tor
     _check("pa_v2_set_timing_events", load().pa_v2_set_timing_events(b, e))
 
 
-def workspace(num_seqs: int, num_heads: int, head_size: int, max_seq_len: int, device) -> tuple:
-    """Allocate (exp_sums, max_logits, tmp_output) for a decode step (caller-owned)."""
+def workspace(num_seqs: int, num_heads: int, head_size: int, max_seq_len: int, device,
+              tmp_dtype: torch.dtype = torch.float32) -> tuple:
+    """Allocate (exp_sums, max_logits, tmp_output) for a decode step (caller-owned);
+    tmp_dtype may be float32 or the query dtype."""
     P = max(1, -(-max_seq_len // PARTITION_SIZE))
     es = torch.empty((num_seqs, num_heads, P), dtype=torch.float32, device=device)
     ml = torch.empty_like(es)
-    tmp = torch.empty((num_seqs, num_heads, P, head_size), dtype=torch.float32, device=device)
+    tmp = torch.empty((num_seqs, num_heads, P, head_size), dtype=tmp_dtype, device=device)
     return es, ml, tmp

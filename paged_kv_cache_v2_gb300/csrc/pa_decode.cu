@@ -75,7 +75,7 @@ struct Phase1Params {
     void* out;
     float* exp_sums;
     float* max_logits;
-    float* tmp_out;
+    void* tmp_out;  // fp32, or the output dtype when tmp16
     const void* query;
     const uint8_t* kcache;
     const uint8_t* vcache;
@@ -86,13 +86,14 @@ struct Phase1Params {
     uint32_t ring_bytes;  // kWarps * nstage * slot bytes
     float qk_scale_log2;  // scale * k_scale * log2(e)
     float v_scale;
+    int tmp16;  // tmp_output holds the output dtype instead of fp32
 };
 
 struct Phase2Params {
     void* out;
     const float* exp_sums;
     const float* max_logits;
-    const float* tmp_out;
+    const void* tmp_out;  // fp32, or the output dtype (template parameter TMP16)
     const int32_t* seq_lens;
     int H, D, Pmax;
 };
@@ -794,8 +795,10 @@ pa_v2_phase1_kernel(const Phase1Params p) {
             const int64_t row = (int64_t)s * H + h0 + hh;
             if (single)
                 store_out<BF16>(p.out, row * D + i, v);
+            else if (p.tmp16)
+                store_out<BF16>(p.tmp_out, (row * p.Pmax + cq) * D + i, v);
             else
-                p.tmp_out[(row * p.Pmax + cq) * D + i] = v;
+                static_cast<float*>(p.tmp_out)[(row * p.Pmax + cq) * D + i] = v;
         }
         if (threadIdx.x < nh) {
             const int hh = threadIdx.x;
@@ -838,7 +841,30 @@ pa_v2_phase1_kernel(const Phase1Params p) {
 constexpr int kP2MaxWarps = 16;
 constexpr int kP2MaxCols = 2;  // float4 columns per lane: head_size <= 256
 
-template <bool BF16>
+// four consecutive tmp_output elements of one partition row as fp32
+template <bool BF16, bool TMP16>
+__device__ __forceinline__ float4 load_tmp4(const void* base, int64_t idx4) {
+    if constexpr (TMP16) {
+        const uint2 w = reinterpret_cast<const uint2*>(base)[idx4];
+        float4 r;
+        if constexpr (BF16) {
+            r.x = __uint_as_float(w.x << 16);
+            r.y = __uint_as_float(w.x & 0xffff0000u);
+            r.z = __uint_as_float(w.y << 16);
+            r.w = __uint_as_float(w.y & 0xffff0000u);
+        } else {
+            r.x = f16_lo_to_f32(w.x);
+            r.y = f16_hi_to_f32(w.x);
+            r.z = f16_lo_to_f32(w.y);
+            r.w = f16_hi_to_f32(w.y);
+        }
+        return r;
+    } else {
+        return reinterpret_cast<const float4*>(base)[idx4];
+    }
+}
+
+template <bool BF16, bool TMP16>
 __global__ void __launch_bounds__(kP2MaxWarps * 32)
 pa_v2_phase2_kernel(const Phase2Params p) {
     extern __shared__ float sm2[];  // [W][D] partial sums
@@ -853,7 +879,7 @@ pa_v2_phase2_kernel(const Phase2Params p) {
     const int64_t row = (int64_t)s * p.H + h;
     const float* ml = p.max_logits + row * p.Pmax;
     const float* es = p.exp_sums + row * p.Pmax;
-    const float4* tmp = reinterpret_cast<const float4*>(p.tmp_out + row * p.Pmax * D);
+    const int64_t tmp4 = row * p.Pmax * nq;  // first float4 group of this (sequence, head)
 
     // Warp w owns partitions w, w + W, ...  Their statistics load one per lane (32 at a
     // time) and reduce with shuffles; the tmp rows then stream with independent loads.
@@ -890,7 +916,7 @@ pa_v2_phase2_kernel(const Phase2Params p) {
             for (int k = 0; k < kP2MaxCols; ++k) {
                 const int c = lane + 32 * k;
                 if (c < nq) {
-                    const float4 x = tmp[i * nq + c];
+                    const float4 x = load_tmp4<BF16, TMP16>(p.tmp_out, tmp4 + i * nq + c);
                     ac[k].x += w * x.x;
                     ac[k].y += w * x.y;
                     ac[k].z += w * x.z;
@@ -1054,11 +1080,12 @@ cudaError_t pa::read_decode_errors(unsigned int* v, bool reset) {
 
 extern "C" pa_status pa_get_device_errors(uint32_t* flags, int reset) {
     if (flags == nullptr) return PA_ERR_INVALID_ARG;
-    unsigned int a = 0, b = 0;
+    unsigned int a = 0, b = 0, c = 0;
     if (cudaDeviceSynchronize() != cudaSuccess) return PA_ERR_CUDA;
     if (read_decode_errors(&a, reset != 0) != cudaSuccess) return PA_ERR_CUDA;
     if (read_cache_errors(&b, reset != 0) != cudaSuccess) return PA_ERR_CUDA;
-    *flags = a | b;
+    if (read_block_errors(&c, reset != 0) != cudaSuccess) return PA_ERR_CUDA;
+    *flags = a | b | c;
     return PA_OK;
 }
 
@@ -1074,7 +1101,7 @@ pa_status pa::validate_decode(const DecodeArgs& a) {
     if (a.num_heads % a.num_kv_heads != 0) return PA_ERR_INVALID_ARG;
     if (a.q_dtype != PA_DT_F16 && a.q_dtype != PA_DT_BF16) return PA_ERR_UNSUPPORTED;
     if (a.kv_cache_dtype != PA_KV_AUTO && a.kv_cache_dtype != PA_KV_FP8_E4M3) return PA_ERR_INVALID_ARG;
-    if (a.tmp_dtype != PA_DT_F32) return PA_ERR_UNSUPPORTED;
+    if (a.tmp_dtype != PA_DT_F32 && a.tmp_dtype != a.q_dtype) return PA_ERR_UNSUPPORTED;
     if (!supported_head_size(a.head_size)) return PA_ERR_UNSUPPORTED;
     const int x = a.kv_cache_dtype == PA_KV_FP8_E4M3 ? 16 : 8;
     if (a.head_size % x != 0) return PA_ERR_INVALID_ARG;
@@ -1103,7 +1130,7 @@ pa_status pa::validate_decode(const DecodeArgs& a) {
     return PA_OK;
 }
 
-pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_logits, float* tmp_out) {
+pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_logits, void* tmp_out) {
     const bool bf16 = a.q_dtype == PA_DT_BF16;
     const bool fp8 = a.kv_cache_dtype == PA_KV_FP8_E4M3;
     const int D = a.head_size, bs = a.block_size;
@@ -1160,6 +1187,7 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
     p1.ring_bytes = ring;
     p1.qk_scale_log2 = a.scale * a.k_scale * kLog2e;
     p1.v_scale = a.v_scale;
+    p1.tmp16 = a.tmp_dtype != PA_DT_F32;
 
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1213,7 +1241,10 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
         int w2 = (a.max_num_partitions + 7) / 8;
         w2 = w2 < 1 ? 1 : (w2 > kP2MaxWarps ? kP2MaxWarps : w2);
         const size_t smem2 = (size_t)w2 * D * sizeof(float);
-        void (*fn2)(const Phase2Params) = bf16 ? pa_v2_phase2_kernel<true> : pa_v2_phase2_kernel<false>;
+        const bool t16 = a.tmp_dtype != PA_DT_F32;
+        void (*fn2)(const Phase2Params) =
+            bf16 ? (t16 ? pa_v2_phase2_kernel<true, true> : pa_v2_phase2_kernel<true, false>)
+                 : (t16 ? pa_v2_phase2_kernel<false, true> : pa_v2_phase2_kernel<false, false>);
         if (ensure_smem((const void*)fn2, smem2) != cudaSuccess) {
             (void)cudaGetLastError();
             return PA_ERR_CUDA;
@@ -1274,7 +1305,7 @@ extern "C" pa_status pa_v2_decode(void* output, float* exp_sums, float* max_logi
     st = host_check_tables(block_tables, max_blocks_per_seq, num_blocks, seq_lens, num_seqs, block_size,
                            max_seq_len, stream);
     if (st != PA_OK) return st;
-    return launch_decode(a, exp_sums, max_logits, (float*)tmp_output);
+    return launch_decode(a, exp_sums, max_logits, tmp_output);
 }
 
 // ---------------------------------------------------------------------------------------

@@ -32,9 +32,10 @@ struct DecodeArgs {
 // Argument checks shared by the decode entry points (no device access).
 pa_status validate_decode(const DecodeArgs& a);
 // Enqueue phase 1 (+ phase 2) with the given workspace.
-pa_status launch_decode(const DecodeArgs& a, float* exp_sums, float* max_logits, float* tmp_out);
+pa_status launch_decode(const DecodeArgs& a, float* exp_sums, float* max_logits, void* tmp_out);
 // Read (and optionally clear) each translation unit's device error word on the current device.
 cudaError_t read_decode_errors(unsigned int* v, bool reset);
 cudaError_t read_cache_errors(unsigned int* v, bool reset);
+cudaError_t read_block_errors(unsigned int* v, bool reset);
 
 }  // namespace pa

@@ -79,7 +79,7 @@ def _decode_raw(**over):
     (dict(tmp_output=None), 1),
     (dict(key_cache=0x10008), 1),                    # bulk copies need 16-byte alignment
     (dict(q_dtype=2), 2),                            # fp32 query not built
-    (dict(tmp=0), 2),                                # fp16 tmp_output not built
+    (dict(tmp=1), 2),                                # tmp_output dtype other than fp32 / q
     (dict(kv=7), 1),
     (dict(num_blocks=0), 1),
     (dict(num_seqs=-1), 1),
@@ -134,3 +134,19 @@ def test_noalloc_entry_point_host_checks():
     assert lib.pa_v2_decode_noalloc(None, P, P, P, 2, 8, 2, 128, 0.088, P, 64, 100, P, 16, 1024,
                                     None, 0, 0, 1.0, 1.0, None) == 1
     assert pa.pa_status_string(4).startswith("step needs more")
+
+
+def test_block_moves_host_checks():
+    lib = pa.load()
+    P = 0x10000
+    two = (ctypes.c_void_p * 2)(P, P)
+    bad = (ctypes.c_void_p * 2)(P, 0x10008)
+    assert lib.pa_copy_blocks(two, two, 2, P, 4, 4100, 10, None) == 1   # block bytes not a multiple of 16
+    assert lib.pa_copy_blocks(two, bad, 2, P, 4, 4096, 10, None) == 1   # misaligned cache
+    assert lib.pa_copy_blocks(two, two, 2, None, 4, 4096, 10, None) == 1
+    assert lib.pa_copy_blocks(two, two, 0, P, 4, 4096, 10, None) == 0   # nothing to do
+    m = (ctypes.c_int64 * 4)(0, 1, 2, 9)
+    assert lib.pa_swap_blocks(P, P, m, 2, 4096, 4, 8, None) == 1        # dst id 9 outside 8 blocks
+    m2 = (ctypes.c_int64 * 2)(5, 1)
+    assert lib.pa_swap_blocks(P, P, m2, 1, 4096, 4, 8, None) == 1       # src id 5 outside 4 blocks
+    assert lib.pa_swap_blocks(P, P, m2, 0, 4096, 4, 8, None) == 0

@@ -409,3 +409,23 @@ def test_p10_seeded_generation_reproduces():
     assert not torch.equal(a.query, c.query)
     ra, rb = oracle.decode_workload(a), oracle.decode_workload(b)
     assert np.array_equal(ra["out"], rb["out"])
+
+
+# ----------------------------------------------------------------------------------------
+# block moves ("paged_attn.py" copy_blocks / swap_blocks)
+# ----------------------------------------------------------------------------------------
+def test_copy_blocks_oracle_matches_numpy_indexing_and_hand_case():
+    rng = np.random.default_rng(8)
+    src = rng.integers(0, 255, size=(40, 2, 8, 16, 8), dtype=np.uint8)
+    dst = rng.integers(0, 255, size=(30, 2, 8, 16, 8), dtype=np.uint8)
+    m = np.stack([rng.permutation(40)[:12], rng.permutation(30)[:12]], axis=1)
+    want = dst.copy()
+    want[m[:, 1]] = src[m[:, 0]]
+    oracle.copy_blocks(dst, src, m)
+    assert np.array_equal(dst, want)
+    # hand case inside one cache: block b holds the value b; (0 -> 2), (3 -> 1)
+    c = np.repeat(np.arange(4, dtype=np.int32)[:, None], 5, axis=1)
+    oracle.copy_blocks(c, c, np.array([[0, 2], [3, 1]]))
+    assert c[:, 0].tolist() == [0, 3, 0, 3]
+    with pytest.raises(ValueError):
+        oracle.copy_blocks(c, c, np.array([[0, 4]]))

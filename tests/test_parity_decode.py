@@ -137,3 +137,12 @@ def test_decode_is_deterministic():
     b = run_decode(wl, dev)
     for x, y in zip(a, b):
         assert torch.equal(x.view(torch.uint8), y.view(torch.uint8))
+
+
+@pytest.mark.parametrize("name", ["llama_gqa_decode", "long_context_gqa", "fp8_kv", "mha_alibi_ragged"])
+def test_tmp_output_in_query_dtype(name):
+    # the pages' forward_decode keeps tmp_output in the output dtype
+    wl = workloads.make(name, reduced=True)
+    gpu = run_decode(wl, tmp_dtype=wl.query.dtype)
+    assert gpu[3].dtype == wl.query.dtype
+    check_decode(wl, gpu, oracle.decode_workload(wl), label=f"tmp16 {name}")
