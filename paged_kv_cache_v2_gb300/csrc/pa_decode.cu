@@ -198,12 +198,21 @@ pa_v2_phase1_kernel(const Phase1Params p) {
         const int ns = (np + pps - 1) >> pps_log2;
         return ns > warp ? (ns - warp + kWarps - 1) / kWarps : 0;
     };
-    // Physical id of page `pg` of partition q with np pages (all lanes): >= 0, -1 if the page
-    // does not exist, -2 if it exists but its table entry is out of range.
-    auto page_id = [&](int q, int np, int r0, int r1, int pg) -> int {
-        const int v = __shfl_sync(0xffffffffu, pg < 32 ? r0 : r1, pg & 31);
-        if (pg >= np) return -1;
-        return (v >= 0 && v < p.num_blocks && q * ppart + pg < p.mbps) ? v : -2;
+    // Check the raw table entries of partition q once: entries of pages that do not exist or
+    // lie outside [0, num_blocks) become -1 (the latter flagged), and bit i of the returned
+    // mask says page i of the partition can be read.
+    auto validate = [&](int q, int& r0, int& r1) -> uint64_t {
+        const int np = npages_of(q), lb = q * ppart;
+        const bool e0 = lane < np, e1 = 32 + lane < np;
+        const bool ok0 = e0 && r0 >= 0 && r0 < p.num_blocks && lb + lane < p.mbps;
+        const bool ok1 = e1 && r1 >= 0 && r1 < p.num_blocks && lb + 32 + lane < p.mbps;
+        if ((e0 && !ok0) || (e1 && !ok1)) flag_error(1u);
+        r0 = ok0 ? r0 : -1;
+        r1 = ok1 ? r1 : -1;
+        return (uint64_t)__ballot_sync(0xffffffffu, ok0) | ((uint64_t)__ballot_sync(0xffffffffu, ok1) << 32);
+    };
+    auto page_id = [&](int r0, int r1, int pg) -> int {
+        return __shfl_sync(0xffffffffu, pg < 32 ? r0 : r1, pg & 31);
     };
 
     uint8_t* ring = smem + (size_t)warp * nstage * slot_bytes;
@@ -230,7 +239,9 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     // runs up to nstage slots ahead of consumption and at most one partition ahead.
     int cq = px;            // partition being consumed
     int iq = px, ii = 0;    // issue cursor: partition, index among this warp's slots in it
-    int i_np = npages_of(iq), i_my = my_slots_of(i_np);
+    int i_my = my_slots_of(npages_of(iq));
+    uint64_t cmask = validate(px, c0, c1);                           // readable pages of cq
+    uint64_t nmask = px + PX < Pl ? validate(px + PX, n0, n1) : 0u;  // and of cq + PX
     uint32_t nis = 0, ncons = 0;  // slots issued / consumed by this warp
     // ring positions of the next slot to issue / consume, and the consumer's phase parity
     // (kept incrementally: a runtime modulo per slot costs more than the rest of the bookkeeping)
@@ -245,33 +256,26 @@ pa_v2_phase1_kernel(const Phase1Params p) {
                 if (iq >= cq + PX || iq + PX >= Pl) break;
                 iq += PX;
                 ii = 0;
-                i_np = npages_of(iq);
-                i_my = my_slots_of(i_np);
+                i_my = my_slots_of(npages_of(iq));
                 continue;
             }
             const bool cur = iq == cq;
             const int r0 = cur ? c0 : n0, r1 = cur ? c1 : n1;
             const int j = warp + ii * kWarps;
-            int b[4] = {-1, -1, -1, -1};
-            uint32_t bytes = 0;
+            const uint32_t ok = (uint32_t)((cur ? cmask : nmask) >> (j * pps)) & ((1u << pps) - 1u);
+            int b[4];
 #pragma unroll
-            for (int pg = 0; pg < 4; ++pg) {
-                if (pg < pps) {
-                    b[pg] = page_id(iq, i_np, r0, r1, j * pps + pg);
-                    if (b[pg] >= 0) bytes += 2u * page_bytes;
-                }
-            }
+            for (int pg = 0; pg < 4; ++pg) b[pg] = pg < pps ? page_id(r0, r1, j * pps + pg) : -1;
             if (lane == 0) {
                 uint64_t* bar = &bars[ipos];
                 uint8_t* kdst = ring + (size_t)ipos * slot_bytes;
                 uint8_t* vdst = kdst + (size_t)pps * page_bytes;
-                mbar_arrive_expect_tx(bar, bytes);
-                for (int pg = 0; pg < pps; ++pg) {
-                    if (b[pg] >= 0) {
+                mbar_arrive_expect_tx(bar, (uint32_t)__popc(ok) * 2u * page_bytes);
+#pragma unroll
+                for (int pg = 0; pg < 4; ++pg) {
+                    if (pg < pps && ((ok >> pg) & 1u)) {
                         bulk_g2s(kdst + pg * page_bytes, kc_head + (size_t)b[pg] * block_stride, page_bytes, bar, policy);
                         bulk_g2s(vdst + pg * page_bytes, vc_head + (size_t)b[pg] * block_stride, page_bytes, bar, policy);
-                    } else if (b[pg] == -2) {
-                        flag_error(1u);
                     }
                 }
             }
@@ -428,10 +432,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
             const uint8_t* kslot = ring + (size_t)pos * slot_bytes;
             const uint8_t* vslot = kslot + (size_t)pps * page_bytes;
             const uint32_t kbase = smem_addr(kslot), vbase = smem_addr(vslot);
-            uint32_t okmask = 0;
-#pragma unroll
-            for (int pg = 0; pg < 4; ++pg)
-                if (pg < pps && page_id(cq, c_np, c0, c1, j * pps + pg) >= 0) okmask |= 1u << pg;
+            const uint32_t okmask = (uint32_t)(cmask >> (j * pps)) & ((1u << pps) - 1u);
             const int stok0 = t0 + j * slot_tokens;
 
             if constexpr (FP8) {
@@ -814,11 +815,14 @@ pa_v2_phase1_kernel(const Phase1Params p) {
         }
         __syncthreads();  // the merge buffers are reused by the next partition
 
-        // move the id buffers one partition on
+        // move the id buffers one partition on (the next ones were checked already; the ones
+        // after them were loaded at the start of this partition)
         c0 = n0;
         c1 = n1;
+        cmask = nmask;
         n0 = nn0;
         n1 = nn1;
+        nmask = cq + 2 * PX < Pl ? validate(cq + 2 * PX, n0, n1) : 0u;
     }
 
     if (aborted) {
