@@ -37,7 +37,9 @@ if ROOT not in sys.path:
 METRIC = "decode attn µs/step and achieved HBM GB/s (fraction of GB300 peak), 1 GPU"
 DEFAULT_WORKLOAD = "llama_gqa_decode"
 L2_BYTES = 129 * 1024 * 1024
-KERNEL_SRC = os.path.join(ROOT, "paged_kv_cache_v2_gb300", "csrc", "pa_decode.cu")
+# the phase-1 kernel's sources: the committed ncu counters are valid while these are unchanged
+KERNEL_SRCS = [os.path.join(ROOT, "paged_kv_cache_v2_gb300", "csrc", f)
+               for f in ("pa_phase1.cuh", "pa_kernels.cuh", "pa_ptx.cuh")]
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 
 
@@ -51,8 +53,11 @@ def _peaks():
 
 
 def _kernel_hash() -> str:
-    with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    h = hashlib.sha256()
+    for path in KERNEL_SRCS:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def _profiled_traffic(workload: str):

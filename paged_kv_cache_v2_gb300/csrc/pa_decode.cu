@@ -44,794 +44,10 @@
 
 #include "pa_v2.h"
 #include "pa_internal.h"
+#include "pa_kernels.cuh"
 #include "pa_ptx.cuh"
 
 namespace pa {
-
-static __device__ unsigned int g_device_errors = 0;
-
-#ifndef PA_PHASE1_WARPS
-#define PA_PHASE1_WARPS 4
-#endif
-#ifndef PA_RING_KIB
-#define PA_RING_KIB 64
-#endif
-#ifndef PA_MIN_STAGES
-#define PA_MIN_STAGES 1
-#endif
-#ifndef PA_GRID_WAVES
-#define PA_GRID_WAVES 16
-#endif
-
-constexpr int kPartition = 512;
-constexpr int kWarps = PA_PHASE1_WARPS;  // phase-1 warps per CTA
-constexpr uint32_t kRingTarget = PA_RING_KIB * 1024u;  // shared-memory page ring per CTA
-constexpr int kMaxHeadsPerCta = 8;     // the MMA N dimension
-constexpr uint64_t kWaitLimitNs = 2000000000ull;
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
-
-struct Phase1Params {
-    void* out;
-    float* exp_sums;
-    float* max_logits;
-    void* tmp_out;  // fp32, or the output dtype when tmp16
-    const void* query;
-    const uint8_t* kcache;
-    const uint8_t* vcache;
-    const int32_t* block_tables;
-    const int32_t* seq_lens;
-    const float* alibi;
-    int H, Hk, G, ngroups, bs, mbps, num_blocks, Pmax, nstage;
-    uint32_t ring_bytes;  // kWarps * nstage * slot bytes
-    float qk_scale_log2;  // scale * k_scale * log2(e)
-    float v_scale;
-    int tmp16;  // tmp_output holds the output dtype instead of fp32
-};
-
-struct Phase2Params {
-    void* out;
-    const float* exp_sums;
-    const float* max_logits;
-    const void* tmp_out;  // fp32, or the output dtype (template parameter TMP16)
-    const int32_t* seq_lens;
-    int H, D, Pmax;
-};
-
-__device__ __forceinline__ void flag_error(unsigned int bit) { atomicOr(&g_device_errors, bit); }
-
-// Token order of the 16 MMA rows for fp8 pages.  An fp8 V row hands each thread four
-// consecutive tokens, while the P operand (via movmatrix) hands thread t logical rows
-// {2t, 2t+1, 8+2t, 9+2t}; this order makes both agree (with the two halves swapped for
-// t >= 2) and keeps the K-row ldmatrix free of bank conflicts.
-__device__ __constant__ int8_t c_fp8_row_token[16] = {0, 1, 4, 5, 10, 11, 14, 15,
-                                                      2, 3, 6, 7, 8, 9, 12, 13};
-
-template <bool BF16>
-__device__ __forceinline__ void store_out(void* out, int64_t idx, float v) {
-    if constexpr (BF16)
-        reinterpret_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
-    else
-        reinterpret_cast<__half*>(out)[idx] = __float2half_rn(v);
-}
-
-// ---------------------------------------------------------------------------------------
-// Phase 1
-// ---------------------------------------------------------------------------------------
-// Several CTAs per SM hide each other's partition boundaries; registers are capped so that
-// twelve warps (sixteen for head sizes <= 96, whose rings are smaller) fit on an SM.
-#ifndef PA_FP8_MIN_CTAS
-#define PA_FP8_MIN_CTAS 3
-#endif
-template <bool BF16, int KVB, int D>
-__global__ void __launch_bounds__(kWarps * 32, KVB == 2 ? (D <= 96 ? 16 : 12) / kWarps
-                                                        : ((BF16 && D >= 192) ? 8 : 4 * PA_FP8_MIN_CTAS) / kWarps)
-pa_v2_phase1_kernel(const Phase1Params p) {
-    constexpr bool FP8 = (KVB == 1);
-    constexpr int NK = (D + 15) / 16;          // 16-wide steps over the head dimension
-    constexpr bool HALF_STEP = (D % 16) != 0;  // head_size 120: last step has 8 elements
-    static_assert(!(FP8 && HALF_STEP), "fp8 pages need head_size % 16 == 0");
-    extern __shared__ __align__(128) uint8_t smem[];
-
-    // This CTA handles partitions px, px + PX, ... of one sequence for one group of <= 8
-    // query heads sharing a kv head.
-    const int px = blockIdx.x, PX = gridDim.x;
-    const int kvh = blockIdx.y / p.ngroups;
-    const int grp = blockIdx.y - kvh * p.ngroups;
-    const int s = blockIdx.z;
-    const int h0 = kvh * p.G + grp * kMaxHeadsPerCta;
-    const int nh = min(kMaxHeadsPerCta, p.G - grp * kMaxHeadsPerCta);
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int g = lane >> 2, t = lane & 3;
-    const int H = p.H, bs = p.bs;
-    const int bs_log2 = bs == 8 ? 3 : (bs == 16 ? 4 : 5);
-    // A slot holds the K and V pages of 16 tokens (32 for fp8 caches: one k32 MMA step).
-    const int pps = FP8 ? 32 / bs : (bs >= 16 ? 1 : 16 / bs);  // pages per slot
-    const int pps_log2 = pps == 1 ? 0 : (pps == 2 ? 1 : 2);
-    const int slot_tokens = pps * bs;
-    const int tiles_per_slot = slot_tokens / 16;
-    const int ppart = kPartition / bs;  // pages in a full partition
-    const uint32_t page_bytes = (uint32_t)D * bs * KVB;
-    const uint32_t slot_bytes = 2u * pps * page_bytes;
-    const int nstage = p.nstage;
-    const int32_t* trow = p.block_tables + (int64_t)s * p.mbps;
-
-    // Raw table entries of partition q: lane i holds pages i and 32 + i.
-    auto load_ids = [&](int q, int& r0, int& r1) {
-        r0 = r1 = -1;
-        if (q < p.Pmax) {
-            const int lb = q * ppart;
-            if (lb + lane < p.mbps) r0 = trow[lb + lane];
-            if (ppart > 32 && lb + 32 + lane < p.mbps) r1 = trow[lb + 32 + lane];
-        }
-    };
-    // The ids of the first two partitions and the length load in parallel, before waiting on
-    // the previous kernel: a cache writer that ran just before changes none of them.
-    int c0, c1, n0, n1;
-    load_ids(px, c0, c1);
-    load_ids(px + PX, n0, n1);
-    const int L = p.seq_lens[s];
-    griddep_wait();  // the cache writer (if it ran just before) must be visible
-
-    const int P = L > 0 ? (L + kPartition - 1) / kPartition : 0;
-    if (threadIdx.x == 0 && px == 0 && (L < 0 || P > p.Pmax)) flag_error(2u);
-    const int Pl = min(P, p.Pmax);  // partitions with tokens that the grid covers
-    // This CTA's partitions past the end: max_logits = -inf, exp_sums = 0.
-    for (int q = px; q < p.Pmax; q += PX) {
-        if (q >= Pl && threadIdx.x < nh) {
-            const int64_t sidx = ((int64_t)s * H + h0 + threadIdx.x) * p.Pmax + q;
-            p.max_logits[sidx] = -INFINITY;
-            p.exp_sums[sidx] = 0.f;
-        }
-    }
-    if (px == 0 && L <= 0) {
-        for (int i = threadIdx.x; i < nh * D; i += blockDim.x)
-            store_out<BF16>(p.out, ((int64_t)s * H + h0) * D + i, 0.f);
-    }
-    if (px >= Pl) {
-        griddep_launch_dependents();
-        return;
-    }
-
-    auto npages_of = [&](int q) { return ((min(L, (q + 1) * kPartition) - 1) >> bs_log2) - q * ppart + 1; };
-    auto my_slots_of = [&](int np) {
-        const int ns = (np + pps - 1) >> pps_log2;
-        return ns > warp ? (ns - warp + kWarps - 1) / kWarps : 0;
-    };
-    // Check the raw table entries of partition q once: entries of pages that do not exist or
-    // lie outside [0, num_blocks) become -1 (the latter flagged), and bit i of the returned
-    // mask says page i of the partition can be read.
-    auto validate = [&](int q, int& r0, int& r1) -> uint64_t {
-        const int np = npages_of(q), lb = q * ppart;
-        const bool e0 = lane < np, e1 = 32 + lane < np;
-        const bool ok0 = e0 && r0 >= 0 && r0 < p.num_blocks && lb + lane < p.mbps;
-        const bool ok1 = e1 && r1 >= 0 && r1 < p.num_blocks && lb + 32 + lane < p.mbps;
-        if ((e0 && !ok0) || (e1 && !ok1)) flag_error(1u);
-        r0 = ok0 ? r0 : -1;
-        r1 = ok1 ? r1 : -1;
-        return (uint64_t)__ballot_sync(0xffffffffu, ok0) | ((uint64_t)__ballot_sync(0xffffffffu, ok1) << 32);
-    };
-    auto page_id = [&](int r0, int r1, int pg) -> int {
-        return __shfl_sync(0xffffffffu, pg < 32 ? r0 : r1, pg & 31);
-    };
-
-    uint8_t* ring = smem + (size_t)warp * nstage * slot_bytes;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.ring_bytes) + warp * nstage;
-    float* red_m = reinterpret_cast<float*>(smem + p.ring_bytes + kWarps * nstage * sizeof(uint64_t));
-    float* red_l = red_m + kWarps * kMaxHeadsPerCta;
-    float* fin_m = red_l + kWarps * kMaxHeadsPerCta;  // [8] merged max (log2 units)
-    float* fin_l = fin_m + kMaxHeadsPerCta;           // [8] merged exp-sum
-    float* red_o = fin_l + kMaxHeadsPerCta;           // [kWarps][nh][D + 4] scaled accumulators
-    constexpr int RS = D + 4;
-
-    if (lane == 0) {
-        for (int k = 0; k < nstage; ++k) mbar_init(&bars[k], 1);
-        fence_mbar_init();
-    }
-    __syncwarp();
-
-    const uint64_t policy = l2_policy_evict_first();
-    const uint8_t* kc_head = p.kcache + (size_t)kvh * page_bytes;
-    const uint8_t* vc_head = p.vcache + (size_t)kvh * page_bytes;
-    const size_t block_stride = (size_t)p.Hk * page_bytes;
-
-    // The warp's pages form one stream across its partitions: the issue cursor (iq, ii)
-    // runs up to nstage slots ahead of consumption and at most one partition ahead.
-    int cq = px;            // partition being consumed
-    int iq = px, ii = 0;    // issue cursor: partition, index among this warp's slots in it
-    int i_my = my_slots_of(npages_of(iq));
-    uint64_t cmask = validate(px, c0, c1);                           // readable pages of cq
-    uint64_t nmask = px + PX < Pl ? validate(px + PX, n0, n1) : 0u;  // and of cq + PX
-    uint32_t nis = 0, ncons = 0;  // slots issued / consumed by this warp
-    // ring positions of the next slot to issue / consume, and the consumer's phase parity
-    // (kept incrementally: a runtime modulo per slot costs more than the rest of the bookkeeping)
-    int ipos = 0, cpos = 0;
-    uint32_t cphase = 0;
-    bool aborted = false;
-    auto issue_more = [&]() {
-        while (!aborted && (int)(nis - ncons) < nstage) {
-            if (ii >= i_my) {
-                // move on (also past partitions where this warp has no slots), but never
-                // more than one partition ahead of the consumer
-                if (iq >= cq + PX || iq + PX >= Pl) break;
-                iq += PX;
-                ii = 0;
-                i_my = my_slots_of(npages_of(iq));
-                continue;
-            }
-            const bool cur = iq == cq;
-            const int r0 = cur ? c0 : n0, r1 = cur ? c1 : n1;
-            const int j = warp + ii * kWarps;
-            const uint32_t ok = (uint32_t)((cur ? cmask : nmask) >> (j * pps)) & ((1u << pps) - 1u);
-            int b[4];
-#pragma unroll
-            for (int pg = 0; pg < 4; ++pg) b[pg] = pg < pps ? page_id(r0, r1, j * pps + pg) : -1;
-            if (lane == 0) {
-                uint64_t* bar = &bars[ipos];
-                uint8_t* kdst = ring + (size_t)ipos * slot_bytes;
-                uint8_t* vdst = kdst + (size_t)pps * page_bytes;
-                mbar_arrive_expect_tx(bar, (uint32_t)__popc(ok) * 2u * page_bytes);
-#pragma unroll
-                for (int pg = 0; pg < 4; ++pg) {
-                    if (pg < pps && ((ok >> pg) & 1u)) {
-                        bulk_g2s(kdst + pg * page_bytes, kc_head + (size_t)b[pg] * block_stride, page_bytes, bar, policy);
-                        bulk_g2s(vdst + pg * page_bytes, vc_head + (size_t)b[pg] * block_stride, page_bytes, bar, policy);
-                    }
-                }
-            }
-            ++nis;
-            ++ii;
-            if (++ipos == nstage) ipos = 0;
-        }
-    };
-
-    // ---- query fragments (MMA B operand: k = head dim, n = query head g) -------------------
-    // 16-bit caches: the query row as f16/bf16 pairs.  fp8 cache with an f16 query: f16 pairs
-    // in the order the widened fp8 K rows deliver the head dimension (4t..4t+3 of each 16).
-    // fp8 cache with a bf16 query: the row scaled by a power of two (per head, so the largest
-    // element lands near 224) and split into three e4m3 terms hi + mid + lo (at least 12
-    // significant bits, so every bf16 value is exact); the scale is undone on the scores.
-    constexpr int NS = (D + 31) / 32;  // k32 steps over the head dimension (fp8)
-    constexpr bool Q8 = FP8 && BF16;   // scores on the e4m3 tensor path
-    uint32_t qf[Q8 ? 1 : NK][2];
-    uint32_t qh[Q8 ? NS : 1][2], qm[Q8 ? NS : 1][2], ql[Q8 ? NS : 1][2];
-    float qs0 = 1.f, qs1 = 1.f;  // per-column score factor from the fp8 query scale
-    {
-        const bool live = g < nh;
-        const uint16_t* qrow = reinterpret_cast<const uint16_t*>(p.query) + ((int64_t)s * H + h0 + g) * D;
-        if constexpr (!FP8) {
-#pragma unroll
-            for (int kk = 0; kk < NK; ++kk) {
-                uint32_t b0 = 0, b1 = 0;
-                if (live) {
-                    b0 = *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 2 * t);
-                    if (!(HALF_STEP && kk == NK - 1))
-                        b1 = *reinterpret_cast<const uint32_t*>(qrow + kk * 16 + 8 + 2 * t);
-                }
-                qf[kk][0] = b0;
-                qf[kk][1] = b1;
-            }
-        } else if constexpr (!Q8) {
-#pragma unroll
-            for (int kk = 0; kk < NK; ++kk) {
-                uint2 v = make_uint2(0u, 0u);
-                if (live) v = *reinterpret_cast<const uint2*>(qrow + kk * 16 + 4 * t);
-                qf[kk][0] = v.x;
-                qf[kk][1] = v.y;
-            }
-        } else {
-            // thread holds elements 32 st + 16 hh + 4t + i of its head g; two passes over them
-            // (largest magnitude, then scale and split) keep few values live at once
-            auto load4 = [&](int idx, float (&f)[4]) {
-                uint2 w = make_uint2(0u, 0u);
-                if (live && idx < D) w = *reinterpret_cast<const uint2*>(qrow + idx);
-                const uint32_t ww[2] = {w.x, w.y};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint16_t bits = (uint16_t)(ww[i >> 1] >> (16 * (i & 1)));
-                    if constexpr (BF16)
-                        f[i] = __uint_as_float((uint32_t)bits << 16);
-                    else
-                        f[i] = __half2float(__ushort_as_half(bits));
-                }
-            };
-            float amax = 0.f;
-#pragma unroll
-            for (int st = 0; st < NS; ++st) {
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    float f[4];
-                    load4(32 * st + 16 * hh + 4 * t, f);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fabsf(f[i]));
-                }
-            }
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-            int e = 0;
-            if (amax > 0.f && amax < INFINITY) e = (int)floorf(__log2f(224.f / amax));
-            e = max(-100, min(100, e));
-            const float alpha = exp2f((float)e);  // exact power of two
-#pragma unroll
-            for (int st = 0; st < NS; ++st) {
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    float x[4];
-                    load4(32 * st + 16 * hh + 4 * t, x);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) x[i] *= alpha;
-                    // three successive e4m3 roundings of the remaining residual
-                    uint32_t term[3];
-#pragma unroll
-                    for (int k3 = 0; k3 < 3; ++k3) {
-                        const uint16_t c01 = f32x2_to_e4m3x2(x[0], x[1]), c23 = f32x2_to_e4m3x2(x[2], x[3]);
-                        const uint32_t d01 = e4m3x2_to_f16x2(c01), d23 = e4m3x2_to_f16x2(c23);
-                        x[0] -= f16_lo_to_f32(d01);
-                        x[1] -= f16_hi_to_f32(d01);
-                        x[2] -= f16_lo_to_f32(d23);
-                        x[3] -= f16_hi_to_f32(d23);
-                        term[k3] = (uint32_t)c01 | ((uint32_t)c23 << 16);
-                    }
-                    qh[st][hh] = term[0];
-                    qm[st][hh] = term[1];
-                    ql[st][hh] = term[2];
-                }
-            }
-            // columns 2t, 2t+1 of the score fragment belong to heads 2t, 2t+1
-            qs0 = 1.f / __shfl_sync(0xffffffffu, alpha, (2 * t) * 4);
-            qs1 = 1.f / __shfl_sync(0xffffffffu, alpha, (2 * t + 1) * 4);
-        }
-    }
-    issue_more();
-
-    // ALiBi slopes of this thread's two head columns (2t, 2t+1), base-2 units.
-    float sl0 = 0.f, sl1 = 0.f;
-    if (p.alibi != nullptr) {
-        if (2 * t < nh) sl0 = p.alibi[h0 + 2 * t] * kLog2e;
-        if (2 * t + 1 < nh) sl1 = p.alibi[h0 + 2 * t + 1] * kLog2e;
-    }
-    const float qk_mul = p.qk_scale_log2;
-    const float qk_mul0 = qk_mul * qs0, qk_mul1 = qk_mul * qs1;  // fp8: per-column query scale
-    // fp8: P enters the P.V product as e4m3 of P * 256
-    const float v_mul = FP8 ? p.v_scale * (1.f / 256.f) : p.v_scale;
-
-    // Per-lane ldmatrix row of the K page: token within the 16-token tile, chunk offset.
-    const int k_tok = FP8 ? c_fp8_row_token[(lane & 7) + 8 * ((lane >> 3) & 1)] : (lane & 7) + 8 * ((lane >> 3) & 1);
-    const int k_chunk = lane >> 4;
-    // Physical tokens of this thread's two MMA rows (g, g + 8).
-    const int tokA = FP8 ? c_fp8_row_token[g] : g;
-    const int tokB = FP8 ? c_fp8_row_token[g + 8] : g + 8;
-    const bool single = (P == 1);
-    uint32_t drain_from = 0;
-
-    for (; cq < Pl; cq += PX) {
-        // ids of the partition after the next one (the issue cursor may need them soon)
-        int nn0 = -1, nn1 = -1;
-        if (cq + 2 * PX < Pl) load_ids(cq + 2 * PX, nn0, nn1);
-        const int t0 = cq * kPartition;
-        const int t1 = min(L, t0 + kPartition);
-        const int tref = t1 - 1;  // ALiBi positions relative to the partition's last token
-        const int c_np = npages_of(cq);
-        const int my = my_slots_of(c_np);
-        issue_more();  // in case the cursor is still behind this partition
-
-        float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-        float acc[NK][4];
-#pragma unroll
-        for (int i = 0; i < NK; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
-
-        for (int k = 0; k < my && !aborted; ++k) {
-            const int pos = cpos;
-            if (!mbar_wait_bounded(&bars[pos], cphase, kWaitLimitNs)) {
-                if (lane == 0) flag_error(4u);
-                aborted = true;
-                drain_from = ncons;
-                break;
-            }
-            const int j = warp + k * kWarps;
-            const uint8_t* kslot = ring + (size_t)pos * slot_bytes;
-            const uint8_t* vslot = kslot + (size_t)pps * page_bytes;
-            const uint32_t kbase = smem_addr(kslot), vbase = smem_addr(vslot);
-            const uint32_t okmask = (uint32_t)(cmask >> (j * pps)) & ((1u << pps) - 1u);
-            const int stok0 = t0 + j * slot_tokens;
-
-            if constexpr (FP8) {
-                // ---- one 32-token slot: two 16-token score tiles, one k32 P.V step ----------
-                const int lim = t1 - stok0;  // tokens [0, lim) of the slot are in range
-                const bool full = lim >= 32 && okmask == (1u << pps) - 1u;
-                auto tok_ok = [&](int tok) -> bool {
-                    return tok < lim && ((okmask >> (tok >> bs_log2)) & 1u);
-                };
-                float sv[2][4];
-#pragma unroll
-                for (int tile = 0; tile < 2; ++tile) {
-                    // S^T = K . Q^T on the e4m3 codes; rows are tokens in c_fp8_row_token order
-                    const int tt = tile * 16 + k_tok;
-                    const uint32_t krow = kbase + (uint32_t)(tt >> bs_log2) * page_bytes +
-                                          (uint32_t)(k_chunk * bs + (tt & (bs - 1))) * 16u;
-                    float sc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int st = 0; st < NS; ++st) {
-                        uint32_t a0, a1, a2, a3;
-                        if (2 * st + 1 < NK) {
-                            ldsm_x4(krow + (uint32_t)st * 32u * bs, a0, a1, a2, a3);
-                        } else {
-                            ldsm_x2(krow + (uint32_t)st * 32u * bs, a0, a1);
-                            a2 = a3 = 0u;
-                        }
-                        if constexpr (Q8) {
-                            mma_e4m3_16832(sc, a0, a1, a2, a3, qh[st][0], qh[st][1]);
-                            mma_e4m3_16832(sc, a0, a1, a2, a3, qm[st][0], qm[st][1]);
-                            mma_e4m3_16832(sc, a0, a1, a2, a3, ql[st][0], ql[st][1]);
-                        } else {
-                            // widen the K codes to f16 (exact): chunk 2st in a0/a1, 2st+1 in a2/a3
-                            mma16816<false>(sc, e4m3x2_to_f16x2(lo16(a0)), e4m3x2_to_f16x2(lo16(a1)),
-                                            e4m3x2_to_f16x2(hi16(a0)), e4m3x2_to_f16x2(hi16(a1)),
-                                            qf[2 * st][0], qf[2 * st][1]);
-                            if (2 * st + 1 < NK)
-                                mma16816<false>(sc, e4m3x2_to_f16x2(lo16(a2)), e4m3x2_to_f16x2(lo16(a3)),
-                                                e4m3x2_to_f16x2(hi16(a2)), e4m3x2_to_f16x2(hi16(a3)),
-                                                qf[2 * st + 1][0], qf[2 * st + 1][1]);
-                        }
-                    }
-                    const int ttok0 = stok0 + tile * 16;
-                    float s0 = sc[0] * qk_mul0, s1 = sc[1] * qk_mul1;
-                    float s2 = sc[2] * qk_mul0, s3 = sc[3] * qk_mul1;
-                    if (p.alibi != nullptr) {
-                        const float ra = (float)(ttok0 + tokA - tref), rb = (float)(ttok0 + tokB - tref);
-                        s0 = fmaf(sl0, ra, s0);
-                        s1 = fmaf(sl1, ra, s1);
-                        s2 = fmaf(sl0, rb, s2);
-                        s3 = fmaf(sl1, rb, s3);
-                    }
-                    if (!full) {
-                        if (!tok_ok(tile * 16 + tokA)) s0 = s1 = -INFINITY;
-                        if (!tok_ok(tile * 16 + tokB)) s2 = s3 = -INFINITY;
-                    }
-                    sv[tile][0] = s0;
-                    sv[tile][1] = s1;
-                    sv[tile][2] = s2;
-                    sv[tile][3] = s3;
-                }
-                // online softmax over the slot's 32 tokens
-                float mx0 = fmaxf(fmaxf(sv[0][0], sv[0][2]), fmaxf(sv[1][0], sv[1][2]));
-                float mx1 = fmaxf(fmaxf(sv[0][1], sv[0][3]), fmaxf(sv[1][1], sv[1][3]));
-#pragma unroll
-                for (int o = 4; o < 32; o <<= 1) {
-                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-                }
-                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-                const float base0 = mn0 == -INFINITY ? 0.f : mn0;
-                const float base1 = mn1 == -INFINITY ? 0.f : mn1;
-                const float al0 = ex2(m0 - base0), al1 = ex2(m1 - base1);
-                float pv[2][4];
-#pragma unroll
-                for (int tile = 0; tile < 2; ++tile) {
-                    pv[tile][0] = ex2(sv[tile][0] - base0);
-                    pv[tile][1] = ex2(sv[tile][1] - base1);
-                    pv[tile][2] = ex2(sv[tile][2] - base0);
-                    pv[tile][3] = ex2(sv[tile][3] - base1);
-                }
-                l0 = fmaf(l0, al0, (pv[0][0] + pv[0][2]) + (pv[1][0] + pv[1][2]));
-                l1 = fmaf(l1, al1, (pv[0][1] + pv[0][3]) + (pv[1][1] + pv[1][3]));
-                if (__any_sync(0xffffffffu, mn0 != m0 || mn1 != m1)) {
-#pragma unroll
-                    for (int i = 0; i < NK; ++i) {
-                        acc[i][0] *= al0;
-                        acc[i][1] *= al1;
-                        acc[i][2] *= al0;
-                        acc[i][3] *= al1;
-                    }
-                }
-                m0 = mn0;
-                m1 = mn1;
-                // P^T operand: P * 256 as f16, transposed with movmatrix, split into e4m3 hi + lo.
-                // After the transpose thread t holds tokens {4t..4t+3} of head g (rows 2t, 2t+1
-                // and 8+2t, 9+2t in the token order above; the halves swap for t >= 2).
-                uint32_t bh[2], bl[2];
-#pragma unroll
-                for (int tile = 0; tile < 2; ++tile) {
-                    const uint32_t x0 = movm_trans(pack2<false>(pv[tile][0] * 256.f, pv[tile][1] * 256.f));
-                    const uint32_t x1 = movm_trans(pack2<false>(pv[tile][2] * 256.f, pv[tile][3] * 256.f));
-                    uint16_t h0, l0b, h1, l1b;
-                    split_e4m3x2(x0, h0, l0b);
-                    split_e4m3x2(x1, h1, l1b);
-                    if (t < 2) {
-                        bh[tile] = (uint32_t)h0 | ((uint32_t)h1 << 16);
-                        bl[tile] = (uint32_t)l0b | ((uint32_t)l1b << 16);
-                    } else {
-                        bh[tile] = (uint32_t)h1 | ((uint32_t)h0 << 16);
-                        bl[tile] = (uint32_t)l1b | ((uint32_t)l0b << 16);
-                    }
-                }
-                // O^T += V^T . P^T: V rows straight from the page, 32 tokens per step
-                uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;  // bytes of masked tokens -> 0
-                if (!full) {
-                    mlo = 0u;
-                    mhi = 0u;
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        if (tok_ok(4 * t + i)) mlo |= 0xffu << (8 * i);
-                        if (tok_ok(16 + 4 * t + i)) mhi |= 0xffu << (8 * i);
-                    }
-                }
-                if (bs >= 16) {
-                    const int vr = (lane & 7) + 8 * ((lane >> 3) & 1);
-                    const int tk = 16 * (lane >> 4);  // token half of this lane's matrix row
-                    const uint32_t vrow = vbase + (uint32_t)(tk >> bs_log2) * page_bytes + (uint32_t)(vr * bs + (tk & (bs - 1)));
-                    if (full) {
-#pragma unroll
-                        for (int mt = 0; mt < NK; ++mt) {
-                            uint32_t a0, a1, a2, a3;
-                            ldsm_x4(vrow + (uint32_t)mt * 16u * bs, a0, a1, a2, a3);
-                            mma_e4m3_16832(acc[mt], a0, a1, a2, a3, bh[0], bh[1]);
-                            mma_e4m3_16832(acc[mt], a0, a1, a2, a3, bl[0], bl[1]);
-                        }
-                    } else {
-#pragma unroll
-                        for (int mt = 0; mt < NK; ++mt) {
-                            uint32_t a0, a1, a2, a3;
-                            ldsm_x4(vrow + (uint32_t)mt * 16u * bs, a0, a1, a2, a3);
-                            a0 &= mlo;
-                            a1 &= mlo;
-                            a2 &= mhi;
-                            a3 &= mhi;
-                            mma_e4m3_16832(acc[mt], a0, a1, a2, a3, bh[0], bh[1]);
-                            mma_e4m3_16832(acc[mt], a0, a1, a2, a3, bl[0], bl[1]);
-                        }
-                    }
-                } else {
-                    // block size 8: a V row holds 8 tokens, so read each thread's 4 tokens
-                    const uint32_t va = vbase + (uint32_t)(t >> 1) * page_bytes + (uint32_t)((4 * t) & 7);
-                    const uint32_t vb = va + 2u * page_bytes;
-#pragma unroll
-                    for (int mt = 0; mt < NK; ++mt) {
-                        const uint32_t r0 = (uint32_t)(mt * 16 + g) * bs, r1 = r0 + 8u * bs;
-                        const uint32_t a0 = lds_u32(va + r0) & mlo, a1 = lds_u32(va + r1) & mlo;
-                        const uint32_t a2 = lds_u32(vb + r0) & mhi, a3 = lds_u32(vb + r1) & mhi;
-                        mma_e4m3_16832(acc[mt], a0, a1, a2, a3, bh[0], bh[1]);
-                        mma_e4m3_16832(acc[mt], a0, a1, a2, a3, bl[0], bl[1]);
-                    }
-                }
-            } else {
-                for (int tile = 0; tile < tiles_per_slot; ++tile) {
-                    const int ttok0 = stok0 + tile * 16;
-                    const int lim = t1 - ttok0;  // tokens [0, lim) of the tile are in range
-                    if (lim <= 0) break;
-                    const bool full = lim >= 16 && okmask == (pps == 1 ? 1u : 3u);
-                    auto tok_ok = [&](int tok) -> bool {
-                        const int pg = pps == 1 ? 0 : (tok >> 3);
-                        return tok < lim && ((okmask >> pg) & 1u);
-                    };
-
-                    // ---- S^T = K . Q^T for 16 tokens x 8 heads ------------------------------------
-                    uint32_t krow;
-                    if (pps == 1)
-                        krow = kbase + (uint32_t)(k_chunk * bs + tile * 16 + k_tok) * 16u;
-                    else
-                        krow = kbase + (uint32_t)(k_tok >> 3) * page_bytes + (uint32_t)(k_chunk * bs + (k_tok & 7)) * 16u;
-                    float sc[4] = {0.f, 0.f, 0.f, 0.f};
-    #pragma unroll
-                        for (int kk = 0; kk < NK; ++kk) {
-                            uint32_t a0, a1, a2, a3;
-                            if (HALF_STEP && kk == NK - 1) {
-                                ldsm_x2(krow + (uint32_t)kk * 32u * bs, a0, a1);
-                                a2 = a3 = 0u;
-                            } else {
-                                ldsm_x4(krow + (uint32_t)kk * 32u * bs, a0, a1, a2, a3);
-                            }
-                            mma16816<BF16>(sc, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
-                        }
-
-                    // ---- scores in base-2 units, masking, online softmax ---------------------------
-                    float s0 = sc[0] * qk_mul, s1 = sc[1] * qk_mul;
-                    float s2 = sc[2] * qk_mul, s3 = sc[3] * qk_mul;
-                    if (p.alibi != nullptr) {
-                        const float ra = (float)(ttok0 + tokA - tref), rb = (float)(ttok0 + tokB - tref);
-                        s0 = fmaf(sl0, ra, s0);
-                        s1 = fmaf(sl1, ra, s1);
-                        s2 = fmaf(sl0, rb, s2);
-                        s3 = fmaf(sl1, rb, s3);
-                    }
-                    if (!full) {
-                        if (!tok_ok(tokA)) s0 = s1 = -INFINITY;
-                        if (!tok_ok(tokB)) s2 = s3 = -INFINITY;
-                    }
-                    float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
-    #pragma unroll
-                    for (int o = 4; o < 32; o <<= 1) {
-                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, o));
-                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, o));
-                    }
-                    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-                    const float base0 = mn0 == -INFINITY ? 0.f : mn0;
-                    const float base1 = mn1 == -INFINITY ? 0.f : mn1;
-                    const float al0 = ex2(m0 - base0), al1 = ex2(m1 - base1);  // m = -inf -> 0
-                    const float p0 = ex2(s0 - base0), p1 = ex2(s1 - base1);
-                    const float p2 = ex2(s2 - base0), p3 = ex2(s3 - base1);
-                    l0 = fmaf(l0, al0, p0 + p2);
-                    l1 = fmaf(l1, al1, p1 + p3);
-                    // Rescale the accumulators only when some head's running max moved (after the
-                    // first tiles of a partition it rarely does); otherwise the factors are 1.
-                    if (__any_sync(0xffffffffu, mn0 != m0 || mn1 != m1)) {
-    #pragma unroll
-                        for (int i = 0; i < NK; ++i) {
-                            acc[i][0] *= al0;
-                            acc[i][1] *= al1;
-                            acc[i][2] *= al0;
-                            acc[i][3] *= al1;
-                        }
-                    }
-                    m0 = mn0;
-                    m1 = mn1;
-
-                    // ---- P into the B operand of O^T += V^T . P^T ----------------------------------
-                    const uint32_t pb0 = movm_trans(pack2<BF16>(p0, p1));
-                    const uint32_t pb1 = movm_trans(pack2<BF16>(p2, p3));
-                    uint32_t pl0 = 0, pl1 = 0;
-                    if constexpr (BF16) {
-                        // bf16 keeps 8 significant bits; add the rounding residual as a second term
-                        // so P enters the product with ~16 bits, as with fp16.
-                        const float q0 = p0 - __bfloat162float(__float2bfloat16_rn(p0));
-                        const float q1 = p1 - __bfloat162float(__float2bfloat16_rn(p1));
-                        const float q2 = p2 - __bfloat162float(__float2bfloat16_rn(p2));
-                        const float q3 = p3 - __bfloat162float(__float2bfloat16_rn(p3));
-                        pl0 = movm_trans(pack2<true>(q0, q1));
-                        pl1 = movm_trans(pack2<true>(q2, q3));
-                    }
-
-                    // ---- O^T += V^T . P^T over the head dimension ---------------------------------
-                        // lane -> (V row within the 16-row tile, token half)
-                        const int vr = (lane & 7) + 8 * ((lane >> 3) & 1);
-                        const int half = lane >> 4;
-                        uint32_t vpage, vtok;
-                        if (pps == 1) {
-                            vpage = vbase;
-                            vtok = (uint32_t)(tile * 16 + 8 * half);
-                        } else {
-                            vpage = vbase + (uint32_t)half * page_bytes;
-                            vtok = 0;
-                        }
-                        if (full) {
-    #pragma unroll
-                            for (int mt = 0; mt < NK; ++mt) {
-                                int row = mt * 16 + vr;
-                                if (HALF_STEP && mt == NK - 1) row = min(row, D - 1);
-                                uint32_t a0, a1, a2, a3;
-                                ldsm_x4(vpage + ((uint32_t)row * bs + vtok) * 2u, a0, a1, a2, a3);
-                                mma16816<BF16>(acc[mt], a0, a1, a2, a3, pb0, pb1);
-                                if constexpr (BF16) mma16816<BF16>(acc[mt], a0, a1, a2, a3, pl0, pl1);
-                            }
-                        } else {
-                            // zero the V columns of masked tokens (0 * NaN would poison every head):
-                            // a0/a1 hold tokens (2t, 2t+1), a2/a3 tokens (8+2t, 9+2t)
-                            const uint32_t mlo = (tok_ok(2 * t) ? 0x0000ffffu : 0u) | (tok_ok(2 * t + 1) ? 0xffff0000u : 0u);
-                            const uint32_t mhi = (tok_ok(8 + 2 * t) ? 0x0000ffffu : 0u) | (tok_ok(9 + 2 * t) ? 0xffff0000u : 0u);
-    #pragma unroll
-                            for (int mt = 0; mt < NK; ++mt) {
-                                int row = mt * 16 + vr;
-                                if (HALF_STEP && mt == NK - 1) row = min(row, D - 1);
-                                uint32_t a0, a1, a2, a3;
-                                ldsm_x4(vpage + ((uint32_t)row * bs + vtok) * 2u, a0, a1, a2, a3);
-                                a0 &= mlo;
-                                a1 &= mlo;
-                                a2 &= mhi;
-                                a3 &= mhi;
-                                mma16816<BF16>(acc[mt], a0, a1, a2, a3, pb0, pb1);
-                                if constexpr (BF16) mma16816<BF16>(acc[mt], a0, a1, a2, a3, pl0, pl1);
-                            }
-                        }
-                }
-            }
-
-            // Order this slot's generic-proxy reads before the async copy that refills it.
-            ++ncons;
-            if (++cpos == nstage) {
-                cpos = 0;
-                cphase ^= 1u;
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            issue_more();
-        }
-
-        // ---- merge the warps' (m, l, acc) of this partition --------------------------------
-#pragma unroll
-        for (int o = 4; o < 32; o <<= 1) {
-            l0 += __shfl_xor_sync(0xffffffffu, l0, o);
-            l1 += __shfl_xor_sync(0xffffffffu, l1, o);
-        }
-        if (g == 0) {
-            red_m[warp * kMaxHeadsPerCta + 2 * t] = m0;
-            red_m[warp * kMaxHeadsPerCta + 2 * t + 1] = m1;
-            red_l[warp * kMaxHeadsPerCta + 2 * t] = l0;
-            red_l[warp * kMaxHeadsPerCta + 2 * t + 1] = l1;
-        }
-        __syncthreads();
-        float M0 = -INFINITY, M1 = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            M0 = fmaxf(M0, red_m[w * kMaxHeadsPerCta + 2 * t]);
-            M1 = fmaxf(M1, red_m[w * kMaxHeadsPerCta + 2 * t + 1]);
-        }
-        const float f0 = m0 == -INFINITY ? 0.f : ex2(m0 - M0);
-        const float f1 = m1 == -INFINITY ? 0.f : ex2(m1 - M1);
-        if (warp == 0 && g == 0) {
-            float L0 = 0.f, L1 = 0.f;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) {
-                const float ma = red_m[w * kMaxHeadsPerCta + 2 * t], mb = red_m[w * kMaxHeadsPerCta + 2 * t + 1];
-                if (ma != -INFINITY) L0 += red_l[w * kMaxHeadsPerCta + 2 * t] * ex2(ma - M0);
-                if (mb != -INFINITY) L1 += red_l[w * kMaxHeadsPerCta + 2 * t + 1] * ex2(mb - M1);
-            }
-            fin_m[2 * t] = M0;
-            fin_m[2 * t + 1] = M1;
-            fin_l[2 * t] = L0;
-            fin_l[2 * t + 1] = L1;
-        }
-#pragma unroll
-        for (int mt = 0; mt < NK; ++mt) {
-            const int r0 = mt * 16 + g, r1 = r0 + 8;
-            if (2 * t < nh) {
-                float* base = red_o + (warp * nh + 2 * t) * RS;
-                if (r0 < D) base[r0] = acc[mt][0] * f0;
-                if (r1 < D) base[r1] = acc[mt][2] * f0;
-            }
-            if (2 * t + 1 < nh) {
-                float* base = red_o + (warp * nh + 2 * t + 1) * RS;
-                if (r0 < D) base[r0] = acc[mt][1] * f1;
-                if (r1 < D) base[r1] = acc[mt][3] * f1;
-            }
-        }
-        __syncthreads();
-
-        for (int e = threadIdx.x; e < nh * D; e += blockDim.x) {
-            const int hh = e / D, i = e - hh * D;
-            float v = 0.f;
-#pragma unroll
-            for (int w = 0; w < kWarps; ++w) v += red_o[(w * nh + hh) * RS + i];
-            const float lt = fin_l[hh];
-            v = lt > 0.f ? v * (v_mul / lt) : 0.f;
-            const int64_t row = (int64_t)s * H + h0 + hh;
-            if (single)
-                store_out<BF16>(p.out, row * D + i, v);
-            else if (p.tmp16)
-                store_out<BF16>(p.tmp_out, (row * p.Pmax + cq) * D + i, v);
-            else
-                static_cast<float*>(p.tmp_out)[(row * p.Pmax + cq) * D + i] = v;
-        }
-        if (threadIdx.x < nh) {
-            const int hh = threadIdx.x;
-            const int64_t sidx = ((int64_t)s * H + h0 + hh) * p.Pmax + cq;
-            const float lt = fin_l[hh];
-            float mlog = -INFINITY;
-            if (lt > 0.f) {
-                mlog = fin_m[hh] * kLn2;
-                if (p.alibi != nullptr) mlog = fmaf(p.alibi[h0 + hh], (float)tref, mlog);
-            }
-            p.max_logits[sidx] = mlog;
-            p.exp_sums[sidx] = lt;
-        }
-        __syncthreads();  // the merge buffers are reused by the next partition
-
-        // move the id buffers one partition on (the next ones were checked already; the ones
-        // after them were loaded at the start of this partition)
-        c0 = n0;
-        c1 = n1;
-        cmask = nmask;
-        n0 = nn0;
-        n1 = nn1;
-        nmask = cq + 2 * PX < Pl ? validate(cq + 2 * PX, n0, n1) : 0u;
-    }
-
-    if (aborted) {
-        // Let every copy this warp started land before the block can exit.
-        for (uint32_t n = drain_from; n < nis; ++n)
-            (void)mbar_wait_bounded(&bars[n % nstage], (n / nstage) & 1u, kWaitLimitNs);
-    }
-    griddep_launch_dependents();
-}
 
 // ---------------------------------------------------------------------------------------
 // Phase 2: log-sum-exp combine across partitions
@@ -984,28 +200,13 @@ static bool supported_head_size(int d) {
     }
 }
 
-using Phase1Fn = void (*)(const Phase1Params);
-
-template <bool BF16, int KVB>
-static Phase1Fn pick_phase1(int d) {
-    switch (d) {
-        case 64: return pa_v2_phase1_kernel<BF16, KVB, 64>;
-        case 80: return pa_v2_phase1_kernel<BF16, KVB, 80>;
-        case 96: return pa_v2_phase1_kernel<BF16, KVB, 96>;
-        case 112: return pa_v2_phase1_kernel<BF16, KVB, 112>;
-        case 128: return pa_v2_phase1_kernel<BF16, KVB, 128>;
-        case 192: return pa_v2_phase1_kernel<BF16, KVB, 192>;
-        case 256: return pa_v2_phase1_kernel<BF16, KVB, 256>;
-        case 120:
-            if constexpr (KVB == 2) return pa_v2_phase1_kernel<BF16, KVB, 120>;
-            else return nullptr;
+static Phase1Fn phase1_for(bool bf16, bool fp8, int d, int bs) {
+    switch (bs) {
+        case 8: return phase1_select<8>(bf16, fp8, d);
+        case 16: return phase1_select<16>(bf16, fp8, d);
+        case 32: return phase1_select<32>(bf16, fp8, d);
         default: return nullptr;
     }
-}
-
-static Phase1Fn phase1_for(bool bf16, bool fp8, int d) {
-    if (bf16) return fp8 ? pick_phase1<true, 1>(d) : pick_phase1<true, 2>(d);
-    return fp8 ? pick_phase1<false, 1>(d) : pick_phase1<false, 2>(d);
 }
 
 // Opt a kernel into `bytes` of dynamic shared memory once per (kernel, device).
@@ -1076,10 +277,12 @@ extern "C" const char* pa_status_string(pa_status status) {
 }
 
 cudaError_t pa::read_decode_errors(unsigned int* v, bool reset) {
-    cudaError_t e = cudaMemcpyFromSymbol(v, g_device_errors, sizeof(*v));
-    if (e != cudaSuccess || !reset) return e;
-    const unsigned int z = 0;
-    return cudaMemcpyToSymbol(g_device_errors, &z, sizeof(z));
+    unsigned int a = 0, b = 0, c = 0;
+    cudaError_t e = phase1_read_errors<8>(&a, reset);
+    if (e == cudaSuccess) e = phase1_read_errors<16>(&b, reset);
+    if (e == cudaSuccess) e = phase1_read_errors<32>(&c, reset);
+    *v = a | b | c;
+    return e;
 }
 
 extern "C" pa_status pa_get_device_errors(uint32_t* flags, int reset) {
@@ -1154,7 +357,7 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
                          (2 * kWarps + 2) * kMaxHeadsPerCta * sizeof(float) +
                          (size_t)kWarps * red_heads * (D + 4) * sizeof(float);
 
-    Phase1Fn fn = phase1_for(bf16, fp8, D);
+    Phase1Fn fn = phase1_for(bf16, fp8, D, bs);
     if (fn == nullptr) return PA_ERR_UNSUPPORTED;
     int dev = 0, optin = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||

@@ -1,0 +1,78 @@
+// pa_kernels.cuh -- definitions shared by the paged-attention kernels and their launchers:
+// tuning constants, kernel parameter blocks, the output store.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace pa {
+
+#ifndef PA_PHASE1_WARPS
+#define PA_PHASE1_WARPS 4
+#endif
+#ifndef PA_RING_KIB
+#define PA_RING_KIB 64
+#endif
+#ifndef PA_MIN_STAGES
+#define PA_MIN_STAGES 1
+#endif
+#ifndef PA_GRID_WAVES
+#define PA_GRID_WAVES 16
+#endif
+
+constexpr int kPartition = 512;
+constexpr int kWarps = PA_PHASE1_WARPS;  // phase-1 warps per CTA
+constexpr uint32_t kRingTarget = PA_RING_KIB * 1024u;  // shared-memory page ring per CTA
+constexpr int kMaxHeadsPerCta = 8;     // the MMA N dimension
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct Phase1Params {
+    void* out;
+    float* exp_sums;
+    float* max_logits;
+    void* tmp_out;  // fp32, or the output dtype when tmp16
+    const void* query;
+    const uint8_t* kcache;
+    const uint8_t* vcache;
+    const int32_t* block_tables;
+    const int32_t* seq_lens;
+    const float* alibi;
+    int H, Hk, G, ngroups, bs, mbps, num_blocks, Pmax, nstage;
+    uint32_t ring_bytes;  // kWarps * nstage * slot bytes
+    float qk_scale_log2;  // scale * k_scale * log2(e)
+    float v_scale;
+    int tmp16;  // tmp_output holds the output dtype instead of fp32
+};
+
+struct Phase2Params {
+    void* out;
+    const float* exp_sums;
+    const float* max_logits;
+    const void* tmp_out;  // fp32, or the output dtype (template parameter TMP16)
+    const int32_t* seq_lens;
+    int H, D, Pmax;
+};
+
+template <bool BF16>
+__device__ __forceinline__ void store_out(void* out, int64_t idx, float v) {
+    if constexpr (BF16)
+        reinterpret_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
+    else
+        reinterpret_cast<__half*>(out)[idx] = __float2half_rn(v);
+}
+
+using Phase1Fn = void (*)(const Phase1Params);
+
+// Phase-1 kernel for (query dtype, fp8 cache?, head size) at block size BS, or nullptr;
+// defined in pa_phase1_bs<BS>.cu.
+template <int BS>
+Phase1Fn phase1_select(bool bf16, bool fp8, int d);
+// Read (and optionally clear) the device error word of the block-size-BS phase-1 kernels.
+template <int BS>
+cudaError_t phase1_read_errors(unsigned int* v, bool reset);
+
+}  // namespace pa
