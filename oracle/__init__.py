@@ -59,6 +59,9 @@ def _load():
                                                         i32, i32, i32, f32, f32]
             lib.pa_oracle_decode_table.restype = i32
             lib.pa_oracle_decode_table.argtypes = [i32, P]
+            lib.pa_oracle_prefix.restype = i32
+            lib.pa_oracle_prefix.argtypes = [P, P, P, i32, P, P, i32, i32, i32, i32, i32, P, i32, P, P,
+                                             f32, P, i32, P, i32]
             lib.pa_oracle_copy_blocks.restype = i32
             lib.pa_oracle_copy_blocks.argtypes = [P, P, P, i32, i64, i32, i32]
             lib.pa_oracle_encode_e4m3.restype = None
@@ -190,3 +193,38 @@ def copy_blocks(dst: np.ndarray, src: np.ndarray, mapping) -> None:
                                    dst.shape[0])
     if rc != 0:
         raise ValueError("oracle copy_blocks: id out of range")
+
+
+def prefix(query, key, value, fmt: str, key_cache, value_cache, *, num_kv_heads: int, block_size: int,
+           block_tables, query_start_loc, context_lens, scale: float, rows=None,
+           threads: int = 0) -> np.ndarray:
+    """fp64 chunked-prefix attention ("paged_attn.py" _forward_prefix_pytorch): every new token
+    attends to its sequence's cached context and, causally, to the new tokens up to itself.
+    query [T, H, d], key/value [T, Hk, d].  Returns out [T, H, d] float64, or [len(rows), d]
+    for an optional int array of (token, head) rows."""
+    lib = _load()
+    q, k, v = _np(query), _np(key), _np(value)
+    kc, vc = _np(key_cache), _np(value_cache)
+    bt = np.ascontiguousarray(_np(block_tables), dtype=np.int32)
+    qsl = np.ascontiguousarray(_np(query_start_loc), dtype=np.int32)
+    cl = np.ascontiguousarray(_np(context_lens), dtype=np.int32)
+    T, H, d = q.shape
+    if rows is None:
+        rp, nr, out = None, 0, np.zeros((T, H, d))
+    else:
+        rr = np.ascontiguousarray(np.asarray(rows, dtype=np.int32).reshape(-1, 2))
+        rp, nr, out = _ptr(rr), rr.shape[0], np.zeros((rr.shape[0], d))
+    rc = lib.pa_oracle_prefix(_ptr(q), _ptr(k), _ptr(v), FMT[fmt], _ptr(kc), _ptr(vc), cl.shape[0], H,
+                              num_kv_heads, d, block_size, _ptr(bt), bt.shape[1], _ptr(qsl), _ptr(cl),
+                              float(scale), rp, nr, _ptr(out), int(threads))
+    if rc != 0:
+        raise ValueError("oracle prefix rejected the arguments")
+    return out
+
+
+def prefix_workload(wl, rows=None, threads: int = 0) -> np.ndarray:
+    """``prefix`` on a chunked-prefill workload (all rows, or the given (token, head) rows)."""
+    return prefix(wl.query, wl.key, wl.value, wl.q_dtype, wl.key_cache, wl.value_cache,
+                  num_kv_heads=wl.num_kv_heads, block_size=wl.block_size,
+                  block_tables=wl.block_tables, query_start_loc=wl.query_start_loc,
+                  context_lens=wl.context_lens, scale=wl.scale, rows=rows, threads=threads)

@@ -348,3 +348,87 @@ int pa_oracle_copy_blocks(void* dst, const void* src, const int64_t* mapping, in
     }
     return 0;
 }
+
+/*
+ * Chunked-prefix attention ("paged_attn.py", _forward_prefix_pytorch): sequence i has
+ * ctx = context_lens[i] tokens already in the paged cache and q_len = qsl[i+1] - qsl[i] new
+ * tokens whose rows are query/key/value[qsl[i] + j].  Query j of head h (absolute position
+ * ctx + j) attends to every context token and to new tokens 0..j:
+ *   s = scale * <q, k> over those keys, out = softmax(s) . v,   kv head = h / (H / Hk).
+ * Rows: query [T][H][d], key/value [T][Hk][d] (contiguous), cache views as for decode.
+ * rows: optional list of (token, head) pairs; out then holds one d-vector per pair, else
+ * out is [T][H][d].  All in fp64.  Returns 0, or -1 on bad sizes.
+ */
+int pa_oracle_prefix(const void* query, const void* key, const void* value, int fmt,
+                     const void* key_cache, const void* value_cache, int num_seqs, int num_heads,
+                     int num_kv_heads, int head_size, int block_size, const int32_t* block_tables,
+                     int max_blocks_per_seq, const int32_t* query_start_loc,
+                     const int32_t* context_lens, float scale, const int32_t* rows, int num_rows,
+                     double* out, int num_threads) {
+    if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads || head_size % 8) return -1;
+    if (fmt != ORC_F16 && fmt != ORC_BF16) return -1;
+    orc_args a = {NULL, fmt, key_cache, value_cache, fmt, num_seqs, num_heads, num_kv_heads,
+                  head_size, block_size, block_tables, max_blocks_per_seq, NULL, (double)scale,
+                  NULL, 1.0, 1.0, 0x7fffffff, 1};
+    const int H = num_heads, Hk = num_kv_heads, d = head_size, G = H / Hk;
+    for (int i = 0; i < num_seqs; ++i) {
+        int ctx = context_lens[i];
+        if (ctx < 0 || (ctx + block_size - 1) / block_size > max_blocks_per_seq) return -1;
+        if (query_start_loc[i + 1] < query_start_loc[i]) return -1;
+    }
+    const int T = query_start_loc[num_seqs];
+    const int64_t n = rows ? (int64_t)num_rows : (int64_t)T * H;
+    for (int64_t r = 0; rows && r < n; ++r)
+        if (rows[2 * r] < 0 || rows[2 * r] >= T || rows[2 * r + 1] < 0 || rows[2 * r + 1] >= H) return -1;
+#ifdef _OPENMP
+    if (num_threads > 0) omp_set_num_threads(num_threads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int64_t r = 0; r < n; ++r) {
+        {
+            const int tq = rows ? rows[2 * r] : (int)(r / H);
+            const int h = rows ? rows[2 * r + 1] : (int)(r % H);
+            int i = 0;
+            while (query_start_loc[i + 1] <= tq) ++i;
+            const int q0 = query_start_loc[i], j = tq - q0, ctx = context_lens[i];
+            const int kvh = h / G;
+            const int nk = ctx + j + 1;
+            double* sc = (double*)malloc(sizeof(double) * nk);
+            double M = -INFINITY;
+            for (int t = 0; t < nk; ++t) {
+                double dot = 0.0;
+                for (int e = 0; e < d; ++e) {
+                    double qv = dec_elem(query, ((int64_t)tq * H + h) * d + e, fmt), kv;
+                    if (t < ctx) {
+                        int64_t b = block_tables[(int64_t)i * max_blocks_per_seq + t / block_size];
+                        kv = k_at(&a, b, kvh, e, t % block_size);
+                    } else {
+                        kv = dec_elem(key, ((int64_t)(q0 + t - ctx) * Hk + kvh) * d + e, fmt);
+                    }
+                    dot += qv * kv;
+                }
+                sc[t] = (double)scale * dot;
+                M = sc[t] > M ? sc[t] : M;
+            }
+            double Z = 0.0;
+            for (int t = 0; t < nk; ++t) Z += exp(sc[t] - M);
+            double* o = out + r * d;
+            for (int e = 0; e < d; ++e) o[e] = 0.0;
+            for (int t = 0; t < nk; ++t) {
+                const double w = exp(sc[t] - M) / Z;
+                for (int e = 0; e < d; ++e) {
+                    double vv;
+                    if (t < ctx) {
+                        int64_t b = block_tables[(int64_t)i * max_blocks_per_seq + t / block_size];
+                        vv = v_at(&a, b, kvh, e, t % block_size);
+                    } else {
+                        vv = dec_elem(value, ((int64_t)(q0 + t - ctx) * Hk + kvh) * d + e, fmt);
+                    }
+                    o[e] += w * vv;
+                }
+            }
+            free(sc);
+        }
+    }
+    return 0;
+}

@@ -354,3 +354,169 @@ def shard(wl_name: str, rank: int, world: int, **kw) -> Workload:
     a rank-specific seed.  Sequences are independent, so ranks share nothing."""
     base = CONFIGS[wl_name]["seed"]
     return make(wl_name, seed=base + 100_003 * rank, **kw)
+
+
+# --------------------------------------------------------------------------------------
+# Chunked-prefix (prefill) inputs: "paged_attn.py", _forward_prefix_pytorch.
+# --------------------------------------------------------------------------------------
+@dataclasses.dataclass
+class PrefixWorkload:
+    """One chunked-prefill step: sequence s has ``context_lens[s]`` tokens already in the
+    paged cache and ``q_len = query_start_loc[s+1] - query_start_loc[s]`` new tokens whose
+    query/key/value rows are dense.  The block table covers context + new tokens (as a
+    serving engine's table would after writing the chunk), but the cache slots of the new
+    tokens hold NaN canaries: the method reads the chunk's keys and values from the dense
+    ``key``/``value`` rows, never from the cache."""
+
+    name: str
+    num_seqs: int
+    num_heads: int
+    num_kv_heads: int
+    head_size: int
+    block_size: int
+    num_blocks: int
+    q_dtype: str
+    scale: float
+    query: torch.Tensor  # [T, H, d]
+    key: torch.Tensor  # [T, Hk, d]
+    value: torch.Tensor  # [T, Hk, d]
+    key_cache: torch.Tensor  # [NB, Hk, d/x, bs, x]
+    value_cache: torch.Tensor  # [NB, Hk, d, bs]
+    block_tables: torch.Tensor  # int32 [S, W]
+    query_start_loc: torch.Tensor  # int32 [S + 1]
+    context_lens: torch.Tensor  # int32 [S]
+    seq_lens: torch.Tensor  # int32 [S] context + new tokens
+    max_query_len: int
+    seed: int = 0
+
+    @property
+    def x(self) -> int:
+        return 8
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.query_start_loc[-1])
+
+    @property
+    def query_lens(self) -> np.ndarray:
+        q = self.query_start_loc.numpy().astype(np.int64)
+        return q[1:] - q[:-1]
+
+    def flops(self) -> int:
+        """Multiply-adds x 2 of the two products: query token j of a sequence with context c
+        sees c + j + 1 keys, each costing d MACs for the score and d for the value sum."""
+        c = self.context_lens.numpy().astype(np.int64)
+        q = self.query_lens
+        keys = (q * c + q * (q + 1) // 2).sum()
+        return int(4 * self.head_size * self.num_heads * keys)
+
+    def algorithmic_bytes(self) -> int:
+        """Bytes read and written once: context K/V per kv head, the chunk's q/k/v rows, out."""
+        c = int(self.context_lens.to(torch.int64).sum())
+        T, H, Hk, d = self.num_tokens, self.num_heads, self.num_kv_heads, self.head_size
+        return 2 * (2 * c * Hk * d + T * (2 * H + 2 * Hk) * d)
+
+
+PREFIX_CONFIGS = {
+    "prefix_tiny": dict(
+        num_seqs=3, num_heads=4, num_kv_heads=2, head_size=64, block_size=16,
+        context_lens=[0, 37, 600], query_lens=[5, 70, 129], q_dtype="f16", seed=2001,
+    ),
+    # The pages' model shape (24 query heads, 4 kv heads, head size 256) with one chunked
+    # prefill step of 4096 new tokens (the pages' max_num_batched_tokens) split over four
+    # sequences whose cached prefixes run from none to ~100K tokens.
+    "prefix_long_gqa": dict(
+        num_seqs=4, num_heads=24, num_kv_heads=4, head_size=256, block_size=16,
+        context_lens=[0, 8192, 32768, 98304], query_lens=[1024] * 4, q_dtype="f16",
+        sigma=0.5, seed=2002,
+    ),
+    # Llama-style GQA (32/8, d 128): eight sequences of 512 new tokens over cached prefixes
+    # drawn uniformly from [0, 16384].
+    "prefix_llama_gqa": dict(
+        num_seqs=8, num_heads=32, num_kv_heads=8, head_size=128, block_size=16,
+        context_lens=("uniform", 0, 16384), query_lens=[512] * 8, q_dtype="bf16", seed=2003,
+    ),
+}
+
+PREFIX_REDUCED = {
+    "prefix_tiny": {},
+    "prefix_long_gqa": dict(num_seqs=3, context_lens=[0, 700, 1500], query_lens=[200, 131, 64]),
+    "prefix_llama_gqa": dict(num_seqs=4, context_lens=("uniform", 0, 900),
+                             query_lens=[100, 1, 257, 64]),
+}
+
+
+def build_prefix(*, name: str = "custom", num_seqs: int, num_heads: int, num_kv_heads: int,
+                 head_size: int, block_size: int, context_lens: Sequence[int],
+                 query_lens: Sequence[int], q_dtype: str = "f16", sigma: float = 1.0,
+                 scale: Optional[float] = None, block_slack: float = 1.25,
+                 table_width: Optional[int] = None, canaries: bool = True,
+                 seed: int = 0) -> PrefixWorkload:
+    """Seeded chunked-prefill inputs; block ids dealt from one permutation as in ``build``."""
+    rng = np.random.default_rng(seed)
+    S, H, Hk, d, bs = num_seqs, num_heads, num_kv_heads, head_size, block_size
+    ctx = np.asarray(context_lens, dtype=np.int64)
+    ql = np.asarray(query_lens, dtype=np.int64)
+    assert ctx.shape == (S,) and ql.shape == (S,) and d % 8 == 0
+    tot = ctx + ql
+    need = [-(-int(L) // bs) for L in tot]
+    total = sum(need)
+    num_blocks = max(total + 1, int(math.ceil(total * block_slack)))
+    width = max(1, max(need)) if table_width is None else int(table_width)
+    assert width >= max(need + [1])
+    perm = rng.permutation(num_blocks).astype(np.int64)
+    tables = np.empty((S, width), dtype=np.int64)
+    canary = int(perm[total])
+    pos = 0
+    for s in range(S):
+        tables[s, :need[s]] = perm[pos:pos + need[s]]
+        tables[s, need[s]:] = canary
+        pos += need[s]
+    T = int(ql.sum())
+    key_cache = _to_storage(_fill_normal((num_blocks, Hk, d // 8, bs, 8), sigma, seed, 11), q_dtype)
+    value_cache = _to_storage(_fill_normal((num_blocks, Hk, d, bs), sigma, seed, 12), q_dtype)
+    query = _to_storage(_fill_normal((T, H, d), sigma, seed, 13), q_dtype)
+    key = _to_storage(_fill_normal((T, Hk, d), sigma, seed, 14), q_dtype)
+    value = _to_storage(_fill_normal((T, Hk, d), sigma, seed, 15), q_dtype)
+    if canaries:
+        used = np.zeros(num_blocks, dtype=bool)
+        used[perm[:total]] = True
+        for b in np.nonzero(~used)[0]:
+            _nan_fill_(key_cache[int(b)], q_dtype)
+            _nan_fill_(value_cache[int(b)], q_dtype)
+        for s in range(S):
+            # every slot from the first new token on: the chunk is read from key/value
+            for t in range(int(ctx[s]), need[s] * bs):
+                b, o = int(tables[s, t // bs]), t % bs
+                _nan_fill_(key_cache[b, :, :, o, :], q_dtype)
+                _nan_fill_(value_cache[b, :, :, o], q_dtype)
+    qsl = np.zeros(S + 1, dtype=np.int64)
+    qsl[1:] = np.cumsum(ql)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    return PrefixWorkload(
+        name=name, num_seqs=S, num_heads=H, num_kv_heads=Hk, head_size=d, block_size=bs,
+        num_blocks=num_blocks, q_dtype=q_dtype, scale=float(np.float32(scale)), query=query,
+        key=key, value=value, key_cache=key_cache, value_cache=value_cache,
+        block_tables=torch.from_numpy(tables.astype(np.int32)),
+        query_start_loc=torch.from_numpy(qsl.astype(np.int32)),
+        context_lens=torch.from_numpy(ctx.astype(np.int32)),
+        seq_lens=torch.from_numpy(tot.astype(np.int32)), max_query_len=int(ql.max(initial=0)),
+        seed=seed,
+    )
+
+
+def make_prefix(name: str, *, reduced: bool = False, seed: Optional[int] = None,
+                **overrides) -> PrefixWorkload:
+    """One of the named chunked-prefill workloads, full size or reduced."""
+    cfg = dict(PREFIX_CONFIGS[name])
+    if reduced:
+        cfg.update(PREFIX_REDUCED[name])
+    cfg.update(overrides)
+    if seed is not None:
+        cfg["seed"] = seed
+    c = cfg["context_lens"]
+    if isinstance(c, tuple):
+        rng = np.random.default_rng(cfg["seed"] + 7)
+        cfg["context_lens"] = _draw_lens(c, cfg["num_seqs"], rng)
+    return build_prefix(name=name, **cfg)
