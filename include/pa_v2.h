@@ -201,6 +201,47 @@ PA_API pa_status pa_swap_blocks(const void* src_cache, void* dst_cache, const in
                                 int num_pairs, int64_t block_bytes, int src_num_blocks,
                                 int dst_num_blocks, cudaStream_t stream);
 
+/*
+ * pa_prefix -- chunked-prefix (prefill) attention: new tokens of each sequence attend to the
+ * sequence's cached context and, causally, to the new tokens before and at themselves.
+ *
+ * Defines: "paged_attn.py", forward_prefix / _forward_prefix_pytorch.  Sequence s has
+ * ctx = context_lens[s] tokens in the paged cache (views as for pa_v2_decode) and
+ * q_len = query_start_loc[s+1] - query_start_loc[s] new tokens, rows
+ * query_start_loc[s] .. query_start_loc[s+1]-1 of query/key/value.  For new token j and
+ * query head h (kv head h / (num_heads / num_kv_heads)):
+ *   keys   = the ctx cached tokens (block_tables[s][t / block_size], slot t % block_size),
+ *            then key rows 0..j of the chunk (the chunk is read from key/value, not the cache);
+ *   output = softmax(scale * q . keys) . values, rounded once to the query dtype.
+ * The pages fix scale = head_size^-0.5; it is an argument here.  The cache holds the query
+ * dtype (fp8 caches have no prefix path on the pages).
+ *
+ * Arguments (device pointers unless noted):
+ *   output       [T][num_heads][head_size] contiguous, T = query_start_loc[num_seqs].
+ *   query        rows of q_row_stride elements, head h at h * head_size; key/value rows of
+ *                kv_row_stride elements, kv head at kvh * head_size.  Strides are multiples
+ *                of 8 elements; every pointer is 16-byte aligned.
+ *   key_cache    [num_blocks][num_kv_heads][head_size/8][block_size][8]
+ *   value_cache  [num_blocks][num_kv_heads][head_size][block_size]
+ *   block_tables int32 [num_seqs][max_blocks_per_seq]
+ *   query_start_loc int32 [num_seqs + 1] non-decreasing; context_lens int32 [num_seqs].
+ *   max_query_len  host int >= every q_len (sizes the grid).
+ *   head_size in {64, 80, 96, 112, 120, 128, 192, 256}; block_size in {8, 16, 32};
+ *   dtype PA_DT_F16 or PA_DT_BF16 (query, key, value, caches and output).
+ * Errors: PA_ERR_INVALID_ARG / PA_ERR_UNSUPPORTED before anything is enqueued.  On the
+ * device, a cached block id outside [0, num_blocks) masks that page (bit 5 of
+ * pa_get_device_errors); a context longer than the table row is capped to the row, as the
+ * pages do (bit 6); a sequence with q_len > max_query_len or a negative length is skipped
+ * (bit 7).
+ */
+PA_API pa_status pa_prefix(void* output, const void* query, const void* key, const void* value,
+                           const void* key_cache, const void* value_cache, int num_seqs,
+                           int num_heads, int num_kv_heads, int head_size, float scale,
+                           const int32_t* block_tables, int max_blocks_per_seq, int num_blocks,
+                           const int32_t* query_start_loc, const int32_t* context_lens,
+                           int max_query_len, int block_size, int64_t q_row_stride,
+                           int64_t kv_row_stride, pa_dtype dtype, cudaStream_t stream);
+
 /* Tokens per partition: 512 ("paged_attention_v2_pytorch.py", _PARTITION_SIZE). */
 PA_API int pa_v2_partition_size(void);
 
@@ -210,7 +251,8 @@ PA_API const char* pa_status_string(pa_status status);
 /* Device-side error flags (bit 0: a block id outside [0, num_blocks) or a table row too
  * short; bit 1: a sequence longer than max_num_partitions * 512 or a negative length;
  * bit 2: a bounded wait for a shared-memory copy gave up; bit 3: a slot outside the
- * cache; bit 4: a pa_copy_blocks id outside the cache).  Reads the flags of the current device (this synchronises the device) into
+ * cache; bit 4: a pa_copy_blocks id outside the cache; bits 5-7: pa_prefix, see there).
+ * Reads the flags of the current device (this synchronises the device) into
  * *flags, and clears them when reset != 0.  Not part of the pages' interface: it reports
  * what the kernels skipped instead of faulting. */
 PA_API pa_status pa_get_device_errors(uint32_t* flags, int reset);

@@ -73,6 +73,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.pa_copy_blocks.argtypes = [P, P, i32, P, i32, i64, i32, P]
     lib.pa_swap_blocks.restype = i32
     lib.pa_swap_blocks.argtypes = [P, P, P, i32, i64, i32, i32, P]
+    lib.pa_prefix.restype = i32
+    lib.pa_prefix.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, f32, P, i32, i32, P, P, i32, i32, i64, i64,
+                              i32, P]
     lib.pa_v2_decode_noalloc.restype = i32
     lib.pa_v2_decode_noalloc.argtypes = [P, P, P, P, i32, i32, i32, i32, f32, P, i32, i32, P, i32, i32,
                                          P, i32, i32, f32, f32, P]
@@ -253,6 +256,43 @@ def pa_swap_blocks(src: torch.Tensor, dst: torch.Tensor, block_mapping: torch.Te
         stream = torch.cuda.current_stream(dst.device if dst.is_cuda else src.device)
     _check("pa_swap_blocks", lib.pa_swap_blocks(_ptr(src), _ptr(dst), _ptr(m), m.shape[0], block_bytes,
                                                 src.shape[0], dst.shape[0], _stream(stream)))
+
+
+def pa_prefix(output: torch.Tensor, query: torch.Tensor, key: torch.Tensor, value: torch.Tensor,
+              key_cache: torch.Tensor, value_cache: torch.Tensor, block_tables: torch.Tensor,
+              query_start_loc: torch.Tensor, context_lens: torch.Tensor, max_query_len: int,
+              scale: Optional[float] = None, stream=None) -> None:
+    """Chunked-prefix attention ("paged_attn.py" forward_prefix): every new token attends to
+    its sequence's cached context and, causally, to the chunk's tokens up to itself.
+    output/query [T, H, d], key/value [T, Hk, d] (rows may be strided, last two dims dense),
+    caches in the decode layouts, int32 block_tables [S, W], query_start_loc [S+1],
+    context_lens [S].  scale defaults to d^-0.5 as on the pages."""
+    lib = load()
+    T, H, d = query.shape
+    Hk = key_cache.shape[1]
+    bs = value_cache.shape[3]
+    for name, t in (("query", query), ("key", key), ("value", value)):
+        if t.dim() != 3 or t.stride(2) != 1 or t.stride(1) != d or not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor [T, heads, d] with dense heads")
+    if key.stride(0) != value.stride(0):
+        raise ValueError("key and value must share a row stride")
+    if not output.is_contiguous() or output.shape != query.shape or output.dtype != query.dtype:
+        raise ValueError("output must be a contiguous tensor shaped like query")
+    for name, t in (("key_cache", key_cache), ("value_cache", value_cache)):
+        if not t.is_contiguous() or t.dtype != query.dtype:
+            raise ValueError(f"{name} must be contiguous in the query dtype")
+    for name, t in (("block_tables", block_tables), ("query_start_loc", query_start_loc),
+                    ("context_lens", context_lens)):
+        if t.dtype != torch.int32 or not t.is_contiguous() or not t.is_cuda:
+            raise TypeError(f"{name} must be a contiguous int32 CUDA tensor")
+    S = context_lens.shape[0]
+    if scale is None:
+        scale = d ** -0.5
+    _check("pa_prefix", lib.pa_prefix(
+        _ptr(output), _ptr(query), _ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache), S, H, Hk, d,
+        float(scale), _ptr(block_tables), block_tables.shape[1], key_cache.shape[0], _ptr(query_start_loc),
+        _ptr(context_lens), int(max_query_len), bs, query.stride(0), key.stride(0), _dt(query.dtype),
+        _stream(stream)))
 
 
 def pa_v2_partition_size() -> int:

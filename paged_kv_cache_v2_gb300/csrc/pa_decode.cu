@@ -292,7 +292,10 @@ extern "C" pa_status pa_get_device_errors(uint32_t* flags, int reset) {
     if (read_decode_errors(&a, reset != 0) != cudaSuccess) return PA_ERR_CUDA;
     if (read_cache_errors(&b, reset != 0) != cudaSuccess) return PA_ERR_CUDA;
     if (read_block_errors(&c, reset != 0) != cudaSuccess) return PA_ERR_CUDA;
-    *flags = a | b | c;
+    unsigned int d = 0, e = 0;
+    if (prefix_read_errors<false>(&d, reset != 0) != cudaSuccess) return PA_ERR_CUDA;
+    if (prefix_read_errors<true>(&e, reset != 0) != cudaSuccess) return PA_ERR_CUDA;
+    *flags = a | b | c | d | e;
     return PA_OK;
 }
 

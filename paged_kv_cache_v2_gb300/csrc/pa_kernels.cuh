@@ -75,4 +75,34 @@ Phase1Fn phase1_select(bool bf16, bool fp8, int d);
 template <int BS>
 cudaError_t phase1_read_errors(unsigned int* v, bool reset);
 
+// ---- chunked-prefix attention ----------------------------------------------------------
+constexpr int kPfxWarps = 8;
+constexpr int kPfxThreads = kPfxWarps * 32;
+constexpr int kPfxBM = kPfxWarps * 16;  // query rows per CTA
+constexpr int kPfxBN = 64;              // keys per tile
+constexpr int kPfxStages = 2;
+
+struct PrefixParams {
+    void* out;
+    const uint8_t* q;  // [T][q_stride] rows, head h at h * d
+    const uint8_t* k;  // [T][kv_stride] rows, kv head at kvh * d
+    const uint8_t* v;
+    const uint8_t* kcache;
+    const uint8_t* vcache;
+    const int32_t* block_tables;
+    const int32_t* qsl;
+    const int32_t* ctx_lens;
+    int H, Hk, G, bs, bs_log2, mbps, num_blocks, max_query_len;
+    int64_t q_stride, kv_stride;  // elements between consecutive tokens
+    float sl2;                    // scale * log2(e)
+};
+
+using PrefixFn = cudaError_t (*)(const PrefixParams&, dim3 grid, cudaStream_t);
+
+// Prefix kernel launcher for (query dtype, head size), or nullptr; defined in pa_prefix_<dtype>.cu.
+template <bool BF16>
+PrefixFn prefix_select(int d);
+template <bool BF16>
+cudaError_t prefix_read_errors(unsigned int* v, bool reset);
+
 }  // namespace pa

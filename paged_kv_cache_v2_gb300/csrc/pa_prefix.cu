@@ -1,0 +1,74 @@
+// pa_prefix.cu -- host entry point of chunked-prefix attention ("paged_attn.py",
+// forward_prefix): argument checks, grid sizing, kernel selection.  The kernels live in
+// pa_prefix.cuh (instantiated per dtype in pa_prefix_f16.cu / pa_prefix_bf16.cu).
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "pa_internal.h"
+#include "pa_kernels.cuh"
+#include "pa_v2.h"
+
+using namespace pa;
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+extern "C" pa_status pa_prefix(void* output, const void* query, const void* key, const void* value,
+                               const void* key_cache, const void* value_cache, int num_seqs, int num_heads,
+                               int num_kv_heads, int head_size, float scale, const int32_t* block_tables,
+                               int max_blocks_per_seq, int num_blocks, const int32_t* query_start_loc,
+                               const int32_t* context_lens, int max_query_len, int block_size,
+                               int64_t q_row_stride, int64_t kv_row_stride, pa_dtype dtype, cudaStream_t stream) {
+    if (num_seqs < 0 || num_seqs > 65535 || max_query_len < 0) return PA_ERR_INVALID_ARG;
+    if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads || num_kv_heads > 65535)
+        return PA_ERR_INVALID_ARG;
+    if (!(scale > 0.f) || !isfinite(scale)) return PA_ERR_INVALID_ARG;
+    if (max_blocks_per_seq <= 0 || num_blocks <= 0) return PA_ERR_INVALID_ARG;
+    if (dtype != PA_DT_F16 && dtype != PA_DT_BF16) return PA_ERR_UNSUPPORTED;
+    if (block_size != 8 && block_size != 16 && block_size != 32) return PA_ERR_UNSUPPORTED;
+    const bool bf16 = dtype == PA_DT_BF16;
+    PrefixFn fn = bf16 ? prefix_select<true>(head_size) : prefix_select<false>(head_size);
+    if (fn == nullptr) return PA_ERR_UNSUPPORTED;
+    const int G = num_heads / num_kv_heads;
+    if ((int64_t)max_query_len * G > (1ll << 30) || (int64_t)max_blocks_per_seq * block_size > (1ll << 30))
+        return PA_ERR_INVALID_ARG;
+    if (q_row_stride < (int64_t)num_heads * head_size || kv_row_stride < (int64_t)num_kv_heads * head_size ||
+        q_row_stride % 8 || kv_row_stride % 8)
+        return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0 || max_query_len == 0) return PA_OK;
+    if (!output || !query || !key || !value || !key_cache || !value_cache || !block_tables || !query_start_loc ||
+        !context_lens)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(output) || !aligned16(query) || !aligned16(key) || !aligned16(value) || !aligned16(key_cache) ||
+        !aligned16(value_cache))
+        return PA_ERR_INVALID_ARG;
+
+    PrefixParams p;
+    p.out = output;
+    p.q = static_cast<const uint8_t*>(query);
+    p.k = static_cast<const uint8_t*>(key);
+    p.v = static_cast<const uint8_t*>(value);
+    p.kcache = static_cast<const uint8_t*>(key_cache);
+    p.vcache = static_cast<const uint8_t*>(value_cache);
+    p.block_tables = block_tables;
+    p.qsl = query_start_loc;
+    p.ctx_lens = context_lens;
+    p.H = num_heads;
+    p.Hk = num_kv_heads;
+    p.G = G;
+    p.bs = block_size;
+    p.bs_log2 = block_size == 8 ? 3 : (block_size == 16 ? 4 : 5);
+    p.mbps = max_blocks_per_seq;
+    p.num_blocks = num_blocks;
+    p.max_query_len = max_query_len;
+    p.q_stride = q_row_stride;
+    p.kv_stride = kv_row_stride;
+    p.sl2 = scale * kLog2e;
+    const int64_t row_tiles = ((int64_t)max_query_len * G + kPfxBM - 1) / kPfxBM;
+    const dim3 grid((unsigned)row_tiles, (unsigned)num_kv_heads, (unsigned)num_seqs);
+    if (fn(p, grid, stream) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return PA_ERR_CUDA;
+    }
+    return PA_OK;
+}

@@ -1,0 +1,8 @@
+// pa_prefix_bf16.cu -- chunked-prefix attention kernels for bf16 queries and caches, one per
+// supported head size (a translation unit per dtype so the two compile in parallel).
+#include "pa_prefix.cuh"
+
+namespace pa {
+template PrefixFn prefix_select<true>(int d);
+template cudaError_t prefix_read_errors<true>(unsigned int* v, bool reset);
+}  // namespace pa

@@ -1,0 +1,8 @@
+// pa_prefix_f16.cu -- chunked-prefix attention kernels for f16 queries and caches, one per
+// supported head size (a translation unit per dtype so the two compile in parallel).
+#include "pa_prefix.cuh"
+
+namespace pa {
+template PrefixFn prefix_select<false>(int d);
+template cudaError_t prefix_read_errors<false>(unsigned int* v, bool reset);
+}  // namespace pa

@@ -128,3 +128,75 @@ def sample_pairs(wl, n=24, seed=0):
     for i, s in enumerate(seqs[:n]):
         pairs.append((s, int(rng.integers(0, H)) if i > 1 else (0 if i == 0 else H - 1)))
     return np.array(pairs, dtype=np.int32)
+
+
+# ---- chunked-prefix attention ------------------------------------------------------------
+# Tolerance (prefix): output max-abs error <= 2e-3 plus half an ulp of the output dtype at
+# the reference value, the decode bar for 16-bit caches.
+TOL_PREFIX = 2e-3
+
+
+def prefix_to_device(wl, device="cuda"):
+    return {k: getattr(wl, k).to(device) for k in
+            ("query", "key", "value", "key_cache", "value_cache", "block_tables", "query_start_loc",
+             "context_lens")}
+
+
+def run_prefix(wl, dev=None, max_query_len=None, poison=True, q_rows=None, kv_rows=None):
+    """pa_prefix on a chunked-prefill workload; returns the CPU output [T, H, d].
+    q_rows / kv_rows: optional wider row buffers the inputs are copied into (strided views)."""
+    if dev is None:
+        dev = prefix_to_device(wl)
+    q, k, v = dev["query"], dev["key"], dev["value"]
+    if q_rows is not None:
+        buf = torch.zeros(q.shape[0], q_rows, dtype=q.dtype, device="cuda")
+        buf[:, : q.shape[1] * q.shape[2]] = q.reshape(q.shape[0], -1)
+        q = buf[:, : q.shape[1] * q.shape[2]].view(q.shape[0], q.shape[1], q.shape[2])
+    if kv_rows is not None:
+        n = k.shape[1] * k.shape[2]
+        buf = torch.zeros(k.shape[0], kv_rows, dtype=k.dtype, device="cuda")
+        buf[:, :n] = k.reshape(k.shape[0], -1)
+        buf[:, kv_rows // 2: kv_rows // 2 + n] = v.reshape(v.shape[0], -1)
+        k = buf[:, :n].view(k.shape)
+        v = buf[:, kv_rows // 2: kv_rows // 2 + n].view(v.shape)
+    out = torch.full(wl.query.shape, float("nan") if poison else 0.0, dtype=wl.query.dtype, device="cuda")
+    mql = wl.max_query_len if max_query_len is None else max_query_len
+    pa.pa_prefix(out, q, k, v, dev["key_cache"], dev["value_cache"], dev["block_tables"],
+                 dev["query_start_loc"], dev["context_lens"], mql, scale=wl.scale)
+    torch.cuda.synchronize()
+    return out.cpu()
+
+
+def check_prefix(wl, out, ref, rows=None, label=""):
+    """Compare a GPU prefix output with the oracle (all rows, or (token, head) rows)."""
+    if rows is None:
+        g = out.double().numpy()
+        r = ref
+    else:
+        rows = np.asarray(rows)
+        g = out[rows[:, 0], rows[:, 1]].double().numpy()
+        r = ref
+    assert np.isfinite(g).all(), f"{label}: non-finite output"
+    err = np.abs(g - r)
+    allow = TOL_PREFIX + half_ulp(r, wl.q_dtype)
+    bad = err > allow
+    if bad.any():
+        idx = np.unravel_index(int(np.argmax(err - allow)), err.shape)
+        raise AssertionError(f"{label}: prefix mismatch at {idx}: err {err[idx]:.3g} allow {allow[idx]:.3g}")
+    return float(err.max())
+
+
+def prefix_sample_rows(wl, n=48, seed=0):
+    """(token, head) rows: first and last token of every sequence's chunk, tokens around
+    64-key tile edges, then random ones."""
+    rng = np.random.default_rng(seed)
+    qsl = wl.query_start_loc.numpy()
+    H = wl.num_heads
+    toks = []
+    for s in range(wl.num_seqs):
+        a, e = int(qsl[s]), int(qsl[s + 1])
+        if e > a:
+            toks += [a, e - 1] + [a + j for j in (63, 64, 127, 128) if a + j < e]
+    T = int(qsl[-1])
+    toks += [int(x) for x in rng.integers(0, T, size=max(0, n - len(toks)))]
+    return np.array([(t, int(rng.integers(0, H))) for t in toks], dtype=np.int32)

@@ -150,3 +150,34 @@ def test_block_moves_host_checks():
     m2 = (ctypes.c_int64 * 2)(5, 1)
     assert lib.pa_swap_blocks(P, P, m2, 1, 4096, 4, 8, None) == 1       # src id 5 outside 4 blocks
     assert lib.pa_swap_blocks(P, P, m2, 0, 4096, 4, 8, None) == 0
+
+
+def _prefix_raw(**over):
+    """Call pa_prefix with fake (never dereferenced) pointers; returns the status."""
+    lib = pa.load()
+    P = 0x10000
+    a = dict(output=P, query=P, key=P, value=P, key_cache=P, value_cache=P, num_seqs=2, num_heads=8,
+             num_kv_heads=2, head_size=128, scale=0.088, block_tables=P, max_blocks_per_seq=64,
+             num_blocks=100, qsl=P, ctx=P, max_query_len=0, block_size=16, q_stride=1024,
+             kv_stride=256, dtype=0)
+    a.update(over)
+    return lib.pa_prefix(a["output"], a["query"], a["key"], a["value"], a["key_cache"], a["value_cache"],
+                         a["num_seqs"], a["num_heads"], a["num_kv_heads"], a["head_size"], a["scale"],
+                         a["block_tables"], a["max_blocks_per_seq"], a["num_blocks"], a["qsl"], a["ctx"],
+                         a["max_query_len"], a["block_size"], a["q_stride"], a["kv_stride"], a["dtype"], None)
+
+
+@pytest.mark.parametrize("over,status", [
+    (dict(num_seqs=-1), 1), (dict(num_heads=6, num_kv_heads=4), 1), (dict(scale=0.0), 1),
+    (dict(scale=float("nan")), 1), (dict(max_query_len=-1), 1), (dict(head_size=72), 2),
+    (dict(block_size=64), 2), (dict(dtype=2), 2), (dict(q_stride=1000), 1), (dict(kv_stride=260), 1),
+    (dict(max_blocks_per_seq=0), 1), (dict(max_query_len=5, output=0x10008), 1),
+    (dict(max_query_len=5, key=None), 1),
+])
+def test_prefix_rejects_invalid_arguments_on_host(over, status):
+    assert _prefix_raw(**over) == status
+
+
+def test_prefix_with_nothing_to_do_is_a_noop():
+    assert _prefix_raw(max_query_len=0) == 0
+    assert _prefix_raw(num_seqs=0, max_query_len=9) == 0

@@ -1,0 +1,132 @@
+"""GPU parity: pa_prefix (chunked-prefix attention, through the C ABI) against the fp64
+oracle on the same seeded inputs.  Reduced chunked-prefill workloads are compared element
+by element; the full-size ones (as the benchmark runs them) on sampled (token, head) rows
+that include every chunk's first and last token and the 64-key tile edges.  Edge cases:
+empty chunks and empty contexts, one-token chunks, contexts ending on and off tile and page
+boundaries, every supported head size and block size, GQA ratios 1..16, strided q/k/v rows,
+pages outside the cache (masked and flagged), contexts longer than the table (capped, as
+the pages do) and NaN canaries in every cache slot the method must not read."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_v2_gb300 as pa
+import workloads
+from gpu_harness import check_prefix, prefix_sample_rows, prefix_to_device, run_prefix
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _clear_device_errors():
+    pa.pa_get_device_errors(reset=True)
+    yield
+
+
+@pytest.mark.parametrize("name", list(workloads.PREFIX_CONFIGS))
+def test_reduced_prefix_workloads_match_oracle(name):
+    wl = workloads.make_prefix(name, reduced=True)
+    check_prefix(wl, run_prefix(wl), oracle.prefix_workload(wl), label=name)
+    assert pa.pa_get_device_errors() == 0
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["prefix_long_gqa", "prefix_llama_gqa"])
+def test_full_size_prefix_sampled(name):
+    wl = workloads.make_prefix(name)
+    out = run_prefix(wl)
+    rows = prefix_sample_rows(wl, n=40)
+    check_prefix(wl, out, oracle.prefix_workload(wl, rows=rows), rows=rows, label=name)
+    assert torch.isfinite(out.float()).all()
+    assert pa.pa_get_device_errors() == 0
+
+
+CTX = [0, 1, 63, 64, 65, 200, 511, 1000]
+QL = [1, 0, 64, 65, 129, 3, 200, 17]
+
+
+@pytest.mark.parametrize("d", [64, 80, 96, 112, 120, 128, 192, 256])
+@pytest.mark.parametrize("bs", [8, 16, 32])
+@pytest.mark.parametrize("q_dtype", ["f16", "bf16"])
+def test_head_block_sizes_and_dtypes(d, bs, q_dtype):
+    wl = workloads.build_prefix(num_seqs=len(CTX), num_heads=8, num_kv_heads=2, head_size=d,
+                                block_size=bs, context_lens=CTX, query_lens=QL, q_dtype=q_dtype,
+                                seed=500 + d + bs)
+    check_prefix(wl, run_prefix(wl), oracle.prefix_workload(wl), label=f"d{d} bs{bs} {q_dtype}")
+
+
+@pytest.mark.parametrize("G", [1, 2, 3, 5, 6, 7, 8, 16])
+def test_gqa_ratios(G):
+    wl = workloads.build_prefix(num_seqs=3, num_heads=2 * G, num_kv_heads=2, head_size=128, block_size=16,
+                                context_lens=[300, 0, 77], query_lens=[90, 150, 1], seed=600 + G)
+    check_prefix(wl, run_prefix(wl), oracle.prefix_workload(wl), label=f"G{G}")
+
+
+def test_strided_rows():
+    # q/k/v as views of wider rows (a fused qkv projection's output)
+    wl = workloads.build_prefix(num_seqs=2, num_heads=8, num_kv_heads=2, head_size=64, block_size=16,
+                                context_lens=[100, 33], query_lens=[70, 40], seed=700)
+    out = run_prefix(wl, q_rows=8 * 64 + 64, kv_rows=2 * (2 * 64 + 16))
+    check_prefix(wl, out, oracle.prefix_workload(wl), label="strided")
+
+
+def test_max_query_len_larger_than_needed():
+    wl = workloads.make_prefix("prefix_tiny")
+    check_prefix(wl, run_prefix(wl, max_query_len=wl.max_query_len + 300), oracle.prefix_workload(wl),
+                 label="wide grid")
+    assert pa.pa_get_device_errors() == 0
+
+
+def test_chunk_longer_than_max_query_len_is_skipped_and_flagged():
+    wl = workloads.make_prefix("prefix_tiny")  # chunks of 5, 70, 129 tokens
+    out = run_prefix(wl, max_query_len=100)
+    assert pa.pa_get_device_errors() & 128
+    qsl = wl.query_start_loc.tolist()
+    assert torch.isnan(out[qsl[2]:qsl[3]].float()).all()  # the 129-token chunk is untouched
+    ref = oracle.prefix_workload(wl)
+    check_prefix(wl, out[:qsl[2]], ref[:qsl[2]], label="other chunks")
+
+
+def test_out_of_range_page_is_masked_and_flagged():
+    wl = workloads.build_prefix(num_seqs=2, num_heads=4, num_kv_heads=2, head_size=64, block_size=16,
+                                context_lens=[100, 40], query_lens=[20, 9], seed=800)
+    bad = wl.block_tables.clone()
+    bad[0, 2] = wl.num_blocks + 5  # context tokens 32..47 of sequence 0
+    out = run_prefix(workloads.PrefixWorkload(**{**wl.__dict__, "block_tables": bad}))
+    assert pa.pa_get_device_errors() & 32
+    # attention has no positional term, so masking a page equals dropping its tokens
+    t = wl.block_tables
+    ref_tables = torch.stack([torch.cat([t[0, :2], t[0, 3:]]), t[1, :-1]]).to(torch.int32)
+    ref_wl = workloads.PrefixWorkload(**{**wl.__dict__, "block_tables": ref_tables,
+                                         "context_lens": torch.tensor([84, 40], dtype=torch.int32)})
+    check_prefix(wl, out, oracle.prefix_workload(ref_wl), label="masked page")
+
+
+def test_context_longer_than_table_is_capped_and_flagged():
+    wl = workloads.build_prefix(num_seqs=1, num_heads=4, num_kv_heads=1, head_size=64, block_size=16,
+                                context_lens=[64], query_lens=[10], table_width=5, seed=900)
+    # a context of 200 tokens is capped to the table's 5 blocks = 80 tokens; slots 64..79
+    # hold chunk canaries in this workload, so give that block real values first
+    kc = wl.key_cache.clone()
+    vc = wl.value_cache.clone()
+    b = int(wl.block_tables[0, 4])
+    g = torch.Generator().manual_seed(1)
+    kc[b] = torch.randn(kc[b].shape, generator=g).to(kc.dtype)
+    vc[b] = torch.randn(vc[b].shape, generator=g).to(vc.dtype)
+    capped = workloads.PrefixWorkload(**{**wl.__dict__, "key_cache": kc, "value_cache": vc,
+                                         "context_lens": torch.tensor([80], dtype=torch.int32)})
+    over = workloads.PrefixWorkload(**{**capped.__dict__, "context_lens": torch.tensor([200], dtype=torch.int32)})
+    out = run_prefix(over)
+    assert pa.pa_get_device_errors() & 64
+    check_prefix(wl, out, oracle.prefix_workload(capped), label="capped")
+
+
+def test_prefix_is_deterministic():
+    wl = workloads.make_prefix("prefix_llama_gqa", reduced=True)
+    dev = prefix_to_device(wl)
+    a = run_prefix(wl, dev)
+    b = run_prefix(wl, dev)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
