@@ -433,6 +433,115 @@ def run_copy_blocks(args):
     return 0
 
 
+def _tensor_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def run_prefix(args):
+    """Chunked-prefix attention ("paged_attn.py" forward_prefix) on one chunked-prefill step:
+    every new token attends to its sequence's cached context and causally to its chunk.
+    value = algorithmic TFLOP/s (4 d H per visible (query, key) pair) of the pa_prefix call;
+    roofline against the measured dense bf16 tensor throughput (fp16 runs at the same rate)."""
+    import numpy as np
+    import torch
+
+    import paged_kv_cache_v2_gb300 as pa
+    import workloads
+
+    name = args.workload if args.workload in workloads.PREFIX_CONFIGS else "prefix_long_gqa"
+    torch.cuda.set_device(0)
+    pa.load()
+    wl = workloads.make_prefix(name)
+    dev = {k: getattr(wl, k).cuda() for k in ("query", "key", "value", "key_cache", "value_cache",
+                                              "block_tables", "query_start_loc", "context_lens")}
+    out = torch.empty_like(dev["query"])
+    flops = wl.flops()
+
+    def call(q, k, v, o):
+        pa.pa_prefix(o, q, k, v, dev["key_cache"], dev["value_cache"], dev["block_tables"],
+                     dev["query_start_loc"], dev["context_lens"], wl.max_query_len, scale=wl.scale)
+
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
+    for _ in range(args.warmup):
+        call(dev["query"], dev["key"], dev["value"], out)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    launches = 0
+    with ClockSampler(0) as clocks:
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record()
+            call(dev["query"], dev["key"], dev["value"], out)
+            ev[i][1].record()
+            launches += 1
+        torch.cuda.synchronize()
+    times = sorted(a.elapsed_time(b) for a, b in ev)
+    ms = sum(times) / len(times)
+    tflops = flops / (ms * 1e-3) / 1e12
+    e2e = None
+    if not args.no_e2e:
+        hq, hk, hv = (getattr(wl, k).pin_memory() for k in ("query", "key", "value"))
+        ho = torch.empty(wl.query.shape, dtype=wl.query.dtype).pin_memory()
+        dq, dk, dv = (torch.empty_like(dev[k]) for k in ("query", "key", "value"))
+        for _ in range(2):
+            dq.copy_(hq, non_blocking=True); dk.copy_(hk, non_blocking=True); dv.copy_(hv, non_blocking=True)
+            call(dq, dk, dv, out)
+            ho.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(args.steps):
+            dq.copy_(hq, non_blocking=True); dk.copy_(hk, non_blocking=True); dv.copy_(hv, non_blocking=True)
+            call(dq, dk, dv, out)
+            ho.copy_(out, non_blocking=True)
+            launches += 1
+        b.record()
+        torch.cuda.synchronize()
+        e_ms = a.elapsed_time(b) / args.steps
+        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+        e2e = {"value": round(flops / (e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(e_ms, 4),
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": ho.numel() * ho.element_size()}
+    cpu = None
+    if not args.no_cpu_baseline:
+        import oracle
+        threads = len(os.sched_getaffinity(0))
+        qsl = wl.query_start_loc.numpy()
+        rng = np.random.default_rng(0)
+        done_flops, t_total, nrows = 0, 0.0, 0
+        while t_total < args.cpu_seconds:
+            tok = int(rng.integers(0, wl.num_tokens))
+            s = int(np.searchsorted(qsl, tok, side="right") - 1)
+            rows = np.array([(tok, h) for h in range(wl.num_heads)], dtype=np.int32)
+            t0 = time.perf_counter()
+            oracle.prefix_workload(wl, rows=rows, threads=threads)
+            t_total += time.perf_counter() - t0
+            keys = int(wl.context_lens[s]) + tok - int(qsl[s]) + 1
+            done_flops += 4 * wl.head_size * wl.num_heads * keys
+            nrows += wl.num_heads
+        cpu = {"value": round(done_flops / t_total / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+               "sample": f"fp64 oracle on {nrows} (token, head) rows: all heads of random new tokens of the "
+                         f"workload, {t_total:.1f} s"}
+    peak, kind = _tensor_peak()
+    print(json.dumps({
+        "metric": "chunked-prefix attention TFLOP/s (4 d H per visible query-key pair), 1 GPU",
+        "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": wl.q_dtype, "data": "synthetic",
+        "config": {"workload": name, "num_seqs": wl.num_seqs, "heads": [wl.num_heads, wl.num_kv_heads],
+                   "head_size": wl.head_size, "block_size": wl.block_size,
+                   "context_lens": wl.context_lens.tolist(), "query_lens": wl.query_lens.tolist(),
+                   "flops_per_step": flops, "l2": "flushed (256 MiB write) before every timed call"},
+        "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(tflops / peak, 4), "traffic": None, "kernel": "pa_prefix_kernel",
+                     "peak_source": f"{kind} bf16_tflops (burst; fp16 has the same dense rate)"},
+        "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": launches, "clocks": clocks.summary()}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -443,8 +552,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--op", choices=["decode", "copy_blocks"], default="decode",
-                    help="decode: the decode step (default); copy_blocks: the block-copy kernel alone")
+    ap.add_argument("--op", choices=["decode", "copy_blocks", "prefix"], default="decode",
+                    help="decode: the decode step (default); copy_blocks: the block-copy kernel alone; "
+                         "prefix: chunked-prefix attention (--workload prefix_long_gqa|prefix_llama_gqa)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -452,6 +562,8 @@ def main():
         return run_reference(args)
     if args.op == "copy_blocks":
         return run_copy_blocks(args)
+    if args.op == "prefix":
+        return run_prefix(args)
     return run_ours(args)
 
 

@@ -4,6 +4,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -76,13 +77,19 @@ template <int BS>
 cudaError_t phase1_read_errors(unsigned int* v, bool reset);
 
 // ---- chunked-prefix attention ----------------------------------------------------------
-constexpr int kPfxWarps = 8;
-constexpr int kPfxThreads = kPfxWarps * 32;
-constexpr int kPfxBM = kPfxWarps * 16;  // query rows per CTA
-constexpr int kPfxBN = 64;              // keys per tile
-constexpr int kPfxStages = 2;
+// Warp roles of the prefix kernel: warps 0-3 run the softmax (warp w owns tensor-memory lanes
+// 32w..32w+31, i.e. query rows 32w..32w+31), warp 4 allocates tensor memory and one of its
+// lanes issues the MMAs, warps 5-8 copy query, key and value tiles into shared memory.
+constexpr int kPfxMmaWarp = 4;
+constexpr int kPfxLoaderWarp0 = 5;
+constexpr int kPfxLoaderThreads = 4 * 32;
+constexpr int kPfxThreads = 9 * 32;
+constexpr int kPfxBM = 128;    // query rows per CTA (the MMA M)
+constexpr int kPfxStages = 2;  // key/value tile stages
 
 struct PrefixParams {
+    CUtensorMap kmap;  // key cache as {8 elems, block_size, d/8, blocks * kv heads}
+    CUtensorMap vmap;  // value cache as {8 keys, block_size/8, d, blocks * kv heads}
     void* out;
     const uint8_t* q;  // [T][q_stride] rows, head h at h * d
     const uint8_t* k;  // [T][kv_stride] rows, kv head at kvh * d

@@ -1,9 +1,13 @@
 // pa_prefix.cu -- host entry point of chunked-prefix attention ("paged_attn.py",
 // forward_prefix): argument checks, grid sizing, kernel selection.  The kernels live in
 // pa_prefix.cuh (instantiated per dtype in pa_prefix_f16.cu / pa_prefix_bf16.cu).
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <math.h>
 #include <stdint.h>
+
+#include <mutex>
 
 #include "pa_internal.h"
 #include "pa_kernels.cuh"
@@ -12,6 +16,48 @@
 using namespace pa;
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link against libcuda).
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// Tensor maps of the paged caches for the prefix kernel's tile copies:
+//   keys   {8 elements, block_size slots, d/8 chunks, blocks * kv heads}, box {8, 8, d/8, 1}:
+//          8 tokens of one page land as [d/8][8 tokens][16 bytes];
+//   values {8 keys, block_size/8, d rows, blocks * kv heads}, box {8, 1, d, 1}:
+//          8 keys of one page land as [d][16 bytes].
+static bool encode_cache_maps(PrefixParams& p, const void* key_cache, const void* value_cache, int num_blocks,
+                              int num_kv_heads, int head_size, int block_size) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (enc == nullptr) return false;
+    const cuuint64_t pages = (cuuint64_t)num_blocks * num_kv_heads;
+    const cuuint64_t d = head_size, bs = block_size;
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    const cuuint64_t kdim[4] = {8, bs, d / 8, pages};
+    const cuuint64_t kstride[3] = {16, bs * 16, d * bs * 2};
+    const cuuint32_t kbox[4] = {8, 8, (cuuint32_t)(d / 8), 1};
+    if (enc(&p.kmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(key_cache), kdim, kstride, kbox, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    const cuuint64_t vdim[4] = {8, bs / 8, d, pages};
+    const cuuint64_t vstride[3] = {16, bs * 2, d * bs * 2};
+    const cuuint32_t vbox[4] = {8, 1, (cuuint32_t)d, 1};
+    return enc(&p.vmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(value_cache), vdim, vstride, vbox, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 extern "C" pa_status pa_prefix(void* output, const void* query, const void* key, const void* value,
                                const void* key_cache, const void* value_cache, int num_seqs, int num_heads,
@@ -44,6 +90,8 @@ extern "C" pa_status pa_prefix(void* output, const void* query, const void* key,
         return PA_ERR_INVALID_ARG;
 
     PrefixParams p;
+    if (!encode_cache_maps(p, key_cache, value_cache, num_blocks, num_kv_heads, head_size, block_size))
+        return PA_ERR_CUDA;
     p.out = output;
     p.q = static_cast<const uint8_t*>(query);
     p.k = static_cast<const uint8_t*>(key);

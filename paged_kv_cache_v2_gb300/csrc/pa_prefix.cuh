@@ -1,5 +1,6 @@
-// pa_prefix.cuh -- chunked-prefix (prefill) attention over the paged cache for sm_103a.
-// "paged_attn.py", forward_prefix / _forward_prefix_pytorch.
+// pa_prefix.cuh -- chunked-prefix (prefill) attention over the paged cache on the sm_103a
+// tensor cores (tcgen05, accumulators in tensor memory).  "paged_attn.py", forward_prefix /
+// _forward_prefix_pytorch.
 //
 // Sequence s has ctx = context_lens[s] tokens in the paged cache and q_len new tokens whose
 // query/key/value rows are dense (rows query_start_loc[s] .. query_start_loc[s+1]-1).  New
@@ -7,18 +8,26 @@
 // through kv head h / G:  out = softmax(scale * q K^T) V.
 //
 // One CTA owns (sequence, kv head, 128 query rows), a row being a (new token j, head g of
-// the kv head's group) pair numbered j * G + g, so every key/value tile is read once per
-// kv head and shared by the whole GQA group.  Eight warps hold 16 rows each; the scores of
-// a 64-key tile are an m16n8k16 product with the query rows in shared memory and the keys
-// straight from the copied pages (a key page [d/8][block_size][8] already has the 16-byte
-// rows ldmatrix wants); the probabilities stay in registers as the A operand of the value
-// product (fp32 accumulators, online softmax with exp2).  Tiles move global -> shared with
-// 16-byte cp.async in a two-stage pipeline: context tiles page by page from the cache,
-// chunk tiles from the dense rows.  Value tiles are [d][64 tokens] for context pages (rows
-// of a value page) and [64 tokens][d] for dense rows (read with ldmatrix.trans).  Row
-// strides carry 16 bytes of padding so the eight rows of every ldmatrix fall in distinct
-// bank groups.  Masked keys never reach the value product as NaN: value chunks past the
-// context or of an invalid page are zero-filled by the copy itself.
+// the kv head's group) pair numbered j * G + g: every key/value tile is read once per kv head
+// and shared by the whole GQA group, and the 128 rows are the M of every MMA.  Per tile of
+// BN keys (128, or 64 above head size 128):
+//   loader warps   copy the key tile and the value tile into shared memory in the canonical
+//                  no-swizzle K-major layouts (8-row x 16-byte core matrices): keys as
+//                  [key/8][d/8][8 keys][8], values as [key/8][d][8 keys].  A tile of full,
+//                  valid pages moves by tensor copies (TMA), one per 8 keys of each cache,
+//                  issued by one thread; a tile with the context's end, a page outside the
+//                  cache or the chunk's dense rows moves by 16-byte cp.async (zero-filling
+//                  what must not count; the dense value rows are transposed on the way).
+//   MMA lane       S = Q K^T (M 128, N BN) into one of two S buffers in tensor memory, then,
+//                  once the softmax has written P, O += P V (N = head size) into the O buffer.
+//   softmax warps  one thread per row: read the row of S from tensor memory, mask, exp2 with
+//                  a running reference max that only moves when the row max grows by more
+//                  than 2^8 (then O and the row sum are rescaled), write P (bf16 as hi + lo
+//                  so probabilities keep ~16 bits) to shared memory in the A layout.
+// S of tile t+1 runs on the tensor cores while the softmax works on tile t.  All waits are
+// bounded (about two seconds); a wait that gives up sets an abort flag every role checks and
+// bit 8 of the device error word, and the CTA still drains its MMAs and frees its tensor
+// memory before it exits.
 #pragma once
 
 #include "pa_kernels.cuh"
@@ -26,29 +35,71 @@
 
 namespace pa {
 
-template <int D>
-struct PfxGeom {
-    static constexpr int DP = (D + 15) / 16 * 16;  // head size padded to the MMA k step
+template <bool BF16, int D>
+struct PfxCfg {
+    static constexpr int DP = (D + 15) / 16 * 16;  // head size padded to the MMA K step
     static constexpr int NCR = D / 8;              // 16-byte chunks of a row that exist
     static constexpr int NCP = DP / 8;             // chunks after padding
-    static constexpr int RS = DP * 2 + 16;         // query / dense-value row stride, bytes
-    static constexpr int VRS = kPfxBN * 2 + 16;    // paged-value row stride (one d row), bytes
-    static constexpr int Q_BYTES = kPfxBM * RS;
-    static constexpr int K_BYTES = NCP * kPfxBN * 16;
-    static constexpr int V_BYTES = (DP * VRS > kPfxBN * RS) ? DP * VRS : kPfxBN * RS;
+    static constexpr int BN = DP <= 128 ? 128 : 64;
+    static constexpr int NP = BF16 ? 2 : 1;  // P buffers: hi (and lo for bf16)
+    static constexpr int Q_BYTES = kPfxBM * DP * 2;
+    static constexpr int K_BYTES = BN * DP * 2;
+    static constexpr int V_BYTES = BN * DP * 2;
     static constexpr int STAGE = K_BYTES + V_BYTES;
-    static constexpr int SMEM = Q_BYTES + kPfxStages * STAGE + 16 * kPfxStages;
-    static constexpr int MIN_CTAS = DP <= 128 ? 2 : 1;
+    static constexpr int P_BYTES = kPfxBM * BN * 2;
+    static constexpr int OFF_STAGE = Q_BYTES;
+    static constexpr int OFF_P = OFF_STAGE + kPfxStages * STAGE;
+    static constexpr int OFF_CTL = OFF_P + NP * P_BYTES;
+    static constexpr int CTL_BYTES = 512;
+    // at least 120 KiB so two CTAs never share an SM (each takes all 512 tensor-memory columns)
+    static constexpr int SMEM = OFF_CTL + CTL_BYTES > 120 * 1024 ? OFF_CTL + CTL_BYTES : 120 * 1024;
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t COL_S = 0;       // two S buffers: columns [0, BN) and [BN, 2 BN)
+    static constexpr uint32_t COL_O = 2 * BN;  // O: columns [2 BN, 2 BN + DP)
+    static constexpr uint32_t IDESC_S = umma_idesc_f16(BF16, kPfxBM, BN);
+    static constexpr uint32_t IDESC_O = umma_idesc_f16(BF16, kPfxBM, DP);
+    // O is read and rescaled in 32-column pieces, so the last piece may run past DP
+    static_assert(2 * BN + (DP + 31) / 32 * 32 <= (int)TMEM_COLS, "tensor memory");
+    static_assert(SMEM <= 227 * 1024, "shared memory");
 };
+
+#ifndef PA_PFX_WAIT_HINT_NS
+#define PA_PFX_WAIT_HINT_NS 20000
+#endif
 
 static __device__ unsigned int g_prefix_errors = 0;
 
 __device__ __forceinline__ void prefix_flag(unsigned int bit) { atomicOr(&g_prefix_errors, bit); }
 
+// Bounded wait on an mbarrier phase; gives up when another role has aborted or after the
+// wait limit (then it raises the abort flag itself).
+__device__ __forceinline__ bool pfx_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait_hint(bar, parity, PA_PFX_WAIT_HINT_NS)) {
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            prefix_flag(256u);
+            return false;
+        }
+    }
+    return true;
+}
+
+// One lane waits, the warp learns the outcome (warp-uniform, as tcgen05.ld/st require).
+__device__ __forceinline__ bool pfx_warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int lane) {
+    int ok = 1;
+    if (lane == 0) ok = pfx_wait(bar, parity, abort_flag);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    return ok != 0;
+}
+
 template <bool BF16, int D>
-__global__ void __launch_bounds__(kPfxThreads, PfxGeom<D>::MIN_CTAS) pa_prefix_kernel(const PrefixParams p) {
-    using Gm = PfxGeom<D>;
-    extern __shared__ __align__(128) uint8_t smem[];
+__global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_constant__ PrefixParams p) {
+    using C = PfxCfg<BF16, D>;
+    constexpr int BN = C::BN;
+    extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int s = blockIdx.z, kvh = blockIdx.y;
     const int row0 = (gridDim.x - 1 - blockIdx.x) * kPfxBM;  // row tiles with more keys first
@@ -67,291 +118,380 @@ __global__ void __launch_bounds__(kPfxThreads, PfxGeom<D>::MIN_CTAS) pa_prefix_k
         ctx = p.mbps * p.bs;
     }
 
-    const uint32_t sQ = smem_addr(smem);
-    const uint32_t sStage0 = sQ + Gm::Q_BYTES;
-    uint32_t* sflags = reinterpret_cast<uint32_t*>(smem + Gm::Q_BYTES + kPfxStages * Gm::STAGE);
+    const uint32_t sbase = smem_addr(smem);
+    const uint32_t sQ = sbase;
+    uint8_t* ctl = smem + C::OFF_CTL;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(ctl);
+    uint64_t* q_full = bars + 0;
+    uint64_t* kv_full = bars + 1;   // [2]
+    uint64_t* kv_empty = bars + 3;  // [2]
+    uint64_t* s_full = bars + 5;    // [2]
+    uint64_t* s_empty = bars + 7;   // [2]
+    uint64_t* p_full = bars + 9;
+    uint64_t* o_done = bars + 10;
+    uint64_t* fin = bars + 11;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctl + 96);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(ctl + 100);
+    uint32_t* bad_mask = reinterpret_cast<uint32_t*>(ctl + 104);  // [2] pages outside the cache
 
-    // Padding chunks of the key tiles are never copied: zero them once so that the zero
-    // query padding meets zeros, not stale bits.
-    if constexpr (Gm::NCP > Gm::NCR) {
-        constexpr int per = (Gm::NCP - Gm::NCR) * kPfxBN;
-        for (int idx = tid; idx < kPfxStages * per; idx += kPfxThreads) {
-            const int st = idx / per, rem = idx % per;
-            const int c = Gm::NCR + rem / kPfxBN, o = rem % kPfxBN;
-            *reinterpret_cast<uint4*>(smem + Gm::Q_BYTES + st * Gm::STAGE + c * (kPfxBN * 16) + o * 16) =
-                make_uint4(0u, 0u, 0u, 0u);
-        }
-    }
-
-    // Query rows of this tile (rows past the chunk and padding chunks read as zero).
-    for (int idx = tid; idx < kPfxBM * Gm::NCP; idx += kPfxThreads) {
-        const int r = idx / Gm::NCP, c = idx % Gm::NCP;
-        const int row = row0 + r;
-        const uint8_t* src = p.q;
-        uint32_t nb = 0;
-        if (row < rows_total && c < Gm::NCR) {
-            const int j = row / G, g = row - (row / G) * G;
-            src = p.q + ((int64_t)(q0 + j) * p.q_stride + (int64_t)(kvh * G + g) * D + c * 8) * 2;
-            nb = 16;
-        }
-        cp_async16(sQ + r * Gm::RS + c * 16, src, nb);
-    }
-
-    const int n_ctx = (ctx + kPfxBN - 1) / kPfxBN;
+    const int n_ctx = (ctx + BN - 1) / BN;
     const int row_last = min(row0 + kPfxBM, rows_total) - 1;
-    const int jmin = row0 / G;
-    const int n_chunk = (row_last / G) / kPfxBN + 1;
-    const int n_tiles = n_ctx + n_chunk;
+    const int n_tiles = n_ctx + (row_last / G) / BN + 1;
+
+    if (tid == 0) {
+        mbar_init(q_full, 4);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&kv_full[i], 4);
+            mbar_init(&kv_empty[i], 1);
+            mbar_init(&s_full[i], 1);
+            mbar_init(&s_empty[i], 4);
+        }
+        mbar_init(p_full, 4);
+        mbar_init(o_done, 1);
+        mbar_init(fin, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    // Padding the copies never write: key chunks c >= D/8 and value rows d >= D, both stages.
+    if constexpr (C::NCP > C::NCR) {
+        constexpr int kpad = (C::NCP - C::NCR) * BN, vpad = (BN / 8) * (C::DP - D);
+        for (int i = tid; i < kPfxStages * (kpad + vpad); i += kPfxThreads) {
+            const int st = i / (kpad + vpad), rem = i % (kpad + vpad);
+            uint8_t* stage = smem + C::OFF_STAGE + st * C::STAGE;
+            const int o = rem % BN, c = C::NCR + rem / BN;
+            uint8_t* dst = rem < kpad ? stage + (o >> 3) * (C::DP * 16) + c * 128 + (o & 7) * 16
+                                      : stage + C::K_BYTES + ((rem - kpad) / (C::DP - D)) * (C::DP * 16) +
+                                            (D + (rem - kpad) % (C::DP - D)) * 16;
+            *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+    fence_proxy_async_smem();
+    if (warp == kPfxMmaWarp) tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tm = *tmem_slot;
     const int32_t* table = p.block_tables + (int64_t)s * p.mbps;
     const int64_t page_bytes = (int64_t)D * p.bs * 2;
 
-    auto load_tile = [&](int t, int st) {
-        const uint32_t sK = sStage0 + st * Gm::STAGE, sV = sK + Gm::K_BYTES;
-        if (t < n_ctx) {
-            const int t0 = t * kPfxBN;
-            // keys: this thread's token o = tid % 64 is the same for all of its chunks
-            {
-                const int o = tid % kPfxBN;
-                const bool live = t0 + o < ctx;
-                const int b = live ? table[(t0 + o) >> p.bs_log2] : -1;
-                const bool ok = live && (unsigned)b < (unsigned)p.num_blocks;
-                const uint8_t* kp = ok ? p.kcache + ((int64_t)b * p.Hk + kvh) * page_bytes : p.kcache;
-                const int slot = (o & (p.bs - 1)) * 16;
-#pragma unroll
-                for (int c = tid / kPfxBN; c < Gm::NCR; c += kPfxThreads / kPfxBN)
-                    cp_async16(sK + c * (kPfxBN * 16) + o * 16, kp + (int64_t)c * p.bs * 16 + slot, ok ? 16u : 0u);
+    if (warp >= kPfxLoaderWarp0) {
+        // ------------------------------------------------------------------ loaders
+        const int lt = tid - kPfxLoaderWarp0 * 32;
+        for (int i = lt; i < kPfxBM * C::NCP; i += kPfxLoaderThreads) {
+            const int c = i / kPfxBM, r = i % kPfxBM;
+            const int row = row0 + r;
+            const uint8_t* src = p.q;
+            uint32_t nb = 0;
+            if (row < rows_total && c < C::NCR) {
+                const int j = row / G, g = row - j * G;
+                src = p.q + ((int64_t)(q0 + j) * p.q_stride + (int64_t)(kvh * G + g) * D + c * 8) * 2;
+                nb = 16;
             }
-            // values: this thread's 8-token chunk kc = tid % 8 (inside one page)
-            {
-                const int kc = tid % 8, o = kc * 8;
-                const int nv = min(max(ctx - t0 - o, 0), 8);
-                const int b = nv > 0 ? table[(t0 + o) >> p.bs_log2] : -1;
-                const bool ok = nv > 0 && (unsigned)b < (unsigned)p.num_blocks;
-                const uint8_t* vp = ok ? p.vcache + ((int64_t)b * p.Hk + kvh) * page_bytes : p.vcache;
-                const int slot = (o & (p.bs - 1)) * 2;
-                for (int dd = tid / 8; dd < D; dd += kPfxThreads / 8)
-                    cp_async16(sV + dd * Gm::VRS + kc * 16, vp + (int64_t)dd * p.bs * 2 + slot,
-                               ok ? (uint32_t)nv * 2u : 0u);
-            }
-            // pages of this tile whose id is outside the cache: masked, and reported
-            if (warp == 0) {
-                const int npg = kPfxBN >> p.bs_log2;
+            cp_async16(sQ + c * (kPfxBM * 16) + r * 16, src, nb);
+        }
+        cp_async_commit();
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(q_full);
+
+        for (int t = 0; t < n_tiles; ++t) {
+            const int st = t & 1;
+            if (t >= 2 && !pfx_warp_wait(&kv_empty[st], ((t >> 1) - 1) & 1, abort_flag, lane)) break;
+            const uint32_t sK = sbase + C::OFF_STAGE + st * C::STAGE, sV = sK + C::K_BYTES;
+            if (t < n_ctx) {
+                const int t0 = t * BN;
+                const int32_t* tile_table = table + (t0 >> p.bs_log2);
+                // pages of the tile whose id is outside the cache (masked); every loader warp
+                // computes the same mask, so all of them take the same path below
                 bool bad = false;
-                if (lane < npg) {
-                    const int first = t0 + (lane << p.bs_log2);
-                    if (first < ctx) {
-                        const int b = table[first >> p.bs_log2];
-                        bad = (unsigned)b >= (unsigned)p.num_blocks;
-                    }
-                }
+                if (lane < (BN >> p.bs_log2) && t0 + (lane << p.bs_log2) < ctx)
+                    bad = (unsigned)tile_table[lane] >= (unsigned)p.num_blocks;
                 const uint32_t m = __ballot_sync(0xffffffffu, bad);
-                if (lane == 0) {
-                    sflags[st * 4] = m;
+                if (lt == 0) {
+                    bad_mask[st] = m;
                     if (m) prefix_flag(32u);
                 }
-            }
-        } else {
-            const int kc0 = (t - n_ctx) * kPfxBN;
-            {
-                const int o = tid % kPfxBN;
-                const int j = kc0 + o;
-                const bool ok = j < q_len;
-                const uint8_t* kr = ok ? p.k + ((int64_t)(q0 + j) * p.kv_stride + (int64_t)kvh * D) * 2 : p.k;
-#pragma unroll
-                for (int c = tid / kPfxBN; c < Gm::NCR; c += kPfxThreads / kPfxBN)
-                    cp_async16(sK + c * (kPfxBN * 16) + o * 16, kr + c * 16, ok ? 16u : 0u);
-            }
-            for (int idx = tid; idx < kPfxBN * Gm::NCR; idx += kPfxThreads) {
-                const int o = idx / Gm::NCR, c = idx % Gm::NCR;
-                const int j = kc0 + o;
-                const bool ok = j < q_len;
-                const uint8_t* vr = ok ? p.v + ((int64_t)(q0 + j) * p.kv_stride + (int64_t)kvh * D) * 2 + c * 16 : p.v;
-                cp_async16(sV + o * Gm::RS + c * 16, vr, ok ? 16u : 0u);
-            }
-        }
-    };
-
-    // Per-thread rows: r_a and r_a + 8 of the CTA's 128; their causal limits in the chunk.
-    const int r_a = warp * 16 + (lane >> 2);
-    int lim[2];
-#pragma unroll
-    for (int i = 0; i < 2; ++i) lim[i] = (row0 + r_a + 8 * i) / G;
-
-    float acc[Gm::DP / 8][4];
-#pragma unroll
-    for (int n = 0; n < Gm::DP / 8; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
-    float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
-
-    load_tile(0, 0);
-    cp_async_commit();
-
-    for (int t = 0; t < n_tiles; ++t) {
-        const int st = t & 1;
-        if (t + 1 < n_tiles) load_tile(t + 1, st ^ 1);
-        cp_async_commit();
-        cp_async_wait<1>();
-        __syncthreads();
-
-        const uint32_t sK = sStage0 + st * Gm::STAGE, sV = sK + Gm::K_BYTES;
-        const bool is_ctx = t < n_ctx;
-
-        // S = Q K^T for this warp's 16 rows and the tile's 64 keys
-        float sc[8][4];
-#pragma unroll
-        for (int n = 0; n < 8; ++n) sc[n][0] = sc[n][1] = sc[n][2] = sc[n][3] = 0.f;
-#pragma unroll
-        for (int ks = 0; ks < Gm::DP / 16; ++ks) {
-            uint32_t a0, a1, a2, a3;
-            ldsm_x4(sQ + (warp * 16 + (lane & 15)) * Gm::RS + (2 * ks + (lane >> 4)) * 16, a0, a1, a2, a3);
-#pragma unroll
-            for (int np = 0; np < 4; ++np) {
-                uint32_t b0, b1, b2, b3;
-                const int tok = np * 16 + ((lane >> 4) << 3) + (lane & 7);
-                const int ch = 2 * ks + ((lane >> 3) & 1);
-                ldsm_x4(sK + ch * (kPfxBN * 16) + tok * 16, b0, b1, b2, b3);
-                mma16816<BF16>(sc[2 * np], a0, a1, a2, a3, b0, b1);
-                mma16816<BF16>(sc[2 * np + 1], a0, a1, a2, a3, b2, b3);
-            }
-        }
-
-        // scale into the exp2 domain, then mask
-#pragma unroll
-        for (int n = 0; n < 8; ++n)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) sc[n][e] *= p.sl2;
-        if (is_ctx) {
-            const int valid = min(kPfxBN, ctx - t * kPfxBN);
-            const uint32_t bad = sflags[st * 4];
-            if (valid < kPfxBN || bad) {
-#pragma unroll
-                for (int n = 0; n < 8; ++n)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int col = n * 8 + (lane & 3) * 2 + (e & 1);
-                        if (col >= valid || ((bad >> (col >> p.bs_log2)) & 1u)) sc[n][e] = -INFINITY;
+                if (m == 0 && t0 + BN <= ctx) {
+                    // a full tile of valid pages: tensor copies straight into the MMA layouts,
+                    // one thread issues them; the other loader warps only arrive
+                    if (lt == 0) {
+                        mbar_arrive_expect_tx(&kv_full[st], 4u * BN * D);
+#pragma unroll 1
+                        for (int i = 0; i < BN / 8; ++i) {
+                            const int o0 = 8 * i;
+                            const int page = tile_table[o0 >> p.bs_log2] * p.Hk + kvh;
+                            const int slot0 = o0 & (p.bs - 1);
+                            tma_load_4d(sK + i * (C::DP * 16), &p.kmap, 0, slot0, 0, page, &kv_full[st]);
+                            tma_load_4d(sV + i * (C::DP * 16), &p.vmap, 0, slot0 >> 3, 0, page, &kv_full[st]);
+                        }
+                    } else if (lane == 0 && lt >= 32) {
+                        mbar_arrive(&kv_full[st]);
                     }
-            }
-        } else {
-            const int kc0 = (t - n_ctx) * kPfxBN;
-            if (kc0 + kPfxBN - 1 > jmin) {
-#pragma unroll
-                for (int n = 0; n < 8; ++n)
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int key = kc0 + n * 8 + (lane & 3) * 2 + (e & 1);
-                        if (key > lim[e >> 1]) sc[n][e] = -INFINITY;
-                    }
-            }
-        }
-
-        // online softmax (row max over the quad that shares a row)
-        float corr[2];
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            float mx = -INFINITY;
-#pragma unroll
-            for (int n = 0; n < 8; ++n) mx = fmaxf(mx, fmaxf(sc[n][2 * i], sc[n][2 * i + 1]));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            const float mn = fmaxf(m_r[i], mx);
-            const float mu = mn == -INFINITY ? 0.f : mn;
-            corr[i] = ex2(m_r[i] - mu);
-            m_r[i] = mn;
-            float sum = 0.f;
-#pragma unroll
-            for (int n = 0; n < 8; ++n) {
-                sc[n][2 * i] = ex2(sc[n][2 * i] - mu);
-                sc[n][2 * i + 1] = ex2(sc[n][2 * i + 1] - mu);
-                sum += sc[n][2 * i] + sc[n][2 * i + 1];
-            }
-            l_r[i] = l_r[i] * corr[i] + sum;
-        }
-#pragma unroll
-        for (int n = 0; n < Gm::DP / 8; ++n) {
-            acc[n][0] *= corr[0];
-            acc[n][1] *= corr[0];
-            acc[n][2] *= corr[1];
-            acc[n][3] *= corr[1];
-        }
-
-        // O += P V; bf16 probabilities go in as hi + lo so they carry f16-like precision
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) {
-            uint32_t pa[4], pl[4];
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    const float x0 = sc[2 * kk + h][2 * i], x1 = sc[2 * kk + h][2 * i + 1];
-                    pa[2 * h + i] = pack2<BF16>(x0, x1);
-                    if constexpr (BF16) {
-                        const float h0 = __uint_as_float(pa[2 * h + i] << 16);
-                        const float h1 = __uint_as_float(pa[2 * h + i] & 0xffff0000u);
-                        pl[2 * h + i] = pack2<BF16>(x0 - h0, x1 - h1);
-                    }
+                    continue;
                 }
-            if (is_ctx) {
-#pragma unroll
-                for (int np = 0; np < Gm::DP / 16; ++np) {
-                    uint32_t b0, b1, b2, b3;
-                    const int dd = np * 16 + ((lane >> 4) << 3) + (lane & 7);
-                    const int ch = 2 * kk + ((lane >> 3) & 1);
-                    ldsm_x4(sV + dd * Gm::VRS + ch * 16, b0, b1, b2, b3);
-                    mma16816<BF16>(acc[2 * np], pa[0], pa[1], pa[2], pa[3], b0, b1);
-                    mma16816<BF16>(acc[2 * np + 1], pa[0], pa[1], pa[2], pa[3], b2, b3);
-                    if constexpr (BF16) {
-                        mma16816<BF16>(acc[2 * np], pl[0], pl[1], pl[2], pl[3], b0, b1);
-                        mma16816<BF16>(acc[2 * np + 1], pl[0], pl[1], pl[2], pl[3], b2, b3);
-                    }
+                // keys: page-local order, so global reads and shared writes are both contiguous
+                const int kper = C::NCR << p.bs_log2;
+                for (int i = lt; i < BN * C::NCR; i += kPfxLoaderThreads) {
+                    const int pg = i / kper, rem = i - pg * kper;
+                    const int c = rem >> p.bs_log2, slot = rem & (p.bs - 1);
+                    const int o = (pg << p.bs_log2) + slot;
+                    const int b = t0 + o < ctx ? tile_table[pg] : -1;
+                    const bool ok = (unsigned)b < (unsigned)p.num_blocks;
+                    const uint8_t* src =
+                        ok ? p.kcache + ((int64_t)b * p.Hk + kvh) * page_bytes + (int64_t)(c * p.bs + slot) * 16 : p.kcache;
+                    cp_async16(sK + (o >> 3) * (C::DP * 16) + c * 128 + (o & 7) * 16, src, ok ? 16u : 0u);
+                }
+                // values: 8-token pieces of each page row; the part past the context reads as zero
+                const int kpp_log2 = p.bs_log2 - 3;
+                const int vper = D << kpp_log2;
+                for (int i = lt; i < (BN / 8) * D; i += kPfxLoaderThreads) {
+                    const int pg = i / vper, rem = i - pg * vper;
+                    const int dd = rem >> kpp_log2, kq = rem & ((1 << kpp_log2) - 1);
+                    const int o = (pg << p.bs_log2) + kq * 8;
+                    const int nv = min(max(ctx - t0 - o, 0), 8);
+                    const int b = nv > 0 ? tile_table[pg] : -1;
+                    const bool ok = (unsigned)b < (unsigned)p.num_blocks;
+                    const uint8_t* src = ok ? p.vcache + ((int64_t)b * p.Hk + kvh) * page_bytes +
+                                                  ((int64_t)dd * p.bs + kq * 8) * 2
+                                            : p.vcache;
+                    cp_async16(sV + (o >> 3) * (C::DP * 16) + dd * 16, src, ok ? (uint32_t)nv * 2u : 0u);
                 }
             } else {
+                const int kc0 = (t - n_ctx) * BN;
+                for (int i = lt; i < BN * C::NCR; i += kPfxLoaderThreads) {
+                    const int c = i / BN, o = i % BN;
+                    const int j = kc0 + o;
+                    const bool ok = j < q_len;
+                    const uint8_t* src =
+                        ok ? p.k + ((int64_t)(q0 + j) * p.kv_stride + (int64_t)kvh * D + c * 8) * 2 : p.k;
+                    cp_async16(sK + (o >> 3) * (C::DP * 16) + c * 128 + (o & 7) * 16, src, ok ? 16u : 0u);
+                }
+                // dense value rows, two tokens at a time, transposed into [key/8][d][8 keys]
+                for (int i = lt; i < (BN / 2) * C::NCR; i += kPfxLoaderThreads) {
+                    const int c = i % C::NCR, t2 = 2 * (i / C::NCR);
+                    const int j = kc0 + t2;
+                    const uint8_t* base = p.v + ((int64_t)kvh * D + c * 8) * 2;
+                    uint4 a = make_uint4(0u, 0u, 0u, 0u), b = make_uint4(0u, 0u, 0u, 0u);
+                    if (j < q_len) a = ld_nc_v4(base + (int64_t)(q0 + j) * p.kv_stride * 2);
+                    if (j + 1 < q_len) b = ld_nc_v4(base + (int64_t)(q0 + j + 1) * p.kv_stride * 2);
+                    const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+                    const uint32_t dst = sV + (t2 >> 3) * (C::DP * 16) + c * 8 * 16 + (t2 & 7) * 2;
 #pragma unroll
-                for (int np = 0; np < Gm::DP / 16; ++np) {
-                    uint32_t b0, b1, b2, b3;
-                    const int tok = kk * 16 + (((lane >> 3) & 1) << 3) + (lane & 7);
-                    const int ch = 2 * np + (lane >> 4);
-                    ldsm_x4_trans(sV + tok * Gm::RS + ch * 16, b0, b1, b2, b3);
-                    mma16816<BF16>(acc[2 * np], pa[0], pa[1], pa[2], pa[3], b0, b1);
-                    mma16816<BF16>(acc[2 * np + 1], pa[0], pa[1], pa[2], pa[3], b2, b3);
-                    if constexpr (BF16) {
-                        mma16816<BF16>(acc[2 * np], pl[0], pl[1], pl[2], pl[3], b0, b1);
-                        mma16816<BF16>(acc[2 * np + 1], pl[0], pl[1], pl[2], pl[3], b2, b3);
+                    for (int e = 0; e < 8; ++e)
+                        sts_u32(dst + e * 16, __byte_perm(av[e >> 1], bv[e >> 1], (e & 1) ? 0x7632 : 0x5410));
+                }
+            }
+            cp_async_commit();
+            cp_async_wait<0>();
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&kv_full[st]);
+        }
+        cp_async_wait<0>();
+    } else if (warp == kPfxMmaWarp) {
+        // ------------------------------------------------------------------ MMA issue
+        if (lane == 0) {
+            auto issue_s = [&](int t) {
+                const int st = t & 1;
+                const uint32_t sK = sbase + C::OFF_STAGE + st * C::STAGE;
+#pragma unroll
+                for (int ks = 0; ks < C::DP / 16; ++ks)
+                    umma_f16(tm + C::COL_S + st * BN, umma_desc(sQ + ks * 2 * (kPfxBM * 16), kPfxBM * 16, 128),
+                             umma_desc(sK + ks * 2 * 128, 128, C::DP * 16), C::IDESC_S, ks > 0);
+                umma_commit(&s_full[st]);
+            };
+            auto issue_pv = [&](int t) {
+                const uint32_t sV = sbase + C::OFF_STAGE + (t & 1) * C::STAGE + C::K_BYTES;
+#pragma unroll
+                for (int h = 0; h < C::NP; ++h)
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        umma_f16(tm + C::COL_O,
+                                 umma_desc(sbase + C::OFF_P + h * C::P_BYTES + kk * 2 * (kPfxBM * 16), kPfxBM * 16, 128),
+                                 umma_desc(sV + kk * 2 * (C::DP * 16), C::DP * 16, 128), C::IDESC_O,
+                                 (t > 0 || kk > 0 || h > 0) ? 1u : 0u);
+                umma_commit(o_done);
+                umma_commit(&kv_empty[t & 1]);
+            };
+            // Issue S of the next tile or P V of the oldest tile, whichever is ready first, so
+            // that a late copy never holds back the P V that frees its stage.
+            bool ok = pfx_wait(q_full, 0, abort_flag);
+            int next_s = 0, next_pv = 0;
+            uint64_t t_idle = 0;
+            while (ok && next_pv < n_tiles) {
+                bool issued = false;
+                if (next_s < n_tiles && next_s <= next_pv + 1 && mbar_try_wait(&kv_full[next_s & 1], (next_s >> 1) & 1) &&
+                    (next_s < 2 || mbar_try_wait(&s_empty[next_s & 1], ((next_s >> 1) - 1) & 1))) {
+                    tc_fence_after();
+                    issue_s(next_s++);
+                    issued = true;
+                }
+                if (next_pv < next_s && mbar_try_wait(p_full, next_pv & 1)) {
+                    tc_fence_after();
+                    issue_pv(next_pv++);
+                    issued = true;
+                }
+                if (issued) {
+                    t_idle = 0;
+                } else if (*abort_flag) {
+                    ok = false;
+                } else if (t_idle == 0) {
+                    t_idle = globaltimer_ns();
+                } else if (globaltimer_ns() - t_idle < kWaitLimitNs) {
+                    __nanosleep(32);
+                } else if (globaltimer_ns() - t_idle > kWaitLimitNs) {
+                    *abort_flag = 1;
+                    prefix_flag(256u);
+                    ok = false;
+                }
+            }
+            // every MMA issued has completed before tensor memory is released
+            umma_commit(fin);
+            if (!mbar_wait_bounded(fin, 0, kWaitLimitNs)) prefix_flag(256u);
+        }
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------------------ softmax
+        const int r = warp * 32 + lane;
+        const int row = row0 + r;
+        const int lim = row / G;  // newest chunk key this row sees (rows past the chunk are never stored)
+        const uint32_t tl = tm + ((uint32_t)(warp * 32) << 16);
+        const uint32_t sP = sbase + C::OFF_P + r * 16;
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int t = 0; t < n_tiles; ++t) {
+            const int st = t & 1;
+            ok = pfx_warp_wait(&kv_full[st], (t >> 1) & 1, abort_flag, lane) &&
+                 pfx_warp_wait(&s_full[st], (t >> 1) & 1, abort_flag, lane);
+            if (!ok) break;
+            tc_fence_after();
+            float sv[BN];
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c)
+                tmem_ld32(tl + C::COL_S + st * BN + c * 32, *reinterpret_cast<float(*)[32]>(&sv[c * 32]));
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_empty[st]);
+
+            if (t < n_ctx) {
+                const int valid = min(BN, ctx - t * BN);
+                const uint32_t bad = bad_mask[st];
+                if (valid < BN || bad) {
+#pragma unroll
+                    for (int i = 0; i < BN; ++i)
+                        if (i >= valid || ((bad >> (i >> p.bs_log2)) & 1u)) sv[i] = -INFINITY;
+                }
+            } else {
+                const int lim_t = lim - (t - n_ctx) * BN;
+                if (lim_t < BN - 1) {
+#pragma unroll
+                    for (int i = 0; i < BN; ++i)
+                        if (i > lim_t) sv[i] = -INFINITY;
+                }
+            }
+            float mt = -INFINITY;
+#pragma unroll
+            for (int i = 0; i < BN; ++i) {
+                sv[i] *= p.sl2;
+                mt = fmaxf(mt, sv[i]);
+            }
+            const bool need = mt > m_ref + 8.f;
+            float corr = 1.f;
+            if (need) {
+                corr = ex2(m_ref - mt);
+                m_ref = mt;
+                l *= corr;
+            }
+            const float mu = m_ref == -INFINITY ? 0.f : m_ref;
+            float sum = 0.f;
+#pragma unroll
+            for (int i = 0; i < BN; ++i) {
+                sv[i] = ex2(sv[i] - mu);
+                sum += sv[i];
+            }
+            l += sum;
+            if (t > 0) {
+                if (!(ok = pfx_warp_wait(o_done, (t - 1) & 1, abort_flag, lane))) break;
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+                    for (int c = 0; c < (C::DP + 31) / 32; ++c) {
+                        float o[32];
+                        tmem_ld32(tl + C::COL_O + c * 32, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) o[e] *= corr;
+                        tmem_st32(tl + C::COL_O + c * 32, o);
+                    }
+                    tmem_wait_st();
+                }
+            }
+#pragma unroll
+            for (int kc = 0; kc < BN / 8; ++kc) {
+                uint32_t hi[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) hi[e] = pack2<BF16>(sv[kc * 8 + 2 * e], sv[kc * 8 + 2 * e + 1]);
+                sts_v4(sP + kc * (kPfxBM * 16), hi[0], hi[1], hi[2], hi[3]);
+                if constexpr (BF16) {
+                    uint32_t lo[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        lo[e] = pack2<BF16>(sv[kc * 8 + 2 * e] - __uint_as_float(hi[e] << 16),
+                                            sv[kc * 8 + 2 * e + 1] - __uint_as_float(hi[e] & 0xffff0000u));
+                    sts_v4(sP + C::P_BYTES + kc * (kPfxBM * 16), lo[0], lo[1], lo[2], lo[3]);
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full);
+        }
+        if (ok) ok = pfx_warp_wait(o_done, (n_tiles - 1) & 1, abort_flag, lane);
+        if (ok) {
+            tc_fence_after();
+            const float inv = 1.f / l;
+            uint8_t* orow = nullptr;
+            if (row < rows_total) {
+                const int j = row / G, g = row - j * G;
+                orow = static_cast<uint8_t*>(p.out) + ((int64_t)(q0 + j) * p.H + kvh * G + g) * (D * 2);
+            }
+#pragma unroll 1
+            for (int c = 0; c < (C::DP + 31) / 32; ++c) {
+                float o[32];
+                tmem_ld32(tl + C::COL_O + c * 32, o);
+                tmem_wait_ld();
+                if (orow != nullptr) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int col = c * 32 + q * 8;
+                        if (col < D) {
+                            uint4 w;
+                            w.x = pack2<BF16>(o[q * 8 + 0] * inv, o[q * 8 + 1] * inv);
+                            w.y = pack2<BF16>(o[q * 8 + 2] * inv, o[q * 8 + 3] * inv);
+                            w.z = pack2<BF16>(o[q * 8 + 4] * inv, o[q * 8 + 5] * inv);
+                            w.w = pack2<BF16>(o[q * 8 + 6] * inv, o[q * 8 + 7] * inv);
+                            *reinterpret_cast<uint4*>(orow + col * 2) = w;
+                        }
                     }
                 }
             }
         }
-        __syncthreads();
     }
-    cp_async_wait<0>();
 
-    // normalise and store the rows that exist
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        float l = l_r[i];
-        l += __shfl_xor_sync(0xffffffffu, l, 1);
-        l += __shfl_xor_sync(0xffffffffu, l, 2);
-        const float inv = 1.f / l;
-        const int row = row0 + r_a + 8 * i;
-        if (row < rows_total) {
-            const int j = row / G, g = row - (row / G) * G;
-            uint8_t* orow = static_cast<uint8_t*>(p.out) + ((int64_t)(q0 + j) * p.H + kvh * G + g) * (D * 2);
-#pragma unroll
-            for (int n = 0; n < Gm::DP / 8; ++n) {
-                const int col = n * 8 + (lane & 3) * 2;
-                if (col < D)
-                    *reinterpret_cast<uint32_t*>(orow + col * 2) =
-                        pack2<BF16>(acc[n][2 * i] * inv, acc[n][2 * i + 1] * inv);
-            }
-        }
-    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kPfxMmaWarp) tmem_dealloc(tm, C::TMEM_COLS);
 }
 
 template <bool BF16, int D>
 cudaError_t launch_prefix_kernel(const PrefixParams& p, dim3 grid, cudaStream_t stream) {
-    cudaError_t e = cudaFuncSetAttribute(pa_prefix_kernel<BF16, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         PfxGeom<D>::SMEM);
+    using C = PfxCfg<BF16, D>;
+    cudaError_t e = cudaFuncSetAttribute(pa_prefix_kernel<BF16, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    pa_prefix_kernel<BF16, D><<<grid, kPfxThreads, PfxGeom<D>::SMEM, stream>>>(p);
+    pa_prefix_kernel<BF16, D><<<grid, kPfxThreads, C::SMEM, stream>>>(p);
     return cudaGetLastError();
 }
 
