@@ -88,8 +88,8 @@ constexpr int kPfxBM = 128;    // query rows per CTA (the MMA M)
 constexpr int kPfxStages = 2;  // key/value tile stages
 
 struct PrefixParams {
-    CUtensorMap kmap;  // key cache as {8 elems, block_size, d/8, blocks * kv heads}
-    CUtensorMap vmap;  // value cache as {8 keys, block_size/8, d, blocks * kv heads}
+    CUtensorMap kmap;  // key cache as {64 elems = 8 tokens x 8, block_size/8, d/8, blocks * kv heads}
+    CUtensorMap vmap;  // value cache as {block_size keys, d, blocks * kv heads}, 32/64-byte swizzle
     void* out;
     const uint8_t* q;  // [T][q_stride] rows, head h at h * d
     const uint8_t* k;  // [T][kv_stride] rows, kv head at kvh * d

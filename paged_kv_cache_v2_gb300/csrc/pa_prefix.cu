@@ -33,10 +33,13 @@ static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // Tensor maps of the paged caches for the prefix kernel's tile copies:
-//   keys   {8 elements, block_size slots, d/8 chunks, blocks * kv heads}, box {8, 8, d/8, 1}:
-//          8 tokens of one page land as [d/8][8 tokens][16 bytes];
-//   values {8 keys, block_size/8, d rows, blocks * kv heads}, box {8, 1, d, 1}:
-//          8 keys of one page land as [d][16 bytes].
+//   keys   {64 elements = 8 tokens x 8, block_size/8 token groups, d/8 chunks, blocks * kv
+//          heads}, box {64, 1, d/8, 1}: 8 tokens of one page land as [d/8][8 tokens][16 bytes]
+//          with 128-byte rows read from global memory;
+//   values {block_size keys, d rows, blocks * kv heads}, box {block_size, d, 1} with the
+//          32-byte (block size 16) or 64-byte (block size 32) swizzle: a whole page lands in the
+//          swizzled K-major layout the value MMA reads.  Block size 8 pages are plain 16-byte
+//          rows and move by 1-d bulk copies (the map is still encoded, unswizzled).
 static bool encode_cache_maps(PrefixParams& p, const void* key_cache, const void* value_cache, int num_blocks,
                               int num_kv_heads, int head_size, int block_size) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
@@ -44,18 +47,21 @@ static bool encode_cache_maps(PrefixParams& p, const void* key_cache, const void
     const cuuint64_t pages = (cuuint64_t)num_blocks * num_kv_heads;
     const cuuint64_t d = head_size, bs = block_size;
     const cuuint32_t estr[4] = {1, 1, 1, 1};
-    const cuuint64_t kdim[4] = {8, bs, d / 8, pages};
-    const cuuint64_t kstride[3] = {16, bs * 16, d * bs * 2};
-    const cuuint32_t kbox[4] = {8, 8, (cuuint32_t)(d / 8), 1};
+    const cuuint64_t kdim[4] = {64, bs / 8, d / 8, pages};
+    const cuuint64_t kstride[3] = {128, bs * 16, d * bs * 2};
+    const cuuint32_t kbox[4] = {64, 1, (cuuint32_t)(d / 8), 1};
     if (enc(&p.kmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(key_cache), kdim, kstride, kbox, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return false;
-    const cuuint64_t vdim[4] = {8, bs / 8, d, pages};
-    const cuuint64_t vstride[3] = {16, bs * 2, d * bs * 2};
-    const cuuint32_t vbox[4] = {8, 1, (cuuint32_t)d, 1};
-    return enc(&p.vmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 4, const_cast<void*>(value_cache), vdim, vstride, vbox, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+    const cuuint64_t vdim[3] = {bs, d, pages};
+    const cuuint64_t vstride[2] = {bs * 2, d * bs * 2};
+    const cuuint32_t vbox[3] = {(cuuint32_t)bs, (cuuint32_t)d, 1};
+    const CUtensorMapSwizzle sw = block_size == 16   ? CU_TENSOR_MAP_SWIZZLE_32B
+                                  : block_size == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                                     : CU_TENSOR_MAP_SWIZZLE_NONE;
+    return enc(&p.vmap, CU_TENSOR_MAP_DATA_TYPE_UINT16, 3, const_cast<void*>(value_cache), vdim, vstride, vbox, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

@@ -12,10 +12,11 @@
 // and shared by the whole GQA group, and the 128 rows are the M of every MMA.  Per tile of
 // BN keys (128, or 64 above head size 128):
 //   loader warps   copy the key tile and the value tile into shared memory in the canonical
-//                  no-swizzle K-major layouts (8-row x 16-byte core matrices): keys as
-//                  [key/8][d/8][8 keys][8], values as [key/8][d][8 keys].  A tile of full,
-//                  valid pages moves by tensor copies (TMA), one per 8 keys of each cache,
-//                  issued by one thread; a tile with the context's end, a page outside the
+//                  K-major layouts: keys as [key/8][d/8][8 keys][8] (no swizzle), values as
+//                  whole pages [d][block_size keys] with the 32- or 64-byte swizzle (block
+//                  size 16 / 32; plain rows for 8).  A tile of full, valid pages moves by
+//                  tensor copies (TMA) issued by one thread: per 8 keys one key box of 128-byte
+//                  rows, per page one value box; a tile with the context's end, a page outside the
 //                  cache or the chunk's dense rows moves by 16-byte cp.async (zero-filling
 //                  what must not count; the dense value rows are transposed on the way).
 //   MMA lane       S = Q K^T (M 128, N BN) into one of two S buffers in tensor memory, then,
@@ -38,29 +39,31 @@ namespace pa {
 template <bool BF16, int D>
 struct PfxCfg {
     static constexpr int DP = (D + 15) / 16 * 16;  // head size padded to the MMA K step
+    static constexpr int DPR = (DP + 31) / 32 * 32;  // O columns read in 32-column pieces
     static constexpr int NCR = D / 8;              // 16-byte chunks of a row that exist
     static constexpr int NCP = DP / 8;             // chunks after padding
-    static constexpr int BN = DP <= 128 ? 128 : 64;
-    static constexpr int NP = BF16 ? 2 : 1;  // P buffers: hi (and lo for bf16)
-    static constexpr int Q_BYTES = kPfxBM * DP * 2;
+    static constexpr int BN = 64;                  // keys per tile
+    static constexpr int NP = BF16 ? 2 : 1;        // P buffers: hi (and lo for bf16)
     static constexpr int K_BYTES = BN * DP * 2;
     static constexpr int V_BYTES = BN * DP * 2;
     static constexpr int STAGE = K_BYTES + V_BYTES;
     static constexpr int P_BYTES = kPfxBM * BN * 2;
-    static constexpr int OFF_STAGE = Q_BYTES;
-    static constexpr int OFF_P = OFF_STAGE + kPfxStages * STAGE;
-    static constexpr int OFF_CTL = OFF_P + NP * P_BYTES;
     static constexpr int CTL_BYTES = 512;
+    static constexpr int FREE = 225 * 1024 - NP * P_BYTES - CTL_BYTES;
+    static constexpr int NS = FREE / STAGE > 8 ? 8 : FREE / STAGE;  // key/value stages in the ring
+    static constexpr int OFF_STAGE = 0;
+    static constexpr int OFF_P = NS * STAGE;
+    static constexpr int OFF_CTL = OFF_P + NP * P_BYTES;
     // at least 120 KiB so two CTAs never share an SM (each takes all 512 tensor-memory columns)
     static constexpr int SMEM = OFF_CTL + CTL_BYTES > 120 * 1024 ? OFF_CTL + CTL_BYTES : 120 * 1024;
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t COL_S = 0;       // two S buffers: columns [0, BN) and [BN, 2 BN)
-    static constexpr uint32_t COL_O = 2 * BN;  // O: columns [2 BN, 2 BN + DP)
+    static constexpr uint32_t COL_S = 0;         // two S buffers: columns [0, BN) and [BN, 2 BN)
+    static constexpr uint32_t COL_O = 2 * BN;    // O: [2 BN, 2 BN + DPR)
+    static constexpr uint32_t COL_Q = 2 * BN + DPR;  // Q, two 16-bit values per column: DP / 2
     static constexpr uint32_t IDESC_S = umma_idesc_f16(BF16, kPfxBM, BN);
     static constexpr uint32_t IDESC_O = umma_idesc_f16(BF16, kPfxBM, DP);
-    // O is read and rescaled in 32-column pieces, so the last piece may run past DP
-    static_assert(2 * BN + (DP + 31) / 32 * 32 <= (int)TMEM_COLS, "tensor memory");
-    static_assert(SMEM <= 227 * 1024, "shared memory");
+    static_assert(COL_Q + DP / 2 <= TMEM_COLS, "tensor memory");
+    static_assert(NS >= 2 && SMEM <= 227 * 1024, "shared memory");
 };
 
 #ifndef PA_PFX_WAIT_HINT_NS
@@ -87,6 +90,18 @@ __device__ __forceinline__ bool pfx_wait(uint64_t* bar, uint32_t parity, volatil
     return true;
 }
 
+// Byte offset of (token o of a tile, value row dd) in a value tile.  The tile is pages of
+// block_size keys, DP * 2 * block_size bytes apart; a page is DP rows of 2 * block_size bytes
+// whose 16-byte chunks are XOR-swizzled the way the value MMA reads them (none for block
+// size 8, row bit 2 for 16 = 32-byte swizzle, row bits 1-2 for 32 = 64-byte swizzle), which
+// is also what a swizzled tensor copy of a whole page writes.
+__device__ __forceinline__ uint32_t pfx_v_off(int o, int dd, int bs_log2, int DP) {
+    const int rowb_log2 = bs_log2 + 1;
+    const int kq = (o >> 3) & ((1 << (bs_log2 - 3)) - 1);
+    const int swz = bs_log2 == 3 ? 0 : (bs_log2 == 4 ? (dd >> 2) & 1 : (dd >> 1) & 3);
+    return (uint32_t)((o >> bs_log2) * (DP << rowb_log2) + (dd << rowb_log2) + ((kq ^ swz) << 4));
+}
+
 // One lane waits, the warp learns the outcome (warp-uniform, as tcgen05.ld/st require).
 __device__ __forceinline__ bool pfx_warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int lane) {
     int ok = 1;
@@ -98,7 +113,7 @@ __device__ __forceinline__ bool pfx_warp_wait(uint64_t* bar, uint32_t parity, vo
 template <bool BF16, int D>
 __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_constant__ PrefixParams p) {
     using C = PfxCfg<BF16, D>;
-    constexpr int BN = C::BN;
+    constexpr int BN = C::BN, NS = C::NS;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int s = blockIdx.z, kvh = blockIdx.y;
@@ -119,49 +134,56 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
     }
 
     const uint32_t sbase = smem_addr(smem);
-    const uint32_t sQ = sbase;
+    if (sbase & 1023u) {  // the swizzled layouts are defined on 1 KiB-aligned addresses
+        if (tid == 0) prefix_flag(256u);
+        return;
+    }
     uint8_t* ctl = smem + C::OFF_CTL;
     uint64_t* bars = reinterpret_cast<uint64_t*>(ctl);
-    uint64_t* q_full = bars + 0;
-    uint64_t* kv_full = bars + 1;   // [2]
-    uint64_t* kv_empty = bars + 3;  // [2]
-    uint64_t* s_full = bars + 5;    // [2]
-    uint64_t* s_empty = bars + 7;   // [2]
-    uint64_t* p_full = bars + 9;
-    uint64_t* o_done = bars + 10;
-    uint64_t* fin = bars + 11;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctl + 96);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(ctl + 100);
-    uint32_t* bad_mask = reinterpret_cast<uint32_t*>(ctl + 104);  // [2] pages outside the cache
+    uint64_t* kv_full = bars;            // [NS]
+    uint64_t* kv_empty = bars + NS;      // [NS]
+    uint64_t* s_full = bars + 2 * NS;    // [2]
+    uint64_t* s_empty = bars + 2 * NS + 2;  // [2]
+    uint64_t* q_full = bars + 2 * NS + 4;
+    uint64_t* p_full = bars + 2 * NS + 5;
+    uint64_t* o_done = bars + 2 * NS + 6;
+    uint64_t* fin = bars + 2 * NS + 7;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctl + 8 * (2 * NS + 8));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(ctl + 8 * (2 * NS + 8) + 4);
+    uint32_t* bad_mask = reinterpret_cast<uint32_t*>(ctl + 8 * (2 * NS + 8) + 8);  // [NS] pages outside the cache
 
     const int n_ctx = (ctx + BN - 1) / BN;
     const int row_last = min(row0 + kPfxBM, rows_total) - 1;
     const int n_tiles = n_ctx + (row_last / G) / BN + 1;
 
     if (tid == 0) {
-        mbar_init(q_full, 4);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < NS; ++i) {
             mbar_init(&kv_full[i], 4);
             mbar_init(&kv_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&s_empty[i], 4);
         }
+        mbar_init(q_full, 4);
         mbar_init(p_full, 4);
         mbar_init(o_done, 1);
         mbar_init(fin, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    // Padding the copies never write: key chunks c >= D/8 and value rows d >= D, both stages.
+    // Padding the copies never write: key chunks c >= D/8 and value rows d >= D, every stage.
     if constexpr (C::NCP > C::NCR) {
         constexpr int kpad = (C::NCP - C::NCR) * BN, vpad = (BN / 8) * (C::DP - D);
-        for (int i = tid; i < kPfxStages * (kpad + vpad); i += kPfxThreads) {
+        for (int i = tid; i < NS * (kpad + vpad); i += kPfxThreads) {
             const int st = i / (kpad + vpad), rem = i % (kpad + vpad);
             uint8_t* stage = smem + C::OFF_STAGE + st * C::STAGE;
             const int o = rem % BN, c = C::NCR + rem / BN;
+            const int kc = (rem - kpad) / (C::DP - D), dd = D + (rem - kpad) % (C::DP - D);
+            const int cpp_log2 = p.bs_log2 - 3;  // 16-byte chunks per value row, log2
             uint8_t* dst = rem < kpad ? stage + (o >> 3) * (C::DP * 16) + c * 128 + (o & 7) * 16
-                                      : stage + C::K_BYTES + ((rem - kpad) / (C::DP - D)) * (C::DP * 16) +
-                                            (D + (rem - kpad) % (C::DP - D)) * 16;
+                                      : stage + C::K_BYTES + (kc >> cpp_log2) * (C::DP << (p.bs_log2 + 1)) +
+                                            (dd << (p.bs_log2 + 1)) + ((kc & ((1 << cpp_log2) - 1)) << 4);
             *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
         }
     }
@@ -177,27 +199,9 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
     if (warp >= kPfxLoaderWarp0) {
         // ------------------------------------------------------------------ loaders
         const int lt = tid - kPfxLoaderWarp0 * 32;
-        for (int i = lt; i < kPfxBM * C::NCP; i += kPfxLoaderThreads) {
-            const int c = i / kPfxBM, r = i % kPfxBM;
-            const int row = row0 + r;
-            const uint8_t* src = p.q;
-            uint32_t nb = 0;
-            if (row < rows_total && c < C::NCR) {
-                const int j = row / G, g = row - j * G;
-                src = p.q + ((int64_t)(q0 + j) * p.q_stride + (int64_t)(kvh * G + g) * D + c * 8) * 2;
-                nb = 16;
-            }
-            cp_async16(sQ + c * (kPfxBM * 16) + r * 16, src, nb);
-        }
-        cp_async_commit();
-        cp_async_wait<0>();
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(q_full);
-
         for (int t = 0; t < n_tiles; ++t) {
-            const int st = t & 1;
-            if (t >= 2 && !pfx_warp_wait(&kv_empty[st], ((t >> 1) - 1) & 1, abort_flag, lane)) break;
+            const int st = t % NS;
+            if (t >= NS && !pfx_warp_wait(&kv_empty[st], ((t / NS) - 1) & 1, abort_flag, lane)) break;
             const uint32_t sK = sbase + C::OFF_STAGE + st * C::STAGE, sV = sK + C::K_BYTES;
             if (t < n_ctx) {
                 const int t0 = t * BN;
@@ -221,9 +225,17 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
                         for (int i = 0; i < BN / 8; ++i) {
                             const int o0 = 8 * i;
                             const int page = tile_table[o0 >> p.bs_log2] * p.Hk + kvh;
-                            const int slot0 = o0 & (p.bs - 1);
-                            tma_load_4d(sK + i * (C::DP * 16), &p.kmap, 0, slot0, 0, page, &kv_full[st]);
-                            tma_load_4d(sV + i * (C::DP * 16), &p.vmap, 0, slot0 >> 3, 0, page, &kv_full[st]);
+                            tma_load_4d(sK + i * (C::DP * 16), &p.kmap, 0, (o0 & (p.bs - 1)) >> 3, 0, page,
+                                        &kv_full[st]);
+                        }
+#pragma unroll 1
+                        for (int pg = 0; pg < (BN >> p.bs_log2); ++pg) {
+                            const int page = tile_table[pg] * p.Hk + kvh;
+                            const uint32_t dst = sV + pg * (C::DP << (p.bs_log2 + 1));
+                            if (p.bs_log2 == 3)
+                                bulk_load(dst, p.vcache + (int64_t)page * page_bytes, (uint32_t)page_bytes, &kv_full[st]);
+                            else
+                                tma_load_3d(dst, &p.vmap, 0, 0, page, &kv_full[st]);
                         }
                     } else if (lane == 0 && lt >= 32) {
                         mbar_arrive(&kv_full[st]);
@@ -255,7 +267,7 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
                     const uint8_t* src = ok ? p.vcache + ((int64_t)b * p.Hk + kvh) * page_bytes +
                                                   ((int64_t)dd * p.bs + kq * 8) * 2
                                             : p.vcache;
-                    cp_async16(sV + (o >> 3) * (C::DP * 16) + dd * 16, src, ok ? (uint32_t)nv * 2u : 0u);
+                    cp_async16(sV + pfx_v_off(o, dd, p.bs_log2, C::DP), src, ok ? (uint32_t)nv * 2u : 0u);
                 }
             } else {
                 const int kc0 = (t - n_ctx) * BN;
@@ -267,7 +279,7 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
                         ok ? p.k + ((int64_t)(q0 + j) * p.kv_stride + (int64_t)kvh * D + c * 8) * 2 : p.k;
                     cp_async16(sK + (o >> 3) * (C::DP * 16) + c * 128 + (o & 7) * 16, src, ok ? 16u : 0u);
                 }
-                // dense value rows, two tokens at a time, transposed into [key/8][d][8 keys]
+                // dense value rows, two tokens at a time, transposed into the value layout
                 for (int i = lt; i < (BN / 2) * C::NCR; i += kPfxLoaderThreads) {
                     const int c = i % C::NCR, t2 = 2 * (i / C::NCR);
                     const int j = kc0 + t2;
@@ -276,10 +288,10 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
                     if (j < q_len) a = ld_nc_v4(base + (int64_t)(q0 + j) * p.kv_stride * 2);
                     if (j + 1 < q_len) b = ld_nc_v4(base + (int64_t)(q0 + j + 1) * p.kv_stride * 2);
                     const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
-                    const uint32_t dst = sV + (t2 >> 3) * (C::DP * 16) + c * 8 * 16 + (t2 & 7) * 2;
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
-                        sts_u32(dst + e * 16, __byte_perm(av[e >> 1], bv[e >> 1], (e & 1) ? 0x7632 : 0x5410));
+                        sts_u32(sV + pfx_v_off(t2, c * 8 + e, p.bs_log2, C::DP) + (t2 & 7) * 2,
+                                __byte_perm(av[e >> 1], bv[e >> 1], (e & 1) ? 0x7632 : 0x5410));
                 }
             }
             cp_async_commit();
@@ -293,35 +305,47 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
         // ------------------------------------------------------------------ MMA issue
         if (lane == 0) {
             auto issue_s = [&](int t) {
-                const int st = t & 1;
-                const uint32_t sK = sbase + C::OFF_STAGE + st * C::STAGE;
+                const uint32_t sK = sbase + C::OFF_STAGE + (t % NS) * C::STAGE;
+                const uint32_t d_s = tm + C::COL_S + (t & 1) * BN;
 #pragma unroll
-                for (int ks = 0; ks < C::DP / 16; ++ks)
-                    umma_f16(tm + C::COL_S + st * BN, umma_desc(sQ + ks * 2 * (kPfxBM * 16), kPfxBM * 16, 128),
-                             umma_desc(sK + ks * 2 * 128, 128, C::DP * 16), C::IDESC_S, ks > 0);
-                umma_commit(&s_full[st]);
+                for (int ks = 0; ks < C::DP / 16; ++ks) {
+                    const uint64_t kd = umma_desc(sK + ks * 2 * 128, 128, C::DP * 16);
+                    asm volatile(
+                        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+                        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_s),
+                        "r"(tm + C::COL_Q + ks * 8), "l"(kd), "r"(C::IDESC_S), "r"(ks > 0 ? 1u : 0u));
+                }
+                umma_commit(&s_full[t & 1]);
             };
             auto issue_pv = [&](int t) {
-                const uint32_t sV = sbase + C::OFF_STAGE + (t & 1) * C::STAGE + C::K_BYTES;
+                const uint32_t sV = sbase + C::OFF_STAGE + (t % NS) * C::STAGE + C::K_BYTES;
 #pragma unroll
                 for (int h = 0; h < C::NP; ++h)
 #pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk)
+                    for (int kk = 0; kk < BN / 16; ++kk) {
+                        // 16 keys of the value tile: two 8-row pages (block size 8), one page
+                        // with the 32-byte swizzle (16), half a page with the 64-byte swizzle (32)
+                        const uint64_t vd =
+                            p.bs_log2 == 3   ? umma_desc(sV + kk * 2 * (C::DP * 16), C::DP * 16, 128)
+                            : p.bs_log2 == 4 ? umma_desc_sw(sV + kk * (C::DP * 32), 256, 6)
+                                             : umma_desc_sw(sV + (kk >> 1) * (C::DP * 64) + (kk & 1) * 32, 512, 4);
                         umma_f16(tm + C::COL_O,
                                  umma_desc(sbase + C::OFF_P + h * C::P_BYTES + kk * 2 * (kPfxBM * 16), kPfxBM * 16, 128),
-                                 umma_desc(sV + kk * 2 * (C::DP * 16), C::DP * 16, 128), C::IDESC_O,
-                                 (t > 0 || kk > 0 || h > 0) ? 1u : 0u);
+                                 vd, C::IDESC_O, (t > 0 || kk > 0 || h > 0) ? 1u : 0u);
+                    }
                 umma_commit(o_done);
-                umma_commit(&kv_empty[t & 1]);
+                umma_commit(&kv_empty[t % NS]);
             };
             // Issue S of the next tile or P V of the oldest tile, whichever is ready first, so
             // that a late copy never holds back the P V that frees its stage.
             bool ok = pfx_wait(q_full, 0, abort_flag);
+            if (ok) tc_fence_after();
             int next_s = 0, next_pv = 0;
             uint64_t t_idle = 0;
             while (ok && next_pv < n_tiles) {
                 bool issued = false;
-                if (next_s < n_tiles && next_s <= next_pv + 1 && mbar_try_wait(&kv_full[next_s & 1], (next_s >> 1) & 1) &&
+                if (next_s < n_tiles && next_s <= next_pv + 1 &&
+                    mbar_try_wait(&kv_full[next_s % NS], (next_s / NS) & 1) &&
                     (next_s < 2 || mbar_try_wait(&s_empty[next_s & 1], ((next_s >> 1) - 1) & 1))) {
                     tc_fence_after();
                     issue_s(next_s++);
@@ -340,7 +364,7 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
                     t_idle = globaltimer_ns();
                 } else if (globaltimer_ns() - t_idle < kWaitLimitNs) {
                     __nanosleep(32);
-                } else if (globaltimer_ns() - t_idle > kWaitLimitNs) {
+                } else {
                     *abort_flag = 1;
                     prefix_flag(256u);
                     ok = false;
@@ -358,22 +382,46 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
         const int lim = row / G;  // newest chunk key this row sees (rows past the chunk are never stored)
         const uint32_t tl = tm + ((uint32_t)(warp * 32) << 16);
         const uint32_t sP = sbase + C::OFF_P + r * 16;
+        // this thread's query row into tensor memory (two 16-bit values per column; rows past
+        // the chunk and the padding past D are zero)
+        {
+            const uint8_t* qrow = nullptr;
+            if (row < rows_total) {
+                const int j = row / G, g = row - j * G;
+                qrow = p.q + ((int64_t)(q0 + j) * p.q_stride + (int64_t)(kvh * G + g) * D) * 2;
+            }
+#pragma unroll 1
+            for (int c = 0; c < C::DP / 16; ++c) {
+                uint4 a = make_uint4(0u, 0u, 0u, 0u), b = make_uint4(0u, 0u, 0u, 0u);
+                if (qrow != nullptr && 2 * c < C::NCR) a = ld_nc_v4(qrow + c * 32);
+                if (qrow != nullptr && 2 * c + 1 < C::NCR) b = ld_nc_v4(qrow + c * 32 + 16);
+                const uint32_t v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+                asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(
+                                 tl + C::COL_Q + c * 8),
+                             "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                             : "memory");
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(q_full);
+        }
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         for (int t = 0; t < n_tiles; ++t) {
-            const int st = t & 1;
-            ok = pfx_warp_wait(&kv_full[st], (t >> 1) & 1, abort_flag, lane) &&
-                 pfx_warp_wait(&s_full[st], (t >> 1) & 1, abort_flag, lane);
+            const int st = t % NS;
+            ok = pfx_warp_wait(&kv_full[st], (t / NS) & 1, abort_flag, lane) &&
+                 pfx_warp_wait(&s_full[t & 1], (t >> 1) & 1, abort_flag, lane);
             if (!ok) break;
             tc_fence_after();
             float sv[BN];
 #pragma unroll
             for (int c = 0; c < BN / 32; ++c)
-                tmem_ld32(tl + C::COL_S + st * BN + c * 32, *reinterpret_cast<float(*)[32]>(&sv[c * 32]));
+                tmem_ld32(tl + C::COL_S + (t & 1) * BN + c * 32, *reinterpret_cast<float(*)[32]>(&sv[c * 32]));
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&s_empty[st]);
+            if (lane == 0) mbar_arrive(&s_empty[t & 1]);
 
             if (t < n_ctx) {
                 const int valid = min(BN, ctx - t * BN);
@@ -417,7 +465,7 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
                 tc_fence_after();
                 if (__any_sync(0xffffffffu, need)) {
 #pragma unroll 1
-                    for (int c = 0; c < (C::DP + 31) / 32; ++c) {
+                    for (int c = 0; c < C::DPR / 32; ++c) {
                         float o[32];
                         tmem_ld32(tl + C::COL_O + c * 32, o);
                         tmem_wait_ld();
@@ -458,7 +506,7 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
                 orow = static_cast<uint8_t*>(p.out) + ((int64_t)(q0 + j) * p.H + kvh * G + g) * (D * 2);
             }
 #pragma unroll 1
-            for (int c = 0; c < (C::DP + 31) / 32; ++c) {
+            for (int c = 0; c < C::DPR / 32; ++c) {
                 float o[32];
                 tmem_ld32(tl + C::COL_O + c * 32, o);
                 tmem_wait_ld();

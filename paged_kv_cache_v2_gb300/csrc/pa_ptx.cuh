@@ -92,6 +92,20 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
         "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
         : "memory");
 }
+// 3-d tiled tensor copy global -> shared; completes (bytes) on an mbarrier.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int c0, int c1, int c2, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(tmap), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
+        : "memory");
+}
+// 1-d bulk copy global -> shared (addresses 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+                 "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
 // 4-d tiled tensor copy global -> shared; completes (bytes) on an mbarrier.
 __device__ __forceinline__ void tma_load_4d(uint32_t dst, const void* tmap, int c0, int c1, int c2, int c3,
                                             uint64_t* bar) {
@@ -250,6 +264,11 @@ __device__ __forceinline__ void split_e4m3x2(uint32_t v, uint16_t& hi, uint16_t&
 __device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
     return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
            ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46);
+}
+// The same with a swizzled layout: `layout` 6 = 32-byte, 4 = 64-byte swizzle (16-byte chunk
+// index XOR address bits 7..); rows of 32 / 64 bytes, `sbo` = 8 rows, `lbo` unused (16).
+__device__ __forceinline__ uint64_t umma_desc_sw(uint32_t saddr, uint32_t sbo, uint32_t layout) {
+    return umma_desc(saddr, 16, sbo) | ((uint64_t)layout << 61);
 }
 // Instruction descriptor of kind::f16 with fp32 accumulation, both operands K-major.
 __host__ __device__ constexpr uint32_t umma_idesc_f16(bool bf16, int m, int n) {
