@@ -37,9 +37,14 @@ if ROOT not in sys.path:
 METRIC = "decode attn µs/step and achieved HBM GB/s (fraction of GB300 peak), 1 GPU"
 DEFAULT_WORKLOAD = "llama_gqa_decode"
 L2_BYTES = 129 * 1024 * 1024
-# the phase-1 kernel's sources: the committed ncu counters are valid while these are unchanged
-KERNEL_SRCS = [os.path.join(ROOT, "paged_kv_cache_v2_gb300", "csrc", f)
-               for f in ("pa_phase1.cuh", "pa_kernels.cuh", "pa_ptx.cuh")]
+# each profiled kernel's sources: its committed ncu counters are valid while these are unchanged
+_CSRC = os.path.join(ROOT, "paged_kv_cache_v2_gb300", "csrc")
+KERNEL_SRCS = {
+    "phase1": [os.path.join(_CSRC, f) for f in ("pa_phase1.cuh", "pa_kernels.cuh", "pa_ptx.cuh")],
+    "prefix": [os.path.join(_CSRC, f) for f in ("pa_prefix.cuh", "pa_prefix.h", "pa_tc.cuh", "pa_kernels.cuh",
+                                                "pa_ptx.cuh")],
+}
+PROFILE_FILES = {"phase1": "pa_v2_phase1_{}.md", "prefix": "pa_prefix_{}.md"}
 PROFILE_DIR = os.path.join(ROOT, "profiles")
 
 
@@ -52,25 +57,25 @@ def _peaks():
         return 6800.0, "fallback"
 
 
-def _kernel_hash() -> str:
+def _kernel_hash(kernel: str = "phase1") -> str:
     h = hashlib.sha256()
-    for path in KERNEL_SRCS:
+    for path in KERNEL_SRCS[kernel]:
         with open(path, "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def _profiled_traffic(workload: str):
-    """DRAM bytes per phase-1 launch from the committed ncu summary, if it was taken on the
-    current kernel source (else None)."""
-    path = os.path.join(PROFILE_DIR, f"pa_v2_phase1_{workload}.md")
+def _profiled_traffic(workload: str, kernel: str = "phase1"):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    path = os.path.join(PROFILE_DIR, PROFILE_FILES[kernel].format(workload))
     try:
         txt = open(path).read()
     except OSError:
         return None
     h = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", txt)
     b = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
-    if not h or not b or h.group(1) != _kernel_hash():
+    if not h or not b or h.group(1) != _kernel_hash(kernel):
         return None
     return float(b.group(1))
 
@@ -536,7 +541,8 @@ def run_prefix(args):
                    "context_lens": wl.context_lens.tolist(), "query_lens": wl.query_lens.tolist(),
                    "flops_per_step": flops, "l2": "flushed (256 MiB write) before every timed call"},
         "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(tflops / peak, 4), "traffic": None, "kernel": "pa_prefix_kernel",
+                     "frac": round(tflops / peak, 4), "traffic": _profiled_traffic(name, "prefix"),
+                     "kernel": "pa_prefix_kernel",
                      "peak_source": f"{kind} bf16_tflops (burst; fp16 has the same dense rate)"},
         "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": launches, "clocks": clocks.summary()}), flush=True)
     return 0

@@ -45,6 +45,7 @@
 #include "pa_v2.h"
 #include "pa_internal.h"
 #include "pa_kernels.cuh"
+#include "pa_prefix.h"
 #include "pa_ptx.cuh"
 
 namespace pa {

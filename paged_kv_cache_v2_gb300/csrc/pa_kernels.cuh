@@ -4,7 +4,6 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
-#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -75,41 +74,5 @@ Phase1Fn phase1_select(bool bf16, bool fp8, int d);
 // Read (and optionally clear) the device error word of the block-size-BS phase-1 kernels.
 template <int BS>
 cudaError_t phase1_read_errors(unsigned int* v, bool reset);
-
-// ---- chunked-prefix attention ----------------------------------------------------------
-// Warp roles of the prefix kernel: warps 0-3 run the softmax (warp w owns tensor-memory lanes
-// 32w..32w+31, i.e. query rows 32w..32w+31), warp 4 allocates tensor memory and one of its
-// lanes issues the MMAs, warps 5-8 copy query, key and value tiles into shared memory.
-constexpr int kPfxMmaWarp = 4;
-constexpr int kPfxLoaderWarp0 = 5;
-constexpr int kPfxLoaderThreads = 4 * 32;
-constexpr int kPfxThreads = 9 * 32;
-constexpr int kPfxBM = 128;    // query rows per CTA (the MMA M)
-constexpr int kPfxStages = 2;  // key/value tile stages
-
-struct PrefixParams {
-    CUtensorMap kmap;  // key cache as {64 elems = 8 tokens x 8, block_size/8, d/8, blocks * kv heads}
-    CUtensorMap vmap;  // value cache as {block_size keys, d, blocks * kv heads}, 32/64-byte swizzle
-    void* out;
-    const uint8_t* q;  // [T][q_stride] rows, head h at h * d
-    const uint8_t* k;  // [T][kv_stride] rows, kv head at kvh * d
-    const uint8_t* v;
-    const uint8_t* kcache;
-    const uint8_t* vcache;
-    const int32_t* block_tables;
-    const int32_t* qsl;
-    const int32_t* ctx_lens;
-    int H, Hk, G, bs, bs_log2, mbps, num_blocks, max_query_len;
-    int64_t q_stride, kv_stride;  // elements between consecutive tokens
-    float sl2;                    // scale * log2(e)
-};
-
-using PrefixFn = cudaError_t (*)(const PrefixParams&, dim3 grid, cudaStream_t);
-
-// Prefix kernel launcher for (query dtype, head size), or nullptr; defined in pa_prefix_<dtype>.cu.
-template <bool BF16>
-PrefixFn prefix_select(int d);
-template <bool BF16>
-cudaError_t prefix_read_errors(unsigned int* v, bool reset);
 
 }  // namespace pa

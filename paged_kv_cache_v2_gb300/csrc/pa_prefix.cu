@@ -11,6 +11,7 @@
 
 #include "pa_internal.h"
 #include "pa_kernels.cuh"
+#include "pa_prefix.h"
 #include "pa_v2.h"
 
 using namespace pa;

@@ -32,7 +32,8 @@
 #pragma once
 
 #include "pa_kernels.cuh"
-#include "pa_ptx.cuh"
+#include "pa_prefix.h"
+#include "pa_tc.cuh"
 
 namespace pa {
 
@@ -345,13 +346,13 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
             while (ok && next_pv < n_tiles) {
                 bool issued = false;
                 if (next_s < n_tiles && next_s <= next_pv + 1 &&
-                    mbar_try_wait(&kv_full[next_s % NS], (next_s / NS) & 1) &&
-                    (next_s < 2 || mbar_try_wait(&s_empty[next_s & 1], ((next_s >> 1) - 1) & 1))) {
+                    mbar_test_wait(&kv_full[next_s % NS], (next_s / NS) & 1) &&
+                    (next_s < 2 || mbar_test_wait(&s_empty[next_s & 1], ((next_s >> 1) - 1) & 1))) {
                     tc_fence_after();
                     issue_s(next_s++);
                     issued = true;
                 }
-                if (next_pv < next_s && mbar_try_wait(p_full, next_pv & 1)) {
+                if (next_pv < next_s && mbar_test_wait(p_full, next_pv & 1)) {
                     tc_fence_after();
                     issue_pv(next_pv++);
                     issued = true;
@@ -362,12 +363,12 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
                     ok = false;
                 } else if (t_idle == 0) {
                     t_idle = globaltimer_ns();
-                } else if (globaltimer_ns() - t_idle < kWaitLimitNs) {
-                    __nanosleep(32);
-                } else {
+                } else if (globaltimer_ns() - t_idle > kWaitLimitNs) {
                     *abort_flag = 1;
                     prefix_flag(256u);
                     ok = false;
+                } else {
+                    __nanosleep(20);  // leave issue slots to the softmax warp on this SM quarter
                 }
             }
             // every MMA issued has completed before tensor memory is released
