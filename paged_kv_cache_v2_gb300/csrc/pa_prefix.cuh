@@ -50,11 +50,11 @@ struct PfxCfg {
     static constexpr int STAGE = K_BYTES + V_BYTES;
     static constexpr int P_BYTES = kPfxBM * BN * 2;
     static constexpr int CTL_BYTES = 512;
-    static constexpr int FREE = 225 * 1024 - NP * P_BYTES - CTL_BYTES;
+    static constexpr int FREE = 225 * 1024 - 2 * NP * P_BYTES - CTL_BYTES;
     static constexpr int NS = FREE / STAGE > 8 ? 8 : FREE / STAGE;  // key/value stages in the ring
     static constexpr int OFF_STAGE = 0;
     static constexpr int OFF_P = NS * STAGE;
-    static constexpr int OFF_CTL = OFF_P + NP * P_BYTES;
+    static constexpr int OFF_CTL = OFF_P + 2 * NP * P_BYTES;  // P double-buffered by tile parity
     // at least 120 KiB so two CTAs never share an SM (each takes all 512 tensor-memory columns)
     static constexpr int SMEM = OFF_CTL + CTL_BYTES > 120 * 1024 ? OFF_CTL + CTL_BYTES : 120 * 1024;
     static constexpr uint32_t TMEM_COLS = 512;
@@ -146,12 +146,15 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
     uint64_t* s_full = bars + 2 * NS;    // [2]
     uint64_t* s_empty = bars + 2 * NS + 2;  // [2]
     uint64_t* q_full = bars + 2 * NS + 4;
+    // [2] each: P of even / odd tiles written, value MMAs of even / odd tiles done.  One
+    // barrier per P buffer: the softmax reaches tile t's arrive only after tile t-2's value
+    // MMA completed, so no barrier ever runs two phases ahead of its waiter.
     uint64_t* p_full = bars + 2 * NS + 5;
-    uint64_t* o_done = bars + 2 * NS + 6;
-    uint64_t* fin = bars + 2 * NS + 7;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctl + 8 * (2 * NS + 8));
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(ctl + 8 * (2 * NS + 8) + 4);
-    uint32_t* bad_mask = reinterpret_cast<uint32_t*>(ctl + 8 * (2 * NS + 8) + 8);  // [NS] pages outside the cache
+    uint64_t* o_done = bars + 2 * NS + 7;
+    uint64_t* fin = bars + 2 * NS + 9;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctl + 8 * (2 * NS + 10));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(ctl + 8 * (2 * NS + 10) + 4);
+    uint32_t* bad_mask = reinterpret_cast<uint32_t*>(ctl + 8 * (2 * NS + 10) + 8);  // [NS] pages outside the cache
 
     const int n_ctx = (ctx + BN - 1) / BN;
     const int row_last = min(row0 + kPfxBM, rows_total) - 1;
@@ -167,8 +170,10 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
             mbar_init(&s_empty[i], 4);
         }
         mbar_init(q_full, 4);
-        mbar_init(p_full, 4);
-        mbar_init(o_done, 1);
+        mbar_init(&p_full[0], 4);
+        mbar_init(&p_full[1], 4);
+        mbar_init(&o_done[0], 1);
+        mbar_init(&o_done[1], 1);
         mbar_init(fin, 1);
         *abort_flag = 0;
         fence_mbar_init();
@@ -200,7 +205,18 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
     if (warp >= kPfxLoaderWarp0) {
         // ------------------------------------------------------------------ loaders
         const int lt = tid - kPfxLoaderWarp0 * 32;
+        const int npg = BN >> p.bs_log2;  // pages per context tile
+        // lane i < npg holds the block id of page i of a context tile (-1 past the context);
+        // the ids of tile t + 1 are loaded while tile t is waited for and issued
+        auto tile_page = [&](int t) {
+            int b = -1;
+            if (t < n_ctx && lane < npg && t * BN + (lane << p.bs_log2) < ctx) b = table[((t * BN) >> p.bs_log2) + lane];
+            return b;
+        };
+        int pid_next = tile_page(0);
         for (int t = 0; t < n_tiles; ++t) {
+            const int pid = pid_next;
+            pid_next = tile_page(t + 1);
             const int st = t % NS;
             if (t >= NS && !pfx_warp_wait(&kv_empty[st], ((t / NS) - 1) & 1, abort_flag, lane)) break;
             const uint32_t sK = sbase + C::OFF_STAGE + st * C::STAGE, sV = sK + C::K_BYTES;
@@ -209,9 +225,7 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
                 const int32_t* tile_table = table + (t0 >> p.bs_log2);
                 // pages of the tile whose id is outside the cache (masked); every loader warp
                 // computes the same mask, so all of them take the same path below
-                bool bad = false;
-                if (lane < (BN >> p.bs_log2) && t0 + (lane << p.bs_log2) < ctx)
-                    bad = (unsigned)tile_table[lane] >= (unsigned)p.num_blocks;
+                const bool bad = lane < npg && t0 + (lane << p.bs_log2) < ctx && (unsigned)pid >= (unsigned)p.num_blocks;
                 const uint32_t m = __ballot_sync(0xffffffffu, bad);
                 if (lt == 0) {
                     bad_mask[st] = m;
@@ -219,26 +233,24 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
                 }
                 if (m == 0 && t0 + BN <= ctx) {
                     // a full tile of valid pages: tensor copies straight into the MMA layouts,
-                    // one thread issues them; the other loader warps only arrive
-                    if (lt == 0) {
-                        mbar_arrive_expect_tx(&kv_full[st], 4u * BN * D);
-#pragma unroll 1
-                        for (int i = 0; i < BN / 8; ++i) {
-                            const int o0 = 8 * i;
-                            const int page = tile_table[o0 >> p.bs_log2] * p.Hk + kvh;
-                            tma_load_4d(sK + i * (C::DP * 16), &p.kmap, 0, (o0 & (p.bs - 1)) >> 3, 0, page,
+                    // issued by the lanes of the first loader warp (lane i: key box i, value
+                    // page i); the other loader warps only arrive
+                    if (lt < 32) {
+                        if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], 4u * BN * D);
+                        __syncwarp();
+                        const int kpage = __shfl_sync(0xffffffffu, pid, (8 * lane) >> p.bs_log2 & 31) * p.Hk + kvh;
+                        if (lane < BN / 8)
+                            tma_load_4d(sK + lane * (C::DP * 16), &p.kmap, 0, ((8 * lane) & (p.bs - 1)) >> 3, 0, kpage,
                                         &kv_full[st]);
-                        }
-#pragma unroll 1
-                        for (int pg = 0; pg < (BN >> p.bs_log2); ++pg) {
-                            const int page = tile_table[pg] * p.Hk + kvh;
-                            const uint32_t dst = sV + pg * (C::DP << (p.bs_log2 + 1));
+                        if (lane < npg) {
+                            const int vpage = pid * p.Hk + kvh;
+                            const uint32_t dst = sV + lane * (C::DP << (p.bs_log2 + 1));
                             if (p.bs_log2 == 3)
-                                bulk_load(dst, p.vcache + (int64_t)page * page_bytes, (uint32_t)page_bytes, &kv_full[st]);
+                                bulk_load(dst, p.vcache + (int64_t)vpage * page_bytes, (uint32_t)page_bytes, &kv_full[st]);
                             else
-                                tma_load_3d(dst, &p.vmap, 0, 0, page, &kv_full[st]);
+                                tma_load_3d(dst, &p.vmap, 0, 0, vpage, &kv_full[st]);
                         }
-                    } else if (lane == 0 && lt >= 32) {
+                    } else if (lane == 0) {
                         mbar_arrive(&kv_full[st]);
                     }
                     continue;
@@ -331,28 +343,30 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
                             : p.bs_log2 == 4 ? umma_desc_sw(sV + kk * (C::DP * 32), 256, 6)
                                              : umma_desc_sw(sV + (kk >> 1) * (C::DP * 64) + (kk & 1) * 32, 512, 4);
                         umma_f16(tm + C::COL_O,
-                                 umma_desc(sbase + C::OFF_P + h * C::P_BYTES + kk * 2 * (kPfxBM * 16), kPfxBM * 16, 128),
+                                 umma_desc(sbase + C::OFF_P + ((t & 1) * C::NP + h) * C::P_BYTES + kk * 2 * (kPfxBM * 16),
+                                           kPfxBM * 16, 128),
                                  vd, C::IDESC_O, (t > 0 || kk > 0 || h > 0) ? 1u : 0u);
                     }
-                umma_commit(o_done);
+                umma_commit(&o_done[t & 1]);
                 umma_commit(&kv_empty[t % NS]);
             };
             // Issue S of the next tile or P V of the oldest tile, whichever is ready first, so
-            // that a late copy never holds back the P V that frees its stage.
+            // that a late copy never holds back the P V that frees its stage.  S may run two
+            // tiles ahead of P V: its two buffers are guarded by s_empty alone.
             bool ok = pfx_wait(q_full, 0, abort_flag);
             if (ok) tc_fence_after();
             int next_s = 0, next_pv = 0;
             uint64_t t_idle = 0;
             while (ok && next_pv < n_tiles) {
                 bool issued = false;
-                if (next_s < n_tiles && next_s <= next_pv + 1 &&
+                if (next_s < n_tiles && next_s <= next_pv + 2 &&
                     mbar_test_wait(&kv_full[next_s % NS], (next_s / NS) & 1) &&
                     (next_s < 2 || mbar_test_wait(&s_empty[next_s & 1], ((next_s >> 1) - 1) & 1))) {
                     tc_fence_after();
                     issue_s(next_s++);
                     issued = true;
                 }
-                if (next_pv < next_s && mbar_test_wait(p_full, next_pv & 1)) {
+                if (next_pv < next_s && mbar_test_wait(&p_full[next_pv & 1], (next_pv >> 1) & 1)) {
                     tc_fence_after();
                     issue_pv(next_pv++);
                     issued = true;
@@ -367,8 +381,15 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
                     *abort_flag = 1;
                     prefix_flag(256u);
                     ok = false;
+                } else if (next_s < n_tiles && next_s <= next_pv + 2) {
+                    // sleep on the event expected next (the hardware wakes the thread when its
+                    // phase completes), at most ~300 ns, then look at both again
+                    if (!mbar_test_wait(&kv_full[next_s % NS], (next_s / NS) & 1))
+                        (void)mbar_try_wait_hint(&kv_full[next_s % NS], (next_s / NS) & 1, 300);
+                    else if (next_s >= 2)
+                        (void)mbar_try_wait_hint(&s_empty[next_s & 1], ((next_s >> 1) - 1) & 1, 300);
                 } else {
-                    __nanosleep(20);  // leave issue slots to the softmax warp on this SM quarter
+                    (void)mbar_try_wait_hint(&p_full[next_pv & 1], (next_pv >> 1) & 1, 300);
                 }
             }
             // every MMA issued has completed before tensor memory is released
@@ -382,7 +403,7 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
         const int row = row0 + r;
         const int lim = row / G;  // newest chunk key this row sees (rows past the chunk are never stored)
         const uint32_t tl = tm + ((uint32_t)(warp * 32) << 16);
-        const uint32_t sP = sbase + C::OFF_P + r * 16;
+        const uint32_t sP0 = sbase + C::OFF_P + r * 16;
         // this thread's query row into tensor memory (two 16-bit values per column; rows past
         // the chunk and the padding past D are zero)
         {
@@ -440,12 +461,11 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
                         if (i > lim_t) sv[i] = -INFINITY;
                 }
             }
-            float mt = -INFINITY;
+            // row max in the exp2 domain (scale > 0 commutes with max); four independent chains
+            float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int i = 0; i < BN; ++i) {
-                sv[i] *= p.sl2;
-                mt = fmaxf(mt, sv[i]);
-            }
+            for (int i = 0; i < BN; ++i) mx[i & 3] = fmaxf(mx[i & 3], sv[i]);
+            const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.sl2;
             const bool need = mt > m_ref + 8.f;
             float corr = 1.f;
             if (need) {
@@ -454,29 +474,32 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
                 l *= corr;
             }
             const float mu = m_ref == -INFINITY ? 0.f : m_ref;
-            float sum = 0.f;
+            float sum[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int i = 0; i < BN; ++i) {
-                sv[i] = ex2(sv[i] - mu);
-                sum += sv[i];
+                sv[i] = ex2(fmaf(sv[i], p.sl2, -mu));
+                sum[i & 3] += sv[i];
             }
-            l += sum;
-            if (t > 0) {
-                if (!(ok = pfx_warp_wait(o_done, (t - 1) & 1, abort_flag, lane))) break;
+            l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
+            // O must hold every earlier tile before it is rescaled; the P buffer of this tile's
+            // parity must have been read by the value MMA of tile t - 2
+            if (t > 0 && __any_sync(0xffffffffu, need)) {
+                if (!(ok = pfx_warp_wait(&o_done[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag, lane))) break;
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, need)) {
 #pragma unroll 1
-                    for (int c = 0; c < C::DPR / 32; ++c) {
-                        float o[32];
-                        tmem_ld32(tl + C::COL_O + c * 32, o);
-                        tmem_wait_ld();
+                for (int c = 0; c < C::DPR / 32; ++c) {
+                    float o[32];
+                    tmem_ld32(tl + C::COL_O + c * 32, o);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] *= corr;
-                        tmem_st32(tl + C::COL_O + c * 32, o);
-                    }
-                    tmem_wait_st();
+                    for (int e = 0; e < 32; ++e) o[e] *= corr;
+                    tmem_st32(tl + C::COL_O + c * 32, o);
                 }
+                tmem_wait_st();
+            } else if (t > 1) {
+                if (!(ok = pfx_warp_wait(&o_done[t & 1], ((t - 2) >> 1) & 1, abort_flag, lane))) break;
             }
+            const uint32_t sP = sP0 + (t & 1) * (C::NP * C::P_BYTES);
 #pragma unroll
             for (int kc = 0; kc < BN / 8; ++kc) {
                 uint32_t hi[4];
@@ -495,9 +518,9 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
+            if (lane == 0) mbar_arrive(&p_full[t & 1]);
         }
-        if (ok) ok = pfx_warp_wait(o_done, (n_tiles - 1) & 1, abort_flag, lane);
+        if (ok) ok = pfx_warp_wait(&o_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, abort_flag, lane);
         if (ok) {
             tc_fence_after();
             const float inv = 1.f / l;
