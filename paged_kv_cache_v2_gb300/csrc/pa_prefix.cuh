@@ -19,8 +19,9 @@
 //                  rows, per page one value box; a tile with the context's end, a page outside the
 //                  cache or the chunk's dense rows moves by 16-byte cp.async (zero-filling
 //                  what must not count; the dense value rows are transposed on the way).
-//   MMA lane       S = Q K^T (M 128, N BN) into one of two S buffers in tensor memory, then,
-//                  once the softmax has written P, O += P V (N = head size) into the O buffer.
+//   MMA lanes      one lane issues S = Q K^T (M 128, N BN, Q in tensor memory) into one of two
+//                  S buffers; another issues O += P V (N = head size) once the softmax has
+//                  written P (an MMA issue blocks its thread until the tensor core takes it).
 //   softmax warps  one thread per row: read the row of S from tensor memory, mask, exp2 with
 //                  a running reference max that only moves when the row max grows by more
 //                  than 2^8 (then O and the row sum are rescaled), write P (bf16 as hi + lo
@@ -151,10 +152,10 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
     // MMA completed, so no barrier ever runs two phases ahead of its waiter.
     uint64_t* p_full = bars + 2 * NS + 5;
     uint64_t* o_done = bars + 2 * NS + 7;
-    uint64_t* fin = bars + 2 * NS + 9;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctl + 8 * (2 * NS + 10));
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(ctl + 8 * (2 * NS + 10) + 4);
-    uint32_t* bad_mask = reinterpret_cast<uint32_t*>(ctl + 8 * (2 * NS + 10) + 8);  // [NS] pages outside the cache
+    uint64_t* fin = bars + 2 * NS + 9;  // [2]: every score / value MMA issued has completed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctl + 8 * (2 * NS + 11));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(ctl + 8 * (2 * NS + 11) + 4);
+    uint32_t* bad_mask = reinterpret_cast<uint32_t*>(ctl + 8 * (2 * NS + 11) + 8);  // [NS] pages outside the cache
 
     const int n_ctx = (ctx + BN - 1) / BN;
     const int row_last = min(row0 + kPfxBM, rows_total) - 1;
@@ -174,7 +175,8 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
         mbar_init(&p_full[1], 4);
         mbar_init(&o_done[0], 1);
         mbar_init(&o_done[1], 1);
-        mbar_init(fin, 1);
+        mbar_init(&fin[0], 1);
+        mbar_init(&fin[1], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -202,7 +204,7 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
     const int32_t* table = p.block_tables + (int64_t)s * p.mbps;
     const int64_t page_bytes = (int64_t)D * p.bs * 2;
 
-    if (warp >= kPfxLoaderWarp0) {
+    if (warp >= kPfxLoaderWarp0 && warp < kPfxPvWarp) {
         // ------------------------------------------------------------------ loaders
         const int lt = tid - kPfxLoaderWarp0 * 32;
         const int npg = BN >> p.bs_log2;  // pages per context tile
@@ -315,9 +317,16 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
         }
         cp_async_wait<0>();
     } else if (warp == kPfxMmaWarp) {
-        // ------------------------------------------------------------------ MMA issue
+        // ------------------------------------------------------------------ score MMAs
         if (lane == 0) {
-            auto issue_s = [&](int t) {
+            // S of tile t as soon as its keys are in and the softmax has read S of tile t - 2
+            // out of the same buffer
+            bool ok = pfx_wait(q_full, 0, abort_flag);
+            for (int t = 0; ok && t < n_tiles; ++t) {
+                ok = pfx_wait(&kv_full[t % NS], (t / NS) & 1, abort_flag) &&
+                     (t < 2 || pfx_wait(&s_empty[t & 1], ((t >> 1) - 1) & 1, abort_flag));
+                if (!ok) break;
+                tc_fence_after();
                 const uint32_t sK = sbase + C::OFF_STAGE + (t % NS) * C::STAGE;
                 const uint32_t d_s = tm + C::COL_S + (t & 1) * BN;
 #pragma unroll
@@ -329,8 +338,19 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
                         "r"(tm + C::COL_Q + ks * 8), "l"(kd), "r"(C::IDESC_S), "r"(ks > 0 ? 1u : 0u));
                 }
                 umma_commit(&s_full[t & 1]);
-            };
-            auto issue_pv = [&](int t) {
+            }
+            // every MMA issued has completed before tensor memory is released
+            umma_commit(&fin[0]);
+            if (!mbar_wait_bounded(&fin[0], 0, kWaitLimitNs)) prefix_flag(256u);
+        }
+        __syncwarp();
+    } else if (warp == kPfxPvWarp) {
+        // ------------------------------------------------------------------ value MMAs
+        if (lane == 0) {
+            bool ok = true;
+            for (int t = 0; ok && t < n_tiles; ++t) {
+                if (!(ok = pfx_wait(&p_full[t & 1], (t >> 1) & 1, abort_flag))) break;
+                tc_fence_after();
                 const uint32_t sV = sbase + C::OFF_STAGE + (t % NS) * C::STAGE + C::K_BYTES;
 #pragma unroll
                 for (int h = 0; h < C::NP; ++h)
@@ -347,54 +367,13 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
                                            kPfxBM * 16, 128),
                                  vd, C::IDESC_O, (t > 0 || kk > 0 || h > 0) ? 1u : 0u);
                     }
+                // the stage's keys were read by S of this tile, which completed before its
+                // softmax began, so the value MMA's completion frees the whole stage
                 umma_commit(&o_done[t & 1]);
                 umma_commit(&kv_empty[t % NS]);
-            };
-            // Issue S of the next tile or P V of the oldest tile, whichever is ready first, so
-            // that a late copy never holds back the P V that frees its stage.  S may run two
-            // tiles ahead of P V: its two buffers are guarded by s_empty alone.
-            bool ok = pfx_wait(q_full, 0, abort_flag);
-            if (ok) tc_fence_after();
-            int next_s = 0, next_pv = 0;
-            uint64_t t_idle = 0;
-            while (ok && next_pv < n_tiles) {
-                bool issued = false;
-                if (next_s < n_tiles && next_s <= next_pv + 2 &&
-                    mbar_test_wait(&kv_full[next_s % NS], (next_s / NS) & 1) &&
-                    (next_s < 2 || mbar_test_wait(&s_empty[next_s & 1], ((next_s >> 1) - 1) & 1))) {
-                    tc_fence_after();
-                    issue_s(next_s++);
-                    issued = true;
-                }
-                if (next_pv < next_s && mbar_test_wait(&p_full[next_pv & 1], (next_pv >> 1) & 1)) {
-                    tc_fence_after();
-                    issue_pv(next_pv++);
-                    issued = true;
-                }
-                if (issued) {
-                    t_idle = 0;
-                } else if (*abort_flag) {
-                    ok = false;
-                } else if (t_idle == 0) {
-                    t_idle = globaltimer_ns();
-                } else if (globaltimer_ns() - t_idle > kWaitLimitNs) {
-                    *abort_flag = 1;
-                    prefix_flag(256u);
-                    ok = false;
-                } else if (next_s < n_tiles && next_s <= next_pv + 2) {
-                    // sleep on the event expected next (the hardware wakes the thread when its
-                    // phase completes), at most ~300 ns, then look at both again
-                    if (!mbar_test_wait(&kv_full[next_s % NS], (next_s / NS) & 1))
-                        (void)mbar_try_wait_hint(&kv_full[next_s % NS], (next_s / NS) & 1, 300);
-                    else if (next_s >= 2)
-                        (void)mbar_try_wait_hint(&s_empty[next_s & 1], ((next_s >> 1) - 1) & 1, 300);
-                } else {
-                    (void)mbar_try_wait_hint(&p_full[next_pv & 1], (next_pv >> 1) & 1, 300);
-                }
             }
-            // every MMA issued has completed before tensor memory is released
-            umma_commit(fin);
-            if (!mbar_wait_bounded(fin, 0, kWaitLimitNs)) prefix_flag(256u);
+            umma_commit(&fin[1]);
+            if (!mbar_wait_bounded(&fin[1], 0, kWaitLimitNs)) prefix_flag(256u);
         }
         __syncwarp();
     } else {
