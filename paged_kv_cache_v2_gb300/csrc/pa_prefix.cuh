@@ -51,20 +51,26 @@ struct PfxCfg {
     static constexpr int STAGE = K_BYTES + V_BYTES;
     static constexpr int P_BYTES = kPfxBM * BN * 2;
     static constexpr int CTL_BYTES = 512;
-    static constexpr int FREE = 225 * 1024 - 2 * NP * P_BYTES - CTL_BYTES;
+    // P (two buffers by tile parity; bf16 as hi + lo) lives in tensor memory, as the A operand
+    // of the value MMA, wherever it fits next to the S buffers, O and Q; else in shared memory
+    static constexpr bool P_TMEM = 2 * BN + DPR + DP / 2 + 2 * NP * (BN / 2) <= 512;
+    static constexpr int P_SMEM = P_TMEM ? 0 : 2 * NP * P_BYTES;
+    static constexpr int FREE = 227 * 1024 - P_SMEM - CTL_BYTES;
     static constexpr int NS = FREE / STAGE > 8 ? 8 : FREE / STAGE;  // key/value stages in the ring
     static constexpr int OFF_STAGE = 0;
     static constexpr int OFF_P = NS * STAGE;
-    static constexpr int OFF_CTL = OFF_P + 2 * NP * P_BYTES;  // P double-buffered by tile parity
+    static constexpr int OFF_CTL = OFF_P + P_SMEM;
     // at least 120 KiB so two CTAs never share an SM (each takes all 512 tensor-memory columns)
     static constexpr int SMEM = OFF_CTL + CTL_BYTES > 120 * 1024 ? OFF_CTL + CTL_BYTES : 120 * 1024;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t COL_S = 0;         // two S buffers: columns [0, BN) and [BN, 2 BN)
     static constexpr uint32_t COL_O = 2 * BN;    // O: [2 BN, 2 BN + DPR)
     static constexpr uint32_t COL_Q = 2 * BN + DPR;  // Q, two 16-bit values per column: DP / 2
+    static constexpr uint32_t COL_P = COL_Q + DP / 2;  // P buffer b, term h: + (b NP + h) BN / 2
     static constexpr uint32_t IDESC_S = umma_idesc_f16(BF16, kPfxBM, BN);
     static constexpr uint32_t IDESC_O = umma_idesc_f16(BF16, kPfxBM, DP);
     static_assert(COL_Q + DP / 2 <= TMEM_COLS, "tensor memory");
+    static_assert(!P_TMEM || COL_P + 2 * NP * (BN / 2) <= TMEM_COLS, "tensor memory");
     static_assert(NS >= 2 && SMEM <= 227 * 1024, "shared memory");
 };
 
@@ -362,10 +368,19 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
                             p.bs_log2 == 3   ? umma_desc(sV + kk * 2 * (C::DP * 16), C::DP * 16, 128)
                             : p.bs_log2 == 4 ? umma_desc_sw(sV + kk * (C::DP * 32), 256, 6)
                                              : umma_desc_sw(sV + (kk >> 1) * (C::DP * 64) + (kk & 1) * 32, 512, 4);
-                        umma_f16(tm + C::COL_O,
-                                 umma_desc(sbase + C::OFF_P + ((t & 1) * C::NP + h) * C::P_BYTES + kk * 2 * (kPfxBM * 16),
-                                           kPfxBM * 16, 128),
-                                 vd, C::IDESC_O, (t > 0 || kk > 0 || h > 0) ? 1u : 0u);
+                        const uint32_t acc = (t > 0 || kk > 0 || h > 0) ? 1u : 0u;
+                        if constexpr (C::P_TMEM) {
+                            asm volatile(
+                                "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+                                "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(tm + C::COL_O),
+                                "r"(tm + C::COL_P + ((t & 1) * C::NP + h) * (BN / 2) + kk * 8), "l"(vd),
+                                "r"(C::IDESC_O), "r"(acc));
+                        } else {
+                            umma_f16(tm + C::COL_O,
+                                     umma_desc(sbase + C::OFF_P + ((t & 1) * C::NP + h) * C::P_BYTES + kk * 2 * (kPfxBM * 16),
+                                               kPfxBM * 16, 128),
+                                     vd, C::IDESC_O, acc);
+                        }
                     }
                 // the stage's keys were read by S of this tile, which completed before its
                 // softmax began, so the value MMA's completion frees the whole stage
@@ -478,23 +493,40 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
             } else if (t > 1) {
                 if (!(ok = pfx_warp_wait(&o_done[t & 1], ((t - 2) >> 1) & 1, abort_flag, lane))) break;
             }
-            const uint32_t sP = sP0 + (t & 1) * (C::NP * C::P_BYTES);
+            if constexpr (C::P_TMEM) {
+                // P row as packed 16-bit pairs into this lane's P columns (bf16: hi, then lo)
+                float hi[BN / 2], lo[BN / 2];
 #pragma unroll
-            for (int kc = 0; kc < BN / 8; ++kc) {
-                uint32_t hi[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) hi[e] = pack2<BF16>(sv[kc * 8 + 2 * e], sv[kc * 8 + 2 * e + 1]);
-                sts_v4(sP + kc * (kPfxBM * 16), hi[0], hi[1], hi[2], hi[3]);
-                if constexpr (BF16) {
-                    uint32_t lo[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        lo[e] = pack2<BF16>(sv[kc * 8 + 2 * e] - __uint_as_float(hi[e] << 16),
-                                            sv[kc * 8 + 2 * e + 1] - __uint_as_float(hi[e] & 0xffff0000u));
-                    sts_v4(sP + C::P_BYTES + kc * (kPfxBM * 16), lo[0], lo[1], lo[2], lo[3]);
+                for (int e = 0; e < BN / 2; ++e) {
+                    const uint32_t h2 = pack2<BF16>(sv[2 * e], sv[2 * e + 1]);
+                    hi[e] = __uint_as_float(h2);
+                    if constexpr (BF16)
+                        lo[e] = __uint_as_float(pack2<BF16>(sv[2 * e] - __uint_as_float(h2 << 16),
+                                                            sv[2 * e + 1] - __uint_as_float(h2 & 0xffff0000u)));
                 }
+                const uint32_t tp = tl + C::COL_P + (t & 1) * C::NP * (BN / 2);
+                tmem_st32(tp, *reinterpret_cast<const float(*)[32]>(&hi[0]));
+                if constexpr (BF16) tmem_st32(tp + BN / 2, *reinterpret_cast<const float(*)[32]>(&lo[0]));
+                tmem_wait_st();
+            } else {
+                const uint32_t sP = sP0 + (t & 1) * (C::NP * C::P_BYTES);
+#pragma unroll
+                for (int kc = 0; kc < BN / 8; ++kc) {
+                    uint32_t hi[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) hi[e] = pack2<BF16>(sv[kc * 8 + 2 * e], sv[kc * 8 + 2 * e + 1]);
+                    sts_v4(sP + kc * (kPfxBM * 16), hi[0], hi[1], hi[2], hi[3]);
+                    if constexpr (BF16) {
+                        uint32_t lo[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            lo[e] = pack2<BF16>(sv[kc * 8 + 2 * e] - __uint_as_float(hi[e] << 16),
+                                                sv[kc * 8 + 2 * e + 1] - __uint_as_float(hi[e] & 0xffff0000u));
+                        sts_v4(sP + C::P_BYTES + kc * (kPfxBM * 16), lo[0], lo[1], lo[2], lo[3]);
+                    }
+                }
+                fence_proxy_async_smem();
             }
-            fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[t & 1]);
