@@ -36,6 +36,9 @@
 #include "pa_prefix.h"
 #include "pa_tc.cuh"
 
+#ifndef PA_PFX_KEY_SHARE
+#define PA_PFX_KEY_SHARE 4
+#endif
 namespace pa {
 
 template <bool BF16, int D>
@@ -45,33 +48,42 @@ struct PfxCfg {
     static constexpr int NCR = D / 8;              // 16-byte chunks of a row that exist
     static constexpr int NCP = DP / 8;             // chunks after padding
     static constexpr int BN = 64;                  // keys per tile
-    static constexpr int NP = BF16 ? 2 : 1;        // P buffers: hi (and lo for bf16)
-    static constexpr int K_BYTES = BN * DP * 2;
+    static constexpr int NP = BF16 ? 2 : 1;        // P terms: hi (and lo for bf16)
+    static constexpr int K_BYTES = BN * DP * 2;    // a key tile; a value tile is as large
     static constexpr int V_BYTES = BN * DP * 2;
-    static constexpr int STAGE = K_BYTES + V_BYTES;
     static constexpr int P_BYTES = kPfxBM * BN * 2;
     static constexpr int CTL_BYTES = 512;
-    // P (two buffers by tile parity; bf16 as hi + lo) lives in tensor memory, as the A operand
-    // of the value MMA, wherever it fits next to the S buffers, O and Q; else in shared memory
-    static constexpr bool P_TMEM = 2 * BN + DPR + DP / 2 + 2 * NP * (BN / 2) <= 512;
+    // Tensor memory: S buffers, O, Q and (where they fit) the two P buffers, the A operand of
+    // the value MMA.  Two S buffers with P in tensor memory, else one S buffer with P in
+    // tensor memory, else two S buffers with P in shared memory.
+    static constexpr int TM_OQ = DPR + DP / 2, TM_P = 2 * NP * (BN / 2);
+    static constexpr bool FIT2 = 2 * BN + TM_OQ + TM_P <= 512;
+    static constexpr bool FIT1 = BN + TM_OQ + TM_P <= 512;
+    static constexpr bool P_TMEM = FIT2 || FIT1;
+    static constexpr int NSB = FIT2 ? 2 : (FIT1 ? 1 : 2);  // S buffers
     static constexpr int P_SMEM = P_TMEM ? 0 : 2 * NP * P_BYTES;
-    static constexpr int FREE = 227 * 1024 - P_SMEM - CTL_BYTES;
-    static constexpr int NS = FREE / STAGE > 8 ? 8 : FREE / STAGE;  // key/value stages in the ring
-    static constexpr int OFF_STAGE = 0;
-    static constexpr int OFF_P = NS * STAGE;
+    // Separate key and value rings: a key slot is free once the score MMA (and the softmax's
+    // look at the tile's masks) is done, a value slot only after the value MMA.
+    static constexpr int SLOTS = (227 * 1024 - P_SMEM - CTL_BYTES) / K_BYTES;
+    static constexpr int NK0 = SLOTS * PA_PFX_KEY_SHARE / 8;  // key share of the slots (in eighths)
+    static constexpr int NK = NK0 > 8 ? 8 : (NK0 < 2 ? 2 : NK0);
+    static constexpr int NV = SLOTS - NK > 8 ? 8 : SLOTS - NK;
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = NK * K_BYTES;
+    static constexpr int OFF_P = OFF_V + NV * V_BYTES;
     static constexpr int OFF_CTL = OFF_P + P_SMEM;
     // at least 120 KiB so two CTAs never share an SM (each takes all 512 tensor-memory columns)
     static constexpr int SMEM = OFF_CTL + CTL_BYTES > 120 * 1024 ? OFF_CTL + CTL_BYTES : 120 * 1024;
     static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t COL_S = 0;         // two S buffers: columns [0, BN) and [BN, 2 BN)
-    static constexpr uint32_t COL_O = 2 * BN;    // O: [2 BN, 2 BN + DPR)
-    static constexpr uint32_t COL_Q = 2 * BN + DPR;  // Q, two 16-bit values per column: DP / 2
-    static constexpr uint32_t COL_P = COL_Q + DP / 2;  // P buffer b, term h: + (b NP + h) BN / 2
+    static constexpr uint32_t COL_S = 0;                 // S buffer b: [b BN, (b + 1) BN)
+    static constexpr uint32_t COL_O = NSB * BN;          // O: [COL_O, COL_O + DPR)
+    static constexpr uint32_t COL_Q = COL_O + DPR;       // Q, two 16-bit values per column: DP / 2
+    static constexpr uint32_t COL_P = COL_Q + DP / 2;    // P buffer b, term h: + (b NP + h) BN / 2
     static constexpr uint32_t IDESC_S = umma_idesc_f16(BF16, kPfxBM, BN);
     static constexpr uint32_t IDESC_O = umma_idesc_f16(BF16, kPfxBM, DP);
     static_assert(COL_Q + DP / 2 <= TMEM_COLS, "tensor memory");
-    static_assert(!P_TMEM || COL_P + 2 * NP * (BN / 2) <= TMEM_COLS, "tensor memory");
-    static_assert(NS >= 2 && SMEM <= 227 * 1024, "shared memory");
+    static_assert(!P_TMEM || COL_P + TM_P <= TMEM_COLS, "tensor memory");
+    static_assert(NV >= 2 && SMEM <= 227 * 1024, "shared memory");
 };
 
 #ifndef PA_PFX_WAIT_HINT_NS
@@ -121,7 +133,7 @@ __device__ __forceinline__ bool pfx_warp_wait(uint64_t* bar, uint32_t parity, vo
 template <bool BF16, int D>
 __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_constant__ PrefixParams p) {
     using C = PfxCfg<BF16, D>;
-    constexpr int BN = C::BN, NS = C::NS;
+    constexpr int BN = C::BN, NK = C::NK, NV = C::NV, NSB = C::NSB;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int s = blockIdx.z, kvh = blockIdx.y;
@@ -148,56 +160,68 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
     }
     uint8_t* ctl = smem + C::OFF_CTL;
     uint64_t* bars = reinterpret_cast<uint64_t*>(ctl);
-    uint64_t* kv_full = bars;            // [NS]
-    uint64_t* kv_empty = bars + NS;      // [NS]
-    uint64_t* s_full = bars + 2 * NS;    // [2]
-    uint64_t* s_empty = bars + 2 * NS + 2;  // [2]
-    uint64_t* q_full = bars + 2 * NS + 4;
+    uint64_t* k_full = bars;                 // [NK] keys (and the tile's page mask) in place
+    uint64_t* k_empty = k_full + NK;         // [NK] score MMA done and masks read
+    uint64_t* v_full = k_empty + NK;         // [NV] values in place
+    uint64_t* v_empty = v_full + NV;         // [NV] value MMA done
+    uint64_t* s_full = v_empty + NV;         // [NSB]
+    uint64_t* s_empty = s_full + NSB;        // [NSB]
+    uint64_t* q_full = s_empty + NSB;
     // [2] each: P of even / odd tiles written, value MMAs of even / odd tiles done.  One
     // barrier per P buffer: the softmax reaches tile t's arrive only after tile t-2's value
     // MMA completed, so no barrier ever runs two phases ahead of its waiter.
-    uint64_t* p_full = bars + 2 * NS + 5;
-    uint64_t* o_done = bars + 2 * NS + 7;
-    uint64_t* fin = bars + 2 * NS + 9;  // [2]: every score / value MMA issued has completed
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctl + 8 * (2 * NS + 11));
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(ctl + 8 * (2 * NS + 11) + 4);
-    uint32_t* bad_mask = reinterpret_cast<uint32_t*>(ctl + 8 * (2 * NS + 11) + 8);  // [NS] pages outside the cache
+    uint64_t* p_full = q_full + 1;
+    uint64_t* o_done = p_full + 2;
+    uint64_t* fin = o_done + 2;  // [2]: every score / value MMA issued has completed
+    constexpr int NBARS = 2 * NK + 2 * NV + 2 * NSB + 7;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctl + 8 * NBARS);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(ctl + 8 * NBARS + 4);
+    uint32_t* bad_mask = reinterpret_cast<uint32_t*>(ctl + 8 * NBARS + 8);  // [NK] pages outside the cache
+    static_assert(8 * NBARS + 8 + 4 * NK <= C::CTL_BYTES, "control block");
 
     const int n_ctx = (ctx + BN - 1) / BN;
     const int row_last = min(row0 + kPfxBM, rows_total) - 1;
     const int n_tiles = n_ctx + (row_last / G) / BN + 1;
 
     if (tid == 0) {
-        for (int i = 0; i < NS; ++i) {
-            mbar_init(&kv_full[i], 4);
-            mbar_init(&kv_empty[i], 1);
+        for (int i = 0; i < NK; ++i) {
+            mbar_init(&k_full[i], 3);   // the key-copy arrive (+ bytes) and the two key warps
+            mbar_init(&k_empty[i], 5);  // the score MMA's commit and the four softmax warps
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < NV; ++i) {
+            mbar_init(&v_full[i], 3);   // the value-copy arrive (+ bytes) and the two value warps
+            mbar_init(&v_empty[i], 1);
+        }
+        for (int i = 0; i < NSB; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&s_empty[i], 4);
         }
         mbar_init(q_full, 4);
-        mbar_init(&p_full[0], 4);
-        mbar_init(&p_full[1], 4);
-        mbar_init(&o_done[0], 1);
-        mbar_init(&o_done[1], 1);
-        mbar_init(&fin[0], 1);
-        mbar_init(&fin[1], 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&p_full[i], 4);
+            mbar_init(&o_done[i], 1);
+            mbar_init(&fin[i], 1);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
-    // Padding the copies never write: key chunks c >= D/8 and value rows d >= D, every stage.
+    // Padding the copies never write: key chunks c >= D/8 of every key slot, value rows d >= D
+    // of every value slot.
     if constexpr (C::NCP > C::NCR) {
         constexpr int kpad = (C::NCP - C::NCR) * BN, vpad = (BN / 8) * (C::DP - D);
-        for (int i = tid; i < NS * (kpad + vpad); i += kPfxThreads) {
-            const int st = i / (kpad + vpad), rem = i % (kpad + vpad);
-            uint8_t* stage = smem + C::OFF_STAGE + st * C::STAGE;
-            const int o = rem % BN, c = C::NCR + rem / BN;
-            const int kc = (rem - kpad) / (C::DP - D), dd = D + (rem - kpad) % (C::DP - D);
-            const int cpp_log2 = p.bs_log2 - 3;  // 16-byte chunks per value row, log2
-            uint8_t* dst = rem < kpad ? stage + (o >> 3) * (C::DP * 16) + c * 128 + (o & 7) * 16
-                                      : stage + C::K_BYTES + (kc >> cpp_log2) * (C::DP << (p.bs_log2 + 1)) +
-                                            (dd << (p.bs_log2 + 1)) + ((kc & ((1 << cpp_log2) - 1)) << 4);
+        for (int i = tid; i < NK * kpad + NV * vpad; i += kPfxThreads) {
+            uint8_t* dst;
+            if (i < NK * kpad) {
+                const int slot = i / kpad, rem = i % kpad;
+                const int o = rem % BN, c = C::NCR + rem / BN;
+                dst = smem + C::OFF_K + slot * C::K_BYTES + (o >> 3) * (C::DP * 16) + c * 128 + (o & 7) * 16;
+            } else {
+                const int j = i - NK * kpad, slot = j / vpad, rem = j % vpad;
+                const int kc = rem / (C::DP - D), dd = D + rem % (C::DP - D);
+                const int cpp_log2 = p.bs_log2 - 3;  // 16-byte chunks per value row, log2
+                dst = smem + C::OFF_V + slot * C::V_BYTES + (kc >> cpp_log2) * (C::DP << (p.bs_log2 + 1)) +
+                      (dd << (p.bs_log2 + 1)) + ((kc & ((1 << cpp_log2) - 1)) << 4);
+            }
             *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
         }
     }
@@ -212,7 +236,9 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
 
     if (warp >= kPfxLoaderWarp0 && warp < kPfxPvWarp) {
         // ------------------------------------------------------------------ loaders
-        const int lt = tid - kPfxLoaderWarp0 * 32;
+        // warps 5-6 fill the key ring, warps 7-8 the value ring; each team runs on its own
+        const bool kteam = warp < kPfxLoaderWarp0 + 2;
+        const int lt = tid - (kteam ? kPfxLoaderWarp0 : kPfxLoaderWarp0 + 2) * 32;  // 0 .. 63 in the team
         const int npg = BN >> p.bs_log2;  // pages per context tile
         // lane i < npg holds the block id of page i of a context tile (-1 past the context);
         // the ids of tile t + 1 are loaded while tile t is waited for and issued
@@ -225,116 +251,153 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
         for (int t = 0; t < n_tiles; ++t) {
             const int pid = pid_next;
             pid_next = tile_page(t + 1);
-            const int st = t % NS;
-            if (t >= NS && !pfx_warp_wait(&kv_empty[st], ((t / NS) - 1) & 1, abort_flag, lane)) break;
-            const uint32_t sK = sbase + C::OFF_STAGE + st * C::STAGE, sV = sK + C::K_BYTES;
+            const int slot = kteam ? t % NK : t % NV;
+            uint64_t* full = kteam ? &k_full[slot] : &v_full[slot];
+            if (kteam ? t >= NK : t >= NV) {
+                if (!pfx_warp_wait(kteam ? &k_empty[slot] : &v_empty[slot], ((t / (kteam ? NK : NV)) - 1) & 1,
+                                   abort_flag, lane))
+                    break;
+            }
+            const uint32_t sK = sbase + C::OFF_K + slot * C::K_BYTES;
+            const uint32_t sV = sbase + C::OFF_V + slot * C::V_BYTES;
             if (t < n_ctx) {
                 const int t0 = t * BN;
-                const int32_t* tile_table = table + (t0 >> p.bs_log2);
-                // pages of the tile whose id is outside the cache (masked); every loader warp
-                // computes the same mask, so all of them take the same path below
+                // pages of the tile whose id is outside the cache (masked); both teams compute
+                // the same mask
                 const bool bad = lane < npg && t0 + (lane << p.bs_log2) < ctx && (unsigned)pid >= (unsigned)p.num_blocks;
                 const uint32_t m = __ballot_sync(0xffffffffu, bad);
-                if (lt == 0) {
-                    bad_mask[st] = m;
-                    if (m) prefix_flag(32u);
-                }
-                if (m == 0 && t0 + BN <= ctx) {
-                    // a full tile of valid pages: tensor copies straight into the MMA layouts,
-                    // issued by the lanes of the first loader warp (lane i: key box i, value
-                    // page i); the other loader warps only arrive
-                    if (lt < 32) {
-                        if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], 4u * BN * D);
-                        __syncwarp();
+                const bool tma = m == 0 && t0 + BN <= ctx;  // a full tile of valid pages
+                if (lt < 32) {
+                    if (lane == 0) {
+                        if (kteam) {
+                            bad_mask[slot] = m;
+                            if (m) prefix_flag(32u);
+                        }
+                        if (tma)
+                            mbar_arrive_expect_tx(full, 2u * BN * D);
+                        else
+                            mbar_arrive(full);
+                    }
+                    __syncwarp();
+                    if (tma && kteam) {
+                        // keys: tensor copies of 128-byte rows, one box of 8 tokens per lane
                         const int kpage = __shfl_sync(0xffffffffu, pid, (8 * lane) >> p.bs_log2 & 31) * p.Hk + kvh;
                         if (lane < BN / 8)
                             tma_load_4d(sK + lane * (C::DP * 16), &p.kmap, 0, ((8 * lane) & (p.bs - 1)) >> 3, 0, kpage,
-                                        &kv_full[st]);
-                        if (lane < npg) {
-                            const int vpage = pid * p.Hk + kvh;
-                            const uint32_t dst = sV + lane * (C::DP << (p.bs_log2 + 1));
-                            if (p.bs_log2 == 3)
-                                bulk_load(dst, p.vcache + (int64_t)vpage * page_bytes, (uint32_t)page_bytes, &kv_full[st]);
-                            else
-                                tma_load_3d(dst, &p.vmap, 0, 0, vpage, &kv_full[st]);
-                        }
-                    } else if (lane == 0) {
-                        mbar_arrive(&kv_full[st]);
+                                        full);
+                    } else if (tma && lane < npg) {
+                        // values: one whole page per lane, swizzled as the value MMA reads it
+                        const int vpage = pid * p.Hk + kvh;
+                        const uint32_t dst = sV + lane * (C::DP << (p.bs_log2 + 1));
+                        if (p.bs_log2 == 3)
+                            bulk_load(dst, p.vcache + (int64_t)vpage * page_bytes, (uint32_t)page_bytes, full);
+                        else
+                            tma_load_3d(dst, &p.vmap, 0, 0, vpage, full);
                     }
-                    continue;
                 }
-                // keys: page-local order, so global reads and shared writes are both contiguous
-                const int kper = C::NCR << p.bs_log2;
-                for (int i = lt; i < BN * C::NCR; i += kPfxLoaderThreads) {
-                    const int pg = i / kper, rem = i - pg * kper;
-                    const int c = rem >> p.bs_log2, slot = rem & (p.bs - 1);
-                    const int o = (pg << p.bs_log2) + slot;
-                    const int b = t0 + o < ctx ? tile_table[pg] : -1;
-                    const bool ok = (unsigned)b < (unsigned)p.num_blocks;
-                    const uint8_t* src =
-                        ok ? p.kcache + ((int64_t)b * p.Hk + kvh) * page_bytes + (int64_t)(c * p.bs + slot) * 16 : p.kcache;
-                    cp_async16(sK + (o >> 3) * (C::DP * 16) + c * 128 + (o & 7) * 16, src, ok ? 16u : 0u);
-                }
-                // values: 8-token pieces of each page row; the part past the context reads as zero
-                const int kpp_log2 = p.bs_log2 - 3;
-                const int vper = D << kpp_log2;
-                for (int i = lt; i < (BN / 8) * D; i += kPfxLoaderThreads) {
-                    const int pg = i / vper, rem = i - pg * vper;
-                    const int dd = rem >> kpp_log2, kq = rem & ((1 << kpp_log2) - 1);
-                    const int o = (pg << p.bs_log2) + kq * 8;
-                    const int nv = min(max(ctx - t0 - o, 0), 8);
-                    const int b = nv > 0 ? tile_table[pg] : -1;
-                    const bool ok = (unsigned)b < (unsigned)p.num_blocks;
-                    const uint8_t* src = ok ? p.vcache + ((int64_t)b * p.Hk + kvh) * page_bytes +
-                                                  ((int64_t)dd * p.bs + kq * 8) * 2
-                                            : p.vcache;
-                    cp_async16(sV + pfx_v_off(o, dd, p.bs_log2, C::DP), src, ok ? (uint32_t)nv * 2u : 0u);
+                if (!tma && kteam) {
+                    // keys of the context's last tile or of a tile with a page outside the cache:
+                    // 16-byte pieces, past the context or of a masked page zero-filled
+                    const int kper = C::NCR << p.bs_log2;
+                    for (int base = 0; base < BN * C::NCR; base += 64) {
+                        const int i = base + lt;
+                        const bool act = i < BN * C::NCR;
+                        const int pg = act ? i / kper : 0, rem = i - pg * kper;
+                        const int b = __shfl_sync(0xffffffffu, pid, pg);
+                        if (act) {
+                            const int c = rem >> p.bs_log2, sl = rem & (p.bs - 1);
+                            const int o = (pg << p.bs_log2) + sl;
+                            const bool ok = t0 + o < ctx && (unsigned)b < (unsigned)p.num_blocks;
+                            const uint8_t* src = ok ? p.kcache + ((int64_t)b * p.Hk + kvh) * page_bytes +
+                                                          (int64_t)(c * p.bs + sl) * 16
+                                                    : p.kcache;
+                            cp_async16(sK + (o >> 3) * (C::DP * 16) + c * 128 + (o & 7) * 16, src, ok ? 16u : 0u);
+                        }
+                    }
+                } else if (!tma) {
+                    // values: 8-key pieces of each page row; the part past the context or of a
+                    // masked page reads as zero
+                    const int kpp_log2 = p.bs_log2 - 3;
+                    const int vper = D << kpp_log2;
+                    for (int base = 0; base < (BN / 8) * D; base += 64) {
+                        const int i = base + lt;
+                        const bool act = i < (BN / 8) * D;
+                        const int pg = act ? i / vper : 0, rem = i - pg * vper;
+                        const int b = __shfl_sync(0xffffffffu, pid, pg);
+                        if (act) {
+                            const int dd = rem >> kpp_log2, kq = rem & ((1 << kpp_log2) - 1);
+                            const int o = (pg << p.bs_log2) + kq * 8;
+                            const int nv = min(max(ctx - t0 - o, 0), 8);
+                            const bool ok = nv > 0 && (unsigned)b < (unsigned)p.num_blocks;
+                            const uint8_t* src = ok ? p.vcache + ((int64_t)b * p.Hk + kvh) * page_bytes +
+                                                          ((int64_t)dd * p.bs + kq * 8) * 2
+                                                    : p.vcache;
+                            cp_async16(sV + pfx_v_off(o, dd, p.bs_log2, C::DP), src, ok ? (uint32_t)nv * 2u : 0u);
+                        }
+                    }
                 }
             } else {
                 const int kc0 = (t - n_ctx) * BN;
-                for (int i = lt; i < BN * C::NCR; i += kPfxLoaderThreads) {
-                    const int c = i / BN, o = i % BN;
-                    const int j = kc0 + o;
-                    const bool ok = j < q_len;
-                    const uint8_t* src =
-                        ok ? p.k + ((int64_t)(q0 + j) * p.kv_stride + (int64_t)kvh * D + c * 8) * 2 : p.k;
-                    cp_async16(sK + (o >> 3) * (C::DP * 16) + c * 128 + (o & 7) * 16, src, ok ? 16u : 0u);
-                }
-                // dense value rows, two tokens at a time, transposed into the value layout
-                for (int i = lt; i < (BN / 2) * C::NCR; i += kPfxLoaderThreads) {
-                    const int c = i % C::NCR, t2 = 2 * (i / C::NCR);
-                    const int j = kc0 + t2;
-                    const uint8_t* base = p.v + ((int64_t)kvh * D + c * 8) * 2;
-                    uint4 a = make_uint4(0u, 0u, 0u, 0u), b = make_uint4(0u, 0u, 0u, 0u);
-                    if (j < q_len) a = ld_nc_v4(base + (int64_t)(q0 + j) * p.kv_stride * 2);
-                    if (j + 1 < q_len) b = ld_nc_v4(base + (int64_t)(q0 + j + 1) * p.kv_stride * 2);
-                    const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+                if (lt == 0) mbar_arrive(full);  // no tensor copies for chunk tiles
+                if (kteam) {
+                    for (int i = lt; i < BN * C::NCR; i += 64) {
+                        const int c = i / BN, o = i % BN;
+                        const int j = kc0 + o;
+                        const bool ok = j < q_len;
+                        const uint8_t* src =
+                            ok ? p.k + ((int64_t)(q0 + j) * p.kv_stride + (int64_t)kvh * D + c * 8) * 2 : p.k;
+                        cp_async16(sK + (o >> 3) * (C::DP * 16) + c * 128 + (o & 7) * 16, src, ok ? 16u : 0u);
+                    }
+                } else {
+                    // dense value rows, two tokens at a time, transposed into the value layout;
+                    // the loads of four such pieces are in flight together
+                    constexpr int ITEMS = (BN / 2) * C::NCR, BATCH = 4;
+                    for (int i0 = 0; i0 < ITEMS; i0 += 64 * BATCH) {
+                        uint4 a[BATCH], b[BATCH];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        sts_u32(sV + pfx_v_off(t2, c * 8 + e, p.bs_log2, C::DP) + (t2 & 7) * 2,
-                                __byte_perm(av[e >> 1], bv[e >> 1], (e & 1) ? 0x7632 : 0x5410));
+                        for (int u = 0; u < BATCH; ++u) {
+                            const int i = i0 + u * 64 + lt;
+                            const int c = i % C::NCR, t2 = 2 * (i / C::NCR), j = kc0 + t2;
+                            const uint8_t* vb = p.v + ((int64_t)kvh * D + c * 8) * 2;
+                            a[u] = b[u] = make_uint4(0u, 0u, 0u, 0u);
+                            if (i < ITEMS && j < q_len) a[u] = ld_nc_v4(vb + (int64_t)(q0 + j) * p.kv_stride * 2);
+                            if (i < ITEMS && j + 1 < q_len) b[u] = ld_nc_v4(vb + (int64_t)(q0 + j + 1) * p.kv_stride * 2);
+                        }
+#pragma unroll
+                        for (int u = 0; u < BATCH; ++u) {
+                            const int i = i0 + u * 64 + lt;
+                            if (i >= ITEMS) continue;
+                            const int c = i % C::NCR, t2 = 2 * (i / C::NCR);
+                            const uint32_t av[4] = {a[u].x, a[u].y, a[u].z, a[u].w};
+                            const uint32_t bv[4] = {b[u].x, b[u].y, b[u].z, b[u].w};
+#pragma unroll
+                            for (int e = 0; e < 8; ++e)
+                                sts_u32(sV + pfx_v_off(t2, c * 8 + e, p.bs_log2, C::DP) + (t2 & 7) * 2,
+                                        __byte_perm(av[e >> 1], bv[e >> 1], (e & 1) ? 0x7632 : 0x5410));
+                        }
+                    }
                 }
             }
             cp_async_commit();
             cp_async_wait<0>();
             fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&kv_full[st]);
+            if (lane == 0) mbar_arrive(full);
         }
         cp_async_wait<0>();
     } else if (warp == kPfxMmaWarp) {
         // ------------------------------------------------------------------ score MMAs
         if (lane == 0) {
-            // S of tile t as soon as its keys are in and the softmax has read S of tile t - 2
-            // out of the same buffer
+            // S of tile t as soon as its keys are in and the softmax has read S of tile
+            // t - NSB out of the same buffer
             bool ok = pfx_wait(q_full, 0, abort_flag);
             for (int t = 0; ok && t < n_tiles; ++t) {
-                ok = pfx_wait(&kv_full[t % NS], (t / NS) & 1, abort_flag) &&
-                     (t < 2 || pfx_wait(&s_empty[t & 1], ((t >> 1) - 1) & 1, abort_flag));
+                ok = pfx_wait(&k_full[t % NK], (t / NK) & 1, abort_flag) &&
+                     (t < NSB || pfx_wait(&s_empty[t % NSB], ((t / NSB) - 1) & 1, abort_flag));
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t sK = sbase + C::OFF_STAGE + (t % NS) * C::STAGE;
-                const uint32_t d_s = tm + C::COL_S + (t & 1) * BN;
+                const uint32_t sK = sbase + C::OFF_K + (t % NK) * C::K_BYTES;
+                const uint32_t d_s = tm + C::COL_S + (t % NSB) * BN;
 #pragma unroll
                 for (int ks = 0; ks < C::DP / 16; ++ks) {
                     const uint64_t kd = umma_desc(sK + ks * 2 * 128, 128, C::DP * 16);
@@ -343,7 +406,8 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
                         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_s),
                         "r"(tm + C::COL_Q + ks * 8), "l"(kd), "r"(C::IDESC_S), "r"(ks > 0 ? 1u : 0u));
                 }
-                umma_commit(&s_full[t & 1]);
+                umma_commit(&s_full[t % NSB]);
+                umma_commit(&k_empty[t % NK]);
             }
             // every MMA issued has completed before tensor memory is released
             umma_commit(&fin[0]);
@@ -355,9 +419,10 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
         if (lane == 0) {
             bool ok = true;
             for (int t = 0; ok && t < n_tiles; ++t) {
-                if (!(ok = pfx_wait(&p_full[t & 1], (t >> 1) & 1, abort_flag))) break;
+                ok = pfx_wait(&p_full[t & 1], (t >> 1) & 1, abort_flag) && pfx_wait(&v_full[t % NV], (t / NV) & 1, abort_flag);
+                if (!ok) break;
                 tc_fence_after();
-                const uint32_t sV = sbase + C::OFF_STAGE + (t % NS) * C::STAGE + C::K_BYTES;
+                const uint32_t sV = sbase + C::OFF_V + (t % NV) * C::V_BYTES;
 #pragma unroll
                 for (int h = 0; h < C::NP; ++h)
 #pragma unroll
@@ -382,10 +447,8 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
                                      vd, C::IDESC_O, acc);
                         }
                     }
-                // the stage's keys were read by S of this tile, which completed before its
-                // softmax began, so the value MMA's completion frees the whole stage
                 umma_commit(&o_done[t & 1]);
-                umma_commit(&kv_empty[t % NS]);
+                umma_commit(&v_empty[t % NV]);
             }
             umma_commit(&fin[1]);
             if (!mbar_wait_bounded(&fin[1], 0, kWaitLimitNs)) prefix_flag(256u);
@@ -425,23 +488,26 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         for (int t = 0; t < n_tiles; ++t) {
-            const int st = t % NS;
-            ok = pfx_warp_wait(&kv_full[st], (t / NS) & 1, abort_flag, lane) &&
-                 pfx_warp_wait(&s_full[t & 1], (t >> 1) & 1, abort_flag, lane);
+            const int ks = t % NK;
+            ok = pfx_warp_wait(&k_full[ks], (t / NK) & 1, abort_flag, lane) &&
+                 pfx_warp_wait(&s_full[t % NSB], (t / NSB) & 1, abort_flag, lane);
             if (!ok) break;
             tc_fence_after();
             float sv[BN];
 #pragma unroll
             for (int c = 0; c < BN / 32; ++c)
-                tmem_ld32(tl + C::COL_S + (t & 1) * BN + c * 32, *reinterpret_cast<float(*)[32]>(&sv[c * 32]));
+                tmem_ld32(tl + C::COL_S + (t % NSB) * BN + c * 32, *reinterpret_cast<float(*)[32]>(&sv[c * 32]));
+            const uint32_t bad = t < n_ctx ? bad_mask[ks] : 0u;
             tmem_wait_ld();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&s_empty[t & 1]);
+            if (lane == 0) {
+                mbar_arrive(&s_empty[t % NSB]);
+                mbar_arrive(&k_empty[ks]);  // the key slot may be refilled: its mask has been read
+            }
 
             if (t < n_ctx) {
                 const int valid = min(BN, ctx - t * BN);
-                const uint32_t bad = bad_mask[st];
                 if (valid < BN || bad) {
 #pragma unroll
                     for (int i = 0; i < BN; ++i)
