@@ -9,27 +9,30 @@
 //
 // One CTA owns (sequence, kv head, 128 query rows), a row being a (new token j, head g of
 // the kv head's group) pair numbered j * G + g: every key/value tile is read once per kv head
-// and shared by the whole GQA group, and the 128 rows are the M of every MMA.  Per tile of
-// BN keys (128, or 64 above head size 128):
-//   loader warps   copy the key tile and the value tile into shared memory in the canonical
-//                  K-major layouts: keys as [key/8][d/8][8 keys][8] (no swizzle), values as
-//                  whole pages [d][block_size keys] with the 32- or 64-byte swizzle (block
-//                  size 16 / 32; plain rows for 8).  A tile of full, valid pages moves by
-//                  tensor copies (TMA) issued by one thread: per 8 keys one key box of 128-byte
-//                  rows, per page one value box; a tile with the context's end, a page outside the
-//                  cache or the chunk's dense rows moves by 16-byte cp.async (zero-filling
-//                  what must not count; the dense value rows are transposed on the way).
-//   MMA lanes      one lane issues S = Q K^T (M 128, N BN, Q in tensor memory) into one of two
-//                  S buffers; another issues O += P V (N = head size) once the softmax has
-//                  written P (an MMA issue blocks its thread until the tensor core takes it).
+// and shared by the whole GQA group, and the 128 rows are the M of every MMA.  Tiles of 64
+// keys; ten warps with fixed roles:
+//   key / value loader warps (two each) fill separate rings of key and value slots in shared
+//                  memory, in the canonical K-major layouts: keys as [key/8][d/8][8 keys][8]
+//                  (no swizzle), values as whole pages [d][block_size keys] with the 32- or
+//                  64-byte swizzle (block size 16 / 32; plain rows for 8).  A tile of full,
+//                  valid pages moves by tensor copies (TMA), one lane per key box (8 tokens,
+//                  128-byte rows) or value page; the context's last tile, a tile with a page
+//                  outside the cache, and the chunk's dense rows move by 16-byte cp.async
+//                  (zero-filling what must not count; dense value rows transposed on the way).
+//                  A key slot is free once its score MMA is done, a value slot only after the
+//                  value MMA, so the key ring runs further ahead.
+//   score-MMA lane S = Q K^T (M 128, N 64, Q in tensor memory) into an S buffer (two, or one
+//                  at head size 256 where tensor memory is full).
+//   value-MMA lane O += P V (N = head size, P in tensor memory where it fits, else in shared
+//                  memory) once the softmax has written P.  An MMA issue blocks the issuing
+//                  thread until the tensor core takes it, so the two products have a lane each.
 //   softmax warps  one thread per row: read the row of S from tensor memory, mask, exp2 with
 //                  a running reference max that only moves when the row max grows by more
 //                  than 2^8 (then O and the row sum are rescaled), write P (bf16 as hi + lo
-//                  so probabilities keep ~16 bits) to shared memory in the A layout.
-// S of tile t+1 runs on the tensor cores while the softmax works on tile t.  All waits are
-// bounded (about two seconds); a wait that gives up sets an abort flag every role checks and
-// bit 8 of the device error word, and the CTA still drains its MMAs and frees its tensor
-// memory before it exits.
+//                  so probabilities keep ~16 bits) in the value MMA's A layout.
+// All waits are bounded (about two seconds); a wait that gives up sets an abort flag every
+// role checks and bit 8 of the device error word, and the CTA still drains its MMAs and frees
+// its tensor memory before it exits.
 #pragma once
 
 #include "pa_kernels.cuh"
