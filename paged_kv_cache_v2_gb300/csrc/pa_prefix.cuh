@@ -21,8 +21,9 @@
 //                  (zero-filling what must not count; dense value rows transposed on the way).
 //                  A key slot is free once its score MMA is done, a value slot only after the
 //                  value MMA, so the key ring runs further ahead.
-//   score-MMA lane S = Q K^T (M 128, N 64, Q in tensor memory) into an S buffer (two, or one
-//                  at head size 256 where tensor memory is full).
+//   score-MMA lane S = Q K^T (M 128, N 64, Q in tensor memory) into one of two S buffers.
+//                  Where tensor memory cannot hold two S buffers next to O, Q and P (head
+//                  size 256, 192 in bf16), the second half of Q is read from shared memory.
 //   value-MMA lane O += P V (N = head size, P in tensor memory where it fits, else in shared
 //                  memory) once the softmax has written P.  An MMA issue blocks the issuing
 //                  thread until the tensor core takes it, so the two products have a lane each.
@@ -39,6 +40,9 @@
 #include "pa_prefix.h"
 #include "pa_tc.cuh"
 
+#ifndef PA_PFX_QSPLIT
+#define PA_PFX_QSPLIT 1
+#endif
 #ifndef PA_PFX_KEY_SHARE
 #define PA_PFX_KEY_SHARE 4
 #endif
@@ -61,30 +65,36 @@ struct PfxCfg {
     // tensor memory, else two S buffers with P in shared memory.
     static constexpr int TM_OQ = DPR + DP / 2, TM_P = 2 * NP * (BN / 2);
     static constexpr bool FIT2 = 2 * BN + TM_OQ + TM_P <= 512;
+    // Where two S buffers do not fit, keeping the second half of Q in shared memory (the
+    // score MMA's A operand for the last DP / 32 K steps) may make them fit.
+    static constexpr bool QSPLIT = !FIT2 && PA_PFX_QSPLIT && 2 * BN + DPR + DP / 4 + TM_P <= 512;
     static constexpr bool FIT1 = BN + TM_OQ + TM_P <= 512;
-    static constexpr bool P_TMEM = FIT2 || FIT1;
-    static constexpr int NSB = FIT2 ? 2 : (FIT1 ? 1 : 2);  // S buffers
+    static constexpr bool P_TMEM = FIT2 || QSPLIT || FIT1;
+    static constexpr int NSB = (FIT2 || QSPLIT) ? 2 : (FIT1 ? 1 : 2);  // S buffers
     static constexpr int P_SMEM = P_TMEM ? 0 : 2 * NP * P_BYTES;
+    static constexpr int QT = QSPLIT ? DP / 2 : DP;  // head elements of Q in tensor memory
+    static constexpr int Q_SMEM = QSPLIT ? kPfxBM * (DP - QT) * 2 : 0;
     // Separate key and value rings: a key slot is free once the score MMA (and the softmax's
     // look at the tile's masks) is done, a value slot only after the value MMA.
-    static constexpr int SLOTS = (227 * 1024 - P_SMEM - CTL_BYTES) / K_BYTES;
+    static constexpr int SLOTS = (227 * 1024 - P_SMEM - Q_SMEM - CTL_BYTES) / K_BYTES;
     static constexpr int NK0 = SLOTS * PA_PFX_KEY_SHARE / 8;  // key share of the slots (in eighths)
     static constexpr int NK = NK0 > 8 ? 8 : (NK0 < 2 ? 2 : NK0);
     static constexpr int NV = SLOTS - NK > 8 ? 8 : SLOTS - NK;
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = NK * K_BYTES;
     static constexpr int OFF_P = OFF_V + NV * V_BYTES;
-    static constexpr int OFF_CTL = OFF_P + P_SMEM;
+    static constexpr int OFF_Q = OFF_P + P_SMEM;  // [chunk][128 rows][16 bytes] of Q's second half
+    static constexpr int OFF_CTL = OFF_Q + Q_SMEM;
     // at least 120 KiB so two CTAs never share an SM (each takes all 512 tensor-memory columns)
     static constexpr int SMEM = OFF_CTL + CTL_BYTES > 120 * 1024 ? OFF_CTL + CTL_BYTES : 120 * 1024;
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr uint32_t COL_S = 0;                 // S buffer b: [b BN, (b + 1) BN)
     static constexpr uint32_t COL_O = NSB * BN;          // O: [COL_O, COL_O + DPR)
     static constexpr uint32_t COL_Q = COL_O + DPR;       // Q, two 16-bit values per column: DP / 2
-    static constexpr uint32_t COL_P = COL_Q + DP / 2;    // P buffer b, term h: + (b NP + h) BN / 2
+    static constexpr uint32_t COL_P = COL_Q + QT / 2;    // P buffer b, term h: + (b NP + h) BN / 2
     static constexpr uint32_t IDESC_S = umma_idesc_f16(BF16, kPfxBM, BN);
     static constexpr uint32_t IDESC_O = umma_idesc_f16(BF16, kPfxBM, DP);
-    static_assert(COL_Q + DP / 2 <= TMEM_COLS, "tensor memory");
+    static_assert(COL_Q + QT / 2 <= TMEM_COLS, "tensor memory");
     static_assert(!P_TMEM || COL_P + TM_P <= TMEM_COLS, "tensor memory");
     static_assert(NV >= 2 && SMEM <= 227 * 1024, "shared memory");
 };
@@ -404,10 +414,15 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
 #pragma unroll
                 for (int ks = 0; ks < C::DP / 16; ++ks) {
                     const uint64_t kd = umma_desc(sK + ks * 2 * 128, 128, C::DP * 16);
-                    asm volatile(
-                        "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-                        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_s),
-                        "r"(tm + C::COL_Q + ks * 8), "l"(kd), "r"(C::IDESC_S), "r"(ks > 0 ? 1u : 0u));
+                    if (ks < C::QT / 16) {
+                        asm volatile(
+                            "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+                            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_s),
+                            "r"(tm + C::COL_Q + ks * 8), "l"(kd), "r"(C::IDESC_S), "r"(ks > 0 ? 1u : 0u));
+                    } else {
+                        umma_f16(d_s, umma_desc(sbase + C::OFF_Q + (ks - C::QT / 16) * 2 * (kPfxBM * 16), kPfxBM * 16, 128),
+                                 kd, C::IDESC_S, 1u);
+                    }
                 }
                 umma_commit(&s_full[t % NSB]);
                 umma_commit(&k_empty[t % NK]);
@@ -473,7 +488,7 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
                 qrow = p.q + ((int64_t)(q0 + j) * p.q_stride + (int64_t)(kvh * G + g) * D) * 2;
             }
 #pragma unroll 1
-            for (int c = 0; c < C::DP / 16; ++c) {
+            for (int c = 0; c < C::QT / 16; ++c) {
                 uint4 a = make_uint4(0u, 0u, 0u, 0u), b = make_uint4(0u, 0u, 0u, 0u);
                 if (qrow != nullptr && 2 * c < C::NCR) a = ld_nc_v4(qrow + c * 32);
                 if (qrow != nullptr && 2 * c + 1 < C::NCR) b = ld_nc_v4(qrow + c * 32 + 16);
@@ -482,6 +497,16 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
                                  tl + C::COL_Q + c * 8),
                              "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
                              : "memory");
+            }
+            if constexpr (C::QSPLIT) {
+                // the second half as 16-byte chunks [chunk][row] (the score MMA's no-swizzle
+                // K-major A layout); the padding past D is zero
+                for (int c = C::QT / 8; c < C::NCP; ++c) {
+                    uint4 a = make_uint4(0u, 0u, 0u, 0u);
+                    if (qrow != nullptr && c < C::NCR) a = ld_nc_v4(qrow + c * 16);
+                    sts_v4(sbase + C::OFF_Q + (c - C::QT / 8) * (kPfxBM * 16) + r * 16, a.x, a.y, a.z, a.w);
+                }
+                fence_proxy_async_smem();
             }
             tmem_wait_st();
             tc_fence_before();
