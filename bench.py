@@ -458,9 +458,19 @@ def run_prefix(args):
     import workloads
 
     name = args.workload if args.workload in workloads.PREFIX_CONFIGS else "prefix_long_gqa"
-    torch.cuda.set_device(0)
+    ws, rank, local = _dist()
+    if ws > 1:
+        import torch.distributed as dist
+
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev_i = torch.cuda.current_device()
     pa.load()
-    wl = workloads.make_prefix(name)
+    # each rank runs its own step of the same shape (sequences are independent: weak scaling)
+    wl = workloads.make_prefix(name, seed=workloads.PREFIX_CONFIGS[name]["seed"] + 100_003 * rank) if ws > 1 \
+        else workloads.make_prefix(name)
     dev = {k: getattr(wl, k).cuda() for k in ("query", "key", "value", "key_cache", "value_cache",
                                               "block_tables", "query_start_loc", "context_lens")}
     out = torch.empty_like(dev["query"])
@@ -474,9 +484,12 @@ def run_prefix(args):
     for _ in range(args.warmup):
         call(dev["query"], dev["key"], dev["value"], out)
     torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
+        torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     launches = 0
-    with ClockSampler(0) as clocks:
+    with ClockSampler(dev_i) as clocks:
         for i in range(args.steps):
             flush.zero_()
             ev[i][0].record()
@@ -484,9 +497,13 @@ def run_prefix(args):
             ev[i][1].record()
             launches += 1
         torch.cuda.synchronize()
+    if ws > 1:
+        torch.distributed.barrier()
     times = sorted(a.elapsed_time(b) for a, b in ev)
-    ms = sum(times) / len(times)
-    tflops = flops / (ms * 1e-3) / 1e12
+    ms_rank = sum(times) / len(times)
+    all_flops, ms = combine_ranks(float(flops), ms_rank, torch.device("cuda", dev_i), ws)
+    tflops = all_flops / (ms * 1e-3) / 1e12
+    rank_tflops = flops / (ms_rank * 1e-3) / 1e12
     e2e = None
     if not args.no_e2e:
         hq, hk, hv = (getattr(wl, k).pin_memory() for k in ("query", "key", "value"))
@@ -507,11 +524,13 @@ def run_prefix(args):
         b.record()
         torch.cuda.synchronize()
         e_ms = a.elapsed_time(b) / args.steps
+        if ws > 1:
+            _, e_ms = combine_ranks(0.0, e_ms, torch.device("cuda", dev_i), ws)
         h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
-        e2e = {"value": round(flops / (e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(e_ms, 4),
+        e2e = {"value": round(all_flops / (e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(e_ms, 4),
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": ho.numel() * ho.element_size()}
     cpu = None
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and rank == 0 and ws == 1:
         import oracle
         threads = len(os.sched_getaffinity(0))
         qsl = wl.query_start_loc.numpy()
@@ -531,20 +550,27 @@ def run_prefix(args):
                "sample": f"fp64 oracle on {nrows} (token, head) rows: all heads of random new tokens of the "
                          f"workload, {t_total:.1f} s"}
     peak, kind = _tensor_peak()
+    if rank != 0:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return 0
     print(json.dumps({
-        "metric": "chunked-prefix attention TFLOP/s (4 d H per visible query-key pair), 1 GPU",
-        "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "metric": f"chunked-prefix attention TFLOP/s (4 d H per visible query-key pair), {ws} GPU",
+        "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": wl.q_dtype, "data": "synthetic",
         "config": {"workload": name, "num_seqs": wl.num_seqs, "heads": [wl.num_heads, wl.num_kv_heads],
                    "head_size": wl.head_size, "block_size": wl.block_size,
                    "context_lens": wl.context_lens.tolist(), "query_lens": wl.query_lens.tolist(),
-                   "flops_per_step": flops, "l2": "flushed (256 MiB write) before every timed call"},
-        "roofline": {"bound": "tensor", "achieved": round(tflops, 2), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(tflops / peak, 4), "traffic": _profiled_traffic(name, "prefix"),
+                   "flops_per_step": flops, "l2": "flushed (256 MiB write) before every timed call",
+                   "parallelism": f"replicas x{ws} (sequence shards)"},
+        "roofline": {"bound": "tensor", "achieved": round(rank_tflops, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(rank_tflops / peak, 4), "traffic": _profiled_traffic(name, "prefix"),
                      "kernel": "pa_prefix_kernel",
                      "peak_source": f"{kind} bf16_tflops (burst; fp16 has the same dense rate)"},
         "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": launches, "clocks": clocks.summary()}), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
     return 0
 
 

@@ -11,9 +11,9 @@ namespace pa {
 // ---- chunked-prefix attention ----------------------------------------------------------
 // Warp roles of the prefix kernel: warps 0-3 run the softmax (warp w owns tensor-memory lanes
 // 32w..32w+31, i.e. query rows 32w..32w+31), warp 4 allocates tensor memory and one of its
-// lanes issues the score MMAs, warps 5-8 copy key and value tiles into shared memory, one
-// lane of warp 9 issues the value MMAs.  (An MMA issue blocks the issuing thread until the
-// tensor core takes it, so the two products get a thread each.)
+// lanes issues the score MMAs, warps 5-6 fill the key ring and warps 7-8 the value ring in
+// shared memory, one lane of warp 9 issues the value MMAs.  (An MMA issue blocks the issuing
+// thread until the tensor core takes it, so the two products get a thread each.)
 constexpr int kPfxMmaWarp = 4;
 constexpr int kPfxLoaderWarp0 = 5;
 constexpr int kPfxLoaderThreads = 4 * 32;

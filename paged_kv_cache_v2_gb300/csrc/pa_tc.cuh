@@ -1,6 +1,6 @@
 // pa_tc.cuh -- PTX wrappers for the sm_103a tensor-core path of the prefix kernel: 5th-
 // generation MMA (tcgen05) with tensor-memory accumulators, tensor-memory loads/stores,
-// tensor (TMA) and bulk copies into shared memory, cp.async, non-blocking mbarrier tests.
+// tensor (TMA) and bulk copies into shared memory, cp.async, shared-memory stores.
 #pragma once
 
 #include <stdint.h>
@@ -9,18 +9,6 @@
 
 namespace pa {
 
-// Non-blocking test of a phase (try_wait may suspend the thread for a while).
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_addr(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
 // ---- cp.async (16 bytes, L2 only; src_bytes < 16 zero-fills the rest of the 16) ------
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
