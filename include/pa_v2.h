@@ -227,6 +227,7 @@ PA_API pa_status pa_swap_blocks(const void* src_cache, void* dst_cache, const in
  *   query_start_loc int32 [num_seqs + 1] non-decreasing; context_lens int32 [num_seqs].
  *   max_query_len  host int >= every q_len (sizes the grid).
  *   head_size in {64, 80, 96, 112, 120, 128, 192, 256}; block_size in {8, 16, 32};
+ *   num_blocks * num_kv_heads < 2^31 (pages are addressed by 32-bit copy coordinates);
  *   dtype PA_DT_F16 or PA_DT_BF16 (query, key, value, caches and output).
  * Errors: PA_ERR_INVALID_ARG / PA_ERR_UNSUPPORTED before anything is enqueued.  On the
  * device, a cached block id outside [0, num_blocks) masks that page (bit 5 of

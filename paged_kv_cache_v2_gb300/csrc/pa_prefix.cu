@@ -85,6 +85,8 @@ extern "C" pa_status pa_prefix(void* output, const void* query, const void* key,
     const int G = num_heads / num_kv_heads;
     if ((int64_t)max_query_len * G > (1ll << 30) || (int64_t)max_blocks_per_seq * block_size > (1ll << 30))
         return PA_ERR_INVALID_ARG;
+    // tensor-copy coordinates are signed 32-bit: a page is addressed as block * kv heads + kv head
+    if ((int64_t)num_blocks * num_kv_heads >= (1ll << 31)) return PA_ERR_INVALID_ARG;
     if (q_row_stride < (int64_t)num_heads * head_size || kv_row_stride < (int64_t)num_kv_heads * head_size ||
         q_row_stride % 8 || kv_row_stride % 8)
         return PA_ERR_INVALID_ARG;

@@ -173,6 +173,7 @@ def _prefix_raw(**over):
     (dict(block_size=64), 2), (dict(dtype=2), 2), (dict(q_stride=1000), 1), (dict(kv_stride=260), 1),
     (dict(max_blocks_per_seq=0), 1), (dict(max_query_len=5, output=0x10008), 1),
     (dict(max_query_len=5, key=None), 1),
+    (dict(num_blocks=1 << 29, num_kv_heads=4, num_heads=8), 1),
 ])
 def test_prefix_rejects_invalid_arguments_on_host(over, status):
     assert _prefix_raw(**over) == status
