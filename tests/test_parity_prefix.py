@@ -130,3 +130,18 @@ def test_prefix_is_deterministic():
     a = run_prefix(wl, dev)
     b = run_prefix(wl, dev)
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_many_sequences_short_chunks():
+    # 300 sequences (grid z), chunks of 0-40 new tokens over contexts of 0-700 tokens, bf16,
+    # block size 32: most CTAs see one partial context tile and one causal chunk tile
+    rng = np.random.default_rng(1100)
+    S = 300
+    ctx = rng.integers(0, 700, S).tolist()
+    ql = rng.integers(0, 41, S).tolist()
+    wl = workloads.build_prefix(num_seqs=S, num_heads=8, num_kv_heads=2, head_size=128, block_size=32,
+                                context_lens=ctx, query_lens=ql, q_dtype="bf16", seed=1100)
+    out = run_prefix(wl)
+    rows = prefix_sample_rows(wl, n=80)
+    check_prefix(wl, out, oracle.prefix_workload(wl, rows=rows), rows=rows, label="many seqs")
+    assert pa.pa_get_device_errors() == 0
