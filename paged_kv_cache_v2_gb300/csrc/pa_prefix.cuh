@@ -40,12 +40,19 @@
 #include "pa_prefix.h"
 #include "pa_tc.cuh"
 
+// Tuning knobs (compile-time): PA_PFX_QSPLIT lets the second half of Q live in shared memory
+// where that buys a second S buffer; PA_PFX_KEY_SHARE is the key ring's share of the
+// key/value slots, in eighths; PA_PFX_WAIT_HINT_NS is the suspend hint of the bounded waits.
 #ifndef PA_PFX_QSPLIT
 #define PA_PFX_QSPLIT 1
 #endif
 #ifndef PA_PFX_KEY_SHARE
 #define PA_PFX_KEY_SHARE 4
 #endif
+#ifndef PA_PFX_WAIT_HINT_NS
+#define PA_PFX_WAIT_HINT_NS 20000
+#endif
+
 namespace pa {
 
 template <bool BF16, int D>
@@ -61,8 +68,9 @@ struct PfxCfg {
     static constexpr int P_BYTES = kPfxBM * BN * 2;
     static constexpr int CTL_BYTES = 512;
     // Tensor memory: S buffers, O, Q and (where they fit) the two P buffers, the A operand of
-    // the value MMA.  Two S buffers with P in tensor memory, else one S buffer with P in
-    // tensor memory, else two S buffers with P in shared memory.
+    // the value MMA.  Two S buffers with P in tensor memory; else the same with half of Q in
+    // shared memory; else one S buffer with P in tensor memory; else two S buffers with P in
+    // shared memory.
     static constexpr int TM_OQ = DPR + DP / 2, TM_P = 2 * NP * (BN / 2);
     static constexpr bool FIT2 = 2 * BN + TM_OQ + TM_P <= 512;
     // Where two S buffers do not fit, keeping the second half of Q in shared memory (the
@@ -98,10 +106,6 @@ struct PfxCfg {
     static_assert(!P_TMEM || COL_P + TM_P <= TMEM_COLS, "tensor memory");
     static_assert(NV >= 2 && SMEM <= 227 * 1024, "shared memory");
 };
-
-#ifndef PA_PFX_WAIT_HINT_NS
-#define PA_PFX_WAIT_HINT_NS 20000
-#endif
 
 static __device__ unsigned int g_prefix_errors = 0;
 

@@ -20,7 +20,6 @@ constexpr int kPfxLoaderThreads = 4 * 32;
 constexpr int kPfxPvWarp = 9;
 constexpr int kPfxThreads = 10 * 32;
 constexpr int kPfxBM = 128;    // query rows per CTA (the MMA M)
-constexpr int kPfxStages = 2;  // key/value tile stages
 
 struct PrefixParams {
     CUtensorMap kmap;  // key cache as {64 elems = 8 tokens x 8, block_size/8, d/8, blocks * kv heads}
