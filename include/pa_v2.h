@@ -269,10 +269,8 @@ PA_API pa_status pa_v2_set_timing_events(cudaEvent_t begin, cudaEvent_t end);
  *
  * Not part of the pages' interface (the paper has no counterpart); it exists for callers
  * that are handed a stream but no allocator: an inference runtime that runs this library as
- * a plugin with a device-memory budget fixed at start-up, code running while a stream is
- * being captured into a CUDA graph (where a cudaMalloc would break the capture or stall on
- * a device-wide synchronisation), or an embedded or real-time service that must not grow
- * its footprint after initialisation.  Such a caller cannot provide the exp_sums,
+ * a plugin with a device-memory budget fixed at start-up, or an embedded or real-time
+ * service that must not grow its footprint after initialisation.  Such a caller cannot provide the exp_sums,
  * max_logits and tmp_output workspace that pa_v2_decode needs.
  *
  * Same computation and the same output as pa_v2_decode (argument meanings and layouts as
@@ -281,8 +279,7 @@ PA_API pa_status pa_v2_set_timing_events(cudaEvent_t begin, cudaEvent_t end);
  * the library defines at file scope: every GPU that loads the library holds it until the
  * process exits.  This call allocates nothing (no cudaMalloc, cudaFree or allocating
  * library routine).  The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call before any stream
- * capture.  The partition statistics a caller of pa_v2_decode would receive are not
+ * (cudaGetSymbolAddress) with that device current.  The partition statistics a caller of pa_v2_decode would receive are not
  * returned.
  *
  * Errors: as pa_v2_decode, plus PA_ERR_SCRATCH_TOO_SMALL when

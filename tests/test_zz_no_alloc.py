@@ -1,6 +1,6 @@
 """GPU: pa_v2_decode_noalloc, the entry point for callers that cannot allocate device memory
-(a plugin handed only a stream and a fixed budget, or code running while a stream is being
-captured into a CUDA graph), gives the same output as pa_v2_decode with a caller-owned
+(a plugin handed only a stream and a fixed budget), gives the same output as pa_v2_decode
+with a caller-owned
 workspace, on two calls in a row (the second call reuses scratch the first one left behind).
 
 This file is named to be collected last, so a run that stops at its first failure has run
