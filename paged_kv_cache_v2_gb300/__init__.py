@@ -75,7 +75,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.pa_swap_blocks.argtypes = [P, P, P, i32, i64, i32, i32, P]
     lib.pa_prefix.restype = i32
     lib.pa_prefix.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, f32, P, i32, i32, P, P, i32, i32, i64, i64,
-                              i32, P]
+                              i32, P, ctypes.c_size_t, i32, i32, P]
+    lib.pa_prefix_workspace_size.restype = ctypes.c_size_t
+    lib.pa_prefix_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
     lib.pa_v2_decode_noalloc.restype = i32
     lib.pa_v2_decode_noalloc.argtypes = [P, P, P, P, i32, i32, i32, i32, f32, P, i32, i32, P, i32, i32,
                                          P, i32, i32, f32, f32, P]
@@ -261,12 +263,19 @@ def pa_swap_blocks(src: torch.Tensor, dst: torch.Tensor, block_mapping: torch.Te
 def pa_prefix(output: torch.Tensor, query: torch.Tensor, key: torch.Tensor, value: torch.Tensor,
               key_cache: torch.Tensor, value_cache: torch.Tensor, block_tables: torch.Tensor,
               query_start_loc: torch.Tensor, context_lens: torch.Tensor, max_query_len: int,
-              scale: Optional[float] = None, stream=None) -> None:
+              scale: Optional[float] = None, stream=None, workspace: Optional[torch.Tensor] = None,
+              max_splits: Optional[int] = None, min_split_keys: int = 0) -> None:
     """Chunked-prefix attention ("paged_attn.py" forward_prefix): every new token attends to
     its sequence's cached context and, causally, to the chunk's tokens up to itself.
     output/query [T, H, d], key/value [T, Hk, d] (rows may be strided, last two dims dense),
     caches in the decode layouts, int32 block_tables [S, W], query_start_loc [S+1],
-    context_lens [S].  scale defaults to d^-0.5 as on the pages."""
+    context_lens [S].  scale defaults to d^-0.5 as on the pages.
+
+    Contexts longer than min_split_keys (0: 16384) are cut into up to max_splits parts that
+    run on separate CTAs and are merged by a second kernel.  workspace is a uint8 CUDA tensor
+    of at least prefix_workspace_size(...) bytes; when it is None and the tables can hold
+    such a context, one is taken from torch's allocator (max_splits defaults to 8;
+    max_splits=1 turns splitting off)."""
     lib = load()
     T, H, d = query.shape
     Hk = key_cache.shape[1]
@@ -288,11 +297,36 @@ def pa_prefix(output: torch.Tensor, query: torch.Tensor, key: torch.Tensor, valu
     S = context_lens.shape[0]
     if scale is None:
         scale = d ** -0.5
+    if max_splits is None:
+        max_splits = 8
+    split_keys = min_split_keys or PREFIX_SPLIT_KEYS
+    if workspace is None and max_splits > 1 and block_tables.shape[1] * bs > split_keys:
+        max_splits = min(max_splits, -(-block_tables.shape[1] * bs // split_keys))
+        nbytes = prefix_workspace_size(S, H, Hk, d, int(max_query_len), max_splits)
+        if nbytes:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=query.device)
+            if stream is not None:
+                workspace.record_stream(stream)  # not reused before the call's work on `stream` ends
+    if workspace is not None and (workspace.dtype != torch.uint8 or not workspace.is_cuda
+                                  or not workspace.is_contiguous()):
+        raise TypeError("workspace must be a contiguous uint8 CUDA tensor")
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (_ptr(workspace), workspace.numel())
     _check("pa_prefix", lib.pa_prefix(
         _ptr(output), _ptr(query), _ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache), S, H, Hk, d,
         float(scale), _ptr(block_tables), block_tables.shape[1], key_cache.shape[0], _ptr(query_start_loc),
         _ptr(context_lens), int(max_query_len), bs, query.stride(0), key.stride(0), _dt(query.dtype),
-        _stream(stream)))
+        ws_ptr, ws_bytes, int(max_splits), int(min_split_keys), _stream(stream)))
+
+
+# Default shortest context (tokens) that pa_prefix cuts into parts.
+PREFIX_SPLIT_KEYS = 16384
+
+
+def prefix_workspace_size(num_seqs: int, num_heads: int, num_kv_heads: int, head_size: int,
+                          max_query_len: int, max_splits: int) -> int:
+    """Bytes of workspace pa_prefix needs to cut contexts into up to max_splits parts."""
+    return int(load().pa_prefix_workspace_size(num_seqs, num_heads, num_kv_heads, head_size, max_query_len,
+                                               max_splits))
 
 
 def pa_v2_partition_size() -> int:

@@ -300,6 +300,11 @@ extern "C" pa_status pa_get_device_errors(uint32_t* flags, int reset) {
     return PA_OK;
 }
 
+void pa::timing_events(cudaEvent_t* begin, cudaEvent_t* end) {
+    *begin = g_t_begin;
+    *end = g_t_end;
+}
+
 extern "C" pa_status pa_v2_set_timing_events(cudaEvent_t begin, cudaEvent_t end) {
     if ((begin == nullptr) != (end == nullptr)) return PA_ERR_INVALID_ARG;
     g_t_begin = begin;

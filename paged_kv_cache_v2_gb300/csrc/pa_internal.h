@@ -37,5 +37,7 @@ pa_status launch_decode(const DecodeArgs& a, float* exp_sums, float* max_logits,
 cudaError_t read_decode_errors(unsigned int* v, bool reset);
 cudaError_t read_cache_errors(unsigned int* v, bool reset);
 cudaError_t read_block_errors(unsigned int* v, bool reset);
+// The events pa_v2_set_timing_events installed (both null when none).
+void timing_events(cudaEvent_t* begin, cudaEvent_t* end);
 
 }  // namespace pa

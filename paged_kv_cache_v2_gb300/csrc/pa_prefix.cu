@@ -7,6 +7,7 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "pa_internal.h"
@@ -66,12 +67,29 @@ static bool encode_cache_maps(PrefixParams& p, const void* key_cache, const void
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Default minimum context per split: 16384 keys (256 tiles of 64).
+static constexpr int kDefaultSplitKeys = 16384;
+static constexpr int kMaxSplits = 32;
+
+static int64_t prefix_row_tiles(int max_query_len, int G) { return ((int64_t)max_query_len * G + kPfxBM - 1) / kPfxBM; }
+
+extern "C" size_t pa_prefix_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                                           int max_query_len, int max_splits) {
+    if (max_splits <= 1 || num_seqs <= 0 || max_query_len <= 0 || num_heads <= 0 || num_kv_heads <= 0 ||
+        head_size <= 0 || num_heads % num_kv_heads || max_splits > kMaxSplits)
+        return 0;
+    const int64_t items =
+        (int64_t)num_seqs * num_kv_heads * prefix_row_tiles(max_query_len, num_heads / num_kv_heads) * max_splits;
+    return (size_t)(items * kPfxBM * ((int64_t)head_size * 4 + 8));
+}
+
 extern "C" pa_status pa_prefix(void* output, const void* query, const void* key, const void* value,
                                const void* key_cache, const void* value_cache, int num_seqs, int num_heads,
                                int num_kv_heads, int head_size, float scale, const int32_t* block_tables,
                                int max_blocks_per_seq, int num_blocks, const int32_t* query_start_loc,
                                const int32_t* context_lens, int max_query_len, int block_size,
-                               int64_t q_row_stride, int64_t kv_row_stride, pa_dtype dtype, cudaStream_t stream) {
+                               int64_t q_row_stride, int64_t kv_row_stride, pa_dtype dtype, void* workspace,
+                               size_t workspace_bytes, int max_splits, int min_split_keys, cudaStream_t stream) {
     if (num_seqs < 0 || num_seqs > 65535 || max_query_len < 0) return PA_ERR_INVALID_ARG;
     if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads || num_kv_heads > 65535)
         return PA_ERR_INVALID_ARG;
@@ -90,6 +108,15 @@ extern "C" pa_status pa_prefix(void* output, const void* query, const void* key,
     if (q_row_stride < (int64_t)num_heads * head_size || kv_row_stride < (int64_t)num_kv_heads * head_size ||
         q_row_stride % 8 || kv_row_stride % 8)
         return PA_ERR_INVALID_ARG;
+    const bool split = max_splits > 1 && workspace != nullptr;
+    if (split) {
+        if (max_splits > kMaxSplits || min_split_keys < 0 || min_split_keys % 64 || !aligned16(workspace))
+            return PA_ERR_INVALID_ARG;
+        if (num_seqs > 0 && max_query_len > 0 &&
+            workspace_bytes <
+                pa_prefix_workspace_size(num_seqs, num_heads, num_kv_heads, head_size, max_query_len, max_splits))
+            return PA_ERR_INVALID_ARG;
+    }
     if (num_seqs == 0 || max_query_len == 0) return PA_OK;
     if (!output || !query || !key || !value || !key_cache || !value_cache || !block_tables || !query_start_loc ||
         !context_lens)
@@ -121,9 +148,34 @@ extern "C" pa_status pa_prefix(void* output, const void* query, const void* key,
     p.q_stride = q_row_stride;
     p.kv_stride = kv_row_stride;
     p.sl2 = scale * kLog2e;
-    const int64_t row_tiles = ((int64_t)max_query_len * G + kPfxBM - 1) / kPfxBM;
-    const dim3 grid((unsigned)row_tiles, (unsigned)num_kv_heads, (unsigned)num_seqs);
-    if (fn(p, grid, stream) != cudaSuccess) {
+    const int64_t row_tiles = prefix_row_tiles(max_query_len, G);
+    p.mt = (int)row_tiles;
+    p.split_tiles = (min_split_keys > 0 ? min_split_keys : kDefaultSplitKeys) / 64;
+    // no more splits than the longest context the tables can hold would use
+    const int64_t max_ctx_tiles = ((int64_t)max_blocks_per_seq * block_size + 63) / 64;
+    p.nsplit = 1;
+    if (split && max_ctx_tiles > p.split_tiles)
+        p.nsplit = (int)std::min<int64_t>(max_splits, (max_ctx_tiles + p.split_tiles - 1) / p.split_tiles);
+    p.ws_o = static_cast<float*>(workspace);
+    p.ws_ml = nullptr;
+    if (p.nsplit > 1) {
+        const int64_t rows = (int64_t)num_seqs * num_kv_heads * row_tiles * p.nsplit * kPfxBM;
+        p.ws_ml = reinterpret_cast<float2*>(static_cast<float*>(workspace) + rows * head_size);
+    }
+    if (row_tiles * p.nsplit > INT32_MAX || ((int64_t)max_query_len * num_heads + 7) / 8 > INT32_MAX)
+        return PA_ERR_INVALID_ARG;
+    const dim3 grid((unsigned)(row_tiles * p.nsplit), (unsigned)num_kv_heads, (unsigned)num_seqs);
+    cudaEvent_t t_begin, t_end;
+    timing_events(&t_begin, &t_end);
+    if (t_begin != nullptr) cudaEventRecord(t_begin, stream);
+    cudaError_t e = fn(p, grid, stream);
+    if (t_end != nullptr) cudaEventRecord(t_end, stream);
+    if (e == cudaSuccess && p.nsplit > 1) {
+        const dim3 cgrid((unsigned)(((int64_t)max_query_len * num_heads + 7) / 8), (unsigned)num_seqs);
+        e = bf16 ? launch_prefix_combine<true>(p, head_size, cgrid, stream)
+                 : launch_prefix_combine<false>(p, head_size, cgrid, stream);
+    }
+    if (e != cudaSuccess) {
         (void)cudaGetLastError();
         return PA_ERR_CUDA;
     }

@@ -139,6 +139,16 @@ __device__ __forceinline__ uint32_t pfx_v_off(int o, int dd, int bs_log2, int DP
     return (uint32_t)((o >> bs_log2) * (DP << rowb_log2) + (dd << rowb_log2) + ((kq ^ swz) << 4));
 }
 
+// How a sequence's n_ctx context tiles are split: {number of splits, tiles per split}.  A
+// context longer than split_tiles tiles is cut into at most nsplit equal parts; every split
+// holds at least one tile, the last one also takes the chunk.
+__device__ __forceinline__ int2 pfx_split_plan(int n_ctx, int nsplit, int split_tiles) {
+    int ns = n_ctx > split_tiles ? min(nsplit, (n_ctx + split_tiles - 1) / split_tiles) : 1;
+    const int per = max(1, (n_ctx + ns - 1) / ns);
+    ns = max(1, (n_ctx + per - 1) / per);
+    return make_int2(ns, per);
+}
+
 // One lane waits, the warp learns the outcome (warp-uniform, as tcgen05.ld/st require).
 __device__ __forceinline__ bool pfx_warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int lane) {
     int ok = 1;
@@ -154,13 +164,14 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int s = blockIdx.z, kvh = blockIdx.y;
-    const int row0 = (gridDim.x - 1 - blockIdx.x) * kPfxBM;  // row tiles with more keys first
+    const int split = blockIdx.x / p.mt;                        // which part of the context
+    const int row0 = (p.mt - 1 - blockIdx.x % p.mt) * kPfxBM;  // row tiles with more keys first
     const int G = p.G;
+    int ctx = p.ctx_lens[s];
     const int q0 = p.qsl[s];
     const int q_len = p.qsl[s + 1] - q0;
-    int ctx = p.ctx_lens[s];
     if (q_len < 0 || q_len > p.max_query_len || ctx < 0) {
-        if (tid == 0) prefix_flag(128u);
+        if (tid == 0 && split == 0) prefix_flag(128u);
         return;
     }
     const int rows_total = q_len * G;
@@ -169,6 +180,13 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
         if (tid == 0) prefix_flag(64u);
         ctx = p.mbps * p.bs;
     }
+    // This CTA's keys: context tiles [tb, tb + n_ctx) of `split`, and the chunk if it is the
+    // sequence's last split.
+    const int2 plan = pfx_split_plan((ctx + BN - 1) / BN, p.nsplit, p.split_tiles);
+    if (split >= plan.x) return;
+    const int tb = split * plan.y;
+    const int n_ctx = min(plan.y, (ctx + BN - 1) / BN - tb);
+    const bool last_split = split == plan.x - 1;
 
     const uint32_t sbase = smem_addr(smem);
     if (sbase & 1023u) {  // the swizzled layouts are defined on 1 KiB-aligned addresses
@@ -196,9 +214,8 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
     uint32_t* bad_mask = reinterpret_cast<uint32_t*>(ctl + 8 * NBARS + 8);  // [NK] pages outside the cache
     static_assert(8 * NBARS + 8 + 4 * NK <= C::CTL_BYTES, "control block");
 
-    const int n_ctx = (ctx + BN - 1) / BN;
     const int row_last = min(row0 + kPfxBM, rows_total) - 1;
-    const int n_tiles = n_ctx + (row_last / G) / BN + 1;
+    const int n_tiles = n_ctx + (last_split ? (row_last / G) / BN + 1 : 0);
 
     if (tid == 0) {
         for (int i = 0; i < NK; ++i) {
@@ -261,7 +278,8 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
         // the ids of tile t + 1 are loaded while tile t is waited for and issued
         auto tile_page = [&](int t) {
             int b = -1;
-            if (t < n_ctx && lane < npg && t * BN + (lane << p.bs_log2) < ctx) b = table[((t * BN) >> p.bs_log2) + lane];
+            if (t < n_ctx && lane < npg && (tb + t) * BN + (lane << p.bs_log2) < ctx)
+                b = table[(((tb + t) * BN) >> p.bs_log2) + lane];
             return b;
         };
         int pid_next = tile_page(0);
@@ -278,7 +296,7 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
             const uint32_t sK = sbase + C::OFF_K + slot * C::K_BYTES;
             const uint32_t sV = sbase + C::OFF_V + slot * C::V_BYTES;
             if (t < n_ctx) {
-                const int t0 = t * BN;
+                const int t0 = (tb + t) * BN;
                 // pages of the tile whose id is outside the cache (masked); both teams compute
                 // the same mask
                 const bool bad = lane < npg && t0 + (lane << p.bs_log2) < ctx && (unsigned)pid >= (unsigned)p.num_blocks;
@@ -539,7 +557,7 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
             }
 
             if (t < n_ctx) {
-                const int valid = min(BN, ctx - t * BN);
+                const int valid = min(BN, ctx - (tb + t) * BN);
                 if (valid < BN || bad) {
 #pragma unroll
                     for (int i = 0; i < BN; ++i)
@@ -630,7 +648,27 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
             if (lane == 0) mbar_arrive(&p_full[t & 1]);
         }
         if (ok) ok = pfx_warp_wait(&o_done[(n_tiles - 1) & 1], ((n_tiles - 1) >> 1) & 1, abort_flag, lane);
-        if (ok) {
+        if (ok && plan.x > 1) {
+            // one split of several: O (fp32, relative to the reference max) and the row's
+            // (reference max, sum) go to the workspace for the combine
+            tc_fence_after();
+            const int64_t item = (((int64_t)s * p.Hk + kvh) * p.mt + row0 / kPfxBM) * p.nsplit + split;
+            float* wrow = row < rows_total ? p.ws_o + (item * kPfxBM + r) * D : nullptr;
+#pragma unroll 1
+            for (int c = 0; c < C::DPR / 32; ++c) {
+                float o[32];
+                tmem_ld32(tl + C::COL_O + c * 32, o);
+                tmem_wait_ld();
+                if (wrow != nullptr) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        if (c * 32 + q * 4 < D)
+                            *reinterpret_cast<float4*>(wrow + c * 32 + q * 4) =
+                                make_float4(o[q * 4], o[q * 4 + 1], o[q * 4 + 2], o[q * 4 + 3]);
+                }
+            }
+            if (wrow != nullptr) p.ws_ml[item * kPfxBM + r] = make_float2(m_ref, l);
+        } else if (ok) {
             tc_fence_after();
             const float inv = 1.f / l;
             uint8_t* orow = nullptr;
@@ -665,6 +703,68 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
     __syncthreads();
     tc_fence_after();
     if (warp == kPfxMmaWarp) tmem_dealloc(tm, C::TMEM_COLS);
+}
+
+// Merge of a split sequence's partial results, the log-sum-exp combine of softmaxes over
+// disjoint key sets: with the splits' reference maxima m_k (exp2 domain), sums l_k and
+// un-normalised outputs O_k, out = sum_k 2^(m_k - M) O_k / sum_k 2^(m_k - M) l_k, M = max m_k.
+// One warp per (new token, query head) row; rows of unsplit sequences were written by the
+// attention kernel and are skipped.
+template <bool BF16>
+__global__ void __launch_bounds__(256) pa_prefix_combine_kernel(const PrefixParams p, int D) {
+    const int s = blockIdx.y, lane = threadIdx.x & 31;
+    const int64_t rr = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);  // j * H + h
+    int ctx = p.ctx_lens[s];
+    const int q0 = p.qsl[s], q_len = p.qsl[s + 1] - q0;
+    if (q_len < 0 || q_len > p.max_query_len || ctx < 0) return;
+    ctx = min(ctx, p.mbps * p.bs);
+    const int j = (int)(rr / p.H), h = (int)(rr - (int64_t)j * p.H);
+    if (j >= q_len) return;
+    const int ns = pfx_split_plan((ctx + 63) / 64, p.nsplit, p.split_tiles).x;
+    if (ns == 1) return;
+    const int kvh = h / p.G, r = j * p.G + (h - kvh * p.G);
+    const int64_t item0 = (((int64_t)s * p.Hk + kvh) * p.mt + r / kPfxBM) * p.nsplit;
+    const int rt = r % kPfxBM;
+    float2 ml = make_float2(-INFINITY, 0.f);
+    if (lane < ns) ml = p.ws_ml[(item0 + lane) * kPfxBM + rt];
+    float mx = ml.x;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const float w = ml.y > 0.f ? exp2f(ml.x - mx) : 0.f;
+    float den = w * ml.y;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+    float4 acc[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+    for (int k = 0; k < ns; ++k) {
+        const float wk = __shfl_sync(0xffffffffu, w, k);
+        const float* orow = p.ws_o + ((item0 + k) * kPfxBM + rt) * D;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            const int c4 = lane + 32 * i;
+            if (c4 < D / 4) {
+                const float4 v = __ldg(reinterpret_cast<const float4*>(orow) + c4);
+                acc[i].x += wk * v.x;
+                acc[i].y += wk * v.y;
+                acc[i].z += wk * v.z;
+                acc[i].w += wk * v.w;
+            }
+        }
+    }
+    const float inv = 1.f / den;
+    uint8_t* out = static_cast<uint8_t*>(p.out) + ((int64_t)(q0 + j) * p.H + h) * (D * 2);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int c4 = lane + 32 * i;
+        if (c4 < D / 4)
+            *reinterpret_cast<uint2*>(out + c4 * 8) =
+                make_uint2(pack2<BF16>(acc[i].x * inv, acc[i].y * inv), pack2<BF16>(acc[i].z * inv, acc[i].w * inv));
+    }
+}
+
+template <bool BF16>
+cudaError_t launch_prefix_combine(const PrefixParams& p, int D, dim3 grid, cudaStream_t stream) {
+    pa_prefix_combine_kernel<BF16><<<grid, 256, 0, stream>>>(p, D);
+    return cudaGetLastError();
 }
 
 template <bool BF16, int D>

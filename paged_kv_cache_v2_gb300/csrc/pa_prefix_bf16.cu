@@ -5,4 +5,5 @@
 namespace pa {
 template PrefixFn prefix_select<true>(int d);
 template cudaError_t prefix_read_errors<true>(unsigned int* v, bool reset);
+template cudaError_t launch_prefix_combine<true>(const PrefixParams& p, int d, dim3 grid, cudaStream_t stream);
 }  // namespace pa

@@ -142,9 +142,11 @@ def prefix_to_device(wl, device="cuda"):
              "context_lens")}
 
 
-def run_prefix(wl, dev=None, max_query_len=None, poison=True, q_rows=None, kv_rows=None):
+def run_prefix(wl, dev=None, max_query_len=None, poison=True, q_rows=None, kv_rows=None, max_splits=None,
+               min_split_keys=0):
     """pa_prefix on a chunked-prefill workload; returns the CPU output [T, H, d].
-    q_rows / kv_rows: optional wider row buffers the inputs are copied into (strided views)."""
+    q_rows / kv_rows: optional wider row buffers the inputs are copied into (strided views);
+    max_splits / min_split_keys: how contexts are cut into parts (binding defaults)."""
     if dev is None:
         dev = prefix_to_device(wl)
     q, k, v = dev["query"], dev["key"], dev["value"]
@@ -162,7 +164,8 @@ def run_prefix(wl, dev=None, max_query_len=None, poison=True, q_rows=None, kv_ro
     out = torch.full(wl.query.shape, float("nan") if poison else 0.0, dtype=wl.query.dtype, device="cuda")
     mql = wl.max_query_len if max_query_len is None else max_query_len
     pa.pa_prefix(out, q, k, v, dev["key_cache"], dev["value_cache"], dev["block_tables"],
-                 dev["query_start_loc"], dev["context_lens"], mql, scale=wl.scale)
+                 dev["query_start_loc"], dev["context_lens"], mql, scale=wl.scale, max_splits=max_splits,
+                 min_split_keys=min_split_keys)
     torch.cuda.synchronize()
     return out.cpu()
 

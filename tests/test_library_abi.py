@@ -159,12 +159,13 @@ def _prefix_raw(**over):
     a = dict(output=P, query=P, key=P, value=P, key_cache=P, value_cache=P, num_seqs=2, num_heads=8,
              num_kv_heads=2, head_size=128, scale=0.088, block_tables=P, max_blocks_per_seq=64,
              num_blocks=100, qsl=P, ctx=P, max_query_len=0, block_size=16, q_stride=1024,
-             kv_stride=256, dtype=0)
+             kv_stride=256, dtype=0, ws=None, ws_bytes=0, max_splits=1, split_keys=0)
     a.update(over)
     return lib.pa_prefix(a["output"], a["query"], a["key"], a["value"], a["key_cache"], a["value_cache"],
                          a["num_seqs"], a["num_heads"], a["num_kv_heads"], a["head_size"], a["scale"],
                          a["block_tables"], a["max_blocks_per_seq"], a["num_blocks"], a["qsl"], a["ctx"],
-                         a["max_query_len"], a["block_size"], a["q_stride"], a["kv_stride"], a["dtype"], None)
+                         a["max_query_len"], a["block_size"], a["q_stride"], a["kv_stride"], a["dtype"], a["ws"],
+                         a["ws_bytes"], a["max_splits"], a["split_keys"], None)
 
 
 @pytest.mark.parametrize("over,status", [
@@ -182,3 +183,36 @@ def test_prefix_rejects_invalid_arguments_on_host(over, status):
 def test_prefix_with_nothing_to_do_is_a_noop():
     assert _prefix_raw(max_query_len=0) == 0
     assert _prefix_raw(num_seqs=0, max_query_len=9) == 0
+
+
+def test_prefix_workspace_size():
+    lib = pa.load()
+    # 2 sequences x 2 kv heads x ceil(100 * 4 / 128) = 4 row tiles x 4 parts x 128 rows x (128 * 4 + 8)
+    assert lib.pa_prefix_workspace_size(2, 8, 2, 128, 100, 4) == 2 * 2 * 4 * 4 * 128 * 520
+    assert lib.pa_prefix_workspace_size(1, 24, 4, 256, 1024, 6) == 4 * 48 * 6 * 128 * 1032
+    assert lib.pa_prefix_workspace_size(2, 8, 2, 128, 100, 1) == 0     # no splitting, no workspace
+    assert lib.pa_prefix_workspace_size(2, 8, 2, 128, 100, 33) == 0    # more parts than allowed
+    assert lib.pa_prefix_workspace_size(2, 6, 4, 128, 100, 4) == 0     # heads not a multiple
+    assert pa.prefix_workspace_size(2, 8, 2, 128, 100, 4) == 2 * 2 * 4 * 4 * 128 * 520
+
+
+_WS = 2 * 2 * 1 * 4 * 128 * 520  # 2 sequences x 2 kv heads x 1 row tile (5 tokens x 4) x 4 parts
+
+
+@pytest.mark.parametrize("over", [
+    dict(max_splits=33),                              # above the 32-part limit
+    dict(split_keys=100),                             # not a multiple of 64
+    dict(split_keys=-64),
+    dict(ws=0x10008),                                 # workspace not 16-byte aligned
+    dict(ws_bytes=_WS - 1),                           # one byte short
+])
+def test_prefix_rejects_bad_split_workspace(over):
+    args = dict(max_query_len=5, ws=0x20000, ws_bytes=_WS, max_splits=4)
+    args.update(over)
+    assert _prefix_raw(**args) == 1
+
+
+def test_prefix_ignores_workspace_arguments_when_not_splitting():
+    # max_splits <= 1 or no workspace: the split arguments are not looked at
+    assert _prefix_raw(max_query_len=0, ws=0x10008, ws_bytes=1, max_splits=1, split_keys=100) == 0
+    assert _prefix_raw(max_query_len=0, ws=None, ws_bytes=0, max_splits=8, split_keys=100) == 0

@@ -5,7 +5,9 @@ that include every chunk's first and last token and the 64-key tile edges.  Edge
 empty chunks and empty contexts, one-token chunks, contexts ending on and off tile and page
 boundaries, every supported head size and block size, GQA ratios 1..16, strided q/k/v rows,
 pages outside the cache (masked and flagged), contexts longer than the table (capped, as
-the pages do) and NaN canaries in every cache slot the method must not read."""
+the pages do) and NaN canaries in every cache slot the method must not read.  Contexts cut
+into parts (the split path and its combine) are checked the same way, at part lengths down
+to one 64-key tile and up to 32 parts."""
 from __future__ import annotations
 
 import numpy as np
@@ -36,12 +38,17 @@ def test_reduced_prefix_workloads_match_oracle(name):
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["prefix_long_gqa", "prefix_llama_gqa"])
 def test_full_size_prefix_sampled(name):
+    # the binding's defaults, as the benchmark runs them (the long contexts are cut into parts);
+    # the long workload also in one part per sequence
     wl = workloads.make_prefix(name)
-    out = run_prefix(wl)
     rows = prefix_sample_rows(wl, n=40)
-    check_prefix(wl, out, oracle.prefix_workload(wl, rows=rows), rows=rows, label=name)
-    assert torch.isfinite(out.float()).all()
-    assert pa.pa_get_device_errors() == 0
+    ref = oracle.prefix_workload(wl, rows=rows)
+    dev = prefix_to_device(wl)
+    for max_splits in ((None, 1) if name == "prefix_long_gqa" else (None,)):
+        out = run_prefix(wl, dev, max_splits=max_splits)
+        check_prefix(wl, out, ref, rows=rows, label=f"{name} max_splits={max_splits}")
+        assert torch.isfinite(out.float()).all()
+        assert pa.pa_get_device_errors() == 0
 
 
 CTX = [0, 1, 63, 64, 65, 200, 511, 1000]
@@ -145,3 +152,81 @@ def test_many_sequences_short_chunks():
     rows = prefix_sample_rows(wl, n=80)
     check_prefix(wl, out, oracle.prefix_workload(wl, rows=rows), rows=rows, label="many seqs")
     assert pa.pa_get_device_errors() == 0
+
+
+# ---- contexts cut into parts ----------------------------------------------------------------
+
+@pytest.mark.parametrize("max_splits", [2, 3, 8, 32])
+def test_split_contexts_match_oracle(max_splits):
+    # parts as short as one 64-key tile: every context above 64 tokens is cut (up to 16 tiles
+    # here, so 32 parts leaves one tile per part)
+    wl = workloads.build_prefix(num_seqs=len(CTX), num_heads=8, num_kv_heads=2, head_size=128, block_size=16,
+                                context_lens=CTX, query_lens=QL, q_dtype="bf16", seed=1200 + max_splits)
+    out = run_prefix(wl, max_splits=max_splits, min_split_keys=64)
+    check_prefix(wl, out, oracle.prefix_workload(wl), label=f"max_splits={max_splits}")
+    assert pa.pa_get_device_errors() == 0
+
+
+@pytest.mark.parametrize("d,bs,q_dtype", [(64, 8, "f16"), (80, 16, "bf16"), (192, 32, "bf16"),
+                                          (256, 16, "f16"), (256, 32, "bf16")])
+def test_split_head_sizes(d, bs, q_dtype):
+    # every tensor-memory plan (two S buffers, Q half in shared memory, one S buffer, P in
+    # shared memory) through the partial-result epilogue
+    ctx = [130, 640, 0, 64 * 9, 64 * 9 + 1, 1500]
+    ql = [33, 70, 20, 1, 128, 9]
+    wl = workloads.build_prefix(num_seqs=len(ctx), num_heads=8, num_kv_heads=2, head_size=d, block_size=bs,
+                                context_lens=ctx, query_lens=ql, q_dtype=q_dtype, seed=1300 + d + bs)
+    out = run_prefix(wl, max_splits=4, min_split_keys=128)
+    check_prefix(wl, out, oracle.prefix_workload(wl), label=f"split d{d} bs{bs} {q_dtype}")
+    assert pa.pa_get_device_errors() == 0
+
+
+def test_split_and_unsplit_agree_closely():
+    # the same inputs in one part and in parts: both within the oracle bar, and close to each
+    # other (they differ only by fp32 summation order and the final rounding)
+    wl = workloads.make_prefix("prefix_long_gqa", reduced=True)
+    dev = prefix_to_device(wl)
+    one = run_prefix(wl, dev, max_splits=1)
+    parts = run_prefix(wl, dev, max_splits=5, min_split_keys=64)
+    ref = oracle.prefix_workload(wl)
+    check_prefix(wl, one, ref, label="one part")
+    check_prefix(wl, parts, ref, label="parts")
+    assert (one.float() - parts.float()).abs().max().item() <= 4e-3
+
+
+def test_split_with_masked_page_and_capped_context():
+    # a page outside the cache in the middle part, and a context longer than its table row
+    wl = workloads.build_prefix(num_seqs=2, num_heads=4, num_kv_heads=2, head_size=64, block_size=16,
+                                context_lens=[400, 40], query_lens=[20, 9], seed=1400)
+    bad = wl.block_tables.clone()
+    bad[0, 10] = wl.num_blocks + 5  # context tokens 160..175 of sequence 0
+    out = run_prefix(workloads.PrefixWorkload(**{**wl.__dict__, "block_tables": bad}), max_splits=4,
+                     min_split_keys=64)
+    assert pa.pa_get_device_errors() & 32
+    t = wl.block_tables
+    ref_tables = torch.stack([torch.cat([t[0, :10], t[0, 11:]]), t[1, :-1]]).to(torch.int32)
+    ref_wl = workloads.PrefixWorkload(**{**wl.__dict__, "block_tables": ref_tables,
+                                         "context_lens": torch.tensor([384, 40], dtype=torch.int32)})
+    check_prefix(wl, out, oracle.prefix_workload(ref_wl), label="split masked page")
+
+    wl = workloads.build_prefix(num_seqs=1, num_heads=4, num_kv_heads=1, head_size=64, block_size=16,
+                                context_lens=[320], query_lens=[10], table_width=21, seed=1401)
+    kc, vc = wl.key_cache.clone(), wl.value_cache.clone()
+    b = int(wl.block_tables[0, 20])
+    g = torch.Generator().manual_seed(2)
+    kc[b] = torch.randn(kc[b].shape, generator=g).to(kc.dtype)
+    vc[b] = torch.randn(vc[b].shape, generator=g).to(vc.dtype)
+    capped = workloads.PrefixWorkload(**{**wl.__dict__, "key_cache": kc, "value_cache": vc,
+                                         "context_lens": torch.tensor([336], dtype=torch.int32)})
+    over = workloads.PrefixWorkload(**{**capped.__dict__, "context_lens": torch.tensor([1000], dtype=torch.int32)})
+    out = run_prefix(over, max_splits=3, min_split_keys=64)
+    assert pa.pa_get_device_errors() & 64
+    check_prefix(wl, out, oracle.prefix_workload(capped), label="split capped")
+
+
+def test_split_is_deterministic():
+    wl = workloads.make_prefix("prefix_llama_gqa", reduced=True)
+    dev = prefix_to_device(wl)
+    a = run_prefix(wl, dev, max_splits=6, min_split_keys=64)
+    b = run_prefix(wl, dev, max_splits=6, min_split_keys=64)
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
