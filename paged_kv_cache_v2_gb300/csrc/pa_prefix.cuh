@@ -295,6 +295,7 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
             }
             const uint32_t sK = sbase + C::OFF_K + slot * C::K_BYTES;
             const uint32_t sV = sbase + C::OFF_V + slot * C::V_BYTES;
+            bool generic = true;  // this warp wrote the slot through the generic proxy (cp.async / st.shared)
             if (t < n_ctx) {
                 const int t0 = (tb + t) * BN;
                 // pages of the tile whose id is outside the cache (masked); both teams compute
@@ -302,6 +303,7 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
                 const bool bad = lane < npg && t0 + (lane << p.bs_log2) < ctx && (unsigned)pid >= (unsigned)p.num_blocks;
                 const uint32_t m = __ballot_sync(0xffffffffu, bad);
                 const bool tma = m == 0 && t0 + BN <= ctx;  // a full tile of valid pages
+                generic = !tma;
                 if (lt < 32) {
                     if (lane == 0) {
                         if (kteam) {
@@ -413,9 +415,11 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
                     }
                 }
             }
-            cp_async_commit();
-            cp_async_wait<0>();
-            fence_proxy_async_smem();
+            if (generic) {  // make those writes visible to the tensor core before the arrive
+                cp_async_commit();
+                cp_async_wait<0>();
+                fence_proxy_async_smem();
+            }
             __syncwarp();
             if (lane == 0) mbar_arrive(full);
         }
@@ -425,26 +429,30 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
         if (lane == 0) {
             // S of tile t as soon as its keys are in and the softmax has read S of tile
             // t - NSB out of the same buffer
+            // Descriptors as a constant high half and a low half that is the start address
+            // (>> 4) plus the layout's fixed low bits: one add per MMA.  A lane that shares its
+            // sub-partition with a softmax warp gets few issue slots while that warp runs a
+            // dense stretch of arithmetic, so every instruction saved here shortens the chain.
+            const uint64_t kd0 = umma_desc(sbase + C::OFF_K, 128, C::DP * 16);
+            const uint32_t kd_lo = (uint32_t)kd0, kd_hi = (uint32_t)(kd0 >> 32);
+            const uint64_t qd0 = umma_desc(sbase + C::OFF_Q, kPfxBM * 16, 128);
+            const uint32_t qd_lo = (uint32_t)qd0, qd_hi = (uint32_t)(qd0 >> 32);
             bool ok = pfx_wait(q_full, 0, abort_flag);
             for (int t = 0; ok && t < n_tiles; ++t) {
                 ok = pfx_wait(&k_full[t % NK], (t / NK) & 1, abort_flag) &&
                      (t < NSB || pfx_wait(&s_empty[t % NSB], ((t / NSB) - 1) & 1, abort_flag));
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t sK = sbase + C::OFF_K + (t % NK) * C::K_BYTES;
+                const uint32_t k_lo = kd_lo + (uint32_t)((t % NK) * (C::K_BYTES >> 4));
                 const uint32_t d_s = tm + C::COL_S + (t % NSB) * BN;
 #pragma unroll
                 for (int ks = 0; ks < C::DP / 16; ++ks) {
-                    const uint64_t kd = umma_desc(sK + ks * 2 * 128, 128, C::DP * 16);
-                    if (ks < C::QT / 16) {
-                        asm volatile(
-                            "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-                            "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_s),
-                            "r"(tm + C::COL_Q + ks * 8), "l"(kd), "r"(C::IDESC_S), "r"(ks > 0 ? 1u : 0u));
-                    } else {
-                        umma_f16(d_s, umma_desc(sbase + C::OFF_Q + (ks - C::QT / 16) * 2 * (kPfxBM * 16), kPfxBM * 16, 128),
-                                 kd, C::IDESC_S, 1u);
-                    }
+                    // K step ks: 16 head elements = two 128-byte chunk columns of the key tile
+                    if (ks < C::QT / 16)
+                        umma_f16_ts(d_s, tm + C::COL_Q + ks * 8, k_lo + ks * 16, kd_hi, C::IDESC_S, ks > 0 ? 1u : 0u);
+                    else
+                        umma_f16_ss(d_s, qd_lo + (ks - C::QT / 16) * (2 * kPfxBM), qd_hi, k_lo + ks * 16, kd_hi,
+                                    C::IDESC_S, 1u);
                 }
                 umma_commit(&s_full[t % NSB]);
                 umma_commit(&k_empty[t % NK]);
@@ -457,35 +465,40 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
     } else if (warp == kPfxPvWarp) {
         // ------------------------------------------------------------------ value MMAs
         if (lane == 0) {
+            // value-tile descriptor: the block size fixes the layout; 16 keys (one K step) are
+            // two 8-row pages (block size 8), one page with the 32-byte swizzle (16) or half a
+            // page with the 64-byte swizzle (32), at these byte offsets in the tile
+            const uint64_t vd0 = p.bs_log2 == 3   ? umma_desc(sbase + C::OFF_V, C::DP * 16, 128)
+                                 : p.bs_log2 == 4 ? umma_desc_sw(sbase + C::OFF_V, 256, 6)
+                                                  : umma_desc_sw(sbase + C::OFF_V, 512, 4);
+            const uint32_t vd_lo = (uint32_t)vd0, vd_hi = (uint32_t)(vd0 >> 32);
+            uint32_t voff[BN / 16];
+#pragma unroll
+            for (int kk = 0; kk < BN / 16; ++kk)
+                voff[kk] = (uint32_t)(p.bs_log2 == 3   ? kk * 2 * (C::DP * 16)
+                                      : p.bs_log2 == 4 ? kk * (C::DP * 32)
+                                                       : (kk >> 1) * (C::DP * 64) + (kk & 1) * 32) >> 4;
+            const uint64_t pd0 = umma_desc(sbase + C::OFF_P, kPfxBM * 16, 128);
+            const uint32_t pd_lo = (uint32_t)pd0, pd_hi = (uint32_t)(pd0 >> 32);
             bool ok = true;
             for (int t = 0; ok && t < n_tiles; ++t) {
                 ok = pfx_wait(&p_full[t & 1], (t >> 1) & 1, abort_flag) && pfx_wait(&v_full[t % NV], (t / NV) & 1, abort_flag);
                 if (!ok) break;
                 tc_fence_after();
-                const uint32_t sV = sbase + C::OFF_V + (t % NV) * C::V_BYTES;
+                const uint32_t v_lo = vd_lo + (uint32_t)((t % NV) * (C::V_BYTES >> 4));
+                const uint32_t acc0 = t > 0 ? 1u : 0u;
 #pragma unroll
                 for (int h = 0; h < C::NP; ++h)
 #pragma unroll
                     for (int kk = 0; kk < BN / 16; ++kk) {
-                        // 16 keys of the value tile: two 8-row pages (block size 8), one page
-                        // with the 32-byte swizzle (16), half a page with the 64-byte swizzle (32)
-                        const uint64_t vd =
-                            p.bs_log2 == 3   ? umma_desc(sV + kk * 2 * (C::DP * 16), C::DP * 16, 128)
-                            : p.bs_log2 == 4 ? umma_desc_sw(sV + kk * (C::DP * 32), 256, 6)
-                                             : umma_desc_sw(sV + (kk >> 1) * (C::DP * 64) + (kk & 1) * 32, 512, 4);
-                        const uint32_t acc = (t > 0 || kk > 0 || h > 0) ? 1u : 0u;
-                        if constexpr (C::P_TMEM) {
-                            asm volatile(
-                                "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-                                "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(tm + C::COL_O),
-                                "r"(tm + C::COL_P + ((t & 1) * C::NP + h) * (BN / 2) + kk * 8), "l"(vd),
-                                "r"(C::IDESC_O), "r"(acc));
-                        } else {
-                            umma_f16(tm + C::COL_O,
-                                     umma_desc(sbase + C::OFF_P + ((t & 1) * C::NP + h) * C::P_BYTES + kk * 2 * (kPfxBM * 16),
-                                               kPfxBM * 16, 128),
-                                     vd, C::IDESC_O, acc);
-                        }
+                        const uint32_t acc = (kk > 0 || h > 0) ? 1u : acc0;
+                        if constexpr (C::P_TMEM)
+                            umma_f16_ts(tm + C::COL_O, tm + C::COL_P + ((t & 1) * C::NP + h) * (BN / 2) + kk * 8,
+                                        v_lo + voff[kk], vd_hi, C::IDESC_O, acc);
+                        else
+                            umma_f16_ss(tm + C::COL_O,
+                                        pd_lo + (((t & 1) * C::NP + h) * C::P_BYTES + kk * 2 * (kPfxBM * 16)) / 16, pd_hi,
+                                        v_lo + voff[kk], vd_hi, C::IDESC_O, acc);
                     }
                 umma_commit(&o_done[t & 1]);
                 umma_commit(&v_empty[t % NV]);
@@ -585,10 +598,24 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
             }
             const float mu = m_ref == -INFINITY ? 0.f : m_ref;
             float sum[4] = {0.f, 0.f, 0.f, 0.f};
+            // P in tensor memory is packed here, between the exponentials: the packing is
+            // dense integer / FMA work that, as one stretch, would hold the sub-partition's
+            // issue slots away from the MMA lanes for hundreds of cycles
+            uint32_t ph[BN / 2], pl[BN / 2];  // 16-bit pairs: P (bf16: its hi), and the bf16 lo
 #pragma unroll
-            for (int i = 0; i < BN; ++i) {
-                sv[i] = ex2(fmaf(sv[i], p.sl2, -mu));
-                sum[i & 3] += sv[i];
+            for (int e = 0; e < BN / 2; ++e) {
+                const float a = ex2(fmaf(sv[2 * e], p.sl2, -mu)), b = ex2(fmaf(sv[2 * e + 1], p.sl2, -mu));
+                sum[(2 * e) & 3] += a;
+                sum[(2 * e + 1) & 3] += b;
+                if constexpr (C::P_TMEM) {
+                    const uint32_t h2 = pack2<BF16>(a, b);
+                    ph[e] = h2;
+                    if constexpr (BF16)
+                        pl[e] = pack2<BF16>(a - __uint_as_float(h2 << 16), b - __uint_as_float(h2 & 0xffff0000u));
+                } else {
+                    sv[2 * e] = a;
+                    sv[2 * e + 1] = b;
+                }
             }
             l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
             // O must hold every earlier tile before it is rescaled; the P buffer of this tile's
@@ -611,18 +638,9 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
             }
             if constexpr (C::P_TMEM) {
                 // P row as packed 16-bit pairs into this lane's P columns (bf16: hi, then lo)
-                float hi[BN / 2], lo[BN / 2];
-#pragma unroll
-                for (int e = 0; e < BN / 2; ++e) {
-                    const uint32_t h2 = pack2<BF16>(sv[2 * e], sv[2 * e + 1]);
-                    hi[e] = __uint_as_float(h2);
-                    if constexpr (BF16)
-                        lo[e] = __uint_as_float(pack2<BF16>(sv[2 * e] - __uint_as_float(h2 << 16),
-                                                            sv[2 * e + 1] - __uint_as_float(h2 & 0xffff0000u)));
-                }
                 const uint32_t tp = tl + C::COL_P + (t & 1) * C::NP * (BN / 2);
-                tmem_st32(tp, *reinterpret_cast<const float(*)[32]>(&hi[0]));
-                if constexpr (BF16) tmem_st32(tp + BN / 2, *reinterpret_cast<const float(*)[32]>(&lo[0]));
+                tmem_st32(tp, *reinterpret_cast<const float(*)[32]>(&ph[0]));
+                if constexpr (BF16) tmem_st32(tp + BN / 2, *reinterpret_cast<const float(*)[32]>(&pl[0]));
                 tmem_wait_st();
             } else {
                 const uint32_t sP = sP0 + (t & 1) * (C::NP * C::P_BYTES);
