@@ -268,11 +268,12 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
     const int32_t* table = p.block_tables + (int64_t)s * p.mbps;
     const int64_t page_bytes = (int64_t)D * p.bs * 2;
 
-    if (warp >= kPfxLoaderWarp0 && warp < kPfxPvWarp) {
+    const bool kteam = warp >= kPfxKeyWarp0 && warp < kPfxKeyWarp0 + 2;
+    const bool vteam = warp >= kPfxValWarp0 && warp < kPfxValWarp0 + 2;
+    if (kteam || vteam) {
         // ------------------------------------------------------------------ loaders
-        // warps 5-6 fill the key ring, warps 7-8 the value ring; each team runs on its own
-        const bool kteam = warp < kPfxLoaderWarp0 + 2;
-        const int lt = tid - (kteam ? kPfxLoaderWarp0 : kPfxLoaderWarp0 + 2) * 32;  // 0 .. 63 in the team
+        // two warps fill the key ring, two the value ring; each team runs on its own
+        const int lt = tid - (kteam ? kPfxKeyWarp0 : kPfxValWarp0) * 32;  // 0 .. 63 in the team
         const int npg = BN >> p.bs_log2;  // pages per context tile
         // lane i < npg holds the block id of page i of a context tile (-1 past the context);
         // the ids of tile t + 1 are loaded while tile t is waited for and issued
@@ -509,10 +510,11 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
         __syncwarp();
     } else {
         // ------------------------------------------------------------------ softmax
-        const int r = warp * 32 + lane;
+        const int sw = warp - kPfxSoftmaxWarp0;  // = warp % 4: this warp's tensor-memory lane quarter
+        const int r = sw * 32 + lane;
         const int row = row0 + r;
         const int lim = row / G;  // newest chunk key this row sees (rows past the chunk are never stored)
-        const uint32_t tl = tm + ((uint32_t)(warp * 32) << 16);
+        const uint32_t tl = tm + ((uint32_t)(sw * 32) << 16);
         const uint32_t sP0 = sbase + C::OFF_P + r * 16;
         // this thread's query row into tensor memory (two 16-bit values per column; rows past
         // the chunk and the padding past D are zero)
@@ -585,9 +587,11 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
                 }
             }
             // row max in the exp2 domain (scale > 0 commutes with max); four independent chains
+            // of three-input maxima.  The arithmetic below runs two lanes per instruction
+            // where it can: fewer issue slots for the same work leave more to the MMA lanes.
             float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int i = 0; i < BN; ++i) mx[i & 3] = fmaxf(mx[i & 3], sv[i]);
+            for (int e = 0; e < BN / 2; ++e) mx[e & 3] = fmax3(mx[e & 3], sv[2 * e], sv[2 * e + 1]);
             const float mt = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * p.sl2;
             const bool need = mt > m_ref + 8.f;
             float corr = 1.f;
@@ -597,27 +601,31 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
                 l *= corr;
             }
             const float mu = m_ref == -INFINITY ? 0.f : m_ref;
-            float sum[4] = {0.f, 0.f, 0.f, 0.f};
+            const float2 sl2v = make_float2(p.sl2, p.sl2), nmu = make_float2(-mu, -mu);
+            float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};  // keys 4k, 4k+1 | 4k+2, 4k+3
             // P in tensor memory is packed here, between the exponentials: the packing is
             // dense integer / FMA work that, as one stretch, would hold the sub-partition's
             // issue slots away from the MMA lanes for hundreds of cycles
             uint32_t ph[BN / 2], pl[BN / 2];  // 16-bit pairs: P (bf16: its hi), and the bf16 lo
 #pragma unroll
             for (int e = 0; e < BN / 2; ++e) {
-                const float a = ex2(fmaf(sv[2 * e], p.sl2, -mu)), b = ex2(fmaf(sv[2 * e + 1], p.sl2, -mu));
-                sum[(2 * e) & 3] += a;
-                sum[(2 * e + 1) & 3] += b;
+                const float2 x = ffma2(make_float2(sv[2 * e], sv[2 * e + 1]), sl2v, nmu);
+                const float a = ex2(x.x), b = ex2(x.y);
+                sum2[e & 1] = fadd2(sum2[e & 1], make_float2(a, b));
                 if constexpr (C::P_TMEM) {
                     const uint32_t h2 = pack2<BF16>(a, b);
                     ph[e] = h2;
-                    if constexpr (BF16)
-                        pl[e] = pack2<BF16>(a - __uint_as_float(h2 << 16), b - __uint_as_float(h2 & 0xffff0000u));
+                    if constexpr (BF16) {
+                        const float2 d = fsub2(make_float2(a, b),
+                                               make_float2(__uint_as_float(h2 << 16), __uint_as_float(h2 & 0xffff0000u)));
+                        pl[e] = pack2<BF16>(d.x, d.y);
+                    }
                 } else {
                     sv[2 * e] = a;
                     sv[2 * e + 1] = b;
                 }
             }
-            l += (sum[0] + sum[1]) + (sum[2] + sum[3]);
+            l += (sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y);
             // O must hold every earlier tile before it is rescaled; the P buffer of this tile's
             // parity must have been read by the value MMA of tile t - 2
             if (t > 0 && __any_sync(0xffffffffu, need)) {
