@@ -148,8 +148,11 @@ extern "C" pa_status pa_prefix(void* output, const void* query, const void* key,
     p.q_stride = q_row_stride;
     p.kv_stride = kv_row_stride;
     p.sl2 = scale * kLog2e;
-    const int64_t row_tiles = prefix_row_tiles(max_query_len, G);
-    p.mt = (int)row_tiles;
+    const int64_t row_tiles = prefix_row_tiles(max_query_len, G);  // of 128 rows: the workspace's unit
+    const int cta_rows = bf16 ? prefix_tile_rows<true>(head_size) : prefix_tile_rows<false>(head_size);
+    const int64_t cta_tiles = ((int64_t)max_query_len * G + cta_rows - 1) / cta_rows;
+    p.mt = (int)cta_tiles;
+    p.mt_ws = (int)row_tiles;
     p.split_tiles = (min_split_keys > 0 ? min_split_keys : kDefaultSplitKeys) / 64;
     // no more splits than the longest context the tables can hold would use
     const int64_t max_ctx_tiles = ((int64_t)max_blocks_per_seq * block_size + 63) / 64;
@@ -164,7 +167,7 @@ extern "C" pa_status pa_prefix(void* output, const void* query, const void* key,
     }
     if (row_tiles * p.nsplit > INT32_MAX || ((int64_t)max_query_len * num_heads + 7) / 8 > INT32_MAX)
         return PA_ERR_INVALID_ARG;
-    const dim3 grid((unsigned)(row_tiles * p.nsplit), (unsigned)num_kv_heads, (unsigned)num_seqs);
+    const dim3 grid((unsigned)(cta_tiles * p.nsplit), (unsigned)num_kv_heads, (unsigned)num_seqs);
     cudaEvent_t t_begin, t_end;
     timing_events(&t_begin, &t_end);
     if (t_begin != nullptr) cudaEventRecord(t_begin, stream);

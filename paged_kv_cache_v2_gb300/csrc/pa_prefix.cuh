@@ -157,6 +157,203 @@ __device__ __forceinline__ bool pfx_warp_wait(uint64_t* bar, uint32_t parity, vo
     return ok != 0;
 }
 
+// Zero the slot bytes the copies never write: key chunks c >= D/8 of every key slot, value
+// rows d >= D of every value slot (the MMAs read the head size padded to 16).
+template <class C, int D>
+__device__ __forceinline__ void pfx_zero_padding(uint8_t* smem, const PrefixParams& p, int tid, int nthreads) {
+    constexpr int BN = C::BN, NK = C::NK, NV = C::NV;
+    if constexpr (C::NCP > C::NCR) {
+        constexpr int kpad = (C::NCP - C::NCR) * BN, vpad = (BN / 8) * (C::DP - D);
+        for (int i = tid; i < NK * kpad + NV * vpad; i += nthreads) {
+            uint8_t* dst;
+            if (i < NK * kpad) {
+                const int slot = i / kpad, rem = i % kpad;
+                const int o = rem % BN, c = C::NCR + rem / BN;
+                dst = smem + C::OFF_K + slot * C::K_BYTES + (o >> 3) * (C::DP * 16) + c * 128 + (o & 7) * 16;
+            } else {
+                const int j = i - NK * kpad, slot = j / vpad, rem = j % vpad;
+                const int kc = rem / (C::DP - D), dd = D + rem % (C::DP - D);
+                const int cpp_log2 = p.bs_log2 - 3;  // 16-byte chunks per value row, log2
+                dst = smem + C::OFF_V + slot * C::V_BYTES + (kc >> cpp_log2) * (C::DP << (p.bs_log2 + 1)) +
+                      (dd << (p.bs_log2 + 1)) + ((kc & ((1 << cpp_log2) - 1)) << 4);
+            }
+            *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+}
+
+// The key range one CTA attends: context tiles [tb, tb + n_ctx) of a sequence with ctx cached
+// tokens (context tile i holds tokens 64 i ..), then, in the sequence's last split, the chunk's
+// tiles; n_tiles in all.  Chunk rows are q0 .. q0 + q_len - 1 of key/value.
+struct PfxRange {
+    int tb, n_ctx, ctx, n_tiles, q0, q_len, kvh;
+    const int32_t* table;  // the sequence's block-table row
+};
+
+// Loader role of the prefix kernels: a team of TEAM threads (whole warps; lanes of the first
+// warp issue the tensor copies) fills the key ring (kteam) or the value ring of the layout C.
+// lt = thread index in the team.
+template <class C, int D, int TEAM>
+__device__ __forceinline__ void pfx_load_tiles(const PrefixParams& p, const PfxRange& g, bool kteam, int lt, int lane,
+                                               uint32_t sbase, uint64_t* k_full, uint64_t* k_empty, uint64_t* v_full,
+                                               uint64_t* v_empty, uint32_t* bad_mask, volatile int* abort_flag) {
+    constexpr int BN = C::BN, NK = C::NK, NV = C::NV;
+    const int tb = g.tb, n_ctx = g.n_ctx, ctx = g.ctx, n_tiles = g.n_tiles, q0 = g.q0, q_len = g.q_len, kvh = g.kvh;
+    const int32_t* table = g.table;
+    const int64_t page_bytes = (int64_t)D * p.bs * 2;
+    const int npg = BN >> p.bs_log2;  // pages per context tile
+    // lane i < npg holds the block id of page i of a context tile (-1 past the context);
+    // the ids of tile t + 1 are loaded while tile t is waited for and issued
+    auto tile_page = [&](int t) {
+        int b = -1;
+        if (t < n_ctx && lane < npg && (tb + t) * BN + (lane << p.bs_log2) < ctx)
+            b = table[(((tb + t) * BN) >> p.bs_log2) + lane];
+        return b;
+    };
+    int pid_next = tile_page(0);
+    for (int t = 0; t < n_tiles; ++t) {
+        const int pid = pid_next;
+        pid_next = tile_page(t + 1);
+        const int slot = kteam ? t % NK : t % NV;
+        uint64_t* full = kteam ? &k_full[slot] : &v_full[slot];
+        if (kteam ? t >= NK : t >= NV) {
+            if (!pfx_warp_wait(kteam ? &k_empty[slot] : &v_empty[slot], ((t / (kteam ? NK : NV)) - 1) & 1,
+                               abort_flag, lane))
+                break;
+        }
+        const uint32_t sK = sbase + C::OFF_K + slot * C::K_BYTES;
+        const uint32_t sV = sbase + C::OFF_V + slot * C::V_BYTES;
+        bool generic = true;  // this warp wrote the slot through the generic proxy (cp.async / st.shared)
+        if (t < n_ctx) {
+            const int t0 = (tb + t) * BN;
+            // pages of the tile whose id is outside the cache (masked); both teams compute
+            // the same mask
+            const bool bad = lane < npg && t0 + (lane << p.bs_log2) < ctx && (unsigned)pid >= (unsigned)p.num_blocks;
+            const uint32_t m = __ballot_sync(0xffffffffu, bad);
+            const bool tma = m == 0 && t0 + BN <= ctx;  // a full tile of valid pages
+            generic = !tma;
+            if (lt < 32) {
+                if (lane == 0) {
+                    if (kteam) {
+                        bad_mask[slot] = m;
+                        if (m) prefix_flag(32u);
+                    }
+                    if (tma)
+                        mbar_arrive_expect_tx(full, 2u * BN * D);
+                    else
+                        mbar_arrive(full);
+                }
+                __syncwarp();
+                if (tma && kteam) {
+                    // keys: tensor copies of 128-byte rows, one box of 8 tokens per lane
+                    const int kpage = __shfl_sync(0xffffffffu, pid, (8 * lane) >> p.bs_log2 & 31) * p.Hk + kvh;
+                    if (lane < BN / 8)
+                        tma_load_4d(sK + lane * (C::DP * 16), &p.kmap, 0, ((8 * lane) & (p.bs - 1)) >> 3, 0, kpage,
+                                    full);
+                } else if (tma && lane < npg) {
+                    // values: one whole page per lane, swizzled as the value MMA reads it
+                    const int vpage = pid * p.Hk + kvh;
+                    const uint32_t dst = sV + lane * (C::DP << (p.bs_log2 + 1));
+                    if (p.bs_log2 == 3)
+                        bulk_load(dst, p.vcache + (int64_t)vpage * page_bytes, (uint32_t)page_bytes, full);
+                    else
+                        tma_load_3d(dst, &p.vmap, 0, 0, vpage, full);
+                }
+            }
+            if (!tma && kteam) {
+                // keys of the context's last tile or of a tile with a page outside the cache:
+                // 16-byte pieces, past the context or of a masked page zero-filled
+                const int kper = C::NCR << p.bs_log2;
+                for (int base = 0; base < BN * C::NCR; base += TEAM) {
+                    const int i = base + lt;
+                    const bool act = i < BN * C::NCR;
+                    const int pg = act ? i / kper : 0, rem = i - pg * kper;
+                    const int b = __shfl_sync(0xffffffffu, pid, pg);
+                    if (act) {
+                        const int c = rem >> p.bs_log2, sl = rem & (p.bs - 1);
+                        const int o = (pg << p.bs_log2) + sl;
+                        const bool ok = t0 + o < ctx && (unsigned)b < (unsigned)p.num_blocks;
+                        const uint8_t* src = ok ? p.kcache + ((int64_t)b * p.Hk + kvh) * page_bytes +
+                                                      (int64_t)(c * p.bs + sl) * 16
+                                                : p.kcache;
+                        cp_async16(sK + (o >> 3) * (C::DP * 16) + c * 128 + (o & 7) * 16, src, ok ? 16u : 0u);
+                    }
+                }
+            } else if (!tma) {
+                // values: 8-key pieces of each page row; the part past the context or of a
+                // masked page reads as zero
+                const int kpp_log2 = p.bs_log2 - 3;
+                const int vper = D << kpp_log2;
+                for (int base = 0; base < (BN / 8) * D; base += TEAM) {
+                    const int i = base + lt;
+                    const bool act = i < (BN / 8) * D;
+                    const int pg = act ? i / vper : 0, rem = i - pg * vper;
+                    const int b = __shfl_sync(0xffffffffu, pid, pg);
+                    if (act) {
+                        const int dd = rem >> kpp_log2, kq = rem & ((1 << kpp_log2) - 1);
+                        const int o = (pg << p.bs_log2) + kq * 8;
+                        const int nv = min(max(ctx - t0 - o, 0), 8);
+                        const bool ok = nv > 0 && (unsigned)b < (unsigned)p.num_blocks;
+                        const uint8_t* src = ok ? p.vcache + ((int64_t)b * p.Hk + kvh) * page_bytes +
+                                                      ((int64_t)dd * p.bs + kq * 8) * 2
+                                                : p.vcache;
+                        cp_async16(sV + pfx_v_off(o, dd, p.bs_log2, C::DP), src, ok ? (uint32_t)nv * 2u : 0u);
+                    }
+                }
+            }
+        } else {
+            const int kc0 = (t - n_ctx) * BN;
+            if (lt == 0) mbar_arrive(full);  // no tensor copies for chunk tiles
+            if (kteam) {
+                for (int i = lt; i < BN * C::NCR; i += TEAM) {
+                    const int c = i / BN, o = i % BN;
+                    const int j = kc0 + o;
+                    const bool ok = j < q_len;
+                    const uint8_t* src =
+                        ok ? p.k + ((int64_t)(q0 + j) * p.kv_stride + (int64_t)kvh * D + c * 8) * 2 : p.k;
+                    cp_async16(sK + (o >> 3) * (C::DP * 16) + c * 128 + (o & 7) * 16, src, ok ? 16u : 0u);
+                }
+            } else {
+                // dense value rows, two tokens at a time, transposed into the value layout;
+                // the loads of four such pieces are in flight together
+                constexpr int ITEMS = (BN / 2) * C::NCR, BATCH = 4;
+                for (int i0 = 0; i0 < ITEMS; i0 += TEAM * BATCH) {
+                    uint4 a[BATCH], b[BATCH];
+#pragma unroll
+                    for (int u = 0; u < BATCH; ++u) {
+                        const int i = i0 + u * TEAM + lt;
+                        const int c = i % C::NCR, t2 = 2 * (i / C::NCR), j = kc0 + t2;
+                        const uint8_t* vb = p.v + ((int64_t)kvh * D + c * 8) * 2;
+                        a[u] = b[u] = make_uint4(0u, 0u, 0u, 0u);
+                        if (i < ITEMS && j < q_len) a[u] = ld_nc_v4(vb + (int64_t)(q0 + j) * p.kv_stride * 2);
+                        if (i < ITEMS && j + 1 < q_len) b[u] = ld_nc_v4(vb + (int64_t)(q0 + j + 1) * p.kv_stride * 2);
+                    }
+#pragma unroll
+                    for (int u = 0; u < BATCH; ++u) {
+                        const int i = i0 + u * TEAM + lt;
+                        if (i >= ITEMS) continue;
+                        const int c = i % C::NCR, t2 = 2 * (i / C::NCR);
+                        const uint32_t av[4] = {a[u].x, a[u].y, a[u].z, a[u].w};
+                        const uint32_t bv[4] = {b[u].x, b[u].y, b[u].z, b[u].w};
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            sts_u32(sV + pfx_v_off(t2, c * 8 + e, p.bs_log2, C::DP) + (t2 & 7) * 2,
+                                    __byte_perm(av[e >> 1], bv[e >> 1], (e & 1) ? 0x7632 : 0x5410));
+                    }
+                }
+            }
+        }
+        if (generic) {  // make those writes visible to the tensor core before the arrive
+            cp_async_commit();
+            cp_async_wait<0>();
+            fence_proxy_async_smem();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(full);
+    }
+    cp_async_wait<0>();
+}
+
 template <bool BF16, int D>
 __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_constant__ PrefixParams p) {
     using C = PfxCfg<BF16, D>;
@@ -239,26 +436,7 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
         *abort_flag = 0;
         fence_mbar_init();
     }
-    // Padding the copies never write: key chunks c >= D/8 of every key slot, value rows d >= D
-    // of every value slot.
-    if constexpr (C::NCP > C::NCR) {
-        constexpr int kpad = (C::NCP - C::NCR) * BN, vpad = (BN / 8) * (C::DP - D);
-        for (int i = tid; i < NK * kpad + NV * vpad; i += kPfxThreads) {
-            uint8_t* dst;
-            if (i < NK * kpad) {
-                const int slot = i / kpad, rem = i % kpad;
-                const int o = rem % BN, c = C::NCR + rem / BN;
-                dst = smem + C::OFF_K + slot * C::K_BYTES + (o >> 3) * (C::DP * 16) + c * 128 + (o & 7) * 16;
-            } else {
-                const int j = i - NK * kpad, slot = j / vpad, rem = j % vpad;
-                const int kc = rem / (C::DP - D), dd = D + rem % (C::DP - D);
-                const int cpp_log2 = p.bs_log2 - 3;  // 16-byte chunks per value row, log2
-                dst = smem + C::OFF_V + slot * C::V_BYTES + (kc >> cpp_log2) * (C::DP << (p.bs_log2 + 1)) +
-                      (dd << (p.bs_log2 + 1)) + ((kc & ((1 << cpp_log2) - 1)) << 4);
-            }
-            *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
-        }
-    }
+    pfx_zero_padding<C, D>(smem, p, tid, kPfxThreads);
     fence_proxy_async_smem();
     if (warp == kPfxMmaWarp) tmem_alloc(tmem_slot, C::TMEM_COLS);
     tc_fence_before();
@@ -266,165 +444,15 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
     tc_fence_after();
     const uint32_t tm = *tmem_slot;
     const int32_t* table = p.block_tables + (int64_t)s * p.mbps;
-    const int64_t page_bytes = (int64_t)D * p.bs * 2;
-
+    const PfxRange rng{tb, n_ctx, ctx, n_tiles, q0, q_len, kvh, table};
     const bool kteam = warp >= kPfxKeyWarp0 && warp < kPfxKeyWarp0 + 2;
     const bool vteam = warp >= kPfxValWarp0 && warp < kPfxValWarp0 + 2;
     if (kteam || vteam) {
         // ------------------------------------------------------------------ loaders
         // two warps fill the key ring, two the value ring; each team runs on its own
         const int lt = tid - (kteam ? kPfxKeyWarp0 : kPfxValWarp0) * 32;  // 0 .. 63 in the team
-        const int npg = BN >> p.bs_log2;  // pages per context tile
-        // lane i < npg holds the block id of page i of a context tile (-1 past the context);
-        // the ids of tile t + 1 are loaded while tile t is waited for and issued
-        auto tile_page = [&](int t) {
-            int b = -1;
-            if (t < n_ctx && lane < npg && (tb + t) * BN + (lane << p.bs_log2) < ctx)
-                b = table[(((tb + t) * BN) >> p.bs_log2) + lane];
-            return b;
-        };
-        int pid_next = tile_page(0);
-        for (int t = 0; t < n_tiles; ++t) {
-            const int pid = pid_next;
-            pid_next = tile_page(t + 1);
-            const int slot = kteam ? t % NK : t % NV;
-            uint64_t* full = kteam ? &k_full[slot] : &v_full[slot];
-            if (kteam ? t >= NK : t >= NV) {
-                if (!pfx_warp_wait(kteam ? &k_empty[slot] : &v_empty[slot], ((t / (kteam ? NK : NV)) - 1) & 1,
-                                   abort_flag, lane))
-                    break;
-            }
-            const uint32_t sK = sbase + C::OFF_K + slot * C::K_BYTES;
-            const uint32_t sV = sbase + C::OFF_V + slot * C::V_BYTES;
-            bool generic = true;  // this warp wrote the slot through the generic proxy (cp.async / st.shared)
-            if (t < n_ctx) {
-                const int t0 = (tb + t) * BN;
-                // pages of the tile whose id is outside the cache (masked); both teams compute
-                // the same mask
-                const bool bad = lane < npg && t0 + (lane << p.bs_log2) < ctx && (unsigned)pid >= (unsigned)p.num_blocks;
-                const uint32_t m = __ballot_sync(0xffffffffu, bad);
-                const bool tma = m == 0 && t0 + BN <= ctx;  // a full tile of valid pages
-                generic = !tma;
-                if (lt < 32) {
-                    if (lane == 0) {
-                        if (kteam) {
-                            bad_mask[slot] = m;
-                            if (m) prefix_flag(32u);
-                        }
-                        if (tma)
-                            mbar_arrive_expect_tx(full, 2u * BN * D);
-                        else
-                            mbar_arrive(full);
-                    }
-                    __syncwarp();
-                    if (tma && kteam) {
-                        // keys: tensor copies of 128-byte rows, one box of 8 tokens per lane
-                        const int kpage = __shfl_sync(0xffffffffu, pid, (8 * lane) >> p.bs_log2 & 31) * p.Hk + kvh;
-                        if (lane < BN / 8)
-                            tma_load_4d(sK + lane * (C::DP * 16), &p.kmap, 0, ((8 * lane) & (p.bs - 1)) >> 3, 0, kpage,
-                                        full);
-                    } else if (tma && lane < npg) {
-                        // values: one whole page per lane, swizzled as the value MMA reads it
-                        const int vpage = pid * p.Hk + kvh;
-                        const uint32_t dst = sV + lane * (C::DP << (p.bs_log2 + 1));
-                        if (p.bs_log2 == 3)
-                            bulk_load(dst, p.vcache + (int64_t)vpage * page_bytes, (uint32_t)page_bytes, full);
-                        else
-                            tma_load_3d(dst, &p.vmap, 0, 0, vpage, full);
-                    }
-                }
-                if (!tma && kteam) {
-                    // keys of the context's last tile or of a tile with a page outside the cache:
-                    // 16-byte pieces, past the context or of a masked page zero-filled
-                    const int kper = C::NCR << p.bs_log2;
-                    for (int base = 0; base < BN * C::NCR; base += 64) {
-                        const int i = base + lt;
-                        const bool act = i < BN * C::NCR;
-                        const int pg = act ? i / kper : 0, rem = i - pg * kper;
-                        const int b = __shfl_sync(0xffffffffu, pid, pg);
-                        if (act) {
-                            const int c = rem >> p.bs_log2, sl = rem & (p.bs - 1);
-                            const int o = (pg << p.bs_log2) + sl;
-                            const bool ok = t0 + o < ctx && (unsigned)b < (unsigned)p.num_blocks;
-                            const uint8_t* src = ok ? p.kcache + ((int64_t)b * p.Hk + kvh) * page_bytes +
-                                                          (int64_t)(c * p.bs + sl) * 16
-                                                    : p.kcache;
-                            cp_async16(sK + (o >> 3) * (C::DP * 16) + c * 128 + (o & 7) * 16, src, ok ? 16u : 0u);
-                        }
-                    }
-                } else if (!tma) {
-                    // values: 8-key pieces of each page row; the part past the context or of a
-                    // masked page reads as zero
-                    const int kpp_log2 = p.bs_log2 - 3;
-                    const int vper = D << kpp_log2;
-                    for (int base = 0; base < (BN / 8) * D; base += 64) {
-                        const int i = base + lt;
-                        const bool act = i < (BN / 8) * D;
-                        const int pg = act ? i / vper : 0, rem = i - pg * vper;
-                        const int b = __shfl_sync(0xffffffffu, pid, pg);
-                        if (act) {
-                            const int dd = rem >> kpp_log2, kq = rem & ((1 << kpp_log2) - 1);
-                            const int o = (pg << p.bs_log2) + kq * 8;
-                            const int nv = min(max(ctx - t0 - o, 0), 8);
-                            const bool ok = nv > 0 && (unsigned)b < (unsigned)p.num_blocks;
-                            const uint8_t* src = ok ? p.vcache + ((int64_t)b * p.Hk + kvh) * page_bytes +
-                                                          ((int64_t)dd * p.bs + kq * 8) * 2
-                                                    : p.vcache;
-                            cp_async16(sV + pfx_v_off(o, dd, p.bs_log2, C::DP), src, ok ? (uint32_t)nv * 2u : 0u);
-                        }
-                    }
-                }
-            } else {
-                const int kc0 = (t - n_ctx) * BN;
-                if (lt == 0) mbar_arrive(full);  // no tensor copies for chunk tiles
-                if (kteam) {
-                    for (int i = lt; i < BN * C::NCR; i += 64) {
-                        const int c = i / BN, o = i % BN;
-                        const int j = kc0 + o;
-                        const bool ok = j < q_len;
-                        const uint8_t* src =
-                            ok ? p.k + ((int64_t)(q0 + j) * p.kv_stride + (int64_t)kvh * D + c * 8) * 2 : p.k;
-                        cp_async16(sK + (o >> 3) * (C::DP * 16) + c * 128 + (o & 7) * 16, src, ok ? 16u : 0u);
-                    }
-                } else {
-                    // dense value rows, two tokens at a time, transposed into the value layout;
-                    // the loads of four such pieces are in flight together
-                    constexpr int ITEMS = (BN / 2) * C::NCR, BATCH = 4;
-                    for (int i0 = 0; i0 < ITEMS; i0 += 64 * BATCH) {
-                        uint4 a[BATCH], b[BATCH];
-#pragma unroll
-                        for (int u = 0; u < BATCH; ++u) {
-                            const int i = i0 + u * 64 + lt;
-                            const int c = i % C::NCR, t2 = 2 * (i / C::NCR), j = kc0 + t2;
-                            const uint8_t* vb = p.v + ((int64_t)kvh * D + c * 8) * 2;
-                            a[u] = b[u] = make_uint4(0u, 0u, 0u, 0u);
-                            if (i < ITEMS && j < q_len) a[u] = ld_nc_v4(vb + (int64_t)(q0 + j) * p.kv_stride * 2);
-                            if (i < ITEMS && j + 1 < q_len) b[u] = ld_nc_v4(vb + (int64_t)(q0 + j + 1) * p.kv_stride * 2);
-                        }
-#pragma unroll
-                        for (int u = 0; u < BATCH; ++u) {
-                            const int i = i0 + u * 64 + lt;
-                            if (i >= ITEMS) continue;
-                            const int c = i % C::NCR, t2 = 2 * (i / C::NCR);
-                            const uint32_t av[4] = {a[u].x, a[u].y, a[u].z, a[u].w};
-                            const uint32_t bv[4] = {b[u].x, b[u].y, b[u].z, b[u].w};
-#pragma unroll
-                            for (int e = 0; e < 8; ++e)
-                                sts_u32(sV + pfx_v_off(t2, c * 8 + e, p.bs_log2, C::DP) + (t2 & 7) * 2,
-                                        __byte_perm(av[e >> 1], bv[e >> 1], (e & 1) ? 0x7632 : 0x5410));
-                        }
-                    }
-                }
-            }
-            if (generic) {  // make those writes visible to the tensor core before the arrive
-                cp_async_commit();
-                cp_async_wait<0>();
-                fence_proxy_async_smem();
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(full);
-        }
-        cp_async_wait<0>();
+        pfx_load_tiles<C, D, 64>(p, rng, kteam, lt, lane, sbase, k_full, k_empty, v_full, v_empty, bad_mask,
+                                 abort_flag);
     } else if (warp == kPfxMmaWarp) {
         // ------------------------------------------------------------------ score MMAs
         if (lane == 0) {
@@ -678,7 +706,7 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
             // one split of several: O (fp32, relative to the reference max) and the row's
             // (reference max, sum) go to the workspace for the combine
             tc_fence_after();
-            const int64_t item = (((int64_t)s * p.Hk + kvh) * p.mt + row0 / kPfxBM) * p.nsplit + split;
+            const int64_t item = (((int64_t)s * p.Hk + kvh) * p.mt_ws + row0 / kPfxBM) * p.nsplit + split;
             float* wrow = row < rows_total ? p.ws_o + (item * kPfxBM + r) * D : nullptr;
 #pragma unroll 1
             for (int c = 0; c < C::DPR / 32; ++c) {
@@ -749,7 +777,7 @@ __global__ void __launch_bounds__(256) pa_prefix_combine_kernel(const PrefixPara
     const int ns = pfx_split_plan((ctx + 63) / 64, p.nsplit, p.split_tiles).x;
     if (ns == 1) return;
     const int kvh = h / p.G, r = j * p.G + (h - kvh * p.G);
-    const int64_t item0 = (((int64_t)s * p.Hk + kvh) * p.mt + r / kPfxBM) * p.nsplit;
+    const int64_t item0 = (((int64_t)s * p.Hk + kvh) * p.mt_ws + r / kPfxBM) * p.nsplit;
     const int rt = r % kPfxBM;
     float2 ml = make_float2(-INFINITY, 0.f);
     if (lane < ns) ml = p.ws_ml[(item0 + lane) * kPfxBM + rt];
@@ -800,21 +828,6 @@ cudaError_t launch_prefix_kernel(const PrefixParams& p, dim3 grid, cudaStream_t 
     if (e != cudaSuccess) return e;
     pa_prefix_kernel<BF16, D><<<grid, kPfxThreads, C::SMEM, stream>>>(p);
     return cudaGetLastError();
-}
-
-template <bool BF16>
-PrefixFn prefix_select(int d) {
-    switch (d) {
-        case 64: return launch_prefix_kernel<BF16, 64>;
-        case 80: return launch_prefix_kernel<BF16, 80>;
-        case 96: return launch_prefix_kernel<BF16, 96>;
-        case 112: return launch_prefix_kernel<BF16, 112>;
-        case 120: return launch_prefix_kernel<BF16, 120>;
-        case 128: return launch_prefix_kernel<BF16, 128>;
-        case 192: return launch_prefix_kernel<BF16, 192>;
-        case 256: return launch_prefix_kernel<BF16, 256>;
-        default: return nullptr;
-    }
 }
 
 template <bool BF16>

@@ -36,11 +36,12 @@ struct PrefixParams {
     int H, Hk, G, bs, bs_log2, mbps, num_blocks, max_query_len;
     int64_t q_stride, kv_stride;  // elements between consecutive tokens
     float sl2;                    // scale * log2(e)
-    // Split contexts: the grid's x is mt row tiles x nsplit splits.  A sequence with more
-    // than split_tiles 64-key context tiles is cut into at most nsplit parts whose partial
-    // results (O rows of d fp32 values, and a (reference max, sum) pair per row) go to ws_o /
-    // ws_ml at [((s * Hk + kvh) * mt + row tile) * nsplit + split][128 rows].
-    int mt, nsplit, split_tiles;
+    // Split contexts: the grid's x is mt row tiles (of the kernel's rows per CTA) x nsplit
+    // splits.  A sequence with more than split_tiles 64-key context tiles is cut into at most
+    // nsplit parts whose partial results (O rows of d fp32 values, and a (reference max, sum)
+    // pair per row) go to ws_o / ws_ml at [((s * Hk + kvh) * mt_ws + r / 128) * nsplit +
+    // split][r % 128] for row r = j * G + g of the kv head's group.
+    int mt, mt_ws, nsplit, split_tiles;
     float* ws_o;
     float2* ws_ml;
 };
@@ -52,6 +53,10 @@ template <bool BF16>
 PrefixFn prefix_select(int d);
 template <bool BF16>
 cudaError_t prefix_read_errors(unsigned int* v, bool reset);
+// Query rows per CTA of the kernel prefix_select picks (128, or 256 where two row groups share
+// each key/value tile).
+template <bool BF16>
+int prefix_tile_rows(int d);
 // The combine of split partial results (grid: ceil(max_query_len * H / 8) x num_seqs).
 template <bool BF16>
 cudaError_t launch_prefix_combine(const PrefixParams& p, int d, dim3 grid, cudaStream_t stream);
