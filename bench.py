@@ -41,8 +41,8 @@ L2_BYTES = 129 * 1024 * 1024
 _CSRC = os.path.join(ROOT, "paged_kv_cache_v2_gb300", "csrc")
 KERNEL_SRCS = {
     "phase1": [os.path.join(_CSRC, f) for f in ("pa_phase1.cuh", "pa_kernels.cuh", "pa_ptx.cuh")],
-    "prefix": [os.path.join(_CSRC, f) for f in ("pa_prefix.cuh", "pa_prefix.h", "pa_tc.cuh", "pa_kernels.cuh",
-                                                "pa_ptx.cuh")],
+    "prefix": [os.path.join(_CSRC, f) for f in ("pa_prefix.cuh", "pa_prefix_m256.cuh", "pa_prefix.h", "pa_tc.cuh",
+                                                "pa_kernels.cuh", "pa_ptx.cuh")],
 }
 PROFILE_FILES = {"phase1": "pa_v2_phase1_{}.md", "prefix": "pa_prefix_{}.md"}
 PROFILE_DIR = os.path.join(ROOT, "profiles")
@@ -583,7 +583,8 @@ def run_prefix(args):
                    "parallelism": f"replicas x{ws} (sequence shards)"},
         "roofline": {"bound": "tensor", "achieved": round(rank_tflops, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(rank_tflops / peak, 4), "traffic": _profiled_traffic(name, "prefix"),
-                     "kernel": "pa_prefix_kernel", "kernel_ms": round(k_ms, 4),
+                     "kernel": "pa_prefix_m256_kernel" if wl.head_size <= 128 else "pa_prefix_kernel",
+                     "kernel_ms": round(k_ms, 4),
                      "peak_source": f"{kind} bf16_tflops (burst; fp16 has the same dense rate)"},
         "e2e": e2e, "cpu_baseline": cpu, "gpu_launches": launches, "clocks": clocks.summary()}), flush=True)
     if ws > 1:
