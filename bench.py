@@ -160,6 +160,26 @@ def combine_ranks(step_bytes: float, ms_per_step: float, device, world: int):
     return float(b.item()), float(t.item())
 
 
+def _percentiles(xs, qs):
+    """Nearest-rank percentiles of a list of floats."""
+    ys = sorted(xs)
+    return [ys[min(len(ys) - 1, max(0, int(round(q / 100 * (len(ys) - 1)))))] for q in qs]
+
+
+def _oracle_tiny_1thread_us() -> float:
+    """The oracle on the tiny decode workload (2 sequences of 37 and 600 tokens) on one host
+    thread: median of five calls, in microseconds."""
+    import oracle
+    import workloads
+    wl = workloads.make("tiny")
+    ts = []
+    for _ in range(5):
+        t0 = time.perf_counter()
+        oracle.decode_workload(wl, threads=1)
+        ts.append(time.perf_counter() - t0)
+    return round(sorted(ts)[2] * 1e6, 1)
+
+
 def _cpu_baseline(wl, seconds: float, threads: int):
     """Time the fp64 oracle, sequence by sequence (all heads of each), cycling over the
     workload until about `seconds` of work is done; returns (GB/s, description, bytes, s)."""
@@ -361,6 +381,8 @@ def run_ours(args):
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(mean_ms_max, 5),
+        # this rank's per-step spread (CUDA events around each step)
+        "us_p10_p50_p90": [round(float(x) * 1e3, 2) for x in _percentiles(step_ms, (10, 50, 90))],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -386,7 +408,7 @@ def run_ours(args):
         threads = len(os.sched_getaffinity(0))
         gbs, desc, _, _ = _cpu_baseline(wl, args.cpu_seconds, threads)
         line["cpu_baseline"] = {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-                                "sample": desc}
+                                "sample": desc, "tiny_1thread_us": _oracle_tiny_1thread_us()}
     print(json.dumps(line), flush=True)
     if ws > 1:
         torch.distributed.destroy_process_group()
