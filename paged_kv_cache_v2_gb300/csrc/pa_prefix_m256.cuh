@@ -7,12 +7,14 @@
 // two S buffers of 64 columns and O (head size <= 128 columns): 2 x 256 = all 512 columns.  The
 // softmax writes P (bf16: hi and lo) back into the S buffer it has just read, and the score MMA
 // of tile t + 2 reuses that buffer only after the value MMA of tile t has completed.  Q of both
-// groups sits in shared memory.  Twelve warps:
-//   warp 0         allocates tensor memory; lane 0 issues the score MMAs of both groups
-//   warp 1         lane 0 issues the value MMAs of both groups
+// groups sits in shared memory.  Fourteen warps:
+//   warp 0         allocates tensor memory; lane 0 issues group 0's score MMAs
+//   warp 1         lane 0 issues group 0's value MMAs
 //   warp 2 / 3     fill the key / the value ring (the loader of pa_prefix.cuh, one warp each)
 //   warps 4-7      softmax of group 0 (warp 4 + w: rows 32 w .. 32 w + 31 of the group)
 //   warps 8-11     softmax of group 1
+//   warps 12 / 13  lane 0 issues group 1's score / value MMAs (a lane per group and product:
+//                  a lane waiting on one group does not hold up the other group's MMAs)
 // so each sub-partition runs two softmax warps, and while one group turns its scores into
 // probabilities the tensor core works on the other group's products.
 #pragma once
@@ -21,9 +23,10 @@
 
 namespace pa {
 
-constexpr int kP2Threads = 12 * 32;
+constexpr int kP2Threads = 14 * 32;
 constexpr int kP2Rows = 256;
 constexpr int kP2MmaWarp = 0, kP2PvWarp = 1, kP2KeyWarp = 2, kP2ValWarp = 3, kP2SoftmaxWarp0 = 4;
+constexpr int kP2MmaWarp1 = 12, kP2PvWarp1 = 13;  // group 1's score / value lanes
 
 template <bool BF16, int D>
 struct Pfx2Cfg {
@@ -100,8 +103,8 @@ __global__ void __launch_bounds__(kP2Threads, 1) pa_prefix_m256_kernel(const __g
     uint64_t* p_full = s_full + 4;        // [2][2] P of the buffer's tile written (4 warps)
     uint64_t* o_done = p_full + 4;        // [2][2] value MMAs of the buffer's tile done
     uint64_t* q_full = o_done + 4;        // both groups' Q in shared memory
-    uint64_t* fin = q_full + 1;           // [2] every MMA issued has completed
-    constexpr int NBARS = 2 * NK + 2 * NV + 15;
+    uint64_t* fin = q_full + 1;           // [4] every MMA an issuing lane issued has completed
+    constexpr int NBARS = 2 * NK + 2 * NV + 17;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctl + 8 * NBARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(ctl + 8 * NBARS + 4);
     uint32_t* bad_mask = reinterpret_cast<uint32_t*>(ctl + 8 * NBARS + 8);
@@ -114,11 +117,11 @@ __global__ void __launch_bounds__(kP2Threads, 1) pa_prefix_m256_kernel(const __g
     if (tid == 0) {
         for (int i = 0; i < NK; ++i) {
             mbar_init(&k_full[i], 2);           // the copy arrive (+ bytes) and the key warp
-            mbar_init(&k_empty[i], 1 + 4 * ng);  // the score MMAs' commit and the softmax warps
+            mbar_init(&k_empty[i], 5 * ng);  // each group's score-MMA commit and its softmax warps
         }
         for (int i = 0; i < NV; ++i) {
             mbar_init(&v_full[i], 2);
-            mbar_init(&v_empty[i], 1);
+            mbar_init(&v_empty[i], ng);  // each group's value-MMA commit
         }
         for (int i = 0; i < 4; ++i) {
             mbar_init(&s_full[i], 1);
@@ -126,7 +129,7 @@ __global__ void __launch_bounds__(kP2Threads, 1) pa_prefix_m256_kernel(const __g
             mbar_init(&o_done[i], 1);
         }
         mbar_init(q_full, 4 * ng);
-        for (int i = 0; i < 2; ++i) mbar_init(&fin[i], 1);
+        for (int i = 0; i < 4; ++i) mbar_init(&fin[i], 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -144,9 +147,10 @@ __global__ void __launch_bounds__(kP2Threads, 1) pa_prefix_m256_kernel(const __g
         // ------------------------------------------------------------------ loaders
         pfx_load_tiles<C, D, 32>(p, rng, warp == kP2KeyWarp, lane, lane, sbase, k_full, k_empty, v_full, v_empty,
                                  bad_mask, abort_flag);
-    } else if (warp == kP2MmaWarp) {
+    } else if (warp == kP2MmaWarp || warp == kP2MmaWarp1) {
         // ------------------------------------------------------------------ score MMAs
-        if (lane == 0) {
+        const int g = warp == kP2MmaWarp1 ? 1 : 0;
+        if (lane == 0 && g < ng) {
             const uint64_t kd0 = umma_desc(sbase + C::OFF_K, 128, C::DP * 16);
             const uint32_t kd_lo = (uint32_t)kd0, kd_hi = (uint32_t)(kd0 >> 32);
             // Q of group g: [chunk][128 rows][16 bytes] at OFF_Q + g * QG_BYTES; a K step (16 head
@@ -157,29 +161,27 @@ __global__ void __launch_bounds__(kP2Threads, 1) pa_prefix_m256_kernel(const __g
             for (int t = 0; ok && t < n_tiles; ++t) {
                 ok = pfx_wait(&k_full[t % NK], (t / NK) & 1, abort_flag);
                 const uint32_t k_lo = kd_lo + (uint32_t)((t % NK) * (C::K_BYTES >> 4));
-                for (int g = 0; ok && g < ng; ++g) {
-                    // this tile's S buffer held P of tile t - 2: its value MMA must be done
-                    if (t >= 2) ok = pfx_wait(&o_done[g * 2 + (t & 1)], ((t - 2) >> 1) & 1, abort_flag);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t d_s = tm + g * 256 + (t & 1) * BN;
-                    const uint32_t q_lo = qd_lo + (uint32_t)(g * (C::QG_BYTES >> 4));
-#pragma unroll
-                    for (int ks = 0; ks < C::DP / 16; ++ks)
-                        umma_f16_ss(d_s, q_lo + ks * (2 * kPfxBM), qd_hi, k_lo + ks * 16, kd_hi, C::IDESC_S,
-                                    ks > 0 ? 1u : 0u);
-                    umma_commit(&s_full[g * 2 + (t & 1)]);
-                }
+                // this tile's S buffer held P of tile t - 2: its value MMA must be done
+                if (ok && t >= 2) ok = pfx_wait(&o_done[g * 2 + (t & 1)], ((t - 2) >> 1) & 1, abort_flag);
                 if (!ok) break;
+                tc_fence_after();
+                const uint32_t d_s = tm + g * 256 + (t & 1) * BN;
+                const uint32_t q_lo = qd_lo + (uint32_t)(g * (C::QG_BYTES >> 4));
+#pragma unroll
+                for (int ks = 0; ks < C::DP / 16; ++ks)
+                    umma_f16_ss(d_s, q_lo + ks * (2 * kPfxBM), qd_hi, k_lo + ks * 16, kd_hi, C::IDESC_S,
+                                ks > 0 ? 1u : 0u);
+                umma_commit(&s_full[g * 2 + (t & 1)]);
                 umma_commit(&k_empty[t % NK]);
             }
-            umma_commit(&fin[0]);
-            if (!mbar_wait_bounded(&fin[0], 0, kWaitLimitNs)) prefix_flag(256u);
+            umma_commit(&fin[2 * g]);
+            if (!mbar_wait_bounded(&fin[2 * g], 0, kWaitLimitNs)) prefix_flag(256u);
         }
         __syncwarp();
-    } else if (warp == kP2PvWarp) {
+    } else if (warp == kP2PvWarp || warp == kP2PvWarp1) {
         // ------------------------------------------------------------------ value MMAs
-        if (lane == 0) {
+        const int g = warp == kP2PvWarp1 ? 1 : 0;
+        if (lane == 0 && g < ng) {
             const uint64_t vd0 = p.bs_log2 == 3   ? umma_desc(sbase + C::OFF_V, C::DP * 16, 128)
                                  : p.bs_log2 == 4 ? umma_desc_sw(sbase + C::OFF_V, 256, 6)
                                                   : umma_desc_sw(sbase + C::OFF_V, 512, 4);
@@ -195,28 +197,25 @@ __global__ void __launch_bounds__(kP2Threads, 1) pa_prefix_m256_kernel(const __g
                 ok = pfx_wait(&v_full[t % NV], (t / NV) & 1, abort_flag);
                 const uint32_t v_lo = vd_lo + (uint32_t)((t % NV) * (C::V_BYTES >> 4));
                 const uint32_t acc0 = t > 0 ? 1u : 0u;
-                for (int g = 0; ok && g < ng; ++g) {
-                    ok = pfx_wait(&p_full[g * 2 + (t & 1)], (t >> 1) & 1, abort_flag);
-                    if (!ok) break;
-                    tc_fence_after();
-                    // P of this tile: its S buffer, bf16 hi in the first 32 columns, lo in the next 32
-                    const uint32_t a_p = tm + g * 256 + (t & 1) * BN;
-#pragma unroll
-                    for (int h = 0; h < C::NP; ++h)
-#pragma unroll
-                        for (int kk = 0; kk < BN / 16; ++kk)
-                            umma_f16_ts(tm + g * 256 + C::COL_O, a_p + h * (BN / 2) + kk * 8, v_lo + voff[kk], vd_hi,
-                                        C::IDESC_O, (kk > 0 || h > 0) ? 1u : acc0);
-                    umma_commit(&o_done[g * 2 + (t & 1)]);
-                }
+                if (ok) ok = pfx_wait(&p_full[g * 2 + (t & 1)], (t >> 1) & 1, abort_flag);
                 if (!ok) break;
+                tc_fence_after();
+                // P of this tile: its S buffer, bf16 hi in the first 32 columns, lo in the next 32
+                const uint32_t a_p = tm + g * 256 + (t & 1) * BN;
+#pragma unroll
+                for (int h = 0; h < C::NP; ++h)
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk)
+                        umma_f16_ts(tm + g * 256 + C::COL_O, a_p + h * (BN / 2) + kk * 8, v_lo + voff[kk], vd_hi,
+                                    C::IDESC_O, (kk > 0 || h > 0) ? 1u : acc0);
+                umma_commit(&o_done[g * 2 + (t & 1)]);
                 umma_commit(&v_empty[t % NV]);
             }
-            umma_commit(&fin[1]);
-            if (!mbar_wait_bounded(&fin[1], 0, kWaitLimitNs)) prefix_flag(256u);
+            umma_commit(&fin[2 * g + 1]);
+            if (!mbar_wait_bounded(&fin[2 * g + 1], 0, kWaitLimitNs)) prefix_flag(256u);
         }
         __syncwarp();
-    } else if ((warp - kP2SoftmaxWarp0) / 4 < ng) {
+    } else if (warp >= kP2SoftmaxWarp0 && warp < kP2SoftmaxWarp0 + 8 && (warp - kP2SoftmaxWarp0) / 4 < ng) {
         // ------------------------------------------------------------------ softmax
         const int g = (warp - kP2SoftmaxWarp0) / 4;
         const int sw = warp & 3;  // tensor-memory lane quarter
