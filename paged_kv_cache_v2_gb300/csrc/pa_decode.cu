@@ -61,6 +61,7 @@ namespace pa {
 // out = sum_p w_p tmp_p / sum_p w_p.
 constexpr int kP2MaxWarps = 16;
 constexpr int kP2MaxCols = 2;  // float4 columns per lane: head_size <= 256
+constexpr int kP2Pre = 8;      // partitions per warp and chunk whose tmp rows load up front
 
 // four consecutive tmp_output elements of one partition row as fp32
 template <bool BF16, bool TMP16>
@@ -90,9 +91,11 @@ __global__ void __launch_bounds__(kP2MaxWarps * 32)
 pa_v2_phase2_kernel(const Phase2Params p) {
     extern __shared__ float sm2[];  // [W][D] partial sums
     __shared__ float wm[kP2MaxWarps], wl[kP2MaxWarps];
-    griddep_wait();
     const int h = blockIdx.x, s = blockIdx.y;
+    // seq_lens is an input of the decode call: phase 1, which this kernel follows, read it
+    // after its own dependency wait, so it can be read before this kernel's wait
     const int L = p.seq_lens[s];
+    griddep_wait();
     const int P = min(L > 0 ? (L + kPartition - 1) / kPartition : 0, p.Pmax);
     if (P <= 1) return;  // written by phase 1 (single pass or empty)
     const int D = p.D, nq = D / 4;
@@ -111,6 +114,18 @@ pa_v2_phase2_kernel(const Phase2Params p) {
     const int mine = P > warp ? (P - warp + W - 1) / W : 0;  // partitions of this warp
     for (int j0 = 0; j0 < mine; j0 += 32) {
         const int nc = min(32, mine - j0);
+        // the tmp rows of this chunk's first kP2Pre partitions, loaded together with the
+        // statistics that weight them rather than after them (one memory round trip fewer)
+        float4 pre[kP2Pre][kP2MaxCols];
+#pragma unroll
+        for (int jj = 0; jj < kP2Pre; ++jj)
+#pragma unroll
+            for (int k = 0; k < kP2MaxCols; ++k) {
+                const int c = lane + 32 * k;
+                pre[jj][k] = jj < nc && c < nq
+                                 ? load_tmp4<BF16, TMP16>(p.tmp_out, tmp4 + (warp + (int64_t)(j0 + jj) * W) * nq + c)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
         float mj = -INFINITY, lj = 0.f;
         if (lane < nc) {
             const int i = warp + (j0 + lane) * W;
@@ -129,8 +144,20 @@ pa_v2_phase2_kernel(const Phase2Params p) {
         float4 ac[kP2MaxCols];
 #pragma unroll
         for (int k = 0; k < kP2MaxCols; ++k) ac[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int jj = 0; jj < kP2Pre; ++jj) {
+            if (jj >= nc) break;  // nc is the same on every lane
+            const float w = __shfl_sync(0xffffffffu, wj, jj);
+#pragma unroll
+            for (int k = 0; k < kP2MaxCols; ++k) {
+                ac[k].x += w * pre[jj][k].x;
+                ac[k].y += w * pre[jj][k].y;
+                ac[k].z += w * pre[jj][k].z;
+                ac[k].w += w * pre[jj][k].w;
+            }
+        }
 #pragma unroll 4
-        for (int jj = 0; jj < nc; ++jj) {
+        for (int jj = kP2Pre; jj < nc; ++jj) {
             const float w = __shfl_sync(0xffffffffu, wj, jj);
             const int64_t i = warp + (int64_t)(j0 + jj) * W;
 #pragma unroll
