@@ -45,25 +45,15 @@ __global__ void __launch_bounds__(128) pa_cache_write_kernel(const CacheParams p
     griddep_wait();
     griddep_launch_dependents();
     const int tok = blockIdx.x;
-    const int64_t slot = p.slots[tok];
-    if (slot < 0) return;
-    if (slot >= (int64_t)p.num_blocks * p.bs) {
-        if (threadIdx.x == 0) atomicOr(&g_cache_errors, 8u);
-        return;
-    }
-    const int64_t b = slot / p.bs;
-    const int o = (int)(slot - b * p.bs);
     constexpr int X = FP8 ? 16 : 8;
     const int nchunk = p.D / X;
     const int kvb = FP8 ? 1 : 2;
-    for (int c = threadIdx.x; c < p.Hk * nchunk; c += blockDim.x) {
+    union Chunk { uint4 v[X / 8]; uint16_t h[X]; };
+    // key / value chunk c = (kv head, X-element group) of this token's rows
+    auto load_chunk = [&](int c, Chunk& kc, Chunk& vc) {
         const int h = c / nchunk, ch = c - h * nchunk;
         const uint16_t* ks = p.key + tok * p.kstride + (int64_t)h * p.D + ch * X;
         const uint16_t* vs = p.value + tok * p.vstride + (int64_t)h * p.D + ch * X;
-        union Chunk { uint4 v[X / 8]; uint16_t h[X]; };
-        Chunk kc, vc;
-        uint16_t* kv = kc.h;
-        uint16_t* vv = vc.h;
         if (p.vec) {
 #pragma unroll
             for (int i = 0; i < X / 8; ++i) {
@@ -73,10 +63,33 @@ __global__ void __launch_bounds__(128) pa_cache_write_kernel(const CacheParams p
         } else {
 #pragma unroll
             for (int i = 0; i < X; ++i) {
-                kv[i] = ks[i];
-                vv[i] = vs[i];
+                kc.h[i] = ks[i];
+                vc.h[i] = vs[i];
             }
         }
+    };
+    // this thread's first chunk is read together with the slot (neither depends on the other)
+    Chunk k0, v0;
+    if (threadIdx.x < p.Hk * nchunk) load_chunk(threadIdx.x, k0, v0);
+    const int64_t slot = p.slots[tok];
+    if (slot < 0) return;
+    if (slot >= (int64_t)p.num_blocks * p.bs) {
+        if (threadIdx.x == 0) atomicOr(&g_cache_errors, 8u);
+        return;
+    }
+    const int64_t b = slot / p.bs;
+    const int o = (int)(slot - b * p.bs);
+    for (int c = threadIdx.x; c < p.Hk * nchunk; c += blockDim.x) {
+        const int h = c / nchunk, ch = c - h * nchunk;
+        Chunk kc, vc;
+        if (c == (int)threadIdx.x) {
+            kc = k0;
+            vc = v0;
+        } else {
+            load_chunk(c, kc, vc);
+        }
+        uint16_t* kv = kc.h;
+        uint16_t* vv = vc.h;
         const int64_t head = b * p.Hk + h;
         uint8_t* kdst = p.kcache + (((head * nchunk + ch) * p.bs + o) * X) * kvb;
         if constexpr (FP8) {

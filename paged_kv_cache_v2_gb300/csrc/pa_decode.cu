@@ -238,6 +238,8 @@ static Phase1Fn phase1_for(bool bf16, bool fp8, int d, int bs) {
 }
 
 // Opt a kernel into `bytes` of dynamic shared memory once per (kernel, device).
+static std::mutex g_host_cache_mu;  // guards the two per-process caches below
+
 static cudaError_t ensure_smem(const void* fn, size_t bytes) {
     struct Entry { const void* fn; int dev; size_t bytes; };
     static Entry cache[256];
@@ -245,11 +247,35 @@ static cudaError_t ensure_smem(const void* fn, size_t bytes) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_host_cache_mu);
     for (int i = 0; i < n; ++i)
         if (cache[i].fn == fn && cache[i].dev == dev && cache[i].bytes >= bytes) return cudaSuccess;
     e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
     if (e != cudaSuccess) return e;
     if (n < 256) cache[n++] = Entry{fn, dev, bytes};
+    return cudaSuccess;
+}
+
+// SM count of the current device and resident CTAs per SM of `fn` at (threads, smem): queried
+// once per (kernel, device, size) -- the occupancy query costs microseconds of host time per
+// call, a visible share of a ~90 us decode step launched from an idle queue.
+static cudaError_t occupancy(const void* fn, int threads, size_t smem, int* sms, int* per_sm) {
+    struct Entry { const void* fn; int dev, threads; size_t smem; int sms, per_sm; };
+    static Entry cache[256];
+    static int n = 0;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lock(g_host_cache_mu);
+    for (int i = 0; i < n; ++i)
+        if (cache[i].fn == fn && cache[i].dev == dev && cache[i].threads == threads && cache[i].smem == smem) {
+            *sms = cache[i].sms;
+            *per_sm = cache[i].per_sm;
+            return cudaSuccess;
+        }
+    if ((e = cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(per_sm, fn, threads, smem)) != cudaSuccess) return e;
+    if (n < 256) cache[n++] = Entry{fn, dev, threads, smem, *sms, *per_sm};
     return cudaSuccess;
 }
 
@@ -442,8 +468,7 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
     // shared-memory slot while it starts.  So PX is capped to keep the grid within about
     // PA_GRID_WAVES full waves, and each CTA takes at most 8 partitions.
     int sms = 0, per_sm = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kWarps * 32, smem1) != cudaSuccess) {
+    if (occupancy((const void*)fn, kWarps * 32, smem1, &sms, &per_sm) != cudaSuccess) {
         (void)cudaGetLastError();
         return PA_ERR_CUDA;
     }
