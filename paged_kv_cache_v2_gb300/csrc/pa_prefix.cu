@@ -1,6 +1,9 @@
 // pa_prefix.cu -- host entry point of chunked-prefix attention ("paged_attn.py",
-// forward_prefix): argument checks, grid sizing, kernel selection.  The kernels live in
-// pa_prefix.cuh (instantiated per dtype in pa_prefix_f16.cu / pa_prefix_bf16.cu).
+// forward_prefix): argument checks, grid sizing, kernel selection, the split-context
+// workspace.  The kernels live in pa_prefix.cuh (128 query rows per CTA: head sizes 192 and
+// 256; the loader, the split plan and the combine) and pa_prefix_m256.cuh (256 rows per CTA:
+// head sizes up to 128; prefix_select), instantiated per dtype in pa_prefix_f16.cu /
+// pa_prefix_bf16.cu.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>

@@ -230,3 +230,39 @@ def test_split_is_deterministic():
     a = run_prefix(wl, dev, max_splits=6, min_split_keys=64)
     b = run_prefix(wl, dev, max_splits=6, min_split_keys=64)
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_auto_workspace_matches_explicit_workspace():
+    # the binding's own workspace (torch allocator) and a caller-owned one give identical bits
+    wl = workloads.make_prefix("prefix_long_gqa", reduced=True)
+    dev = prefix_to_device(wl)
+    auto = run_prefix(wl, dev, max_splits=4, min_split_keys=64)
+    nbytes = pa.prefix_workspace_size(wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_size,
+                                      wl.max_query_len, 4)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    out = torch.full(wl.query.shape, float("nan"), dtype=wl.query.dtype, device="cuda")
+    pa.pa_prefix(out, dev["query"], dev["key"], dev["value"], dev["key_cache"], dev["value_cache"],
+                 dev["block_tables"], dev["query_start_loc"], dev["context_lens"], wl.max_query_len,
+                 scale=wl.scale, workspace=ws, max_splits=4, min_split_keys=64)
+    torch.cuda.synchronize()
+    assert torch.equal(auto.view(torch.int16), out.cpu().view(torch.int16))
+
+
+def test_concurrent_calls_on_two_streams():
+    # two split calls in flight at once on separate streams, each with its own workspace
+    a = workloads.make_prefix("prefix_long_gqa", reduced=True)
+    b = workloads.make_prefix("prefix_llama_gqa", reduced=True)
+    da, db = prefix_to_device(a), prefix_to_device(b)
+    oa = torch.full(a.query.shape, float("nan"), dtype=a.query.dtype, device="cuda")
+    ob = torch.full(b.query.shape, float("nan"), dtype=b.query.dtype, device="cuda")
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    for wl, d, o, st in ((a, da, oa, sa), (b, db, ob, sb)):
+        with torch.cuda.stream(st):
+            pa.pa_prefix(o, d["query"], d["key"], d["value"], d["key_cache"], d["value_cache"], d["block_tables"],
+                         d["query_start_loc"], d["context_lens"], wl.max_query_len, scale=wl.scale, stream=st,
+                         max_splits=3, min_split_keys=64)
+    torch.cuda.synchronize()
+    check_prefix(a, oa.cpu(), oracle.prefix_workload(a), label="stream a")
+    check_prefix(b, ob.cpu(), oracle.prefix_workload(b), label="stream b")
+    assert pa.pa_get_device_errors() == 0
