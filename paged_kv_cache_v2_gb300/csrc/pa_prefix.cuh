@@ -149,6 +149,45 @@ __device__ __forceinline__ int2 pfx_split_plan(int n_ctx, int nsplit, int split_
     return make_int2(ns, per);
 }
 
+// Sequence order of the grid's z: sequences sorted by the work of one of their CTAs (its
+// context part plus the chunk tiles of its heaviest row tile), largest first, ties by index.
+// The hardware hands out CTAs roughly in grid order, so long CTAs start first and short ones
+// fill the end of the grid instead of long ones trailing behind.  Every CTA ranks all
+// sequences itself (one parallel load per sequence and a rank count; no workspace, no extra
+// launch); above kPfxOrderSeqs sequences the grid order stands.  Called by every thread at
+// kernel entry; `scratch` holds kPfxOrderSeqs + 1 words of shared memory, free afterwards.
+constexpr int kPfxOrderSeqs = 120;
+__device__ __forceinline__ int pfx_seq_order(const PrefixParams& p, int z, uint32_t* scratch) {
+    const int S = gridDim.z;
+    if (S == 1 || S > kPfxOrderSeqs) return z;
+    for (int t = threadIdx.x; t < S; t += blockDim.x) {
+        int c = p.ctx_lens[t];
+        const int q = p.qsl[t + 1] - p.qsl[t];
+        uint32_t w = 0;
+        if (c >= 0 && q >= 0 && q <= p.max_query_len) {
+            c = min(c, p.mbps * p.bs);
+            const int n = (c + 63) / 64;
+            const int2 plan = pfx_split_plan(n, p.nsplit, p.split_tiles);
+            w = (uint32_t)(min(plan.y, n) + (q + 63) / 64);
+        }
+        scratch[t] = w;
+    }
+    __syncthreads();
+    for (int t = threadIdx.x; t < S; t += blockDim.x) {
+        const uint32_t w = scratch[t];
+        int r = 0;
+        for (int j = 0; j < S; ++j) {
+            const uint32_t wj = scratch[j];
+            r += (wj > w || (wj == w && j < t)) ? 1 : 0;
+        }
+        if (r == z) scratch[kPfxOrderSeqs] = (uint32_t)t;
+    }
+    __syncthreads();
+    const int s = (int)scratch[kPfxOrderSeqs];
+    __syncthreads();
+    return s;
+}
+
 // One lane waits, the warp learns the outcome (warp-uniform, as tcgen05.ld/st require).
 __device__ __forceinline__ bool pfx_warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag, int lane) {
     int ok = 1;
@@ -360,7 +399,7 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
     constexpr int BN = C::BN, NK = C::NK, NV = C::NV, NSB = C::NSB;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int s = blockIdx.z, kvh = blockIdx.y;
+    const int s = pfx_seq_order(p, blockIdx.z, reinterpret_cast<uint32_t*>(smem + C::OFF_CTL)), kvh = blockIdx.y;
     const int split = blockIdx.x / p.mt;                        // which part of the context
     const int row0 = (p.mt - 1 - blockIdx.x % p.mt) * kPfxBM;  // row tiles with more keys first
     const int G = p.G;
@@ -410,6 +449,7 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
     volatile int* abort_flag = reinterpret_cast<volatile int*>(ctl + 8 * NBARS + 4);
     uint32_t* bad_mask = reinterpret_cast<uint32_t*>(ctl + 8 * NBARS + 8);  // [NK] pages outside the cache
     static_assert(8 * NBARS + 8 + 4 * NK <= C::CTL_BYTES, "control block");
+    static_assert(4 * (kPfxOrderSeqs + 1) <= C::CTL_BYTES, "sequence-order scratch");
 
     const int row_last = min(row0 + kPfxBM, rows_total) - 1;
     const int n_tiles = n_ctx + (last_split ? (row_last / G) / BN + 1 : 0);

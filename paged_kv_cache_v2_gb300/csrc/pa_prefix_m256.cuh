@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(kP2Threads, 1) pa_prefix_m256_kernel(const __g
     constexpr int BN = C::BN, NK = C::NK, NV = C::NV;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int s = blockIdx.z, kvh = blockIdx.y;
+    const int s = pfx_seq_order(p, blockIdx.z, reinterpret_cast<uint32_t*>(smem + C::OFF_CTL)), kvh = blockIdx.y;
     const int split = blockIdx.x / p.mt;
     const int row0 = (p.mt - 1 - blockIdx.x % p.mt) * kP2Rows;  // row tiles with more keys first
     const int G = p.G;
@@ -113,6 +113,7 @@ __global__ void __launch_bounds__(kP2Threads, 1) pa_prefix_m256_kernel(const __g
     volatile int* abort_flag = reinterpret_cast<volatile int*>(ctl + 8 * NBARS + 4);
     uint32_t* bad_mask = reinterpret_cast<uint32_t*>(ctl + 8 * NBARS + 8);
     static_assert(8 * NBARS + 8 + 4 * NK <= C::CTL_BYTES, "control block");
+    static_assert(4 * (kPfxOrderSeqs + 1) <= C::CTL_BYTES, "sequence-order scratch");
 
     // Barrier phases: S buffer b of group g holds tiles b, b + 2, ...; the score MMA of tile t
     // waits for the value MMA of tile t - 2 (o_done), the softmax of tile t for its scores
