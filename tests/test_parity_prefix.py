@@ -266,3 +266,27 @@ def test_concurrent_calls_on_two_streams():
     check_prefix(a, oa.cpu(), oracle.prefix_workload(a), label="stream a")
     check_prefix(b, ob.cpu(), oracle.prefix_workload(b), label="stream b")
     assert pa.pa_get_device_errors() == 0
+
+
+def test_timing_hook_brackets_the_attention_kernel():
+    # events installed with pa_v2_set_timing_events are recorded around the prefix attention
+    # kernel: positive, and no longer than the whole call (which adds the combine)
+    wl = workloads.make_prefix("prefix_long_gqa", reduced=True)
+    dev = prefix_to_device(wl)
+    out = torch.empty_like(dev["query"])
+    kb, ke = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    cb, ce = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    kb.record(); ke.record()  # create the events
+    torch.cuda.synchronize()
+    pa.pa_v2_set_timing_events(kb, ke)
+    try:
+        cb.record()
+        pa.pa_prefix(out, dev["query"], dev["key"], dev["value"], dev["key_cache"], dev["value_cache"],
+                     dev["block_tables"], dev["query_start_loc"], dev["context_lens"], wl.max_query_len,
+                     scale=wl.scale, max_splits=4, min_split_keys=64)
+        ce.record()
+    finally:
+        pa.pa_v2_set_timing_events(None, None)
+    torch.cuda.synchronize()
+    k_ms, c_ms = kb.elapsed_time(ke), cb.elapsed_time(ce)
+    assert 0.0 < k_ms <= c_ms
