@@ -2,9 +2,10 @@
 
 A step is the whole hot path for one batch: the cache writer stores every sequence's newest
 token (pa_reshape_and_cache), then pa_v2_decode runs phase 1 (with the single-pass path for
-one-partition sequences) and phase 2.  The default workload is the Llama-style GQA decode
-batch (64 sequences, 32 query / 8 kv heads, head size 128, block size 16, lengths uniform in
-[1, 4096], fp16 query and cache); --workload picks another named workload.
+one-partition sequences) and phase 2.  The default workload is the largest decode batch,
+MHA with ALiBi over a ragged batch (256 sequences, 16 heads, head size 96, block size 32,
+lognormal lengths with median 1024 capped at 32768, bf16 query and cache: about 2.6 GB of
+K and V per step); --workload picks another named workload.
 
 Printed (rank 0, one JSON line): achieved HBM GB/s over the step (value), microseconds per
 step, the phase-1 kernel's roofline fraction against the measured HBM copy bandwidth, an
@@ -35,7 +36,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "decode attn µs/step and achieved HBM GB/s (fraction of GB300 peak), 1 GPU"
-DEFAULT_WORKLOAD = "llama_gqa_decode"
+DEFAULT_WORKLOAD = "mha_alibi_ragged"
 L2_BYTES = 129 * 1024 * 1024
 # each profiled kernel's sources: its committed ncu counters are valid while these are unchanged
 _CSRC = os.path.join(ROOT, "paged_kv_cache_v2_gb300", "csrc")
@@ -80,8 +81,75 @@ def _profiled_traffic(workload: str, kernel: str = "phase1"):
     return float(b.group(1))
 
 
+class _NvmlPoller:
+    """SM clock and clock-event reasons read through NVML (read-only queries) every
+    `period_s` from a thread, so that a timed region of a few milliseconds still gets samples.
+    Reason bits: 0x4 sw_power_cap, 0x8 hw_slowdown, 0x20 sw_thermal_slowdown,
+    0x40 hw_thermal_slowdown."""
+
+    BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, torch_device_index: int, period_s: float = 0.001):
+        import ctypes
+
+        self.period = period_s
+        self.samples = []  # (sm_mhz, reasons bitmask)
+        self.max_mhz = None
+        self._stop = threading.Event()
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.lib = lib
+        self.h = ctypes.c_void_p()
+        ok = False
+        try:
+            import torch
+
+            uuid = str(torch.cuda.get_device_properties(torch_device_index).uuid)
+            name = (uuid if uuid.startswith("GPU-") else "GPU-" + uuid).encode()
+            ok = lib.nvmlDeviceGetHandleByUUID(ctypes.c_char_p(name), ctypes.byref(self.h)) == 0
+        except Exception:
+            ok = False
+        if not ok and lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(torch_device_index), ctypes.byref(self.h)) != 0:
+            raise OSError("no NVML handle")
+        mx = ctypes.c_uint()
+        if lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0:  # 1 = NVML_CLOCK_SM
+            self.max_mhz = float(mx.value)
+        fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+        self._reasons_fn = fn if fn is not None else lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        self._ctypes = ctypes
+
+    def _run(self):
+        ct = self._ctypes
+        mhz, rs = ct.c_uint(), ct.c_ulonglong()
+        while not self._stop.is_set():
+            if self.lib.nvmlDeviceGetClockInfo(self.h, 1, ct.byref(mhz)) == 0:
+                r = rs.value if self._reasons_fn(self.h, ct.byref(rs)) == 0 else 0
+                self.samples.append((float(mhz.value), int(r)))
+            time.sleep(self.period)
+
+    def start(self):
+        self._t = threading.Thread(target=self._run, daemon=True)
+        self._t.start()
+
+    def stop(self):
+        self._stop.set()
+        self._t.join(timeout=2)
+        self.lib.nvmlShutdown()
+
+    def summary(self):
+        if not self.samples:
+            return None
+        sm = [s for s, _ in self.samples]
+        reasons = sorted({n for _, r in self.samples for b, n in self.BITS.items() if r & b})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples": len(sm), "sm_mhz_min": min(sm), "source": f"NVML every {self.period * 1e3:g} ms"}
+
+
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while the timed region runs."""
+    """SM clock and throttle reasons sampled while the timed region runs: NVML polled every
+    millisecond (the timed region of a short run lasts only milliseconds), and nvidia-smi at
+    its 100 ms interval as a fallback when NVML cannot be loaded."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -91,8 +159,15 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.lines = []
+        self.nvml = None
 
     def __enter__(self):
+        try:
+            self.nvml = _NvmlPoller(self.gpu)
+            self.nvml.start()
+            return self
+        except Exception:
+            self.nvml = None
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
@@ -109,6 +184,8 @@ class ClockSampler:
             self.lines.append(ln.strip())
 
     def __exit__(self, *exc):
+        if self.nvml is not None:
+            self.nvml.stop()
         if self.proc is not None:
             time.sleep(0.25)
             self.proc.terminate()
@@ -118,6 +195,10 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
+        if self.nvml is not None:
+            s = self.nvml.summary()
+            if s is not None:
+                return s
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
@@ -135,7 +216,7 @@ class ClockSampler:
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "source": "nvidia-smi every 100 ms"}
 
 
 def _dist():
@@ -222,6 +303,16 @@ def _cpu_baseline(wl, seconds: float, threads: int):
     return gbs, desc, done_bytes, t_total
 
 
+def workload_config(name: str, wl, world: int) -> dict:
+    """The `config` object of a decode line: the workload's name and shape, the same for the
+    GPU arm and the reference arm."""
+    return {"workload": name, "num_seqs": wl.num_seqs, "num_heads": wl.num_heads,
+            "num_kv_heads": wl.num_kv_heads, "head_size": wl.head_size, "block_size": wl.block_size,
+            "kv_cache_dtype": wl.kv_cache_dtype, "tokens": int(wl.seq_lens.sum()), "max_seq_len": wl.max_seq_len,
+            "bytes_per_step": int(wl.algorithmic_bytes() + wl.writer_bytes()),
+            "parallelism": f"replicas x{world} (sequence shards)"}
+
+
 def run_reference(args):
     """Reference arm: the CPU oracle, as it stands, on the host cores."""
     ws, rank, _ = _dist()
@@ -246,10 +337,8 @@ def run_reference(args):
         "ms_per_step": round(1e3 * tot_t / len(per_step), 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": wl.q_dtype if wl.kv_cache_dtype == "auto" else "fp8_e4m3",
         "data": "synthetic (seeded)",
-        "config": {"workload": args.workload, "num_seqs": wl.num_seqs, "num_heads": wl.num_heads,
-                   "num_kv_heads": wl.num_kv_heads, "head_size": wl.head_size,
-                   "block_size": wl.block_size, "kv_cache_dtype": wl.kv_cache_dtype,
-                   "l2": "n/a (host)"},
+        "config": workload_config(args.workload, wl, ws),
+        "l2": "n/a (host)",
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": per_step[-1][3] + " per step"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -278,7 +367,10 @@ def run_ours(args):
     wl = workloads.shard(args.workload, rank, ws, canaries=False) if ws > 1 else \
         workloads.make(args.workload, canaries=False)
     S, H, d = wl.query.shape
-    nrot = 2  # rotate between cache copies so no step finds the previous step's pages in L2
+    # rotate between cache copies so that no step finds the previous steps' pages in L2: at
+    # least two, and enough that the copies together span 2.5x the L2 (small batches)
+    kv_bytes = wl.key_cache.numel() * wl.key_cache.element_size() * 2
+    nrot = args.cache_copies or min(16, max(2, -(-int(2.5 * L2_BYTES) // kv_bytes)))
     kcs = [wl.key_cache.to(dev) for _ in range(nrot)]
     vcs = [wl.value_cache.to(dev) for _ in range(nrot)]
     q = wl.query.to(dev)
@@ -404,12 +496,10 @@ def run_ours(args):
         "vs_baseline": None,
         "dtype": wl.q_dtype if wl.kv_cache_dtype == "auto" else f"{wl.q_dtype}+fp8_e4m3",
         "data": "synthetic (seeded N(0, sigma) values, random block tables)",
-        "config": {"workload": args.workload, "num_seqs": S, "num_heads": H, "num_kv_heads": wl.num_kv_heads,
-                   "head_size": d, "block_size": wl.block_size, "kv_cache_dtype": wl.kv_cache_dtype,
-                   "tokens": int(wl.seq_lens.sum()), "max_seq_len": wl.max_seq_len,
-                   "bytes_per_step": int(step_bytes), "fraction_of_peak": round(value / peak, 4),
-                   "l2": f"inputs larger than L2 ({decode_bytes / 2**20:.0f} MiB KV per step) and "
-                         f"{nrot} rotating cache copies", "parallelism": f"replicas x{ws} (sequence shards)"},
+        "config": workload_config(args.workload, wl, ws),
+        "fraction_of_peak": round(value / peak, 4),
+        "l2": f"{decode_bytes / 2**20:.0f} MiB of K/V read per step from {nrot} rotating cache copies of "
+              f"{kv_bytes / 2**20:.0f} MiB ({nrot * kv_bytes / L2_BYTES:.1f}x the L2 together)",
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": "pa_v2_phase1_kernel", "kernel_us": round(k_mean * 1e3, 2),
@@ -642,6 +732,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--cache-copies", type=int, default=0,
+                    help="decode: copies of the K/V caches the steps rotate through (0: at least 2 and enough "
+                         "to span 2.5x the L2, so no step finds earlier steps' pages there; 1 for profiler runs)")
     ap.add_argument("--op", choices=["decode", "copy_blocks", "prefix"], default="decode",
                     help="decode: the decode step (default); copy_blocks: the block-copy kernel alone; "
                          "prefix: chunked-prefix attention (--workload prefix_long_gqa|prefix_llama_gqa)")

@@ -77,13 +77,15 @@ pa_v2_phase1_kernel(const Phase1Params p) {
             if (ppart > 32 && lb + 32 + lane < p.mbps) r1 = trow[lb + 32 + lane];
         }
     };
-    // The ids of the first two partitions and the length load in parallel, before waiting on
-    // the previous kernel: a cache writer that ran just before changes none of them.
+    // Every input is read only after the wait on the previous kernel in the stream: that
+    // kernel may have written the tables, the lengths or the query (a serving loop prepares
+    // them on the device each step), and only the wait makes its writes visible.  The ids of
+    // the first two partitions and the length then load in parallel.
+    griddep_wait();
     int c0, c1, n0, n1;
     load_ids(px, c0, c1);
     load_ids(px + PX, n0, n1);
     const int L = p.seq_lens[s];
-    griddep_wait();  // the cache writer (if it ran just before) must be visible
 
     const int P = L > 0 ? (L + kPartition - 1) / kPartition : 0;
     if (threadIdx.x == 0 && px == 0 && (L < 0 || P > p.Pmax)) flag_error(2u);

@@ -109,7 +109,8 @@ class Workload:
 
 
 # --------------------------------------------------------------------------------------
-# Named workloads: the five decode configurations this library is measured on.
+# Named workloads: the five decode configurations this library is measured on, and a
+# small batch.
 # --------------------------------------------------------------------------------------
 CONFIGS = {
     "tiny": dict(
@@ -137,6 +138,13 @@ CONFIGS = {
         lens=("lognormal", 1024.0, 1.0, 32768, {0: 0, 1: 1}), q_dtype="bf16",
         kv_cache_dtype="auto", sigma=1.0, alibi=True, seed=1005,
     ),
+    # A small batch: two Llama-style sequences of 4K-8K tokens.  Its grid has fewer 512-token
+    # units (kv heads x partitions) than the GPU has CTA slots.
+    "small_batch_gqa": dict(
+        num_seqs=2, num_heads=32, num_kv_heads=8, head_size=128, block_size=16,
+        lens=("uniform", 4096, 8192), q_dtype="f16", kv_cache_dtype="auto",
+        sigma=1.0, alibi=False, seed=1006,
+    ),
 }
 
 # Reduced-size stand-ins the oracle finishes in seconds: same heads, head size, block
@@ -148,6 +156,7 @@ REDUCED = {
     "long_context_gqa": dict(num_seqs=2, lens=("fixed", [3000, 2561])),
     "fp8_kv": dict(num_seqs=6, lens=("uniform", 512, 1800)),
     "mha_alibi_ragged": dict(num_seqs=8, lens=("lognormal", 300.0, 1.0, 2000, {0: 0, 1: 1})),
+    "small_batch_gqa": dict(lens=("uniform", 1200, 2600)),
 }
 
 
