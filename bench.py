@@ -1,8 +1,10 @@
 """Benchmark: one decode step of paged attention on GB300 through the pa_v2 C ABI.
 
 A step is the whole hot path for one batch: the cache writer stores every sequence's newest
-token (pa_reshape_and_cache), then pa_v2_decode runs phase 1 (with the single-pass path for
-one-partition sequences) and phase 2.  The default workload is the largest decode batch,
+token (pa_reshape_and_cache), then pa_v2_decode_fused runs phase 1 (with the single-pass path
+for one-partition sequences) and the partition combine, done by the last CTA of each
+(sequence, head group) inside phase 1 (--decode two-kernel: pa_v2_decode, phase 1 and the
+phase-2 kernel).  The default workload is the largest decode batch,
 MHA with ALiBi over a ragged batch (256 sequences, 16 heads, head size 96, block size 32,
 lognormal lengths with median 1024 capped at 32768, bf16 query and cache: about 2.6 GB of
 K and V per step); --workload picks another named workload.
@@ -89,7 +91,7 @@ class _NvmlPoller:
 
     BITS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown"}
 
-    def __init__(self, torch_device_index: int, period_s: float = 0.001):
+    def __init__(self, torch_device_index: int, period_s: float = 0.0002):
         import ctypes
 
         self.period = period_s
@@ -148,7 +150,7 @@ class _NvmlPoller:
 
 class ClockSampler:
     """SM clock and throttle reasons sampled while the timed region runs: NVML polled every
-    millisecond (the timed region of a short run lasts only milliseconds), and nvidia-smi at
+    0.2 ms (the timed region of a short run lasts only milliseconds), and nvidia-smi at
     its 100 ms interval as a fallback when NVML cannot be loaded."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -379,18 +381,22 @@ def run_ours(args):
     slopes = None if wl.alibi_slopes is None else wl.alibi_slopes.to(dev)
     out = torch.empty_like(q)
     es, ml, tmp = pa.workspace(S, H, d, wl.max_seq_len, dev)
+    # the fused entry point's arrival counters: zeroed once, left at zero by every call
+    ctr = pa.decode_counters(S, H, wl.num_kv_heads, dev) if args.decode == "fused" else None
     stream = torch.cuda.current_stream()
 
     def step(i):
         kc, vc = kcs[i % nrot], vcs[i % nrot]
         pa.pa_reshape_and_cache(nk, nv, kc, vc, slots, wl.kv_cache_dtype, wl.k_scale, wl.v_scale)
         pa.pa_v2_decode(out, es, ml, tmp, q, kc, vc, wl.num_kv_heads, wl.scale, bt, sl, wl.block_size,
-                        wl.max_seq_len, slopes, wl.kv_cache_dtype, wl.k_scale, wl.v_scale)
+                        wl.max_seq_len, slopes, wl.kv_cache_dtype, wl.k_scale, wl.v_scale, counters=ctr)
 
     decode_bytes = wl.algorithmic_bytes()
     step_bytes = decode_bytes + wl.writer_bytes()
     kv_q_bytes = decode_bytes - S * H * d * wl.q_elem_bytes  # phase-1 share: K, V and Q
-    launches_per_step = 2 + (1 if wl.max_num_partitions > 1 else 0)
+    # writer + phase 1 (+ phase 2 on the two-kernel path; the fused path with an fp32
+    # tmp_output always runs the combine inside phase 1)
+    launches_per_step = 2 + (1 if wl.max_num_partitions > 1 and ctr is None else 0)
 
     for i in range(args.warmup):
         step(i)
@@ -497,6 +503,7 @@ def run_ours(args):
         "dtype": wl.q_dtype if wl.kv_cache_dtype == "auto" else f"{wl.q_dtype}+fp8_e4m3",
         "data": "synthetic (seeded N(0, sigma) values, random block tables)",
         "config": workload_config(args.workload, wl, ws),
+        "decode_entry": "pa_v2_decode_fused" if ctr is not None else "pa_v2_decode",
         "fraction_of_peak": round(value / peak, 4),
         "l2": f"{decode_bytes / 2**20:.0f} MiB of K/V read per step from {nrot} rotating cache copies of "
               f"{kv_bytes / 2**20:.0f} MiB ({nrot * kv_bytes / L2_BYTES:.1f}x the L2 together)",
@@ -732,6 +739,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--decode", choices=["fused", "two-kernel"], default="fused",
+                    help="decode entry point: pa_v2_decode_fused (the combine inside phase 1, default) or "
+                         "pa_v2_decode (phase 1 + the phase-2 kernel)")
     ap.add_argument("--cache-copies", type=int, default=0,
                     help="decode: copies of the K/V caches the steps rotate through (0: at least 2 and enough "
                          "to span 2.5x the L2, so no step finds earlier steps' pages there; 1 for profiler runs)")

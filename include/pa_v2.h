@@ -129,6 +129,47 @@ PA_API pa_status pa_v2_decode(void* output, float* exp_sums, float* max_logits, 
                        float k_scale, float v_scale, cudaStream_t stream);
 
 /*
+ * pa_v2_decode_fused -- pa_v2_decode with the partition combine done inside phase 1.
+ *
+ * Defines: the same step as pa_v2_decode ("paged_attention_v2_pytorch.py",
+ * paged_attention_v2_pytorch; "paged_attention_v2_triton.py", _paged_attn_v2_reduce_kernel),
+ * with the V1/V2 dispatch of "paged_attn.py" (forward_decode) re-decided for this GPU: the
+ * pages choose per call between a single pass (V1) and partitions plus a reduce kernel (V2);
+ * here every sequence is partitioned, and the last CTA of each (sequence, head group) to
+ * finish runs the reduce (an arrival counter, no waiting), so no second kernel waits for the
+ * whole grid.  A sequence that one CTA covers entirely (one partition) is a single pass.
+ *
+ * Arguments and results: as pa_v2_decode (output, max_logits and exp_sums identical in
+ * meaning), except
+ *   tmp_output   scratch: its contents after the call are unspecified (with an fp32
+ *                tmp_output each CTA merges the partitions it streams into one row).
+ *   counters     device uint32 [num_counters], num_counters >=
+ *                pa_v2_decode_num_counters(num_seqs, num_heads, num_kv_heads); 4-byte aligned.
+ *                Every entry must be zero before the first call that uses the array (clear
+ *                it once when it is allocated); every call leaves it all zero again.  Like
+ *                the workspace, it must not be used by calls that can overlap on the GPU.
+ *                NULL: exactly pa_v2_decode.
+ * When the combine would read more than 64 KiB of rows per (sequence, head group) (a 16-bit
+ * tmp_output over many partitions), the call falls back to pa_v2_decode's two kernels and the
+ * counters are not touched.
+ * Errors: as pa_v2_decode; PA_ERR_INVALID_ARG also for a misaligned or too short counters array.
+ */
+PA_API pa_status pa_v2_decode_fused(void* output, float* exp_sums, float* max_logits, void* tmp_output,
+                                    const void* query, const void* key_cache, const void* value_cache,
+                                    int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                                    float scale, const int32_t* block_tables, int max_blocks_per_seq,
+                                    int num_blocks, const int32_t* seq_lens, int block_size,
+                                    int max_seq_len, int max_num_partitions, const float* alibi_slopes,
+                                    pa_dtype q_dtype, pa_kv_cache_dtype kv_cache_dtype, pa_dtype tmp_dtype,
+                                    float k_scale, float v_scale, uint32_t* counters, int64_t num_counters,
+                                    cudaStream_t stream);
+
+/* Arrival counters pa_v2_decode_fused needs: num_seqs * num_kv_heads *
+ * ceil((num_heads / num_kv_heads) / 8) (one per sequence and group of up to 8 query heads of a
+ * kv head); 0 for invalid sizes. */
+PA_API int64_t pa_v2_decode_num_counters(int num_seqs, int num_heads, int num_kv_heads);
+
+/*
  * pa_reshape_and_cache -- scatter new key/value rows into the paged caches by slot.
  *
  * Defines: "paged_attn.py", write_to_paged_cache (-> reshape_and_cache with the flattened

@@ -13,6 +13,8 @@ Entry points mirror ``include/pa_v2.h``:
   (paged_attention_v2_pytorch) without its unused tensor-parallel / block-sparse arguments.
 * ``pa_reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, kv_cache_dtype,
   k_scale, v_scale)`` -- "paged_attn.py" write_to_paged_cache.
+* ``pa_v2_decode(..., counters=decode_counters(S, H, Hk, device))`` -- pa_v2_decode_fused:
+  the same step with the partition combine inside phase 1.
 """
 from __future__ import annotations
 
@@ -58,6 +60,11 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.pa_v2_decode.restype = i32
     lib.pa_v2_decode.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, f32, P, i32, i32, P, i32, i32,
                                  i32, P, i32, i32, i32, f32, f32, P]
+    lib.pa_v2_decode_fused.restype = i32
+    lib.pa_v2_decode_fused.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, f32, P, i32, i32, P, i32, i32,
+                                       i32, P, i32, i32, i32, f32, f32, P, i64, P]
+    lib.pa_v2_decode_num_counters.restype = i64
+    lib.pa_v2_decode_num_counters.argtypes = [i32, i32, i32]
     lib.pa_reshape_and_cache.restype = i32
     lib.pa_reshape_and_cache.argtypes = [P, P, i64, i64, P, P, P, i32, i32, i32, i32, i32, i32, i32,
                                          f32, f32, P]
@@ -122,13 +129,17 @@ def pa_v2_decode(output: torch.Tensor, exp_sums: torch.Tensor, max_logits: torch
                  block_tables: torch.Tensor, seq_lens: torch.Tensor, block_size: int,
                  max_seq_len: int, alibi_slopes: Optional[torch.Tensor] = None,
                  kv_cache_dtype: str = "auto", k_scale: float = 1.0, v_scale: float = 1.0,
-                 num_blocks: Optional[int] = None, stream=None) -> None:
+                 num_blocks: Optional[int] = None, stream=None, counters: Optional[torch.Tensor] = None) -> None:
     """Enqueue one decode step (phase 1 + phase 2) on ``stream`` (default: current stream).
 
     Shapes: query/output [S, H, d]; key_cache [NB, Hk, d/x, bs, x]; value_cache
     [NB, Hk, d, bs]; block_tables int32 [S, W]; seq_lens int32 [S]; exp_sums/max_logits
     fp32 [S, H, P]; tmp_output fp32 [S, H, P, d].  The fp8 cache may be passed as uint8
     codes or as torch.float8_e4m3fn.
+
+    With ``counters`` (from :func:`decode_counters`, zeroed once when allocated) the call is
+    ``pa_v2_decode_fused``: the partition combine runs inside phase 1 and tmp_output is
+    scratch.
     """
     lib = load()
     for name, t in (("output", output), ("exp_sums", exp_sums), ("max_logits", max_logits),
@@ -154,14 +165,18 @@ def pa_v2_decode(output: torch.Tensor, exp_sums: torch.Tensor, max_logits: torch
     S, H, d = query.shape
     if num_blocks is None:
         num_blocks = key_cache.shape[0]
-    st = lib.pa_v2_decode(_ptr(output), _ptr(exp_sums), _ptr(max_logits), _ptr(tmp_output),
-                          _ptr(query), _ptr(key_cache), _ptr(value_cache), S, H, int(num_kv_heads),
-                          d, float(scale), _ptr(block_tables), int(block_tables.shape[1]),
-                          int(num_blocks), _ptr(seq_lens), int(block_size), int(max_seq_len),
-                          int(tmp_output.shape[2]), _ptr(alibi_slopes), _dt(query.dtype),
-                          _kv(kv_cache_dtype), tmp_dtype, float(k_scale), float(v_scale),
-                          _stream(stream))
-    _check("pa_v2_decode", st)
+    args = (_ptr(output), _ptr(exp_sums), _ptr(max_logits), _ptr(tmp_output),
+            _ptr(query), _ptr(key_cache), _ptr(value_cache), S, H, int(num_kv_heads),
+            d, float(scale), _ptr(block_tables), int(block_tables.shape[1]),
+            int(num_blocks), _ptr(seq_lens), int(block_size), int(max_seq_len),
+            int(tmp_output.shape[2]), _ptr(alibi_slopes), _dt(query.dtype),
+            _kv(kv_cache_dtype), tmp_dtype, float(k_scale), float(v_scale))
+    if counters is None:
+        _check("pa_v2_decode", lib.pa_v2_decode(*args, _stream(stream)))
+        return
+    if counters.dtype != torch.int32 or not counters.is_cuda or not counters.is_contiguous():
+        raise TypeError("counters must be a contiguous int32 CUDA tensor (see decode_counters)")
+    _check("pa_v2_decode_fused", lib.pa_v2_decode_fused(*args, _ptr(counters), counters.numel(), _stream(stream)))
 
 
 def pa_reshape_and_cache(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor,
@@ -349,6 +364,19 @@ def pa_v2_set_timing_events(begin: Optional[torch.cuda.Event], end: Optional[tor
     b = None if begin is None else ctypes.c_void_p(begin.cuda_event)
     e = None if end is None else ctypes.c_void_p(end.cuda_event)
     _check("pa_v2_set_timing_events", load().pa_v2_set_timing_events(b, e))
+
+
+def decode_num_counters(num_seqs: int, num_heads: int, num_kv_heads: int) -> int:
+    """Arrival counters pa_v2_decode_fused needs for a step of this shape."""
+    return int(load().pa_v2_decode_num_counters(num_seqs, num_heads, num_kv_heads))
+
+
+def decode_counters(num_seqs: int, num_heads: int, num_kv_heads: int, device) -> torch.Tensor:
+    """Zeroed arrival counters for pa_v2_decode_fused (int32 storage of the uint32 array).
+    Every fused call leaves them at zero, so one array serves every later call on one
+    stream; calls that can overlap need one array each."""
+    return torch.zeros(max(1, decode_num_counters(num_seqs, num_heads, num_kv_heads)), dtype=torch.int32,
+                       device=device)
 
 
 def workspace(num_seqs: int, num_heads: int, head_size: int, max_seq_len: int, device,

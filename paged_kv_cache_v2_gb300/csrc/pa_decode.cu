@@ -399,7 +399,23 @@ pa_status pa::validate_decode(const DecodeArgs& a) {
     return PA_OK;
 }
 
-pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_logits, void* tmp_out) {
+int64_t pa::decode_num_counters(int num_seqs, int num_heads, int num_kv_heads) {
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0) return 0;
+    const int G = num_heads / num_kv_heads;
+    return (int64_t)num_seqs * num_kv_heads * ((G + kMaxHeadsPerCta - 1) / kMaxHeadsPerCta);
+}
+
+// Partition stride override for tuning runs (PA_DECODE_PX=n; 0 or unset: the heuristic).
+static int px_override() {
+    static const int v = [] {
+        const char* e = getenv("PA_DECODE_PX");
+        return e ? atoi(e) : 0;
+    }();
+    return v;
+}
+
+pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_logits, void* tmp_out,
+                            uint32_t* counters) {
     const bool bf16 = a.q_dtype == PA_DT_BF16;
     const bool fp8 = a.kv_cache_dtype == PA_KV_FP8_E4M3;
     const int D = a.head_size, bs = a.block_size;
@@ -416,7 +432,7 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
     const uint32_t ring = (uint32_t)kWarps * nstage * slot_bytes;
     const int red_heads = G < kMaxHeadsPerCta ? G : kMaxHeadsPerCta;
     const size_t smem1 = ring + kWarps * nstage * sizeof(uint64_t) +
-                         (2 * kWarps + 2) * kMaxHeadsPerCta * sizeof(float) +
+                         (2 * kWarps + 4) * kMaxHeadsPerCta * sizeof(float) +
                          (size_t)kWarps * red_heads * (D + 4) * sizeof(float);
 
     Phase1Fn fn = phase1_for(bf16, fp8, D, bs);
@@ -457,6 +473,8 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
     p1.qk_scale_log2 = a.scale * a.k_scale * kLog2e;
     p1.v_scale = a.v_scale;
     p1.tmp16 = a.tmp_dtype != PA_DT_F32;
+    p1.counters = nullptr;
+    p1.merge = 0;
 
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -480,6 +498,36 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
     if (PX > a.max_num_partitions) PX = a.max_num_partitions;
     if (PX < 1) PX = 1;
 
+    // Fused combine (V1/V2 dispatch, "paged_attn.py" forward_decode, re-decided for this GPU):
+    // with arrival counters the last CTA of each (sequence, head group) merges the partitions,
+    // so no second kernel waits for the whole grid.  With an fp32 tmp_output every CTA first
+    // folds its own partitions into one row, and the partition stride is capped so that the
+    // last CTA merges at most kFusedRowBytes of rows (a long sequence then streams several
+    // partitions per CTA).  A 16-bit tmp_output keeps one row per partition, so the fused
+    // combine is taken only while all of them fit that bound.
+    bool fused = counters != nullptr && a.max_num_partitions > 1;
+    if (fused) {
+        const bool merge = a.tmp_dtype == PA_DT_F32;
+        const int64_t row_bytes = (int64_t)red_heads * D * (merge ? 4 : 2);
+        if (merge) {
+            int64_t cap = kFusedRowBytes / row_bytes;
+            if (cap < 1) cap = 1;
+            if (PX > cap) PX = cap;
+        }
+        if (px_override() > 0) PX = px_override() < a.max_num_partitions ? px_override() : a.max_num_partitions;
+        const int64_t R = merge ? PX : a.max_num_partitions;
+        // the row weights live in the idle page ring during the combine
+        if ((kMaxHeadsPerCta + (int64_t)red_heads * R) * (int64_t)sizeof(float) > (int64_t)ring ||
+            (!merge && R * row_bytes > kFusedRowBytes))
+            fused = false;
+        if (fused) {
+            p1.counters = counters;
+            p1.merge = merge ? 1 : 0;
+        }
+    } else if (px_override() > 0) {
+        PX = px_override() < a.max_num_partitions ? px_override() : a.max_num_partitions;
+    }
+
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)PX, (unsigned)(a.num_kv_heads * ngroups), (unsigned)a.num_seqs);
     cfg.blockDim = dim3(kWarps * 32, 1, 1);
@@ -495,7 +543,7 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
         return PA_ERR_CUDA;
     }
 
-    if (a.max_num_partitions > 1) {
+    if (a.max_num_partitions > 1 && !fused) {
         Phase2Params p2;
         p2.out = a.output;
         p2.exp_sums = exp_sums;
@@ -574,6 +622,57 @@ extern "C" pa_status pa_v2_decode(void* output, float* exp_sums, float* max_logi
                            max_seq_len, stream);
     if (st != PA_OK) return st;
     return launch_decode(a, exp_sums, max_logits, tmp_output);
+}
+
+extern "C" int64_t pa_v2_decode_num_counters(int num_seqs, int num_heads, int num_kv_heads) {
+    return decode_num_counters(num_seqs, num_heads, num_kv_heads);
+}
+
+extern "C" pa_status pa_v2_decode_fused(void* output, float* exp_sums, float* max_logits, void* tmp_output,
+                                        const void* query, const void* key_cache, const void* value_cache,
+                                        int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                                        float scale, const int32_t* block_tables, int max_blocks_per_seq,
+                                        int num_blocks, const int32_t* seq_lens, int block_size,
+                                        int max_seq_len, int max_num_partitions, const float* alibi_slopes,
+                                        pa_dtype q_dtype, pa_kv_cache_dtype kv_cache_dtype, pa_dtype tmp_dtype,
+                                        float k_scale, float v_scale, uint32_t* counters, int64_t num_counters,
+                                        cudaStream_t stream) {
+    DecodeArgs a;
+    a.output = output;
+    a.exp_sums = exp_sums;
+    a.max_logits = max_logits;
+    a.tmp_output = tmp_output;
+    a.query = query;
+    a.key_cache = key_cache;
+    a.value_cache = value_cache;
+    a.num_seqs = num_seqs;
+    a.num_heads = num_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_size = head_size;
+    a.scale = scale;
+    a.block_tables = block_tables;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.seq_lens = seq_lens;
+    a.block_size = block_size;
+    a.max_seq_len = max_seq_len;
+    a.max_num_partitions = max_num_partitions;
+    a.alibi_slopes = alibi_slopes;
+    a.q_dtype = q_dtype;
+    a.kv_cache_dtype = kv_cache_dtype;
+    a.tmp_dtype = tmp_dtype;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.stream = stream;
+    pa_status st = validate_decode(a);
+    if (st != PA_OK || num_seqs == 0) return st;
+    if (counters != nullptr &&
+        (!aligned(counters, 4) || num_counters < decode_num_counters(num_seqs, num_heads, num_kv_heads)))
+        return PA_ERR_INVALID_ARG;
+    st = host_check_tables(block_tables, max_blocks_per_seq, num_blocks, seq_lens, num_seqs, block_size,
+                           max_seq_len, stream);
+    if (st != PA_OK) return st;
+    return launch_decode(a, exp_sums, max_logits, tmp_output, counters);
 }
 
 // ---------------------------------------------------------------------------------------

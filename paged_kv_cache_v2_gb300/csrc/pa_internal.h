@@ -31,8 +31,13 @@ struct DecodeArgs {
 
 // Argument checks shared by the decode entry points (no device access).
 pa_status validate_decode(const DecodeArgs& a);
-// Enqueue phase 1 (+ phase 2) with the given workspace.
-pa_status launch_decode(const DecodeArgs& a, float* exp_sums, float* max_logits, void* tmp_out);
+// Enqueue phase 1 (+ phase 2) with the given workspace.  With `counters` (zeroed arrival
+// counters, one per (sequence, kv head, head group)) the combine runs inside phase 1 when
+// the step's shape allows it, and phase 2 is not launched.
+pa_status launch_decode(const DecodeArgs& a, float* exp_sums, float* max_logits, void* tmp_out,
+                        uint32_t* counters = nullptr);
+// Arrival counters the fused combine needs for a step of this shape.
+int64_t decode_num_counters(int num_seqs, int num_heads, int num_kv_heads);
 // Read (and optionally clear) each translation unit's device error word on the current device.
 cudaError_t read_decode_errors(unsigned int* v, bool reset);
 cudaError_t read_cache_errors(unsigned int* v, bool reset);

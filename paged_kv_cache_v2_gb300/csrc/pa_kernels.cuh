@@ -26,6 +26,11 @@ constexpr int kPartition = 512;
 constexpr int kWarps = PA_PHASE1_WARPS;  // phase-1 warps per CTA
 constexpr uint32_t kRingTarget = PA_RING_KIB * 1024u;  // shared-memory page ring per CTA
 constexpr int kMaxHeadsPerCta = 8;     // the MMA N dimension
+// Fused combine: most bytes of rows the last CTA of a (sequence, head group) merges.
+#ifndef PA_FUSED_ROW_KIB
+#define PA_FUSED_ROW_KIB 64
+#endif
+constexpr int64_t kFusedRowBytes = PA_FUSED_ROW_KIB * 1024;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -46,6 +51,14 @@ struct Phase1Params {
     float qk_scale_log2;  // scale * k_scale * log2(e)
     float v_scale;
     int tmp16;  // tmp_output holds the output dtype instead of fp32
+    // Combine fused into phase 1 (counters != nullptr): the last CTA of a (sequence, head
+    // group) to finish merges the partitions; counters[s * gridDim.y + blockIdx.y] counts the
+    // CTAs that have finished and is reset to 0 by the last one.
+    uint32_t* counters;
+    // With the fused combine: each CTA merges its own partitions px, px + PX, ... into fp32
+    // row px of tmp_output (instead of one row per partition), so the last CTA merges at
+    // most PX rows.
+    int merge;
 };
 
 struct Phase2Params {

@@ -25,6 +25,96 @@ __device__ __forceinline__ void flag_error(unsigned int bit) { atomicOr(&g_phase
 static __device__ __constant__ int8_t c_fp8_row_token[16] = {0, 1, 4, 5, 10, 11, 14, 15,
                                                       2, 3, 6, 7, 8, 9, 12, 13};
 
+// One step of a running log-sum-exp merge of normalised rows: the row so far has max A and
+// exp-sum Lc (log2 units), the new part max a and exp-sum l.  Returns the factors that the
+// merged normalised row takes from the old row (fo) and from the new part (fn), and updates
+// (A, Lc).  An empty side (max -inf) gets factor 0, so its contents are never read.
+__device__ __forceinline__ void merge_factors(float& A, float& Lc, float a, float l, float& fo, float& fn) {
+    const float An = fmaxf(A, a);
+    if (An == -INFINITY) {
+        fo = fn = 0.f;
+        return;
+    }
+    const float x = Lc * ex2(A - An), y = l * ex2(a - An);  // a side at -inf contributes 0
+    const float Ln = x + y;
+    fo = Ln > 0.f ? x / Ln : 0.f;
+    fn = Ln > 0.f ? y / Ln : 0.f;
+    A = An;
+    Lc = Ln;
+}
+
+// The combine of phase 2 ("paged_attention_v2_triton.py", _paged_attn_v2_reduce_kernel), run
+// by the last CTA of a (sequence, head group) to finish: g = max_p m_p and weights
+// exp(m_p - g) l_p from the partition statistics, and the weighted mean of the rows.  Row r
+// of tmp_output holds the normalised merge of partitions r, r + rstride, ... (one partition
+// per row when rstride >= Pl), so its weight is the sum of theirs.  Reads go to L2 (ld.cg):
+// the rows were written by other CTAs.  `wsm` is shared memory for 8 + nh * rows floats.
+template <bool BF16, int D>
+__device__ __forceinline__ void fused_combine(const Phase1Params& p, int s, int h0, int nh, int Pl, int rstride,
+                                           float* wsm) {
+    const int R = min(rstride, Pl);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float* tot = wsm;
+    float* wts = wsm + kMaxHeadsPerCta;
+    for (int hh = warp; hh < nh; hh += kWarps) {
+        const int64_t srow = ((int64_t)s * p.H + h0 + hh) * p.Pmax;
+        float gm = -INFINITY;
+        for (int q = lane; q < Pl; q += 32)
+            if (__ldcg(p.exp_sums + srow + q) > 0.f) gm = fmaxf(gm, __ldcg(p.max_logits + srow + q) * kLog2e);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, o));
+        float sum = 0.f;
+        for (int r = lane; r < R; r += 32) {
+            float w = 0.f;
+            for (int q = r; q < Pl; q += rstride) {
+                const float l = __ldcg(p.exp_sums + srow + q);
+                if (l > 0.f) w += l * ex2(__ldcg(p.max_logits + srow + q) * kLog2e - gm);
+            }
+            wts[hh * R + r] = w;
+            sum += w;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+        if (lane == 0) tot[hh] = sum;
+    }
+    __syncthreads();
+    constexpr int D4 = D / 4;  // four output elements per thread and step
+    for (int e = threadIdx.x; e < nh * D4; e += blockDim.x) {
+        const int hh = e / D4, c = e - hh * D4;
+        const int64_t row = (int64_t)s * p.H + h0 + hh;
+        const float* w = wts + hh * R;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+        for (int r = 0; r < R; ++r) {
+            const int64_t i4 = (row * p.Pmax + r) * D4 + c;
+            float4 x;
+            if (p.tmp16) {
+                const uint2 u = __ldcg(reinterpret_cast<const uint2*>(p.tmp_out) + i4);
+                if constexpr (BF16) {
+                    x = make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u),
+                                    __uint_as_float(u.y << 16), __uint_as_float(u.y & 0xffff0000u));
+                } else {
+                    x = make_float4(f16_lo_to_f32(u.x), f16_hi_to_f32(u.x), f16_lo_to_f32(u.y), f16_hi_to_f32(u.y));
+                }
+            } else {
+                x = __ldcg(reinterpret_cast<const float4*>(p.tmp_out) + i4);
+            }
+            const float wr = w[r];
+            acc.x = fmaf(wr, x.x, acc.x);
+            acc.y = fmaf(wr, x.y, acc.y);
+            acc.z = fmaf(wr, x.z, acc.z);
+            acc.w = fmaf(wr, x.w, acc.w);
+        }
+        const float t = tot[hh];
+        const float inv = t > 0.f ? 1.f / t : 0.f;
+        const int64_t o = row * D + 4 * c;
+        store_out<BF16>(p.out, o, acc.x * inv);
+        store_out<BF16>(p.out, o + 1, acc.y * inv);
+        store_out<BF16>(p.out, o + 2, acc.z * inv);
+        store_out<BF16>(p.out, o + 3, acc.w * inv);
+    }
+}
+
 // ---------------------------------------------------------------------------------------
 // Phase 1
 // ---------------------------------------------------------------------------------------
@@ -135,7 +225,9 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     float* red_l = red_m + kWarps * kMaxHeadsPerCta;
     float* fin_m = red_l + kWarps * kMaxHeadsPerCta;  // [8] merged max (log2 units)
     float* fin_l = fin_m + kMaxHeadsPerCta;           // [8] merged exp-sum
-    float* red_o = fin_l + kMaxHeadsPerCta;           // [kWarps][nh][D + 4] scaled accumulators
+    float* fac_o = fin_l + kMaxHeadsPerCta;           // [8] CTA merge: factor on the row so far
+    float* fac_n = fac_o + kMaxHeadsPerCta;           // [8] CTA merge: factor on this partition
+    float* red_o = fac_n + kMaxHeadsPerCta;           // [kWarps][nh][D + 4] scaled accumulators
     constexpr int RS = D + 4;
 
     if (lane == 0) {
@@ -315,7 +407,17 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     // Physical tokens of this thread's two MMA rows (g, g + 8).
     const int tokA = FP8 ? c_fp8_row_token[g] : g;
     const int tokB = FP8 ? c_fp8_row_token[g + 8] : g + 8;
-    const bool single = (P == 1);
+    // Where a partition's result goes.  A one-partition sequence writes the output directly
+    // (single pass).  Otherwise each partition writes its own tmp_output row -- or, when the
+    // CTA merges its partitions (fused combine), the CTA folds them into fp32 row px, and a
+    // CTA that covers every partition of the sequence (PX == 1) writes the output directly.
+    const int nwork = min(PX, Pl);  // CTAs of this (sequence, head group) that have partitions
+    const bool fused = p.counters != nullptr;
+    const bool merge = fused && p.merge != 0;
+    const bool direct = (Pl == 1) || (merge && nwork == 1);
+    // The CTA's running merge (lane t < 4 of warp 0 holds heads 2t and 2t + 1): max in log2
+    // units relative to the sequence's last token, and the exp-sum at that max.
+    float cA0 = -INFINITY, cA1 = -INFINITY, cL0 = 0.f, cL1 = 0.f;
     uint32_t drain_from = 0;
 
     for (; cq < Pl; cq += PX) {
@@ -683,6 +785,14 @@ pa_v2_phase1_kernel(const Phase1Params p) {
             fin_m[2 * t + 1] = M1;
             fin_l[2 * t] = L0;
             fin_l[2 * t + 1] = L1;
+            if (merge) {
+                // fold this partition into the CTA's row, in log2 units relative to the last
+                // token (the ALiBi bias of the scores is relative to this partition's last)
+                const float rel = (float)(tref - (L - 1));
+                merge_factors(cA0, cL0, L0 > 0.f ? fmaf(sl0, rel, M0) : -INFINITY, L0, fac_o[2 * t], fac_n[2 * t]);
+                merge_factors(cA1, cL1, L1 > 0.f ? fmaf(sl1, rel, M1) : -INFINITY, L1, fac_o[2 * t + 1],
+                              fac_n[2 * t + 1]);
+            }
         }
 #pragma unroll
         for (int mt = 0; mt < NK; ++mt) {
@@ -708,7 +818,18 @@ pa_v2_phase1_kernel(const Phase1Params p) {
             const float lt = fin_l[hh];
             v = lt > 0.f ? v * (v_mul / lt) : 0.f;
             const int64_t row = (int64_t)s * H + h0 + hh;
-            if (single)
+            if (merge) {
+                // row px so far (written by this thread for the CTA's previous partition) and
+                // this partition, each with its share of the merged exp-sum
+                float* mrow = static_cast<float*>(p.tmp_out) + (row * p.Pmax + px) * D;
+                const float fo = fac_o[hh];
+                float r = v * fac_n[hh];
+                if (fo != 0.f) r = fmaf(mrow[i], fo, r);
+                if (direct && cq + PX >= Pl)
+                    store_out<BF16>(p.out, row * D + i, r);
+                else
+                    mrow[i] = r;
+            } else if (direct)
                 store_out<BF16>(p.out, row * D + i, v);
             else if (p.tmp16)
                 store_out<BF16>(p.tmp_out, (row * p.Pmax + cq) * D + i, v);
@@ -743,6 +864,27 @@ pa_v2_phase1_kernel(const Phase1Params p) {
         // Let every copy this warp started land before the block can exit.
         for (uint32_t n = drain_from; n < nis; ++n)
             (void)mbar_wait_bounded(&bars[n % nstage], (n / nstage) & 1u, kWaitLimitNs);
+    }
+
+    // Fused combine: count this CTA in; the last of the (sequence, head group) to arrive
+    // merges the rows of all of them.  Nothing waits: every CTA but the last just exits.
+    if (fused && Pl > 1 && !direct) {
+        __threadfence();  // this thread's rows and statistics are visible GPU-wide ...
+        __syncthreads();  // ... for every thread of the CTA, before the arrival
+        int* last = reinterpret_cast<int*>(red_m);
+        if (threadIdx.x == 0) {
+            uint32_t* ctr = p.counters + (int64_t)s * gridDim.y + blockIdx.y;
+            const uint32_t before = atomicAdd(ctr, 1u);
+            const bool is_last = before == (uint32_t)(nwork - 1);
+            if (is_last) atomicExch(ctr, 0u);  // left at zero for the next call
+            __threadfence();
+            *last = is_last ? 1 : 0;
+        }
+        __syncthreads();
+        if (*last) {
+            // the page ring is idle now (every copy has landed): it holds the row weights
+            fused_combine<BF16, D>(p, s, h0, nh, Pl, merge ? PX : Pl, reinterpret_cast<float*>(smem));
+        }
     }
     griddep_launch_dependents();
 }

@@ -40,8 +40,9 @@ def to_device(wl, device="cuda"):
 
 
 def run_decode(wl, dev=None, max_num_partitions=None, max_seq_len=None, poison=True,
-               tmp_dtype=torch.float32):
-    """pa_v2_decode on a workload; returns CPU tensors (out, exp_sums, max_logits, tmp)."""
+               tmp_dtype=torch.float32, counters=None, stream=None):
+    """pa_v2_decode on a workload (pa_v2_decode_fused when `counters` is given); returns CPU
+    tensors (out, exp_sums, max_logits, tmp)."""
     if dev is None:
         dev = to_device(wl)
     S, H, d = wl.query.shape
@@ -54,7 +55,8 @@ def run_decode(wl, dev=None, max_num_partitions=None, max_seq_len=None, poison=T
     tmp = torch.full((S, H, P, d), fill, dtype=tmp_dtype, device="cuda")
     pa.pa_v2_decode(out, es, ml, tmp, dev["query"], dev["key_cache"], dev["value_cache"],
                     wl.num_kv_heads, wl.scale, dev["block_tables"], dev["seq_lens"], wl.block_size,
-                    msl, dev["alibi"], wl.kv_cache_dtype, wl.k_scale, wl.v_scale)
+                    msl, dev["alibi"], wl.kv_cache_dtype, wl.k_scale, wl.v_scale, counters=counters,
+                    stream=stream)
     torch.cuda.synchronize()
     return out.cpu(), es.cpu(), ml.cpu(), tmp.cpu()
 
@@ -63,11 +65,12 @@ def out_f64(t: torch.Tensor) -> np.ndarray:
     return t.to(torch.float64).numpy()
 
 
-def check_decode(wl, gpu, ref, pairs=None, label=""):
+def check_decode(wl, gpu, ref, pairs=None, label="", check_tmp=True):
     """Compare GPU results with oracle results (optionally only on (s, h) pairs).
     With a 16-bit tmp_output each partition's output is rounded once more to the output
     dtype, so both the tmp and the output bounds add half an ulp of the largest partition
-    value.  Returns a dict of the worst errors seen."""
+    value.  check_tmp=False skips tmp_output (scratch for pa_v2_decode_fused).  Returns a
+    dict of the worst errors seen."""
     out, es, ml, tmp = gpu
     tmp16 = tmp.dtype != torch.float32
     H = wl.num_heads
@@ -103,7 +106,7 @@ def check_decode(wl, gpu, ref, pairs=None, label=""):
                 assert de <= TOL_STAT, f"{label} exp_sum s={s} h={h} p={p}: {ge} vs {re_}"
                 worst["ml"] = max(worst["ml"], dm / max(abs(rm), 1.0))
                 worst["es"] = max(worst["es"], de)
-                if Ps > 1:
+                if Ps > 1 and check_tmp:
                     rt = ref["tmp_out"][n, p]
                     te = np.abs(tmp[s, h, p].double().numpy() - rt)
                     tallow = tol + (half_ulp(rt, wl.q_dtype) if tmp16 else 0.0)

@@ -94,6 +94,24 @@ def test_decode_with_zero_sequences_is_a_noop():
     assert _decode_raw(num_seqs=0, output=None, query=None) == 0
 
 
+def test_fused_decode_host_checks():
+    lib = pa.load()
+    P = 0x10000
+    # one counter per (sequence, kv head, group of <= 8 query heads)
+    assert pa.decode_num_counters(2, 8, 2) == 4
+    assert pa.decode_num_counters(3, 32, 2) == 12        # 16 query heads per kv head: 2 groups
+    assert pa.decode_num_counters(2, 6, 4) == 0          # H % Hk != 0
+    args = [P, P, P, P, P, P, P, 2, 8, 2, 128, 0.088, P, 64, 100, P, 16, 1024, 2, None, 0, 0, 2, 1.0, 1.0]
+    assert lib.pa_v2_decode_fused(*args, 0x10002, 4, None) == 1    # counters not 4-byte aligned
+    assert lib.pa_v2_decode_fused(*args, P, 3, None) == 1          # fewer counters than the step needs
+    bad = list(args)
+    bad[9] = 3                                                     # H % Hk != 0, as pa_v2_decode
+    assert lib.pa_v2_decode_fused(*bad, P, 4, None) == 1
+    zero = list(args)
+    zero[7] = 0                                                    # no sequences: nothing to do
+    assert lib.pa_v2_decode_fused(*zero, None, 0, None) == 0
+
+
 def _cache_raw(**over):
     lib = pa.load()
     P = 0x10000
