@@ -346,8 +346,12 @@ PA_API pa_status pa_v2_set_timing_events(cudaEvent_t begin, cudaEvent_t end);
  * the library defines at file scope: every GPU that loads the library holds it until the
  * process exits.  This call allocates nothing (no cudaMalloc, cudaFree or allocating
  * library routine).  The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current.  The partition statistics a caller of pa_v2_decode would receive are not
- * returned.
+ * (cudaGetSymbolAddress) with that device current, and later calls reuse it; the call works
+ * on the current device, so make the device of the pointers current.  A device reset
+ * (cudaDeviceReset, or the primary context destroyed and created again) moves the array, and
+ * the address looked up before it is then stale: do not call this entry point again in a
+ * process after resetting a device it ran on.  The partition statistics a caller of
+ * pa_v2_decode would receive are not returned.
  *
  * Errors: as pa_v2_decode, plus PA_ERR_SCRATCH_TOO_SMALL when
  *   2 * align256(S*H*P*4) + S*H*P*head_size*4 > PA_NOALLOC_SCRATCH_BYTES,

@@ -208,9 +208,10 @@ def pa_v2_decode_noalloc(output: torch.Tensor, query: torch.Tensor, key_cache: t
                          kv_cache_dtype: str = "auto", k_scale: float = 1.0, v_scale: float = 1.0,
                          num_blocks: Optional[int] = None, stream=None) -> None:
     """pa_v2_decode without a caller-provided workspace: for callers that cannot allocate
-    device memory (a plugin with a fixed memory budget, code running under stream capture).
-    The workspace is the library's fixed per-device scratch, shared by every call; calls that
-    can overlap on the GPU race on it."""
+    device memory (a plugin handed a stream and a device-memory budget fixed at start-up).
+    The workspace is the library's fixed per-device scratch, shared by every call: order the
+    calls on one stream (calls that can overlap on the GPU race on it).  The call runs with
+    the query's device current, since the scratch address is looked up per device."""
     lib = load()
     for name, t in (("output", output), ("query", query), ("key_cache", key_cache),
                     ("value_cache", value_cache), ("block_tables", block_tables), ("seq_lens", seq_lens)):
@@ -223,12 +224,13 @@ def pa_v2_decode_noalloc(output: torch.Tensor, query: torch.Tensor, key_cache: t
     S, H, d = query.shape
     if num_blocks is None:
         num_blocks = key_cache.shape[0]
-    st = lib.pa_v2_decode_noalloc(_ptr(output), _ptr(query), _ptr(key_cache), _ptr(value_cache), S, H,
-                                  int(num_kv_heads), d, float(scale), _ptr(block_tables),
-                                  int(block_tables.shape[1]), int(num_blocks), _ptr(seq_lens),
-                                  int(block_size), int(max_seq_len), _ptr(alibi_slopes),
-                                  _dt(query.dtype), _kv(kv_cache_dtype), float(k_scale), float(v_scale),
-                                  _stream(stream))
+    with torch.cuda.device(query.device):
+        st = lib.pa_v2_decode_noalloc(_ptr(output), _ptr(query), _ptr(key_cache), _ptr(value_cache), S, H,
+                                      int(num_kv_heads), d, float(scale), _ptr(block_tables),
+                                      int(block_tables.shape[1]), int(num_blocks), _ptr(seq_lens),
+                                      int(block_size), int(max_seq_len), _ptr(alibi_slopes),
+                                      _dt(query.dtype), _kv(kv_cache_dtype), float(k_scale), float(v_scale),
+                                      _stream(stream))
     _check("pa_v2_decode_noalloc", st)
 
 

@@ -1,7 +1,7 @@
 // pa_cache.cu -- slot-mapping cache writer ("paged_attn.py", write_to_paged_cache ->
 // reshape_and_cache; cache views from split_kv_cache) for sm_103a.
 //
-// One CTA per new token.  Each thread moves one x-element chunk of one kv head: the K
+// One CTA per new token, one thread per x-element chunk of one kv head: the K
 // chunk is contiguous in both the source row and the cache (x elements = 16 bytes), so it
 // is one 16-byte store; the V elements of a chunk land block_size elements apart
 // (value_cache[b][h][i][o]).  fp16/bf16 caches get a bitwise copy; an fp8 cache gets
@@ -41,7 +41,7 @@ __device__ __forceinline__ float to_f32(uint16_t v) {
 }
 
 template <bool FP8, bool BF16>
-__global__ void __launch_bounds__(128) pa_cache_write_kernel(const CacheParams p) {
+__global__ void __launch_bounds__(512) pa_cache_write_kernel(const CacheParams p) {
     griddep_wait();
     griddep_launch_dependents();
     const int tok = blockIdx.x;
@@ -177,7 +177,11 @@ extern "C" pa_status pa_reshape_and_cache(const void* key, const void* value, in
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)num_tokens, 1, 1);
-    cfg.blockDim = dim3(128, 1, 1);
+    // one thread per (kv head, x-element chunk) of a token, so one pass covers the token
+    // (every load of the CTA in one round trip); at most 512 threads
+    int threads = ((num_kv_heads * (head_size / x) + 31) / 32) * 32;
+    threads = threads > 512 ? 512 : threads;
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;

@@ -216,6 +216,74 @@ pa_v2_phase2_kernel(const Phase2Params p) {
     }
 }
 
+// Phase 2, one warp per (sequence, query head) row and eight rows per CTA: the form for
+// steps of at most 64 partitions and head size <= 128 (lane c holds output columns 4c..4c+3).
+// A batch of many rows then needs few CTAs, and each row costs about one memory round trip:
+// the statistics (two per lane) and the tmp rows of its first kP2RowChunk partitions load
+// together, before any of them is used.
+constexpr int kP2RowsPerCta = 8;
+constexpr int kP2RowChunk = 16;
+
+template <bool BF16, bool TMP16>
+__global__ void __launch_bounds__(kP2RowsPerCta * 32)
+pa_v2_phase2_rows_kernel(const Phase2Params p) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t row = (int64_t)blockIdx.x * kP2RowsPerCta + warp;  // s * H + h
+    const bool live = row < (int64_t)p.S * p.H;
+    // seq_lens is an input that phase 1 only read: safe to read before the wait
+    const int L = live ? p.seq_lens[row / p.H] : 0;
+    griddep_wait();
+    const int P = min(L > 0 ? (L + kPartition - 1) / kPartition : 0, p.Pmax);
+    if (!live || P <= 1) return;  // written by phase 1 (single pass or empty)
+    const int nq = p.D / 4;
+    const bool col = lane < nq;
+    const float* ml = p.max_logits + row * p.Pmax;
+    const float* es = p.exp_sums + row * p.Pmax;
+    const int64_t tmp4 = row * p.Pmax * nq + lane;
+    // issue every load of the first chunk before any arithmetic
+    const float m0 = lane < P ? ml[lane] : -INFINITY, l0 = lane < P ? es[lane] : 0.f;
+    const float m1 = lane + 32 < P ? ml[lane + 32] : -INFINITY, l1 = lane + 32 < P ? es[lane + 32] : 0.f;
+    float4 x[kP2RowChunk];
+#pragma unroll
+    for (int j = 0; j < kP2RowChunk; ++j)
+        x[j] = (j < P && col) ? load_tmp4<BF16, TMP16>(p.tmp_out, tmp4 + (int64_t)j * nq) : make_float4(0.f, 0.f, 0.f, 0.f);
+    // weights exp(m_q - g) l_q, lane q holding partitions q and q + 32
+    const float a0 = l0 > 0.f ? m0 * kLog2e : -INFINITY, a1 = l1 > 0.f ? m1 * kLog2e : -INFINITY;
+    float gm = fmaxf(a0, a1);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, o));
+    const float w0 = a0 == -INFINITY ? 0.f : l0 * ex2(a0 - gm), w1 = a1 == -INFINITY ? 0.f : l1 * ex2(a1 - gm);
+    float tot = w0 + w1;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q0 = 0; q0 < P; q0 += kP2RowChunk) {
+        if (q0 > 0) {
+#pragma unroll
+            for (int j = 0; j < kP2RowChunk; ++j)
+                x[j] = (q0 + j < P && col) ? load_tmp4<BF16, TMP16>(p.tmp_out, tmp4 + (int64_t)(q0 + j) * nq)
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int j = 0; j < kP2RowChunk; ++j) {
+            const int q = q0 + j;  // the same on every lane
+            const float w = __shfl_sync(0xffffffffu, q < 32 ? w0 : w1, q & 31);
+            acc.x = fmaf(w, x[j].x, acc.x);
+            acc.y = fmaf(w, x[j].y, acc.y);
+            acc.z = fmaf(w, x[j].z, acc.z);
+            acc.w = fmaf(w, x[j].w, acc.w);
+        }
+    }
+    if (col) {
+        const float inv = tot > 0.f ? 1.f / tot : 0.f;
+        const int64_t o = row * p.D + 4 * lane;
+        store_out<BF16>(p.out, o, acc.x * inv);
+        store_out<BF16>(p.out, o + 1, acc.y * inv);
+        store_out<BF16>(p.out, o + 2, acc.z * inv);
+        store_out<BF16>(p.out, o + 3, acc.w * inv);
+    }
+}
+
 // ---------------------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------------------
@@ -405,13 +473,39 @@ int64_t pa::decode_num_counters(int num_seqs, int num_heads, int num_kv_heads) {
     return (int64_t)num_seqs * num_kv_heads * ((G + kMaxHeadsPerCta - 1) / kMaxHeadsPerCta);
 }
 
-// Partition stride override for tuning runs (PA_DECODE_PX=n; 0 or unset: the heuristic).
+// Overrides for tuning runs, read once: the partition stride (PA_DECODE_PX=n) and the page
+// ring per CTA in KiB (PA_DECODE_RING_KIB=n); 0 or unset: the heuristics.
+static int env_int(const char* name) {
+    const char* e = getenv(name);
+    return e ? atoi(e) : 0;
+}
 static int px_override() {
-    static const int v = [] {
-        const char* e = getenv("PA_DECODE_PX");
-        return e ? atoi(e) : 0;
-    }();
+    static const int v = env_int("PA_DECODE_PX");
     return v;
+}
+static int ring_override_kib() {
+    static const int v = env_int("PA_DECODE_RING_KIB");
+    return v;
+}
+
+// SM count and opt-in shared memory per block of a device, queried once per device.
+static cudaError_t sm_count(int dev, int* sms, int* optin) {
+    constexpr int kMaxDev = 64;
+    static int cache_sms[kMaxDev] = {}, cache_optin[kMaxDev] = {};
+    static std::mutex mu;
+    if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache_sms[dev] == 0) {
+        cudaError_t e = cudaDeviceGetAttribute(&cache_sms[dev], cudaDevAttrMultiProcessorCount, dev);
+        if (e == cudaSuccess) e = cudaDeviceGetAttribute(&cache_optin[dev], cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+        if (e != cudaSuccess) {
+            cache_sms[dev] = 0;
+            return e;
+        }
+    }
+    *sms = cache_sms[dev];
+    *optin = cache_optin[dev];
+    return cudaSuccess;
 }
 
 pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_logits, void* tmp_out,
@@ -425,24 +519,38 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
     const int pps = fp8 ? 32 / bs : (bs >= 16 ? 1 : 16 / bs);  // pages per ring slot, as in the kernel
     const uint32_t page_bytes = (uint32_t)D * bs * kvb;
     const uint32_t slot_bytes = 2u * pps * page_bytes;
-    // Ring depth: about kRingTarget bytes of pages per CTA, at least one slot per warp.
-    int nstage = (int)(kRingTarget / (kWarps * slot_bytes));
-    nstage = nstage < 1 ? 1 : (nstage > 8 ? 8 : nstage);
-    if (nstage < PA_MIN_STAGES && (uint32_t)PA_MIN_STAGES * kWarps * slot_bytes <= 160u * 1024u) nstage = PA_MIN_STAGES;
-    const uint32_t ring = (uint32_t)kWarps * nstage * slot_bytes;
-    const int red_heads = G < kMaxHeadsPerCta ? G : kMaxHeadsPerCta;
-    const size_t smem1 = ring + kWarps * nstage * sizeof(uint64_t) +
-                         (2 * kWarps + 4) * kMaxHeadsPerCta * sizeof(float) +
-                         (size_t)kWarps * red_heads * (D + 4) * sizeof(float);
-
-    Phase1Fn fn = phase1_for(bf16, fp8, D, bs);
-    if (fn == nullptr) return PA_ERR_UNSUPPORTED;
-    int dev = 0, optin = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess) {
+    int dev = 0, optin = 0, nsm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || sm_count(dev, &nsm, &optin) != cudaSuccess) {
         (void)cudaGetLastError();
         return PA_ERR_CUDA;
     }
+    // Ring depth: about kRingTarget bytes of pages per CTA, at least one slot per warp.  A
+    // grid of fewer CTAs than two per SM (a small batch: few sequences x kv heads x
+    // partitions) gets a deeper ring, since its few CTAs must each keep more bytes in flight
+    // to cover the memory latency.
+    uint32_t target = kRingTarget;
+    const int64_t max_ctas = (int64_t)a.num_seqs * a.num_kv_heads * ngroups * a.max_num_partitions;
+    if (ring_override_kib() > 0)
+        target = (uint32_t)ring_override_kib() * 1024u;
+    else if (max_ctas <= nsm)
+        target = 192u * 1024u;
+    else if (max_ctas <= 2 * (int64_t)nsm)
+        target = 96u * 1024u;
+    int nstage = (int)(target / (kWarps * slot_bytes));
+    nstage = nstage < 1 ? 1 : (nstage > 8 ? 8 : nstage);
+    if (nstage < PA_MIN_STAGES && (uint32_t)PA_MIN_STAGES * kWarps * slot_bytes <= 160u * 1024u) nstage = PA_MIN_STAGES;
+    const int red_heads = G < kMaxHeadsPerCta ? G : kMaxHeadsPerCta;
+    auto smem_for = [&](int ns) {
+        return (size_t)kWarps * ns * slot_bytes + kWarps * ns * sizeof(uint64_t) +
+               (2 * kWarps + 4) * kMaxHeadsPerCta * sizeof(float) +
+               (size_t)kWarps * red_heads * (D + 4) * sizeof(float);
+    };
+    while (nstage > 1 && smem_for(nstage) > (size_t)optin) --nstage;  // a deep ring that does not fit
+    const uint32_t ring = (uint32_t)kWarps * nstage * slot_bytes;
+    const size_t smem1 = smem_for(nstage);
+
+    Phase1Fn fn = phase1_for(bf16, fp8, D, bs);
+    if (fn == nullptr) return PA_ERR_UNSUPPORTED;
     if (smem1 > (size_t)optin) return PA_ERR_UNSUPPORTED;
     if (ensure_smem((const void*)fn, smem1) != cudaSuccess) {
         (void)cudaGetLastError();
@@ -484,52 +592,57 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
     // (PX = max_num_partitions) schedules finest, but a ragged batch whose longest sequence
     // is far above the typical one would then launch mostly empty CTAs, each holding a
     // shared-memory slot while it starts.  So PX is capped to keep the grid within about
-    // PA_GRID_WAVES full waves, and each CTA takes at most 8 partitions.
+    // PA_GRID_WAVES full waves, and each CTA takes at most 8 partitions.  A batch of few rows
+    // (sequences x kv heads x head groups, fewer than the GPU has CTA slots) of long sequences
+    // instead gets exactly one wave: PX = slots / rows, each CTA streaming its partitions
+    // back to back (measured on 4 x 100K tokens: 251 us against 264 us for one partition per
+    // CTA and 317 us for 1.3 waves).
     int sms = 0, per_sm = 0;
     if (occupancy((const void*)fn, kWarps * 32, smem1, &sms, &per_sm) != cudaSuccess) {
         (void)cudaGetLastError();
         return PA_ERR_CUDA;
     }
+    const int64_t Pmax = a.max_num_partitions;
     const int64_t rows = (int64_t)a.num_kv_heads * ngroups * a.num_seqs;
-    const int64_t budget = (int64_t)PA_GRID_WAVES * sms * (per_sm > 0 ? per_sm : 1);
-    int64_t PX = budget / rows;
-    const int64_t px_min = (a.max_num_partitions + 7) / 8;
-    if (PX < px_min) PX = px_min;
-    if (PX > a.max_num_partitions) PX = a.max_num_partitions;
+    const int64_t slots = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
+    int64_t PX;
+    if (rows < slots && rows * Pmax > slots) {
+        PX = slots / rows;
+    } else {
+        PX = (int64_t)PA_GRID_WAVES * slots / rows;
+        const int64_t px_min = (Pmax + 7) / 8;
+        if (PX < px_min) PX = px_min;
+    }
+    if (px_override() > 0) PX = px_override();
+    if (PX > Pmax) PX = Pmax;
     if (PX < 1) PX = 1;
 
     // Fused combine (V1/V2 dispatch, "paged_attn.py" forward_decode, re-decided for this GPU):
     // with arrival counters the last CTA of each (sequence, head group) merges the partitions,
-    // so no second kernel waits for the whole grid.  With an fp32 tmp_output every CTA first
-    // folds its own partitions into one row, and the partition stride is capped so that the
-    // last CTA merges at most kFusedRowBytes of rows (a long sequence then streams several
-    // partitions per CTA).  A 16-bit tmp_output keeps one row per partition, so the fused
-    // combine is taken only while all of them fit that bound.
-    bool fused = counters != nullptr && a.max_num_partitions > 1;
+    // so no second kernel waits for the whole grid.  Arriving costs every CTA a fence and an
+    // atomic round trip at its end (about 2 us of its slot), which a grid of many waves pays
+    // many times over; a grid of at most two waves pays it once and saves the second
+    // kernel's launch and wait.  So the combine is fused only there.  With an fp32 tmp_output
+    // every CTA folds its own partitions into one row (the last CTA merges PX rows); a 16-bit
+    // one keeps a row per partition.  Either way the rows the last CTA merges are bounded by
+    // kFusedRowBytes.
+    bool fused = counters != nullptr && Pmax > 1 && rows * PX <= 2 * slots;
     if (fused) {
         const bool merge = a.tmp_dtype == PA_DT_F32;
+        const int64_t R = merge ? PX : Pmax;
         const int64_t row_bytes = (int64_t)red_heads * D * (merge ? 4 : 2);
-        if (merge) {
-            int64_t cap = kFusedRowBytes / row_bytes;
-            if (cap < 1) cap = 1;
-            if (PX > cap) PX = cap;
-        }
-        if (px_override() > 0) PX = px_override() < a.max_num_partitions ? px_override() : a.max_num_partitions;
-        const int64_t R = merge ? PX : a.max_num_partitions;
         // the row weights live in the idle page ring during the combine
         if ((kMaxHeadsPerCta + (int64_t)red_heads * R) * (int64_t)sizeof(float) > (int64_t)ring ||
-            (!merge && R * row_bytes > kFusedRowBytes))
+            R * row_bytes > kFusedRowBytes)
             fused = false;
         if (fused) {
             p1.counters = counters;
             p1.merge = merge ? 1 : 0;
         }
-    } else if (px_override() > 0) {
-        PX = px_override() < a.max_num_partitions ? px_override() : a.max_num_partitions;
     }
 
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)PX, (unsigned)(a.num_kv_heads * ngroups), (unsigned)a.num_seqs);
+    cfg.gridDim = dim3((unsigned)(PX * ngroups), (unsigned)a.num_kv_heads, (unsigned)a.num_seqs);
     cfg.blockDim = dim3(kWarps * 32, 1, 1);
     cfg.dynamicSmemBytes = smem1;
     cfg.stream = a.stream;
@@ -550,14 +663,34 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
         p2.max_logits = max_logits;
         p2.tmp_out = tmp_out;
         p2.seq_lens = a.seq_lens;
+        p2.S = a.num_seqs;
         p2.H = a.num_heads;
         p2.D = D;
         p2.Pmax = a.max_num_partitions;
+        const bool t16 = a.tmp_dtype != PA_DT_F32;
+        if (a.max_num_partitions <= 64 && D <= 128) {
+            // one warp per row (a wide batch of short and medium sequences)
+            void (*fr)(const Phase2Params) =
+                bf16 ? (t16 ? pa_v2_phase2_rows_kernel<true, true> : pa_v2_phase2_rows_kernel<true, false>)
+                     : (t16 ? pa_v2_phase2_rows_kernel<false, true> : pa_v2_phase2_rows_kernel<false, false>);
+            const int64_t nrows = (int64_t)a.num_seqs * a.num_heads;
+            cudaLaunchConfig_t cr = {};
+            cr.gridDim = dim3((unsigned)((nrows + kP2RowsPerCta - 1) / kP2RowsPerCta), 1, 1);
+            cr.blockDim = dim3(kP2RowsPerCta * 32, 1, 1);
+            cr.dynamicSmemBytes = 0;
+            cr.stream = a.stream;
+            cr.attrs = attr;
+            cr.numAttrs = 1;
+            if (cudaLaunchKernelEx(&cr, fr, p2) != cudaSuccess) {
+                (void)cudaGetLastError();
+                return PA_ERR_CUDA;
+            }
+            return PA_OK;
+        }
         // Warps per combine: about 8 partitions per warp, 1 .. 16 warps.
         int w2 = (a.max_num_partitions + 7) / 8;
         w2 = w2 < 1 ? 1 : (w2 > kP2MaxWarps ? kP2MaxWarps : w2);
         const size_t smem2 = (size_t)w2 * D * sizeof(float);
-        const bool t16 = a.tmp_dtype != PA_DT_F32;
         void (*fn2)(const Phase2Params) =
             bf16 ? (t16 ? pa_v2_phase2_kernel<true, true> : pa_v2_phase2_kernel<true, false>)
                  : (t16 ? pa_v2_phase2_kernel<false, true> : pa_v2_phase2_kernel<false, false>);

@@ -28,7 +28,7 @@ constexpr uint32_t kRingTarget = PA_RING_KIB * 1024u;  // shared-memory page rin
 constexpr int kMaxHeadsPerCta = 8;     // the MMA N dimension
 // Fused combine: most bytes of rows the last CTA of a (sequence, head group) merges.
 #ifndef PA_FUSED_ROW_KIB
-#define PA_FUSED_ROW_KIB 64
+#define PA_FUSED_ROW_KIB 128
 #endif
 constexpr int64_t kFusedRowBytes = PA_FUSED_ROW_KIB * 1024;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;
@@ -67,7 +67,7 @@ struct Phase2Params {
     const float* max_logits;
     const void* tmp_out;  // fp32, or the output dtype (template parameter TMP16)
     const int32_t* seq_lens;
-    int H, D, Pmax;
+    int S, H, D, Pmax;
 };
 
 template <bool BF16>

@@ -135,9 +135,14 @@ pa_v2_phase1_kernel(const Phase1Params p) {
 
     // This CTA handles partitions px, px + PX, ... of one sequence for one group of <= 8
     // query heads sharing a kv head.
-    const int px = blockIdx.x, PX = gridDim.x;
-    const int kvh = blockIdx.y / p.ngroups;
-    const int grp = blockIdx.y - kvh * p.ngroups;
+    // blockIdx.x = px * ngroups + grp: the head groups of one kv head (more than 8 query
+    // heads per kv head) are neighbours in the grid, so they start together and stream the
+    // same pages at about the same time -- the later ones find them in L2.
+    const int ng = p.ngroups;
+    const int px = ng == 1 ? (int)blockIdx.x : (int)blockIdx.x / ng;
+    const int PX = ng == 1 ? (int)gridDim.x : (int)gridDim.x / ng;
+    const int grp = (int)blockIdx.x - px * ng;
+    const int kvh = blockIdx.y;
     const int s = blockIdx.z;
     const int h0 = kvh * p.G + grp * kMaxHeadsPerCta;
     const int nh = min(kMaxHeadsPerCta, p.G - grp * kMaxHeadsPerCta);
@@ -236,7 +241,9 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     }
     __syncwarp();
 
-    const uint64_t policy = l2_policy_evict_first();
+    // Pages are read once: evict-first, except by head groups other than the last of their
+    // kv head, whose pages a neighbouring CTA reads right after them.
+    const uint64_t policy = grp == ng - 1 ? l2_policy_evict_first() : l2_policy_evict_normal();
     const uint8_t* kc_head = p.kcache + (size_t)kvh * page_bytes;
     const uint8_t* vc_head = p.vcache + (size_t)kvh * page_bytes;
     const size_t block_stride = (size_t)p.Hk * page_bytes;
@@ -752,6 +759,20 @@ pa_v2_phase1_kernel(const Phase1Params p) {
             issue_more();
         }
 
+        // CTA merge: the row built from this CTA's earlier partitions, loaded now so that the
+        // loads overlap the cross-warp merge below (thread t owns elements t, t + 128, ...)
+        constexpr int NE = (kMaxHeadsPerCta * D + kWarps * 32 - 1) / (kWarps * 32);
+        float prev[NE];
+        if (merge && cq != px) {
+            const float* mrow0 = static_cast<const float*>(p.tmp_out) + ((int64_t)s * H + h0) * p.Pmax * D + (int64_t)px * D;
+#pragma unroll
+            for (int k = 0; k < NE; ++k) {
+                const int e = threadIdx.x + k * kWarps * 32;
+                const int hh = e / D;
+                prev[k] = e < nh * D ? mrow0[(int64_t)hh * p.Pmax * D + (e - hh * D)] : 0.f;
+            }
+        }
+
         // ---- merge the warps' (m, l, acc) of this partition --------------------------------
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) {
@@ -810,7 +831,31 @@ pa_v2_phase1_kernel(const Phase1Params p) {
         }
         __syncthreads();
 
-        for (int e = threadIdx.x; e < nh * D; e += blockDim.x) {
+        if (merge) {
+            // row px so far and this partition, each with its share of the merged exp-sum
+            const bool to_out = direct && cq + PX >= Pl;
+#pragma unroll
+            for (int k = 0; k < NE; ++k) {
+                const int e = threadIdx.x + k * kWarps * 32;
+                if (e < nh * D) {
+                    const int hh = e / D, i = e - hh * D;
+                    float v = 0.f;
+#pragma unroll
+                    for (int w = 0; w < kWarps; ++w) v += red_o[(w * nh + hh) * RS + i];
+                    const float lt = fin_l[hh];
+                    v = lt > 0.f ? v * (v_mul / lt) : 0.f;
+                    const float fo = fac_o[hh];
+                    float r = v * fac_n[hh];
+                    if (fo != 0.f && cq != px) r = fmaf(prev[k], fo, r);
+                    const int64_t row = (int64_t)s * H + h0 + hh;
+                    if (to_out)
+                        store_out<BF16>(p.out, row * D + i, r);
+                    else
+                        static_cast<float*>(p.tmp_out)[(row * p.Pmax + px) * D + i] = r;
+                }
+            }
+        }
+        for (int e = threadIdx.x; e < nh * D && !merge; e += blockDim.x) {
             const int hh = e / D, i = e - hh * D;
             float v = 0.f;
 #pragma unroll
@@ -818,18 +863,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
             const float lt = fin_l[hh];
             v = lt > 0.f ? v * (v_mul / lt) : 0.f;
             const int64_t row = (int64_t)s * H + h0 + hh;
-            if (merge) {
-                // row px so far (written by this thread for the CTA's previous partition) and
-                // this partition, each with its share of the merged exp-sum
-                float* mrow = static_cast<float*>(p.tmp_out) + (row * p.Pmax + px) * D;
-                const float fo = fac_o[hh];
-                float r = v * fac_n[hh];
-                if (fo != 0.f) r = fmaf(mrow[i], fo, r);
-                if (direct && cq + PX >= Pl)
-                    store_out<BF16>(p.out, row * D + i, r);
-                else
-                    mrow[i] = r;
-            } else if (direct)
+            if (direct)
                 store_out<BF16>(p.out, row * D + i, v);
             else if (p.tmp16)
                 store_out<BF16>(p.tmp_out, (row * p.Pmax + cq) * D + i, v);
@@ -869,11 +903,13 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     // Fused combine: count this CTA in; the last of the (sequence, head group) to arrive
     // merges the rows of all of them.  Nothing waits: every CTA but the last just exits.
     if (fused && Pl > 1 && !direct) {
-        __threadfence();  // this thread's rows and statistics are visible GPU-wide ...
-        __syncthreads();  // ... for every thread of the CTA, before the arrival
+        // the CTA's rows and statistics are written; one thread publishes them GPU-wide (the
+        // fence after the barrier covers the writes of every thread of the CTA) and arrives
+        __syncthreads();
         int* last = reinterpret_cast<int*>(red_m);
         if (threadIdx.x == 0) {
-            uint32_t* ctr = p.counters + (int64_t)s * gridDim.y + blockIdx.y;
+            __threadfence();
+            uint32_t* ctr = p.counters + ((int64_t)s * gridDim.y + kvh) * ng + grp;
             const uint32_t before = atomicAdd(ctr, 1u);
             const bool is_last = before == (uint32_t)(nwork - 1);
             if (is_last) atomicExch(ctr, 0u);  // left at zero for the next call

@@ -250,7 +250,8 @@ __device__ __forceinline__ void pfx_load_tiles(const PrefixParams& p, const PfxR
         return b;
     };
     int pid_next = tile_page(0);
-    for (int t = 0; t < n_tiles; ++t) {
+    int t = 0;
+    for (; t < n_tiles; ++t) {
         const int pid = pid_next;
         pid_next = tile_page(t + 1);
         const int slot = kteam ? t % NK : t % NV;
@@ -391,6 +392,14 @@ __device__ __forceinline__ void pfx_load_tiles(const PrefixParams& p, const PfxR
         if (lane == 0) mbar_arrive(full);
     }
     cp_async_wait<0>();
+    if (t < n_tiles && lt == 0) {
+        // Aborted: tensor copies this team issued for its last tiles may still be landing in
+        // shared memory.  Wait (bounded) until each slot's latest fill is complete, so that
+        // no copy outlives the CTA.
+        const int ns = kteam ? NK : NV;
+        for (int u = t > ns ? t - ns : 0; u < t; ++u)
+            (void)mbar_wait_bounded(kteam ? &k_full[u % ns] : &v_full[u % ns], (uint32_t)(u / ns) & 1u, kWaitLimitNs);
+    }
 }
 
 template <bool BF16, int D>

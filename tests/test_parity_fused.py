@@ -70,16 +70,14 @@ def test_full_size_workloads_sampled(name):
     assert pa.pa_get_device_errors() == 0
 
 
-@pytest.mark.parametrize("alibi", [False, True])
-@pytest.mark.parametrize("q_dtype", ["f16", "bf16"])
-def test_ctas_merging_several_partitions(alibi, q_dtype):
-    # 8 query heads of head size 256 per CTA: 8 KiB of fp32 row per CTA, so the partition
-    # stride is capped and every CTA folds two or three partitions into its row
-    wl = workloads.build(num_seqs=3, num_heads=16, num_kv_heads=2, head_size=256, block_size=16,
-                         seq_lens=[9000, 4097, 11264], q_dtype=q_dtype, alibi=alibi, seed=400 + alibi)
+@pytest.mark.parametrize("G", [1, 6, 9, 12, 16])
+def test_gqa_ratios(G):
+    # above 8 query heads per kv head several CTAs (head groups) share a kv head's pages and
+    # each has its own arrival counter
+    wl = workloads.build(num_seqs=3, num_heads=2 * G, num_kv_heads=2, head_size=128, block_size=16,
+                         seq_lens=[700, 33, 2600], seed=440 + G)
     ctr = _counters(wl)
-    gpu = run_decode(wl, counters=ctr)
-    check_decode(wl, gpu, oracle.decode_workload(wl), label=f"merge alibi={alibi}", check_tmp=False)
+    check_decode(wl, run_decode(wl, counters=ctr), oracle.decode_workload(wl), label=f"fused G{G}", check_tmp=False)
     assert torch.count_nonzero(ctr) == 0
 
 
@@ -167,22 +165,37 @@ import sys, torch
 sys.path.insert(0, {here!r}); sys.path.insert(0, {root!r})
 import oracle, workloads, paged_kv_cache_v2_gb300 as pa
 from gpu_harness import check_decode, run_decode
-for alibi in (False, True):
-    wl = workloads.build(num_seqs=4, num_heads=8, num_kv_heads=2, head_size=128, block_size=16,
-                         seq_lens=[3000, 1, 700, 2600], alibi=alibi, seed=430 + alibi)
-    ctr = pa.decode_counters(4, 8, 2, "cuda")
-    check_decode(wl, run_decode(wl, counters=ctr), oracle.decode_workload(wl), label="px", check_tmp=False)
+for spec in {specs!r}:
+    wl = workloads.build(**spec)
+    ctr = pa.decode_counters(wl.num_seqs, wl.num_heads, wl.num_kv_heads, "cuda")
+    ref = oracle.decode_workload(wl)
+    check_decode(wl, run_decode(wl, counters=ctr), ref, label=f"fused {{spec}}", check_tmp=False)
     assert int(torch.count_nonzero(ctr)) == 0
-    check_decode(wl, run_decode(wl), oracle.decode_workload(wl), label="px two kernels")
+    check_decode(wl, run_decode(wl), ref, label=f"two kernels {{spec}}")
 print("child ok")
 """
+
+
+def _run_child(px, specs):
+    """Run the decode checks of `specs` in a fresh process with the partition stride forced
+    to `px` (the library reads the override once per process)."""
+    env = dict(os.environ, PA_DECODE_PX=str(px))
+    code = _CHILD.format(here=HERE, root=os.path.dirname(HERE), specs=specs)
+    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0 and "child ok" in r.stdout, r.stdout[-2000:] + r.stderr[-4000:]
 
 
 @pytest.mark.parametrize("px", [1, 2, 5])
 def test_partition_strides(px):
     # PX = 1: one CTA covers each whole sequence (a single pass over all its partitions);
     # PX = 2, 5: CTAs fold several partitions, some CTAs have fewer than others or none
-    env = dict(os.environ, PA_DECODE_PX=str(px))
-    code = _CHILD.format(here=HERE, root=os.path.dirname(HERE))
-    r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
-    assert r.returncode == 0 and "child ok" in r.stdout, r.stdout[-2000:] + r.stderr[-4000:]
+    _run_child(px, [dict(num_seqs=4, num_heads=8, num_kv_heads=2, head_size=128, block_size=16,
+                         seq_lens=[3000, 1, 700, 2600], alibi=alibi, seed=430 + alibi) for alibi in (False, True)])
+
+
+def test_ctas_merging_several_partitions_head_size_256():
+    # 8 query heads of head size 256 per CTA, three to six partitions folded per CTA, both
+    # query dtypes, with and without ALiBi (the merge weights are relative to the last token)
+    _run_child(4, [dict(num_seqs=3, num_heads=16, num_kv_heads=2, head_size=256, block_size=16,
+                        seq_lens=[9000, 4097, 11264], q_dtype=q, alibi=alibi, seed=400 + alibi)
+                   for q in ("f16", "bf16") for alibi in (False, True)])

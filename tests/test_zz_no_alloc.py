@@ -1,7 +1,8 @@
 """GPU: pa_v2_decode_noalloc, the entry point for callers that cannot allocate device memory
 (a plugin handed only a stream and a fixed budget), gives the same output as pa_v2_decode
-with a caller-owned
-workspace, on two calls in a row (the second call reuses scratch the first one left behind).
+with a caller-owned fp32 workspace (bit for bit: the same kernels run) and matches the fp64
+oracle, on two calls in a row (the second call reuses scratch the first one left behind),
+including the full long-context step that fills 19.4 MB of the scratch.
 
 This file is named to be collected last, so a run that stops at its first failure has run
 every other test before it; it also passes on its own in a fresh process.
@@ -14,9 +15,10 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import paged_kv_cache_v2_gb300 as pa
 import workloads
-from gpu_harness import TOL_OUT, half_ulp, run_decode, to_device
+from gpu_harness import TOL_OUT, half_ulp, run_decode, sample_pairs, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -38,22 +40,40 @@ def _noalloc_raw(wl, dev, out, max_seq_len=None):
         wl.k_scale, wl.v_scale, P(torch.cuda.current_stream().cuda_stream))
 
 
-@pytest.mark.parametrize("name", ["llama_gqa_decode", "long_context_gqa", "fp8_kv", "mha_alibi_ragged"])
+@pytest.mark.parametrize("name", ["tiny", "llama_gqa_decode", "long_context_gqa", "fp8_kv", "mha_alibi_ragged"])
 def test_noalloc_matches_workspace_entry_point_twice(name):
     wl = workloads.make(name, reduced=True)
     dev = to_device(wl)
-    ref = run_decode(wl, dev)[0].double().numpy()
-    tol = TOL_OUT[wl.kv_cache_dtype]
-    allow = tol + half_ulp(ref, wl.q_dtype)
+    # same kernels and launch as pa_v2_decode with an fp32 workspace: bit-identical output
+    ref_gpu = run_decode(wl, dev, tmp_dtype=torch.float32)[0]
+    ref = oracle.decode_workload(wl)["out"].reshape(wl.query.shape)
+    allow = TOL_OUT[wl.kv_cache_dtype] + half_ulp(ref, wl.q_dtype)
     for call in range(2):
         out = torch.full(wl.query.shape, float("nan"), dtype=wl.query.dtype, device="cuda")
         st = _noalloc_raw(wl, dev, out)
         assert st == 0, f"call {call}: status {st} ({pa.STATUS.get(st)})"
         torch.cuda.synchronize()
+        assert torch.equal(out.cpu().view(torch.int16), ref_gpu.view(torch.int16)), f"call {call}: differs"
         got = out.cpu().double().numpy()
         assert np.isfinite(got).all(), f"call {call}: non-finite output"
         err = np.abs(got - ref)
-        assert (err <= allow).all(), f"call {call}: max error {err.max():.3g}"
+        assert (err <= allow).all(), f"call {call}: max error {err.max():.3g} against the oracle"
+
+
+@pytest.mark.slow
+def test_noalloc_full_long_context_against_the_oracle():
+    # 4 sequences x 24 heads x head size 256 at 100K tokens: 19.4 MB of the fixed scratch
+    wl = workloads.make("long_context_gqa")
+    dev = to_device(wl)
+    pairs = sample_pairs(wl, n=12)
+    ref = oracle.decode_workload(wl, pairs=pairs)["out"]
+    for call in range(2):
+        out = torch.full(wl.query.shape, float("nan"), dtype=wl.query.dtype, device="cuda")
+        assert _noalloc_raw(wl, dev, out) == 0
+        torch.cuda.synchronize()
+        got = out.cpu().double().numpy()[pairs[:, 0], pairs[:, 1]]
+        err = np.abs(got - ref)
+        assert (err <= TOL_OUT["auto"] + half_ulp(ref, wl.q_dtype)).all(), f"call {call}: {err.max():.3g}"
 
 
 def test_noalloc_rejects_a_step_larger_than_its_scratch():

@@ -109,8 +109,8 @@ class Workload:
 
 
 # --------------------------------------------------------------------------------------
-# Named workloads: the five decode configurations this library is measured on, and a
-# small batch.
+# Named workloads: the five decode configurations this library is measured on, a small
+# batch and a 16:1 GQA batch.
 # --------------------------------------------------------------------------------------
 CONFIGS = {
     "tiny": dict(
@@ -145,6 +145,12 @@ CONFIGS = {
         lens=("uniform", 4096, 8192), q_dtype="f16", kv_cache_dtype="auto",
         sigma=1.0, alibi=False, seed=1006,
     ),
+    # 16 query heads per kv head: more than one MMA tile of heads shares each kv head.
+    "gqa16_decode": dict(
+        num_seqs=64, num_heads=64, num_kv_heads=4, head_size=128, block_size=16,
+        lens=("uniform", 1, 4096), q_dtype="f16", kv_cache_dtype="auto",
+        sigma=1.0, alibi=False, seed=1007,
+    ),
 }
 
 # Reduced-size stand-ins the oracle finishes in seconds: same heads, head size, block
@@ -157,6 +163,7 @@ REDUCED = {
     "fp8_kv": dict(num_seqs=6, lens=("uniform", 512, 1800)),
     "mha_alibi_ragged": dict(num_seqs=8, lens=("lognormal", 300.0, 1.0, 2000, {0: 0, 1: 1})),
     "small_batch_gqa": dict(lens=("uniform", 1200, 2600)),
+    "gqa16_decode": dict(num_seqs=4, lens=("uniform", 1, 1600)),
 }
 
 
