@@ -524,18 +524,11 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
         (void)cudaGetLastError();
         return PA_ERR_CUDA;
     }
-    // Ring depth: about kRingTarget bytes of pages per CTA, at least one slot per warp.  A
-    // grid of fewer CTAs than two per SM (a small batch: few sequences x kv heads x
-    // partitions) gets a deeper ring, since its few CTAs must each keep more bytes in flight
-    // to cover the memory latency.
-    uint32_t target = kRingTarget;
-    const int64_t max_ctas = (int64_t)a.num_seqs * a.num_kv_heads * ngroups * a.max_num_partitions;
-    if (ring_override_kib() > 0)
-        target = (uint32_t)ring_override_kib() * 1024u;
-    else if (max_ctas <= nsm)
-        target = 192u * 1024u;
-    else if (max_ctas <= 2 * (int64_t)nsm)
-        target = 96u * 1024u;
+    // Ring depth: about kRingTarget bytes of pages per CTA, at least one slot per warp.  (A
+    // deeper ring for small grids measured slower: 96 / 128 / 192 KiB gave 22.4 / 26.9 /
+    // 27.3 us against 22.0 us on a two-sequence batch, as fewer CTAs then fit an SM.)
+    const uint32_t target = ring_override_kib() > 0 ? (uint32_t)ring_override_kib() * 1024u : kRingTarget;
+    (void)nsm;
     int nstage = (int)(target / (kWarps * slot_bytes));
     nstage = nstage < 1 ? 1 : (nstage > 8 ? 8 : nstage);
     if (nstage < PA_MIN_STAGES && (uint32_t)PA_MIN_STAGES * kWarps * slot_bytes <= 160u * 1024u) nstage = PA_MIN_STAGES;
@@ -547,7 +540,7 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
     };
     while (nstage > 1 && smem_for(nstage) > (size_t)optin) --nstage;  // a deep ring that does not fit
     const uint32_t ring = (uint32_t)kWarps * nstage * slot_bytes;
-    const size_t smem1 = smem_for(nstage);
+    size_t smem1 = smem_for(nstage);
 
     Phase1Fn fn = phase1_for(bf16, fp8, D, bs);
     if (fn == nullptr) return PA_ERR_UNSUPPORTED;
@@ -597,25 +590,30 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
     // instead gets exactly one wave: PX = slots / rows, each CTA streaming its partitions
     // back to back (measured on 4 x 100K tokens: 251 us against 264 us for one partition per
     // CTA and 317 us for 1.3 waves).
-    int sms = 0, per_sm = 0;
-    if (occupancy((const void*)fn, kWarps * 32, smem1, &sms, &per_sm) != cudaSuccess) {
+    const int64_t Pmax = a.max_num_partitions;
+    const int64_t rows = (int64_t)a.num_kv_heads * ngroups * a.num_seqs;
+    int64_t slots = 0, PX = 1;
+    // CTA slots of the GPU at this shared-memory size, and the partition stride for them
+    auto plan = [&](size_t smem) -> bool {
+        int sms = 0, per_sm = 0;
+        if (occupancy((const void*)fn, kWarps * 32, smem, &sms, &per_sm) != cudaSuccess) return false;
+        slots = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
+        if (rows < slots && rows * Pmax > slots) {
+            PX = slots / rows;
+        } else {
+            PX = (int64_t)PA_GRID_WAVES * slots / rows;
+            const int64_t px_min = (Pmax + 7) / 8;
+            if (PX < px_min) PX = px_min;
+        }
+        if (px_override() > 0) PX = px_override();
+        if (PX > Pmax) PX = Pmax;
+        if (PX < 1) PX = 1;
+        return true;
+    };
+    if (!plan(smem1)) {
         (void)cudaGetLastError();
         return PA_ERR_CUDA;
     }
-    const int64_t Pmax = a.max_num_partitions;
-    const int64_t rows = (int64_t)a.num_kv_heads * ngroups * a.num_seqs;
-    const int64_t slots = (int64_t)sms * (per_sm > 0 ? per_sm : 1);
-    int64_t PX;
-    if (rows < slots && rows * Pmax > slots) {
-        PX = slots / rows;
-    } else {
-        PX = (int64_t)PA_GRID_WAVES * slots / rows;
-        const int64_t px_min = (Pmax + 7) / 8;
-        if (PX < px_min) PX = px_min;
-    }
-    if (px_override() > 0) PX = px_override();
-    if (PX > Pmax) PX = Pmax;
-    if (PX < 1) PX = 1;
 
     // Fused combine (V1/V2 dispatch, "paged_attn.py" forward_decode, re-decided for this GPU):
     // with arrival counters the last CTA of each (sequence, head group) merges the partitions,
@@ -627,12 +625,22 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
     // one keeps a row per partition.  Either way the rows the last CTA merges are bounded by
     // kFusedRowBytes.
     bool fused = counters != nullptr && Pmax > 1 && rows * PX <= 2 * slots;
+    const bool merge = fused && a.tmp_dtype == PA_DT_F32;
+    if (merge && PX < Pmax) {
+        // CTAs that stream several partitions keep their running row in shared memory
+        const size_t with_row = smem1 + (size_t)red_heads * D * sizeof(float);
+        if (with_row > (size_t)optin || ensure_smem((const void*)fn, with_row) != cudaSuccess || !plan(with_row)) {
+            (void)cudaGetLastError();
+            return PA_ERR_CUDA;
+        }
+        smem1 = with_row;
+        fused = rows * PX <= 2 * slots;
+    }
     if (fused) {
-        const bool merge = a.tmp_dtype == PA_DT_F32;
         const int64_t R = merge ? PX : Pmax;
         const int64_t row_bytes = (int64_t)red_heads * D * (merge ? 4 : 2);
-        // the row weights live in the idle page ring during the combine
-        if ((kMaxHeadsPerCta + (int64_t)red_heads * R) * (int64_t)sizeof(float) > (int64_t)ring ||
+        // the row weights and partition statistics live in the idle page ring during the combine
+        if ((kMaxHeadsPerCta + (int64_t)red_heads * (R + 2 * Pmax)) * (int64_t)sizeof(float) > (int64_t)ring ||
             R * row_bytes > kFusedRowBytes)
             fused = false;
         if (fused) {

@@ -48,27 +48,38 @@ __device__ __forceinline__ void merge_factors(float& A, float& Lc, float a, floa
 // exp(m_p - g) l_p from the partition statistics, and the weighted mean of the rows.  Row r
 // of tmp_output holds the normalised merge of partitions r, r + rstride, ... (one partition
 // per row when rstride >= Pl), so its weight is the sum of theirs.  Reads go to L2 (ld.cg):
-// the rows were written by other CTAs.  `wsm` is shared memory for 8 + nh * rows floats.
+// the rows were written by other CTAs.  Two memory round trips: every partition's statistics
+// together, then the rows (sixteen in flight per thread).  `wsm` is shared memory for
+// 8 + nh * (rows + 2 * Pl) floats.
 template <bool BF16, int D>
 __device__ __forceinline__ void fused_combine(const Phase1Params& p, int s, int h0, int nh, int Pl, int rstride,
-                                           float* wsm) {
+                                              float* wsm) {
     const int R = min(rstride, Pl);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     float* tot = wsm;
-    float* wts = wsm + kMaxHeadsPerCta;
+    float* wts = tot + kMaxHeadsPerCta;  // [nh][R] row weights
+    float* pa2 = wts + nh * R;           // [nh][Pl] partition max, log2 units (-inf: empty)
+    float* pl = pa2 + nh * Pl;           // [nh][Pl] partition exp-sum
     for (int hh = warp; hh < nh; hh += kWarps) {
         const int64_t srow = ((int64_t)s * p.H + h0 + hh) * p.Pmax;
         float gm = -INFINITY;
-        for (int q = lane; q < Pl; q += 32)
-            if (__ldcg(p.exp_sums + srow + q) > 0.f) gm = fmaxf(gm, __ldcg(p.max_logits + srow + q) * kLog2e);
+#pragma unroll 4
+        for (int q = lane; q < Pl; q += 32) {
+            const float l = __ldcg(p.exp_sums + srow + q), m = __ldcg(p.max_logits + srow + q);
+            const float a = l > 0.f ? m * kLog2e : -INFINITY;
+            pa2[hh * Pl + q] = a;
+            pl[hh * Pl + q] = l;
+            gm = fmaxf(gm, a);
+        }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, o));
+        __syncwarp();
         float sum = 0.f;
         for (int r = lane; r < R; r += 32) {
             float w = 0.f;
             for (int q = r; q < Pl; q += rstride) {
-                const float l = __ldcg(p.exp_sums + srow + q);
-                if (l > 0.f) w += l * ex2(__ldcg(p.max_logits + srow + q) * kLog2e - gm);
+                const float a = pa2[hh * Pl + q];
+                if (a != -INFINITY) w += pl[hh * Pl + q] * ex2(a - gm);
             }
             wts[hh * R + r] = w;
             sum += w;
@@ -84,7 +95,7 @@ __device__ __forceinline__ void fused_combine(const Phase1Params& p, int s, int 
         const int64_t row = (int64_t)s * p.H + h0 + hh;
         const float* w = wts + hh * R;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
+#pragma unroll 16
         for (int r = 0; r < R; ++r) {
             const int64_t i4 = (row * p.Pmax + r) * D4 + c;
             float4 x;
@@ -234,6 +245,8 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     float* fac_n = fac_o + kMaxHeadsPerCta;           // [8] CTA merge: factor on this partition
     float* red_o = fac_n + kMaxHeadsPerCta;           // [kWarps][nh][D + 4] scaled accumulators
     constexpr int RS = D + 4;
+    // CTA merge over several partitions: the running row [nh][D] (only when PX < Pmax)
+    float* mrg = red_o + kWarps * nh * RS;
 
     if (lane == 0) {
         for (int k = 0; k < nstage; ++k) mbar_init(&bars[k], 1);
@@ -305,7 +318,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     // element lands near 224) and split into three e4m3 terms hi + mid + lo (at least 12
     // significant bits, so every bf16 value is exact); the scale is undone on the scores.
     constexpr int NS = (D + 31) / 32;  // k32 steps over the head dimension (fp8)
-    constexpr bool Q8 = FP8 && BF16;   // scores on the e4m3 tensor path
+    constexpr bool Q8 = FP8;            // scores on the e4m3 tensor path
     uint32_t qf[Q8 ? 1 : NK][2];
     uint32_t qh[Q8 ? NS : 1][2], qm[Q8 ? NS : 1][2], ql[Q8 ? NS : 1][2];
     float qs0 = 1.f, qs1 = 1.f;  // per-column score factor from the fp8 query scale
@@ -759,20 +772,6 @@ pa_v2_phase1_kernel(const Phase1Params p) {
             issue_more();
         }
 
-        // CTA merge: the row built from this CTA's earlier partitions, loaded now so that the
-        // loads overlap the cross-warp merge below (thread t owns elements t, t + 128, ...)
-        constexpr int NE = (kMaxHeadsPerCta * D + kWarps * 32 - 1) / (kWarps * 32);
-        float prev[NE];
-        if (merge && cq != px) {
-            const float* mrow0 = static_cast<const float*>(p.tmp_out) + ((int64_t)s * H + h0) * p.Pmax * D + (int64_t)px * D;
-#pragma unroll
-            for (int k = 0; k < NE; ++k) {
-                const int e = threadIdx.x + k * kWarps * 32;
-                const int hh = e / D;
-                prev[k] = e < nh * D ? mrow0[(int64_t)hh * p.Pmax * D + (e - hh * D)] : 0.f;
-            }
-        }
-
         // ---- merge the warps' (m, l, acc) of this partition --------------------------------
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) {
@@ -832,27 +831,26 @@ pa_v2_phase1_kernel(const Phase1Params p) {
         __syncthreads();
 
         if (merge) {
-            // row px so far and this partition, each with its share of the merged exp-sum
-            const bool to_out = direct && cq + PX >= Pl;
+            // the CTA's row so far (in shared memory) and this partition, each with its share
+            // of the merged exp-sum; the last partition writes the row out (or the output)
+            const bool first = cq == px, last_part = cq + PX >= Pl;
+            for (int e = threadIdx.x; e < nh * D; e += blockDim.x) {
+                const int hh = e / D, i = e - hh * D;
+                float v = 0.f;
 #pragma unroll
-            for (int k = 0; k < NE; ++k) {
-                const int e = threadIdx.x + k * kWarps * 32;
-                if (e < nh * D) {
-                    const int hh = e / D, i = e - hh * D;
-                    float v = 0.f;
-#pragma unroll
-                    for (int w = 0; w < kWarps; ++w) v += red_o[(w * nh + hh) * RS + i];
-                    const float lt = fin_l[hh];
-                    v = lt > 0.f ? v * (v_mul / lt) : 0.f;
-                    const float fo = fac_o[hh];
-                    float r = v * fac_n[hh];
-                    if (fo != 0.f && cq != px) r = fmaf(prev[k], fo, r);
-                    const int64_t row = (int64_t)s * H + h0 + hh;
-                    if (to_out)
-                        store_out<BF16>(p.out, row * D + i, r);
-                    else
-                        static_cast<float*>(p.tmp_out)[(row * p.Pmax + px) * D + i] = r;
-                }
+                for (int w = 0; w < kWarps; ++w) v += red_o[(w * nh + hh) * RS + i];
+                const float lt = fin_l[hh];
+                v = lt > 0.f ? v * (v_mul / lt) : 0.f;
+                const float fo = fac_o[hh];
+                float r = v * fac_n[hh];
+                if (fo != 0.f && !first) r = fmaf(mrg[e], fo, r);
+                const int64_t row = (int64_t)s * H + h0 + hh;
+                if (!last_part)
+                    mrg[e] = r;
+                else if (direct)
+                    store_out<BF16>(p.out, row * D + i, r);
+                else
+                    static_cast<float*>(p.tmp_out)[(row * p.Pmax + px) * D + i] = r;
             }
         }
         for (int e = threadIdx.x; e < nh * D && !merge; e += blockDim.x) {
