@@ -473,8 +473,9 @@ int64_t pa::decode_num_counters(int num_seqs, int num_heads, int num_kv_heads) {
     return (int64_t)num_seqs * num_kv_heads * ((G + kMaxHeadsPerCta - 1) / kMaxHeadsPerCta);
 }
 
-// Overrides for tuning runs, read once: the partition stride (PA_DECODE_PX=n) and the page
-// ring per CTA in KiB (PA_DECODE_RING_KIB=n); 0 or unset: the heuristics.
+// Overrides for tuning runs and tests, read once: the partition stride (PA_DECODE_PX=n), the
+// page ring per CTA in KiB (PA_DECODE_RING_KIB=n) and the CTAs per partition
+// (PA_DECODE_SPLIT=k); 0 or unset: the heuristics.
 static int env_int(const char* name) {
     const char* e = getenv(name);
     return e ? atoi(e) : 0;
@@ -485,6 +486,14 @@ static int px_override() {
 }
 static int ring_override_kib() {
     static const int v = env_int("PA_DECODE_RING_KIB");
+    return v;
+}
+// CTAs per partition (PA_DECODE_SPLIT = 1, 2 or 4), when the grid has one partition per CTA
+static int split_override() {
+    static const int v = [] {
+        const int k = env_int("PA_DECODE_SPLIT");
+        return (k == 1 || k == 2 || k == 4) ? k : 0;
+    }();
     return v;
 }
 
@@ -576,6 +585,7 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
     p1.tmp16 = a.tmp_dtype != PA_DT_F32;
     p1.counters = nullptr;
     p1.merge = 0;
+    p1.csplit = 1;
 
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -625,7 +635,7 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
     // one keeps a row per partition.  Either way the rows the last CTA merges are bounded by
     // kFusedRowBytes.
     bool fused = counters != nullptr && Pmax > 1 && rows * PX <= 2 * slots;
-    const bool merge = fused && a.tmp_dtype == PA_DT_F32;
+    const bool merge = fused && a.tmp_dtype == PA_DT_F32 && PX < Pmax;
     if (merge && PX < Pmax) {
         // CTAs that stream several partitions keep their running row in shared memory
         const size_t with_row = smem1 + (size_t)red_heads * D * sizeof(float);
@@ -638,7 +648,7 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
     }
     if (fused) {
         const int64_t R = merge ? PX : Pmax;
-        const int64_t row_bytes = (int64_t)red_heads * D * (merge ? 4 : 2);
+        const int64_t row_bytes = (int64_t)red_heads * D * (a.tmp_dtype == PA_DT_F32 ? 4 : 2);
         // the row weights and partition statistics live in the idle page ring during the combine
         if ((kMaxHeadsPerCta + (int64_t)red_heads * (R + 2 * Pmax)) * (int64_t)sizeof(float) > (int64_t)ring ||
             R * row_bytes > kFusedRowBytes)
@@ -649,13 +659,36 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
         }
     }
 
+    // Cluster split for a grid of less than about a wave of one-partition CTAs (a small
+    // batch): K CTAs share each partition, so the SMs run more warps.  The partners' partials
+    // travel to the cluster's first CTA, into its idle page ring.
+    int K = 1;
+    if (PX == Pmax && !p1.merge) {
+        const int64_t ctas = rows * Pmax;
+        if (split_override() > 0)
+            K = split_override();
+        else if (ctas * 4 * 4 <= slots * 5)
+            K = 4;
+        else if (ctas * 2 * 4 <= slots * 5)
+            K = 2;
+        while (K > 1 && (int64_t)(K - 1) * (2 * kMaxHeadsPerCta + red_heads * D) * (int64_t)sizeof(float) > (int64_t)ring)
+            K /= 2;
+    }
+    p1.csplit = K;
+    cudaLaunchAttribute attrs1[2];
+    attrs1[0] = attr[0];
+    attrs1[1].id = cudaLaunchAttributeClusterDimension;
+    attrs1[1].val.clusterDim.x = (unsigned)K;
+    attrs1[1].val.clusterDim.y = 1;
+    attrs1[1].val.clusterDim.z = 1;
+
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(PX * ngroups), (unsigned)a.num_kv_heads, (unsigned)a.num_seqs);
+    cfg.gridDim = dim3((unsigned)(PX * ngroups * K), (unsigned)a.num_kv_heads, (unsigned)a.num_seqs);
     cfg.blockDim = dim3(kWarps * 32, 1, 1);
     cfg.dynamicSmemBytes = smem1;
     cfg.stream = a.stream;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.attrs = attrs1;
+    cfg.numAttrs = K > 1 ? 2 : 1;
     if (g_t_begin != nullptr) cudaEventRecord(g_t_begin, a.stream);
     cudaError_t e = cudaLaunchKernelEx(&cfg, fn, p1);
     if (g_t_end != nullptr) cudaEventRecord(g_t_end, a.stream);

@@ -59,6 +59,10 @@ struct Phase1Params {
     // row px of tmp_output (instead of one row per partition), so the last CTA merges at
     // most PX rows.
     int merge;
+    // CTAs per partition (1, 2 or 4; more than 1 only with one partition per CTA): a cluster
+    // of csplit CTAs shares each partition's pages, and the others hand their partial
+    // (max, exp-sum, rows) to the cluster's first CTA through distributed shared memory.
+    int csplit;
 };
 
 struct Phase2Params {

@@ -149,15 +149,22 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     // blockIdx.x = px * ngroups + grp: the head groups of one kv head (more than 8 query
     // heads per kv head) are neighbours in the grid, so they start together and stream the
     // same pages at about the same time -- the later ones find them in L2.
-    const int ng = p.ngroups;
-    const int px = ng == 1 ? (int)blockIdx.x : (int)blockIdx.x / ng;
-    const int PX = ng == 1 ? (int)gridDim.x : (int)gridDim.x / ng;
-    const int grp = (int)blockIdx.x - px * ng;
+    // With csplit > 1, blockIdx.x = (px * ngroups + grp) * csplit + kc and the csplit CTAs of
+    // one partition form a cluster (kc = rank in it).
+    const int ng = p.ngroups, K = p.csplit;
+    const int kc = K == 1 ? 0 : (int)(blockIdx.x % (unsigned)K);
+    const int bx = K == 1 ? (int)blockIdx.x : (int)(blockIdx.x / (unsigned)K);
+    const int gx = K == 1 ? (int)gridDim.x : (int)(gridDim.x / (unsigned)K);
+    const int px = ng == 1 ? bx : bx / ng;
+    const int PX = ng == 1 ? gx : gx / ng;
+    const int grp = bx - px * ng;
     const int kvh = blockIdx.y;
     const int s = blockIdx.z;
     const int h0 = kvh * p.G + grp * kMaxHeadsPerCta;
     const int nh = min(kMaxHeadsPerCta, p.G - grp * kMaxHeadsPerCta);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    // the partition's slots are dealt to the cluster's K * kWarps warps: this warp is gw
+    const int gw = kc * kWarps + warp, KW = K * kWarps;
     const int g = lane >> 2, t = lane & 3;
     const int H = p.H;
     constexpr int bs = BS;
@@ -183,6 +190,9 @@ pa_v2_phase1_kernel(const Phase1Params p) {
             if (ppart > 32 && lb + 32 + lane < p.mbps) r1 = trow[lb + 32 + lane];
         }
     };
+    // A cluster's CTAs write into the first one's shared memory at the end of a partition;
+    // this arrival (waited for before that) guarantees every CTA of the cluster has started.
+    if (K > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     // Every input is read only after the wait on the previous kernel in the stream: that
     // kernel may have written the tables, the lengths or the query (a serving loop prepares
     // them on the device each step), and only the wait makes its writes visible.  The ids of
@@ -194,17 +204,17 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     const int L = p.seq_lens[s];
 
     const int P = L > 0 ? (L + kPartition - 1) / kPartition : 0;
-    if (threadIdx.x == 0 && px == 0 && (L < 0 || P > p.Pmax)) flag_error(2u);
+    if (threadIdx.x == 0 && px == 0 && kc == 0 && (L < 0 || P > p.Pmax)) flag_error(2u);
     const int Pl = min(P, p.Pmax);  // partitions with tokens that the grid covers
     // This CTA's partitions past the end: max_logits = -inf, exp_sums = 0.
-    for (int q = px; q < p.Pmax; q += PX) {
+    for (int q = px; q < p.Pmax && kc == 0; q += PX) {
         if (q >= Pl && threadIdx.x < nh) {
             const int64_t sidx = ((int64_t)s * H + h0 + threadIdx.x) * p.Pmax + q;
             p.max_logits[sidx] = -INFINITY;
             p.exp_sums[sidx] = 0.f;
         }
     }
-    if (px == 0 && L <= 0) {
+    if (px == 0 && L <= 0 && kc == 0) {
         for (int i = threadIdx.x; i < nh * D; i += blockDim.x)
             store_out<BF16>(p.out, ((int64_t)s * H + h0) * D + i, 0.f);
     }
@@ -216,7 +226,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     auto npages_of = [&](int q) { return ((min(L, (q + 1) * kPartition) - 1) >> bs_log2) - q * ppart + 1; };
     auto my_slots_of = [&](int np) {
         const int ns = (np + pps - 1) >> pps_log2;
-        return ns > warp ? (ns - warp + kWarps - 1) / kWarps : 0;
+        return ns > gw ? (ns - gw + KW - 1) / KW : 0;
     };
     // Check the raw table entries of partition q once: entries of pages that do not exist or
     // lie outside [0, num_blocks) become -1 (the latter flagged), and bit i of the returned
@@ -287,7 +297,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
             }
             const bool cur = iq == cq;
             const int r0 = cur ? c0 : n0, r1 = cur ? c1 : n1;
-            const int j = warp + ii * kWarps;
+            const int j = gw + ii * KW;
             const uint32_t ok = (uint32_t)((cur ? cmask : nmask) >> (j * pps)) & ((1u << pps) - 1u);
             int b[4];
 #pragma unroll
@@ -318,7 +328,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     // element lands near 224) and split into three e4m3 terms hi + mid + lo (at least 12
     // significant bits, so every bf16 value is exact); the scale is undone on the scores.
     constexpr int NS = (D + 31) / 32;  // k32 steps over the head dimension (fp8)
-    constexpr bool Q8 = FP8;            // scores on the e4m3 tensor path
+    constexpr bool Q8 = FP8 && BF16;   // scores on the e4m3 tensor path
     uint32_t qf[Q8 ? 1 : NK][2];
     uint32_t qh[Q8 ? NS : 1][2], qm[Q8 ? NS : 1][2], ql[Q8 ? NS : 1][2];
     float qs0 = 1.f, qs1 = 1.f;  // per-column score factor from the fp8 query scale
@@ -464,7 +474,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
                 drain_from = ncons;
                 break;
             }
-            const int j = warp + k * kWarps;
+            const int j = gw + k * KW;
             const uint8_t* kslot = ring + (size_t)pos * slot_bytes;
             const uint8_t* vslot = kslot + (size_t)pps * page_bytes;
             const uint32_t kbase = smem_addr(kslot), vbase = smem_addr(vslot);
@@ -830,6 +840,57 @@ pa_v2_phase1_kernel(const Phase1Params p) {
         }
         __syncthreads();
 
+        // Cluster split: each CTA but the first hands its partial (max, exp-sum and normalised
+        // rows) to the first one, whose page ring is idle now (one partition per CTA); the
+        // first CTA merges them into the partition's result and alone writes it.
+        bool skip_out = false;
+        float* pbuf = reinterpret_cast<float*>(smem);
+        const int pstride = 2 * kMaxHeadsPerCta + nh * D;
+        if (K > 1) {
+            asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // every CTA has started
+            if (kc != 0) {
+                const uint32_t dst = mapa_cluster(smem_addr(pbuf + (kc - 1) * pstride), 0);
+                if (threadIdx.x < nh) {
+                    st_cluster_f32(dst + 4u * threadIdx.x, fin_m[threadIdx.x]);
+                    st_cluster_f32(dst + 4u * (kMaxHeadsPerCta + threadIdx.x), fin_l[threadIdx.x]);
+                }
+                for (int e = threadIdx.x; e < nh * D; e += blockDim.x) {
+                    const int hh = e / D, i = e - hh * D;
+                    float v = 0.f;
+#pragma unroll
+                    for (int w = 0; w < kWarps; ++w) v += red_o[(w * nh + hh) * RS + i];
+                    const float lt = fin_l[hh];
+                    st_cluster_f32(dst + 4u * (2 * kMaxHeadsPerCta + e), lt > 0.f ? v * (v_mul / lt) : 0.f);
+                }
+            }
+            cluster_sync_all();
+            skip_out = kc != 0;
+            if (!skip_out) {
+                if (threadIdx.x < nh) {
+                    // merged max and exp-sum; factor on this CTA's unnormalised sums (fac_o)
+                    // and on each partner's normalised rows (over the partner's max slot)
+                    const int hh = threadIdx.x;
+                    const float ml = fin_m[hh], ll = fin_l[hh];
+                    float M = ll > 0.f ? ml : -INFINITY;
+                    for (int k = 0; k < K - 1; ++k)
+                        if (pbuf[k * pstride + kMaxHeadsPerCta + hh] > 0.f) M = fmaxf(M, pbuf[k * pstride + hh]);
+                    float Ls = ll > 0.f ? ll * ex2(ml - M) : 0.f;
+                    for (int k = 0; k < K - 1; ++k) {
+                        const float lk = pbuf[k * pstride + kMaxHeadsPerCta + hh];
+                        if (lk > 0.f) Ls += lk * ex2(pbuf[k * pstride + hh] - M);
+                    }
+                    fac_o[hh] = (ll > 0.f && Ls > 0.f) ? ex2(ml - M) / Ls : 0.f;
+                    for (int k = 0; k < K - 1; ++k) {
+                        const float lk = pbuf[k * pstride + kMaxHeadsPerCta + hh];
+                        pbuf[k * pstride + hh] = (lk > 0.f && Ls > 0.f) ? lk * ex2(pbuf[k * pstride + hh] - M) / Ls : 0.f;
+                    }
+                    fin_m[hh] = M;
+                    fin_l[hh] = Ls;
+                }
+                __syncthreads();
+            }
+        }
+
         if (merge) {
             // the CTA's row so far (in shared memory) and this partition, each with its share
             // of the merged exp-sum; the last partition writes the row out (or the output)
@@ -853,13 +914,18 @@ pa_v2_phase1_kernel(const Phase1Params p) {
                     static_cast<float*>(p.tmp_out)[(row * p.Pmax + px) * D + i] = r;
             }
         }
-        for (int e = threadIdx.x; e < nh * D && !merge; e += blockDim.x) {
+        for (int e = threadIdx.x; e < nh * D && !merge && !skip_out; e += blockDim.x) {
             const int hh = e / D, i = e - hh * D;
             float v = 0.f;
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) v += red_o[(w * nh + hh) * RS + i];
-            const float lt = fin_l[hh];
-            v = lt > 0.f ? v * (v_mul / lt) : 0.f;
+            if (K > 1) {
+                v *= v_mul * fac_o[hh];
+                for (int k = 0; k < K - 1; ++k) v = fmaf(pbuf[k * pstride + 2 * kMaxHeadsPerCta + e], pbuf[k * pstride + hh], v);
+            } else {
+                const float lt = fin_l[hh];
+                v = lt > 0.f ? v * (v_mul / lt) : 0.f;
+            }
             const int64_t row = (int64_t)s * H + h0 + hh;
             if (direct)
                 store_out<BF16>(p.out, row * D + i, v);
@@ -868,7 +934,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
             else
                 static_cast<float*>(p.tmp_out)[(row * p.Pmax + cq) * D + i] = v;
         }
-        if (threadIdx.x < nh) {
+        if (threadIdx.x < nh && !skip_out) {
             const int hh = threadIdx.x;
             const int64_t sidx = ((int64_t)s * H + h0 + hh) * p.Pmax + cq;
             const float lt = fin_l[hh];
@@ -900,7 +966,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
 
     // Fused combine: count this CTA in; the last of the (sequence, head group) to arrive
     // merges the rows of all of them.  Nothing waits: every CTA but the last just exits.
-    if (fused && Pl > 1 && !direct) {
+    if (fused && Pl > 1 && !direct && kc == 0) {
         // the CTA's rows and statistics are written; one thread publishes them GPU-wide (the
         // fence after the barrier covers the writes of every thread of the CTA) and arrives
         __syncthreads();

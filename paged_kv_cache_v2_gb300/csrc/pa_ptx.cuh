@@ -103,6 +103,22 @@ __device__ __forceinline__ uint64_t l2_policy_evict_normal() {
     return p;
 }
 
+// ---- thread-block clusters (distributed shared memory) ----------------------------------
+// The shared::cluster address of the same variable in the cluster's CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_cluster(uint32_t smem_addr_local, uint32_t rank) {
+    uint32_t d;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(smem_addr_local), "r"(rank));
+    return d;
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+// Every thread of every CTA of the cluster: the writes before it are visible to the reads
+// after it in all of them.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // ---- ldmatrix / movmatrix -------------------------------------------------------------
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                         uint32_t& r3) {

@@ -176,10 +176,15 @@ print("child ok")
 """
 
 
-def _run_child(px, specs):
+def _run_child(px, specs, split=None):
     """Run the decode checks of `specs` in a fresh process with the partition stride forced
-    to `px` (the library reads the override once per process)."""
-    env = dict(os.environ, PA_DECODE_PX=str(px))
+    to `px` (or, with `split`, the CTAs per partition forced to `split`); the library reads
+    the overrides once per process."""
+    env = dict(os.environ)
+    if px:
+        env["PA_DECODE_PX"] = str(px)
+    if split:
+        env["PA_DECODE_SPLIT"] = str(split)
     code = _CHILD.format(here=HERE, root=os.path.dirname(HERE), specs=specs)
     r = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0 and "child ok" in r.stdout, r.stdout[-2000:] + r.stderr[-4000:]
@@ -199,3 +204,24 @@ def test_ctas_merging_several_partitions_head_size_256():
     _run_child(4, [dict(num_seqs=3, num_heads=16, num_kv_heads=2, head_size=256, block_size=16,
                         seq_lens=[9000, 4097, 11264], q_dtype=q, alibi=alibi, seed=400 + alibi)
                    for q in ("f16", "bf16") for alibi in (False, True)])
+
+
+_SPLIT_SPECS = [
+    dict(num_seqs=13, num_heads=8, num_kv_heads=2, head_size=128, block_size=16,
+         seq_lens=[0, 1, 2, 15, 16, 17, 511, 512, 513, 1024, 1025, 1536, 2047], seed=450),
+    dict(num_seqs=3, num_heads=8, num_kv_heads=8, head_size=96, block_size=32, seq_lens=[8000, 700, 1],
+         q_dtype="bf16", alibi=True, seed=451),
+    dict(num_seqs=4, num_heads=12, num_kv_heads=3, head_size=128, block_size=8, seq_lens=[1030, 64, 2500, 517],
+         kv_cache_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.07, seed=452),
+    dict(num_seqs=3, num_heads=32, num_kv_heads=2, head_size=64, block_size=16, seq_lens=[700, 33, 1500], seed=453),
+    dict(num_seqs=2, num_heads=24, num_kv_heads=4, head_size=256, block_size=16, seq_lens=[3000, 2561],
+         sigma=0.5, seed=454),
+]
+
+
+@pytest.mark.parametrize("split", [2, 4])
+def test_cluster_split_partitions(split):
+    # 2 or 4 CTAs of a cluster share each partition's pages; the partners' partials merge in
+    # the first CTA through distributed shared memory (edge lengths, ALiBi over 8K tokens,
+    # fp8 caches with block size 8, 16 query heads per kv head, head size 256)
+    _run_child(None, _SPLIT_SPECS, split=split)
