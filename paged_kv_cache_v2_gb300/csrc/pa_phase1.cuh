@@ -190,9 +190,6 @@ pa_v2_phase1_kernel(const Phase1Params p) {
             if (ppart > 32 && lb + 32 + lane < p.mbps) r1 = trow[lb + 32 + lane];
         }
     };
-    // A cluster's CTAs write into the first one's shared memory at the end of a partition;
-    // this arrival (waited for before that) guarantees every CTA of the cluster has started.
-    if (K > 1) asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     // Every input is read only after the wait on the previous kernel in the stream: that
     // kernel may have written the tables, the lengths or the query (a serving loop prepares
     // them on the device each step), and only the wait makes its writes visible.  The ids of
@@ -847,7 +844,9 @@ pa_v2_phase1_kernel(const Phase1Params p) {
         float* pbuf = reinterpret_cast<float*>(smem);
         const int pstride = 2 * kMaxHeadsPerCta + nh * D;
         if (K > 1) {
-            asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // every CTA has started
+            // every CTA of the cluster is past its page loop: the first CTA's ring is idle
+            // (all its copies have landed and been read) before any partner writes into it
+            cluster_sync_all();
             if (kc != 0) {
                 const uint32_t dst = mapa_cluster(smem_addr(pbuf + (kc - 1) * pstride), 0);
                 if (threadIdx.x < nh) {
