@@ -1,10 +1,9 @@
 """Benchmark: one decode step of paged attention on GB300 through the pa_v2 C ABI.
 
 A step is the whole hot path for one batch: the cache writer stores every sequence's newest
-token (pa_reshape_and_cache), then pa_v2_decode_fused runs phase 1 (with the single-pass path
-for one-partition sequences) and the partition combine, done by the last CTA of each
-(sequence, head group) inside phase 1 (--decode two-kernel: pa_v2_decode, phase 1 and the
-phase-2 kernel).  The default workload is the largest decode batch,
+token (pa_reshape_and_cache), then pa_v2_decode runs phase 1 (with the single-pass path for
+one-partition sequences) and the phase-2 combine (--decode fused: pa_v2_decode_fused, the
+combine by the last CTA of each (sequence, head group) inside phase 1).  The default workload is the largest decode batch,
 MHA with ALiBi over a ragged batch (256 sequences, 16 heads, head size 96, block size 32,
 lognormal lengths with median 1024 capped at 32768, bf16 query and cache: about 2.6 GB of
 K and V per step); --workload picks another named workload.
@@ -739,9 +738,10 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--decode", choices=["fused", "two-kernel"], default="fused",
-                    help="decode entry point: pa_v2_decode_fused (the combine inside phase 1, default) or "
-                         "pa_v2_decode (phase 1 + the phase-2 kernel)")
+    ap.add_argument("--decode", choices=["fused", "two-kernel"], default="two-kernel",
+                    help="decode entry point: pa_v2_decode (phase 1 + the phase-2 kernel, default) or "
+                         "pa_v2_decode_fused (the combine by the last CTA inside phase 1 on grids of at most "
+                         "two waves; measured slower on every workload here)")
     ap.add_argument("--cache-copies", type=int, default=0,
                     help="decode: copies of the K/V caches the steps rotate through (0: at least 2 and enough "
                          "to span 2.5x the L2, so no step finds earlier steps' pages there; 1 for profiler runs)")

@@ -659,18 +659,15 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
         }
     }
 
-    // Cluster split for a grid of less than about a wave of one-partition CTAs (a small
-    // batch): K CTAs share each partition, so the SMs run more warps.  The partners' partials
-    // travel to the cluster's first CTA, into its idle page ring.
+    // Cluster split of one-partition CTAs: K CTAs share each partition's pages, so a small
+    // grid runs more warps per SM; the partners' partials travel to the cluster's first CTA,
+    // into its idle page ring.
+    // Off unless asked for (PA_DECODE_SPLIT): on a two-sequence batch (16 rows x 15
+    // partitions) two CTAs per partition measured 18.4 us against 16.3 us for one, the two
+    // cluster barriers and the partner hand-off costing more than the finer spread of pages.
     int K = 1;
     if (PX == Pmax && !p1.merge) {
-        const int64_t ctas = rows * Pmax;
-        if (split_override() > 0)
-            K = split_override();
-        else if (ctas * 4 * 4 <= slots * 5)
-            K = 4;
-        else if (ctas * 2 * 4 <= slots * 5)
-            K = 2;
+        if (split_override() > 0) K = split_override();
         while (K > 1 && (int64_t)(K - 1) * (2 * kMaxHeadsPerCta + red_heads * D) * (int64_t)sizeof(float) > (int64_t)ring)
             K /= 2;
     }
