@@ -386,6 +386,11 @@ def run_ours(args):
 
     def step(i):
         kc, vc = kcs[i % nrot], vcs[i % nrot]
+        if args.decode == "append":
+            # the writer of the newest token fused into the decode
+            pa.pa_v2_decode_append(out, es, ml, tmp, q, nk, nv, kc, vc, wl.num_kv_heads, wl.scale, bt, sl,
+                                   wl.block_size, wl.max_seq_len, slopes, wl.kv_cache_dtype, wl.k_scale, wl.v_scale)
+            return
         pa.pa_reshape_and_cache(nk, nv, kc, vc, slots, wl.kv_cache_dtype, wl.k_scale, wl.v_scale)
         pa.pa_v2_decode(out, es, ml, tmp, q, kc, vc, wl.num_kv_heads, wl.scale, bt, sl, wl.block_size,
                         wl.max_seq_len, slopes, wl.kv_cache_dtype, wl.k_scale, wl.v_scale, counters=ctr)
@@ -395,7 +400,7 @@ def run_ours(args):
     kv_q_bytes = decode_bytes - S * H * d * wl.q_elem_bytes  # phase-1 share: K, V and Q
     # writer + phase 1 (+ phase 2 on the two-kernel path; the fused path with an fp32
     # tmp_output always runs the combine inside phase 1)
-    launches_per_step = 2 + (1 if wl.max_num_partitions > 1 and ctr is None else 0)
+    launches_per_step = (1 if args.decode == "append" else 2) + (1 if wl.max_num_partitions > 1 and ctr is None else 0)
 
     for i in range(args.warmup):
         step(i)
@@ -446,7 +451,8 @@ def run_ours(args):
         hbt, hsl = wl.block_tables.pin_memory(), wl.seq_lens.pin_memory()
         hnk, hnv, hslots = wl.new_key.pin_memory(), wl.new_value.pin_memory(), wl.slot_mapping.pin_memory()
         hout = torch.empty_like(wl.query).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in (hq, hbt, hsl, hnk, hnv, hslots))
+        copied = (hq, hbt, hsl, hnk, hnv) + (() if args.decode == "append" else (hslots,))
+        h2d = sum(t.numel() * t.element_size() for t in copied)
         d2h = hout.numel() * hout.element_size()
 
         def e2e_step(i):
@@ -455,7 +461,8 @@ def run_ours(args):
             sl.copy_(hsl, non_blocking=True)
             nk.copy_(hnk, non_blocking=True)
             nv.copy_(hnv, non_blocking=True)
-            slots.copy_(hslots, non_blocking=True)
+            if args.decode != "append":  # the append step takes the slots from the tables
+                slots.copy_(hslots, non_blocking=True)
             step(i)
             hout.copy_(out, non_blocking=True)
 
@@ -502,7 +509,8 @@ def run_ours(args):
         "dtype": wl.q_dtype if wl.kv_cache_dtype == "auto" else f"{wl.q_dtype}+fp8_e4m3",
         "data": "synthetic (seeded N(0, sigma) values, random block tables)",
         "config": workload_config(args.workload, wl, ws),
-        "decode_entry": "pa_v2_decode_fused" if ctr is not None else "pa_v2_decode",
+        "decode_entry": {"append": "pa_v2_decode_append", "fused": "pa_v2_decode_fused"}.get(args.decode,
+                                                                                               "pa_v2_decode"),
         "fraction_of_peak": round(value / peak, 4),
         "l2": f"{decode_bytes / 2**20:.0f} MiB of K/V read per step from {nrot} rotating cache copies of "
               f"{kv_bytes / 2**20:.0f} MiB ({nrot * kv_bytes / L2_BYTES:.1f}x the L2 together)",
@@ -738,8 +746,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--decode", choices=["fused", "two-kernel"], default="two-kernel",
-                    help="decode entry point: pa_v2_decode (phase 1 + the phase-2 kernel, default) or "
+    ap.add_argument("--decode", choices=["append", "fused", "two-kernel"], default="two-kernel",
+                    help="decode entry point: pa_v2_decode after pa_reshape_and_cache (two-kernel, the "
+                         "default), pa_v2_decode_append (the newest token's cache write inside phase 1), or "
                          "pa_v2_decode_fused (the combine by the last CTA inside phase 1 on grids of at most "
                          "two waves; measured slower on every workload here)")
     ap.add_argument("--cache-copies", type=int, default=0,

@@ -164,6 +164,41 @@ PA_API pa_status pa_v2_decode_fused(void* output, float* exp_sums, float* max_lo
                                     float k_scale, float v_scale, uint32_t* counters, int64_t num_counters,
                                     cudaStream_t stream);
 
+/*
+ * pa_v2_decode_append -- one decode step that also appends each sequence's newest token to
+ * the cache: pa_reshape_and_cache of that token followed by pa_v2_decode, in one kernel.
+ *
+ * Defines: "paged_attn.py", forward_decode after write_to_paged_cache (the decode writes the
+ * new key/value into the paged cache, then attends over it), with the slot of sequence s's
+ * new token taken from its block table: position t = seq_lens[s] - 1, slot
+ * block_tables[s][t / block_size] * block_size + t % block_size (what slot_mapping holds in a
+ * decode step).  The token is encoded exactly as pa_reshape_and_cache encodes it (bitwise
+ * copy, or e4m3fn of x / k_scale resp. x / v_scale in IEEE fp32), and attention uses the
+ * encoded value.  The CTA that streams the token's page writes it into the caches and into
+ * its shared-memory copy of that page, so the step has no separate writer kernel.
+ *
+ * Arguments: as pa_v2_decode, plus
+ *   key, value          device [num_seqs][num_kv_heads][head_size] rows in q_dtype (the
+ *                       newest token of each sequence); consecutive sequences' rows are
+ *                       key_stride_s / value_stride_s ELEMENTS apart (>= num_kv_heads *
+ *                       head_size, multiples of 8); 16-byte aligned.
+ *   key_cache, value_cache  written (the new token's slot) as well as read.
+ * Sequences with seq_lens[s] == 0 append nothing.  Every other sequence must have its newest
+ * token at position seq_lens[s] - 1 of its table row; a page id outside the cache there
+ * masks the token (and is flagged) as in pa_v2_decode.
+ * Errors: as pa_v2_decode; PA_ERR_INVALID_ARG also for a null, misaligned or short row.
+ */
+PA_API pa_status pa_v2_decode_append(void* output, float* exp_sums, float* max_logits, void* tmp_output,
+                                     const void* query, const void* key, const void* value,
+                                     int64_t key_stride_s, int64_t value_stride_s, void* key_cache,
+                                     void* value_cache, int num_seqs, int num_heads, int num_kv_heads,
+                                     int head_size, float scale, const int32_t* block_tables,
+                                     int max_blocks_per_seq, int num_blocks, const int32_t* seq_lens,
+                                     int block_size, int max_seq_len, int max_num_partitions,
+                                     const float* alibi_slopes, pa_dtype q_dtype,
+                                     pa_kv_cache_dtype kv_cache_dtype, pa_dtype tmp_dtype, float k_scale,
+                                     float v_scale, cudaStream_t stream);
+
 /* Arrival counters pa_v2_decode_fused needs: num_seqs * num_kv_heads *
  * ceil((num_heads / num_kv_heads) / 8) (one per sequence and group of up to 8 query heads of a
  * kv head); 0 for invalid sizes. */

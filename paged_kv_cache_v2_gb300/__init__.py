@@ -15,6 +15,8 @@ Entry points mirror ``include/pa_v2.h``:
   k_scale, v_scale)`` -- "paged_attn.py" write_to_paged_cache.
 * ``pa_v2_decode(..., counters=decode_counters(S, H, Hk, device))`` -- pa_v2_decode_fused:
   the same step with the partition combine inside phase 1.
+* ``pa_v2_decode_append(...)`` -- the cache writer of each sequence's newest token and the
+  decode in one kernel ("paged_attn.py" forward_decode after write_to_paged_cache).
 """
 from __future__ import annotations
 
@@ -63,6 +65,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.pa_v2_decode_fused.restype = i32
     lib.pa_v2_decode_fused.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, f32, P, i32, i32, P, i32, i32,
                                        i32, P, i32, i32, i32, f32, f32, P, i64, P]
+    lib.pa_v2_decode_append.restype = i32
+    lib.pa_v2_decode_append.argtypes = [P, P, P, P, P, P, P, i64, i64, P, P, i32, i32, i32, i32, f32, P, i32, i32, P,
+                                        i32, i32, i32, P, i32, i32, i32, f32, f32, P]
     lib.pa_v2_decode_num_counters.restype = i64
     lib.pa_v2_decode_num_counters.argtypes = [i32, i32, i32]
     lib.pa_reshape_and_cache.restype = i32
@@ -177,6 +182,50 @@ def pa_v2_decode(output: torch.Tensor, exp_sums: torch.Tensor, max_logits: torch
     if counters.dtype != torch.int32 or not counters.is_cuda or not counters.is_contiguous():
         raise TypeError("counters must be a contiguous int32 CUDA tensor (see decode_counters)")
     _check("pa_v2_decode_fused", lib.pa_v2_decode_fused(*args, _ptr(counters), counters.numel(), _stream(stream)))
+
+
+def pa_v2_decode_append(output: torch.Tensor, exp_sums: torch.Tensor, max_logits: torch.Tensor,
+                        tmp_output: torch.Tensor, query: torch.Tensor, key: torch.Tensor, value: torch.Tensor,
+                        key_cache: torch.Tensor, value_cache: torch.Tensor, num_kv_heads: int, scale: float,
+                        block_tables: torch.Tensor, seq_lens: torch.Tensor, block_size: int, max_seq_len: int,
+                        alibi_slopes: Optional[torch.Tensor] = None, kv_cache_dtype: str = "auto",
+                        k_scale: float = 1.0, v_scale: float = 1.0, num_blocks: Optional[int] = None,
+                        stream=None) -> None:
+    """One decode step that first appends every sequence's newest token (key/value [S, Hk, d]
+    rows, position seq_lens[s] - 1, slot from the block table) to the caches: the cache
+    writer and pa_v2_decode in one kernel.  Other arguments as pa_v2_decode."""
+    lib = load()
+    for name, t in (("output", output), ("exp_sums", exp_sums), ("max_logits", max_logits),
+                    ("tmp_output", tmp_output), ("query", query), ("key_cache", key_cache),
+                    ("value_cache", value_cache), ("block_tables", block_tables), ("seq_lens", seq_lens)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    S, H, d = query.shape
+    for name, t in (("key", key), ("value", value)):
+        if t.dim() != 3 or t.shape[0] != S or t.shape[1] != num_kv_heads or t.shape[2] != d or \
+                t.stride(2) != 1 or t.stride(1) != d or t.dtype != query.dtype or not t.is_cuda:
+            raise ValueError(f"{name} must be a CUDA tensor [num_seqs, num_kv_heads, head_size] in the query "
+                             "dtype with dense rows")
+    if block_tables.dtype != torch.int32 or seq_lens.dtype != torch.int32:
+        raise TypeError("block_tables and seq_lens must be int32")
+    if exp_sums.dtype != torch.float32 or max_logits.dtype != torch.float32:
+        raise TypeError("exp_sums and max_logits must be float32")
+    if tmp_output.dtype == torch.float32:
+        tmp_dtype = PA_DT_F32
+    elif tmp_output.dtype == query.dtype:
+        tmp_dtype = _dt(query.dtype)
+    else:
+        raise TypeError("tmp_output must be float32 or the query dtype")
+    if alibi_slopes is not None and (alibi_slopes.dtype != torch.float32 or not alibi_slopes.is_cuda):
+        raise TypeError("alibi_slopes must be a float32 CUDA tensor")
+    if num_blocks is None:
+        num_blocks = key_cache.shape[0]
+    _check("pa_v2_decode_append", lib.pa_v2_decode_append(
+        _ptr(output), _ptr(exp_sums), _ptr(max_logits), _ptr(tmp_output), _ptr(query), _ptr(key), _ptr(value),
+        key.stride(0), value.stride(0), _ptr(key_cache), _ptr(value_cache), S, H, int(num_kv_heads), d,
+        float(scale), _ptr(block_tables), int(block_tables.shape[1]), int(num_blocks), _ptr(seq_lens),
+        int(block_size), int(max_seq_len), int(tmp_output.shape[2]), _ptr(alibi_slopes), _dt(query.dtype),
+        _kv(kv_cache_dtype), tmp_dtype, float(k_scale), float(v_scale), _stream(stream)))
 
 
 def pa_reshape_and_cache(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor,

@@ -547,9 +547,12 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
                (2 * kWarps + 4) * kMaxHeadsPerCta * sizeof(float) +
                (size_t)kWarps * red_heads * (D + 4) * sizeof(float);
     };
-    while (nstage > 1 && smem_for(nstage) > (size_t)optin) --nstage;  // a deep ring that does not fit
+    // staged rows of the fused append: 2 x D 16-bit values after the rest
+    const size_t app_bytes = a.new_key != nullptr ? (size_t)4 * D : 0;
+    while (nstage > 1 && smem_for(nstage) + app_bytes > (size_t)optin) --nstage;  // a deep ring that does not fit
     const uint32_t ring = (uint32_t)kWarps * nstage * slot_bytes;
-    size_t smem1 = smem_for(nstage);
+    const size_t nrow_off = (smem_for(nstage) + 15) & ~(size_t)15;
+    size_t smem1 = nrow_off + app_bytes;
 
     Phase1Fn fn = phase1_for(bf16, fp8, D, bs);
     if (fn == nullptr) return PA_ERR_UNSUPPORTED;
@@ -586,6 +589,14 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
     p1.counters = nullptr;
     p1.merge = 0;
     p1.csplit = 1;
+    p1.mrg_off = (uint32_t)smem1;  // used only when a merge row is added below
+    p1.new_k = (const uint16_t*)a.new_key;
+    p1.new_v = (const uint16_t*)a.new_value;
+    p1.nk_stride = a.new_key_stride;
+    p1.nv_stride = a.new_value_stride;
+    p1.k_enc = a.k_scale;
+    p1.v_enc = a.v_scale;
+    p1.nrow_off = (uint32_t)nrow_off;
 
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -844,6 +855,59 @@ extern "C" pa_status pa_v2_decode_fused(void* output, float* exp_sums, float* ma
                            max_seq_len, stream);
     if (st != PA_OK) return st;
     return launch_decode(a, exp_sums, max_logits, tmp_output, counters);
+}
+
+extern "C" pa_status pa_v2_decode_append(void* output, float* exp_sums, float* max_logits, void* tmp_output,
+                                         const void* query, const void* key, const void* value,
+                                         int64_t key_stride_s, int64_t value_stride_s, void* key_cache,
+                                         void* value_cache, int num_seqs, int num_heads, int num_kv_heads,
+                                         int head_size, float scale, const int32_t* block_tables,
+                                         int max_blocks_per_seq, int num_blocks, const int32_t* seq_lens,
+                                         int block_size, int max_seq_len, int max_num_partitions,
+                                         const float* alibi_slopes, pa_dtype q_dtype,
+                                         pa_kv_cache_dtype kv_cache_dtype, pa_dtype tmp_dtype, float k_scale,
+                                         float v_scale, cudaStream_t stream) {
+    DecodeArgs a;
+    a.output = output;
+    a.exp_sums = exp_sums;
+    a.max_logits = max_logits;
+    a.tmp_output = tmp_output;
+    a.query = query;
+    a.key_cache = key_cache;
+    a.value_cache = value_cache;
+    a.num_seqs = num_seqs;
+    a.num_heads = num_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.head_size = head_size;
+    a.scale = scale;
+    a.block_tables = block_tables;
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.seq_lens = seq_lens;
+    a.block_size = block_size;
+    a.max_seq_len = max_seq_len;
+    a.max_num_partitions = max_num_partitions;
+    a.alibi_slopes = alibi_slopes;
+    a.q_dtype = q_dtype;
+    a.kv_cache_dtype = kv_cache_dtype;
+    a.tmp_dtype = tmp_dtype;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.stream = stream;
+    a.new_key = key;
+    a.new_value = value;
+    a.new_key_stride = key_stride_s;
+    a.new_value_stride = value_stride_s;
+    pa_status st = validate_decode(a);
+    if (st != PA_OK || num_seqs == 0) return st;
+    const int64_t row = (int64_t)num_kv_heads * head_size;
+    if (key == nullptr || value == nullptr || key_stride_s < row || value_stride_s < row || key_stride_s % 8 != 0 ||
+        value_stride_s % 8 != 0 || !aligned(key, 16) || !aligned(value, 16))
+        return PA_ERR_INVALID_ARG;
+    st = host_check_tables(block_tables, max_blocks_per_seq, num_blocks, seq_lens, num_seqs, block_size,
+                           max_seq_len, stream);
+    if (st != PA_OK) return st;
+    return launch_decode(a, exp_sums, max_logits, tmp_output);
 }
 
 // ---------------------------------------------------------------------------------------

@@ -27,6 +27,10 @@ struct DecodeArgs {
     pa_dtype tmp_dtype;
     float k_scale, v_scale;
     cudaStream_t stream;
+    // fused cache append (pa_v2_decode_append): the newest token's key/value rows, or null
+    const void* new_key = nullptr;
+    const void* new_value = nullptr;
+    int64_t new_key_stride = 0, new_value_stride = 0;  // elements between sequences' rows
 };
 
 // Argument checks shared by the decode entry points (no device access).

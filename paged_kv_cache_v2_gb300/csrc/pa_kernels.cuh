@@ -63,6 +63,17 @@ struct Phase1Params {
     // of csplit CTAs shares each partition's pages, and the others hand their partial
     // (max, exp-sum, rows) to the cluster's first CTA through distributed shared memory.
     int csplit;
+    uint32_t mrg_off;  // shared-memory byte offset of the CTA merge row (merge with PX < Pmax)
+    // Fused cache append (new_k != nullptr): the key/value rows of each sequence's newest
+    // token, position seq_lens[s] - 1 ([S][Hk][D] in the query dtype, rows nk_stride /
+    // nv_stride elements apart).  The CTA that streams that token's page writes them into
+    // the caches (encoded as the cache writer does) and into its shared-memory copy of the
+    // page, so the step needs no separate writer kernel.
+    const uint16_t* new_k;
+    const uint16_t* new_v;
+    int64_t nk_stride, nv_stride;
+    float k_enc, v_enc;   // k_scale, v_scale (the fp8 encode divides by them)
+    uint32_t nrow_off;    // shared-memory byte offset of the staged new rows (2 x D x 2 bytes)
 };
 
 struct Phase2Params {

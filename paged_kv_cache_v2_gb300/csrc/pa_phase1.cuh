@@ -126,6 +126,59 @@ __device__ __forceinline__ void fused_combine(const Phase1Params& p, int s, int 
     }
 }
 
+// Encode of the cache writer ("paged_attn.py", write_to_paged_cache): a bitwise copy for a
+// 16-bit cache, e4m3fn (round to nearest even, saturating) of x / scale for an fp8 cache,
+// the division in IEEE fp32.
+template <bool BF16>
+__device__ __forceinline__ float row_f32(uint16_t v) {
+    if constexpr (BF16)
+        return __uint_as_float(static_cast<uint32_t>(v) << 16);
+    else
+        return __half2float(__ushort_as_half(v));
+}
+
+// Write the staged key/value rows of one token (slot o of a page) into the shared-memory copy
+// of its K and V pages and, when page >= 0 (the page's (block, kv head) index), into the
+// caches.  Lane c moves K chunk c (16 bytes of the x-packed page) and V elements lane,
+// lane + 32, ...
+template <bool BF16, int KVB, int D, int BS>
+__device__ __forceinline__ void append_token(const Phase1Params& p, const uint16_t* nrow, uint8_t* kpage,
+                                             uint8_t* vpage, int o, int64_t page, int lane) {
+    constexpr int X = 16 / KVB;  // elements per 16-byte chunk
+    constexpr uint32_t page_bytes = (uint32_t)D * BS * KVB;
+    uint8_t* kc = page >= 0 ? const_cast<uint8_t*>(p.kcache) + page * page_bytes : nullptr;
+    uint8_t* vc = page >= 0 ? const_cast<uint8_t*>(p.vcache) + page * page_bytes : nullptr;
+    for (int c = lane; c < D / X; c += 32) {
+        uint4 chunk;
+        if constexpr (KVB == 2) {
+            chunk = reinterpret_cast<const uint4*>(nrow)[c];
+        } else {
+            uint16_t q[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                q[i] = f32x2_to_e4m3x2(__fdiv_rn(row_f32<BF16>(nrow[c * X + 2 * i]), p.k_enc),
+                                       __fdiv_rn(row_f32<BF16>(nrow[c * X + 2 * i + 1]), p.k_enc));
+            chunk = make_uint4((uint32_t)q[0] | ((uint32_t)q[1] << 16), (uint32_t)q[2] | ((uint32_t)q[3] << 16),
+                               (uint32_t)q[4] | ((uint32_t)q[5] << 16), (uint32_t)q[6] | ((uint32_t)q[7] << 16));
+        }
+        const uint32_t off = (uint32_t)(c * BS + o) * 16u;
+        *reinterpret_cast<uint4*>(kpage + off) = chunk;
+        if (kc) *reinterpret_cast<uint4*>(kc + off) = chunk;
+    }
+    for (int i = lane; i < D; i += 32) {
+        const uint32_t off = (uint32_t)(i * BS + o) * KVB;
+        if constexpr (KVB == 2) {
+            const uint16_t v = nrow[D + i];
+            *reinterpret_cast<uint16_t*>(vpage + off) = v;
+            if (vc) *reinterpret_cast<uint16_t*>(vc + off) = v;
+        } else {
+            const uint8_t v = (uint8_t)(f32x2_to_e4m3x2(__fdiv_rn(row_f32<BF16>(nrow[D + i]), p.v_enc), 0.f) & 0xffu);
+            vpage[off] = v;
+            if (vc) vc[off] = v;
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------------------
 // Phase 1
 // ---------------------------------------------------------------------------------------
@@ -253,7 +306,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     float* red_o = fac_n + kMaxHeadsPerCta;           // [kWarps][nh][D + 4] scaled accumulators
     constexpr int RS = D + 4;
     // CTA merge over several partitions: the running row [nh][D] (only when PX < Pmax)
-    float* mrg = red_o + kWarps * nh * RS;
+    float* mrg = reinterpret_cast<float*>(smem + p.mrg_off);
 
     if (lane == 0) {
         for (int k = 0; k < nstage; ++k) mbar_init(&bars[k], 1);
@@ -417,6 +470,24 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     }
     issue_more();
 
+    // Fused append: the warp that will consume the slot holding the sequence's newest token
+    // (position L - 1) stages that token's key and value rows in shared memory now, while the
+    // first pages are in flight.
+    const bool app = p.new_k != nullptr && L > 0 && P <= p.Pmax && (Pl - 1 - px) % PX == 0;
+    const int pg_last = app ? ((L - 1) >> bs_log2) - (Pl - 1) * ppart : 0;  // page in the last partition
+    const int j_last = pg_last >> pps_log2;                                   // its slot
+    const bool app_warp = app && (j_last % KW) == gw;
+    uint16_t* nrow = reinterpret_cast<uint16_t*>(smem + p.nrow_off);  // [2][D]: key row, value row
+    if (app_warp) {
+        const uint16_t* ks = p.new_k + (int64_t)s * p.nk_stride + (int64_t)kvh * D;
+        const uint16_t* vs = p.new_v + (int64_t)s * p.nv_stride + (int64_t)kvh * D;
+        for (int c = lane; c < D / 8; c += 32) {
+            reinterpret_cast<uint4*>(nrow)[c] = reinterpret_cast<const uint4*>(ks)[c];
+            reinterpret_cast<uint4*>(nrow + D)[c] = reinterpret_cast<const uint4*>(vs)[c];
+        }
+        __syncwarp();
+    }
+
     // ALiBi slopes of this thread's two head columns (2t, 2t+1), base-2 units.
     float sl0 = 0.f, sl1 = 0.f;
     if (p.alibi != nullptr) {
@@ -477,6 +548,19 @@ pa_v2_phase1_kernel(const Phase1Params p) {
             const uint32_t kbase = smem_addr(kslot), vbase = smem_addr(vslot);
             const uint32_t okmask = (uint32_t)(cmask >> (j * pps)) & ((1u << pps) - 1u);
             const int stok0 = t0 + j * slot_tokens;
+            if (app_warp && cq == Pl - 1 && j == j_last) {
+                // the newest token: encode its staged rows into this page's copy in shared
+                // memory and (one CTA per kv head) into the caches
+                const int pg = pg_last & (pps - 1);
+                if ((okmask >> pg) & 1u) {
+                    const int b = page_id(c0, c1, pg_last);
+                    const bool to_cache = grp == 0;
+                    append_token<BF16, KVB, D, BS>(p, nrow, const_cast<uint8_t*>(kslot) + (size_t)pg * page_bytes,
+                                                   const_cast<uint8_t*>(vslot) + (size_t)pg * page_bytes, (L - 1) & (bs - 1),
+                                                   to_cache ? (int64_t)b * p.Hk + kvh : -1, lane);
+                }
+                __syncwarp();
+            }
 
             if constexpr (FP8) {
                 // ---- one 32-token slot: two 16-token score tiles, one k32 P.V step ----------

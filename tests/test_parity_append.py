@@ -1,0 +1,168 @@
+"""GPU parity: pa_v2_decode_append (the cache writer of each sequence's newest token fused
+into phase 1) against the fp64 oracle: the oracle writer stores the new rows at the token's
+slot, then the oracle decode attends over the updated caches.
+
+Checked: the output, the partition statistics and tmp_output as for pa_v2_decode, and the
+caches after the call bit for bit (only the new tokens' slots change).  Covered: every named
+workload at reduced size, edge lengths for every block size, fp8 caches with both query
+dtypes, ALiBi, more than 8 query heads per kv head (several CTAs share the page; one writes
+it), strided rows, a new token on a page outside the cache (masked and flagged), CTAs
+striding over partitions and the cluster split.
+"""
+from __future__ import annotations
+
+import os
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_v2_gb300 as pa
+import workloads
+from gpu_harness import check_decode
+
+pytestmark = pytest.mark.gpu
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+@pytest.fixture(autouse=True)
+def _clear_device_errors():
+    pa.pa_get_device_errors(reset=True)
+    yield
+
+
+def _as_int(t: torch.Tensor) -> np.ndarray:
+    return (t.view(torch.uint8) if t.dtype == torch.uint8 else t.view(torch.int16)).cpu().numpy()
+
+
+def oracle_append(wl, slots=None):
+    """The oracle caches after the writer, and the oracle decode over them."""
+    kr, vr = oracle._np(wl.key_cache).copy(), oracle._np(wl.value_cache).copy()
+    oracle.reshape_and_cache(wl.new_key, wl.new_value, wl.q_dtype, kr, vr, wl.kv_storage,
+                             wl.slot_mapping if slots is None else slots, block_size=wl.block_size,
+                             k_scale=wl.k_scale, v_scale=wl.v_scale)
+    return kr, vr, oracle.decode_workload(wl, key_cache=kr, value_cache=vr)
+
+
+def run_append(wl, key=None, value=None):
+    """pa_v2_decode_append on device copies of the workload; returns (out, es, ml, tmp), caches."""
+    dev = "cuda"
+    S, H, d = wl.query.shape
+    P = wl.max_num_partitions
+    q = wl.query.to(dev)
+    kc, vc = wl.key_cache.to(dev), wl.value_cache.to(dev)
+    bt, sl = wl.block_tables.to(dev), wl.seq_lens.to(dev)
+    slopes = None if wl.alibi_slopes is None else wl.alibi_slopes.to(dev)
+    out = torch.full((S, H, d), float("nan"), dtype=wl.query.dtype, device=dev)
+    es = torch.full((S, H, P), float("nan"), dtype=torch.float32, device=dev)
+    ml = torch.full_like(es, float("nan"))
+    tmp = torch.full((S, H, P, d), float("nan"), dtype=torch.float32, device=dev)
+    nk = wl.new_key.to(dev) if key is None else key
+    nv = wl.new_value.to(dev) if value is None else value
+    pa.pa_v2_decode_append(out, es, ml, tmp, q, nk, nv, kc, vc, wl.num_kv_heads, wl.scale, bt, sl, wl.block_size,
+                           wl.max_seq_len, slopes, wl.kv_cache_dtype, wl.k_scale, wl.v_scale)
+    torch.cuda.synchronize()
+    return (out.cpu(), es.cpu(), ml.cpu(), tmp.cpu()), kc.cpu(), vc.cpu()
+
+
+def _check_all(wl, label):
+    kr, vr, ref = oracle_append(wl)
+    gpu, kc, vc = run_append(wl)
+    check_decode(wl, gpu, ref, label=label)
+    assert np.array_equal(_as_int(kc), kr.view(np.uint8 if kr.dtype == np.uint8 else np.int16)), f"{label}: key cache"
+    assert np.array_equal(_as_int(vc), vr.view(np.uint8 if vr.dtype == np.uint8 else np.int16)), f"{label}: value cache"
+
+
+@pytest.mark.parametrize("name", list(workloads.CONFIGS))
+def test_reduced_workloads(name):
+    _check_all(workloads.make(name, reduced=True), f"append {name}")
+    assert pa.pa_get_device_errors() == 0
+
+
+@pytest.mark.parametrize("bs", [8, 16, 32])
+def test_edge_lengths(bs):
+    wl = workloads.build(num_seqs=13, num_heads=8, num_kv_heads=2, head_size=128, block_size=bs,
+                         seq_lens=[0, 1, 2, 15, 16, 17, 511, 512, 513, 1024, 1025, 1536, 2047], seed=500 + bs)
+    _check_all(wl, f"append bs{bs}")
+
+
+@pytest.mark.parametrize("q_dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("kv", ["auto", "fp8_e4m3"])
+@pytest.mark.parametrize("alibi", [False, True])
+def test_dtypes_alibi(q_dtype, kv, alibi):
+    wl = workloads.build(num_seqs=5, num_heads=12, num_kv_heads=3, head_size=128, block_size=16,
+                         seq_lens=[1, 517, 1030, 64, 2500], q_dtype=q_dtype, kv_cache_dtype=kv, alibi=alibi,
+                         k_scale=0.05 if kv != "auto" else 1.0, v_scale=0.07 if kv != "auto" else 1.0, seed=510)
+    _check_all(wl, f"append {q_dtype} {kv} alibi={alibi}")
+
+
+@pytest.mark.parametrize("G", [12, 16])
+def test_more_than_eight_heads_per_kv_head(G):
+    wl = workloads.build(num_seqs=3, num_heads=2 * G, num_kv_heads=2, head_size=96, block_size=32,
+                         seq_lens=[700, 33, 1500], q_dtype="bf16", seed=520 + G)
+    _check_all(wl, f"append G{G}")
+
+
+def test_strided_rows():
+    wl = workloads.make("llama_gqa_decode", reduced=True)
+    S, Hk, d = wl.new_key.shape
+    buf = torch.zeros(S, 3 * Hk * d, dtype=wl.new_key.dtype, device="cuda")
+    buf[:, :Hk * d] = wl.new_key.reshape(S, -1).cuda()
+    buf[:, 2 * Hk * d:] = wl.new_value.reshape(S, -1).cuda()
+    key = buf[:, :Hk * d].view(S, Hk, d)
+    value = buf[:, 2 * Hk * d:].view(S, Hk, d)
+    kr, vr, ref = oracle_append(wl)
+    gpu, kc, vc = run_append(wl, key, value)
+    check_decode(wl, gpu, ref, label="strided rows")
+    assert np.array_equal(_as_int(kc), kr.view(np.int16)) and np.array_equal(_as_int(vc), vr.view(np.int16))
+
+
+def test_new_token_on_a_page_outside_the_cache_is_masked_and_flagged():
+    wl = workloads.build(num_seqs=2, num_heads=4, num_kv_heads=2, head_size=64, block_size=16,
+                         seq_lens=[100, 40], seed=530)
+    bad = wl.block_tables.clone()
+    bad[0, 6] = wl.num_blocks + 3  # tokens 96..99 of sequence 0, the new token among them
+    wlb = workloads.Workload(**{**wl.__dict__, "block_tables": bad})
+    gpu, kc, vc = run_append(wlb)
+    assert pa.pa_get_device_errors() & 1
+    # nothing was written (the new token of sequence 1 is, as its page is in the cache)
+    kr, vr = oracle._np(wl.key_cache).copy(), oracle._np(wl.value_cache).copy()
+    oracle.reshape_and_cache(wl.new_key[1:], wl.new_value[1:], wl.q_dtype, kr, vr, wl.kv_storage,
+                             wl.slot_mapping[1:], block_size=wl.block_size)
+    assert np.array_equal(_as_int(kc), kr.view(np.int16)) and np.array_equal(_as_int(vc), vr.view(np.int16))
+    # sequence 0 attends over its first 96 tokens only (no ALiBi: order does not matter)
+    wl_ref = workloads.Workload(**{**wl.__dict__, "block_tables": wl.block_tables[:1].clone(),
+                                   "seq_lens": torch.tensor([96], dtype=torch.int32), "num_seqs": 1,
+                                   "query": wl.query[:1].clone()})
+    ref0 = oracle.decode_workload(wl_ref)
+    got0 = gpu[0][0].double().numpy()
+    assert np.abs(got0 - ref0["out"].reshape(got0.shape)).max() <= 2e-3 + 2 ** -11 * np.abs(ref0["out"]).max()
+
+
+_CHILD = r"""
+import sys
+sys.path.insert(0, {here!r}); sys.path.insert(0, {root!r})
+import workloads
+from test_parity_append import _check_all
+for spec in {specs!r}:
+    _check_all(workloads.build(**spec), f"child {{spec}}")
+print("child ok")
+"""
+
+
+@pytest.mark.parametrize("env", [{"PA_DECODE_PX": "2"}, {"PA_DECODE_SPLIT": "2"}, {"PA_DECODE_SPLIT": "4"}])
+def test_strides_and_cluster_split(env):
+    # the CTA that streams the newest token's page is the last of its stride, or a cluster
+    # partner other than the first one
+    specs = [dict(num_seqs=4, num_heads=8, num_kv_heads=2, head_size=128, block_size=16,
+                  seq_lens=[3000, 1, 700, 2600], alibi=True, seed=540),
+             dict(num_seqs=3, num_heads=12, num_kv_heads=3, head_size=128, block_size=8, seq_lens=[1030, 64, 2500],
+                  kv_cache_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.07, seed=541)]
+    code = _CHILD.format(here=HERE, root=os.path.dirname(HERE), specs=specs)
+    r = subprocess.run([sys.executable, "-c", code], env=dict(os.environ, **env), capture_output=True, text=True,
+                       timeout=900)
+    assert r.returncode == 0 and "child ok" in r.stdout, r.stdout[-2000:] + r.stderr[-4000:]
