@@ -1,9 +1,11 @@
 """Benchmark: one decode step of paged attention on GB300 through the pa_v2 C ABI.
 
-A step is the whole hot path for one batch: the cache writer stores every sequence's newest
-token (pa_reshape_and_cache), then pa_v2_decode runs phase 1 (with the single-pass path for
-one-partition sequences) and the phase-2 combine (--decode fused: pa_v2_decode_fused, the
-combine by the last CTA of each (sequence, head group) inside phase 1).  The default workload is the largest decode batch,
+A step is the whole hot path for one batch: every sequence's newest token is written into the
+cache and the decode attends over it -- by default one pa_v2_decode_append call (phase 1
+writes the token while streaming its page, then the phase-2 combine); --decode two-kernel
+runs pa_reshape_and_cache then pa_v2_decode, --decode fused pa_reshape_and_cache then
+pa_v2_decode_fused (the combine by the last CTA of each (sequence, head group) inside phase
+1).  The default workload is the largest decode batch,
 MHA with ALiBi over a ragged batch (256 sequences, 16 heads, head size 96, block size 32,
 lognormal lengths with median 1024 capped at 32768, bf16 query and cache: about 2.6 GB of
 K and V per step); --workload picks another named workload.
@@ -746,9 +748,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--decode", choices=["append", "fused", "two-kernel"], default="two-kernel",
-                    help="decode entry point: pa_v2_decode after pa_reshape_and_cache (two-kernel, the "
-                         "default), pa_v2_decode_append (the newest token's cache write inside phase 1), or "
+    ap.add_argument("--decode", choices=["append", "fused", "two-kernel"], default="append",
+                    help="decode entry point: pa_v2_decode_append (the newest token's cache write inside phase "
+                         "1, the default), pa_v2_decode after pa_reshape_and_cache (two-kernel), or "
                          "pa_v2_decode_fused (the combine by the last CTA inside phase 1 on grids of at most "
                          "two waves; measured slower on every workload here)")
     ap.add_argument("--cache-copies", type=int, default=0,
