@@ -177,7 +177,10 @@ PA_API pa_status pa_v2_decode_fused(void* output, float* exp_sums, float* max_lo
  * encoded value.  The CTA that streams the token's page writes it into the caches and into
  * its shared-memory copy of that page, so the step has no separate writer kernel.
  *
- * Arguments: as pa_v2_decode, plus
+ * Arguments: as pa_v2_decode, except that tmp_output is scratch (its contents after the call
+ * are unspecified: a CTA that streams several partitions of a long sequence folds them into
+ * one fp32 row, and phase 2 merges those rows); output, max_logits and exp_sums are as there.
+ * In addition:
  *   key, value          device [num_seqs][num_kv_heads][head_size] rows in q_dtype (the
  *                       newest token of each sequence); consecutive sequences' rows are
  *                       key_stride_s / value_stride_s ELEMENTS apart (>= num_kv_heads *

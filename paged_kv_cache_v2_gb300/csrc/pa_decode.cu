@@ -284,6 +284,83 @@ pa_v2_phase2_rows_kernel(const Phase2Params p) {
     }
 }
 
+// Phase 2 over merged rows: phase-1 CTA px folded partitions px, px + R, ... into fp32 row
+// px, so row r's weight is the sum of its partitions' exp(m_p - g) l_p.  One CTA per
+// (query head, sequence), 256 threads: the statistics of every partition load together, then
+// four groups of threads each take every fourth row over all columns (float4), and the
+// groups' sums add in shared memory.
+constexpr int kP2mThreads = 256;
+
+template <bool BF16>
+__global__ void __launch_bounds__(kP2mThreads)
+pa_v2_phase2_merged_kernel(const Phase2Params p) {
+    extern __shared__ float smm[];  // [Pmax] log2 max, [Pmax] exp-sum, [R] row weights, [4][D] sums
+    __shared__ float red[kP2mThreads / 32];
+    const int h = blockIdx.x, s = blockIdx.y;
+    const int L = p.seq_lens[s];  // an input phase 1 only read
+    griddep_wait();
+    const int P = min(L > 0 ? (L + kPartition - 1) / kPartition : 0, p.Pmax);
+    if (P <= 1) return;
+    const int R = min(p.rstride, P);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t row = (int64_t)s * p.H + h;
+    float* pa2 = smm;
+    float* pl = pa2 + p.Pmax;
+    float* wr = pl + p.Pmax;
+    float* part = wr + p.rstride;
+    float gm = -INFINITY;
+    for (int q = tid; q < P; q += kP2mThreads) {
+        const float l = p.exp_sums[row * p.Pmax + q], m = p.max_logits[row * p.Pmax + q];
+        const float a = l > 0.f ? m * kLog2e : -INFINITY;
+        pa2[q] = a;
+        pl[q] = l;
+        gm = fmaxf(gm, a);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, o));
+    if (lane == 0) red[warp] = gm;
+    __syncthreads();
+    gm = red[0];
+#pragma unroll
+    for (int w = 1; w < kP2mThreads / 32; ++w) gm = fmaxf(gm, red[w]);
+    float wsum = 0.f;
+    for (int r = tid; r < R; r += kP2mThreads) {
+        float w = 0.f;
+        for (int q = r; q < P; q += p.rstride)
+            if (pa2[q] != -INFINITY) w += pl[q] * ex2(pa2[q] - gm);
+        wr[r] = w;
+        wsum += w;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, o);
+    __syncthreads();  // every warp is done with red[] as the maximum
+    if (lane == 0) red[warp] = wsum;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kP2mThreads / 32; ++w) tot += red[w];
+    // group gq takes rows gq, gq + 4, ...; its threads cover the row's float4 columns
+    const int nq = p.D / 4, per = kP2mThreads / 4, gq = tid / per, c = tid - gq * per;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (c < nq) {
+        const float4* rows = reinterpret_cast<const float4*>(p.tmp_out) + row * p.Pmax * nq + c;
+#pragma unroll 4
+        for (int r = gq; r < R; r += 4) {
+            const float4 x = rows[(int64_t)r * nq];
+            const float w = wr[r];
+            acc.x = fmaf(w, x.x, acc.x);
+            acc.y = fmaf(w, x.y, acc.y);
+            acc.z = fmaf(w, x.z, acc.z);
+            acc.w = fmaf(w, x.w, acc.w);
+        }
+        reinterpret_cast<float4*>(part + gq * p.D)[c] = acc;
+    }
+    __syncthreads();
+    const float inv = tot > 0.f ? 1.f / tot : 0.f;
+    for (int i = tid; i < p.D; i += kP2mThreads)
+        store_out<BF16>(p.out, row * p.D + i, (part[i] + part[p.D + i] + part[2 * p.D + i] + part[3 * p.D + i]) * inv);
+}
+
 // ---------------------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------------------
@@ -646,8 +723,8 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
     // one keeps a row per partition.  Either way the rows the last CTA merges are bounded by
     // kFusedRowBytes.
     bool fused = counters != nullptr && Pmax > 1 && rows * PX <= 2 * slots;
-    const bool merge = fused && a.tmp_dtype == PA_DT_F32 && PX < Pmax;
-    if (merge && PX < Pmax) {
+    const bool merge = (fused || a.tmp_scratch) && a.tmp_dtype == PA_DT_F32 && PX < Pmax;
+    if (merge) {
         // CTAs that stream several partitions keep their running row in shared memory
         const size_t with_row = smem1 + (size_t)red_heads * D * sizeof(float);
         if (with_row > (size_t)optin || ensure_smem((const void*)fn, with_row) != cudaSuccess || !plan(with_row)) {
@@ -655,8 +732,9 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
             return PA_ERR_CUDA;
         }
         smem1 = with_row;
-        fused = rows * PX <= 2 * slots;
+        fused = fused && rows * PX <= 2 * slots;
     }
+    p1.merge = merge ? 1 : 0;
     if (fused) {
         const int64_t R = merge ? PX : Pmax;
         const int64_t row_bytes = (int64_t)red_heads * D * (a.tmp_dtype == PA_DT_F32 ? 4 : 2);
@@ -664,10 +742,7 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
         if ((kMaxHeadsPerCta + (int64_t)red_heads * (R + 2 * Pmax)) * (int64_t)sizeof(float) > (int64_t)ring ||
             R * row_bytes > kFusedRowBytes)
             fused = false;
-        if (fused) {
-            p1.counters = counters;
-            p1.merge = merge ? 1 : 0;
-        }
+        if (fused) p1.counters = counters;
     }
 
     // Cluster split of one-partition CTAs: K CTAs share each partition's pages, so a small
@@ -716,7 +791,25 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
         p2.H = a.num_heads;
         p2.D = D;
         p2.Pmax = a.max_num_partitions;
+        p2.rstride = (int)PX;
         const bool t16 = a.tmp_dtype != PA_DT_F32;
+        const size_t smem_m = (size_t)(2 * a.max_num_partitions + PX + 4 * D) * sizeof(float);
+        if (p1.merge && smem_m <= 48 * 1024) {
+            // rows merged by the phase-1 CTAs (PX of them per sequence and head)
+            void (*fm)(const Phase2Params) = bf16 ? pa_v2_phase2_merged_kernel<true> : pa_v2_phase2_merged_kernel<false>;
+            cudaLaunchConfig_t cm = {};
+            cm.gridDim = dim3((unsigned)a.num_heads, (unsigned)a.num_seqs, 1);
+            cm.blockDim = dim3(kP2mThreads, 1, 1);
+            cm.dynamicSmemBytes = smem_m;
+            cm.stream = a.stream;
+            cm.attrs = attr;
+            cm.numAttrs = 1;
+            if (cudaLaunchKernelEx(&cm, fm, p2) != cudaSuccess) {
+                (void)cudaGetLastError();
+                return PA_ERR_CUDA;
+            }
+            return PA_OK;
+        }
         if (a.max_num_partitions <= 64 && D <= 128) {
             // one warp per row (a wide batch of short and medium sequences)
             void (*fr)(const Phase2Params) =
@@ -851,6 +944,7 @@ extern "C" pa_status pa_v2_decode_fused(void* output, float* exp_sums, float* ma
     if (counters != nullptr &&
         (!aligned(counters, 4) || num_counters < decode_num_counters(num_seqs, num_heads, num_kv_heads)))
         return PA_ERR_INVALID_ARG;
+    a.tmp_scratch = counters != nullptr;
     st = host_check_tables(block_tables, max_blocks_per_seq, num_blocks, seq_lens, num_seqs, block_size,
                            max_seq_len, stream);
     if (st != PA_OK) return st;
@@ -898,6 +992,7 @@ extern "C" pa_status pa_v2_decode_append(void* output, float* exp_sums, float* m
     a.new_value = value;
     a.new_key_stride = key_stride_s;
     a.new_value_stride = value_stride_s;
+    a.tmp_scratch = true;
     pa_status st = validate_decode(a);
     if (st != PA_OK || num_seqs == 0) return st;
     const int64_t row = (int64_t)num_kv_heads * head_size;

@@ -31,6 +31,9 @@ struct DecodeArgs {
     const void* new_key = nullptr;
     const void* new_value = nullptr;
     int64_t new_key_stride = 0, new_value_stride = 0;  // elements between sequences' rows
+    // tmp_output is the caller's scratch (its contents after the call are unspecified), so
+    // CTAs that stream several partitions may fold them into one row
+    bool tmp_scratch = false;
 };
 
 // Argument checks shared by the decode entry points (no device access).

@@ -55,9 +55,9 @@ struct Phase1Params {
     // group) to finish merges the partitions; counters[s * gridDim.y + blockIdx.y] counts the
     // CTAs that have finished and is reset to 0 by the last one.
     uint32_t* counters;
-    // With the fused combine: each CTA merges its own partitions px, px + PX, ... into fp32
-    // row px of tmp_output (instead of one row per partition), so the last CTA merges at
-    // most PX rows.
+    // Each CTA merges its own partitions px, px + PX, ... into fp32 row px of tmp_output
+    // (instead of one row per partition; tmp_output is then the caller's scratch), so the
+    // combine -- the last CTA's or phase 2's -- merges at most PX rows.
     int merge;
     // CTAs per partition (1, 2 or 4; more than 1 only with one partition per CTA): a cluster
     // of csplit CTAs shares each partition's pages, and the others hand their partial
@@ -83,6 +83,7 @@ struct Phase2Params {
     const void* tmp_out;  // fp32, or the output dtype (template parameter TMP16)
     const int32_t* seq_lens;
     int S, H, D, Pmax;
+    int rstride;  // merged rows: row r holds partitions r, r + rstride, ... (phase-1 CTA merge)
 };
 
 template <bool BF16>

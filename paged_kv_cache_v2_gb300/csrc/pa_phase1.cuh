@@ -507,11 +507,12 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     const int tokB = FP8 ? c_fp8_row_token[g + 8] : g + 8;
     // Where a partition's result goes.  A one-partition sequence writes the output directly
     // (single pass).  Otherwise each partition writes its own tmp_output row -- or, when the
-    // CTA merges its partitions (fused combine), the CTA folds them into fp32 row px, and a
-    // CTA that covers every partition of the sequence (PX == 1) writes the output directly.
+    // CTA merges its partitions (p.merge: tmp_output is the caller's scratch), the CTA folds
+    // them into fp32 row px, and a CTA that covers every partition of the sequence (PX == 1)
+    // writes the output directly.
     const int nwork = min(PX, Pl);  // CTAs of this (sequence, head group) that have partitions
     const bool fused = p.counters != nullptr;
-    const bool merge = fused && p.merge != 0;
+    const bool merge = p.merge != 0;
     const bool direct = (Pl == 1) || (merge && nwork == 1);
     // The CTA's running merge (lane t < 4 of warp 0 holds heads 2t and 2t + 1): max in log2
     // units relative to the sequence's last token, and the exp-sum at that max.

@@ -2,8 +2,10 @@
 into phase 1) against the fp64 oracle: the oracle writer stores the new rows at the token's
 slot, then the oracle decode attends over the updated caches.
 
-Checked: the output, the partition statistics and tmp_output as for pa_v2_decode, and the
-caches after the call bit for bit (only the new tokens' slots change).  Covered: every named
+Checked: the output and the partition statistics as for pa_v2_decode (tmp_output is scratch
+for this entry point), and the caches after the call bit for bit (only the new tokens' slots
+change).  The full-size long-context step runs CTAs that fold ten partitions each into one
+row and phase 2 over those rows.  Covered: every named
 workload at reduced size, edge lengths for every block size, fp8 caches with both query
 dtypes, ALiBi, more than 8 query heads per kv head (several CTAs share the page; one writes
 it), strided rows, a new token on a page outside the cache (masked and flagged), CTAs
@@ -22,7 +24,7 @@ import torch
 import oracle
 import paged_kv_cache_v2_gb300 as pa
 import workloads
-from gpu_harness import check_decode
+from gpu_harness import check_decode, sample_pairs
 
 pytestmark = pytest.mark.gpu
 
@@ -72,7 +74,8 @@ def run_append(wl, key=None, value=None):
 def _check_all(wl, label):
     kr, vr, ref = oracle_append(wl)
     gpu, kc, vc = run_append(wl)
-    check_decode(wl, gpu, ref, label=label)
+    # tmp_output is scratch here (CTAs streaming several partitions fold them into one row)
+    check_decode(wl, gpu, ref, label=label, check_tmp=False)
     assert np.array_equal(_as_int(kc), kr.view(np.uint8 if kr.dtype == np.uint8 else np.int16)), f"{label}: key cache"
     assert np.array_equal(_as_int(vc), vr.view(np.uint8 if vr.dtype == np.uint8 else np.int16)), f"{label}: value cache"
 
@@ -117,7 +120,7 @@ def test_strided_rows():
     value = buf[:, 2 * Hk * d:].view(S, Hk, d)
     kr, vr, ref = oracle_append(wl)
     gpu, kc, vc = run_append(wl, key, value)
-    check_decode(wl, gpu, ref, label="strided rows")
+    check_decode(wl, gpu, ref, label="strided rows", check_tmp=False)
     assert np.array_equal(_as_int(kc), kr.view(np.int16)) and np.array_equal(_as_int(vc), vr.view(np.int16))
 
 
@@ -141,6 +144,23 @@ def test_new_token_on_a_page_outside_the_cache_is_masked_and_flagged():
     ref0 = oracle.decode_workload(wl_ref)
     got0 = gpu[0][0].double().numpy()
     assert np.abs(got0 - ref0["out"].reshape(got0.shape)).max() <= 2e-3 + 2 ** -11 * np.abs(ref0["out"]).max()
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["llama_gqa_decode", "long_context_gqa"])
+def test_full_size_sampled(name):
+    # the benchmark's launch configuration (for the long context: one wave of CTAs, each
+    # folding about ten partitions into one row, and phase 2 over those rows)
+    wl = workloads.make(name)
+    pairs = sample_pairs(wl, n=16)
+    kr, vr = oracle._np(wl.key_cache).copy(), oracle._np(wl.value_cache).copy()
+    oracle.reshape_and_cache(wl.new_key, wl.new_value, wl.q_dtype, kr, vr, wl.kv_storage, wl.slot_mapping,
+                             block_size=wl.block_size, k_scale=wl.k_scale, v_scale=wl.v_scale)
+    ref = oracle.decode_workload(wl, pairs=pairs, key_cache=kr, value_cache=vr)
+    gpu, kc, vc = run_append(wl)
+    check_decode(wl, gpu, ref, pairs=pairs, label=f"append {name}", check_tmp=False)
+    assert np.array_equal(_as_int(kc), kr) and np.array_equal(_as_int(vc), vr)
+    assert pa.pa_get_device_errors() == 0
 
 
 _CHILD = r"""
