@@ -294,7 +294,8 @@ constexpr int kP2mThreads = 256;
 template <bool BF16>
 __global__ void __launch_bounds__(kP2mThreads)
 pa_v2_phase2_merged_kernel(const Phase2Params p) {
-    extern __shared__ float smm[];  // [Pmax] log2 max, [Pmax] exp-sum, [R] row weights, [4][D] sums
+    // [Pmax] log2 max, [Pmax] exp-sum, [R] row weights, then (16-byte aligned) [4][D] sums
+    extern __shared__ __align__(16) float smm[];
     __shared__ float red[kP2mThreads / 32];
     const int h = blockIdx.x, s = blockIdx.y;
     const int L = p.seq_lens[s];  // an input phase 1 only read
@@ -307,7 +308,7 @@ pa_v2_phase2_merged_kernel(const Phase2Params p) {
     float* pa2 = smm;
     float* pl = pa2 + p.Pmax;
     float* wr = pl + p.Pmax;
-    float* part = wr + p.rstride;
+    float* part = smm + ((2 * p.Pmax + p.rstride + 3) & ~3);  // float4 stores: 16-byte aligned
     float gm = -INFINITY;
     for (int q = tid; q < P; q += kP2mThreads) {
         const float l = p.exp_sums[row * p.Pmax + q], m = p.max_logits[row * p.Pmax + q];
@@ -793,7 +794,7 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
         p2.Pmax = a.max_num_partitions;
         p2.rstride = (int)PX;
         const bool t16 = a.tmp_dtype != PA_DT_F32;
-        const size_t smem_m = (size_t)(2 * a.max_num_partitions + PX + 4 * D) * sizeof(float);
+        const size_t smem_m = (size_t)(((2 * a.max_num_partitions + PX + 3) & ~(int64_t)3) + 4 * D) * sizeof(float);
         if (p1.merge && smem_m <= 48 * 1024) {
             // rows merged by the phase-1 CTAs (PX of them per sequence and head)
             void (*fm)(const Phase2Params) = bf16 ? pa_v2_phase2_merged_kernel<true> : pa_v2_phase2_merged_kernel<false>;
