@@ -577,7 +577,9 @@ pa_v2_phase1_kernel(const Phase1Params p) {
                     const int tt = tile * 16 + k_tok;
                     const uint32_t krow = kbase + (uint32_t)(tt >> bs_log2) * page_bytes +
                                           (uint32_t)(k_chunk * bs + (tt & (bs - 1))) * 16u;
-                    float sc[4] = {0.f, 0.f, 0.f, 0.f};
+                    // two accumulators, so the MMAs of a tile form two dependency chains of
+                    // half the length; summed after the last step
+                    float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                     for (int st = 0; st < NS; ++st) {
                         uint32_t a0, a1, a2, a3;
@@ -589,19 +591,21 @@ pa_v2_phase1_kernel(const Phase1Params p) {
                         }
                         if constexpr (Q8) {
                             mma_e4m3_16832(sc, a0, a1, a2, a3, qh[st][0], qh[st][1]);
-                            mma_e4m3_16832(sc, a0, a1, a2, a3, qm[st][0], qm[st][1]);
-                            mma_e4m3_16832(sc, a0, a1, a2, a3, ql[st][0], ql[st][1]);
+                            mma_e4m3_16832(sd, a0, a1, a2, a3, qm[st][0], qm[st][1]);
+                            mma_e4m3_16832(st & 1 ? sd : sc, a0, a1, a2, a3, ql[st][0], ql[st][1]);
                         } else {
                             // widen the K codes to f16 (exact): chunk 2st in a0/a1, 2st+1 in a2/a3
                             mma16816<false>(sc, e4m3x2_to_f16x2(lo16(a0)), e4m3x2_to_f16x2(lo16(a1)),
                                             e4m3x2_to_f16x2(hi16(a0)), e4m3x2_to_f16x2(hi16(a1)),
                                             qf[2 * st][0], qf[2 * st][1]);
                             if (2 * st + 1 < NK)
-                                mma16816<false>(sc, e4m3x2_to_f16x2(lo16(a2)), e4m3x2_to_f16x2(lo16(a3)),
+                                mma16816<false>(sd, e4m3x2_to_f16x2(lo16(a2)), e4m3x2_to_f16x2(lo16(a3)),
                                                 e4m3x2_to_f16x2(hi16(a2)), e4m3x2_to_f16x2(hi16(a3)),
                                                 qf[2 * st + 1][0], qf[2 * st + 1][1]);
                         }
                     }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) sc[i] += sd[i];
                     const int ttok0 = stok0 + tile * 16;
                     float s0 = sc[0] * qk_mul0, s1 = sc[1] * qk_mul1;
                     float s2 = sc[2] * qk_mul0, s3 = sc[3] * qk_mul1;
