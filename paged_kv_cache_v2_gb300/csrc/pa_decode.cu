@@ -18,7 +18,8 @@
 //    accumulate): 16 tokens x 8 query heads per MMA, K rows fed straight from the x-packed
 //    page with ldmatrix, V^T rows straight from the token-contiguous page, P moved from
 //    the score fragment into the P.V operand with movmatrix.  fp8 e4m3 pages are widened
-//    to f16/bf16 in registers (exact); k_scale and the softmax scale fold into one fp32
+//    to f16 in registers (exact) for both products (a bf16 query is scaled per head by a
+//    power of two into f16, also exact); k_scale and the softmax scale fold into one fp32
 //    multiplier on the scores, v_scale into the final normalisation.
 //  * The online softmax runs per warp in the base-2 domain; the warps' (m, l, acc) merge
 //    through shared memory at the end of the partition.  A one-partition sequence writes

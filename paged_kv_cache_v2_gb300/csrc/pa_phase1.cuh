@@ -378,10 +378,8 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     // element lands near 224) and split into three e4m3 terms hi + mid + lo (at least 12
     // significant bits, so every bf16 value is exact); the scale is undone on the scores.
     constexpr int NS = (D + 31) / 32;  // k32 steps over the head dimension (fp8)
-    constexpr bool Q8 = FP8 && BF16;   // scores on the e4m3 tensor path
-    uint32_t qf[Q8 ? 1 : NK][2];
-    uint32_t qh[Q8 ? NS : 1][2], qm[Q8 ? NS : 1][2], ql[Q8 ? NS : 1][2];
-    float qs0 = 1.f, qs1 = 1.f;  // per-column score factor from the fp8 query scale
+    uint32_t qf[NK][2];
+    float qs0 = 1.f, qs1 = 1.f;  // per-column score factor undoing the query's scale (fp8, bf16 query)
     {
         const bool live = g < nh;
         const uint16_t* qrow = reinterpret_cast<const uint16_t*>(p.query) + ((int64_t)s * H + h0 + g) * D;
@@ -397,7 +395,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
                 qf[kk][0] = b0;
                 qf[kk][1] = b1;
             }
-        } else if constexpr (!Q8) {
+        } else if constexpr (!BF16) {
 #pragma unroll
             for (int kk = 0; kk < NK; ++kk) {
                 uint2 v = make_uint2(0u, 0u);
@@ -406,62 +404,28 @@ pa_v2_phase1_kernel(const Phase1Params p) {
                 qf[kk][1] = v.y;
             }
         } else {
-            // thread holds elements 32 st + 16 hh + 4t + i of its head g; two passes over them
-            // (largest magnitude, then scale and split) keep few values live at once
-            auto load4 = [&](int idx, float (&f)[4]) {
-                uint2 w = make_uint2(0u, 0u);
-                if (live && idx < D) w = *reinterpret_cast<const uint2*>(qrow + idx);
-                const uint32_t ww[2] = {w.x, w.y};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint16_t bits = (uint16_t)(ww[i >> 1] >> (16 * (i & 1)));
-                    if constexpr (BF16)
-                        f[i] = __uint_as_float((uint32_t)bits << 16);
-                    else
-                        f[i] = __half2float(__ushort_as_half(bits));
-                }
-            };
+            // A bf16 query meets the widened fp8 keys in f16: each head's row is scaled by a
+            // power of two so its largest element lands in [8192, 16384), which makes every
+            // element exact in f16 (8 significant bits of 11, down to 2^-14 of the largest);
+            // the scale is undone on the scores.  The thread holds elements 16 kk + 4t + i.
+            uint2 w[NK];
             float amax = 0.f;
 #pragma unroll
-            for (int st = 0; st < NS; ++st) {
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    float f[4];
-                    load4(32 * st + 16 * hh + 4 * t, f);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) amax = fmaxf(amax, fabsf(f[i]));
-                }
+            for (int kk = 0; kk < NK; ++kk) {
+                w[kk] = live ? *reinterpret_cast<const uint2*>(qrow + kk * 16 + 4 * t) : make_uint2(0u, 0u);
+                amax = fmaxf(amax, fmaxf(fmaxf(fabsf(__uint_as_float(w[kk].x << 16)), fabsf(__uint_as_float(w[kk].x & 0xffff0000u))),
+                                         fmaxf(fabsf(__uint_as_float(w[kk].y << 16)), fabsf(__uint_as_float(w[kk].y & 0xffff0000u)))));
             }
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
             amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
             int e = 0;
-            if (amax > 0.f && amax < INFINITY) e = (int)floorf(__log2f(224.f / amax));
-            e = max(-100, min(100, e));
+            if (amax > 0.f && amax < INFINITY) e = (int)floorf(__log2f(16384.f / amax));
+            e = max(-120, min(120, e));
             const float alpha = exp2f((float)e);  // exact power of two
 #pragma unroll
-            for (int st = 0; st < NS; ++st) {
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    float x[4];
-                    load4(32 * st + 16 * hh + 4 * t, x);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) x[i] *= alpha;
-                    // three successive e4m3 roundings of the remaining residual
-                    uint32_t term[3];
-#pragma unroll
-                    for (int k3 = 0; k3 < 3; ++k3) {
-                        const uint16_t c01 = f32x2_to_e4m3x2(x[0], x[1]), c23 = f32x2_to_e4m3x2(x[2], x[3]);
-                        const uint32_t d01 = e4m3x2_to_f16x2(c01), d23 = e4m3x2_to_f16x2(c23);
-                        x[0] -= f16_lo_to_f32(d01);
-                        x[1] -= f16_hi_to_f32(d01);
-                        x[2] -= f16_lo_to_f32(d23);
-                        x[3] -= f16_hi_to_f32(d23);
-                        term[k3] = (uint32_t)c01 | ((uint32_t)c23 << 16);
-                    }
-                    qh[st][hh] = term[0];
-                    qm[st][hh] = term[1];
-                    ql[st][hh] = term[2];
-                }
+            for (int kk = 0; kk < NK; ++kk) {
+                qf[kk][0] = pack2<false>(__uint_as_float(w[kk].x << 16) * alpha, __uint_as_float(w[kk].x & 0xffff0000u) * alpha);
+                qf[kk][1] = pack2<false>(__uint_as_float(w[kk].y << 16) * alpha, __uint_as_float(w[kk].y & 0xffff0000u) * alpha);
             }
             // columns 2t, 2t+1 of the score fragment belong to heads 2t, 2t+1
             qs0 = 1.f / __shfl_sync(0xffffffffu, alpha, (2 * t) * 4);
@@ -495,9 +459,8 @@ pa_v2_phase1_kernel(const Phase1Params p) {
         if (2 * t + 1 < nh) sl1 = p.alibi[h0 + 2 * t + 1] * kLog2e;
     }
     const float qk_mul = p.qk_scale_log2;
-    const float qk_mul0 = qk_mul * qs0, qk_mul1 = qk_mul * qs1;  // fp8: per-column query scale
-    // fp8: P enters the P.V product as e4m3 of P * 256
-    const float v_mul = FP8 ? p.v_scale * (1.f / 256.f) : p.v_scale;
+    const float qk_mul0 = qk_mul * qs0, qk_mul1 = qk_mul * qs1;  // fp8 with a bf16 query: per-column scale
+    const float v_mul = p.v_scale;
 
     // Per-lane ldmatrix row of the K page: token within the 16-token tile, chunk offset.
     const int k_tok = FP8 ? c_fp8_row_token[(lane & 7) + 8 * ((lane >> 3) & 1)] : (lane & 7) + 8 * ((lane >> 3) & 1);
@@ -573,7 +536,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
                 float sv[2][4];
 #pragma unroll
                 for (int tile = 0; tile < 2; ++tile) {
-                    // S^T = K . Q^T on the e4m3 codes; rows are tokens in c_fp8_row_token order
+                    // S^T = K . Q^T with K widened to f16; rows are tokens in c_fp8_row_token order
                     const int tt = tile * 16 + k_tok;
                     const uint32_t krow = kbase + (uint32_t)(tt >> bs_log2) * page_bytes +
                                           (uint32_t)(k_chunk * bs + (tt & (bs - 1))) * 16u;
@@ -589,20 +552,14 @@ pa_v2_phase1_kernel(const Phase1Params p) {
                             ldsm_x2(krow + (uint32_t)st * 32u * bs, a0, a1);
                             a2 = a3 = 0u;
                         }
-                        if constexpr (Q8) {
-                            mma_e4m3_16832(sc, a0, a1, a2, a3, qh[st][0], qh[st][1]);
-                            mma_e4m3_16832(sd, a0, a1, a2, a3, qm[st][0], qm[st][1]);
-                            mma_e4m3_16832(st & 1 ? sd : sc, a0, a1, a2, a3, ql[st][0], ql[st][1]);
-                        } else {
-                            // widen the K codes to f16 (exact): chunk 2st in a0/a1, 2st+1 in a2/a3
-                            mma16816<false>(sc, e4m3x2_to_f16x2(lo16(a0)), e4m3x2_to_f16x2(lo16(a1)),
-                                            e4m3x2_to_f16x2(hi16(a0)), e4m3x2_to_f16x2(hi16(a1)),
-                                            qf[2 * st][0], qf[2 * st][1]);
-                            if (2 * st + 1 < NK)
-                                mma16816<false>(sd, e4m3x2_to_f16x2(lo16(a2)), e4m3x2_to_f16x2(lo16(a3)),
-                                                e4m3x2_to_f16x2(hi16(a2)), e4m3x2_to_f16x2(hi16(a3)),
-                                                qf[2 * st + 1][0], qf[2 * st + 1][1]);
-                        }
+                        // widen the K codes to f16 (exact): chunk 2st in a0/a1, 2st+1 in a2/a3
+                        mma16816<false>(sc, e4m3x2_to_f16x2(lo16(a0)), e4m3x2_to_f16x2(lo16(a1)),
+                                        e4m3x2_to_f16x2(hi16(a0)), e4m3x2_to_f16x2(hi16(a1)), qf[2 * st][0],
+                                        qf[2 * st][1]);
+                        if (2 * st + 1 < NK)
+                            mma16816<false>(sd, e4m3x2_to_f16x2(lo16(a2)), e4m3x2_to_f16x2(lo16(a3)),
+                                            e4m3x2_to_f16x2(hi16(a2)), e4m3x2_to_f16x2(hi16(a3)), qf[2 * st + 1][0],
+                                            qf[2 * st + 1][1]);
                     }
 #pragma unroll
                     for (int i = 0; i < 4; ++i) sc[i] += sd[i];
@@ -658,26 +615,22 @@ pa_v2_phase1_kernel(const Phase1Params p) {
                 }
                 m0 = mn0;
                 m1 = mn1;
-                // P^T operand: P * 256 as f16, transposed with movmatrix, split into e4m3 hi + lo.
-                // After the transpose thread t holds tokens {4t..4t+3} of head g (rows 2t, 2t+1
-                // and 8+2t, 9+2t in the token order above; the halves swap for t >= 2).
-                uint32_t bh[2], bl[2];
+                // P^T operand in f16, transposed with movmatrix.  After the transpose thread t
+                // holds P of tokens {4t..4t+3} of head g (rows 2t, 2t+1 and 8+2t, 9+2t in the
+                // token order above; the two halves swap for t >= 2).
+                uint32_t pb[2][2];
 #pragma unroll
                 for (int tile = 0; tile < 2; ++tile) {
-                    const uint32_t x0 = movm_trans(pack2<false>(pv[tile][0] * 256.f, pv[tile][1] * 256.f));
-                    const uint32_t x1 = movm_trans(pack2<false>(pv[tile][2] * 256.f, pv[tile][3] * 256.f));
-                    uint16_t h0, l0b, h1, l1b;
-                    split_e4m3x2(x0, h0, l0b);
-                    split_e4m3x2(x1, h1, l1b);
-                    if (t < 2) {
-                        bh[tile] = (uint32_t)h0 | ((uint32_t)h1 << 16);
-                        bl[tile] = (uint32_t)l0b | ((uint32_t)l1b << 16);
-                    } else {
-                        bh[tile] = (uint32_t)h1 | ((uint32_t)h0 << 16);
-                        bl[tile] = (uint32_t)l1b | ((uint32_t)l0b << 16);
-                    }
+                    const uint32_t x0 = movm_trans(pack2<false>(pv[tile][0], pv[tile][1]));
+                    const uint32_t x1 = movm_trans(pack2<false>(pv[tile][2], pv[tile][3]));
+                    pb[tile][0] = t < 2 ? x0 : x1;  // tokens 4t, 4t + 1
+                    pb[tile][1] = t < 2 ? x1 : x0;  // tokens 4t + 2, 4t + 3
                 }
-                // O^T += V^T . P^T: V rows straight from the page, 32 tokens per step
+                // O^T += V^T . P^T in f16: the V codes of a row (four consecutive tokens per
+                // register, straight from the page) widened to f16 in registers (exact); for
+                // the m16n8k16 step of tile u, k = 2t, 2t + 1, 2t + 8, 2t + 9 stand for tokens
+                // 4t .. 4t + 3 of the tile, on both operands.  (The e4m3 tensor path, with P
+                // split into two e4m3 terms, measured slower on this GPU.)
                 uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;  // bytes of masked tokens -> 0
                 if (!full) {
                     mlo = 0u;
@@ -688,30 +641,27 @@ pa_v2_phase1_kernel(const Phase1Params p) {
                         if (tok_ok(16 + 4 * t + i)) mhi |= 0xffu << (8 * i);
                     }
                 }
+                auto pv_step = [&](float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3) {
+                    mma16816<false>(c, e4m3x2_to_f16x2(lo16(a0)), e4m3x2_to_f16x2(lo16(a1)), e4m3x2_to_f16x2(hi16(a0)),
+                                    e4m3x2_to_f16x2(hi16(a1)), pb[0][0], pb[0][1]);
+                    mma16816<false>(c, e4m3x2_to_f16x2(lo16(a2)), e4m3x2_to_f16x2(lo16(a3)), e4m3x2_to_f16x2(hi16(a2)),
+                                    e4m3x2_to_f16x2(hi16(a3)), pb[1][0], pb[1][1]);
+                };
                 if (bs >= 16) {
                     const int vr = (lane & 7) + 8 * ((lane >> 3) & 1);
                     const int tk = 16 * (lane >> 4);  // token half of this lane's matrix row
                     const uint32_t vrow = vbase + (uint32_t)(tk >> bs_log2) * page_bytes + (uint32_t)(vr * bs + (tk & (bs - 1)));
-                    if (full) {
 #pragma unroll
-                        for (int mt = 0; mt < NK; ++mt) {
-                            uint32_t a0, a1, a2, a3;
-                            ldsm_x4(vrow + (uint32_t)mt * 16u * bs, a0, a1, a2, a3);
-                            mma_e4m3_16832(acc[mt], a0, a1, a2, a3, bh[0], bh[1]);
-                            mma_e4m3_16832(acc[mt], a0, a1, a2, a3, bl[0], bl[1]);
-                        }
-                    } else {
-#pragma unroll
-                        for (int mt = 0; mt < NK; ++mt) {
-                            uint32_t a0, a1, a2, a3;
-                            ldsm_x4(vrow + (uint32_t)mt * 16u * bs, a0, a1, a2, a3);
+                    for (int mt = 0; mt < NK; ++mt) {
+                        uint32_t a0, a1, a2, a3;
+                        ldsm_x4(vrow + (uint32_t)mt * 16u * bs, a0, a1, a2, a3);
+                        if (!full) {
                             a0 &= mlo;
                             a1 &= mlo;
                             a2 &= mhi;
                             a3 &= mhi;
-                            mma_e4m3_16832(acc[mt], a0, a1, a2, a3, bh[0], bh[1]);
-                            mma_e4m3_16832(acc[mt], a0, a1, a2, a3, bl[0], bl[1]);
                         }
+                        pv_step(acc[mt], a0, a1, a2, a3);
                     }
                 } else {
                     // block size 8: a V row holds 8 tokens, so read each thread's 4 tokens
@@ -720,10 +670,8 @@ pa_v2_phase1_kernel(const Phase1Params p) {
 #pragma unroll
                     for (int mt = 0; mt < NK; ++mt) {
                         const uint32_t r0 = (uint32_t)(mt * 16 + g) * bs, r1 = r0 + 8u * bs;
-                        const uint32_t a0 = lds_u32(va + r0) & mlo, a1 = lds_u32(va + r1) & mlo;
-                        const uint32_t a2 = lds_u32(vb + r0) & mhi, a3 = lds_u32(vb + r1) & mhi;
-                        mma_e4m3_16832(acc[mt], a0, a1, a2, a3, bh[0], bh[1]);
-                        mma_e4m3_16832(acc[mt], a0, a1, a2, a3, bl[0], bl[1]);
+                        pv_step(acc[mt], lds_u32(va + r0) & mlo, lds_u32(va + r1) & mlo, lds_u32(vb + r0) & mhi,
+                                lds_u32(vb + r1) & mhi);
                     }
                 }
             } else {

@@ -163,16 +163,6 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
     }
 }
 
-// fp8 e4m3 x e4m3 -> fp32, m16n8k32: each 32-bit A/B register holds four consecutive k.
-__device__ __forceinline__ void mma_e4m3_16832(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                               uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, "
-        "{%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-
 // ---- conversions ------------------------------------------------------------------------
 // Two floats -> packed 16-bit pair, `lo` in the low half.
 template <bool BF16>
@@ -200,15 +190,6 @@ __device__ __forceinline__ float f16_hi_to_f32(uint32_t v) {
     asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tcvt.f32.f16 %0, hi;\n\t}" : "=f"(f) : "r"(v));
     return f;
 }
-// Two e4m3fn codes -> packed pair in the MMA type (exact for both f16 and bf16).
-template <bool BF16>
-__device__ __forceinline__ uint32_t e4m3x2_to_mma(uint16_t v) {
-    const uint32_t h = e4m3x2_to_f16x2(v);
-    if constexpr (BF16)
-        return pack2<true>(f16_lo_to_f32(h), f16_hi_to_f32(h));
-    else
-        return h;
-}
 __device__ __forceinline__ uint16_t lo16(uint32_t v) { return static_cast<uint16_t>(v & 0xffffu); }
 __device__ __forceinline__ uint16_t hi16(uint32_t v) { return static_cast<uint16_t>(v >> 16); }
 
@@ -217,24 +198,6 @@ __device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
     uint16_t d;
     asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(d) : "f"(hi), "f"(lo));
     return d;
-}
-
-// f16x2 -> two e4m3fn codes (RNE, saturating); the low half becomes the low byte.
-__device__ __forceinline__ uint16_t f16x2_to_e4m3x2(uint32_t v) {
-    uint16_t d;
-    asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(d) : "r"(v));
-    return d;
-}
-__device__ __forceinline__ uint32_t hsub2(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-// A value split into two e4m3 terms, hi + lo: hi = e4m3(v), lo = e4m3(v - hi).  For the
-// f16x2 pair v the residual is exact in f16 (hi is within 2^-4 of v).
-__device__ __forceinline__ void split_e4m3x2(uint32_t v, uint16_t& hi, uint16_t& lo) {
-    hi = f16x2_to_e4m3x2(v);
-    lo = f16x2_to_e4m3x2(hsub2(v, e4m3x2_to_f16x2(hi)));
 }
 
 __device__ __forceinline__ float ex2(float x) {
