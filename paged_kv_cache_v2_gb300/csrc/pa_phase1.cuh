@@ -553,13 +553,16 @@ pa_v2_phase1_kernel(const Phase1Params p) {
                             a2 = a3 = 0u;
                         }
                         // widen the K codes to f16 (exact): chunk 2st in a0/a1, 2st+1 in a2/a3
-                        mma16816<false>(sc, e4m3x2_to_f16x2(lo16(a0)), e4m3x2_to_f16x2(lo16(a1)),
-                                        e4m3x2_to_f16x2(hi16(a0)), e4m3x2_to_f16x2(hi16(a1)), qf[2 * st][0],
-                                        qf[2 * st][1]);
-                        if (2 * st + 1 < NK)
-                            mma16816<false>(sd, e4m3x2_to_f16x2(lo16(a2)), e4m3x2_to_f16x2(lo16(a3)),
-                                            e4m3x2_to_f16x2(hi16(a2)), e4m3x2_to_f16x2(hi16(a3)), qf[2 * st + 1][0],
-                                            qf[2 * st + 1][1]);
+                        uint32_t w0l, w0h, w1l, w1h;
+                        e4m3x4_to_f16x2x2(a0, w0l, w0h);
+                        e4m3x4_to_f16x2x2(a1, w1l, w1h);
+                        mma16816<false>(sc, w0l, w1l, w0h, w1h, qf[2 * st][0], qf[2 * st][1]);
+                        if (2 * st + 1 < NK) {
+                            uint32_t w2l, w2h, w3l, w3h;
+                            e4m3x4_to_f16x2x2(a2, w2l, w2h);
+                            e4m3x4_to_f16x2x2(a3, w3l, w3h);
+                            mma16816<false>(sd, w2l, w3l, w2h, w3h, qf[2 * st + 1][0], qf[2 * st + 1][1]);
+                        }
                     }
 #pragma unroll
                     for (int i = 0; i < 4; ++i) sc[i] += sd[i];
@@ -642,10 +645,13 @@ pa_v2_phase1_kernel(const Phase1Params p) {
                     }
                 }
                 auto pv_step = [&](float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3) {
-                    mma16816<false>(c, e4m3x2_to_f16x2(lo16(a0)), e4m3x2_to_f16x2(lo16(a1)), e4m3x2_to_f16x2(hi16(a0)),
-                                    e4m3x2_to_f16x2(hi16(a1)), pb[0][0], pb[0][1]);
-                    mma16816<false>(c, e4m3x2_to_f16x2(lo16(a2)), e4m3x2_to_f16x2(lo16(a3)), e4m3x2_to_f16x2(hi16(a2)),
-                                    e4m3x2_to_f16x2(hi16(a3)), pb[1][0], pb[1][1]);
+                    uint32_t x0l, x0h, x1l, x1h, x2l, x2h, x3l, x3h;
+                    e4m3x4_to_f16x2x2(a0, x0l, x0h);
+                    e4m3x4_to_f16x2x2(a1, x1l, x1h);
+                    e4m3x4_to_f16x2x2(a2, x2l, x2h);
+                    e4m3x4_to_f16x2x2(a3, x3l, x3h);
+                    mma16816<false>(c, x0l, x1l, x0h, x1h, pb[0][0], pb[0][1]);
+                    mma16816<false>(c, x2l, x3l, x2h, x3h, pb[1][0], pb[1][1]);
                 };
                 if (bs >= 16) {
                     const int vr = (lane & 7) + 8 * ((lane >> 3) & 1);
