@@ -697,18 +697,22 @@ pa_v2_phase1_kernel(const Phase1Params p) {
                         krow = kbase + (uint32_t)(k_chunk * bs + tile * 16 + k_tok) * 16u;
                     else
                         krow = kbase + (uint32_t)(k_tok >> 3) * page_bytes + (uint32_t)(k_chunk * bs + (k_tok & 7)) * 16u;
-                    float sc[4] = {0.f, 0.f, 0.f, 0.f};
-    #pragma unroll
-                        for (int kk = 0; kk < NK; ++kk) {
-                            uint32_t a0, a1, a2, a3;
-                            if (HALF_STEP && kk == NK - 1) {
-                                ldsm_x2(krow + (uint32_t)kk * 32u * bs, a0, a1);
-                                a2 = a3 = 0u;
-                            } else {
-                                ldsm_x4(krow + (uint32_t)kk * 32u * bs, a0, a1, a2, a3);
-                            }
-                            mma16816<BF16>(sc, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+                    // two accumulators (even and odd steps): two MMA dependency chains of half
+                    // the length, which matters when few warps share a scheduler (small batches)
+                    float sc[4] = {0.f, 0.f, 0.f, 0.f}, sd[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int kk = 0; kk < NK; ++kk) {
+                        uint32_t a0, a1, a2, a3;
+                        if (HALF_STEP && kk == NK - 1) {
+                            ldsm_x2(krow + (uint32_t)kk * 32u * bs, a0, a1);
+                            a2 = a3 = 0u;
+                        } else {
+                            ldsm_x4(krow + (uint32_t)kk * 32u * bs, a0, a1, a2, a3);
                         }
+                        mma16816<BF16>(kk & 1 ? sd : sc, a0, a1, a2, a3, qf[kk][0], qf[kk][1]);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) sc[i] += sd[i];
 
                     // ---- scores in base-2 units, masking, online softmax ---------------------------
                     float s0 = sc[0] * qk_mul, s1 = sc[1] * qk_mul;
