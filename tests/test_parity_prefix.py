@@ -112,6 +112,25 @@ def test_out_of_range_page_is_masked_and_flagged():
     check_prefix(wl, out, oracle.prefix_workload(ref_wl), label="masked page")
 
 
+def test_bf16_values_beyond_f16_range_are_flagged():
+    # head sizes up to 128 run the value product in f16 (the value tiles are converted); a
+    # bf16 value the f16 range cannot hold saturates and is flagged (bit 9), a large one it
+    # can hold is exact
+    wl = workloads.build_prefix(num_seqs=2, num_heads=8, num_kv_heads=2, head_size=128, block_size=16,
+                                context_lens=[300, 70], query_lens=[40, 9], q_dtype="bf16", seed=810)
+    big = wl.value_cache.clone()
+    b0 = int(wl.block_tables[0, 3])  # context tokens 48..63 of sequence 0
+    big[b0, 1, 7, 5] = 60160.0       # exact in bf16 and in f16
+    wl_big = workloads.PrefixWorkload(**{**wl.__dict__, "value_cache": big})
+    out = run_prefix(wl_big)
+    assert pa.pa_get_device_errors() == 0
+    check_prefix(wl_big, out, oracle.prefix_workload(wl_big), label="large bf16 value")
+    huge = wl.value_cache.clone()
+    huge[b0, 1, 7, 5] = 1.0e5        # beyond +-65504
+    run_prefix(workloads.PrefixWorkload(**{**wl.__dict__, "value_cache": huge}))
+    assert pa.pa_get_device_errors() & 512
+
+
 def test_context_longer_than_table_is_capped_and_flagged():
     wl = workloads.build_prefix(num_seqs=1, num_heads=4, num_kv_heads=1, head_size=64, block_size=16,
                                 context_lens=[64], query_lens=[10], table_width=5, seed=900)
