@@ -17,7 +17,7 @@ import torch
 import oracle
 import paged_kv_cache_v2_gb300 as pa
 import workloads
-from gpu_harness import check_prefix, prefix_sample_rows, prefix_to_device, run_prefix
+from gpu_harness import half_ulp, check_prefix, prefix_sample_rows, prefix_to_device, run_prefix
 
 pytestmark = pytest.mark.gpu
 
@@ -122,9 +122,13 @@ def test_bf16_values_beyond_f16_range_are_flagged():
     b0 = int(wl.block_tables[0, 3])  # context tokens 48..63 of sequence 0
     big[b0, 1, 7, 5] = 60160.0       # exact in bf16 and in f16
     wl_big = workloads.PrefixWorkload(**{**wl.__dict__, "value_cache": big})
-    out = run_prefix(wl_big)
+    out = run_prefix(wl_big).double().numpy()
     assert pa.pa_get_device_errors() == 0
-    check_prefix(wl_big, out, oracle.prefix_workload(wl_big), label="large bf16 value")
+    # outputs reach ~1e2 here, so the bar is relative: P enters in f16 (2^-11), the output is
+    # rounded to bf16
+    ref = oracle.prefix_workload(wl_big)
+    assert np.isfinite(out).all()
+    assert np.all(np.abs(out - ref) <= 2e-3 * np.maximum(1.0, np.abs(ref)) + half_ulp(ref, "bf16"))
     huge = wl.value_cache.clone()
     huge[b0, 1, 7, 5] = 1.0e5        # beyond +-65504
     run_prefix(workloads.PrefixWorkload(**{**wl.__dict__, "value_cache": huge}))
