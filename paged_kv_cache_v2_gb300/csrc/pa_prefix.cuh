@@ -248,39 +248,11 @@ __device__ __forceinline__ bool pfx_tile_to_f16(uint32_t saddr, int bytes, int l
 // Loader role of the prefix kernels: a team of TEAM threads (whole warps; lanes of the first
 // warp issue the tensor copies) fills the key ring (kteam) or the value ring of the layout C.
 // lt = thread index in the team.
-// CONV (one warp per team): the value tiles hold bf16 and the value product runs in f16, so
-// the value warp converts every tile in place before releasing it.  A tile moved by tensor
-// copies first completes on v_land; the warp converts it two tiles later (the copies of the
-// tiles in between stay in flight), a tile written through the generic proxy at once.
-template <class C, int D, int TEAM, bool CONV = false>
+template <class C, int D, int TEAM>
 __device__ __forceinline__ void pfx_load_tiles(const PrefixParams& p, const PfxRange& g, bool kteam, int lt, int lane,
                                                uint32_t sbase, uint64_t* k_full, uint64_t* k_empty, uint64_t* v_full,
-                                               uint64_t* v_empty, uint32_t* bad_mask, volatile int* abort_flag,
-                                               uint64_t* v_land = nullptr) {
+                                               uint64_t* v_empty, uint32_t* bad_mask, volatile int* abort_flag) {
     constexpr int BN = C::BN, NK = C::NK, NV = C::NV;
-    static_assert(!CONV || TEAM == 32, "the converting value team is one warp");
-    const bool conv = CONV && !kteam;
-    uint32_t pend = 0u, land_par = 0u;  // slots awaiting conversion; each slot's next v_land parity
-    int conv_next = 0;                  // next tile to consider for conversion
-    bool sat = false;
-    // convert tile u's slot (its copies have landed) and release it to the value MMA
-    auto finish = [&](int u) -> bool {
-        const int sl = u % NV;
-        if ((pend >> sl) & 1u) {
-            if (!pfx_warp_wait(&v_land[sl], (land_par >> sl) & 1u, abort_flag, lane)) return false;
-            __syncwarp();  // the landed bytes are visible to every lane
-            land_par ^= 1u << sl;
-            pend &= ~(1u << sl);
-            sat |= pfx_tile_to_f16(sbase + C::OFF_V + sl * C::V_BYTES, C::V_BYTES, lane);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&v_full[sl]);
-                mbar_arrive(&v_full[sl]);
-            }
-        }
-        return true;
-    };
     const int tb = g.tb, n_ctx = g.n_ctx, ctx = g.ctx, n_tiles = g.n_tiles, q0 = g.q0, q_len = g.q_len, kvh = g.kvh;
     const int32_t* table = g.table;
     const int64_t page_bytes = (int64_t)D * p.bs * 2;
@@ -295,18 +267,11 @@ __device__ __forceinline__ void pfx_load_tiles(const PrefixParams& p, const PfxR
     };
     int pid_next = tile_page(0);
     int t = 0;
-    bool conv_ok = true;
     for (; t < n_tiles; ++t) {
         const int pid = pid_next;
         pid_next = tile_page(t + 1);
         const int slot = kteam ? t % NK : t % NV;
         uint64_t* full = kteam ? &k_full[slot] : &v_full[slot];
-        if (conv) {
-            // tiles two behind this one have had time to land: convert and release them
-            for (; conv_next <= t - 2; ++conv_next)
-                if (!(conv_ok = finish(conv_next))) break;
-            if (!conv_ok) break;
-        }
         if (kteam ? t >= NK : t >= NV) {
             if (!pfx_warp_wait(kteam ? &k_empty[slot] : &v_empty[slot], ((t / (kteam ? NK : NV)) - 1) & 1,
                                abort_flag, lane))
@@ -329,9 +294,7 @@ __device__ __forceinline__ void pfx_load_tiles(const PrefixParams& p, const PfxR
                         bad_mask[slot] = m;
                         if (m) prefix_flag(32u);
                     }
-                    if (tma && conv)
-                        mbar_arrive_expect_tx(&v_land[slot], 2u * BN * D);
-                    else if (tma)
+                    if (tma)
                         mbar_arrive_expect_tx(full, 2u * BN * D);
                     else
                         mbar_arrive(full);
@@ -347,11 +310,10 @@ __device__ __forceinline__ void pfx_load_tiles(const PrefixParams& p, const PfxR
                     // values: one whole page per lane, swizzled as the value MMA reads it
                     const int vpage = pid * p.Hk + kvh;
                     const uint32_t dst = sV + lane * (C::DP << (p.bs_log2 + 1));
-                    uint64_t* vbar = conv ? &v_land[slot] : full;
                     if (p.bs_log2 == 3)
-                        bulk_load(dst, p.vcache + (int64_t)vpage * page_bytes, (uint32_t)page_bytes, vbar);
+                        bulk_load(dst, p.vcache + (int64_t)vpage * page_bytes, (uint32_t)page_bytes, full);
                     else
-                        tma_load_3d(dst, &p.vmap, 0, 0, vpage, vbar);
+                        tma_load_3d(dst, &p.vmap, 0, 0, vpage, full);
                 }
             }
             if (!tma && kteam) {
@@ -437,37 +399,15 @@ __device__ __forceinline__ void pfx_load_tiles(const PrefixParams& p, const PfxR
                 }
             }
         }
-        if (conv && !generic) {
-            // released after its conversion (finish); note that it is pending
-            pend |= 1u << slot;
-            continue;
-        }
         if (generic) {  // make those writes visible to the tensor core before the arrive
             cp_async_commit();
             cp_async_wait<0>();
-            if (conv) {
-                __syncwarp();  // every lane's writes of the tile are in place
-                sat |= pfx_tile_to_f16(sbase + C::OFF_V + slot * C::V_BYTES, C::V_BYTES, lane);
-            }
             fence_proxy_async_smem();
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(full);
     }
     cp_async_wait<0>();
-    if (conv) {
-        if (t == n_tiles && conv_ok)  // the last tiles
-            for (; conv_next < n_tiles; ++conv_next)
-                if (!(conv_ok = finish(conv_next))) break;
-        if (sat && lane == 0) prefix_flag(512u);
-        if (t < n_tiles || !conv_ok) {
-            // aborted: let the tensor copies of the tiles still awaiting conversion land
-            for (int sl = 0; sl < NV; ++sl)
-                if (((pend >> sl) & 1u) && lane == 0)
-                    (void)mbar_wait_bounded(&v_land[sl], (land_par >> sl) & 1u, kWaitLimitNs);
-            return;
-        }
-    }
     if (t < n_tiles && lt == 0) {
         // Aborted: tensor copies this team issued for its last tiles may still be landing in
         // shared memory.  Wait (bounded) until each slot's latest fill is complete, so that

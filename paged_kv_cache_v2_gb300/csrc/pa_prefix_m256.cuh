@@ -8,7 +8,7 @@
 // softmax writes P (in f16: with bf16 inputs the value warp converts every value tile to f16
 // in shared memory) back into the S buffer it has just read, and the score MMA
 // of tile t + 2 reuses that buffer only after the value MMA of tile t has completed.  Q of both
-// groups sits in shared memory.  Fourteen warps:
+// groups sits in shared memory.  Fifteen warps:
 //   warp 0         allocates tensor memory; lane 0 issues group 0's score MMAs
 //   warp 1         lane 0 issues group 0's value MMAs
 //   warp 2 / 3     fill the key / the value ring (the loader of pa_prefix.cuh, one warp each)
@@ -16,6 +16,9 @@
 //   warps 8-11     softmax of group 1
 //   warps 12 / 13  lane 0 issues group 1's score / value MMAs (a lane per group and product:
 //                  a lane waiting on one group does not hold up the other group's MMAs)
+//   warp 14        bf16 inputs: converts each value tile to f16 in place once it has landed
+//                  (v_land) and releases it to the value MMAs (v_full), so the loader keeps
+//                  running ahead
 // so each sub-partition runs two softmax warps, and while one group turns its scores into
 // probabilities the tensor core works on the other group's products.
 #pragma once
@@ -24,10 +27,11 @@
 
 namespace pa {
 
-constexpr int kP2Threads = 14 * 32;
+constexpr int kP2Threads = 15 * 32;
 constexpr int kP2Rows = 256;
 constexpr int kP2MmaWarp = 0, kP2PvWarp = 1, kP2KeyWarp = 2, kP2ValWarp = 3, kP2SoftmaxWarp0 = 4;
 constexpr int kP2MmaWarp1 = 12, kP2PvWarp1 = 13;  // group 1's score / value lanes
+constexpr int kP2ConvWarp = 14;                   // bf16 inputs: converts value tiles to f16
 
 template <bool BF16, int D>
 struct Pfx2Cfg {
@@ -130,9 +134,9 @@ __global__ void __launch_bounds__(kP2Threads, 1) pa_prefix_m256_kernel(const __g
             mbar_init(&k_empty[i], 5 * ng);  // each group's score-MMA commit and its softmax warps
         }
         for (int i = 0; i < NV; ++i) {
-            mbar_init(&v_full[i], 2);
-            mbar_init(&v_empty[i], ng);  // each group's value-MMA commit
-            mbar_init(&v_land[i], 1);    // the copy arrive (+ bytes)
+            mbar_init(&v_full[i], C::PV16 ? 1 : 2);  // the converter, or the copy arrive (+ bytes) and the loader
+            mbar_init(&v_empty[i], ng);              // each group's value-MMA commit
+            mbar_init(&v_land[i], 2);                // (PV16) the copy arrive (+ bytes) and the loader
         }
         for (int i = 0; i < 4; ++i) {
             mbar_init(&s_full[i], 1);
@@ -156,8 +160,24 @@ __global__ void __launch_bounds__(kP2Threads, 1) pa_prefix_m256_kernel(const __g
 
     if (warp == kP2KeyWarp || warp == kP2ValWarp) {
         // ------------------------------------------------------------------ loaders
-        pfx_load_tiles<C, D, 32, C::PV16>(p, rng, warp == kP2KeyWarp, lane, lane, sbase, k_full, k_empty, v_full,
-                                          v_empty, bad_mask, abort_flag, v_land);
+        // with bf16 inputs the value tiles land on v_land for the converter warp
+        pfx_load_tiles<C, D, 32>(p, rng, warp == kP2KeyWarp, lane, lane, sbase, k_full, k_empty,
+                                 C::PV16 ? v_land : v_full, v_empty, bad_mask, abort_flag);
+    } else if (warp == kP2ConvWarp) {
+        // ------------------------------------------------------------------ value converter
+        if constexpr (C::PV16) {
+            bool sat = false;
+            for (int t = 0; t < n_tiles; ++t) {
+                const int sl = t % NV;
+                if (!pfx_warp_wait(&v_land[sl], (t / NV) & 1, abort_flag, lane)) break;
+                __syncwarp();
+                sat |= pfx_tile_to_f16(sbase + C::OFF_V + sl * C::V_BYTES, C::V_BYTES, lane);
+                fence_proxy_async_smem();  // the f16 tile is visible to the tensor core
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&v_full[sl]);
+            }
+            if (sat && lane == 0) prefix_flag(512u);
+        }
     } else if (warp == kP2MmaWarp || warp == kP2MmaWarp1) {
         // ------------------------------------------------------------------ score MMAs
         const int g = warp == kP2MmaWarp1 ? 1 : 0;
