@@ -328,9 +328,7 @@ PA_API pa_status pa_swap_blocks(const void* src_cache, void* dst_cache, const in
  * included).  On the device, a cached block id outside [0, num_blocks) masks that page (bit 5
  * of pa_get_device_errors); a context longer than the table row is capped to the row, as the
  * pages do (bit 6); a sequence with q_len > max_query_len or a negative length is skipped
- * (bit 7).  Head sizes up to 128 run the value product in f16 (bf16 value tiles are converted
- * in shared memory, exactly for |v| <= 65504): a bf16 value beyond that range saturates to
- * +-65504 and sets bit 9.
+ * (bit 7).
  */
 PA_API pa_status pa_prefix(void* output, const void* query, const void* key, const void* value,
                            const void* key_cache, const void* value_cache, int num_seqs,
@@ -358,7 +356,7 @@ PA_API const char* pa_status_string(pa_status status);
 /* Device-side error flags (bit 0: a block id outside [0, num_blocks) or a table row too
  * short; bit 1: a sequence longer than max_num_partitions * 512 or a negative length;
  * bit 2: a bounded wait for a shared-memory copy gave up; bit 3: a slot outside the
- * cache; bit 4: a pa_copy_blocks id outside the cache; bits 5-7 and 9: pa_prefix, see there).
+ * cache; bit 4: a pa_copy_blocks id outside the cache; bits 5-7: pa_prefix, see there).
  * Reads the flags of the current device (this synchronises the device) into
  * *flags, and clears them when reset != 0.  Not part of the pages' interface: it reports
  * what the kernels skipped instead of faulting. */

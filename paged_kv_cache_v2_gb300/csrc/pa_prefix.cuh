@@ -229,22 +229,6 @@ struct PfxRange {
     const int32_t* table;  // the sequence's block-table row
 };
 
-// bf16 -> f16 in place over `bytes` of shared memory (16-byte words), by one warp.  Returns
-// (on every lane) whether some element lay beyond the f16 range (|x| >= 65536 in bf16,
-// which then saturates to +-65504).
-__device__ __forceinline__ bool pfx_tile_to_f16(uint32_t saddr, int bytes, int lane) {
-    uint32_t big = 0u;
-#pragma unroll 4
-    for (int i = lane * 16; i < bytes; i += 32 * 16) {
-        uint4 w = lds_v4(saddr + i);
-        big |= __vcmpgeu2(w.x & 0x7fff7fffu, 0x47804780u) | __vcmpgeu2(w.y & 0x7fff7fffu, 0x47804780u) |
-               __vcmpgeu2(w.z & 0x7fff7fffu, 0x47804780u) | __vcmpgeu2(w.w & 0x7fff7fffu, 0x47804780u);
-        sts_v4(saddr + i, bf16x2_to_f16x2_sat(w.x), bf16x2_to_f16x2_sat(w.y), bf16x2_to_f16x2_sat(w.z),
-               bf16x2_to_f16x2_sat(w.w));
-    }
-    return __any_sync(0xffffffffu, big != 0u);
-}
-
 // Loader role of the prefix kernels: a team of TEAM threads (whole warps; lanes of the first
 // warp issue the tensor copies) fills the key ring (kteam) or the value ring of the layout C.
 // lt = thread index in the team.

@@ -5,10 +5,9 @@
 // The CTA's rows are two groups of 128 (rows j * G + g of the kv head's group, as there), and
 // both groups use every key/value tile the loaders bring in.  Tensor memory holds, per group,
 // two S buffers of 64 columns and O (head size <= 128 columns): 2 x 256 = all 512 columns.  The
-// softmax writes P (in f16: with bf16 inputs the value warp converts every value tile to f16
-// in shared memory) back into the S buffer it has just read, and the score MMA
+// softmax writes P (bf16: hi and lo) back into the S buffer it has just read, and the score MMA
 // of tile t + 2 reuses that buffer only after the value MMA of tile t has completed.  Q of both
-// groups sits in shared memory.  Fifteen warps:
+// groups sits in shared memory.  Fourteen warps:
 //   warp 0         allocates tensor memory; lane 0 issues group 0's score MMAs
 //   warp 1         lane 0 issues group 0's value MMAs
 //   warp 2 / 3     fill the key / the value ring (the loader of pa_prefix.cuh, one warp each)
@@ -16,9 +15,6 @@
 //   warps 8-11     softmax of group 1
 //   warps 12 / 13  lane 0 issues group 1's score / value MMAs (a lane per group and product:
 //                  a lane waiting on one group does not hold up the other group's MMAs)
-//   warp 14        bf16 inputs: converts each value tile to f16 in place once it has landed
-//                  (v_land) and releases it to the value MMAs (v_full), so the loader keeps
-//                  running ahead
 // so each sub-partition runs two softmax warps, and while one group turns its scores into
 // probabilities the tensor core works on the other group's products.
 #pragma once
@@ -27,11 +23,10 @@
 
 namespace pa {
 
-constexpr int kP2Threads = 15 * 32;
+constexpr int kP2Threads = 14 * 32;
 constexpr int kP2Rows = 256;
 constexpr int kP2MmaWarp = 0, kP2PvWarp = 1, kP2KeyWarp = 2, kP2ValWarp = 3, kP2SoftmaxWarp0 = 4;
 constexpr int kP2MmaWarp1 = 12, kP2PvWarp1 = 13;  // group 1's score / value lanes
-constexpr int kP2ConvWarp = 14;                   // bf16 inputs: converts value tiles to f16
 
 template <bool BF16, int D>
 struct Pfx2Cfg {
@@ -40,10 +35,7 @@ struct Pfx2Cfg {
     static constexpr int NCR = D / 8;
     static constexpr int NCP = DP / 8;
     static constexpr int BN = 64;
-    // bf16 inputs: the value warp converts every value tile to f16 in shared memory, so P
-    // enters the value product as one f16 term (the score product stays in bf16)
-    static constexpr bool PV16 = BF16;
-    static constexpr int NP = 1;
+    static constexpr int NP = BF16 ? 2 : 1;
     static constexpr int K_BYTES = BN * DP * 2;
     static constexpr int V_BYTES = BN * DP * 2;
     static constexpr int QG_BYTES = kPfxBM * DP * 2;  // one group's Q: [chunk][128 rows][16 bytes]
@@ -63,7 +55,7 @@ struct Pfx2Cfg {
     // tensor memory of group g at g * 256: S buffers [0, 64) and [64, 128), O [128, 128 + DPR)
     static constexpr uint32_t TMEM_COLS = 512, COL_O = 128;
     static constexpr uint32_t IDESC_S = umma_idesc_f16(BF16, kPfxBM, BN);
-    static constexpr uint32_t IDESC_O = umma_idesc_f16(false, kPfxBM, DP);  // P and V in f16
+    static constexpr uint32_t IDESC_O = umma_idesc_f16(BF16, kPfxBM, DP);
     static_assert(DPR <= 128, "two groups' S buffers and O fill the 512 columns only up to head size 128");
     static_assert(NK >= 2 && NV >= 2 && SMEM <= 227 * 1024, "shared memory");
 };
@@ -116,8 +108,7 @@ __global__ void __launch_bounds__(kP2Threads, 1) pa_prefix_m256_kernel(const __g
     uint64_t* o_done = p_full + 4;        // [2][2] value MMAs of the buffer's tile done
     uint64_t* q_full = o_done + 4;        // both groups' Q in shared memory
     uint64_t* fin = q_full + 1;           // [4] every MMA an issuing lane issued has completed
-    uint64_t* v_land = fin + 4;           // [NV] a value tile's tensor copies have landed (PV16)
-    constexpr int NBARS = 2 * NK + 3 * NV + 17;
+    constexpr int NBARS = 2 * NK + 2 * NV + 17;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctl + 8 * NBARS);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(ctl + 8 * NBARS + 4);
     uint32_t* bad_mask = reinterpret_cast<uint32_t*>(ctl + 8 * NBARS + 8);
@@ -134,9 +125,8 @@ __global__ void __launch_bounds__(kP2Threads, 1) pa_prefix_m256_kernel(const __g
             mbar_init(&k_empty[i], 5 * ng);  // each group's score-MMA commit and its softmax warps
         }
         for (int i = 0; i < NV; ++i) {
-            mbar_init(&v_full[i], C::PV16 ? 1 : 2);  // the converter, or the copy arrive (+ bytes) and the loader
-            mbar_init(&v_empty[i], ng);              // each group's value-MMA commit
-            mbar_init(&v_land[i], 2);                // (PV16) the copy arrive (+ bytes) and the loader
+            mbar_init(&v_full[i], 2);
+            mbar_init(&v_empty[i], ng);  // each group's value-MMA commit
         }
         for (int i = 0; i < 4; ++i) {
             mbar_init(&s_full[i], 1);
@@ -160,24 +150,8 @@ __global__ void __launch_bounds__(kP2Threads, 1) pa_prefix_m256_kernel(const __g
 
     if (warp == kP2KeyWarp || warp == kP2ValWarp) {
         // ------------------------------------------------------------------ loaders
-        // with bf16 inputs the value tiles land on v_land for the converter warp
-        pfx_load_tiles<C, D, 32>(p, rng, warp == kP2KeyWarp, lane, lane, sbase, k_full, k_empty,
-                                 C::PV16 ? v_land : v_full, v_empty, bad_mask, abort_flag);
-    } else if (warp == kP2ConvWarp) {
-        // ------------------------------------------------------------------ value converter
-        if constexpr (C::PV16) {
-            bool sat = false;
-            for (int t = 0; t < n_tiles; ++t) {
-                const int sl = t % NV;
-                if (!pfx_warp_wait(&v_land[sl], (t / NV) & 1, abort_flag, lane)) break;
-                __syncwarp();
-                sat |= pfx_tile_to_f16(sbase + C::OFF_V + sl * C::V_BYTES, C::V_BYTES, lane);
-                fence_proxy_async_smem();  // the f16 tile is visible to the tensor core
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&v_full[sl]);
-            }
-            if (sat && lane == 0) prefix_flag(512u);
-        }
+        pfx_load_tiles<C, D, 32>(p, rng, warp == kP2KeyWarp, lane, lane, sbase, k_full, k_empty, v_full, v_empty,
+                                 bad_mask, abort_flag);
     } else if (warp == kP2MmaWarp || warp == kP2MmaWarp1) {
         // ------------------------------------------------------------------ score MMAs
         const int g = warp == kP2MmaWarp1 ? 1 : 0;
@@ -231,7 +205,7 @@ __global__ void __launch_bounds__(kP2Threads, 1) pa_prefix_m256_kernel(const __g
                 if (ok) ok = pfx_wait(&p_full[g * 2 + (t & 1)], (t >> 1) & 1, abort_flag);
                 if (!ok) break;
                 tc_fence_after();
-                // P of this tile: the first 32 columns of its S buffer (64 f16 values)
+                // P of this tile: its S buffer, bf16 hi in the first 32 columns, lo in the next 32
                 const uint32_t a_p = tm + g * 256 + (t & 1) * BN;
 #pragma unroll
                 for (int h = 0; h < C::NP; ++h)
@@ -318,15 +292,19 @@ __global__ void __launch_bounds__(kP2Threads, 1) pa_prefix_m256_kernel(const __g
             const float mu = m_ref == -INFINITY ? 0.f : m_ref;
             const float2 sl2v = make_float2(p.sl2, p.sl2), nmu = make_float2(-mu, -mu);
             float2 sum2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-            uint32_t ph[BN / 2];
+            uint32_t ph[BN / 2], pl[BN / 2];
 #pragma unroll
             for (int e = 0; e < BN / 2; ++e) {
                 const float2 x = ffma2(make_float2(sv[2 * e], sv[2 * e + 1]), sl2v, nmu);
                 const float a = ex2(x.x), bb = ex2(x.y);
                 sum2[e & 1] = fadd2(sum2[e & 1], make_float2(a, bb));
-                // P in the value product's type: f16 (with bf16 inputs the value tiles are
-                // converted to f16 by the value warp)
-                ph[e] = pack2<false>(a, bb);
+                const uint32_t h2 = pack2<BF16>(a, bb);
+                ph[e] = h2;
+                if constexpr (BF16) {
+                    const float2 d = fsub2(make_float2(a, bb),
+                                           make_float2(__uint_as_float(h2 << 16), __uint_as_float(h2 & 0xffff0000u)));
+                    pl[e] = pack2<BF16>(d.x, d.y);
+                }
             }
             l += (sum2[0].x + sum2[0].y) + (sum2[1].x + sum2[1].y);
             // O holds every earlier tile before it is rescaled
@@ -344,8 +322,9 @@ __global__ void __launch_bounds__(kP2Threads, 1) pa_prefix_m256_kernel(const __g
                 }
                 tmem_wait_st();
             }
-            // P into the S buffer just read
+            // P into the S buffer just read (bf16: hi, then lo)
             tmem_st32(ts, *reinterpret_cast<const float(*)[32]>(&ph[0]));
+            if constexpr (BF16) tmem_st32(ts + BN / 2, *reinterpret_cast<const float(*)[32]>(&pl[0]));
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
