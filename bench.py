@@ -306,6 +306,25 @@ def _cpu_baseline(wl, seconds: float, threads: int):
     return gbs, desc, done_bytes, t_total
 
 
+def pack_inputs(tensors, device):
+    """One pinned host buffer holding `tensors` (CPU) back to back at 256-byte offsets, a
+    device buffer of the same size, and typed views of the device buffer shaped like them."""
+    import torch
+
+    offs, n = [], 0
+    for t in tensors:
+        offs.append(n)
+        n += -(-t.numel() * t.element_size() // 256) * 256
+    hbuf = torch.empty(n, dtype=torch.uint8).pin_memory()
+    dbuf = torch.empty(n, dtype=torch.uint8, device=device)
+    views = []
+    for t, o in zip(tensors, offs):
+        nb = t.numel() * t.element_size()
+        hbuf[o:o + nb].copy_(t.contiguous().view(-1).view(torch.uint8))
+        views.append(dbuf[o:o + nb].view(t.dtype).view(t.shape))
+    return hbuf, dbuf, views
+
+
 def workload_config(name: str, wl, world: int) -> dict:
     """The `config` object of a decode line: the workload's name and shape, the same for the
     GPU arm and the reference arm."""
@@ -386,15 +405,16 @@ def run_ours(args):
     ctr = pa.decode_counters(S, H, wl.num_kv_heads, dev) if args.decode == "fused" else None
     stream = torch.cuda.current_stream()
 
-    def step(i):
+    def step(i, inp=None):
+        q_, bt_, sl_, nk_, nv_, slots_ = (q, bt, sl, nk, nv, slots) if inp is None else inp
         kc, vc = kcs[i % nrot], vcs[i % nrot]
         if args.decode == "append":
             # the writer of the newest token fused into the decode
-            pa.pa_v2_decode_append(out, es, ml, tmp, q, nk, nv, kc, vc, wl.num_kv_heads, wl.scale, bt, sl,
+            pa.pa_v2_decode_append(out, es, ml, tmp, q_, nk_, nv_, kc, vc, wl.num_kv_heads, wl.scale, bt_, sl_,
                                    wl.block_size, wl.max_seq_len, slopes, wl.kv_cache_dtype, wl.k_scale, wl.v_scale)
             return
-        pa.pa_reshape_and_cache(nk, nv, kc, vc, slots, wl.kv_cache_dtype, wl.k_scale, wl.v_scale)
-        pa.pa_v2_decode(out, es, ml, tmp, q, kc, vc, wl.num_kv_heads, wl.scale, bt, sl, wl.block_size,
+        pa.pa_reshape_and_cache(nk_, nv_, kc, vc, slots_, wl.kv_cache_dtype, wl.k_scale, wl.v_scale)
+        pa.pa_v2_decode(out, es, ml, tmp, q_, kc, vc, wl.num_kv_heads, wl.scale, bt_, sl_, wl.block_size,
                         wl.max_seq_len, slopes, wl.kv_cache_dtype, wl.k_scale, wl.v_scale, counters=ctr)
 
     decode_bytes = wl.algorithmic_bytes()
@@ -451,23 +471,20 @@ def run_ours(args):
     # ---- end to end through host buffers (pinned), same metric --------------------------
     e2e = None
     if not args.no_e2e:
-        hq = wl.query.pin_memory()
-        hbt, hsl = wl.block_tables.pin_memory(), wl.seq_lens.pin_memory()
-        hnk, hnv, hslots = wl.new_key.pin_memory(), wl.new_value.pin_memory(), wl.slot_mapping.pin_memory()
+        # The step's inputs travel in one pinned host buffer and one copy (a serving loop
+        # stages them together), the output back in one copy.
+        srcs = [wl.query, wl.block_tables, wl.seq_lens, wl.new_key, wl.new_value]
+        if args.decode != "append":  # the append step takes the slots from the tables
+            srcs.append(wl.slot_mapping)
+        hbuf, dbuf, views = pack_inputs(srcs, dev)
+        inp = tuple(views) + (() if args.decode != "append" else (slots,))
         hout = torch.empty_like(wl.query).pin_memory()
-        copied = (hq, hbt, hsl, hnk, hnv) + (() if args.decode == "append" else (hslots,))
-        h2d = sum(t.numel() * t.element_size() for t in copied)
+        h2d = sum(t.numel() * t.element_size() for t in srcs)
         d2h = hout.numel() * hout.element_size()
 
         def e2e_step(i):
-            q.copy_(hq, non_blocking=True)
-            bt.copy_(hbt, non_blocking=True)
-            sl.copy_(hsl, non_blocking=True)
-            nk.copy_(hnk, non_blocking=True)
-            nv.copy_(hnv, non_blocking=True)
-            if args.decode != "append":  # the append step takes the slots from the tables
-                slots.copy_(hslots, non_blocking=True)
-            step(i)
+            dbuf.copy_(hbuf, non_blocking=True)
+            step(i, inp)
             hout.copy_(out, non_blocking=True)
 
         for i in range(max(1, args.warmup)):
@@ -670,18 +687,19 @@ def run_prefix(args):
     rank_tflops = flops / (k_ms * 1e-3) / 1e12
     e2e = None
     if not args.no_e2e:
-        hq, hk, hv = (getattr(wl, k).pin_memory() for k in ("query", "key", "value"))
+        # the step's q/k/v rows in one pinned host buffer and one copy, the output back in one
+        srcs = [getattr(wl, k) for k in ("query", "key", "value")]
+        hbuf, dbuf, (dq, dk, dv) = pack_inputs(srcs, dev["query"].device)
         ho = torch.empty(wl.query.shape, dtype=wl.query.dtype).pin_memory()
-        dq, dk, dv = (torch.empty_like(dev[k]) for k in ("query", "key", "value"))
         for _ in range(2):
-            dq.copy_(hq, non_blocking=True); dk.copy_(hk, non_blocking=True); dv.copy_(hv, non_blocking=True)
+            dbuf.copy_(hbuf, non_blocking=True)
             call(dq, dk, dv, out)
             ho.copy_(out, non_blocking=True)
         torch.cuda.synchronize()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
         for _ in range(args.steps):
-            dq.copy_(hq, non_blocking=True); dk.copy_(hk, non_blocking=True); dv.copy_(hv, non_blocking=True)
+            dbuf.copy_(hbuf, non_blocking=True)
             call(dq, dk, dv, out)
             ho.copy_(out, non_blocking=True)
             launches += n_kernels
@@ -690,7 +708,7 @@ def run_prefix(args):
         e_ms = a.elapsed_time(b) / args.steps
         if ws > 1:
             _, e_ms = combine_ranks(0.0, e_ms, torch.device("cuda", dev_i), ws)
-        h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
+        h2d = sum(t.numel() * t.element_size() for t in srcs)
         e2e = {"value": round(all_flops / (e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s", "ms_per_step": round(e_ms, 4),
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": ho.numel() * ho.element_size()}
     cpu = None
