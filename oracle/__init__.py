@@ -53,10 +53,10 @@ def _load():
             i32, i64, f32 = ctypes.c_int, ctypes.c_int64, ctypes.c_float
             lib.pa_oracle_decode.restype = i32
             lib.pa_oracle_decode.argtypes = [P, i32, P, P, i32, i32, i32, i32, i32, i32, P, i32, P,
-                                             f32, P, f32, f32, i32, i32, P, i32, P, P, P, P, P, i32]
+                                             f32, P, f32, f32, P, P, i32, i32, P, i32, P, P, P, P, P, i32]
             lib.pa_oracle_reshape_and_cache.restype = i32
             lib.pa_oracle_reshape_and_cache.argtypes = [P, P, i32, i64, i64, P, P, i32, P, i32, i32,
-                                                        i32, i32, i32, f32, f32]
+                                                        i32, i32, i32, f32, f32, P, P]
             lib.pa_oracle_decode_table.restype = i32
             lib.pa_oracle_decode_table.argtypes = [i32, P]
             lib.pa_oracle_prefix.restype = i32
@@ -91,13 +91,25 @@ def _ptr(a: Optional[np.ndarray]):
     return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
 
 
+def _scale_arg(s, num_kv_heads: int):
+    """A scale given as one float (per tensor) or as num_kv_heads floats (per kv head):
+    returns (the float, or 1.0) and (None, or the float32 array)."""
+    if isinstance(s, (int, float)):
+        return float(s), None
+    a = np.ascontiguousarray(np.asarray(_np(s) if hasattr(s, "numpy") else s, dtype=np.float32).reshape(-1))
+    if a.shape != (num_kv_heads,):
+        raise ValueError("per-head scales need one value per kv head")
+    return 1.0, a
+
+
 def decode(query, q_fmt: str, key_cache, value_cache, kv_fmt: str, *, num_kv_heads: int,
            block_size: int, block_tables, seq_lens, scale: float, alibi_slopes=None,
-           k_scale: float = 1.0, v_scale: float = 1.0, partition_size: int = 512,
+           k_scale=1.0, v_scale=1.0, partition_size: int = 512,
            max_num_partitions: Optional[int] = None,
            pairs: Optional[Sequence[Sequence[int]]] = None, threads: int = 0) -> dict:
     """fp64 decode attention for the requested (sequence, head) pairs (all pairs by default).
 
+    ``k_scale`` / ``v_scale``: one float, or one per kv head (a sequence of num_kv_heads).
     Returns a dict of float64 arrays: ``out`` and ``out_onepass`` [n, d], ``max_logits`` and
     ``exp_sums`` [n, Pmax], ``tmp_out`` [n, Pmax, d] and the ``pairs`` [n, 2] used.
     """
@@ -120,9 +132,11 @@ def decode(query, q_fmt: str, key_cache, value_cache, kv_fmt: str, *, num_kv_hea
     out = np.zeros((n, d)); out1 = np.zeros((n, d))
     ml = np.zeros((n, P)); es = np.zeros((n, P)); tmp = np.zeros((n, P, d))
     sl_f = None if alibi_slopes is None else np.ascontiguousarray(_np(alibi_slopes), dtype=np.float32)
+    ks, ka = _scale_arg(k_scale, num_kv_heads)
+    vs, va = _scale_arg(v_scale, num_kv_heads)
     rc = lib.pa_oracle_decode(_ptr(q), FMT[q_fmt], _ptr(kc), _ptr(vc), FMT[kv_fmt], S, H,
                               num_kv_heads, d, block_size, _ptr(bt), bt.shape[1], _ptr(sl),
-                              float(scale), _ptr(sl_f), float(k_scale), float(v_scale),
+                              float(scale), _ptr(sl_f), ks, vs, _ptr(ka), _ptr(va),
                               int(partition_size), P, _ptr(pr), n, _ptr(out), _ptr(out1),
                               _ptr(ml), _ptr(es), _ptr(tmp), int(threads))
     if rc != 0:
@@ -140,25 +154,28 @@ def decode_workload(wl, pairs=None, partition_size: int = 512, threads: int = 0,
                   wl.value_cache if value_cache is None else value_cache, kv_fmt,
                   num_kv_heads=wl.num_kv_heads, block_size=wl.block_size,
                   block_tables=wl.block_tables, seq_lens=wl.seq_lens, scale=wl.scale,
-                  alibi_slopes=wl.alibi_slopes, k_scale=wl.k_scale, v_scale=wl.v_scale,
-                  partition_size=partition_size,
+                  alibi_slopes=wl.alibi_slopes, k_scale=wl.k_scales_or_scalar(),
+                  v_scale=wl.v_scales_or_scalar(), partition_size=partition_size,
                   max_num_partitions=wl.max_num_partitions if partition_size == 512 else None,
                   pairs=pairs, threads=threads)
 
 
 def reshape_and_cache(key, value, src_fmt: str, key_cache: np.ndarray, value_cache: np.ndarray,
-                      kv_fmt: str, slot_mapping, *, block_size: int, k_scale: float = 1.0,
-                      v_scale: float = 1.0) -> None:
-    """Scatter rows key/value [T, Hk, d] into the numpy caches in place (by slot)."""
+                      kv_fmt: str, slot_mapping, *, block_size: int, k_scale=1.0,
+                      v_scale=1.0) -> None:
+    """Scatter rows key/value [T, Hk, d] into the numpy caches in place (by slot).  The scales
+    are one float each, or one per kv head."""
     lib = _load()
     k, v = _np(key), _np(value)
     T, Hk, d = k.shape
     sm = np.ascontiguousarray(_np(slot_mapping), dtype=np.int64)
     assert key_cache.flags.c_contiguous and value_cache.flags.c_contiguous
+    ks, ka = _scale_arg(k_scale, Hk)
+    vs, va = _scale_arg(v_scale, Hk)
     rc = lib.pa_oracle_reshape_and_cache(_ptr(k), _ptr(v), FMT[src_fmt], Hk * d, Hk * d,
                                          _ptr(key_cache), _ptr(value_cache), FMT[kv_fmt],
                                          _ptr(sm), T, Hk, d, block_size, key_cache.shape[0],
-                                         float(k_scale), float(v_scale))
+                                         ks, vs, _ptr(ka), _ptr(va))
     if rc != 0:
         raise ValueError("oracle writer rejected the arguments")
 

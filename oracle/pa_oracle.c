@@ -23,6 +23,9 @@
  *   - head h reads kv head h / (H / Hk)   (the [kv_h, gqa, 1, d] view of the query).
  *   - ALiBi adds slope[h] * t with t the absolute position 0 .. L-1.
  *   - k_scale and v_scale always multiply the decoded cache values.
+ *   - per-kv-head scales (an extension: the pages pass one float each): with arrays
+ *     k_scales[Hk], v_scales[Hk] the keys and values of kv head j are multiplied by
+ *     k_scales[j] and v_scales[j] instead, and the writer divides head j's rows by them.
  *   - fp8 cache bytes are OCP e4m3fn codes (bias 7, subnormals, 0x7F/0xFF NaN, no inf).
  *   - writer: fp16/bf16 caches get a bitwise copy; an fp8 cache gets
  *     RNE-satfinite-e4m3( (float)x / k_scale ) with the division in IEEE binary32.
@@ -140,6 +143,8 @@ typedef struct {
     double scale;
     const float* alibi;
     double k_scale, v_scale;
+    const float* k_scales; /* [Hk] or NULL: per-kv-head scales replace k_scale */
+    const float* v_scales; /* [Hk] or NULL */
     int part;  /* partition size in tokens */
     int Pmax;
 } orc_args;
@@ -148,13 +153,13 @@ typedef struct {
 static double k_at(const orc_args* a, int64_t b, int kvh, int i, int o) {
     int x = 16 / elem_bytes(a->kv_fmt);
     int64_t idx = ((((b * a->Hk + kvh) * (a->d / x) + i / x) * a->bs + o) * x) + i % x;
-    return dec_elem(a->key_cache, idx, a->kv_fmt) * a->k_scale;
+    return dec_elem(a->key_cache, idx, a->kv_fmt) * (a->k_scales ? (double)a->k_scales[kvh] : a->k_scale);
 }
 
 /* value_cache[b][kvh][i][o] */
 static double v_at(const orc_args* a, int64_t b, int kvh, int i, int o) {
     int64_t idx = ((b * a->Hk + kvh) * a->d + i) * (int64_t)a->bs + o;
-    return dec_elem(a->value_cache, idx, a->kv_fmt) * a->v_scale;
+    return dec_elem(a->value_cache, idx, a->kv_fmt) * (a->v_scales ? (double)a->v_scales[kvh] : a->v_scale);
 }
 
 /* One (sequence, query head).  Outputs: out[d] (phase 2 of the partitioned pass),
@@ -236,14 +241,15 @@ static void decode_one(const orc_args* a, int s, int h, double* out, double* out
  * Decode attention for a list of (sequence, head) pairs.
  *   pairs[2*n], pairs[2*n+1] = (s, h) for n < n_pairs
  *   out, out1: [n_pairs][d]; max_logits, exp_sums: [n_pairs][Pmax]; tmp_out: [n_pairs][Pmax][d]
- * partition_size <= 0 means one partition per sequence.  Returns 0, or -1 on bad sizes.
+ * partition_size <= 0 means one partition per sequence.  k_scales / v_scales (NULL, or
+ * num_kv_heads floats) replace k_scale / v_scale per kv head.  Returns 0, or -1 on bad sizes.
  */
 int pa_oracle_decode(const void* query, int q_fmt, const void* key_cache, const void* value_cache,
                      int kv_fmt, int num_seqs, int num_heads, int num_kv_heads, int head_size,
                      int block_size, const int32_t* block_tables, int max_blocks_per_seq,
                      const int32_t* seq_lens, float scale, const float* alibi_slopes,
-                     float k_scale, float v_scale, int partition_size, int max_num_partitions,
-                     const int32_t* pairs, int n_pairs, double* out, double* out1,
+                     float k_scale, float v_scale, const float* k_scales, const float* v_scales,
+                     int partition_size, int max_num_partitions, const int32_t* pairs, int n_pairs, double* out, double* out1,
                      double* max_logits, double* exp_sums, double* tmp_out, int num_threads) {
     if (num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads || head_size <= 0 ||
         block_size <= 0 || max_num_partitions <= 0)
@@ -253,7 +259,7 @@ int pa_oracle_decode(const void* query, int q_fmt, const void* key_cache, const 
     orc_args a = {query, q_fmt, key_cache, value_cache, kv_fmt, num_seqs, num_heads,
                   num_kv_heads, head_size, block_size, block_tables, max_blocks_per_seq,
                   seq_lens, (double)scale, alibi_slopes, (double)k_scale, (double)v_scale,
-                  partition_size > 0 ? partition_size : 0x7fffffff, max_num_partitions};
+                  k_scales, v_scales, partition_size > 0 ? partition_size : 0x7fffffff, max_num_partitions};
     for (int n = 0; n < n_pairs; ++n) {
         int s = pairs[2 * n], h = pairs[2 * n + 1];
         if (s < 0 || s >= num_seqs || h < 0 || h >= num_heads) return -1;
@@ -278,13 +284,15 @@ int pa_oracle_decode(const void* query, int q_fmt, const void* key_cache, const 
  * key/value rows: [num_tokens][num_kv_heads][head_size], token stride given in elements.
  * For token t with slot = slot_mapping[t] >= 0, b = slot / block_size, o = slot % block_size:
  *   key_cache[b][h][i / x][o][i % x] = enc(key[t][h][i]),  value_cache[b][h][i][o] = enc(value[t][h][i])
+ * k_scales / v_scales (NULL, or num_kv_heads floats) replace k_scale / v_scale per kv head.
  * Returns 0, or -1 on bad arguments.
  */
 int pa_oracle_reshape_and_cache(const void* key, const void* value, int src_fmt,
                                 int64_t key_stride_t, int64_t value_stride_t, void* key_cache,
                                 void* value_cache, int kv_fmt, const int64_t* slot_mapping,
                                 int num_tokens, int num_kv_heads, int head_size, int block_size,
-                                int num_blocks, float k_scale, float v_scale) {
+                                int num_blocks, float k_scale, float v_scale, const float* k_scales,
+                                const float* v_scales) {
     if (src_fmt != ORC_F16 && src_fmt != ORC_BF16) return -1;
     if (kv_fmt != src_fmt && kv_fmt != ORC_E4M3) return -1;
     const int x = 16 / elem_bytes(kv_fmt);
@@ -296,6 +304,8 @@ int pa_oracle_reshape_and_cache(const void* key, const void* value, int src_fmt,
         int o = (int)(slot % block_size);
         if (b >= num_blocks) return -1;
         for (int h = 0; h < num_kv_heads; ++h) {
+            const float kdiv = k_scales ? k_scales[h] : k_scale;
+            const float vdiv = v_scales ? v_scales[h] : v_scale;
             for (int i = 0; i < head_size; ++i) {
                 int64_t ks = t * key_stride_t + (int64_t)h * head_size + i;
                 int64_t vs = t * value_stride_t + (int64_t)h * head_size + i;
@@ -304,8 +314,8 @@ int pa_oracle_reshape_and_cache(const void* key, const void* value, int src_fmt,
                 if (kv_fmt == ORC_E4M3) {
                     float kx = (float)dec_elem(key, ks, src_fmt);
                     float vx = (float)dec_elem(value, vs, src_fmt);
-                    ((uint8_t*)key_cache)[kd] = orc_enc_e4m3(kx / k_scale);
-                    ((uint8_t*)value_cache)[vd] = orc_enc_e4m3(vx / v_scale);
+                    ((uint8_t*)key_cache)[kd] = orc_enc_e4m3(kx / kdiv);
+                    ((uint8_t*)value_cache)[vd] = orc_enc_e4m3(vx / vdiv);
                 } else {
                     ((uint16_t*)key_cache)[kd] = ((const uint16_t*)key)[ks];
                     ((uint16_t*)value_cache)[vd] = ((const uint16_t*)value)[vs];
@@ -369,7 +379,7 @@ int pa_oracle_prefix(const void* query, const void* key, const void* value, int 
     if (fmt != ORC_F16 && fmt != ORC_BF16) return -1;
     orc_args a = {NULL, fmt, key_cache, value_cache, fmt, num_seqs, num_heads, num_kv_heads,
                   head_size, block_size, block_tables, max_blocks_per_seq, NULL, (double)scale,
-                  NULL, 1.0, 1.0, 0x7fffffff, 1};
+                  NULL, 1.0, 1.0, NULL, NULL, 0x7fffffff, 1};
     const int H = num_heads, Hk = num_kv_heads, d = head_size, G = H / Hk;
     for (int i = 0; i < num_seqs; ++i) {
         int ctx = context_lens[i];

@@ -397,6 +397,86 @@ def test_p9_writer(storage):
 
 
 # ----------------------------------------------------------------------------------------
+# P11: per-kv-head scales (k_scales[Hk], v_scales[Hk] in place of one k_scale / v_scale)
+# ----------------------------------------------------------------------------------------
+def _head_slice(wl, j):
+    """The workload reduced to kv head j and its query heads, with head j's scales as the
+    per-tensor k_scale / v_scale."""
+    G = wl.num_heads // wl.num_kv_heads
+    hs = slice(j * G, (j + 1) * G)
+    return workloads.Workload(**{
+        **wl.__dict__, "num_heads": G, "num_kv_heads": 1,
+        "query": wl.query[:, hs].contiguous(),
+        "key_cache": wl.key_cache[:, j:j + 1].contiguous(),
+        "value_cache": wl.value_cache[:, j:j + 1].contiguous(),
+        "alibi_slopes": None if wl.alibi_slopes is None else wl.alibi_slopes[hs].contiguous(),
+        "k_scale": float(wl.k_scales[j]), "v_scale": float(wl.v_scales[j]),
+        "k_scales": None, "v_scales": None})
+
+
+@pytest.mark.parametrize("alibi", [False, True])
+def test_p11_head_scales_split_by_kv_head(alibi):
+    # attention over kv head j sees only head j's keys and values: with per-head scales the
+    # result for its query heads equals the per-tensor decode of that head alone at its
+    # scales (a wrong head index, or a scale taken from another head, fails this)
+    wl = workloads.build(num_seqs=3, num_heads=12, num_kv_heads=3, head_size=64, block_size=16,
+                         seq_lens=[700, 1, 1300], kv_cache_dtype="fp8_e4m3", alibi=alibi,
+                         k_scales=[0.05, 0.11, 0.02], v_scales=[0.07, 0.013, 0.3], seed=31)
+    r = oracle.decode_workload(wl)
+    G = 4
+    for j in range(3):
+        rj = oracle.decode_workload(_head_slice(wl, j))
+        rows = [s * 12 + j * G + g for s in range(3) for g in range(G)]
+        for key in ("out", "max_logits", "exp_sums", "tmp_out"):
+            assert np.array_equal(r[key][rows], rj[key]), (j, key)
+    # and the heads really differ from a decode at one shared scale
+    r1 = oracle.decode_workload(workloads.Workload(**{**wl.__dict__, "k_scales": None, "v_scales": None}))
+    assert not np.allclose(r["out"], r1["out"])
+
+
+def test_p11_head_scales_single_token():
+    # L = 1: out = v_scales[j] * V[t0], max_logit = scale * k_scales[j] * <q, K[t0]>
+    ks, vs = [0.05, 0.5], [0.25, 0.03]
+    wl = workloads.build(num_seqs=2, num_heads=4, num_kv_heads=2, head_size=64, block_size=16,
+                         seq_lens=[1, 1], kv_cache_dtype="fp8_e4m3", k_scales=ks, v_scales=vs, seed=32)
+    r = oracle.decode_workload(wl)
+    vtab = storage_to_f64(wl.value_cache, "fp8_e4m3")
+    ktab = storage_to_f64(wl.key_cache, "fp8_e4m3")
+    q = storage_to_f64(wl.query, "f16")
+    for s in range(2):
+        b = int(wl.block_tables[s, 0])
+        for h in range(4):
+            n, j = s * 4 + h, h // 2
+            assert np.array_equal(r["out"][n], vtab[b, j, :, 0] * np.float64(np.float32(vs[j])))
+            k = ktab[b, j, :, 0, :].reshape(-1) * np.float64(np.float32(ks[j]))
+            s0 = wl.scale * float(q[s, h] @ k)
+            assert abs(r["max_logits"][n, 0] - s0) < 1e-12 * max(1, abs(s0))
+
+
+def test_p11_writer_head_scales():
+    # head j's rows are encoded as e4m3(x / k_scales[j]) (torch's cast of the fp32 quotient)
+    ks, vs = [0.05, 0.2, 0.011, 1.5], [0.03, 0.4, 0.09, 0.007]
+    wl = workloads.build(num_seqs=4, num_heads=8, num_kv_heads=4, head_size=64, block_size=16,
+                         seq_lens=[3, 40, 0, 17], kv_cache_dtype="fp8_e4m3", k_scales=ks, v_scales=vs,
+                         seed=33)
+    kc = oracle._np(wl.key_cache).copy()
+    vc = oracle._np(wl.value_cache).copy()
+    oracle.reshape_and_cache(wl.new_key, wl.new_value, "f16", kc, vc, "fp8_e4m3", wl.slot_mapping,
+                             block_size=16, k_scale=wl.k_scales, v_scale=wl.v_scales)
+    for s, slot in enumerate(wl.slot_mapping.tolist()):
+        if slot < 0:
+            continue
+        b, o = slot // 16, slot % 16
+        for j in range(4):
+            kf = storage_to_f64(wl.new_key[s, j], "f16").astype(np.float32) / np.float32(ks[j])
+            vf = storage_to_f64(wl.new_value[s, j], "f16").astype(np.float32) / np.float32(vs[j])
+            kw = torch.from_numpy(kf).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+            vw = torch.from_numpy(vf).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+            assert np.array_equal(kc[b, j, :, o, :].reshape(-1), kw), (s, j)
+            assert np.array_equal(vc[b, j, :, o], vw), (s, j)
+
+
+# ----------------------------------------------------------------------------------------
 # P10: seeds reproduce
 # ----------------------------------------------------------------------------------------
 def test_p10_seeded_generation_reproduces():

@@ -68,6 +68,15 @@ class Workload:
     slot_mapping: torch.Tensor  # int64 [S]; -1 for empty sequences
     sigma: float = 1.0
     seed: int = 0
+    # One scale per kv head (float32 [Hk]) in place of k_scale / v_scale, or None.
+    k_scales: Optional[torch.Tensor] = None
+    v_scales: Optional[torch.Tensor] = None
+
+    def k_scales_or_scalar(self):
+        return self.k_scale if self.k_scales is None else self.k_scales
+
+    def v_scales_or_scalar(self):
+        return self.v_scale if self.v_scales is None else self.v_scales
 
     @property
     def x(self) -> int:
@@ -219,14 +228,16 @@ def _fill_normal(shape, sigma: float, seed: int, stream: int) -> np.ndarray:
     return out.reshape(shape)
 
 
-def _to_storage(a: np.ndarray, storage: str, inv_scale: float = 1.0) -> torch.Tensor:
+def _to_storage(a: np.ndarray, storage: str, inv_scale=1.0) -> torch.Tensor:
     t = torch.from_numpy(a)
     if storage == "f16":
         return t.to(torch.float16)
     if storage == "bf16":
         return t.to(torch.bfloat16)
     if storage == "fp8_e4m3":
-        if inv_scale != 1.0:
+        if isinstance(inv_scale, np.ndarray):  # one scale per kv head, broadcast
+            t = t * torch.from_numpy(inv_scale).to(t.dtype)
+        elif inv_scale != 1.0:
             t = t * inv_scale
         return t.to(torch.float8_e4m3fn).view(torch.uint8)
     raise ValueError(storage)
@@ -259,6 +270,8 @@ def build(
     alibi: bool = False,
     k_scale: float = 1.0,
     v_scale: float = 1.0,
+    k_scales: Optional[Sequence[float]] = None,
+    v_scales: Optional[Sequence[float]] = None,
     scale: Optional[float] = None,
     num_blocks: Optional[int] = None,
     block_slack: float = 1.25,
@@ -271,6 +284,8 @@ def build(
 
     Physical block ids come from one ``permutation(num_blocks)`` dealt out sequence by
     sequence; the first unused id is the canary block every padding entry points at.
+    ``k_scales`` / ``v_scales`` (num_kv_heads values each) replace k_scale / v_scale per kv
+    head: an fp8 cache then holds head j's values quantised as x / k_scales[j].
     """
     rng = np.random.default_rng(seed)
     S, H, Hk, d, bs = num_seqs, num_heads, num_kv_heads, head_size, block_size
@@ -303,9 +318,15 @@ def build(
     # Values: K and V caches over all physical blocks, then the query and new-token rows.
     kshape = (num_blocks, Hk, d // x, bs, x)
     vshape = (num_blocks, Hk, d, bs)
+    ksv = None if k_scales is None else np.asarray(k_scales, dtype=np.float32).reshape(Hk)
+    vsv = None if v_scales is None else np.asarray(v_scales, dtype=np.float32).reshape(Hk)
     inv = 1.0 / k_scale if storage == "fp8_e4m3" else 1.0
+    if ksv is not None and storage == "fp8_e4m3":
+        inv = (1.0 / ksv).astype(np.float32).reshape(1, Hk, 1, 1, 1)
     key_cache = _to_storage(_fill_normal(kshape, sigma, seed, 1), storage, inv)
     inv = 1.0 / v_scale if storage == "fp8_e4m3" else 1.0
+    if vsv is not None and storage == "fp8_e4m3":
+        inv = (1.0 / vsv).astype(np.float32).reshape(1, Hk, 1, 1)
     value_cache = _to_storage(_fill_normal(vshape, sigma, seed, 2), storage, inv)
     query = _to_storage(_fill_normal((S, H, d), sigma, seed, 3), q_dtype)
     new_key = _to_storage(_fill_normal((S, Hk, d), sigma, seed, 4), q_dtype)
@@ -347,6 +368,8 @@ def build(
         seq_lens=torch.from_numpy(lens.astype(np.int32)), alibi_slopes=slopes,
         max_seq_len=msl, new_key=new_key, new_value=new_value,
         slot_mapping=torch.from_numpy(slots), sigma=sigma, seed=seed,
+        k_scales=None if ksv is None else torch.from_numpy(ksv.copy()),
+        v_scales=None if vsv is None else torch.from_numpy(vsv.copy()),
     )
 
 
