@@ -202,6 +202,46 @@ PA_API pa_status pa_v2_decode_append(void* output, float* exp_sums, float* max_l
                                      pa_kv_cache_dtype kv_cache_dtype, pa_dtype tmp_dtype, float k_scale,
                                      float v_scale, cudaStream_t stream);
 
+/*
+ * pa_v2_decode_head_scales, pa_v2_decode_append_head_scales -- pa_v2_decode and
+ * pa_v2_decode_append with one k_scale and one v_scale per kv head.
+ *
+ * Defines: the step of pa_v2_decode (resp. pa_v2_decode_append) with the dequantisation of
+ * "paged_attention_v2_pytorch.py" (paged_attention_v2_pytorch: cache values times k_scale /
+ * v_scale) taken per kv head, the per-head scale variant of that step: keys and values of
+ * kv head j are multiplied by k_scales[j] and v_scales[j], and the appended rows of head j
+ * are encoded as e4m3fn((float)x / k_scales[j]) (resp. v_scales[j]) for an fp8 cache.  The
+ * pages pass one float each; these entry points are this library's extension.
+ *
+ * Arguments: as pa_v2_decode (resp. pa_v2_decode_append), with k_scale / v_scale replaced by
+ *   k_scales, v_scales  device float [num_kv_heads], 4-byte aligned, read after the previous
+ *                       kernel in the stream has completed (so a kernel that writes them
+ *                       right before the call is seen).  Each must be finite and > 0: a
+ *                       value that is not is used as given and recorded in the device error
+ *                       flags (bit 8).
+ * With every entry equal to one value v the results are bit-identical to the per-tensor
+ * entry point called with k_scale = v (resp. v_scale = v): the score multiplier is rounded
+ * as scale * k_scale, then times log2(e), in binary32 on both paths.
+ * Errors: as the per-tensor entry points; PA_ERR_INVALID_ARG also for a null or misaligned
+ * scale array.
+ */
+PA_API pa_status pa_v2_decode_head_scales(void* output, float* exp_sums, float* max_logits, void* tmp_output,
+                                          const void* query, const void* key_cache, const void* value_cache,
+                                          int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                                          float scale, const int32_t* block_tables, int max_blocks_per_seq,
+                                          int num_blocks, const int32_t* seq_lens, int block_size,
+                                          int max_seq_len, int max_num_partitions, const float* alibi_slopes,
+                                          pa_dtype q_dtype, pa_kv_cache_dtype kv_cache_dtype, pa_dtype tmp_dtype,
+                                          const float* k_scales, const float* v_scales, cudaStream_t stream);
+
+PA_API pa_status pa_v2_decode_append_head_scales(
+    void* output, float* exp_sums, float* max_logits, void* tmp_output, const void* query, const void* key,
+    const void* value, int64_t key_stride_s, int64_t value_stride_s, void* key_cache, void* value_cache,
+    int num_seqs, int num_heads, int num_kv_heads, int head_size, float scale, const int32_t* block_tables,
+    int max_blocks_per_seq, int num_blocks, const int32_t* seq_lens, int block_size, int max_seq_len,
+    int max_num_partitions, const float* alibi_slopes, pa_dtype q_dtype, pa_kv_cache_dtype kv_cache_dtype,
+    pa_dtype tmp_dtype, const float* k_scales, const float* v_scales, cudaStream_t stream);
+
 /* Arrival counters pa_v2_decode_fused needs: num_seqs * num_kv_heads *
  * ceil((num_heads / num_kv_heads) / 8) (one per sequence and group of up to 8 query heads of a
  * kv head); 0 for invalid sizes. */
@@ -237,6 +277,25 @@ PA_API pa_status pa_reshape_and_cache(const void* key, const void* value, int64_
                                int head_size, int block_size, int num_blocks,
                                pa_dtype src_dtype, pa_kv_cache_dtype kv_cache_dtype,
                                float k_scale, float v_scale, cudaStream_t stream);
+
+/*
+ * pa_reshape_and_cache_head_scales -- pa_reshape_and_cache with one k_scale and one v_scale
+ * per kv head: for an fp8 cache head h's rows are encoded as e4m3fn((float)x / k_scales[h])
+ * (resp. v_scales[h]); a PA_KV_AUTO cache is a bitwise copy as there.  The pages' writer
+ * takes one float each; this is the per-head variant of the same encode.
+ * Arguments: as pa_reshape_and_cache, with k_scale / v_scale replaced by device float arrays
+ * k_scales, v_scales [num_kv_heads] (4-byte aligned; read after the previous kernel in the
+ * stream has completed; a value that is not finite and > 0 is used as given and recorded in
+ * the device error flags, bit 8).
+ * Errors: as pa_reshape_and_cache; PA_ERR_INVALID_ARG also for a null or misaligned array.
+ */
+PA_API pa_status pa_reshape_and_cache_head_scales(const void* key, const void* value, int64_t key_stride_t,
+                                                  int64_t value_stride_t, void* key_cache, void* value_cache,
+                                                  const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                                                  int head_size, int block_size, int num_blocks,
+                                                  pa_dtype src_dtype, pa_kv_cache_dtype kv_cache_dtype,
+                                                  const float* k_scales, const float* v_scales,
+                                                  cudaStream_t stream);
 
 /*
  * pa_copy_blocks -- copy whole blocks inside every layer's K and V cache (copy-on-write of
@@ -356,7 +415,8 @@ PA_API const char* pa_status_string(pa_status status);
 /* Device-side error flags (bit 0: a block id outside [0, num_blocks) or a table row too
  * short; bit 1: a sequence longer than max_num_partitions * 512 or a negative length;
  * bit 2: a bounded wait for a shared-memory copy gave up; bit 3: a slot outside the
- * cache; bit 4: a pa_copy_blocks id outside the cache; bits 5-7: pa_prefix, see there).
+ * cache; bit 4: a pa_copy_blocks id outside the cache; bits 5-7: pa_prefix, see there;
+ * bit 8: a per-kv-head k or v scale that is not finite and > 0).
  * Reads the flags of the current device (this synchronises the device) into
  * *flags, and clears them when reset != 0.  Not part of the pages' interface: it reports
  * what the kernels skipped instead of faulting. */

@@ -73,6 +73,15 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
     lib.pa_reshape_and_cache.restype = i32
     lib.pa_reshape_and_cache.argtypes = [P, P, i64, i64, P, P, P, i32, i32, i32, i32, i32, i32, i32,
                                          f32, f32, P]
+    lib.pa_v2_decode_head_scales.restype = i32
+    lib.pa_v2_decode_head_scales.argtypes = [P, P, P, P, P, P, P, i32, i32, i32, i32, f32, P, i32, i32, P, i32,
+                                             i32, i32, P, i32, i32, i32, P, P, P]
+    lib.pa_v2_decode_append_head_scales.restype = i32
+    lib.pa_v2_decode_append_head_scales.argtypes = [P, P, P, P, P, P, P, i64, i64, P, P, i32, i32, i32, i32, f32, P,
+                                                    i32, i32, P, i32, i32, i32, P, i32, i32, i32, P, P, P]
+    lib.pa_reshape_and_cache_head_scales.restype = i32
+    lib.pa_reshape_and_cache_head_scales.argtypes = [P, P, i64, i64, P, P, P, i32, i32, i32, i32, i32, i32, i32,
+                                                     P, P, P]
     lib.pa_v2_partition_size.restype = i32
     lib.pa_v2_partition_size.argtypes = []
     lib.pa_status_string.restype = ctypes.c_char_p
@@ -128,12 +137,26 @@ def _check(call: str, st: int) -> None:
         raise PagedAttentionError(call, st)
 
 
+def _head_scales(k_scale, v_scale, num_kv_heads: int):
+    """None for per-tensor scales (two floats); the two pointers for per-kv-head scales
+    (two float32 CUDA tensors of num_kv_heads values)."""
+    kt, vt = isinstance(k_scale, torch.Tensor), isinstance(v_scale, torch.Tensor)
+    if not kt and not vt:
+        return None
+    if not (kt and vt):
+        raise TypeError("k_scale and v_scale must both be floats or both be per-kv-head tensors")
+    for name, t in (("k_scale", k_scale), ("v_scale", v_scale)):
+        if t.dtype != torch.float32 or not t.is_cuda or not t.is_contiguous() or t.numel() != num_kv_heads:
+            raise TypeError(f"{name} per kv head must be a contiguous float32 CUDA tensor of num_kv_heads values")
+    return _ptr(k_scale), _ptr(v_scale)
+
+
 def pa_v2_decode(output: torch.Tensor, exp_sums: torch.Tensor, max_logits: torch.Tensor,
                  tmp_output: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,
                  value_cache: torch.Tensor, num_kv_heads: int, scale: float,
                  block_tables: torch.Tensor, seq_lens: torch.Tensor, block_size: int,
                  max_seq_len: int, alibi_slopes: Optional[torch.Tensor] = None,
-                 kv_cache_dtype: str = "auto", k_scale: float = 1.0, v_scale: float = 1.0,
+                 kv_cache_dtype: str = "auto", k_scale=1.0, v_scale=1.0,
                  num_blocks: Optional[int] = None, stream=None, counters: Optional[torch.Tensor] = None) -> None:
     """Enqueue one decode step (phase 1 + phase 2) on ``stream`` (default: current stream).
 
@@ -144,7 +167,8 @@ def pa_v2_decode(output: torch.Tensor, exp_sums: torch.Tensor, max_logits: torch
 
     With ``counters`` (from :func:`decode_counters`, zeroed once when allocated) the call is
     ``pa_v2_decode_fused``: the partition combine runs inside phase 1 and tmp_output is
-    scratch.
+    scratch.  ``k_scale`` / ``v_scale`` as float32 CUDA tensors of num_kv_heads values make
+    the call ``pa_v2_decode_head_scales`` (one scale per kv head).
     """
     lib = load()
     for name, t in (("output", output), ("exp_sums", exp_sums), ("max_logits", max_logits),
@@ -170,12 +194,19 @@ def pa_v2_decode(output: torch.Tensor, exp_sums: torch.Tensor, max_logits: torch
     S, H, d = query.shape
     if num_blocks is None:
         num_blocks = key_cache.shape[0]
+    hs = _head_scales(k_scale, v_scale, int(num_kv_heads))
     args = (_ptr(output), _ptr(exp_sums), _ptr(max_logits), _ptr(tmp_output),
             _ptr(query), _ptr(key_cache), _ptr(value_cache), S, H, int(num_kv_heads),
             d, float(scale), _ptr(block_tables), int(block_tables.shape[1]),
             int(num_blocks), _ptr(seq_lens), int(block_size), int(max_seq_len),
             int(tmp_output.shape[2]), _ptr(alibi_slopes), _dt(query.dtype),
-            _kv(kv_cache_dtype), tmp_dtype, float(k_scale), float(v_scale))
+            _kv(kv_cache_dtype), tmp_dtype)
+    if hs is not None:
+        if counters is not None:
+            raise TypeError("the fused combine takes per-tensor scales only")
+        _check("pa_v2_decode_head_scales", lib.pa_v2_decode_head_scales(*args, *hs, _stream(stream)))
+        return
+    args = args + (float(k_scale), float(v_scale))
     if counters is None:
         _check("pa_v2_decode", lib.pa_v2_decode(*args, _stream(stream)))
         return
@@ -189,11 +220,12 @@ def pa_v2_decode_append(output: torch.Tensor, exp_sums: torch.Tensor, max_logits
                         key_cache: torch.Tensor, value_cache: torch.Tensor, num_kv_heads: int, scale: float,
                         block_tables: torch.Tensor, seq_lens: torch.Tensor, block_size: int, max_seq_len: int,
                         alibi_slopes: Optional[torch.Tensor] = None, kv_cache_dtype: str = "auto",
-                        k_scale: float = 1.0, v_scale: float = 1.0, num_blocks: Optional[int] = None,
+                        k_scale=1.0, v_scale=1.0, num_blocks: Optional[int] = None,
                         stream=None) -> None:
     """One decode step that first appends every sequence's newest token (key/value [S, Hk, d]
     rows, position seq_lens[s] - 1, slot from the block table) to the caches: the cache
-    writer and pa_v2_decode in one kernel.  Other arguments as pa_v2_decode."""
+    writer and pa_v2_decode in one kernel.  Other arguments as pa_v2_decode (per-kv-head
+    scale tensors make the call ``pa_v2_decode_append_head_scales``)."""
     lib = load()
     for name, t in (("output", output), ("exp_sums", exp_sums), ("max_logits", max_logits),
                     ("tmp_output", tmp_output), ("query", query), ("key_cache", key_cache),
@@ -220,19 +252,25 @@ def pa_v2_decode_append(output: torch.Tensor, exp_sums: torch.Tensor, max_logits
         raise TypeError("alibi_slopes must be a float32 CUDA tensor")
     if num_blocks is None:
         num_blocks = key_cache.shape[0]
-    _check("pa_v2_decode_append", lib.pa_v2_decode_append(
-        _ptr(output), _ptr(exp_sums), _ptr(max_logits), _ptr(tmp_output), _ptr(query), _ptr(key), _ptr(value),
-        key.stride(0), value.stride(0), _ptr(key_cache), _ptr(value_cache), S, H, int(num_kv_heads), d,
-        float(scale), _ptr(block_tables), int(block_tables.shape[1]), int(num_blocks), _ptr(seq_lens),
-        int(block_size), int(max_seq_len), int(tmp_output.shape[2]), _ptr(alibi_slopes), _dt(query.dtype),
-        _kv(kv_cache_dtype), tmp_dtype, float(k_scale), float(v_scale), _stream(stream)))
+    args = (_ptr(output), _ptr(exp_sums), _ptr(max_logits), _ptr(tmp_output), _ptr(query), _ptr(key), _ptr(value),
+            key.stride(0), value.stride(0), _ptr(key_cache), _ptr(value_cache), S, H, int(num_kv_heads), d,
+            float(scale), _ptr(block_tables), int(block_tables.shape[1]), int(num_blocks), _ptr(seq_lens),
+            int(block_size), int(max_seq_len), int(tmp_output.shape[2]), _ptr(alibi_slopes), _dt(query.dtype),
+            _kv(kv_cache_dtype), tmp_dtype)
+    hs = _head_scales(k_scale, v_scale, int(num_kv_heads))
+    if hs is not None:
+        _check("pa_v2_decode_append_head_scales",
+               lib.pa_v2_decode_append_head_scales(*args, *hs, _stream(stream)))
+        return
+    _check("pa_v2_decode_append", lib.pa_v2_decode_append(*args, float(k_scale), float(v_scale), _stream(stream)))
 
 
 def pa_reshape_and_cache(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor,
                          value_cache: torch.Tensor, slot_mapping: torch.Tensor,
-                         kv_cache_dtype: str = "auto", k_scale: float = 1.0, v_scale: float = 1.0,
+                         kv_cache_dtype: str = "auto", k_scale=1.0, v_scale=1.0,
                          stream=None) -> None:
-    """Enqueue the slot-mapping cache writer: key/value [T, Hk, d] rows into the caches."""
+    """Enqueue the slot-mapping cache writer: key/value [T, Hk, d] rows into the caches
+    (per-kv-head scale tensors make the call ``pa_reshape_and_cache_head_scales``)."""
     lib = load()
     if key.dim() != 3 or value.shape != key.shape:
         raise ValueError("key and value must be [num_tokens, num_kv_heads, head_size]")
@@ -242,12 +280,43 @@ def pa_reshape_and_cache(key: torch.Tensor, value: torch.Tensor, key_cache: torc
     if slot_mapping.dtype != torch.int64 or not slot_mapping.is_contiguous():
         raise TypeError("slot_mapping must be a contiguous int64 tensor")
     bs = value_cache.shape[-1]
-    st = lib.pa_reshape_and_cache(_ptr(key), _ptr(value), key.stride(0), value.stride(0),
-                                  _ptr(key_cache), _ptr(value_cache), _ptr(slot_mapping), T, Hk, d,
-                                  int(bs), int(key_cache.shape[0]), _dt(key.dtype),
-                                  _kv(kv_cache_dtype), float(k_scale), float(v_scale),
-                                  _stream(stream))
-    _check("pa_reshape_and_cache", st)
+    args = (_ptr(key), _ptr(value), key.stride(0), value.stride(0), _ptr(key_cache), _ptr(value_cache),
+            _ptr(slot_mapping), T, Hk, d, int(bs), int(key_cache.shape[0]), _dt(key.dtype), _kv(kv_cache_dtype))
+    hs = _head_scales(k_scale, v_scale, Hk)
+    if hs is not None:
+        _check("pa_reshape_and_cache_head_scales", lib.pa_reshape_and_cache_head_scales(*args, *hs, _stream(stream)))
+        return
+    _check("pa_reshape_and_cache", lib.pa_reshape_and_cache(*args, float(k_scale), float(v_scale), _stream(stream)))
+
+
+def pa_v2_decode_head_scales(output, exp_sums, max_logits, tmp_output, query, key_cache, value_cache,
+                             num_kv_heads: int, scale: float, block_tables, seq_lens, block_size: int,
+                             max_seq_len: int, alibi_slopes=None, kv_cache_dtype: str = "auto", *,
+                             k_scales: torch.Tensor, v_scales: torch.Tensor, num_blocks: Optional[int] = None,
+                             stream=None) -> None:
+    """pa_v2_decode with one k_scale / v_scale per kv head (float32 CUDA tensors [Hk])."""
+    pa_v2_decode(output, exp_sums, max_logits, tmp_output, query, key_cache, value_cache, num_kv_heads, scale,
+                 block_tables, seq_lens, block_size, max_seq_len, alibi_slopes, kv_cache_dtype, k_scales, v_scales,
+                 num_blocks=num_blocks, stream=stream)
+
+
+def pa_v2_decode_append_head_scales(output, exp_sums, max_logits, tmp_output, query, key, value, key_cache,
+                                    value_cache, num_kv_heads: int, scale: float, block_tables, seq_lens,
+                                    block_size: int, max_seq_len: int, alibi_slopes=None,
+                                    kv_cache_dtype: str = "auto", *, k_scales: torch.Tensor,
+                                    v_scales: torch.Tensor, num_blocks: Optional[int] = None, stream=None) -> None:
+    """pa_v2_decode_append with one k_scale / v_scale per kv head (float32 CUDA tensors [Hk])."""
+    pa_v2_decode_append(output, exp_sums, max_logits, tmp_output, query, key, value, key_cache, value_cache,
+                        num_kv_heads, scale, block_tables, seq_lens, block_size, max_seq_len, alibi_slopes,
+                        kv_cache_dtype, k_scales, v_scales, num_blocks=num_blocks, stream=stream)
+
+
+def pa_reshape_and_cache_head_scales(key, value, key_cache, value_cache, slot_mapping,
+                                     kv_cache_dtype: str = "auto", *, k_scales: torch.Tensor,
+                                     v_scales: torch.Tensor, stream=None) -> None:
+    """pa_reshape_and_cache with one k_scale / v_scale per kv head (float32 CUDA tensors [Hk])."""
+    pa_reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, kv_cache_dtype, k_scales, v_scales,
+                         stream=stream)
 
 
 def pa_v2_decode_noalloc(output: torch.Tensor, query: torch.Tensor, key_cache: torch.Tensor,

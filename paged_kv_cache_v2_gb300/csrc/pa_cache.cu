@@ -29,6 +29,8 @@ struct CacheParams {
     const int64_t* slots;
     int Hk, D, bs, num_blocks;
     float k_scale, v_scale;
+    const float* k_scales;  // [Hk] per-kv-head scales replacing k_scale / v_scale, or nullptr
+    const float* v_scales;
     int vec;  // 1 when 16-byte source loads are aligned
 };
 
@@ -93,16 +95,24 @@ __global__ void __launch_bounds__(512) pa_cache_write_kernel(const CacheParams p
         const int64_t head = b * p.Hk + h;
         uint8_t* kdst = p.kcache + (((head * nchunk + ch) * p.bs + o) * X) * kvb;
         if constexpr (FP8) {
+            float ksc = p.k_scale, vsc = p.v_scale;
+            if (p.k_scales != nullptr) {
+                // this kv head's scales; one that is not finite and positive is flagged (bit 8)
+                ksc = p.k_scales[h];
+                vsc = p.v_scales[h];
+                if (ch == 0 && tok == 0 && !(ksc > 0.f && ksc < INFINITY && vsc > 0.f && vsc < INFINITY))
+                    atomicOr(&g_cache_errors, 256u);
+            }
             union { uint4 v; uint16_t h[8]; } kq;
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-                kq.h[i] = f32x2_to_e4m3x2(__fdiv_rn(to_f32<BF16>(kv[2 * i]), p.k_scale),
-                                          __fdiv_rn(to_f32<BF16>(kv[2 * i + 1]), p.k_scale));
+                kq.h[i] = f32x2_to_e4m3x2(__fdiv_rn(to_f32<BF16>(kv[2 * i]), ksc),
+                                          __fdiv_rn(to_f32<BF16>(kv[2 * i + 1]), ksc));
             *reinterpret_cast<uint4*>(kdst) = kq.v;
 #pragma unroll
             for (int i = 0; i < X; i += 2) {
-                const uint16_t q = f32x2_to_e4m3x2(__fdiv_rn(to_f32<BF16>(vv[i]), p.v_scale),
-                                                   __fdiv_rn(to_f32<BF16>(vv[i + 1]), p.v_scale));
+                const uint16_t q = f32x2_to_e4m3x2(__fdiv_rn(to_f32<BF16>(vv[i]), vsc),
+                                                   __fdiv_rn(to_f32<BF16>(vv[i + 1]), vsc));
                 const int64_t r = (head * p.D + ch * X + i) * p.bs + o;
                 p.vcache[r] = (uint8_t)(q & 0xff);
                 p.vcache[r + p.bs] = (uint8_t)(q >> 8);
@@ -127,12 +137,11 @@ cudaError_t pa::read_cache_errors(unsigned int* v, bool reset) {
     return cudaMemcpyToSymbol(g_cache_errors, &z, sizeof(z));
 }
 
-extern "C" pa_status pa_reshape_and_cache(const void* key, const void* value, int64_t key_stride_t,
-                                          int64_t value_stride_t, void* key_cache, void* value_cache,
-                                          const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
-                                          int head_size, int block_size, int num_blocks,
-                                          pa_dtype src_dtype, pa_kv_cache_dtype kv_cache_dtype,
-                                          float k_scale, float v_scale, cudaStream_t stream) {
+static pa_status cache_impl(const void* key, const void* value, int64_t key_stride_t, int64_t value_stride_t,
+                            void* key_cache, void* value_cache, const int64_t* slot_mapping, int num_tokens,
+                            int num_kv_heads, int head_size, int block_size, int num_blocks, pa_dtype src_dtype,
+                            pa_kv_cache_dtype kv_cache_dtype, float k_scale, float v_scale, const float* k_scales,
+                            const float* v_scales, cudaStream_t stream) {
     if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks <= 0) return PA_ERR_INVALID_ARG;
     if (src_dtype != PA_DT_F16 && src_dtype != PA_DT_BF16) return PA_ERR_UNSUPPORTED;
     if (kv_cache_dtype != PA_KV_AUTO && kv_cache_dtype != PA_KV_FP8_E4M3) return PA_ERR_INVALID_ARG;
@@ -145,6 +154,9 @@ extern "C" pa_status pa_reshape_and_cache(const void* key, const void* value, in
     if (head_size % x) return PA_ERR_INVALID_ARG;
     if (block_size != 8 && block_size != 16 && block_size != 32) return PA_ERR_UNSUPPORTED;
     if (!(k_scale > 0.f) || !isfinite(k_scale) || !(v_scale > 0.f) || !isfinite(v_scale)) return PA_ERR_INVALID_ARG;
+    if ((k_scales == nullptr) != (v_scales == nullptr) || (reinterpret_cast<uintptr_t>(k_scales) & 3) ||
+        (reinterpret_cast<uintptr_t>(v_scales) & 3))
+        return PA_ERR_INVALID_ARG;
     if (key_stride_t < (int64_t)num_kv_heads * head_size || value_stride_t < (int64_t)num_kv_heads * head_size)
         return PA_ERR_INVALID_ARG;
     if (num_tokens == 0) return PA_OK;
@@ -167,6 +179,8 @@ extern "C" pa_status pa_reshape_and_cache(const void* key, const void* value, in
     p.num_blocks = num_blocks;
     p.k_scale = k_scale;
     p.v_scale = v_scale;
+    p.k_scales = k_scales;
+    p.v_scales = v_scales;
     p.vec = ((reinterpret_cast<uintptr_t>(key) | reinterpret_cast<uintptr_t>(value)) & 15) == 0 &&
             (key_stride_t % 8) == 0 && (value_stride_t % 8) == 0;
     const bool bf16 = src_dtype == PA_DT_BF16;
@@ -190,4 +204,28 @@ extern "C" pa_status pa_reshape_and_cache(const void* key, const void* value, in
         return PA_ERR_CUDA;
     }
     return PA_OK;
+}
+
+extern "C" pa_status pa_reshape_and_cache(const void* key, const void* value, int64_t key_stride_t,
+                                          int64_t value_stride_t, void* key_cache, void* value_cache,
+                                          const int64_t* slot_mapping, int num_tokens, int num_kv_heads,
+                                          int head_size, int block_size, int num_blocks,
+                                          pa_dtype src_dtype, pa_kv_cache_dtype kv_cache_dtype,
+                                          float k_scale, float v_scale, cudaStream_t stream) {
+    return cache_impl(key, value, key_stride_t, value_stride_t, key_cache, value_cache, slot_mapping, num_tokens,
+                      num_kv_heads, head_size, block_size, num_blocks, src_dtype, kv_cache_dtype, k_scale, v_scale,
+                      nullptr, nullptr, stream);
+}
+
+extern "C" pa_status pa_reshape_and_cache_head_scales(const void* key, const void* value, int64_t key_stride_t,
+                                                      int64_t value_stride_t, void* key_cache, void* value_cache,
+                                                      const int64_t* slot_mapping, int num_tokens,
+                                                      int num_kv_heads, int head_size, int block_size,
+                                                      int num_blocks, pa_dtype src_dtype,
+                                                      pa_kv_cache_dtype kv_cache_dtype, const float* k_scales,
+                                                      const float* v_scales, cudaStream_t stream) {
+    if (k_scales == nullptr || v_scales == nullptr) return PA_ERR_INVALID_ARG;
+    return cache_impl(key, value, key_stride_t, value_stride_t, key_cache, value_cache, slot_mapping, num_tokens,
+                      num_kv_heads, head_size, block_size, num_blocks, src_dtype, kv_cache_dtype, 1.f, 1.f,
+                      k_scales, v_scales, stream);
 }

@@ -524,6 +524,8 @@ pa_status pa::validate_decode(const DecodeArgs& a) {
     if (a.block_size <= 0 || kPartition % a.block_size != 0) return PA_ERR_INVALID_ARG;
     if (a.block_size != 8 && a.block_size != 16 && a.block_size != 32) return PA_ERR_UNSUPPORTED;
     if (!(a.scale == a.scale) || !isfinite(a.scale)) return PA_ERR_INVALID_ARG;
+    if ((a.k_scales == nullptr) != (a.v_scales == nullptr) || !aligned(a.k_scales, 4) || !aligned(a.v_scales, 4))
+        return PA_ERR_INVALID_ARG;
     if (!(a.k_scale > 0.f) || !isfinite(a.k_scale) || !(a.v_scale > 0.f) || !isfinite(a.v_scale))
         return PA_ERR_INVALID_ARG;
     if (a.max_seq_len < 0 || a.max_num_partitions < 1) return PA_ERR_INVALID_ARG;
@@ -612,6 +614,7 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
         (void)cudaGetLastError();
         return PA_ERR_CUDA;
     }
+    optin -= kPhase1StaticSmem;  // the kernel's static shared memory comes out of the same budget
     // Ring depth: about kRingTarget bytes of pages per CTA, at least one slot per warp.  (A
     // deeper ring for small grids measured slower: 96 / 128 / 192 KiB gave 22.4 / 26.9 /
     // 27.3 us against 22.0 us on a two-sequence batch, as fewer CTAs then fit an SM.)
@@ -664,6 +667,9 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
     p1.ring_bytes = ring;
     p1.qk_scale_log2 = a.scale * a.k_scale * kLog2e;
     p1.v_scale = a.v_scale;
+    p1.k_scales = a.k_scales;
+    p1.v_scales = a.v_scales;
+    p1.scale = a.scale;
     p1.tmp16 = a.tmp_dtype != PA_DT_F32;
     p1.counters = nullptr;
     p1.merge = 0;
@@ -863,14 +869,14 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
     return PA_OK;
 }
 
-extern "C" pa_status pa_v2_decode(void* output, float* exp_sums, float* max_logits, void* tmp_output,
-                                  const void* query, const void* key_cache, const void* value_cache,
-                                  int num_seqs, int num_heads, int num_kv_heads, int head_size,
-                                  float scale, const int32_t* block_tables, int max_blocks_per_seq,
-                                  int num_blocks, const int32_t* seq_lens, int block_size,
-                                  int max_seq_len, int max_num_partitions, const float* alibi_slopes,
-                                  pa_dtype q_dtype, pa_kv_cache_dtype kv_cache_dtype, pa_dtype tmp_dtype,
-                                  float k_scale, float v_scale, cudaStream_t stream) {
+static pa_status decode_impl(void* output, float* exp_sums, float* max_logits, void* tmp_output,
+                             const void* query, const void* key_cache, const void* value_cache, int num_seqs,
+                             int num_heads, int num_kv_heads, int head_size, float scale,
+                             const int32_t* block_tables, int max_blocks_per_seq, int num_blocks,
+                             const int32_t* seq_lens, int block_size, int max_seq_len, int max_num_partitions,
+                             const float* alibi_slopes, pa_dtype q_dtype, pa_kv_cache_dtype kv_cache_dtype,
+                             pa_dtype tmp_dtype, float k_scale, float v_scale, const float* k_scales,
+                             const float* v_scales, cudaStream_t stream) {
     DecodeArgs a;
     a.output = output;
     a.exp_sums = exp_sums;
@@ -897,6 +903,8 @@ extern "C" pa_status pa_v2_decode(void* output, float* exp_sums, float* max_logi
     a.tmp_dtype = tmp_dtype;
     a.k_scale = k_scale;
     a.v_scale = v_scale;
+    a.k_scales = k_scales;
+    a.v_scales = v_scales;
     a.stream = stream;
     pa_status st = validate_decode(a);
     if (st != PA_OK || num_seqs == 0) return st;
@@ -904,6 +912,36 @@ extern "C" pa_status pa_v2_decode(void* output, float* exp_sums, float* max_logi
                            max_seq_len, stream);
     if (st != PA_OK) return st;
     return launch_decode(a, exp_sums, max_logits, tmp_output);
+}
+
+extern "C" pa_status pa_v2_decode(void* output, float* exp_sums, float* max_logits, void* tmp_output,
+                                  const void* query, const void* key_cache, const void* value_cache,
+                                  int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                                  float scale, const int32_t* block_tables, int max_blocks_per_seq,
+                                  int num_blocks, const int32_t* seq_lens, int block_size,
+                                  int max_seq_len, int max_num_partitions, const float* alibi_slopes,
+                                  pa_dtype q_dtype, pa_kv_cache_dtype kv_cache_dtype, pa_dtype tmp_dtype,
+                                  float k_scale, float v_scale, cudaStream_t stream) {
+    return decode_impl(output, exp_sums, max_logits, tmp_output, query, key_cache, value_cache, num_seqs,
+                       num_heads, num_kv_heads, head_size, scale, block_tables, max_blocks_per_seq, num_blocks,
+                       seq_lens, block_size, max_seq_len, max_num_partitions, alibi_slopes, q_dtype,
+                       kv_cache_dtype, tmp_dtype, k_scale, v_scale, nullptr, nullptr, stream);
+}
+
+extern "C" pa_status pa_v2_decode_head_scales(void* output, float* exp_sums, float* max_logits, void* tmp_output,
+                                              const void* query, const void* key_cache, const void* value_cache,
+                                              int num_seqs, int num_heads, int num_kv_heads, int head_size,
+                                              float scale, const int32_t* block_tables, int max_blocks_per_seq,
+                                              int num_blocks, const int32_t* seq_lens, int block_size,
+                                              int max_seq_len, int max_num_partitions, const float* alibi_slopes,
+                                              pa_dtype q_dtype, pa_kv_cache_dtype kv_cache_dtype,
+                                              pa_dtype tmp_dtype, const float* k_scales, const float* v_scales,
+                                              cudaStream_t stream) {
+    if (k_scales == nullptr || v_scales == nullptr) return PA_ERR_INVALID_ARG;
+    return decode_impl(output, exp_sums, max_logits, tmp_output, query, key_cache, value_cache, num_seqs,
+                       num_heads, num_kv_heads, head_size, scale, block_tables, max_blocks_per_seq, num_blocks,
+                       seq_lens, block_size, max_seq_len, max_num_partitions, alibi_slopes, q_dtype,
+                       kv_cache_dtype, tmp_dtype, 1.f, 1.f, k_scales, v_scales, stream);
 }
 
 extern "C" int64_t pa_v2_decode_num_counters(int num_seqs, int num_heads, int num_kv_heads) {
@@ -958,16 +996,15 @@ extern "C" pa_status pa_v2_decode_fused(void* output, float* exp_sums, float* ma
     return launch_decode(a, exp_sums, max_logits, tmp_output, counters);
 }
 
-extern "C" pa_status pa_v2_decode_append(void* output, float* exp_sums, float* max_logits, void* tmp_output,
-                                         const void* query, const void* key, const void* value,
-                                         int64_t key_stride_s, int64_t value_stride_s, void* key_cache,
-                                         void* value_cache, int num_seqs, int num_heads, int num_kv_heads,
-                                         int head_size, float scale, const int32_t* block_tables,
-                                         int max_blocks_per_seq, int num_blocks, const int32_t* seq_lens,
-                                         int block_size, int max_seq_len, int max_num_partitions,
-                                         const float* alibi_slopes, pa_dtype q_dtype,
-                                         pa_kv_cache_dtype kv_cache_dtype, pa_dtype tmp_dtype, float k_scale,
-                                         float v_scale, cudaStream_t stream) {
+static pa_status append_impl(void* output, float* exp_sums, float* max_logits, void* tmp_output,
+                             const void* query, const void* key, const void* value, int64_t key_stride_s,
+                             int64_t value_stride_s, void* key_cache, void* value_cache, int num_seqs,
+                             int num_heads, int num_kv_heads, int head_size, float scale,
+                             const int32_t* block_tables, int max_blocks_per_seq, int num_blocks,
+                             const int32_t* seq_lens, int block_size, int max_seq_len, int max_num_partitions,
+                             const float* alibi_slopes, pa_dtype q_dtype, pa_kv_cache_dtype kv_cache_dtype,
+                             pa_dtype tmp_dtype, float k_scale, float v_scale, const float* k_scales,
+                             const float* v_scales, cudaStream_t stream) {
     DecodeArgs a;
     a.output = output;
     a.exp_sums = exp_sums;
@@ -995,6 +1032,8 @@ extern "C" pa_status pa_v2_decode_append(void* output, float* exp_sums, float* m
     a.k_scale = k_scale;
     a.v_scale = v_scale;
     a.stream = stream;
+    a.k_scales = k_scales;
+    a.v_scales = v_scales;
     a.new_key = key;
     a.new_value = value;
     a.new_key_stride = key_stride_s;
@@ -1010,6 +1049,36 @@ extern "C" pa_status pa_v2_decode_append(void* output, float* exp_sums, float* m
                            max_seq_len, stream);
     if (st != PA_OK) return st;
     return launch_decode(a, exp_sums, max_logits, tmp_output);
+}
+
+extern "C" pa_status pa_v2_decode_append(void* output, float* exp_sums, float* max_logits, void* tmp_output,
+                                         const void* query, const void* key, const void* value,
+                                         int64_t key_stride_s, int64_t value_stride_s, void* key_cache,
+                                         void* value_cache, int num_seqs, int num_heads, int num_kv_heads,
+                                         int head_size, float scale, const int32_t* block_tables,
+                                         int max_blocks_per_seq, int num_blocks, const int32_t* seq_lens,
+                                         int block_size, int max_seq_len, int max_num_partitions,
+                                         const float* alibi_slopes, pa_dtype q_dtype,
+                                         pa_kv_cache_dtype kv_cache_dtype, pa_dtype tmp_dtype, float k_scale,
+                                         float v_scale, cudaStream_t stream) {
+    return append_impl(output, exp_sums, max_logits, tmp_output, query, key, value, key_stride_s, value_stride_s,
+                       key_cache, value_cache, num_seqs, num_heads, num_kv_heads, head_size, scale, block_tables,
+                       max_blocks_per_seq, num_blocks, seq_lens, block_size, max_seq_len, max_num_partitions,
+                       alibi_slopes, q_dtype, kv_cache_dtype, tmp_dtype, k_scale, v_scale, nullptr, nullptr, stream);
+}
+
+extern "C" pa_status pa_v2_decode_append_head_scales(
+    void* output, float* exp_sums, float* max_logits, void* tmp_output, const void* query, const void* key,
+    const void* value, int64_t key_stride_s, int64_t value_stride_s, void* key_cache, void* value_cache,
+    int num_seqs, int num_heads, int num_kv_heads, int head_size, float scale, const int32_t* block_tables,
+    int max_blocks_per_seq, int num_blocks, const int32_t* seq_lens, int block_size, int max_seq_len,
+    int max_num_partitions, const float* alibi_slopes, pa_dtype q_dtype, pa_kv_cache_dtype kv_cache_dtype,
+    pa_dtype tmp_dtype, const float* k_scales, const float* v_scales, cudaStream_t stream) {
+    if (k_scales == nullptr || v_scales == nullptr) return PA_ERR_INVALID_ARG;
+    return append_impl(output, exp_sums, max_logits, tmp_output, query, key, value, key_stride_s, value_stride_s,
+                       key_cache, value_cache, num_seqs, num_heads, num_kv_heads, head_size, scale, block_tables,
+                       max_blocks_per_seq, num_blocks, seq_lens, block_size, max_seq_len, max_num_partitions,
+                       alibi_slopes, q_dtype, kv_cache_dtype, tmp_dtype, 1.f, 1.f, k_scales, v_scales, stream);
 }
 
 // ---------------------------------------------------------------------------------------

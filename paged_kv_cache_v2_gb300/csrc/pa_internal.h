@@ -26,6 +26,9 @@ struct DecodeArgs {
     pa_kv_cache_dtype kv_cache_dtype;
     pa_dtype tmp_dtype;
     float k_scale, v_scale;
+    // one scale per kv head (device, [num_kv_heads]) in place of k_scale / v_scale, or null
+    const float* k_scales = nullptr;
+    const float* v_scales = nullptr;
     cudaStream_t stream;
     // fused cache append (pa_v2_decode_append): the newest token's key/value rows, or null
     const void* new_key = nullptr;

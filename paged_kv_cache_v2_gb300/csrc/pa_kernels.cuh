@@ -24,6 +24,8 @@ namespace pa {
 
 constexpr int kPartition = 512;
 constexpr int kWarps = PA_PHASE1_WARPS;  // phase-1 warps per CTA
+// phase 1's static shared memory: per warp, the value scale and the two encode divisors
+constexpr int kPhase1StaticSmem = kWarps * 3 * (int)sizeof(float);
 constexpr uint32_t kRingTarget = PA_RING_KIB * 1024u;  // shared-memory page ring per CTA
 constexpr int kMaxHeadsPerCta = 8;     // the MMA N dimension
 // Fused combine: most bytes of rows the last CTA of a (sequence, head group) merges.
@@ -50,6 +52,12 @@ struct Phase1Params {
     uint32_t ring_bytes;  // kWarps * nstage * slot bytes
     float qk_scale_log2;  // scale * k_scale * log2(e)
     float v_scale;
+    // One k_scale / v_scale per kv head ([Hk] floats, device), or nullptr: then qk_scale_log2,
+    // v_scale, k_enc and v_enc come from k_scales[kvh] / v_scales[kvh] (scale * k * log2(e)
+    // rounded in that order, as the host rounds the per-tensor product).
+    const float* k_scales;
+    const float* v_scales;
+    float scale;
     int tmp16;  // tmp_output holds the output dtype instead of fp32
     // Combine fused into phase 1 (counters != nullptr): the last CTA of a (sequence, head
     // group) to finish merges the partitions; counters[s * gridDim.y + blockIdx.y] counts the

@@ -143,7 +143,8 @@ __device__ __forceinline__ float row_f32(uint16_t v) {
 // lane + 32, ...
 template <bool BF16, int KVB, int D, int BS>
 __device__ __forceinline__ void append_token(const Phase1Params& p, const uint16_t* nrow, uint8_t* kpage,
-                                             uint8_t* vpage, int o, int64_t page, int lane) {
+                                             uint8_t* vpage, int o, int64_t page, int lane, float k_enc,
+                                             float v_enc) {
     constexpr int X = 16 / KVB;  // elements per 16-byte chunk
     constexpr uint32_t page_bytes = (uint32_t)D * BS * KVB;
     uint8_t* kc = page >= 0 ? const_cast<uint8_t*>(p.kcache) + page * page_bytes : nullptr;
@@ -156,8 +157,8 @@ __device__ __forceinline__ void append_token(const Phase1Params& p, const uint16
             uint16_t q[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-                q[i] = f32x2_to_e4m3x2(__fdiv_rn(row_f32<BF16>(nrow[c * X + 2 * i]), p.k_enc),
-                                       __fdiv_rn(row_f32<BF16>(nrow[c * X + 2 * i + 1]), p.k_enc));
+                q[i] = f32x2_to_e4m3x2(__fdiv_rn(row_f32<BF16>(nrow[c * X + 2 * i]), k_enc),
+                                       __fdiv_rn(row_f32<BF16>(nrow[c * X + 2 * i + 1]), k_enc));
             chunk = make_uint4((uint32_t)q[0] | ((uint32_t)q[1] << 16), (uint32_t)q[2] | ((uint32_t)q[3] << 16),
                                (uint32_t)q[4] | ((uint32_t)q[5] << 16), (uint32_t)q[6] | ((uint32_t)q[7] << 16));
         }
@@ -172,7 +173,7 @@ __device__ __forceinline__ void append_token(const Phase1Params& p, const uint16
             *reinterpret_cast<uint16_t*>(vpage + off) = v;
             if (vc) *reinterpret_cast<uint16_t*>(vc + off) = v;
         } else {
-            const uint8_t v = (uint8_t)(f32x2_to_e4m3x2(__fdiv_rn(row_f32<BF16>(nrow[D + i]), p.v_enc), 0.f) & 0xffu);
+            const uint8_t v = (uint8_t)(f32x2_to_e4m3x2(__fdiv_rn(row_f32<BF16>(nrow[D + i]), v_enc), 0.f) & 0xffu);
             vpage[off] = v;
             if (vc) vc[off] = v;
         }
@@ -458,9 +459,31 @@ pa_v2_phase1_kernel(const Phase1Params p) {
         if (2 * t < nh) sl0 = p.alibi[h0 + 2 * t] * kLog2e;
         if (2 * t + 1 < nh) sl1 = p.alibi[h0 + 2 * t + 1] * kLog2e;
     }
-    const float qk_mul = p.qk_scale_log2;
+    // k_scale / v_scale: per tensor, or this kv head's (read after the dependency wait, like
+    // every input); a per-head scale that is not finite and positive is flagged (bit 8) and
+    // used as given.  The value-side factor and the encode divisors wait in shared memory
+    // (one copy per warp) for the epilogue and the append, so the page loop holds only the
+    // score multiplier in a register.
+    __shared__ float wscale[kWarps][3];  // v_scale, k_scale and v_scale of the fp8 encode
+    static_assert(sizeof(wscale) == kPhase1StaticSmem, "the host sizes shared memory with this");
+    float qk_mul = p.qk_scale_log2;
+    if (p.k_scales != nullptr) {
+        const float ks = p.k_scales[kvh], vs = p.v_scales[kvh];
+        if (threadIdx.x == 0 && bx == 0 && s == 0 && !(ks > 0.f && ks < INFINITY && vs > 0.f && vs < INFINITY))
+            flag_error(256u);
+        qk_mul = __fmul_rn(__fmul_rn(p.scale, ks), kLog2e);
+        if (lane == 0) {
+            wscale[warp][0] = vs;
+            wscale[warp][1] = ks;
+            wscale[warp][2] = vs;
+        }
+    } else if (lane == 0) {
+        wscale[warp][0] = p.v_scale;
+        wscale[warp][1] = p.k_enc;
+        wscale[warp][2] = p.v_enc;
+    }
+    __syncwarp();
     const float qk_mul0 = qk_mul * qs0, qk_mul1 = qk_mul * qs1;  // fp8 with a bf16 query: per-column scale
-    const float v_mul = p.v_scale;
 
     // Per-lane ldmatrix row of the K page: token within the 16-token tile, chunk offset.
     const int k_tok = FP8 ? c_fp8_row_token[(lane & 7) + 8 * ((lane >> 3) & 1)] : (lane & 7) + 8 * ((lane >> 3) & 1);
@@ -521,7 +544,8 @@ pa_v2_phase1_kernel(const Phase1Params p) {
                     const bool to_cache = grp == 0;
                     append_token<BF16, KVB, D, BS>(p, nrow, const_cast<uint8_t*>(kslot) + (size_t)pg * page_bytes,
                                                    const_cast<uint8_t*>(vslot) + (size_t)pg * page_bytes, (L - 1) & (bs - 1),
-                                                   to_cache ? (int64_t)b * p.Hk + kvh : -1, lane);
+                                                   to_cache ? (int64_t)b * p.Hk + kvh : -1, lane, wscale[warp][1],
+                                                   wscale[warp][2]);
                 }
                 __syncwarp();
             }
@@ -906,7 +930,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
 #pragma unroll
                     for (int w = 0; w < kWarps; ++w) v += red_o[(w * nh + hh) * RS + i];
                     const float lt = fin_l[hh];
-                    st_cluster_f32(dst + 4u * (2 * kMaxHeadsPerCta + e), lt > 0.f ? v * (v_mul / lt) : 0.f);
+                    st_cluster_f32(dst + 4u * (2 * kMaxHeadsPerCta + e), lt > 0.f ? v * (wscale[0][0] / lt) : 0.f);
                 }
             }
             cluster_sync_all();
@@ -947,7 +971,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
 #pragma unroll
                 for (int w = 0; w < kWarps; ++w) v += red_o[(w * nh + hh) * RS + i];
                 const float lt = fin_l[hh];
-                v = lt > 0.f ? v * (v_mul / lt) : 0.f;
+                v = lt > 0.f ? v * (wscale[0][0] / lt) : 0.f;
                 const float fo = fac_o[hh];
                 float r = v * fac_n[hh];
                 if (fo != 0.f && !first) r = fmaf(mrg[e], fo, r);
@@ -966,11 +990,11 @@ pa_v2_phase1_kernel(const Phase1Params p) {
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) v += red_o[(w * nh + hh) * RS + i];
             if (K > 1) {
-                v *= v_mul * fac_o[hh];
+                v *= wscale[0][0] * fac_o[hh];
                 for (int k = 0; k < K - 1; ++k) v = fmaf(pbuf[k * pstride + 2 * kMaxHeadsPerCta + e], pbuf[k * pstride + hh], v);
             } else {
                 const float lt = fin_l[hh];
-                v = lt > 0.f ? v * (v_mul / lt) : 0.f;
+                v = lt > 0.f ? v * (wscale[0][0] / lt) : 0.f;
             }
             const int64_t row = (int64_t)s * H + h0 + hh;
             if (direct)

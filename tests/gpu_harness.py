@@ -39,6 +39,14 @@ def to_device(wl, device="cuda"):
     )
 
 
+def device_scales(wl):
+    """The workload's k/v scales as the binding takes them: two floats, or two float32 CUDA
+    tensors of num_kv_heads values (per-kv-head scales)."""
+    if wl.k_scales is None:
+        return wl.k_scale, wl.v_scale
+    return wl.k_scales.to("cuda"), wl.v_scales.to("cuda")
+
+
 def run_decode(wl, dev=None, max_num_partitions=None, max_seq_len=None, poison=True,
                tmp_dtype=torch.float32, counters=None, stream=None):
     """pa_v2_decode on a workload (pa_v2_decode_fused when `counters` is given); returns CPU
@@ -53,9 +61,10 @@ def run_decode(wl, dev=None, max_num_partitions=None, max_seq_len=None, poison=T
     es = torch.full((S, H, P), fill, dtype=torch.float32, device="cuda")
     ml = torch.full((S, H, P), fill, dtype=torch.float32, device="cuda")
     tmp = torch.full((S, H, P, d), fill, dtype=tmp_dtype, device="cuda")
+    ks, vs = device_scales(wl)
     pa.pa_v2_decode(out, es, ml, tmp, dev["query"], dev["key_cache"], dev["value_cache"],
                     wl.num_kv_heads, wl.scale, dev["block_tables"], dev["seq_lens"], wl.block_size,
-                    msl, dev["alibi"], wl.kv_cache_dtype, wl.k_scale, wl.v_scale, counters=counters,
+                    msl, dev["alibi"], wl.kv_cache_dtype, ks, vs, counters=counters,
                     stream=stream)
     torch.cuda.synchronize()
     return out.cpu(), es.cpu(), ml.cpu(), tmp.cpu()

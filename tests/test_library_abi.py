@@ -112,6 +112,37 @@ def test_fused_decode_host_checks():
     assert lib.pa_v2_decode_fused(*zero, None, 0, None) == 0
 
 
+def test_head_scale_entry_points_host_checks():
+    # arguments as the per-tensor entry points, with two device arrays in place of the floats;
+    # every case below is rejected (or is a no-op) before anything touches the device
+    lib = pa.load()
+    P = 0x10000
+    for name in ("pa_v2_decode_head_scales", "pa_v2_decode_append_head_scales", "pa_reshape_and_cache_head_scales"):
+        assert name in _declared()
+    dec = [P, P, P, P, P, P, P, 2, 8, 2, 128, 0.088, P, 64, 100, P, 16, 1024, 2, None, 0, 0, 2]
+    assert lib.pa_v2_decode_head_scales(*dec, None, P, None) == 1          # no k_scales
+    assert lib.pa_v2_decode_head_scales(*dec, P, None, None) == 1          # no v_scales
+    assert lib.pa_v2_decode_head_scales(*dec, P + 2, P, None) == 1         # misaligned
+    bad = list(dec)
+    bad[9] = 3                                                             # H % Hk != 0
+    assert lib.pa_v2_decode_head_scales(*bad, P, P, None) == 1
+    zero = list(dec)
+    zero[7] = 0
+    assert lib.pa_v2_decode_head_scales(*zero, P, P, None) == 0            # no sequences
+    app = [P, P, P, P, P, P, P, 256, 256, P, P, 2, 8, 2, 128, 0.088, P, 64, 100, P, 16, 1024, 2, None, 0, 0, 2]
+    assert lib.pa_v2_decode_append_head_scales(*app, None, P, None) == 1
+    assert lib.pa_v2_decode_append_head_scales(*app, P, P + 1, None) == 1
+    short = list(app)
+    short[7] = 100                                                         # key rows shorter than Hk * d
+    assert lib.pa_v2_decode_append_head_scales(*short, P, P, None) == 1
+    wr = [P, P, 256, 256, P, P, P, 4, 2, 128, 16, 10, 0, 1]
+    assert lib.pa_reshape_and_cache_head_scales(*wr, None, P, None) == 1
+    assert lib.pa_reshape_and_cache_head_scales(*wr, P, P + 2, None) == 1
+    wr0 = list(wr)
+    wr0[7] = 0
+    assert lib.pa_reshape_and_cache_head_scales(*wr0, P, P, None) == 0     # no tokens
+
+
 def _cache_raw(**over):
     lib = pa.load()
     P = 0x10000

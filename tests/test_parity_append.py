@@ -24,7 +24,7 @@ import torch
 import oracle
 import paged_kv_cache_v2_gb300 as pa
 import workloads
-from gpu_harness import check_decode, sample_pairs
+from gpu_harness import check_decode, device_scales, sample_pairs
 
 pytestmark = pytest.mark.gpu
 
@@ -46,7 +46,7 @@ def oracle_append(wl, slots=None):
     kr, vr = oracle._np(wl.key_cache).copy(), oracle._np(wl.value_cache).copy()
     oracle.reshape_and_cache(wl.new_key, wl.new_value, wl.q_dtype, kr, vr, wl.kv_storage,
                              wl.slot_mapping if slots is None else slots, block_size=wl.block_size,
-                             k_scale=wl.k_scale, v_scale=wl.v_scale)
+                             k_scale=wl.k_scales_or_scalar(), v_scale=wl.v_scales_or_scalar())
     return kr, vr, oracle.decode_workload(wl, key_cache=kr, value_cache=vr)
 
 
@@ -65,8 +65,9 @@ def run_append(wl, key=None, value=None):
     tmp = torch.full((S, H, P, d), float("nan"), dtype=torch.float32, device=dev)
     nk = wl.new_key.to(dev) if key is None else key
     nv = wl.new_value.to(dev) if value is None else value
+    ks, vs = device_scales(wl)
     pa.pa_v2_decode_append(out, es, ml, tmp, q, nk, nv, kc, vc, wl.num_kv_heads, wl.scale, bt, sl, wl.block_size,
-                           wl.max_seq_len, slopes, wl.kv_cache_dtype, wl.k_scale, wl.v_scale)
+                           wl.max_seq_len, slopes, wl.kv_cache_dtype, ks, vs)
     torch.cuda.synchronize()
     return (out.cpu(), es.cpu(), ml.cpu(), tmp.cpu()), kc.cpu(), vc.cpu()
 
