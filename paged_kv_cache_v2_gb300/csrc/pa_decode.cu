@@ -375,11 +375,11 @@ static bool supported_head_size(int d) {
     }
 }
 
-static Phase1Fn phase1_for(bool bf16, bool fp8, int d, int bs) {
+static Phase1Fn phase1_for(bool bf16, bool fp8, int d, int bs, bool head_scales) {
     switch (bs) {
-        case 8: return phase1_select<8>(bf16, fp8, d);
-        case 16: return phase1_select<16>(bf16, fp8, d);
-        case 32: return phase1_select<32>(bf16, fp8, d);
+        case 8: return fp8 ? phase1_select<8, 1>(bf16, d, head_scales) : phase1_select<8, 2>(bf16, d, head_scales);
+        case 16: return fp8 ? phase1_select<16, 1>(bf16, d, head_scales) : phase1_select<16, 2>(bf16, d, head_scales);
+        case 32: return fp8 ? phase1_select<32, 1>(bf16, d, head_scales) : phase1_select<32, 2>(bf16, d, head_scales);
         default: return nullptr;
     }
 }
@@ -478,11 +478,14 @@ extern "C" const char* pa_status_string(pa_status status) {
 }
 
 cudaError_t pa::read_decode_errors(unsigned int* v, bool reset) {
-    unsigned int a = 0, b = 0, c = 0;
-    cudaError_t e = phase1_read_errors<8>(&a, reset);
-    if (e == cudaSuccess) e = phase1_read_errors<16>(&b, reset);
-    if (e == cudaSuccess) e = phase1_read_errors<32>(&c, reset);
-    *v = a | b | c;
+    unsigned int w[6] = {};
+    cudaError_t e = phase1_read_errors<8, 2>(&w[0], reset);
+    if (e == cudaSuccess) e = phase1_read_errors<16, 2>(&w[1], reset);
+    if (e == cudaSuccess) e = phase1_read_errors<32, 2>(&w[2], reset);
+    if (e == cudaSuccess) e = phase1_read_errors<8, 1>(&w[3], reset);
+    if (e == cudaSuccess) e = phase1_read_errors<16, 1>(&w[4], reset);
+    if (e == cudaSuccess) e = phase1_read_errors<32, 1>(&w[5], reset);
+    *v = w[0] | w[1] | w[2] | w[3] | w[4] | w[5];
     return e;
 }
 
@@ -636,7 +639,7 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
     const size_t nrow_off = (smem_for(nstage) + 15) & ~(size_t)15;
     size_t smem1 = nrow_off + app_bytes;
 
-    Phase1Fn fn = phase1_for(bf16, fp8, D, bs);
+    Phase1Fn fn = phase1_for(bf16, fp8, D, bs, a.k_scales != nullptr);
     if (fn == nullptr) return PA_ERR_UNSUPPORTED;
     if (smem1 > (size_t)optin) return PA_ERR_UNSUPPORTED;
     if (ensure_smem((const void*)fn, smem1) != cudaSuccess) {

@@ -104,12 +104,14 @@ __device__ __forceinline__ void store_out(void* out, int64_t idx, float v) {
 
 using Phase1Fn = void (*)(const Phase1Params);
 
-// Phase-1 kernel for (query dtype, fp8 cache?, head size) at block size BS, or nullptr;
-// defined in pa_phase1_bs<BS>.cu.
-template <int BS>
-Phase1Fn phase1_select(bool bf16, bool fp8, int d);
-// Read (and optionally clear) the device error word of the block-size-BS phase-1 kernels.
-template <int BS>
+// Phase-1 kernel for (query dtype, head size, per-kv-head scales?) at block size BS and cache
+// element bytes KVB (2: fp16/bf16, 1: fp8), or nullptr; defined in pa_phase1_bs<BS>.cu
+// (KVB 2) and pa_phase1_bs<BS>_fp8.cu (KVB 1), one translation unit each so they build in
+// parallel.
+template <int BS, int KVB>
+Phase1Fn phase1_select(bool bf16, int d, bool head_scales);
+// Read (and optionally clear) the device error word of those kernels (one per unit).
+template <int BS, int KVB>
 cudaError_t phase1_read_errors(unsigned int* v, bool reset);
 
 }  // namespace pa

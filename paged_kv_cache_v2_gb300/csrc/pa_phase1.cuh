@@ -188,7 +188,11 @@ __device__ __forceinline__ void append_token(const Phase1Params& p, const uint16
 #ifndef PA_FP8_MIN_CTAS
 #define PA_FP8_MIN_CTAS 3
 #endif
-template <bool BF16, int KVB, int D, int BS>
+// HS: the kernel reads per-kv-head scales when p.k_scales is set.  16-bit caches always take
+// that form; fp8 caches also have an HS = false form for per-tensor scales, whose page loop
+// keeps the score multiplier in the constant bank (one register fewer: measured 1.3% on the
+// fp8 batch, where the kernel is at its register cap).
+template <bool BF16, int KVB, int D, int BS, bool HS>
 __global__ void __launch_bounds__(kWarps * 32, KVB == 2 ? (D <= 96 ? 16 : 12) / kWarps
                                                         : ((BF16 && D >= 192) ? 8 : 4 * PA_FP8_MIN_CTAS) / kWarps)
 pa_v2_phase1_kernel(const Phase1Params p) {
@@ -467,22 +471,37 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     __shared__ float wscale[kWarps][3];  // v_scale, k_scale and v_scale of the fp8 encode
     static_assert(sizeof(wscale) == kPhase1StaticSmem, "the host sizes shared memory with this");
     float qk_mul = p.qk_scale_log2;
-    if (p.k_scales != nullptr) {
-        const float ks = p.k_scales[kvh], vs = p.v_scales[kvh];
-        if (threadIdx.x == 0 && bx == 0 && s == 0 && !(ks > 0.f && ks < INFINITY && vs > 0.f && vs < INFINITY))
-            flag_error(256u);
-        qk_mul = __fmul_rn(__fmul_rn(p.scale, ks), kLog2e);
-        if (lane == 0) {
-            wscale[warp][0] = vs;
-            wscale[warp][1] = ks;
-            wscale[warp][2] = vs;
+    if constexpr (HS) {
+        if (p.k_scales != nullptr) {
+            const float ks = p.k_scales[kvh], vs = p.v_scales[kvh];
+            if (threadIdx.x == 0 && bx == 0 && s == 0 && !(ks > 0.f && ks < INFINITY && vs > 0.f && vs < INFINITY))
+                flag_error(256u);
+            qk_mul = __fmul_rn(__fmul_rn(p.scale, ks), kLog2e);
+            if (lane == 0) {
+                wscale[warp][0] = vs;
+                wscale[warp][1] = ks;
+                wscale[warp][2] = vs;
+            }
+        } else if (lane == 0) {
+            wscale[warp][0] = p.v_scale;
+            wscale[warp][1] = p.k_enc;
+            wscale[warp][2] = p.v_enc;
         }
-    } else if (lane == 0) {
-        wscale[warp][0] = p.v_scale;
-        wscale[warp][1] = p.k_enc;
-        wscale[warp][2] = p.v_enc;
+        __syncwarp();
     }
-    __syncwarp();
+    // the value scale (read in the epilogue, after CTA barriers) and the encode divisors
+    auto v_mul = [&]() -> float {
+        if constexpr (HS) return wscale[0][0];
+        else return p.v_scale;
+    };
+    auto enc_k = [&]() -> float {
+        if constexpr (HS) return wscale[warp][1];
+        else return p.k_enc;
+    };
+    auto enc_v = [&]() -> float {
+        if constexpr (HS) return wscale[warp][2];
+        else return p.v_enc;
+    };
     const float qk_mul0 = qk_mul * qs0, qk_mul1 = qk_mul * qs1;  // fp8 with a bf16 query: per-column scale
 
     // Per-lane ldmatrix row of the K page: token within the 16-token tile, chunk offset.
@@ -544,8 +563,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
                     const bool to_cache = grp == 0;
                     append_token<BF16, KVB, D, BS>(p, nrow, const_cast<uint8_t*>(kslot) + (size_t)pg * page_bytes,
                                                    const_cast<uint8_t*>(vslot) + (size_t)pg * page_bytes, (L - 1) & (bs - 1),
-                                                   to_cache ? (int64_t)b * p.Hk + kvh : -1, lane, wscale[warp][1],
-                                                   wscale[warp][2]);
+                                                   to_cache ? (int64_t)b * p.Hk + kvh : -1, lane, enc_k(), enc_v());
                 }
                 __syncwarp();
             }
@@ -930,7 +948,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
 #pragma unroll
                     for (int w = 0; w < kWarps; ++w) v += red_o[(w * nh + hh) * RS + i];
                     const float lt = fin_l[hh];
-                    st_cluster_f32(dst + 4u * (2 * kMaxHeadsPerCta + e), lt > 0.f ? v * (wscale[0][0] / lt) : 0.f);
+                    st_cluster_f32(dst + 4u * (2 * kMaxHeadsPerCta + e), lt > 0.f ? v * (v_mul() / lt) : 0.f);
                 }
             }
             cluster_sync_all();
@@ -971,7 +989,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
 #pragma unroll
                 for (int w = 0; w < kWarps; ++w) v += red_o[(w * nh + hh) * RS + i];
                 const float lt = fin_l[hh];
-                v = lt > 0.f ? v * (wscale[0][0] / lt) : 0.f;
+                v = lt > 0.f ? v * (v_mul() / lt) : 0.f;
                 const float fo = fac_o[hh];
                 float r = v * fac_n[hh];
                 if (fo != 0.f && !first) r = fmaf(mrg[e], fo, r);
@@ -990,11 +1008,11 @@ pa_v2_phase1_kernel(const Phase1Params p) {
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) v += red_o[(w * nh + hh) * RS + i];
             if (K > 1) {
-                v *= wscale[0][0] * fac_o[hh];
+                v *= v_mul() * fac_o[hh];
                 for (int k = 0; k < K - 1; ++k) v = fmaf(pbuf[k * pstride + 2 * kMaxHeadsPerCta + e], pbuf[k * pstride + hh], v);
             } else {
                 const float lt = fin_l[hh];
-                v = lt > 0.f ? v * (wscale[0][0] / lt) : 0.f;
+                v = lt > 0.f ? v * (v_mul() / lt) : 0.f;
             }
             const int64_t row = (int64_t)s * H + h0 + hh;
             if (direct)
@@ -1060,30 +1078,34 @@ pa_v2_phase1_kernel(const Phase1Params p) {
 }
 
 
-template <bool BF16, int KVB, int BS>
+template <bool BF16, int KVB, int BS, bool HS>
 static Phase1Fn pick_phase1(int d) {
     switch (d) {
-        case 64: return pa_v2_phase1_kernel<BF16, KVB, 64, BS>;
-        case 80: return pa_v2_phase1_kernel<BF16, KVB, 80, BS>;
-        case 96: return pa_v2_phase1_kernel<BF16, KVB, 96, BS>;
-        case 112: return pa_v2_phase1_kernel<BF16, KVB, 112, BS>;
-        case 128: return pa_v2_phase1_kernel<BF16, KVB, 128, BS>;
-        case 192: return pa_v2_phase1_kernel<BF16, KVB, 192, BS>;
-        case 256: return pa_v2_phase1_kernel<BF16, KVB, 256, BS>;
+        case 64: return pa_v2_phase1_kernel<BF16, KVB, 64, BS, HS>;
+        case 80: return pa_v2_phase1_kernel<BF16, KVB, 80, BS, HS>;
+        case 96: return pa_v2_phase1_kernel<BF16, KVB, 96, BS, HS>;
+        case 112: return pa_v2_phase1_kernel<BF16, KVB, 112, BS, HS>;
+        case 128: return pa_v2_phase1_kernel<BF16, KVB, 128, BS, HS>;
+        case 192: return pa_v2_phase1_kernel<BF16, KVB, 192, BS, HS>;
+        case 256: return pa_v2_phase1_kernel<BF16, KVB, 256, BS, HS>;
         case 120:
-            if constexpr (KVB == 2) return pa_v2_phase1_kernel<BF16, KVB, 120, BS>;
+            if constexpr (KVB == 2) return pa_v2_phase1_kernel<BF16, KVB, 120, BS, HS>;
             else return nullptr;
         default: return nullptr;
     }
 }
 
-template <int BS>
-Phase1Fn phase1_select(bool bf16, bool fp8, int d) {
-    if (bf16) return fp8 ? pick_phase1<true, 1, BS>(d) : pick_phase1<true, 2, BS>(d);
-    return fp8 ? pick_phase1<false, 1, BS>(d) : pick_phase1<false, 2, BS>(d);
+template <int BS, int KVB>
+Phase1Fn phase1_select(bool bf16, int d, bool head_scales) {
+    if constexpr (KVB == 2) {
+        return bf16 ? pick_phase1<true, 2, BS, true>(d) : pick_phase1<false, 2, BS, true>(d);
+    } else {
+        if (head_scales) return bf16 ? pick_phase1<true, 1, BS, true>(d) : pick_phase1<false, 1, BS, true>(d);
+        return bf16 ? pick_phase1<true, 1, BS, false>(d) : pick_phase1<false, 1, BS, false>(d);
+    }
 }
 
-template <int BS>
+template <int BS, int KVB>
 cudaError_t phase1_read_errors(unsigned int* v, bool reset) {
     cudaError_t e = cudaMemcpyFromSymbol(v, g_phase1_errors, sizeof(*v));
     if (e != cudaSuccess || !reset) return e;
