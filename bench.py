@@ -403,6 +403,10 @@ def run_ours(args):
     es, ml, tmp = pa.workspace(S, H, d, wl.max_seq_len, dev)
     # the fused entry point's arrival counters: zeroed once, left at zero by every call
     ctr = pa.decode_counters(S, H, wl.num_kv_heads, dev) if args.decode == "fused" else None
+    # scratch for the append entry's grid order (longest sequences first where CTAs stride);
+    # filled with -1, so that after the warm-up it shows whether the library launched the
+    # order kernel
+    order = torch.full((S,), -1, dtype=torch.int32, device=dev) if args.order else None
     stream = torch.cuda.current_stream()
 
     def step(i, inp=None):
@@ -411,7 +415,8 @@ def run_ours(args):
         if args.decode == "append":
             # the writer of the newest token fused into the decode
             pa.pa_v2_decode_append(out, es, ml, tmp, q_, nk_, nv_, kc, vc, wl.num_kv_heads, wl.scale, bt_, sl_,
-                                   wl.block_size, wl.max_seq_len, slopes, wl.kv_cache_dtype, wl.k_scale, wl.v_scale)
+                                   wl.block_size, wl.max_seq_len, slopes, wl.kv_cache_dtype, wl.k_scale, wl.v_scale,
+                                   order=order)
             return
         pa.pa_reshape_and_cache(nk_, nv_, kc, vc, slots_, wl.kv_cache_dtype, wl.k_scale, wl.v_scale)
         pa.pa_v2_decode(out, es, ml, tmp, q_, kc, vc, wl.num_kv_heads, wl.scale, bt_, sl_, wl.block_size,
@@ -427,6 +432,8 @@ def run_ours(args):
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
+    ordered = order is not None and args.decode == "append" and bool((order >= 0).all().item())
+    launches_per_step += 1 if ordered else 0
 
     def barrier():
         if ws > 1:
@@ -532,6 +539,7 @@ def run_ours(args):
         "config": workload_config(args.workload, wl, ws),
         "decode_entry": {"append": "pa_v2_decode_append", "fused": "pa_v2_decode_fused"}.get(args.decode,
                                                                                                "pa_v2_decode"),
+        "grid_order": "longest-first (pa_v2_decode_order inside the call)" if ordered else "index order",
         "fraction_of_peak": round(value / peak, 4),
         "l2": f"{decode_bytes / 2**20:.0f} MiB of K/V read per step from {nrot} rotating cache copies of "
               f"{kv_bytes / 2**20:.0f} MiB ({nrot * kv_bytes / L2_BYTES:.1f}x the L2 together)",
@@ -773,6 +781,8 @@ def main():
                          "1, the default), pa_v2_decode after pa_reshape_and_cache (two-kernel), or "
                          "pa_v2_decode_fused (the combine by the last CTA inside phase 1 on grids of at most "
                          "two waves; measured slower on every workload here)")
+    ap.add_argument("--no-order", dest="order", action="store_false",
+                    help="decode (append): no grid-order scratch, so the grid serves sequences in index order")
     ap.add_argument("--cache-copies", type=int, default=0,
                     help="decode: copies of the K/V caches the steps rotate through (0: at least 2 and enough "
                          "to span 2.5x the L2, so no step finds earlier steps' pages there; 1 for profiler runs)")

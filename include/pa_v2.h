@@ -186,10 +186,17 @@ PA_API pa_status pa_v2_decode_fused(void* output, float* exp_sums, float* max_lo
  *                       key_stride_s / value_stride_s ELEMENTS apart (>= num_kv_heads *
  *                       head_size, multiples of 8); 16-byte aligned.
  *   key_cache, value_cache  written (the new token's slot) as well as read.
+ *   order               device int32 [num_seqs] scratch (4-byte aligned), or NULL.  Where
+ *                       the step's CTAs stride over several partitions each (wide ragged
+ *                       batches), the call first writes the pa_v2_decode_order permutation
+ *                       into it and serves the sequences in that order, so the CTAs with the
+ *                       most partitions start first instead of forming the grid's tail.  The
+ *                       results do not depend on it.
  * Sequences with seq_lens[s] == 0 append nothing.  Every other sequence must have its newest
  * token at position seq_lens[s] - 1 of its table row; a page id outside the cache there
  * masks the token (and is flagged) as in pa_v2_decode.
- * Errors: as pa_v2_decode; PA_ERR_INVALID_ARG also for a null, misaligned or short row.
+ * Errors: as pa_v2_decode; PA_ERR_INVALID_ARG also for a null, misaligned or short row or a
+ * misaligned order buffer.
  */
 PA_API pa_status pa_v2_decode_append(void* output, float* exp_sums, float* max_logits, void* tmp_output,
                                      const void* query, const void* key, const void* value,
@@ -200,7 +207,22 @@ PA_API pa_status pa_v2_decode_append(void* output, float* exp_sums, float* max_l
                                      int block_size, int max_seq_len, int max_num_partitions,
                                      const float* alibi_slopes, pa_dtype q_dtype,
                                      pa_kv_cache_dtype kv_cache_dtype, pa_dtype tmp_dtype, float k_scale,
-                                     float v_scale, cudaStream_t stream);
+                                     float v_scale, int32_t* order, cudaStream_t stream);
+
+/*
+ * pa_v2_decode_order -- the order in which the decode grid serves the sequences: order[0 ..
+ * num_seqs) becomes a permutation of 0 .. num_seqs - 1 by decreasing partition count
+ * ceil(seq_lens[s] / 512) (counts above 1022 share one class; the order inside a class is
+ * unspecified).  A scheduling aid, not part of the pages' method (their grid is
+ * (sequences, heads, partitions) in index order): with partitions dealt to CTAs in strides,
+ * a CTA's work grows with its sequence's length, and starting the longest first shortens the
+ * grid's tail (longest-job-first).  pa_v2_decode_append calls it itself when given an order
+ * buffer.
+ * Arguments: seq_lens device int32 [num_seqs]; num_seqs 0 .. 65535; order device int32
+ * [num_seqs]; both 4-byte aligned.  Reads seq_lens after the previous kernel in the stream.
+ * Errors: PA_ERR_INVALID_ARG before anything is enqueued; PA_ERR_CUDA on a launch failure.
+ */
+PA_API pa_status pa_v2_decode_order(const int32_t* seq_lens, int num_seqs, int32_t* order, cudaStream_t stream);
 
 /*
  * pa_v2_decode_head_scales, pa_v2_decode_append_head_scales -- pa_v2_decode and
@@ -240,7 +262,7 @@ PA_API pa_status pa_v2_decode_append_head_scales(
     int num_seqs, int num_heads, int num_kv_heads, int head_size, float scale, const int32_t* block_tables,
     int max_blocks_per_seq, int num_blocks, const int32_t* seq_lens, int block_size, int max_seq_len,
     int max_num_partitions, const float* alibi_slopes, pa_dtype q_dtype, pa_kv_cache_dtype kv_cache_dtype,
-    pa_dtype tmp_dtype, const float* k_scales, const float* v_scales, cudaStream_t stream);
+    pa_dtype tmp_dtype, const float* k_scales, const float* v_scales, int32_t* order, cudaStream_t stream);
 
 /* Arrival counters pa_v2_decode_fused needs: num_seqs * num_kv_heads *
  * ceil((num_heads / num_kv_heads) / 8) (one per sequence and group of up to 8 query heads of a
@@ -416,7 +438,8 @@ PA_API const char* pa_status_string(pa_status status);
  * short; bit 1: a sequence longer than max_num_partitions * 512 or a negative length;
  * bit 2: a bounded wait for a shared-memory copy gave up; bit 3: a slot outside the
  * cache; bit 4: a pa_copy_blocks id outside the cache; bits 5-7: pa_prefix, see there;
- * bit 8: a per-kv-head k or v scale that is not finite and > 0).
+ * bit 8: a per-kv-head k or v scale that is not finite and > 0; bit 9: a grid-order entry
+ * outside [0, num_seqs), whose grid slice is then skipped).
  * Reads the flags of the current device (this synchronises the device) into
  * *flags, and clears them when reset != 0.  Not part of the pages' interface: it reports
  * what the kernels skipped instead of faulting. */

@@ -67,7 +67,9 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                        i32, P, i32, i32, i32, f32, f32, P, i64, P]
     lib.pa_v2_decode_append.restype = i32
     lib.pa_v2_decode_append.argtypes = [P, P, P, P, P, P, P, i64, i64, P, P, i32, i32, i32, i32, f32, P, i32, i32, P,
-                                        i32, i32, i32, P, i32, i32, i32, f32, f32, P]
+                                        i32, i32, i32, P, i32, i32, i32, f32, f32, P, P]
+    lib.pa_v2_decode_order.restype = i32
+    lib.pa_v2_decode_order.argtypes = [P, i32, P, P]
     lib.pa_v2_decode_num_counters.restype = i64
     lib.pa_v2_decode_num_counters.argtypes = [i32, i32, i32]
     lib.pa_reshape_and_cache.restype = i32
@@ -78,7 +80,7 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                                              i32, i32, P, i32, i32, i32, P, P, P]
     lib.pa_v2_decode_append_head_scales.restype = i32
     lib.pa_v2_decode_append_head_scales.argtypes = [P, P, P, P, P, P, P, i64, i64, P, P, i32, i32, i32, i32, f32, P,
-                                                    i32, i32, P, i32, i32, i32, P, i32, i32, i32, P, P, P]
+                                                    i32, i32, P, i32, i32, i32, P, i32, i32, i32, P, P, P, P]
     lib.pa_reshape_and_cache_head_scales.restype = i32
     lib.pa_reshape_and_cache_head_scales.argtypes = [P, P, i64, i64, P, P, P, i32, i32, i32, i32, i32, i32, i32,
                                                      P, P, P]
@@ -221,11 +223,13 @@ def pa_v2_decode_append(output: torch.Tensor, exp_sums: torch.Tensor, max_logits
                         block_tables: torch.Tensor, seq_lens: torch.Tensor, block_size: int, max_seq_len: int,
                         alibi_slopes: Optional[torch.Tensor] = None, kv_cache_dtype: str = "auto",
                         k_scale=1.0, v_scale=1.0, num_blocks: Optional[int] = None,
-                        stream=None) -> None:
+                        stream=None, order: Optional[torch.Tensor] = None) -> None:
     """One decode step that first appends every sequence's newest token (key/value [S, Hk, d]
     rows, position seq_lens[s] - 1, slot from the block table) to the caches: the cache
     writer and pa_v2_decode in one kernel.  Other arguments as pa_v2_decode (per-kv-head
-    scale tensors make the call ``pa_v2_decode_append_head_scales``)."""
+    scale tensors make the call ``pa_v2_decode_append_head_scales``).  ``order``: an int32
+    CUDA tensor of num_seqs entries the call may use as scratch for a longest-first grid
+    order (see :func:`pa_v2_decode_order`), or None."""
     lib = load()
     for name, t in (("output", output), ("exp_sums", exp_sums), ("max_logits", max_logits),
                     ("tmp_output", tmp_output), ("query", query), ("key_cache", key_cache),
@@ -257,12 +261,28 @@ def pa_v2_decode_append(output: torch.Tensor, exp_sums: torch.Tensor, max_logits
             float(scale), _ptr(block_tables), int(block_tables.shape[1]), int(num_blocks), _ptr(seq_lens),
             int(block_size), int(max_seq_len), int(tmp_output.shape[2]), _ptr(alibi_slopes), _dt(query.dtype),
             _kv(kv_cache_dtype), tmp_dtype)
+    if order is not None and (order.dtype != torch.int32 or not order.is_cuda or not order.is_contiguous()
+                              or order.numel() < S):
+        raise TypeError("order must be a contiguous int32 CUDA tensor of num_seqs entries")
     hs = _head_scales(k_scale, v_scale, int(num_kv_heads))
     if hs is not None:
         _check("pa_v2_decode_append_head_scales",
-               lib.pa_v2_decode_append_head_scales(*args, *hs, _stream(stream)))
+               lib.pa_v2_decode_append_head_scales(*args, *hs, _ptr(order), _stream(stream)))
         return
-    _check("pa_v2_decode_append", lib.pa_v2_decode_append(*args, float(k_scale), float(v_scale), _stream(stream)))
+    _check("pa_v2_decode_append", lib.pa_v2_decode_append(*args, float(k_scale), float(v_scale), _ptr(order),
+                                                          _stream(stream)))
+
+
+def pa_v2_decode_order(seq_lens: torch.Tensor, order: torch.Tensor, stream=None) -> None:
+    """Write into ``order`` (int32 CUDA [num_seqs]) the sequences by decreasing partition count."""
+    lib = load()
+    for name, t in (("seq_lens", seq_lens), ("order", order)):
+        if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{name} must be a contiguous int32 CUDA tensor")
+    if order.numel() < seq_lens.numel():
+        raise ValueError("order needs one entry per sequence")
+    _check("pa_v2_decode_order", lib.pa_v2_decode_order(_ptr(seq_lens), seq_lens.numel(), _ptr(order),
+                                                        _stream(stream)))
 
 
 def pa_reshape_and_cache(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor,
@@ -304,11 +324,12 @@ def pa_v2_decode_append_head_scales(output, exp_sums, max_logits, tmp_output, qu
                                     value_cache, num_kv_heads: int, scale: float, block_tables, seq_lens,
                                     block_size: int, max_seq_len: int, alibi_slopes=None,
                                     kv_cache_dtype: str = "auto", *, k_scales: torch.Tensor,
-                                    v_scales: torch.Tensor, num_blocks: Optional[int] = None, stream=None) -> None:
+                                    v_scales: torch.Tensor, num_blocks: Optional[int] = None, stream=None,
+                                    order: Optional[torch.Tensor] = None) -> None:
     """pa_v2_decode_append with one k_scale / v_scale per kv head (float32 CUDA tensors [Hk])."""
     pa_v2_decode_append(output, exp_sums, max_logits, tmp_output, query, key, value, key_cache, value_cache,
                         num_kv_heads, scale, block_tables, seq_lens, block_size, max_seq_len, alibi_slopes,
-                        kv_cache_dtype, k_scales, v_scales, num_blocks=num_blocks, stream=stream)
+                        kv_cache_dtype, k_scales, v_scales, num_blocks=num_blocks, stream=stream, order=order)
 
 
 def pa_reshape_and_cache_head_scales(key, value, key_cache, value_cache, slot_mapping,

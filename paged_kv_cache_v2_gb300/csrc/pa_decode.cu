@@ -222,6 +222,75 @@ pa_v2_phase2_kernel(const Phase2Params p) {
 // A batch of many rows then needs few CTAs, and each row costs about one memory round trip:
 // the statistics (two per lane) and the tmp rows of its first kP2RowChunk partitions load
 // together, before any of them is used.
+// ---------------------------------------------------------------------------------------
+// Grid order: the sequences by decreasing partition count (most work first)
+// ---------------------------------------------------------------------------------------
+// One CTA: a counting sort on min(ceil(L / 512), kOrderBuckets - 1), largest first.  Within a
+// bucket the order is whatever the shared-memory atomics give: it only schedules, and every
+// sequence's results are the same in any order.
+constexpr int kOrderThreads = 1024;
+constexpr int kOrderMinSeqs = 16;  // below this the grid has few sequences to reorder
+constexpr int kOrderBuckets = 1024;
+
+__global__ void __launch_bounds__(kOrderThreads) pa_v2_order_kernel(const int32_t* seq_lens, int S, int32_t* order) {
+    __shared__ int cnt[kOrderBuckets];
+    __shared__ int wsum[kOrderThreads / 32];
+    // the lengths may come from the previous kernel in the stream
+    griddep_wait();
+    for (int b = threadIdx.x; b < kOrderBuckets; b += blockDim.x) cnt[b] = 0;
+    __syncthreads();
+    // bucket 0 holds the most partitions
+    auto bucket = [&](int L) {
+        const int P = L > 0 ? (int)(((int64_t)L + kPartition - 1) / kPartition) : 0;
+        return kOrderBuckets - 1 - min(P, kOrderBuckets - 1);
+    };
+    for (int i = threadIdx.x; i < S; i += blockDim.x) atomicAdd(&cnt[bucket(seq_lens[i])], 1);
+    __syncthreads();
+    // exclusive scan of the bucket counts (one bucket per thread: kOrderBuckets == blockDim.x)
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int v = cnt[threadIdx.x];
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int w = wsum[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += y;
+        }
+        wsum[lane] = w;  // inclusive sums of the warps
+    }
+    __syncthreads();
+    cnt[threadIdx.x] = x - v + (warp > 0 ? wsum[warp - 1] : 0);
+    __syncthreads();
+    for (int i = threadIdx.x; i < S; i += blockDim.x) order[atomicAdd(&cnt[bucket(seq_lens[i])], 1)] = i;
+    griddep_launch_dependents();
+}
+
+pa_status launch_order(const int32_t* seq_lens, int S, int32_t* order, cudaStream_t stream) {
+    static_assert(kOrderBuckets == kOrderThreads, "one bucket per thread in the scan");
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, 1, 1);
+    cfg.blockDim = dim3(kOrderThreads, 1, 1);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, pa_v2_order_kernel, seq_lens, S, order) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return PA_ERR_CUDA;
+    }
+    return PA_OK;
+}
+
 constexpr int kP2RowsPerCta = 8;
 constexpr int kP2RowChunk = 16;
 
@@ -684,6 +753,7 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
     p1.nv_stride = a.new_value_stride;
     p1.k_enc = a.k_scale;
     p1.v_enc = a.v_scale;
+    p1.order = nullptr;
     p1.nrow_off = (uint32_t)nrow_off;
 
     cudaLaunchAttribute attr[1];
@@ -774,6 +844,15 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
             K /= 2;
     }
     p1.csplit = K;
+    // Grid order: where CTAs stride over several partitions (PX < Pmax) their work differs by
+    // up to 8x, and a long sequence scheduled last leaves a tail; serving the sequences with
+    // the most partitions first removes it (ragged MHA batch, inputs permuted longest-first:
+    // 432 us against 450 us; one partition per CTA, as on the Llama batch, gains nothing).
+    if (a.order != nullptr && K == 1 && !few_rows && PX < Pmax && a.num_seqs >= kOrderMinSeqs) {
+        const pa_status so = launch_order(a.seq_lens, a.num_seqs, a.order, a.stream);
+        if (so != PA_OK) return so;
+        p1.order = a.order;
+    }
     cudaLaunchAttribute attrs1[2];
     attrs1[0] = attr[0];
     attrs1[1].id = cudaLaunchAttributeClusterDimension;
@@ -1007,7 +1086,7 @@ static pa_status append_impl(void* output, float* exp_sums, float* max_logits, v
                              const int32_t* seq_lens, int block_size, int max_seq_len, int max_num_partitions,
                              const float* alibi_slopes, pa_dtype q_dtype, pa_kv_cache_dtype kv_cache_dtype,
                              pa_dtype tmp_dtype, float k_scale, float v_scale, const float* k_scales,
-                             const float* v_scales, cudaStream_t stream) {
+                             const float* v_scales, int32_t* order, cudaStream_t stream) {
     DecodeArgs a;
     a.output = output;
     a.exp_sums = exp_sums;
@@ -1037,6 +1116,7 @@ static pa_status append_impl(void* output, float* exp_sums, float* max_logits, v
     a.stream = stream;
     a.k_scales = k_scales;
     a.v_scales = v_scales;
+    a.order = order;
     a.new_key = key;
     a.new_value = value;
     a.new_key_stride = key_stride_s;
@@ -1046,7 +1126,7 @@ static pa_status append_impl(void* output, float* exp_sums, float* max_logits, v
     if (st != PA_OK || num_seqs == 0) return st;
     const int64_t row = (int64_t)num_kv_heads * head_size;
     if (key == nullptr || value == nullptr || key_stride_s < row || value_stride_s < row || key_stride_s % 8 != 0 ||
-        value_stride_s % 8 != 0 || !aligned(key, 16) || !aligned(value, 16))
+        value_stride_s % 8 != 0 || !aligned(key, 16) || !aligned(value, 16) || !aligned(order, 4))
         return PA_ERR_INVALID_ARG;
     st = host_check_tables(block_tables, max_blocks_per_seq, num_blocks, seq_lens, num_seqs, block_size,
                            max_seq_len, stream);
@@ -1063,11 +1143,12 @@ extern "C" pa_status pa_v2_decode_append(void* output, float* exp_sums, float* m
                                          int block_size, int max_seq_len, int max_num_partitions,
                                          const float* alibi_slopes, pa_dtype q_dtype,
                                          pa_kv_cache_dtype kv_cache_dtype, pa_dtype tmp_dtype, float k_scale,
-                                         float v_scale, cudaStream_t stream) {
+                                         float v_scale, int32_t* order, cudaStream_t stream) {
     return append_impl(output, exp_sums, max_logits, tmp_output, query, key, value, key_stride_s, value_stride_s,
                        key_cache, value_cache, num_seqs, num_heads, num_kv_heads, head_size, scale, block_tables,
                        max_blocks_per_seq, num_blocks, seq_lens, block_size, max_seq_len, max_num_partitions,
-                       alibi_slopes, q_dtype, kv_cache_dtype, tmp_dtype, k_scale, v_scale, nullptr, nullptr, stream);
+                       alibi_slopes, q_dtype, kv_cache_dtype, tmp_dtype, k_scale, v_scale, nullptr, nullptr, order,
+                       stream);
 }
 
 extern "C" pa_status pa_v2_decode_append_head_scales(
@@ -1076,12 +1157,20 @@ extern "C" pa_status pa_v2_decode_append_head_scales(
     int num_seqs, int num_heads, int num_kv_heads, int head_size, float scale, const int32_t* block_tables,
     int max_blocks_per_seq, int num_blocks, const int32_t* seq_lens, int block_size, int max_seq_len,
     int max_num_partitions, const float* alibi_slopes, pa_dtype q_dtype, pa_kv_cache_dtype kv_cache_dtype,
-    pa_dtype tmp_dtype, const float* k_scales, const float* v_scales, cudaStream_t stream) {
+    pa_dtype tmp_dtype, const float* k_scales, const float* v_scales, int32_t* order, cudaStream_t stream) {
     if (k_scales == nullptr || v_scales == nullptr) return PA_ERR_INVALID_ARG;
     return append_impl(output, exp_sums, max_logits, tmp_output, query, key, value, key_stride_s, value_stride_s,
                        key_cache, value_cache, num_seqs, num_heads, num_kv_heads, head_size, scale, block_tables,
                        max_blocks_per_seq, num_blocks, seq_lens, block_size, max_seq_len, max_num_partitions,
-                       alibi_slopes, q_dtype, kv_cache_dtype, tmp_dtype, 1.f, 1.f, k_scales, v_scales, stream);
+                       alibi_slopes, q_dtype, kv_cache_dtype, tmp_dtype, 1.f, 1.f, k_scales, v_scales, order, stream);
+}
+
+extern "C" pa_status pa_v2_decode_order(const int32_t* seq_lens, int num_seqs, int32_t* order, cudaStream_t stream) {
+    if (num_seqs < 0 || num_seqs > 65535) return PA_ERR_INVALID_ARG;
+    if (num_seqs == 0) return PA_OK;
+    if (seq_lens == nullptr || order == nullptr || !aligned(seq_lens, 4) || !aligned(order, 4))
+        return PA_ERR_INVALID_ARG;
+    return launch_order(seq_lens, num_seqs, order, stream);
 }
 
 // ---------------------------------------------------------------------------------------

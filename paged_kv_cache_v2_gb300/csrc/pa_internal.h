@@ -37,6 +37,9 @@ struct DecodeArgs {
     // tmp_output is the caller's scratch (its contents after the call are unspecified), so
     // CTAs that stream several partitions may fold them into one row
     bool tmp_scratch = false;
+    // caller scratch of num_seqs ints for a grid order (most partitions first), or null; used
+    // where CTAs stride over several partitions each
+    int32_t* order = nullptr;
 };
 
 // Argument checks shared by the decode entry points (no device access).
@@ -46,6 +49,8 @@ pa_status validate_decode(const DecodeArgs& a);
 // the step's shape allows it, and phase 2 is not launched.
 pa_status launch_decode(const DecodeArgs& a, float* exp_sums, float* max_logits, void* tmp_out,
                         uint32_t* counters = nullptr);
+// Enqueue the grid-order kernel: order[0..S) = the sequences by decreasing partition count.
+pa_status launch_order(const int32_t* seq_lens, int S, int32_t* order, cudaStream_t stream);
 // Arrival counters the fused combine needs for a step of this shape.
 int64_t decode_num_counters(int num_seqs, int num_heads, int num_kv_heads);
 // Read (and optionally clear) each translation unit's device error word on the current device.

@@ -81,6 +81,10 @@ struct Phase1Params {
     const uint16_t* new_v;
     int64_t nk_stride, nv_stride;
     float k_enc, v_enc;   // k_scale, v_scale (the fp8 encode divides by them)
+    // Grid order (or nullptr): blockIdx.z = z serves sequence order[z], a permutation of the
+    // sequences that puts those with the most partitions first, so the CTAs that stream
+    // many partitions start early instead of forming the grid's tail.
+    const int32_t* order;
     uint32_t nrow_off;    // shared-memory byte offset of the staged new rows (2 x D x 2 bytes)
 };
 

@@ -217,7 +217,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     const int PX = ng == 1 ? gx : gx / ng;
     const int grp = bx - px * ng;
     const int kvh = blockIdx.y;
-    const int s = blockIdx.z;
+    int s = blockIdx.z;  // the sequence: blockIdx.z, or order[blockIdx.z] (read after the wait)
     const int h0 = kvh * p.G + grp * kMaxHeadsPerCta;
     const int nh = min(kMaxHeadsPerCta, p.G - grp * kMaxHeadsPerCta);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -237,7 +237,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     constexpr uint32_t page_bytes = (uint32_t)D * bs * KVB;
     constexpr uint32_t slot_bytes = 2u * pps * page_bytes;
     const int nstage = p.nstage;
-    const int32_t* trow = p.block_tables + (int64_t)s * p.mbps;
+    const int32_t* trow = p.block_tables;  // this sequence's table row (set after the wait)
 
     // Raw table entries of partition q: lane i holds pages i and 32 + i.
     auto load_ids = [&](int q, int& r0, int& r1) {
@@ -253,6 +253,16 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     // them on the device each step), and only the wait makes its writes visible.  The ids of
     // the first two partitions and the length then load in parallel.
     griddep_wait();
+    if (p.order != nullptr) {
+        s = p.order[blockIdx.z];
+        if (s < 0 || s >= (int)gridDim.z) {
+            // not a permutation of the sequences: nothing to serve (flagged)
+            if (threadIdx.x == 0) flag_error(512u);
+            griddep_launch_dependents();
+            return;
+        }
+    }
+    trow += (int64_t)s * p.mbps;
     int c0, c1, n0, n1;
     load_ids(px, c0, c1);
     load_ids(px + PX, n0, n1);
@@ -379,9 +389,8 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     // ---- query fragments (MMA B operand: k = head dim, n = query head g) -------------------
     // 16-bit caches: the query row as f16/bf16 pairs.  fp8 cache with an f16 query: f16 pairs
     // in the order the widened fp8 K rows deliver the head dimension (4t..4t+3 of each 16).
-    // fp8 cache with a bf16 query: the row scaled by a power of two (per head, so the largest
-    // element lands near 224) and split into three e4m3 terms hi + mid + lo (at least 12
-    // significant bits, so every bf16 value is exact); the scale is undone on the scores.
+    // fp8 cache with a bf16 query: the row scaled by a power of two per head, so that it is
+    // exact in f16 (below); the scale is undone on the scores.
     constexpr int NS = (D + 31) / 32;  // k32 steps over the head dimension (fp8)
     uint32_t qf[NK][2];
     float qs0 = 1.f, qs1 = 1.f;  // per-column score factor undoing the query's scale (fp8, bf16 query)

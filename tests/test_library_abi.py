@@ -130,17 +130,29 @@ def test_head_scale_entry_points_host_checks():
     zero[7] = 0
     assert lib.pa_v2_decode_head_scales(*zero, P, P, None) == 0            # no sequences
     app = [P, P, P, P, P, P, P, 256, 256, P, P, 2, 8, 2, 128, 0.088, P, 64, 100, P, 16, 1024, 2, None, 0, 0, 2]
-    assert lib.pa_v2_decode_append_head_scales(*app, None, P, None) == 1
-    assert lib.pa_v2_decode_append_head_scales(*app, P, P + 1, None) == 1
+    assert lib.pa_v2_decode_append_head_scales(*app, None, P, None, None) == 1
+    assert lib.pa_v2_decode_append_head_scales(*app, P, P + 1, None, None) == 1
+    assert lib.pa_v2_decode_append_head_scales(*app, P, P, P + 2, None) == 1   # misaligned order buffer
     short = list(app)
     short[7] = 100                                                         # key rows shorter than Hk * d
-    assert lib.pa_v2_decode_append_head_scales(*short, P, P, None) == 1
+    assert lib.pa_v2_decode_append_head_scales(*short, P, P, None, None) == 1
     wr = [P, P, 256, 256, P, P, P, 4, 2, 128, 16, 10, 0, 1]
     assert lib.pa_reshape_and_cache_head_scales(*wr, None, P, None) == 1
     assert lib.pa_reshape_and_cache_head_scales(*wr, P, P + 2, None) == 1
     wr0 = list(wr)
     wr0[7] = 0
     assert lib.pa_reshape_and_cache_head_scales(*wr0, P, P, None) == 0     # no tokens
+
+
+def test_order_entry_point_host_checks():
+    lib = pa.load()
+    P = 0x10000
+    assert "pa_v2_decode_order" in _declared()
+    assert lib.pa_v2_decode_order(P, -1, P, None) == 1          # negative count
+    assert lib.pa_v2_decode_order(P, 65536, P, None) == 1       # beyond the grid's z extent
+    assert lib.pa_v2_decode_order(None, 4, P, None) == 1
+    assert lib.pa_v2_decode_order(P, 4, P + 2, None) == 1       # misaligned
+    assert lib.pa_v2_decode_order(None, 0, None, None) == 0     # nothing to order
 
 
 def _cache_raw(**over):

@@ -50,8 +50,9 @@ def oracle_append(wl, slots=None):
     return kr, vr, oracle.decode_workload(wl, key_cache=kr, value_cache=vr)
 
 
-def run_append(wl, key=None, value=None):
-    """pa_v2_decode_append on device copies of the workload; returns (out, es, ml, tmp), caches."""
+def run_append(wl, key=None, value=None, order=None):
+    """pa_v2_decode_append on device copies of the workload; returns (out, es, ml, tmp), caches.
+    ``order``: an int32 CUDA scratch for the grid order, or None."""
     dev = "cuda"
     S, H, d = wl.query.shape
     P = wl.max_num_partitions
@@ -67,14 +68,14 @@ def run_append(wl, key=None, value=None):
     nv = wl.new_value.to(dev) if value is None else value
     ks, vs = device_scales(wl)
     pa.pa_v2_decode_append(out, es, ml, tmp, q, nk, nv, kc, vc, wl.num_kv_heads, wl.scale, bt, sl, wl.block_size,
-                           wl.max_seq_len, slopes, wl.kv_cache_dtype, ks, vs)
+                           wl.max_seq_len, slopes, wl.kv_cache_dtype, ks, vs, order=order)
     torch.cuda.synchronize()
     return (out.cpu(), es.cpu(), ml.cpu(), tmp.cpu()), kc.cpu(), vc.cpu()
 
 
-def _check_all(wl, label):
+def _check_all(wl, label, order=None):
     kr, vr, ref = oracle_append(wl)
-    gpu, kc, vc = run_append(wl)
+    gpu, kc, vc = run_append(wl, order=order)
     # tmp_output is scratch here (CTAs streaming several partitions fold them into one row)
     check_decode(wl, gpu, ref, label=label, check_tmp=False)
     assert np.array_equal(_as_int(kc), kr.view(np.uint8 if kr.dtype == np.uint8 else np.int16)), f"{label}: key cache"
@@ -148,17 +149,21 @@ def test_new_token_on_a_page_outside_the_cache_is_masked_and_flagged():
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["llama_gqa_decode", "long_context_gqa"])
+@pytest.mark.parametrize("name", ["llama_gqa_decode", "long_context_gqa", "mha_alibi_ragged"])
 def test_full_size_sampled(name):
     # the benchmark's launch configuration (for the long context: one wave of CTAs, each
-    # folding about ten partitions into one row, and phase 2 over those rows)
+    # folding about ten partitions into one row, and phase 2 over those rows; for the ragged
+    # MHA batch: CTAs striding over partitions, sequences served longest first)
     wl = workloads.make(name)
     pairs = sample_pairs(wl, n=16)
     kr, vr = oracle._np(wl.key_cache).copy(), oracle._np(wl.value_cache).copy()
     oracle.reshape_and_cache(wl.new_key, wl.new_value, wl.q_dtype, kr, vr, wl.kv_storage, wl.slot_mapping,
                              block_size=wl.block_size, k_scale=wl.k_scale, v_scale=wl.v_scale)
     ref = oracle.decode_workload(wl, pairs=pairs, key_cache=kr, value_cache=vr)
-    gpu, kc, vc = run_append(wl)
+    order = torch.full((wl.num_seqs,), -1, dtype=torch.int32, device="cuda")
+    gpu, kc, vc = run_append(wl, order=order)
+    if name == "mha_alibi_ragged":  # the grid was ordered: the scratch holds a permutation
+        assert sorted(order.cpu().tolist()) == list(range(wl.num_seqs))
     check_decode(wl, gpu, ref, pairs=pairs, label=f"append {name}", check_tmp=False)
     assert np.array_equal(_as_int(kc), kr) and np.array_equal(_as_int(vc), vr)
     assert pa.pa_get_device_errors() == 0
@@ -167,10 +172,15 @@ def test_full_size_sampled(name):
 _CHILD = r"""
 import sys
 sys.path.insert(0, {here!r}); sys.path.insert(0, {root!r})
+import torch
 import workloads
 from test_parity_append import _check_all
 for spec in {specs!r}:
-    _check_all(workloads.build(**spec), f"child {{spec}}")
+    wl = workloads.build(**spec)
+    order = torch.full((wl.num_seqs,), -1, dtype=torch.int32, device="cuda") if {order!r} else None
+    _check_all(wl, f"child {{spec}}", order=order)
+    if order is not None and wl.num_seqs >= 16:
+        assert sorted(order.cpu().tolist()) == list(range(wl.num_seqs)), "grid order not written"
 print("child ok")
 """
 
@@ -183,7 +193,33 @@ def test_strides_and_cluster_split(env):
                   seq_lens=[3000, 1, 700, 2600], alibi=True, seed=540),
              dict(num_seqs=3, num_heads=12, num_kv_heads=3, head_size=128, block_size=8, seq_lens=[1030, 64, 2500],
                   kv_cache_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.07, seed=541)]
-    code = _CHILD.format(here=HERE, root=os.path.dirname(HERE), specs=specs)
+    code = _CHILD.format(here=HERE, root=os.path.dirname(HERE), specs=specs, order=False)
     r = subprocess.run([sys.executable, "-c", code], env=dict(os.environ, **env), capture_output=True, text=True,
                        timeout=900)
+    assert r.returncode == 0 and "child ok" in r.stdout, r.stdout[-2000:] + r.stderr[-4000:]
+
+
+def test_grid_order_is_a_longest_first_permutation():
+    rng = np.random.default_rng(560)
+    lens = np.concatenate([rng.integers(0, 60000, size=997), [0, 1, 600000]]).astype(np.int32)
+    sl = torch.from_numpy(lens).cuda()
+    order = torch.full((lens.size,), -1, dtype=torch.int32, device="cuda")
+    pa.pa_v2_decode_order(sl, order)
+    torch.cuda.synchronize()
+    o = order.cpu().numpy()
+    assert sorted(o.tolist()) == list(range(lens.size))
+    parts = np.minimum(-(-lens.astype(np.int64) // 512), 1023)[o]
+    assert np.all(np.diff(parts) <= 0)
+
+
+def test_strided_grid_in_longest_first_order():
+    # CTAs striding over two partitions each, sequences served longest first: same results
+    specs = [dict(num_seqs=20, num_heads=8, num_kv_heads=2, head_size=128, block_size=16,
+                  seq_lens=[3000, 1, 700, 2600, 0, 512, 513, 1500, 2999, 17] * 2, alibi=True, seed=570),
+             dict(num_seqs=24, num_heads=12, num_kv_heads=3, head_size=128, block_size=8,
+                  seq_lens=[1030, 64, 2500, 3072, 1, 777] * 4, kv_cache_dtype="fp8_e4m3", k_scale=0.05,
+                  v_scale=0.07, seed=571)]
+    code = _CHILD.format(here=HERE, root=os.path.dirname(HERE), specs=specs, order=True)
+    r = subprocess.run([sys.executable, "-c", code], env=dict(os.environ, PA_DECODE_PX="2"), capture_output=True,
+                       text=True, timeout=900)
     assert r.returncode == 0 and "child ok" in r.stdout, r.stdout[-2000:] + r.stderr[-4000:]
