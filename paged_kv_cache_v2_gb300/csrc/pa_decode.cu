@@ -444,11 +444,17 @@ static bool supported_head_size(int d) {
     }
 }
 
+template <int BS>
+static Phase1Fn phase1_pick(bool bf16, bool fp8, int d, bool head_scales) {
+    if (fp8) return head_scales ? phase1_select<BS, 1, true>(bf16, d) : phase1_select<BS, 1, false>(bf16, d);
+    return head_scales ? phase1_select<BS, 2, true>(bf16, d) : phase1_select<BS, 2, false>(bf16, d);
+}
+
 static Phase1Fn phase1_for(bool bf16, bool fp8, int d, int bs, bool head_scales) {
     switch (bs) {
-        case 8: return fp8 ? phase1_select<8, 1>(bf16, d, head_scales) : phase1_select<8, 2>(bf16, d, head_scales);
-        case 16: return fp8 ? phase1_select<16, 1>(bf16, d, head_scales) : phase1_select<16, 2>(bf16, d, head_scales);
-        case 32: return fp8 ? phase1_select<32, 1>(bf16, d, head_scales) : phase1_select<32, 2>(bf16, d, head_scales);
+        case 8: return phase1_pick<8>(bf16, fp8, d, head_scales);
+        case 16: return phase1_pick<16>(bf16, fp8, d, head_scales);
+        case 32: return phase1_pick<32>(bf16, fp8, d, head_scales);
         default: return nullptr;
     }
 }
@@ -547,15 +553,20 @@ extern "C" const char* pa_status_string(pa_status status) {
 }
 
 cudaError_t pa::read_decode_errors(unsigned int* v, bool reset) {
-    unsigned int w[6] = {};
-    cudaError_t e = phase1_read_errors<8, 2>(&w[0], reset);
-    if (e == cudaSuccess) e = phase1_read_errors<16, 2>(&w[1], reset);
-    if (e == cudaSuccess) e = phase1_read_errors<32, 2>(&w[2], reset);
-    if (e == cudaSuccess) e = phase1_read_errors<8, 1>(&w[3], reset);
-    if (e == cudaSuccess) e = phase1_read_errors<16, 1>(&w[4], reset);
-    if (e == cudaSuccess) e = phase1_read_errors<32, 1>(&w[5], reset);
-    *v = w[0] | w[1] | w[2] | w[3] | w[4] | w[5];
-    return e;
+    cudaError_t (*readers[])(unsigned int*, bool) = {
+        phase1_read_errors<8, 2, false>,  phase1_read_errors<16, 2, false>, phase1_read_errors<32, 2, false>,
+        phase1_read_errors<8, 1, false>,  phase1_read_errors<16, 1, false>, phase1_read_errors<32, 1, false>,
+        phase1_read_errors<8, 2, true>,   phase1_read_errors<16, 2, true>,  phase1_read_errors<32, 2, true>,
+        phase1_read_errors<8, 1, true>,   phase1_read_errors<16, 1, true>,  phase1_read_errors<32, 1, true>};
+    unsigned int all = 0;
+    for (auto rd : readers) {
+        unsigned int w = 0;
+        const cudaError_t e = rd(&w, reset);
+        if (e != cudaSuccess) return e;
+        all |= w;
+    }
+    *v = all;
+    return cudaSuccess;
 }
 
 extern "C" pa_status pa_get_device_errors(uint32_t* flags, int reset) {
@@ -844,11 +855,14 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
             K /= 2;
     }
     p1.csplit = K;
-    // Grid order: where CTAs stride over several partitions (PX < Pmax) their work differs by
-    // up to 8x, and a long sequence scheduled last leaves a tail; serving the sequences with
-    // the most partitions first removes it (ragged MHA batch, inputs permuted longest-first:
-    // 432 us against 450 us; one partition per CTA, as on the Llama batch, gains nothing).
-    if (a.order != nullptr && K == 1 && !few_rows && PX < Pmax && a.num_seqs >= kOrderMinSeqs) {
+    // Grid order: where CTAs stride over several partitions their work differs by up to 8x,
+    // and a long sequence scheduled last leaves a tail; serving the sequences with the most
+    // partitions first removes it.  Measured (step, with the order kernel and the extra
+    // dependent load at every CTA's start): ragged MHA batch, CTAs of up to 8 partitions,
+    // 448.8 against 458.3 us; fp8 batch, up to 3 partitions, 198.8 against 197.9 us; one
+    // partition per CTA (Llama batch, inputs permuted) no gain.  So only grids whose CTAs
+    // take 4 or more partitions are ordered.
+    if (a.order != nullptr && K == 1 && !few_rows && (Pmax + PX - 1) / PX >= 4 && a.num_seqs >= kOrderMinSeqs) {
         const pa_status so = launch_order(a.seq_lens, a.num_seqs, a.order, a.stream);
         if (so != PA_OK) return so;
         p1.order = a.order;

@@ -188,10 +188,10 @@ __device__ __forceinline__ void append_token(const Phase1Params& p, const uint16
 #ifndef PA_FP8_MIN_CTAS
 #define PA_FP8_MIN_CTAS 3
 #endif
-// HS: the kernel reads per-kv-head scales when p.k_scales is set.  16-bit caches always take
-// that form; fp8 caches also have an HS = false form for per-tensor scales, whose page loop
-// keeps the score multiplier in the constant bank (one register fewer: measured 1.3% on the
-// fp8 batch, where the kernel is at its register cap).
+// HS: the kernel reads per-kv-head scales (p.k_scales set).  The HS = false form takes the
+// per-tensor scales from the constant bank, so its page loop holds one register fewer and
+// its epilogue no shared-memory read (measured 1.3% on the fp8 batch and 2.8% on the long
+// context, kernels at their register caps).
 template <bool BF16, int KVB, int D, int BS, bool HS>
 __global__ void __launch_bounds__(kWarps * 32, KVB == 2 ? (D <= 96 ? 16 : 12) / kWarps
                                                         : ((BF16 && D >= 192) ? 8 : 4 * PA_FP8_MIN_CTAS) / kWarps)
@@ -218,6 +218,12 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     const int grp = bx - px * ng;
     const int kvh = blockIdx.y;
     int s = blockIdx.z;  // the sequence: blockIdx.z, or order[blockIdx.z] (read after the wait)
+    // Per warp: the value scale and the two encode divisors (per-kv-head scales), and the
+    // sequence when the grid is ordered.  Shared memory, so that the page loop holds neither:
+    // the loop and the epilogue read them back (blockIdx.z itself costs no register).
+    __shared__ float wscale[kWarps][3];
+    __shared__ int wseq[kWarps];
+    static_assert(sizeof(wscale) + sizeof(wseq) == kPhase1StaticSmem, "the host sizes shared memory with this");
     const int h0 = kvh * p.G + grp * kMaxHeadsPerCta;
     const int nh = min(kMaxHeadsPerCta, p.G - grp * kMaxHeadsPerCta);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -237,10 +243,14 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     constexpr uint32_t page_bytes = (uint32_t)D * bs * KVB;
     constexpr uint32_t slot_bytes = 2u * pps * page_bytes;
     const int nstage = p.nstage;
-    const int32_t* trow = p.block_tables;  // this sequence's table row (set after the wait)
 
+    // The sequence, after the prologue (the ordered grid's from shared memory).
+    auto seq = [&]() -> int {
+        return p.order != nullptr ? *reinterpret_cast<volatile int*>(&wseq[warp]) : (int)blockIdx.z;
+    };
     // Raw table entries of partition q: lane i holds pages i and 32 + i.
     auto load_ids = [&](int q, int& r0, int& r1) {
+        const int32_t* trow = p.block_tables + (int64_t)seq() * p.mbps;
         r0 = r1 = -1;
         if (q < p.Pmax) {
             const int lb = q * ppart;
@@ -261,8 +271,9 @@ pa_v2_phase1_kernel(const Phase1Params p) {
             griddep_launch_dependents();
             return;
         }
+        if (lane == 0) wseq[warp] = s;
+        __syncwarp();
     }
-    trow += (int64_t)s * p.mbps;
     int c0, c1, n0, n1;
     load_ids(px, c0, c1);
     load_ids(px + PX, n0, n1);
@@ -477,8 +488,6 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     // used as given.  The value-side factor and the encode divisors wait in shared memory
     // (one copy per warp) for the epilogue and the append, so the page loop holds only the
     // score multiplier in a register.
-    __shared__ float wscale[kWarps][3];  // v_scale, k_scale and v_scale of the fp8 encode
-    static_assert(sizeof(wscale) == kPhase1StaticSmem, "the host sizes shared memory with this");
     float qk_mul = p.qk_scale_log2;
     if constexpr (HS) {
         if (p.k_scales != nullptr) {
@@ -939,6 +948,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
         // rows) to the first one, whose page ring is idle now (one partition per CTA); the
         // first CTA merges them into the partition's result and alone writes it.
         bool skip_out = false;
+        const float vmul = v_mul();  // read once: the loops below also write shared memory
         float* pbuf = reinterpret_cast<float*>(smem);
         const int pstride = 2 * kMaxHeadsPerCta + nh * D;
         if (K > 1) {
@@ -957,7 +967,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
 #pragma unroll
                     for (int w = 0; w < kWarps; ++w) v += red_o[(w * nh + hh) * RS + i];
                     const float lt = fin_l[hh];
-                    st_cluster_f32(dst + 4u * (2 * kMaxHeadsPerCta + e), lt > 0.f ? v * (v_mul() / lt) : 0.f);
+                    st_cluster_f32(dst + 4u * (2 * kMaxHeadsPerCta + e), lt > 0.f ? v * (vmul / lt) : 0.f);
                 }
             }
             cluster_sync_all();
@@ -998,11 +1008,11 @@ pa_v2_phase1_kernel(const Phase1Params p) {
 #pragma unroll
                 for (int w = 0; w < kWarps; ++w) v += red_o[(w * nh + hh) * RS + i];
                 const float lt = fin_l[hh];
-                v = lt > 0.f ? v * (v_mul() / lt) : 0.f;
+                v = lt > 0.f ? v * (vmul / lt) : 0.f;
                 const float fo = fac_o[hh];
                 float r = v * fac_n[hh];
                 if (fo != 0.f && !first) r = fmaf(mrg[e], fo, r);
-                const int64_t row = (int64_t)s * H + h0 + hh;
+                const int64_t row = (int64_t)seq() * H + h0 + hh;
                 if (!last_part)
                     mrg[e] = r;
                 else if (direct)
@@ -1017,13 +1027,13 @@ pa_v2_phase1_kernel(const Phase1Params p) {
 #pragma unroll
             for (int w = 0; w < kWarps; ++w) v += red_o[(w * nh + hh) * RS + i];
             if (K > 1) {
-                v *= v_mul() * fac_o[hh];
+                v *= vmul * fac_o[hh];
                 for (int k = 0; k < K - 1; ++k) v = fmaf(pbuf[k * pstride + 2 * kMaxHeadsPerCta + e], pbuf[k * pstride + hh], v);
             } else {
                 const float lt = fin_l[hh];
-                v = lt > 0.f ? v * (v_mul() / lt) : 0.f;
+                v = lt > 0.f ? v * (vmul / lt) : 0.f;
             }
-            const int64_t row = (int64_t)s * H + h0 + hh;
+            const int64_t row = (int64_t)seq() * H + h0 + hh;
             if (direct)
                 store_out<BF16>(p.out, row * D + i, v);
             else if (p.tmp16)
@@ -1033,7 +1043,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
         }
         if (threadIdx.x < nh && !skip_out) {
             const int hh = threadIdx.x;
-            const int64_t sidx = ((int64_t)s * H + h0 + hh) * p.Pmax + cq;
+            const int64_t sidx = ((int64_t)seq() * H + h0 + hh) * p.Pmax + cq;
             const float lt = fin_l[hh];
             float mlog = -INFINITY;
             if (lt > 0.f) {
@@ -1070,7 +1080,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
         int* last = reinterpret_cast<int*>(red_m);
         if (threadIdx.x == 0) {
             __threadfence();
-            uint32_t* ctr = p.counters + ((int64_t)s * gridDim.y + kvh) * ng + grp;
+            uint32_t* ctr = p.counters + ((int64_t)seq() * gridDim.y + kvh) * ng + grp;
             const uint32_t before = atomicAdd(ctr, 1u);
             const bool is_last = before == (uint32_t)(nwork - 1);
             if (is_last) atomicExch(ctr, 0u);  // left at zero for the next call
@@ -1080,7 +1090,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
         __syncthreads();
         if (*last) {
             // the page ring is idle now (every copy has landed): it holds the row weights
-            fused_combine<BF16, D>(p, s, h0, nh, Pl, merge ? PX : Pl, reinterpret_cast<float*>(smem));
+            fused_combine<BF16, D>(p, seq(), h0, nh, Pl, merge ? PX : Pl, reinterpret_cast<float*>(smem));
         }
     }
     griddep_launch_dependents();
@@ -1104,17 +1114,12 @@ static Phase1Fn pick_phase1(int d) {
     }
 }
 
-template <int BS, int KVB>
-Phase1Fn phase1_select(bool bf16, int d, bool head_scales) {
-    if constexpr (KVB == 2) {
-        return bf16 ? pick_phase1<true, 2, BS, true>(d) : pick_phase1<false, 2, BS, true>(d);
-    } else {
-        if (head_scales) return bf16 ? pick_phase1<true, 1, BS, true>(d) : pick_phase1<false, 1, BS, true>(d);
-        return bf16 ? pick_phase1<true, 1, BS, false>(d) : pick_phase1<false, 1, BS, false>(d);
-    }
+template <int BS, int KVB, bool HS>
+Phase1Fn phase1_select(bool bf16, int d) {
+    return bf16 ? pick_phase1<true, KVB, BS, HS>(d) : pick_phase1<false, KVB, BS, HS>(d);
 }
 
-template <int BS, int KVB>
+template <int BS, int KVB, bool HS>
 cudaError_t phase1_read_errors(unsigned int* v, bool reset) {
     cudaError_t e = cudaMemcpyFromSymbol(v, g_phase1_errors, sizeof(*v));
     if (e != cudaSuccess || !reset) return e;
