@@ -444,17 +444,21 @@ static bool supported_head_size(int d) {
     }
 }
 
-template <int BS>
-static Phase1Fn phase1_pick(bool bf16, bool fp8, int d, bool head_scales) {
-    if (fp8) return head_scales ? phase1_select<BS, 1, true>(bf16, d) : phase1_select<BS, 1, false>(bf16, d);
-    return head_scales ? phase1_select<BS, 2, true>(bf16, d) : phase1_select<BS, 2, false>(bf16, d);
+template <int BS, int KVB>
+static Phase1Fn phase1_form(bool bf16, int d, int form) {
+    switch (form) {
+        case 1: return phase1_select<BS, KVB, 1>(bf16, d);
+        case 2: return phase1_select<BS, KVB, 2>(bf16, d);
+        default: return phase1_select<BS, KVB, 0>(bf16, d);
+    }
 }
 
-static Phase1Fn phase1_for(bool bf16, bool fp8, int d, int bs, bool head_scales) {
+// form: 0 per-tensor scales, 1 per-kv-head scales, 2 per-tensor scales with an ordered grid
+static Phase1Fn phase1_for(bool bf16, bool fp8, int d, int bs, int form) {
     switch (bs) {
-        case 8: return phase1_pick<8>(bf16, fp8, d, head_scales);
-        case 16: return phase1_pick<16>(bf16, fp8, d, head_scales);
-        case 32: return phase1_pick<32>(bf16, fp8, d, head_scales);
+        case 8: return fp8 ? phase1_form<8, 1>(bf16, d, form) : phase1_form<8, 2>(bf16, d, form);
+        case 16: return fp8 ? phase1_form<16, 1>(bf16, d, form) : phase1_form<16, 2>(bf16, d, form);
+        case 32: return fp8 ? phase1_form<32, 1>(bf16, d, form) : phase1_form<32, 2>(bf16, d, form);
         default: return nullptr;
     }
 }
@@ -554,10 +558,12 @@ extern "C" const char* pa_status_string(pa_status status) {
 
 cudaError_t pa::read_decode_errors(unsigned int* v, bool reset) {
     cudaError_t (*readers[])(unsigned int*, bool) = {
-        phase1_read_errors<8, 2, false>,  phase1_read_errors<16, 2, false>, phase1_read_errors<32, 2, false>,
-        phase1_read_errors<8, 1, false>,  phase1_read_errors<16, 1, false>, phase1_read_errors<32, 1, false>,
-        phase1_read_errors<8, 2, true>,   phase1_read_errors<16, 2, true>,  phase1_read_errors<32, 2, true>,
-        phase1_read_errors<8, 1, true>,   phase1_read_errors<16, 1, true>,  phase1_read_errors<32, 1, true>};
+        phase1_read_errors<8, 2, 0>, phase1_read_errors<16, 2, 0>, phase1_read_errors<32, 2, 0>,
+        phase1_read_errors<8, 1, 0>, phase1_read_errors<16, 1, 0>, phase1_read_errors<32, 1, 0>,
+        phase1_read_errors<8, 2, 1>, phase1_read_errors<16, 2, 1>, phase1_read_errors<32, 2, 1>,
+        phase1_read_errors<8, 1, 1>, phase1_read_errors<16, 1, 1>, phase1_read_errors<32, 1, 1>,
+        phase1_read_errors<8, 2, 2>, phase1_read_errors<16, 2, 2>, phase1_read_errors<32, 2, 2>,
+        phase1_read_errors<8, 1, 2>, phase1_read_errors<16, 1, 2>, phase1_read_errors<32, 1, 2>};
     unsigned int all = 0;
     for (auto rd : readers) {
         unsigned int w = 0;
@@ -719,7 +725,7 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
     const size_t nrow_off = (smem_for(nstage) + 15) & ~(size_t)15;
     size_t smem1 = nrow_off + app_bytes;
 
-    Phase1Fn fn = phase1_for(bf16, fp8, D, bs, a.k_scales != nullptr);
+    Phase1Fn fn = phase1_for(bf16, fp8, D, bs, a.k_scales != nullptr ? 1 : 0);
     if (fn == nullptr) return PA_ERR_UNSUPPORTED;
     if (smem1 > (size_t)optin) return PA_ERR_UNSUPPORTED;
     if (ensure_smem((const void*)fn, smem1) != cudaSuccess) {
@@ -861,8 +867,15 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
     // dependent load at every CTA's start): ragged MHA batch, CTAs of up to 8 partitions,
     // 448.8 against 458.3 us; fp8 batch, up to 3 partitions, 198.8 against 197.9 us; one
     // partition per CTA (Llama batch, inputs permuted) no gain.  So only grids whose CTAs
-    // take 4 or more partitions are ordered.
-    if (a.order != nullptr && K == 1 && !few_rows && (Pmax + PX - 1) / PX >= 4 && a.num_seqs >= kOrderMinSeqs) {
+    // take 4 or more partitions are ordered.  (With per-kv-head scales the grid keeps its
+    // index order: the ordered form exists for per-tensor scales only.)
+    if (a.order != nullptr && a.k_scales == nullptr && K == 1 && !few_rows && (Pmax + PX - 1) / PX >= 4 &&
+        a.num_seqs >= kOrderMinSeqs) {
+        fn = phase1_for(bf16, fp8, D, bs, 2);
+        if (fn == nullptr || ensure_smem((const void*)fn, smem1) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return PA_ERR_CUDA;
+        }
         const pa_status so = launch_order(a.seq_lens, a.num_seqs, a.order, a.stream);
         if (so != PA_OK) return so;
         p1.order = a.order;

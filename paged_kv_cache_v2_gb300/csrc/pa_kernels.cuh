@@ -24,9 +24,8 @@ namespace pa {
 
 constexpr int kPartition = 512;
 constexpr int kWarps = PA_PHASE1_WARPS;  // phase-1 warps per CTA
-// phase 1's static shared memory: per warp, the value scale, the two encode divisors and the
-// sequence of an ordered grid
-constexpr int kPhase1StaticSmem = kWarps * (3 * (int)sizeof(float) + (int)sizeof(int));
+// phase 1's static shared memory: per warp, the value scale and the two encode divisors
+constexpr int kPhase1StaticSmem = kWarps * 3 * (int)sizeof(float);
 constexpr uint32_t kRingTarget = PA_RING_KIB * 1024u;  // shared-memory page ring per CTA
 constexpr int kMaxHeadsPerCta = 8;     // the MMA N dimension
 // Fused combine: most bytes of rows the last CTA of a (sequence, head group) merges.
@@ -110,12 +109,13 @@ __device__ __forceinline__ void store_out(void* out, int64_t idx, float v) {
 using Phase1Fn = void (*)(const Phase1Params);
 
 // Phase-1 kernel for (query dtype, head size) at block size BS, cache element bytes KVB (2:
-// fp16/bf16, 1: fp8) and scale form HS (per-kv-head scales), or nullptr; defined in
-// pa_phase1_bs<BS>[_fp8][_hs].cu, one translation unit each so they build in parallel.
-template <int BS, int KVB, bool HS>
+// fp16/bf16, 1: fp8) and FORM (0: per-tensor scales; 1: per-kv-head scales; 2: per-tensor
+// scales and an ordered grid), or nullptr; defined in pa_phase1_bs<BS>[_fp8][_hs|_ord].cu,
+// one translation unit each so they build in parallel.
+template <int BS, int KVB, int FORM>
 Phase1Fn phase1_select(bool bf16, int d);
 // Read (and optionally clear) the device error word of those kernels (one per unit).
-template <int BS, int KVB, bool HS>
+template <int BS, int KVB, int FORM>
 cudaError_t phase1_read_errors(unsigned int* v, bool reset);
 
 }  // namespace pa

@@ -188,14 +188,16 @@ __device__ __forceinline__ void append_token(const Phase1Params& p, const uint16
 #ifndef PA_FP8_MIN_CTAS
 #define PA_FP8_MIN_CTAS 3
 #endif
-// HS: the kernel reads per-kv-head scales (p.k_scales set).  The HS = false form takes the
-// per-tensor scales from the constant bank, so its page loop holds one register fewer and
-// its epilogue no shared-memory read (measured 1.3% on the fp8 batch and 2.8% on the long
-// context, kernels at their register caps).
-template <bool BF16, int KVB, int D, int BS, bool HS>
+// FORM 0: per-tensor scales, sequences in grid order; 1: per-kv-head scales (p.k_scales);
+// 2: per-tensor scales, sequence order[blockIdx.z] (p.order).  Form 0 keeps the scale
+// factors in the constant bank and the sequence index as blockIdx.z, so its page loop holds
+// no register for them: the kernels run at their register caps, and each of those registers
+// measured 1-3% (fp8 batch, long context) when the forms were one kernel.
+template <bool BF16, int KVB, int D, int BS, int FORM>
 __global__ void __launch_bounds__(kWarps * 32, KVB == 2 ? (D <= 96 ? 16 : 12) / kWarps
                                                         : ((BF16 && D >= 192) ? 8 : 4 * PA_FP8_MIN_CTAS) / kWarps)
 pa_v2_phase1_kernel(const Phase1Params p) {
+    constexpr bool HS = FORM == 1, ORD = FORM == 2;
     constexpr bool FP8 = (KVB == 1);
     constexpr int NK = (D + 15) / 16;          // 16-wide steps over the head dimension
     constexpr bool HALF_STEP = (D % 16) != 0;  // head_size 120: last step has 8 elements
@@ -218,12 +220,10 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     const int grp = bx - px * ng;
     const int kvh = blockIdx.y;
     int s = blockIdx.z;  // the sequence: blockIdx.z, or order[blockIdx.z] (read after the wait)
-    // Per warp: the value scale and the two encode divisors (per-kv-head scales), and the
-    // sequence when the grid is ordered.  Shared memory, so that the page loop holds neither:
-    // the loop and the epilogue read them back (blockIdx.z itself costs no register).
+    // Per warp: the value scale and the two encode divisors (per-kv-head scales), in shared
+    // memory so that the page loop does not hold them.
     __shared__ float wscale[kWarps][3];
-    __shared__ int wseq[kWarps];
-    static_assert(sizeof(wscale) + sizeof(wseq) == kPhase1StaticSmem, "the host sizes shared memory with this");
+    static_assert(sizeof(wscale) == kPhase1StaticSmem, "the host sizes shared memory with this");
     const int h0 = kvh * p.G + grp * kMaxHeadsPerCta;
     const int nh = min(kMaxHeadsPerCta, p.G - grp * kMaxHeadsPerCta);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -244,13 +244,9 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     constexpr uint32_t slot_bytes = 2u * pps * page_bytes;
     const int nstage = p.nstage;
 
-    // The sequence, after the prologue (the ordered grid's from shared memory).
-    auto seq = [&]() -> int {
-        return p.order != nullptr ? *reinterpret_cast<volatile int*>(&wseq[warp]) : (int)blockIdx.z;
-    };
     // Raw table entries of partition q: lane i holds pages i and 32 + i.
     auto load_ids = [&](int q, int& r0, int& r1) {
-        const int32_t* trow = p.block_tables + (int64_t)seq() * p.mbps;
+        const int32_t* trow = p.block_tables + (int64_t)s * p.mbps;
         r0 = r1 = -1;
         if (q < p.Pmax) {
             const int lb = q * ppart;
@@ -263,7 +259,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     // them on the device each step), and only the wait makes its writes visible.  The ids of
     // the first two partitions and the length then load in parallel.
     griddep_wait();
-    if (p.order != nullptr) {
+    if (ORD && p.order != nullptr) {
         s = p.order[blockIdx.z];
         if (s < 0 || s >= (int)gridDim.z) {
             // not a permutation of the sequences: nothing to serve (flagged)
@@ -271,8 +267,6 @@ pa_v2_phase1_kernel(const Phase1Params p) {
             griddep_launch_dependents();
             return;
         }
-        if (lane == 0) wseq[warp] = s;
-        __syncwarp();
     }
     int c0, c1, n0, n1;
     load_ids(px, c0, c1);
@@ -1012,7 +1006,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
                 const float fo = fac_o[hh];
                 float r = v * fac_n[hh];
                 if (fo != 0.f && !first) r = fmaf(mrg[e], fo, r);
-                const int64_t row = (int64_t)seq() * H + h0 + hh;
+                const int64_t row = (int64_t)s * H + h0 + hh;
                 if (!last_part)
                     mrg[e] = r;
                 else if (direct)
@@ -1033,7 +1027,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
                 const float lt = fin_l[hh];
                 v = lt > 0.f ? v * (vmul / lt) : 0.f;
             }
-            const int64_t row = (int64_t)seq() * H + h0 + hh;
+            const int64_t row = (int64_t)s * H + h0 + hh;
             if (direct)
                 store_out<BF16>(p.out, row * D + i, v);
             else if (p.tmp16)
@@ -1043,7 +1037,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
         }
         if (threadIdx.x < nh && !skip_out) {
             const int hh = threadIdx.x;
-            const int64_t sidx = ((int64_t)seq() * H + h0 + hh) * p.Pmax + cq;
+            const int64_t sidx = ((int64_t)s * H + h0 + hh) * p.Pmax + cq;
             const float lt = fin_l[hh];
             float mlog = -INFINITY;
             if (lt > 0.f) {
@@ -1080,7 +1074,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
         int* last = reinterpret_cast<int*>(red_m);
         if (threadIdx.x == 0) {
             __threadfence();
-            uint32_t* ctr = p.counters + ((int64_t)seq() * gridDim.y + kvh) * ng + grp;
+            uint32_t* ctr = p.counters + ((int64_t)s * gridDim.y + kvh) * ng + grp;
             const uint32_t before = atomicAdd(ctr, 1u);
             const bool is_last = before == (uint32_t)(nwork - 1);
             if (is_last) atomicExch(ctr, 0u);  // left at zero for the next call
@@ -1090,36 +1084,36 @@ pa_v2_phase1_kernel(const Phase1Params p) {
         __syncthreads();
         if (*last) {
             // the page ring is idle now (every copy has landed): it holds the row weights
-            fused_combine<BF16, D>(p, seq(), h0, nh, Pl, merge ? PX : Pl, reinterpret_cast<float*>(smem));
+            fused_combine<BF16, D>(p, s, h0, nh, Pl, merge ? PX : Pl, reinterpret_cast<float*>(smem));
         }
     }
     griddep_launch_dependents();
 }
 
 
-template <bool BF16, int KVB, int BS, bool HS>
+template <bool BF16, int KVB, int BS, int FORM>
 static Phase1Fn pick_phase1(int d) {
     switch (d) {
-        case 64: return pa_v2_phase1_kernel<BF16, KVB, 64, BS, HS>;
-        case 80: return pa_v2_phase1_kernel<BF16, KVB, 80, BS, HS>;
-        case 96: return pa_v2_phase1_kernel<BF16, KVB, 96, BS, HS>;
-        case 112: return pa_v2_phase1_kernel<BF16, KVB, 112, BS, HS>;
-        case 128: return pa_v2_phase1_kernel<BF16, KVB, 128, BS, HS>;
-        case 192: return pa_v2_phase1_kernel<BF16, KVB, 192, BS, HS>;
-        case 256: return pa_v2_phase1_kernel<BF16, KVB, 256, BS, HS>;
+        case 64: return pa_v2_phase1_kernel<BF16, KVB, 64, BS, FORM>;
+        case 80: return pa_v2_phase1_kernel<BF16, KVB, 80, BS, FORM>;
+        case 96: return pa_v2_phase1_kernel<BF16, KVB, 96, BS, FORM>;
+        case 112: return pa_v2_phase1_kernel<BF16, KVB, 112, BS, FORM>;
+        case 128: return pa_v2_phase1_kernel<BF16, KVB, 128, BS, FORM>;
+        case 192: return pa_v2_phase1_kernel<BF16, KVB, 192, BS, FORM>;
+        case 256: return pa_v2_phase1_kernel<BF16, KVB, 256, BS, FORM>;
         case 120:
-            if constexpr (KVB == 2) return pa_v2_phase1_kernel<BF16, KVB, 120, BS, HS>;
+            if constexpr (KVB == 2) return pa_v2_phase1_kernel<BF16, KVB, 120, BS, FORM>;
             else return nullptr;
         default: return nullptr;
     }
 }
 
-template <int BS, int KVB, bool HS>
+template <int BS, int KVB, int FORM>
 Phase1Fn phase1_select(bool bf16, int d) {
-    return bf16 ? pick_phase1<true, KVB, BS, HS>(d) : pick_phase1<false, KVB, BS, HS>(d);
+    return bf16 ? pick_phase1<true, KVB, BS, FORM>(d) : pick_phase1<false, KVB, BS, FORM>(d);
 }
 
-template <int BS, int KVB, bool HS>
+template <int BS, int KVB, int FORM>
 cudaError_t phase1_read_errors(unsigned int* v, bool reset) {
     cudaError_t e = cudaMemcpyFromSymbol(v, g_phase1_errors, sizeof(*v));
     if (e != cudaSuccess || !reset) return e;
