@@ -436,7 +436,8 @@ PA_API const char* pa_status_string(pa_status status);
 
 /* Device-side error flags (bit 0: a block id outside [0, num_blocks) or a table row too
  * short; bit 1: a sequence longer than max_num_partitions * 512 or a negative length;
- * bit 2: a bounded wait for a shared-memory copy gave up; bit 3: a slot outside the
+ * bit 2: a bounded wait for a shared-memory copy gave up (decode or pa_prefix; pa_prefix
+ * also when its shared memory is not 1 KiB aligned); bit 3: a slot outside the
  * cache; bit 4: a pa_copy_blocks id outside the cache; bits 5-7: pa_prefix, see there;
  * bit 8: a per-kv-head k or v scale that is not finite and > 0; bit 9: a grid-order entry
  * outside [0, num_seqs), whose grid slice is then skipped).

@@ -32,7 +32,7 @@
 //                  than 2^8 (then O and the row sum are rescaled), write P (bf16 as hi + lo
 //                  so probabilities keep ~16 bits) in the value MMA's A layout.
 // All waits are bounded (about two seconds); a wait that gives up sets an abort flag every
-// role checks and bit 8 of the device error word, and the CTA still drains its MMAs and frees
+// role checks and bit 2 of the device error word, and the CTA still drains its MMAs and frees
 // its tensor memory before it exits.
 #pragma once
 
@@ -120,7 +120,7 @@ __device__ __forceinline__ bool pfx_wait(uint64_t* bar, uint32_t parity, volatil
         if (*abort_flag) return false;
         if (globaltimer_ns() - t0 > kWaitLimitNs) {
             *abort_flag = 1;
-            prefix_flag(256u);
+            prefix_flag(4u);
             return false;
         }
     }
@@ -435,7 +435,7 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
 
     const uint32_t sbase = smem_addr(smem);
     if (sbase & 1023u) {  // the swizzled layouts are defined on 1 KiB-aligned addresses
-        if (tid == 0) prefix_flag(256u);
+        if (tid == 0) prefix_flag(4u);
         return;
     }
     uint8_t* ctl = smem + C::OFF_CTL;
@@ -537,7 +537,7 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
             }
             // every MMA issued has completed before tensor memory is released
             umma_commit(&fin[0]);
-            if (!mbar_wait_bounded(&fin[0], 0, kWaitLimitNs)) prefix_flag(256u);
+            if (!mbar_wait_bounded(&fin[0], 0, kWaitLimitNs)) prefix_flag(4u);
         }
         __syncwarp();
     } else if (warp == kPfxPvWarp) {
@@ -582,7 +582,7 @@ __global__ void __launch_bounds__(kPfxThreads, 1) pa_prefix_kernel(const __grid_
                 umma_commit(&v_empty[t % NV]);
             }
             umma_commit(&fin[1]);
-            if (!mbar_wait_bounded(&fin[1], 0, kWaitLimitNs)) prefix_flag(256u);
+            if (!mbar_wait_bounded(&fin[1], 0, kWaitLimitNs)) prefix_flag(4u);
         }
         __syncwarp();
     } else {

@@ -94,7 +94,7 @@ __global__ void __launch_bounds__(kP2Threads, 1) pa_prefix_m256_kernel(const __g
 
     const uint32_t sbase = smem_addr(smem);
     if (sbase & 1023u) {
-        if (tid == 0) prefix_flag(256u);
+        if (tid == 0) prefix_flag(4u);
         return;
     }
     uint8_t* ctl = smem + C::OFF_CTL;
@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(kP2Threads, 1) pa_prefix_m256_kernel(const __g
                 umma_commit(&k_empty[t % NK]);
             }
             umma_commit(&fin[2 * g]);
-            if (!mbar_wait_bounded(&fin[2 * g], 0, kWaitLimitNs)) prefix_flag(256u);
+            if (!mbar_wait_bounded(&fin[2 * g], 0, kWaitLimitNs)) prefix_flag(4u);
         }
         __syncwarp();
     } else if (warp == kP2PvWarp || warp == kP2PvWarp1) {
@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kP2Threads, 1) pa_prefix_m256_kernel(const __g
                 umma_commit(&v_empty[t % NV]);
             }
             umma_commit(&fin[2 * g + 1]);
-            if (!mbar_wait_bounded(&fin[2 * g + 1], 0, kWaitLimitNs)) prefix_flag(256u);
+            if (!mbar_wait_bounded(&fin[2 * g + 1], 0, kWaitLimitNs)) prefix_flag(4u);
         }
         __syncwarp();
     } else if (warp >= kP2SoftmaxWarp0 && warp < kP2SoftmaxWarp0 + 8 && (warp - kP2SoftmaxWarp0) / 4 < ng) {
