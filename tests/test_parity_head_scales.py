@@ -125,3 +125,34 @@ def test_invalid_head_scale_is_flagged():
                                  "v_scale": 0.07})
     ref = oracle.decode_workload(good)["out"].reshape(out.shape)
     assert np.abs(out[:, :2].double().numpy() - ref[:, :2]).max() <= 2e-2 + 1e-3
+
+
+_CHILD = r"""
+import sys
+sys.path.insert(0, {here!r}); sys.path.insert(0, {root!r})
+import oracle, workloads
+from gpu_harness import check_decode, run_decode
+from test_parity_append import _check_all
+for spec in {specs!r}:
+    wl = workloads.build(**spec)
+    check_decode(wl, run_decode(wl), oracle.decode_workload(wl), label=f"child decode {{spec}}")
+    _check_all(wl, f"child append {{spec}}")
+print("child ok")
+"""
+
+
+@pytest.mark.parametrize("env", [{"PA_DECODE_PX": "2"}, {"PA_DECODE_SPLIT": "2"}])
+def test_head_scales_with_strides_and_cluster_split(env):
+    # the per-head kernel form with CTAs striding over partitions, and with a 2-CTA cluster
+    # sharing each partition (the partners hand their rows to the first CTA)
+    import os
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    specs = [dict(num_seqs=4, num_heads=16, num_kv_heads=4, head_size=128, block_size=16,
+                  seq_lens=[3000, 1, 700, 2600], kv_cache_dtype="fp8_e4m3", alibi=True,
+                  k_scales=_scales(4, 11), v_scales=_scales(4, 12), seed=660)]
+    code = _CHILD.format(here=here, root=os.path.dirname(here), specs=specs)
+    r = subprocess.run([sys.executable, "-c", code], env=dict(os.environ, **env), capture_output=True, text=True,
+                       timeout=900)
+    assert r.returncode == 0 and "child ok" in r.stdout, r.stdout[-2000:] + r.stderr[-4000:]
