@@ -372,17 +372,33 @@ pa_v2_phase1_kernel(const Phase1Params p) {
             int b[4];
 #pragma unroll
             for (int pg = 0; pg < 4; ++pg) b[pg] = pg < pps ? page_id(r0, r1, j * pps + pg) : -1;
-            if (lane == 0) {
-                uint64_t* bar = &bars[ipos];
-                uint8_t* kdst = ring + (size_t)ipos * slot_bytes;
-                uint8_t* vdst = kdst + (size_t)pps * page_bytes;
-                mbar_arrive_expect_tx(bar, (uint32_t)__popc(ok) * 2u * page_bytes);
-#pragma unroll
-                for (int pg = 0; pg < 4; ++pg) {
-                    if (pg < pps && ((ok >> pg) & 1u)) {
-                        bulk_g2s(kdst + pg * page_bytes, kc_head + (size_t)b[pg] * block_stride, page_bytes, bar, policy);
-                        bulk_g2s(vdst + pg * page_bytes, vc_head + (size_t)b[pg] * block_stride, page_bytes, bar, policy);
+            uint64_t* bar = &bars[ipos];
+            uint8_t* kdst = ring + (size_t)ipos * slot_bytes;
+            uint8_t* vdst = kdst + (size_t)pps * page_bytes;
+            if constexpr (pps == 1) {
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(bar, (uint32_t)__popc(ok) * 2u * page_bytes);
+                    if (ok & 1u) {
+                        bulk_g2s(kdst, kc_head + (size_t)b[0] * block_stride, page_bytes, bar, policy);
+                        bulk_g2s(vdst, vc_head + (size_t)b[0] * block_stride, page_bytes, bar, policy);
                     }
+                }
+            } else {
+                // Several pages a slot: lanes 2 pg and 2 pg + 1 copy page pg's keys and values,
+                // so one copy instruction serves the slot (each copy instruction holds the
+                // issuing warp ~0.1 us; fp8 batch 188.3 against 190.6 us).  With one page a slot
+                // lane 0 alone issues both (the extra warp barrier cost more than it saved).
+                if (lane == 0) mbar_arrive_expect_tx(bar, (uint32_t)__popc(ok) * 2u * page_bytes);
+                __syncwarp();
+                const int pg = lane >> 1;
+                if (lane < 2 * pps && ((ok >> pg) & 1u)) {
+                    int bsel = b[0];
+#pragma unroll
+                    for (int q = 1; q < 4; ++q)
+                        if (q < pps && pg == q) bsel = b[q];
+                    const bool isv = lane & 1;
+                    bulk_g2s((isv ? vdst : kdst) + pg * page_bytes,
+                             (isv ? vc_head : kc_head) + (size_t)bsel * block_stride, page_bytes, bar, policy);
                 }
             }
             ++nis;
