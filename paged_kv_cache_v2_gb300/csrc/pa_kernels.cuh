@@ -106,6 +106,30 @@ __device__ __forceinline__ void store_out(void* out, int64_t idx, float v) {
         reinterpret_cast<__half*>(out)[idx] = __float2half_rn(v);
 }
 
+// Four consecutive output elements (idx a multiple of 4): one 8-byte store where the buffer
+// allows it (the ABI asks only 4-byte alignment of the output), else four element stores.
+template <bool BF16>
+__device__ __forceinline__ void store_out4(void* out, int64_t idx, float4 v) {
+    if (reinterpret_cast<uintptr_t>(out) & 7u) {
+        store_out<BF16>(out, idx, v.x);
+        store_out<BF16>(out, idx + 1, v.y);
+        store_out<BF16>(out, idx + 2, v.z);
+        store_out<BF16>(out, idx + 3, v.w);
+        return;
+    }
+    uint2 w;
+    if constexpr (BF16) {
+        const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+        w.x = *reinterpret_cast<const uint32_t*>(&a);
+        w.y = *reinterpret_cast<const uint32_t*>(&b);
+    } else {
+        const __half2 a = __floats2half2_rn(v.x, v.y), b = __floats2half2_rn(v.z, v.w);
+        w.x = *reinterpret_cast<const uint32_t*>(&a);
+        w.y = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    reinterpret_cast<uint2*>(out)[idx >> 2] = w;
+}
+
 using Phase1Fn = void (*)(const Phase1Params);
 
 // Phase-1 kernel for (query dtype, head size) at block size BS, cache element bytes KVB (2:

@@ -1044,25 +1044,50 @@ pa_v2_phase1_kernel(const Phase1Params p) {
                     static_cast<float*>(p.tmp_out)[(row * p.Pmax + px) * D + i] = r;
             }
         }
-        for (int e = threadIdx.x; e < nh * D && !merge && !skip_out; e += blockDim.x) {
-            const int hh = e / D, i = e - hh * D;
-            float v = 0.f;
+        if (K == 1) {
+            // four consecutive elements a thread: float4 rows in shared memory (D and the row
+            // stride D + 4 are multiples of 4), one 8- or 16-byte store
+            for (int e4 = threadIdx.x; e4 < nh * D / 4 && !merge && !skip_out; e4 += blockDim.x) {
+                const int e = 4 * e4, hh = e / D, i = e - hh * D;
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int w = 0; w < kWarps; ++w) v += red_o[(w * nh + hh) * RS + i];
-            if (K > 1) {
+                for (int w = 0; w < kWarps; ++w) {
+                    const float4 r = *reinterpret_cast<const float4*>(red_o + (w * nh + hh) * RS + i);
+                    v.x += r.x;
+                    v.y += r.y;
+                    v.z += r.z;
+                    v.w += r.w;
+                }
+                const float lt = fin_l[hh];
+                const float f = lt > 0.f ? vmul / lt : 0.f;
+                v.x *= f;
+                v.y *= f;
+                v.z *= f;
+                v.w *= f;
+                const int64_t row = (int64_t)s * H + h0 + hh;
+                if (direct)
+                    store_out4<BF16>(p.out, row * D + i, v);
+                else if (p.tmp16)
+                    store_out4<BF16>(p.tmp_out, (row * p.Pmax + cq) * D + i, v);
+                else
+                    reinterpret_cast<float4*>(p.tmp_out)[((row * p.Pmax + cq) * D + i) >> 2] = v;
+            }
+        } else {
+            for (int e = threadIdx.x; e < nh * D && !merge && !skip_out; e += blockDim.x) {
+                const int hh = e / D, i = e - hh * D;
+                float v = 0.f;
+#pragma unroll
+                for (int w = 0; w < kWarps; ++w) v += red_o[(w * nh + hh) * RS + i];
                 v *= vmul * fac_o[hh];
                 for (int k = 0; k < K - 1; ++k) v = fmaf(pbuf[k * pstride + 2 * kMaxHeadsPerCta + e], pbuf[k * pstride + hh], v);
-            } else {
-                const float lt = fin_l[hh];
-                v = lt > 0.f ? v * (vmul / lt) : 0.f;
+                const int64_t row = (int64_t)s * H + h0 + hh;
+                if (direct)
+                    store_out<BF16>(p.out, row * D + i, v);
+                else if (p.tmp16)
+                    store_out<BF16>(p.tmp_out, (row * p.Pmax + cq) * D + i, v);
+                else
+                    static_cast<float*>(p.tmp_out)[(row * p.Pmax + cq) * D + i] = v;
             }
-            const int64_t row = (int64_t)s * H + h0 + hh;
-            if (direct)
-                store_out<BF16>(p.out, row * D + i, v);
-            else if (p.tmp16)
-                store_out<BF16>(p.tmp_out, (row * p.Pmax + cq) * D + i, v);
-            else
-                static_cast<float*>(p.tmp_out)[(row * p.Pmax + cq) * D + i] = v;
         }
         if (threadIdx.x < nh && !skip_out) {
             const int hh = threadIdx.x;

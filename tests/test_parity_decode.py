@@ -146,3 +146,28 @@ def test_tmp_output_in_query_dtype(name):
     gpu = run_decode(wl, tmp_dtype=wl.query.dtype)
     assert gpu[3].dtype == wl.query.dtype
     check_decode(wl, gpu, oracle.decode_workload(wl), label=f"tmp16 {name}")
+
+
+@pytest.mark.parametrize("q_dtype", ["f16", "bf16"])
+def test_output_only_four_byte_aligned(q_dtype):
+    # the ABI asks 4-byte alignment of the output: an output that starts 4 bytes past an
+    # 8-byte boundary takes the element-store path of the epilogue (one-partition sequences
+    # write it directly)
+    wl = workloads.build(num_seqs=3, num_heads=8, num_kv_heads=2, head_size=128, block_size=16,
+                         seq_lens=[300, 1, 1500], q_dtype=q_dtype, seed=71)
+    ref = oracle.decode_workload(wl)
+    dev = {k: v for k, v in (("query", wl.query.cuda()), ("key_cache", wl.key_cache.cuda()),
+                             ("value_cache", wl.value_cache.cuda()), ("block_tables", wl.block_tables.cuda()),
+                             ("seq_lens", wl.seq_lens.cuda()))}
+    S, H, d = wl.query.shape
+    P = wl.max_num_partitions
+    buf = torch.full((S * H * d + 2,), float("nan"), dtype=wl.query.dtype, device="cuda")
+    out = buf[2:].view(S, H, d)  # 4 bytes past the allocation's start
+    assert out.data_ptr() % 8 == 4
+    es = torch.empty((S, H, P), dtype=torch.float32, device="cuda")
+    ml = torch.empty_like(es)
+    tmp = torch.empty((S, H, P, d), dtype=torch.float32, device="cuda")
+    pa.pa_v2_decode(out, es, ml, tmp, dev["query"], dev["key_cache"], dev["value_cache"], wl.num_kv_heads, wl.scale,
+                    dev["block_tables"], dev["seq_lens"], wl.block_size, wl.max_seq_len)
+    torch.cuda.synchronize()
+    check_decode(wl, (out.cpu(), es.cpu(), ml.cpu(), tmp.cpu()), ref, label=f"4-byte aligned output {q_dtype}")
