@@ -139,29 +139,18 @@ __device__ __forceinline__ float row_f32(uint16_t v) {
 
 // Write the staged key/value rows of one token (slot o of a page) into the shared-memory copy
 // of its K and V pages and, when page >= 0 (the page's (block, kv head) index), into the
-// caches.  Lane c moves K chunk c (16 bytes of the x-packed page) and V elements lane,
-// lane + 32, ...
-template <bool BF16, int KVB, int D, int BS>
-__device__ __forceinline__ void append_token(const Phase1Params& p, const uint16_t* nrow, uint8_t* kpage,
-                                             uint8_t* vpage, int o, int64_t page, int lane, float k_enc,
-                                             float v_enc) {
+// caches.  The rows are staged as the cache stores them (the bits of a 16-bit cache, the e4m3
+// codes of an fp8 one): the key row (D elements), then the value row.  Lane c moves K chunk c
+// (16 bytes of the x-packed page) and V elements lane, lane + 32, ...
+template <int KVB, int D, int BS>
+__device__ __forceinline__ void append_token(const Phase1Params& p, const uint8_t* nrow, uint8_t* kpage,
+                                             uint8_t* vpage, int o, int64_t page, int lane) {
     constexpr int X = 16 / KVB;  // elements per 16-byte chunk
     constexpr uint32_t page_bytes = (uint32_t)D * BS * KVB;
     uint8_t* kc = page >= 0 ? const_cast<uint8_t*>(p.kcache) + page * page_bytes : nullptr;
     uint8_t* vc = page >= 0 ? const_cast<uint8_t*>(p.vcache) + page * page_bytes : nullptr;
     for (int c = lane; c < D / X; c += 32) {
-        uint4 chunk;
-        if constexpr (KVB == 2) {
-            chunk = reinterpret_cast<const uint4*>(nrow)[c];
-        } else {
-            uint16_t q[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                q[i] = f32x2_to_e4m3x2(__fdiv_rn(row_f32<BF16>(nrow[c * X + 2 * i]), k_enc),
-                                       __fdiv_rn(row_f32<BF16>(nrow[c * X + 2 * i + 1]), k_enc));
-            chunk = make_uint4((uint32_t)q[0] | ((uint32_t)q[1] << 16), (uint32_t)q[2] | ((uint32_t)q[3] << 16),
-                               (uint32_t)q[4] | ((uint32_t)q[5] << 16), (uint32_t)q[6] | ((uint32_t)q[7] << 16));
-        }
+        const uint4 chunk = reinterpret_cast<const uint4*>(nrow)[c];
         const uint32_t off = (uint32_t)(c * BS + o) * 16u;
         *reinterpret_cast<uint4*>(kpage + off) = chunk;
         if (kc) *reinterpret_cast<uint4*>(kc + off) = chunk;
@@ -169,11 +158,11 @@ __device__ __forceinline__ void append_token(const Phase1Params& p, const uint16
     for (int i = lane; i < D; i += 32) {
         const uint32_t off = (uint32_t)(i * BS + o) * KVB;
         if constexpr (KVB == 2) {
-            const uint16_t v = nrow[D + i];
+            const uint16_t v = reinterpret_cast<const uint16_t*>(nrow)[D + i];
             *reinterpret_cast<uint16_t*>(vpage + off) = v;
             if (vc) *reinterpret_cast<uint16_t*>(vc + off) = v;
         } else {
-            const uint8_t v = (uint8_t)(f32x2_to_e4m3x2(__fdiv_rn(row_f32<BF16>(nrow[D + i]), v_enc), 0.f) & 0xffu);
+            const uint8_t v = nrow[D + i];
             vpage[off] = v;
             if (vc) vc[off] = v;
         }
@@ -476,16 +465,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     const int pg_last = app ? ((L - 1) >> bs_log2) - (Pl - 1) * ppart : 0;  // page in the last partition
     const int j_last = pg_last >> pps_log2;                                   // its slot
     const bool app_warp = app && (j_last % KW) == gw;
-    uint16_t* nrow = reinterpret_cast<uint16_t*>(smem + p.nrow_off);  // [2][D]: key row, value row
-    if (app_warp) {
-        const uint16_t* ks = p.new_k + (int64_t)s * p.nk_stride + (int64_t)kvh * D;
-        const uint16_t* vs = p.new_v + (int64_t)s * p.nv_stride + (int64_t)kvh * D;
-        for (int c = lane; c < D / 8; c += 32) {
-            reinterpret_cast<uint4*>(nrow)[c] = reinterpret_cast<const uint4*>(ks)[c];
-            reinterpret_cast<uint4*>(nrow + D)[c] = reinterpret_cast<const uint4*>(vs)[c];
-        }
-        __syncwarp();
-    }
+    uint8_t* nrow = smem + p.nrow_off;  // the key row, then the value row, as the cache stores them
 
     // ALiBi slopes of this thread's two head columns (2t, 2t+1), base-2 units.
     float sl0 = 0.f, sl1 = 0.f;
@@ -530,6 +510,43 @@ pa_v2_phase1_kernel(const Phase1Params p) {
         if constexpr (HS) return wscale[warp][2];
         else return p.v_enc;
     };
+    if (app_warp) {
+        const uint16_t* ks = p.new_k + (int64_t)s * p.nk_stride + (int64_t)kvh * D;
+        const uint16_t* vs = p.new_v + (int64_t)s * p.nv_stride + (int64_t)kvh * D;
+        if constexpr (KVB == 2) {
+            for (int c = lane; c < D / 8; c += 32) {
+                reinterpret_cast<uint4*>(nrow)[c] = reinterpret_cast<const uint4*>(ks)[c];
+                reinterpret_cast<uint4*>(nrow + 2 * D)[c] = reinterpret_cast<const uint4*>(vs)[c];
+            }
+        } else {
+            // encoded here, while the first pages are in flight, exactly as the cache writer
+            // encodes (e4m3fn, saturating, of x / scale with an IEEE fp32 divide), so that the
+            // slot holding the token only copies bytes
+            const float ke = enc_k(), ve = enc_v();
+            for (int c = lane; c < D / 8; c += 32) {  // 8 elements of each row a lane
+                const uint4 kr = reinterpret_cast<const uint4*>(ks)[c];
+                const uint4 vr = reinterpret_cast<const uint4*>(vs)[c];
+                const uint32_t kw[4] = {kr.x, kr.y, kr.z, kr.w}, vw[4] = {vr.x, vr.y, vr.z, vr.w};
+                uint32_t kq[2], vq[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint16_t k01 = f32x2_to_e4m3x2(__fdiv_rn(row_f32<BF16>(lo16(kw[2 * h])), ke),
+                                                         __fdiv_rn(row_f32<BF16>(hi16(kw[2 * h])), ke));
+                    const uint16_t k23 = f32x2_to_e4m3x2(__fdiv_rn(row_f32<BF16>(lo16(kw[2 * h + 1])), ke),
+                                                         __fdiv_rn(row_f32<BF16>(hi16(kw[2 * h + 1])), ke));
+                    const uint16_t v01 = f32x2_to_e4m3x2(__fdiv_rn(row_f32<BF16>(lo16(vw[2 * h])), ve),
+                                                         __fdiv_rn(row_f32<BF16>(hi16(vw[2 * h])), ve));
+                    const uint16_t v23 = f32x2_to_e4m3x2(__fdiv_rn(row_f32<BF16>(lo16(vw[2 * h + 1])), ve),
+                                                         __fdiv_rn(row_f32<BF16>(hi16(vw[2 * h + 1])), ve));
+                    kq[h] = (uint32_t)k01 | ((uint32_t)k23 << 16);
+                    vq[h] = (uint32_t)v01 | ((uint32_t)v23 << 16);
+                }
+                reinterpret_cast<uint2*>(nrow)[c] = make_uint2(kq[0], kq[1]);
+                reinterpret_cast<uint2*>(nrow + D)[c] = make_uint2(vq[0], vq[1]);
+            }
+        }
+        __syncwarp();
+    }
     const float qk_mul0 = qk_mul * qs0, qk_mul1 = qk_mul * qs1;  // fp8 with a bf16 query: per-column scale
 
     // Per-lane ldmatrix row of the K page: token within the 16-token tile, chunk offset.
@@ -589,9 +606,9 @@ pa_v2_phase1_kernel(const Phase1Params p) {
                 if ((okmask >> pg) & 1u) {
                     const int b = page_id(c0, c1, pg_last);
                     const bool to_cache = grp == 0;
-                    append_token<BF16, KVB, D, BS>(p, nrow, const_cast<uint8_t*>(kslot) + (size_t)pg * page_bytes,
-                                                   const_cast<uint8_t*>(vslot) + (size_t)pg * page_bytes, (L - 1) & (bs - 1),
-                                                   to_cache ? (int64_t)b * p.Hk + kvh : -1, lane, enc_k(), enc_v());
+                    append_token<KVB, D, BS>(p, nrow, const_cast<uint8_t*>(kslot) + (size_t)pg * page_bytes,
+                                             const_cast<uint8_t*>(vslot) + (size_t)pg * page_bytes, (L - 1) & (bs - 1),
+                                             to_cache ? (int64_t)b * p.Hk + kvh : -1, lane);
                 }
                 __syncwarp();
             }
