@@ -346,11 +346,7 @@ pa_v2_phase2_rows_kernel(const Phase2Params p) {
     }
     if (col) {
         const float inv = tot > 0.f ? 1.f / tot : 0.f;
-        const int64_t o = row * p.D + 4 * lane;
-        store_out<BF16>(p.out, o, acc.x * inv);
-        store_out<BF16>(p.out, o + 1, acc.y * inv);
-        store_out<BF16>(p.out, o + 2, acc.z * inv);
-        store_out<BF16>(p.out, o + 3, acc.w * inv);
+        store_out4<BF16>(p.out, row * p.D + 4 * lane, make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
     }
 }
 
@@ -428,8 +424,18 @@ pa_v2_phase2_merged_kernel(const Phase2Params p) {
     }
     __syncthreads();
     const float inv = tot > 0.f ? 1.f / tot : 0.f;
-    for (int i = tid; i < p.D; i += kP2mThreads)
-        store_out<BF16>(p.out, row * p.D + i, (part[i] + part[p.D + i] + part[2 * p.D + i] + part[3 * p.D + i]) * inv);
+    for (int i4 = tid; i4 < p.D / 4; i4 += kP2mThreads) {
+        float4 v = reinterpret_cast<const float4*>(part)[i4];
+#pragma unroll
+        for (int g2 = 1; g2 < 4; ++g2) {
+            const float4 u = reinterpret_cast<const float4*>(part + g2 * p.D)[i4];
+            v.x += u.x;
+            v.y += u.y;
+            v.z += u.z;
+            v.w += u.w;
+        }
+        store_out4<BF16>(p.out, row * p.D + 4 * i4, make_float4(v.x * inv, v.y * inv, v.z * inv, v.w * inv));
+    }
 }
 
 // ---------------------------------------------------------------------------------------
