@@ -230,6 +230,8 @@ pa_v2_phase2_kernel(const Phase2Params p) {
 // sequence's results are the same in any order.
 constexpr int kOrderThreads = 1024;
 constexpr int kOrderMinSeqs = 16;  // below this the grid has few sequences to reorder
+constexpr int kOrderedWaves = 8;     // an ordered grid's stride: about this many waves of CTAs
+constexpr int kOrderedMaxParts = 16; // and at most this many partitions a CTA
 constexpr int kOrderBuckets = 1024;
 
 __global__ void __launch_bounds__(kOrderThreads) pa_v2_order_kernel(const int32_t* seq_lens, int S, int32_t* order) {
@@ -818,6 +820,26 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
         (void)cudaGetLastError();
         return PA_ERR_CUDA;
     }
+    // An ordered grid (order scratch, per-tensor scales, a wide batch) takes fewer, longer
+    // CTAs: about 8 waves of them, up to 16 partitions each, since the longest start first
+    // and the tail no longer waits on them.  Measured (phase 1, ordered): fp8 batch PX 2 / 3 /
+    // 4 172.4 / 172.1 / 172.6 us against 175.3 us at PX 7 (16 waves, index order); ragged MHA
+    // batch PX 4 / 5 / 6 432.9 / 434.1 / 436.1 us against 438.3 us at PX 7.  Where that still
+    // leaves CTAs of fewer than 4 partitions (the Llama batch: PX 7 of 8) the grid keeps its
+    // index order and the 16-wave stride.
+    bool ordered = false;
+    if (a.order != nullptr && a.k_scales == nullptr && !few_rows && a.num_seqs >= kOrderMinSeqs && px_override() <= 0) {
+        int64_t px_ord = (int64_t)kOrderedWaves * slots / rows;
+        const int64_t px_min = (Pmax + kOrderedMaxParts - 1) / kOrderedMaxParts;
+        if (px_ord < px_min) px_ord = px_min;
+        if (px_ord > Pmax) px_ord = Pmax;
+        if (px_ord >= 1 && (Pmax + px_ord - 1) / px_ord >= 4) {
+            PX = px_ord;
+            ordered = true;
+        }
+    } else if (a.order != nullptr && a.k_scales == nullptr && !few_rows && a.num_seqs >= kOrderMinSeqs) {
+        ordered = (Pmax + PX - 1) / PX >= 4;  // a stride set for a tuning run
+    }
 
     // Fused combine (V1/V2 dispatch, "paged_attn.py" forward_decode, re-decided for this GPU):
     // with arrival counters the last CTA of each (sequence, head group) merges the partitions,
@@ -867,16 +889,15 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
             K /= 2;
     }
     p1.csplit = K;
-    // Grid order: where CTAs stride over several partitions their work differs by up to 8x,
+    // Grid order: where CTAs stride over several partitions their work differs several-fold,
     // and a long sequence scheduled last leaves a tail; serving the sequences with the most
-    // partitions first removes it.  Measured (step, with the order kernel and the extra
-    // dependent load at every CTA's start): ragged MHA batch, CTAs of up to 8 partitions,
-    // 448.8 against 458.3 us; fp8 batch, up to 3 partitions, 198.8 against 197.9 us; one
-    // partition per CTA (Llama batch, inputs permuted) no gain.  So only grids whose CTAs
-    // take 4 or more partitions are ordered.  (With per-kv-head scales the grid keeps its
-    // index order: the ordered form exists for per-tensor scales only.)
-    if (a.order != nullptr && a.k_scales == nullptr && K == 1 && !few_rows && (Pmax + PX - 1) / PX >= 4 &&
-        a.num_seqs >= kOrderMinSeqs) {
+    // partitions first removes it (the order kernel runs first; every CTA then loads its
+    // sequence from the order).  Measured at the 16-wave stride: ragged MHA step 448.8 against
+    // 458.3 us; fp8 batch (CTAs of up to 3 partitions) 198.8 against 197.9 us, the order
+    // kernel costing more than it saved there -- hence grids are ordered only with CTAs of 4
+    // or more partitions.  (With per-kv-head scales the grid keeps its index order: the
+    // ordered form exists for per-tensor scales only.)
+    if (ordered && K == 1) {
         fn = phase1_for(bf16, fp8, D, bs, 2);
         if (fn == nullptr || ensure_smem((const void*)fn, smem1) != cudaSuccess) {
             (void)cudaGetLastError();
