@@ -8,13 +8,15 @@
  * allocate nothing, never synchronise the stream, and return as soon as the work is
  * enqueued.  Results are valid in stream order.
  *
- * The decode, append, cache-writer and block-move calls may be captured into a CUDA graph
- * (stream capture).  What they choose on the host (grid, kernel form, partitions per CTA,
- * cluster split) follows from the sizes, dtypes and pointer alignments passed, never from
- * the contents of device buffers, so a replay is correct for whatever the captured buffers
- * hold then (lengths up to the captured max_seq_len).  Make one uncaptured call of each
- * configuration first, which sets the kernels' shared-memory attributes; the PA_CHECK=1
- * host check synchronises the stream and cannot be captured.
+ * Every call may be captured into a CUDA graph (stream capture).  What the decode, append,
+ * cache-writer, copy_blocks and prefix calls choose on the host (grid, kernel form,
+ * partitions per CTA, cluster split, context split plan) follows from the sizes, dtypes and
+ * pointer alignments passed, never from the contents of device buffers, so a replay is
+ * correct for whatever the captured buffers hold then (lengths up to the captured
+ * max_seq_len or table width).  pa_swap_blocks reads its mapping on the host: a replay
+ * repeats the captured pairs.  Make one uncaptured call of each configuration first, which
+ * sets the kernels' shared-memory attributes; the PA_CHECK=1 host check synchronises the
+ * stream and cannot be captured.
  *
  * Layouts are row-major C arrays:
  *   query        [num_seqs][num_heads][head_size]                      q dtype

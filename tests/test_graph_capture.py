@@ -163,3 +163,92 @@ def test_two_replays_in_a_row_on_ping_pong_buffers():
         torch.cuda.synchronize()
         for i, s in enumerate(steps):
             _same(s.results(), refs[i], f"replay round {rep} step {i}")
+
+
+def _capture(fn):
+    fn()  # uncaptured first
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    return g
+
+
+def test_copy_blocks_replay_reads_the_mapping_at_replay():
+    # the mapping lives on the device: a replay copies the pairs the buffer holds then
+    gen = torch.Generator().manual_seed(5)
+    NB, layers = 40, 3
+    kcs = [torch.randint(0, 255, (NB, 2, 8, 16, 16), generator=gen, dtype=torch.uint8).cuda() for _ in range(layers)]
+    vcs = [torch.randint(0, 255, (NB, 2, 128, 16), generator=gen, dtype=torch.uint8).cuda() for _ in range(layers)]
+    m = torch.tensor([[1, 2], [3, 4]], dtype=torch.int64, device="cuda")
+    g = _capture(lambda: pa.pa_copy_blocks(kcs, vcs, m))
+    for pairs in ([[5, 6], [7, 8]], [[30, 0], [12, 39]]):
+        want = [t.cpu().numpy().copy() for t in kcs + vcs]
+        mm = torch.tensor(pairs, dtype=torch.int64)
+        for a in want:
+            oracle.copy_blocks(a, a, mm)
+        m.copy_(mm)
+        g.replay()
+        torch.cuda.synchronize()
+        for a, b in zip(kcs + vcs, want):
+            assert np.array_equal(a.cpu().numpy(), b)
+
+
+def test_swap_blocks_replay_moves_the_captured_pairs():
+    # the mapping is read on the host when the call is made: a replay repeats the captured
+    # pairs, with whatever the source blocks hold then
+    gen = torch.Generator().manual_seed(6)
+    src = torch.randint(0, 255, (16, 4, 64, 16), generator=gen, dtype=torch.uint8).cuda()
+    dst = torch.zeros((12, 4, 64, 16), dtype=torch.uint8).pin_memory()
+    m = torch.tensor([[3, 0], [15, 11], [7, 5]], dtype=torch.int64)
+    g = _capture(lambda: pa.pa_swap_blocks(src, dst, m))
+    src.copy_(torch.randint(0, 255, src.shape, generator=gen, dtype=torch.uint8))
+    want = dst.numpy().copy()
+    oracle.copy_blocks(want, src.cpu().numpy(), m)
+    g.replay()
+    torch.cuda.synchronize()
+    assert np.array_equal(dst.numpy(), want)
+
+
+def test_prefix_replay_with_split_contexts():
+    # contexts above 16K tokens are cut into parts (caller-owned workspace); a replay on a
+    # second workload's lengths, tables and rows matches an eager call bit for bit and the
+    # oracle
+    from gpu_harness import check_prefix, prefix_to_device
+    kw = dict(num_seqs=3, num_heads=8, num_kv_heads=2, head_size=128, block_size=16, query_lens=[100, 37, 64],
+              q_dtype="bf16", table_width=1280)
+    wl1 = workloads.build_prefix(context_lens=[20000, 0, 700], seed=1, **kw)
+    wl2 = workloads.build_prefix(context_lens=[300, 18000, 5], seed=2, **kw)
+    assert wl2.key_cache.shape[0] <= wl1.key_cache.shape[0]
+    dev = prefix_to_device(wl1)
+    S, H, Hk, d = 3, 8, 2, 128
+    mql = 100
+    ws = torch.empty(pa.prefix_workspace_size(S, H, Hk, d, mql, 8), dtype=torch.uint8, device="cuda")
+    out = torch.empty_like(dev["query"])
+
+    def call():
+        pa.pa_prefix(out, dev["query"], dev["key"], dev["value"], dev["key_cache"], dev["value_cache"],
+                     dev["block_tables"], dev["query_start_loc"], dev["context_lens"], mql, scale=wl1.scale,
+                     workspace=ws, max_splits=8)
+
+    def load(wl):
+        for k in ("query", "key", "value", "block_tables", "query_start_loc", "context_lens"):
+            dev[k].copy_(getattr(wl, k))
+        for k in ("key_cache", "value_cache"):
+            dev[k][:getattr(wl, k).shape[0]].copy_(getattr(wl, k))
+        out.fill_(float("nan"))
+
+    eager = []
+    for wl in (wl1, wl2):
+        load(wl)
+        call()
+        torch.cuda.synchronize()
+        eager.append(out.cpu())
+    load(wl1)
+    g = _capture(call)
+    for wl, ref in ((wl1, eager[0]), (wl2, eager[1])):
+        load(wl)
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out.cpu().view(torch.int16), ref.view(torch.int16))
+    check_prefix(wl2, eager[1], oracle.prefix_workload(wl2), label="prefix replay, second inputs")
