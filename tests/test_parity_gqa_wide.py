@@ -1,0 +1,76 @@
+"""GPU parity: more than 8 query heads per kv head with 16-bit caches (the GQA view of
+"paged_attention_v2_pytorch.py": query heads h * G .. h * G + G - 1 share kv head h).  The
+grid then runs ceil(G / 8) CTAs per (partition, kv head), each serving up to 8 of the heads
+over the same pages.
+
+Checked against the fp64 oracle: G from 9 to 32 (partial last groups, two and four groups),
+head sizes 64 to 128 including 120, block sizes 8/16/32, both query dtypes, ALiBi, edge
+lengths, a 16-bit tmp_output, the fused append, and the few-rows grid whose CTAs fold their
+partitions into one row.
+"""
+from __future__ import annotations
+
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_v2_gb300 as pa
+import workloads
+from gpu_harness import check_decode, run_decode
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _clear_device_errors():
+    pa.pa_get_device_errors(reset=True)
+    yield
+    assert pa.pa_get_device_errors() == 0
+
+
+@pytest.mark.parametrize("G", [9, 12, 16, 24, 32])
+def test_gqa_ratios_above_eight(G):
+    Hk = 2
+    wl = workloads.build(num_seqs=3, num_heads=G * Hk, num_kv_heads=Hk, head_size=128, block_size=16,
+                         seq_lens=[700, 33, 1500], seed=800 + G)
+    check_decode(wl, run_decode(wl), oracle.decode_workload(wl), label=f"G{G}")
+
+
+@pytest.mark.parametrize("d", [64, 80, 96, 112, 120, 128])
+@pytest.mark.parametrize("bs", [8, 16, 32])
+def test_head_sizes_and_block_sizes(d, bs):
+    wl = workloads.build(num_seqs=4, num_heads=32, num_kv_heads=2, head_size=d, block_size=bs,
+                         seq_lens=[1, 513, 1030, 2047], q_dtype="bf16", alibi=True, seed=820 + d + bs)
+    check_decode(wl, run_decode(wl), oracle.decode_workload(wl), label=f"G16 d{d} bs{bs}")
+
+
+@pytest.mark.parametrize("q_dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("alibi", [False, True])
+def test_dtypes_alibi_and_edge_lengths(q_dtype, alibi):
+    wl = workloads.build(num_seqs=9, num_heads=28, num_kv_heads=2, head_size=128, block_size=16,
+                         seq_lens=[0, 1, 15, 16, 17, 511, 512, 513, 3000], q_dtype=q_dtype, alibi=alibi,
+                         seed=840)
+    check_decode(wl, run_decode(wl), oracle.decode_workload(wl), label=f"G14 {q_dtype} alibi={alibi}")
+
+
+def test_sixteen_bit_tmp_output():
+    wl = workloads.build(num_seqs=3, num_heads=32, num_kv_heads=2, head_size=96, block_size=32,
+                         seq_lens=[2600, 700, 1], q_dtype="f16", alibi=True, seed=850)
+    check_decode(wl, run_decode(wl, tmp_dtype=torch.float16), oracle.decode_workload(wl), label="G16 tmp16")
+
+
+@pytest.mark.parametrize("G", [12, 16, 20])
+def test_append(G):
+    from test_parity_append import _check_all
+    wl = workloads.build(num_seqs=4, num_heads=2 * G, num_kv_heads=2, head_size=128, block_size=16,
+                         seq_lens=[1, 700, 2049, 4000], q_dtype="bf16", alibi=True, seed=860 + G)
+    _check_all(wl, f"append G{G}")
+
+
+def test_few_long_rows_fold_partitions():
+    # 2 sequences x 2 kv heads of 40K tokens: fewer rows than CTA slots, so CTAs stream many
+    # partitions and (append entry, tmp_output as scratch) fold them into one row each
+    from test_parity_append import _check_all
+    wl = workloads.build(num_seqs=2, num_heads=32, num_kv_heads=2, head_size=128, block_size=16,
+                         seq_lens=[40000, 23456], q_dtype="f16", alibi=True, seed=870)
+    _check_all(wl, "append G16 few rows")
