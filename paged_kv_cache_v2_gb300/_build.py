@@ -17,7 +17,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libpa_v2.so")
 SOURCES = ["pa_decode.cu"] + [f"pa_phase1_bs{bs}{kv}{form}.cu" for bs in (8, 16, 32) for kv in ("", "_fp8")
-                               for form in ("", "_hs", "_ord")] + ["pa_cache.cu",
+                               for form in ("", "_hs", "_ord", "_pair")] + ["pa_cache.cu",
            "pa_blocks.cu", "pa_prefix.cu", "pa_prefix_f16.cu", "pa_prefix_bf16.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

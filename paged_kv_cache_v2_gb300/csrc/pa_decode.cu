@@ -457,11 +457,13 @@ static Phase1Fn phase1_form(bool bf16, int d, int form) {
     switch (form) {
         case 1: return phase1_select<BS, KVB, 1>(bf16, d);
         case 2: return phase1_select<BS, KVB, 2>(bf16, d);
+        case 3: return phase1_select<BS, KVB, 3>(bf16, d);
         default: return phase1_select<BS, KVB, 0>(bf16, d);
     }
 }
 
-// form: 0 per-tensor scales, 1 per-kv-head scales, 2 per-tensor scales with an ordered grid
+// form: 0 per-tensor scales, 1 per-kv-head scales, 2 per-tensor scales with an ordered grid,
+// 3 per-tensor scales with the cross-warp value reduction in pairs of warps
 static Phase1Fn phase1_for(bool bf16, bool fp8, int d, int bs, int form) {
     switch (bs) {
         case 8: return fp8 ? phase1_form<8, 1>(bf16, d, form) : phase1_form<8, 2>(bf16, d, form);
@@ -571,7 +573,9 @@ cudaError_t pa::read_decode_errors(unsigned int* v, bool reset) {
         phase1_read_errors<8, 2, 1>, phase1_read_errors<16, 2, 1>, phase1_read_errors<32, 2, 1>,
         phase1_read_errors<8, 1, 1>, phase1_read_errors<16, 1, 1>, phase1_read_errors<32, 1, 1>,
         phase1_read_errors<8, 2, 2>, phase1_read_errors<16, 2, 2>, phase1_read_errors<32, 2, 2>,
-        phase1_read_errors<8, 1, 2>, phase1_read_errors<16, 1, 2>, phase1_read_errors<32, 1, 2>};
+        phase1_read_errors<8, 1, 2>, phase1_read_errors<16, 1, 2>, phase1_read_errors<32, 1, 2>,
+        phase1_read_errors<8, 2, 3>, phase1_read_errors<16, 2, 3>, phase1_read_errors<32, 2, 3>,
+        phase1_read_errors<8, 1, 3>, phase1_read_errors<16, 1, 3>, phase1_read_errors<32, 1, 3>};
     unsigned int all = 0;
     for (auto rd : readers) {
         unsigned int w = 0;
@@ -666,6 +670,14 @@ static int ring_override_kib() {
     static const int v = env_int("PA_DECODE_RING_KIB");
     return v;
 }
+// The paired cross-warp reduction where it raises the CTAs an SM (PA_DECODE_PAIR = 0 turns it off)
+static bool pair_enabled() {
+    static const bool v = [] {
+        const char* e = getenv("PA_DECODE_PAIR");
+        return e == nullptr || atoi(e) != 0;
+    }();
+    return v;
+}
 // CTAs per partition (PA_DECODE_SPLIT = 1, 2 or 4), when the grid has one partition per CTA
 static int split_override() {
     static const int v = [] {
@@ -721,16 +733,18 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
     nstage = nstage < 1 ? 1 : (nstage > 8 ? 8 : nstage);
     if (nstage < PA_MIN_STAGES && (uint32_t)PA_MIN_STAGES * kWarps * slot_bytes <= 160u * 1024u) nstage = PA_MIN_STAGES;
     const int red_heads = G < kMaxHeadsPerCta ? G : kMaxHeadsPerCta;
-    auto smem_for = [&](int ns) {
+    // red_rows: rows of the cross-warp value reduction, one a warp (kWarps) or, in form 3, one
+    // a pair of warps
+    auto smem_for = [&](int ns, int red_rows) {
         return (size_t)kWarps * ns * slot_bytes + kWarps * ns * sizeof(uint64_t) +
                (2 * kWarps + 4) * kMaxHeadsPerCta * sizeof(float) +
-               (size_t)kWarps * red_heads * (D + 4) * sizeof(float);
+               (size_t)red_rows * red_heads * (D + 4) * sizeof(float);
     };
     // staged rows of the fused append: 2 x D 16-bit values after the rest
     const size_t app_bytes = a.new_key != nullptr ? (size_t)4 * D : 0;
-    while (nstage > 1 && smem_for(nstage) + app_bytes > (size_t)optin) --nstage;  // a deep ring that does not fit
+    while (nstage > 1 && smem_for(nstage, kWarps) + app_bytes > (size_t)optin) --nstage;  // a deep ring that does not fit
     const uint32_t ring = (uint32_t)kWarps * nstage * slot_bytes;
-    const size_t nrow_off = (smem_for(nstage) + 15) & ~(size_t)15;
+    size_t nrow_off = (smem_for(nstage, kWarps) + 15) & ~(size_t)15;
     size_t smem1 = nrow_off + app_bytes;
 
     Phase1Fn fn = phase1_for(bf16, fp8, D, bs, a.k_scales != nullptr ? 1 : 0);
@@ -739,6 +753,27 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
     if (ensure_smem((const void*)fn, smem1) != cudaSuccess) {
         (void)cudaGetLastError();
         return PA_ERR_CUDA;
+    }
+    // Form 3 (per-tensor scales): the cross-warp value reduction in half the rows (pairs of
+    // warps add into one), where the shared memory it saves lets one more CTA share an SM --
+    // 8 query heads a CTA at head size 128: 81 against 73 KiB, three CTAs an SM instead of two
+    // (16:1 GQA batch, phase 1 69.3 against 84.3 us).  Elsewhere the extra barrier and the
+    // read-modify-write cost 0.3-2% (Llama, ragged MHA, fp8, long-context batches), so the
+    // form is taken only where it raises the CTAs an SM.
+    bool paired = false;
+    if (a.k_scales == nullptr && pair_enabled()) {
+        const size_t off2 = (smem_for(nstage, kWarps / 2) + 15) & ~(size_t)15;
+        Phase1Fn f3 = phase1_for(bf16, fp8, D, bs, 3);
+        int sms0 = 0, per0 = 0, sms3 = 0, per3 = 0;
+        if (f3 != nullptr && occupancy((const void*)fn, kWarps * 32, smem1, &sms0, &per0) == cudaSuccess &&
+            ensure_smem((const void*)f3, off2 + app_bytes) == cudaSuccess &&
+            occupancy((const void*)f3, kWarps * 32, off2 + app_bytes, &sms3, &per3) == cudaSuccess && per3 > per0) {
+            fn = f3;
+            nrow_off = off2;
+            smem1 = off2 + app_bytes;
+            paired = true;
+        }
+        (void)cudaGetLastError();
     }
 
     Phase1Params p1;
@@ -834,7 +869,8 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
     // leaves CTAs of fewer than 4 partitions (the Llama batch: PX 7 of 8) the grid keeps its
     // index order and the 16-wave stride.
     bool ordered = false;
-    if (a.order != nullptr && a.k_scales == nullptr && !few_rows && a.num_seqs >= kOrderMinSeqs && px_override() <= 0) {
+    if (a.order != nullptr && a.k_scales == nullptr && !paired && !few_rows && a.num_seqs >= kOrderMinSeqs &&
+        px_override() <= 0) {
         int64_t px_ord = (int64_t)kOrderedWaves * slots / rows;
         const int64_t px_min = (Pmax + kOrderedMaxParts - 1) / kOrderedMaxParts;
         if (px_ord < px_min) px_ord = px_min;
@@ -843,7 +879,7 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
             PX = px_ord;
             ordered = true;
         }
-    } else if (a.order != nullptr && a.k_scales == nullptr && !few_rows && a.num_seqs >= kOrderMinSeqs) {
+    } else if (a.order != nullptr && a.k_scales == nullptr && !paired && !few_rows && a.num_seqs >= kOrderMinSeqs) {
         ordered = (Pmax + PX - 1) / PX >= 4;  // a stride set for a tuning run
     }
 

@@ -24,6 +24,7 @@ namespace pa {
 
 constexpr int kPartition = 512;
 constexpr int kWarps = PA_PHASE1_WARPS;  // phase-1 warps per CTA
+static_assert(kWarps % 2 == 0, "warps pair up in the cross-warp reduction of phase-1 form 3");
 // phase 1's static shared memory: per warp, the value scale and the two encode divisors
 constexpr int kPhase1StaticSmem = kWarps * 3 * (int)sizeof(float);
 constexpr uint32_t kRingTarget = PA_RING_KIB * 1024u;  // shared-memory page ring per CTA

@@ -178,7 +178,8 @@ __device__ __forceinline__ void append_token(const Phase1Params& p, const uint8_
 #define PA_FP8_MIN_CTAS 3
 #endif
 // FORM 0: per-tensor scales, sequences in grid order; 1: per-kv-head scales (p.k_scales);
-// 2: per-tensor scales, sequence order[blockIdx.z] (p.order).  Form 0 keeps the scale
+// 2: per-tensor scales, sequence order[blockIdx.z] (p.order); 3: per-tensor scales, the
+// cross-warp value reduction in pairs of warps (half its shared memory).  Form 0 keeps the scale
 // factors in the constant bank and the sequence index as blockIdx.z, so its page loop holds
 // no register for them: the kernels run at their register caps, and each of those registers
 // measured 1-3% (fp8 batch, long context) when the forms were one kernel.
@@ -187,6 +188,9 @@ __global__ void __launch_bounds__(kWarps * 32, KVB == 2 ? (D <= 96 ? 16 : 12) / 
                                                         : ((BF16 && D >= 192) ? 8 : 4 * PA_FP8_MIN_CTAS) / kWarps)
 pa_v2_phase1_kernel(const Phase1Params p) {
     constexpr bool HS = FORM == 1, ORD = FORM == 2;
+    // rows of the cross-warp reduction of the value accumulators: one a warp, or (form 3) one
+    // a pair of warps, half the shared memory, where that lets one more CTA share an SM
+    constexpr int RED = FORM == 3 ? kWarps / 2 : kWarps;
     constexpr bool FP8 = (KVB == 1);
     constexpr int NK = (D + 15) / 16;          // 16-wide steps over the head dimension
     constexpr bool HALF_STEP = (D % 16) != 0;  // head_size 120: last step has 8 elements
@@ -312,7 +316,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
     float* fin_l = fin_m + kMaxHeadsPerCta;           // [8] merged exp-sum
     float* fac_o = fin_l + kMaxHeadsPerCta;           // [8] CTA merge: factor on the row so far
     float* fac_n = fac_o + kMaxHeadsPerCta;           // [8] CTA merge: factor on this partition
-    float* red_o = fac_n + kMaxHeadsPerCta;           // [kWarps][nh][D + 4] scaled accumulators
+    float* red_o = fac_n + kMaxHeadsPerCta;           // [RED][nh][D + 4] scaled accumulators
     constexpr int RS = D + 4;
     // CTA merge over several partitions: the running row [nh][D] (only when PX < Pmax)
     float* mrg = reinterpret_cast<float*>(smem + p.mrg_off);
@@ -968,19 +972,43 @@ pa_v2_phase1_kernel(const Phase1Params p) {
                               fac_n[2 * t + 1]);
             }
         }
+        // Each warp's scaled accumulators go to row `warp` of red_o.  Form 3: warps RED ..
+        // kWarps - 1 write theirs to rows 0 .. RED - 1, then warps 0 .. RED - 1 add theirs.
+        if constexpr (RED == kWarps) {
 #pragma unroll
-        for (int mt = 0; mt < NK; ++mt) {
-            const int r0 = mt * 16 + g, r1 = r0 + 8;
-            if (2 * t < nh) {
-                float* base = red_o + (warp * nh + 2 * t) * RS;
-                if (r0 < D) base[r0] = acc[mt][0] * f0;
-                if (r1 < D) base[r1] = acc[mt][2] * f0;
+            for (int mt = 0; mt < NK; ++mt) {
+                const int r0 = mt * 16 + g, r1 = r0 + 8;
+                if (2 * t < nh) {
+                    float* base = red_o + (warp * nh + 2 * t) * RS;
+                    if (r0 < D) base[r0] = acc[mt][0] * f0;
+                    if (r1 < D) base[r1] = acc[mt][2] * f0;
+                }
+                if (2 * t + 1 < nh) {
+                    float* base = red_o + (warp * nh + 2 * t + 1) * RS;
+                    if (r0 < D) base[r0] = acc[mt][1] * f1;
+                    if (r1 < D) base[r1] = acc[mt][3] * f1;
+                }
             }
-            if (2 * t + 1 < nh) {
-                float* base = red_o + (warp * nh + 2 * t + 1) * RS;
-                if (r0 < D) base[r0] = acc[mt][1] * f1;
-                if (r1 < D) base[r1] = acc[mt][3] * f1;
-            }
+        } else {
+            auto put_rows = [&](int row, bool add) {
+#pragma unroll
+                for (int mt = 0; mt < NK; ++mt) {
+                    const int r0 = mt * 16 + g, r1 = r0 + 8;
+                    if (2 * t < nh) {
+                        float* base = red_o + (row * nh + 2 * t) * RS;
+                        if (r0 < D) base[r0] = add ? fmaf(acc[mt][0], f0, base[r0]) : acc[mt][0] * f0;
+                        if (r1 < D) base[r1] = add ? fmaf(acc[mt][2], f0, base[r1]) : acc[mt][2] * f0;
+                    }
+                    if (2 * t + 1 < nh) {
+                        float* base = red_o + (row * nh + 2 * t + 1) * RS;
+                        if (r0 < D) base[r0] = add ? fmaf(acc[mt][1], f1, base[r0]) : acc[mt][1] * f1;
+                        if (r1 < D) base[r1] = add ? fmaf(acc[mt][3], f1, base[r1]) : acc[mt][3] * f1;
+                    }
+                }
+            };
+            if (warp >= RED) put_rows(warp - RED, false);
+            __syncthreads();
+            if (warp < RED) put_rows(warp, true);
         }
         __syncthreads();
 
@@ -1005,7 +1033,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
                     const int hh = e / D, i = e - hh * D;
                     float v = 0.f;
 #pragma unroll
-                    for (int w = 0; w < kWarps; ++w) v += red_o[(w * nh + hh) * RS + i];
+                    for (int w = 0; w < RED; ++w) v += red_o[(w * nh + hh) * RS + i];
                     const float lt = fin_l[hh];
                     st_cluster_f32(dst + 4u * (2 * kMaxHeadsPerCta + e), lt > 0.f ? v * (vmul / lt) : 0.f);
                 }
@@ -1046,7 +1074,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
                 const int hh = e / D, i = e - hh * D;
                 float v = 0.f;
 #pragma unroll
-                for (int w = 0; w < kWarps; ++w) v += red_o[(w * nh + hh) * RS + i];
+                for (int w = 0; w < RED; ++w) v += red_o[(w * nh + hh) * RS + i];
                 const float lt = fin_l[hh];
                 v = lt > 0.f ? v * (vmul / lt) : 0.f;
                 const float fo = fac_o[hh];
@@ -1068,7 +1096,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
                 const int e = 4 * e4, hh = e / D, i = e - hh * D;
                 float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                for (int w = 0; w < kWarps; ++w) {
+                for (int w = 0; w < RED; ++w) {
                     const float4 r = *reinterpret_cast<const float4*>(red_o + (w * nh + hh) * RS + i);
                     v.x += r.x;
                     v.y += r.y;
@@ -1094,7 +1122,7 @@ pa_v2_phase1_kernel(const Phase1Params p) {
                 const int hh = e / D, i = e - hh * D;
                 float v = 0.f;
 #pragma unroll
-                for (int w = 0; w < kWarps; ++w) v += red_o[(w * nh + hh) * RS + i];
+                for (int w = 0; w < RED; ++w) v += red_o[(w * nh + hh) * RS + i];
                 v *= vmul * fac_o[hh];
                 for (int k = 0; k < K - 1; ++k) v = fmaf(pbuf[k * pstride + 2 * kMaxHeadsPerCta + e], pbuf[k * pstride + hh], v);
                 const int64_t row = (int64_t)s * H + h0 + hh;

@@ -5,8 +5,10 @@ over the same pages.
 
 Checked against the fp64 oracle: G from 9 to 32 (partial last groups, two and four groups),
 head sizes 64 to 128 including 120, block sizes 8/16/32, both query dtypes, ALiBi, edge
-lengths, a 16-bit tmp_output, the fused append, and the few-rows grid whose CTAs fold their
-partitions into one row.
+lengths, a 16-bit tmp_output, the fused append, the few-rows grid whose CTAs fold their
+partitions into one row, and fp8 caches at G 8 to 16.  With 8 heads a CTA at head size 128
+the library takes the kernel form whose warps pair up in the cross-warp reduction (three
+CTAs an SM instead of two); the unpaired form is checked there too (PA_DECODE_PAIR=0).
 """
 from __future__ import annotations
 
@@ -74,3 +76,42 @@ def test_few_long_rows_fold_partitions():
     wl = workloads.build(num_seqs=2, num_heads=32, num_kv_heads=2, head_size=128, block_size=16,
                          seq_lens=[40000, 23456], q_dtype="f16", alibi=True, seed=870)
     _check_all(wl, "append G16 few rows")
+
+
+@pytest.mark.parametrize("G,q_dtype,bs", [(8, "f16", 16), (8, "bf16", 32), (16, "bf16", 16), (12, "f16", 8)])
+def test_fp8_cache(G, q_dtype, bs):
+    wl = workloads.build(num_seqs=4, num_heads=2 * G, num_kv_heads=2, head_size=128, block_size=bs,
+                         seq_lens=[1, 513, 1030, 3000], q_dtype=q_dtype, kv_cache_dtype="fp8_e4m3", k_scale=0.05,
+                         v_scale=0.07, alibi=True, seed=890 + G)
+    check_decode(wl, run_decode(wl), oracle.decode_workload(wl), label=f"fp8 G{G} {q_dtype} bs{bs}")
+
+
+_CHILD = r"""
+import sys
+sys.path.insert(0, {here!r}); sys.path.insert(0, {root!r})
+import oracle, workloads
+from gpu_harness import check_decode, run_decode
+from test_parity_append import _check_all
+for spec in {specs!r}:
+    wl = workloads.build(**spec)
+    check_decode(wl, run_decode(wl), oracle.decode_workload(wl), label=f"child decode {{spec}}")
+    _check_all(wl, f"child append {{spec}}")
+print("child ok")
+"""
+
+
+def test_unpaired_reduction_where_the_pairs_would_be_taken():
+    # PA_DECODE_PAIR=0: 8-head CTAs at head size 128 keep one reduction row a warp (two CTAs
+    # an SM); the paired form is what the library takes there by default
+    import os
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    specs = [dict(num_seqs=4, num_heads=32, num_kv_heads=2, head_size=128, block_size=16,
+                  seq_lens=[3000, 1, 700, 2600], q_dtype="bf16", alibi=True, seed=900),
+             dict(num_seqs=3, num_heads=16, num_kv_heads=2, head_size=128, block_size=16,
+                  seq_lens=[5000, 17, 1025], kv_cache_dtype="fp8_e4m3", k_scale=0.05, v_scale=0.07, seed=901)]
+    code = _CHILD.format(here=here, root=os.path.dirname(here), specs=specs)
+    r = subprocess.run([sys.executable, "-c", code], env=dict(os.environ, PA_DECODE_PAIR="0"), capture_output=True,
+                       text=True, timeout=900)
+    assert r.returncode == 0 and "child ok" in r.stdout, r.stdout[-2000:] + r.stderr[-4000:]
