@@ -26,6 +26,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import re
 import statistics
@@ -244,6 +245,8 @@ def combine_ranks(step_bytes: float, ms_per_step: float, device, world: int):
     return float(b.item()), float(t.item())
 
 
+# decode e2e: steps a captured CUDA graph holds
+GRAPH_STEPS = 4
 SLEEP_CYCLES = 2_000_000  # about 1 ms of GPU time at the SM clock
 
 
@@ -511,17 +514,18 @@ def run_ours(args):
         d2h_done = [torch.cuda.Event() for _ in range(2)]
 
         def e2e_pipelined(i0, n):
-            cstream.wait_stream(stream)
+            cur = torch.cuda.current_stream()  # the compute stream (a capture stream in a graph)
+            cstream.wait_stream(cur)
             with torch.cuda.stream(cstream):
                 dbufs[0].copy_(hbuf, non_blocking=True)
                 h2d_done[0].record(cstream)
             for j in range(n):
                 b = j % 2
-                stream.wait_event(h2d_done[b])
+                cur.wait_event(h2d_done[b])
                 if j >= 2:  # the output buffer's previous read-back has finished
-                    stream.wait_event(d2h_done[b])
+                    cur.wait_event(d2h_done[b])
                 step(i0 + j, inps[b], outs[b])
-                step_done[b].record(stream)
+                step_done[b].record(cur)
                 with torch.cuda.stream(cstream):
                     if j + 1 < n:  # the other input buffer was last read by step j-1,
                         # whose read-back below already waited for it on this stream
@@ -530,43 +534,28 @@ def run_ours(args):
                     cstream.wait_event(step_done[b])
                     houts[b].copy_(outs[b], non_blocking=True)
                     d2h_done[b].record(cstream)
-            stream.wait_stream(cstream)
-
-        # Graphs: two steps with their copies per graph, step b's inputs travelling and step
-        # a's output returning while the other step runs; one graph per pair of cache copies
-        # in the rotation, each replayed in turn (one host launch per two steps).
-        def pair(i0):
-            cur = torch.cuda.current_stream()
-            cstream.wait_stream(cur)
-            with torch.cuda.stream(cstream):
-                dbufs[1].copy_(hbuf, non_blocking=True)
-            dbufs[0].copy_(hbuf, non_blocking=True)
-            step(i0, inps[0], outs[0])
-            cur.wait_stream(cstream)  # step b's inputs are in
-            cstream.wait_stream(cur)  # step a is done: its output can leave
-            with torch.cuda.stream(cstream):
-                houts[0].copy_(outs[0], non_blocking=True)
-            step(i0 + 1, inps[1], outs[1])
-            houts[1].copy_(outs[1], non_blocking=True)
             cur.wait_stream(cstream)
 
+        # Graphs: GRAPH_STEPS steps with their copies per graph, pipelined as above inside it;
+        # one graph per stretch of the cache-copy rotation, each replayed in turn (one host
+        # launch per GRAPH_STEPS steps).
         graphs, graph_error = [], None
         if args.graphs:
             try:
-                for k in range(nrot if nrot % 2 else nrot // 2):
-                    pair(2 * k)  # eager once: kernel attributes are set outside the capture
+                for k in range(nrot // math.gcd(nrot, GRAPH_STEPS)):
+                    e2e_pipelined(GRAPH_STEPS * k, GRAPH_STEPS)  # eager once: kernel attributes are set
                     torch.cuda.synchronize()
                     g = torch.cuda.CUDAGraph()
                     with torch.cuda.graph(g):
-                        pair(2 * k)
+                        e2e_pipelined(GRAPH_STEPS * k, GRAPH_STEPS)
                     graphs.append(g)
                 torch.cuda.synchronize()
             except RuntimeError as exc:  # reported in the line; the eager schedules stand
                 graphs, graph_error = [], str(exc).splitlines()[0][:200]
-        n_pairs = -(-args.steps // 2)
+        n_replays = -(-args.steps // GRAPH_STEPS)
 
         def replay_all():
-            for j in range(n_pairs):
+            for j in range(n_replays):
                 graphs[j % len(graphs)].replay()
 
         def timed(fn, nsteps=args.steps):
@@ -593,9 +582,9 @@ def run_ours(args):
                                "eager calls; a second stream, double-buffered: step i+1's inputs in and "
                                "step i's output out while step i runs")}
         if graphs:
-            sched["graphs"] = (timed(replay_all, 2 * n_pairs),
-                               "CUDA graphs of two steps each with their copies (pipelined within the "
-                               "pair), replayed")
+            sched["graphs"] = (timed(replay_all, GRAPH_STEPS * n_replays),
+                               f"CUDA graphs of {GRAPH_STEPS} steps each with their copies (pipelined "
+                               "within the graph), replayed")
         best = min(sched, key=lambda k: sched[k][0])
         e_ms = sched[best][0]
         e2e = {"value": round(all_bytes / (e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
