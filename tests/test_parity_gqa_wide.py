@@ -8,7 +8,8 @@ head sizes 64 to 128 including 120, block sizes 8/16/32, both query dtypes, ALiB
 lengths, a 16-bit tmp_output, the fused append, the few-rows grid whose CTAs fold their
 partitions into one row, and fp8 caches at G 8 to 16.  With 8 heads a CTA at head size 128
 the library takes the kernel form whose warps pair up in the cross-warp reduction (three
-CTAs an SM instead of two); the unpaired form is checked there too (PA_DECODE_PAIR=0).
+CTAs an SM instead of two); the unpaired form is checked there too (PA_DECODE_PAIR=0), and
+the paired one under 2- and 4-CTA clusters per partition and strided grids.
 """
 from __future__ import annotations
 
@@ -114,4 +115,20 @@ def test_unpaired_reduction_where_the_pairs_would_be_taken():
     code = _CHILD.format(here=here, root=os.path.dirname(here), specs=specs)
     r = subprocess.run([sys.executable, "-c", code], env=dict(os.environ, PA_DECODE_PAIR="0"), capture_output=True,
                        text=True, timeout=900)
+    assert r.returncode == 0 and "child ok" in r.stdout, r.stdout[-2000:] + r.stderr[-4000:]
+
+
+@pytest.mark.parametrize("env", [{"PA_DECODE_SPLIT": "2"}, {"PA_DECODE_SPLIT": "4"}, {"PA_DECODE_PX": "2"}])
+def test_paired_reduction_with_cluster_split_and_strides(env):
+    # the paired form under a 2- or 4-CTA cluster per partition (the partners hand their
+    # summed rows to the first CTA) and with CTAs striding over partitions
+    import os
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    specs = [dict(num_seqs=3, num_heads=32, num_kv_heads=2, head_size=128, block_size=16,
+                  seq_lens=[3000, 1, 1400], q_dtype="f16", alibi=True, seed=910)]
+    code = _CHILD.format(here=here, root=os.path.dirname(here), specs=specs)
+    r = subprocess.run([sys.executable, "-c", code], env=dict(os.environ, **env), capture_output=True, text=True,
+                       timeout=900)
     assert r.returncode == 0 and "child ok" in r.stdout, r.stdout[-2000:] + r.stderr[-4000:]
