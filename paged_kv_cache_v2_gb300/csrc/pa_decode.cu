@@ -757,7 +757,7 @@ pa_status pa::launch_decode(const DecodeArgs& a, float* exp_sums, float* max_log
     // Form 3 (per-tensor scales): the cross-warp value reduction in half the rows (pairs of
     // warps add into one), where the shared memory it saves lets one more CTA share an SM --
     // 8 query heads a CTA at head size 128: 81 against 73 KiB, three CTAs an SM instead of two
-    // (16:1 GQA batch, phase 1 69.3 against 84.3 us).  Elsewhere the extra barrier and the
+    // (16:1 GQA batch, phase 1 67.9 against 84.2 us).  Elsewhere the extra barrier and the
     // read-modify-write cost 0.3-2% (Llama, ragged MHA, fp8, long-context batches), so the
     // form is taken only where it raises the CTAs an SM.
     bool paired = false;
