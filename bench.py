@@ -731,9 +731,11 @@ def run_prefix(args):
                                               "block_tables", "query_start_loc", "context_lens")}
     out = torch.empty_like(dev["query"])
     flops = wl.flops()
-    # contexts longer than 16384 tokens are cut into up to 8 parts (the binding's defaults);
+    # contexts longer than 16384 tokens are cut into up to 8 parts (the binding's defaults;
+    # --min-split-keys / --max-splits change them);
     # the workspace for their partial results is allocated once, outside the timed region
-    max_splits = max(1, min(8, -(-wl.block_tables.shape[1] * wl.block_size // pa.PREFIX_SPLIT_KEYS)))
+    split_keys = args.min_split_keys or pa.PREFIX_SPLIT_KEYS
+    max_splits = max(1, min(args.max_splits, -(-wl.block_tables.shape[1] * wl.block_size // split_keys)))
     ws_bytes = pa.prefix_workspace_size(wl.num_seqs, wl.num_heads, wl.num_kv_heads, wl.head_size,
                                         wl.max_query_len, max_splits)
     work = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda") if ws_bytes else None
@@ -741,7 +743,7 @@ def run_prefix(args):
     def call(q, k, v, o):
         pa.pa_prefix(o, q, k, v, dev["key_cache"], dev["value_cache"], dev["block_tables"],
                      dev["query_start_loc"], dev["context_lens"], wl.max_query_len, scale=wl.scale,
-                     workspace=work, max_splits=max_splits)
+                     workspace=work, max_splits=max_splits, min_split_keys=args.min_split_keys)
 
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device="cuda")
     for _ in range(args.warmup):
@@ -756,7 +758,10 @@ def run_prefix(args):
         a.record()
         b.record()
     torch.cuda.synchronize()
-    n_kernels = 2 if max_splits > 1 else 1  # the attention kernel (+ the combine of split contexts)
+    parts = pa.prefix_num_parts(wl.num_heads, wl.num_kv_heads, wl.head_size, dev["query"].dtype, wl.max_query_len,
+                                wl.block_tables.shape[1], wl.block_size, max_splits, args.min_split_keys,
+                                work is not None)
+    n_kernels = 2 if parts > 1 else 1  # the attention kernel (+ the combine of split contexts)
     launches = 0
     with ClockSampler(dev_i) as clocks:
         queue_ahead()
@@ -837,7 +842,7 @@ def run_prefix(args):
                    "head_size": wl.head_size, "block_size": wl.block_size,
                    "context_lens": wl.context_lens.tolist(), "query_lens": wl.query_lens.tolist(),
                    "flops_per_step": flops, "l2": "flushed (256 MiB write) before every timed call",
-                   "max_splits": max_splits, "min_split_keys": pa.PREFIX_SPLIT_KEYS,
+                   "max_splits": max_splits, "min_split_keys": split_keys, "context_parts": parts,
                    "parallelism": f"replicas x{ws} (sequence shards)"},
         "roofline": {"bound": "tensor", "achieved": round(rank_tflops, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(rank_tflops / peak, 4), "traffic": _profiled_traffic(name, "prefix"),
@@ -872,6 +877,10 @@ def main():
     ap.add_argument("--cache-copies", type=int, default=0,
                     help="decode: copies of the K/V caches the steps rotate through (0: at least 2 and enough "
                          "to span 2.5x the L2, so no step finds earlier steps' pages there; 1 for profiler runs)")
+    ap.add_argument("--max-splits", type=int, default=8,
+                    help="prefix: most parts a long context is cut into (1: no split)")
+    ap.add_argument("--min-split-keys", type=int, default=0,
+                    help="prefix: shortest context (keys, a multiple of 64) that is cut (0: the library's 16384)")
     ap.add_argument("--op", choices=["decode", "copy_blocks", "prefix"], default="decode",
                     help="decode: the decode step (default); copy_blocks: the block-copy kernel alone; "
                          "prefix: chunked-prefix attention (--workload prefix_long_gqa|prefix_llama_gqa)")

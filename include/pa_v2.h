@@ -402,8 +402,12 @@ PA_API pa_status pa_swap_blocks(const void* src_cache, void* dst_cache, const in
  *
  * Split contexts (not on the pages; it changes where the work runs, not the result): with a
  * workspace and max_splits > 1, a sequence whose context exceeds min_split_keys tokens
- * (0 = 16384; otherwise a multiple of 64) is cut into at most max_splits equal parts of whole
- * 64-token tiles, each attended by its own CTAs (the chunk goes with the last part).  Each
+ * (a multiple of 64) is cut into at most max_splits equal parts of whole 64-token tiles, each
+ * attended by its own CTAs (the chunk goes with the last part).  min_split_keys = 0 asks for
+ * the library's plan: contexts over 16384 tokens are cut only where one sequence's row tiles
+ * (of all its kv heads) would occupy fewer than half the GPU's SMs, since a grid that already
+ * spreads each sequence over the GPU runs faster unsplit (4 sequences x 1024 new tokens over
+ * contexts up to 96K at head size 256: 2.82 against 3.04 ms cut into up to 7 parts).  Each
  * part leaves its un-normalised output and its rows' (max, sum) in the workspace, and a second
  * kernel merges the parts by the log-sum-exp rule and writes the output rows of those
  * sequences.  Long contexts then spread over the GPU instead of leaving a tail of a few CTAs.
@@ -437,6 +441,16 @@ PA_API pa_status pa_prefix(void* output, const void* query, const void* key, con
  * range. */
 PA_API size_t pa_prefix_workspace_size(int num_seqs, int num_heads, int num_kv_heads,
                                        int head_size, int max_query_len, int max_splits);
+
+/* Parts each context is cut into by a pa_prefix call with these arguments (has_workspace: a
+ * non-NULL workspace is passed), written to *parts: 1 for no cut (one kernel), else the parts
+ * (the attention kernel and the combine).  The library's plan (min_split_keys = 0) depends
+ * on the current device's SM count.  Errors: PA_ERR_INVALID_ARG for a NULL parts or an
+ * argument pa_prefix would reject; PA_ERR_UNSUPPORTED for a dtype or head size it does not
+ * implement; PA_ERR_CUDA when the device cannot be queried. */
+PA_API pa_status pa_prefix_num_parts(int num_heads, int num_kv_heads, int head_size, pa_dtype dtype,
+                                     int max_query_len, int max_blocks_per_seq, int block_size,
+                                     int max_splits, int min_split_keys, int has_workspace, int* parts);
 
 /* Tokens per partition: 512 ("paged_attention_v2_pytorch.py", _PARTITION_SIZE). */
 PA_API int pa_v2_partition_size(void);

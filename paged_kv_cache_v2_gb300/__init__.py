@@ -101,6 +101,8 @@ def load(build_if_missing: bool = True) -> ctypes.CDLL:
                               i32, P, ctypes.c_size_t, i32, i32, P]
     lib.pa_prefix_workspace_size.restype = ctypes.c_size_t
     lib.pa_prefix_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
+    lib.pa_prefix_num_parts.restype = i32
+    lib.pa_prefix_num_parts.argtypes = [i32, i32, i32, i32, i32, i32, i32, i32, i32, i32, ctypes.POINTER(i32)]
     lib.pa_v2_decode_noalloc.restype = i32
     lib.pa_v2_decode_noalloc.argtypes = [P, P, P, P, i32, i32, i32, i32, f32, P, i32, i32, P, i32, i32,
                                          P, i32, i32, f32, f32, P]
@@ -427,11 +429,13 @@ def pa_prefix(output: torch.Tensor, query: torch.Tensor, key: torch.Tensor, valu
     caches in the decode layouts, int32 block_tables [S, W], query_start_loc [S+1],
     context_lens [S].  scale defaults to d^-0.5 as on the pages.
 
-    Contexts longer than min_split_keys (0: 16384) are cut into up to max_splits parts that
-    run on separate CTAs and are merged by a second kernel.  workspace is a uint8 CUDA tensor
-    of at least prefix_workspace_size(...) bytes; when it is None and the tables can hold
-    such a context, one is taken from torch's allocator (max_splits defaults to 8;
-    max_splits=1 turns splitting off)."""
+    Contexts longer than min_split_keys are cut into up to max_splits parts that run on
+    separate CTAs and are merged by a second kernel; min_split_keys=0 takes the library's plan
+    (contexts over 16384 tokens, cut only where one sequence's CTAs would occupy fewer than
+    half the SMs; prefix_num_parts says what a call will do).  workspace is a uint8 CUDA tensor
+    of at least prefix_workspace_size(...) bytes; when it is None and the call would cut a
+    context, one is taken from torch's allocator (max_splits defaults to 8; max_splits=1
+    turns splitting off)."""
     lib = load()
     T, H, d = query.shape
     Hk = key_cache.shape[1]
@@ -456,7 +460,9 @@ def pa_prefix(output: torch.Tensor, query: torch.Tensor, key: torch.Tensor, valu
     if max_splits is None:
         max_splits = 8
     split_keys = min_split_keys or PREFIX_SPLIT_KEYS
-    if workspace is None and max_splits > 1 and block_tables.shape[1] * bs > split_keys:
+    if workspace is None and max_splits > 1 and block_tables.shape[1] * bs > split_keys and prefix_num_parts(
+            H, Hk, d, query.dtype, int(max_query_len), block_tables.shape[1], bs, min(max_splits, 32),
+            int(min_split_keys)) > 1:
         max_splits = min(max_splits, -(-block_tables.shape[1] * bs // split_keys))
         nbytes = prefix_workspace_size(S, H, Hk, d, int(max_query_len), max_splits)
         if nbytes:
@@ -483,6 +489,17 @@ def prefix_workspace_size(num_seqs: int, num_heads: int, num_kv_heads: int, head
     """Bytes of workspace pa_prefix needs to cut contexts into up to max_splits parts."""
     return int(load().pa_prefix_workspace_size(num_seqs, num_heads, num_kv_heads, head_size, max_query_len,
                                                max_splits))
+
+
+def prefix_num_parts(num_heads: int, num_kv_heads: int, head_size: int, dtype: torch.dtype, max_query_len: int,
+                     max_blocks_per_seq: int, block_size: int, max_splits: int = 8, min_split_keys: int = 0,
+                     has_workspace: bool = True) -> int:
+    """Parts each context is cut into by a pa_prefix call with these arguments (1: no cut)."""
+    out = ctypes.c_int(0)
+    _check("pa_prefix_num_parts", load().pa_prefix_num_parts(
+        num_heads, num_kv_heads, head_size, _dt(dtype), max_query_len, max_blocks_per_seq, block_size, max_splits,
+        min_split_keys, 1 if has_workspace else 0, ctypes.byref(out)))
+    return int(out.value)
 
 
 def pa_v2_partition_size() -> int:

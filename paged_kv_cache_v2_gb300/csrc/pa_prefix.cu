@@ -86,6 +86,51 @@ extern "C" size_t pa_prefix_workspace_size(int num_seqs, int num_heads, int num_
     return (size_t)(items * kPfxBM * ((int64_t)head_size * 4 + 8));
 }
 
+// Parts each context is cut into (1: none), for a call with these sizes and a workspace
+// (has_ws): contexts over split_keys tokens (min_split_keys, 0: 16384) into up to max_splits
+// parts, no more than the longest context the tables can hold would use; with min_split_keys
+// = 0 only where one sequence's CTAs (cta_tiles row tiles of each kv head, one attention CTA
+// an SM) would occupy fewer than half the SMs: a grid that already spreads every sequence over
+// the GPU ran faster unsplit (4 sequences x 1024 new tokens over contexts up to 96K, head size
+// 256: 2.82 against 3.04 ms cut into up to 7 parts).
+static pa_status prefix_parts(int64_t cta_tiles, int num_kv_heads, int max_blocks_per_seq, int block_size,
+                              int max_splits, int min_split_keys, bool has_ws, int* parts) {
+    *parts = 1;
+    if (!has_ws || max_splits <= 1) return PA_OK;
+    const int64_t split_tiles = (min_split_keys > 0 ? min_split_keys : kDefaultSplitKeys) / 64;
+    const int64_t max_ctx_tiles = ((int64_t)max_blocks_per_seq * block_size + 63) / 64;
+    if (max_ctx_tiles <= split_tiles) return PA_OK;
+    const int n = (int)std::min<int64_t>(max_splits, (max_ctx_tiles + split_tiles - 1) / split_tiles);
+    if (min_split_keys == 0) {
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return PA_ERR_CUDA;
+        }
+        if (2 * cta_tiles * num_kv_heads >= sms) return PA_OK;
+    }
+    *parts = n;
+    return PA_OK;
+}
+
+extern "C" pa_status pa_prefix_num_parts(int num_heads, int num_kv_heads, int head_size, pa_dtype dtype,
+                                         int max_query_len, int max_blocks_per_seq, int block_size, int max_splits,
+                                         int min_split_keys, int has_workspace, int* parts) {
+    if (parts == nullptr || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads || max_query_len < 0 ||
+        max_blocks_per_seq <= 0 || (block_size != 8 && block_size != 16 && block_size != 32) || max_splits < 1 ||
+        max_splits > kMaxSplits || min_split_keys < 0 || min_split_keys % 64)
+        return PA_ERR_INVALID_ARG;
+    if (dtype != PA_DT_F16 && dtype != PA_DT_BF16) return PA_ERR_UNSUPPORTED;
+    const bool bf16 = dtype == PA_DT_BF16;
+    if ((bf16 ? prefix_select<true>(head_size) : prefix_select<false>(head_size)) == nullptr) return PA_ERR_UNSUPPORTED;
+    const int G = num_heads / num_kv_heads;
+    const int cta_rows = bf16 ? prefix_tile_rows<true>(head_size) : prefix_tile_rows<false>(head_size);
+    const int64_t cta_tiles = ((int64_t)max_query_len * G + cta_rows - 1) / cta_rows;
+    return prefix_parts(cta_tiles, num_kv_heads, max_blocks_per_seq, block_size, max_splits, min_split_keys,
+                        has_workspace != 0, parts);
+}
+
 extern "C" pa_status pa_prefix(void* output, const void* query, const void* key, const void* value,
                                const void* key_cache, const void* value_cache, int num_seqs, int num_heads,
                                int num_kv_heads, int head_size, float scale, const int32_t* block_tables,
@@ -157,11 +202,9 @@ extern "C" pa_status pa_prefix(void* output, const void* query, const void* key,
     p.mt = (int)cta_tiles;
     p.mt_ws = (int)row_tiles;
     p.split_tiles = (min_split_keys > 0 ? min_split_keys : kDefaultSplitKeys) / 64;
-    // no more splits than the longest context the tables can hold would use
-    const int64_t max_ctx_tiles = ((int64_t)max_blocks_per_seq * block_size + 63) / 64;
-    p.nsplit = 1;
-    if (split && max_ctx_tiles > p.split_tiles)
-        p.nsplit = (int)std::min<int64_t>(max_splits, (max_ctx_tiles + p.split_tiles - 1) / p.split_tiles);
+    const pa_status plan = prefix_parts(cta_tiles, num_kv_heads, max_blocks_per_seq, block_size, max_splits,
+                                        min_split_keys, split, &p.nsplit);
+    if (plan != PA_OK) return plan;
     p.ws_o = static_cast<float*>(workspace);
     p.ws_ml = nullptr;
     if (p.nsplit > 1) {

@@ -277,3 +277,22 @@ def test_prefix_ignores_workspace_arguments_when_not_splitting():
     # max_splits <= 1 or no workspace: the split arguments are not looked at
     assert _prefix_raw(max_query_len=0, ws=0x10008, ws_bytes=1, max_splits=1, split_keys=100) == 0
     assert _prefix_raw(max_query_len=0, ws=None, ws_bytes=0, max_splits=8, split_keys=100) == 0
+
+
+def test_prefix_num_parts_host_plan():
+    # no device is touched on these paths: argument checks, no workspace, an explicit split size
+    lib = pa.load()
+    n = ctypes.c_int(-1)
+    F16 = pa.PA_DT_F16
+    assert lib.pa_prefix_num_parts(32, 8, 128, F16, 512, 1024, 16, 8, 0, 1, None) == 1  # no output
+    assert lib.pa_prefix_num_parts(30, 8, 128, F16, 512, 1024, 16, 8, 0, 1, ctypes.byref(n)) == 1  # H % Hk
+    assert lib.pa_prefix_num_parts(32, 8, 128, F16, 512, 1024, 16, 33, 0, 1, ctypes.byref(n)) == 1  # > 32 parts
+    assert lib.pa_prefix_num_parts(32, 8, 128, F16, 512, 1024, 16, 8, 100, 1, ctypes.byref(n)) == 1  # % 64
+    assert lib.pa_prefix_num_parts(32, 8, 100, F16, 512, 1024, 16, 8, 0, 1, ctypes.byref(n)) == 2  # head size
+    assert lib.pa_prefix_num_parts(32, 8, 128, F16, 512, 1024, 16, 8, 0, 0, ctypes.byref(n)) == 0 and n.value == 1
+    assert lib.pa_prefix_num_parts(32, 8, 128, F16, 512, 1024, 16, 1, 0, 1, ctypes.byref(n)) == 0 and n.value == 1
+    # 16384-token tables cut at 4096 keys: 4 parts (at most max_splits)
+    assert lib.pa_prefix_num_parts(32, 8, 128, F16, 512, 1024, 16, 8, 4096, 1, ctypes.byref(n)) == 0 and n.value == 4
+    assert lib.pa_prefix_num_parts(32, 8, 128, F16, 512, 1024, 16, 3, 4096, 1, ctypes.byref(n)) == 0 and n.value == 3
+    # tables no longer than the split size: never cut
+    assert lib.pa_prefix_num_parts(32, 8, 128, F16, 512, 256, 16, 8, 4096, 1, ctypes.byref(n)) == 0 and n.value == 1

@@ -38,15 +38,16 @@ def test_reduced_prefix_workloads_match_oracle(name):
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["prefix_long_gqa", "prefix_llama_gqa"])
 def test_full_size_prefix_sampled(name):
-    # the binding's defaults, as the benchmark runs them (the long contexts are cut into parts);
-    # the long workload also in one part per sequence
+    # the binding's defaults, as the benchmark runs them (the library's plan: the long
+    # workload's sequences each fill the GPU, so nothing is cut); the long workload also cut
+    # into parts (an explicit split size)
     wl = workloads.make_prefix(name)
     rows = prefix_sample_rows(wl, n=40)
     ref = oracle.prefix_workload(wl, rows=rows)
     dev = prefix_to_device(wl)
-    for max_splits in ((None, 1) if name == "prefix_long_gqa" else (None,)):
-        out = run_prefix(wl, dev, max_splits=max_splits)
-        check_prefix(wl, out, ref, rows=rows, label=f"{name} max_splits={max_splits}")
+    for max_splits, keys in (((None, 0), (8, 16384)) if name == "prefix_long_gqa" else ((None, 0),)):
+        out = run_prefix(wl, dev, max_splits=max_splits, min_split_keys=keys)
+        check_prefix(wl, out, ref, rows=rows, label=f"{name} max_splits={max_splits} min_split_keys={keys}")
         assert torch.isfinite(out.float()).all()
         assert pa.pa_get_device_errors() == 0
 
@@ -155,6 +156,20 @@ def test_many_sequences_short_chunks():
 
 
 # ---- contexts cut into parts ----------------------------------------------------------------
+
+def test_library_split_plan():
+    # the library's plan cuts contexts only where one sequence's CTAs would fill less than half
+    # the GPU: a few new tokens over a long context are cut, the long-context prefill is not
+    assert pa.prefix_num_parts(24, 4, 256, torch.float16, 1024, 99328 // 16, 16) == 1
+    n = pa.prefix_num_parts(32, 8, 128, torch.bfloat16, 64, 40960 // 16, 16)
+    assert n == 3  # 40960 tokens in parts of at least 16384: up to 3
+    assert pa.prefix_num_parts(32, 8, 128, torch.bfloat16, 64, 40960 // 16, 16, has_workspace=False) == 1
+    wl = workloads.build_prefix(num_seqs=2, num_heads=32, num_kv_heads=8, head_size=128, block_size=16,
+                                context_lens=[40000, 700], query_lens=[64, 9], q_dtype="bf16", seed=1190)
+    out = run_prefix(wl)  # the binding takes a workspace and the library cuts the long context
+    check_prefix(wl, out, oracle.prefix_workload(wl), label="library plan, cut")
+    assert pa.pa_get_device_errors() == 0
+
 
 @pytest.mark.parametrize("max_splits", [2, 3, 8, 32])
 def test_split_contexts_match_oracle(max_splits):
