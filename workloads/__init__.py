@@ -154,6 +154,13 @@ CONFIGS = {
         lens=("uniform", 4096, 8192), q_dtype="f16", kv_cache_dtype="auto",
         sigma=1.0, alibi=False, seed=1006,
     ),
+    # 8 query heads per kv head (the 64-query / 8-kv-head shape of the larger Llama-style
+    # models): a full MMA tile of heads a CTA.
+    "gqa8_decode": dict(
+        num_seqs=64, num_heads=64, num_kv_heads=8, head_size=128, block_size=16,
+        lens=("uniform", 1, 4096), q_dtype="f16", kv_cache_dtype="auto",
+        sigma=1.0, alibi=False, seed=1008,
+    ),
     # 16 query heads per kv head: more than one MMA tile of heads shares each kv head.
     "gqa16_decode": dict(
         num_seqs=64, num_heads=64, num_kv_heads=4, head_size=128, block_size=16,
@@ -172,6 +179,7 @@ REDUCED = {
     "fp8_kv": dict(num_seqs=6, lens=("uniform", 512, 1800)),
     "mha_alibi_ragged": dict(num_seqs=8, lens=("lognormal", 300.0, 1.0, 2000, {0: 0, 1: 1})),
     "small_batch_gqa": dict(lens=("uniform", 1200, 2600)),
+    "gqa8_decode": dict(num_seqs=4, lens=("uniform", 1, 1600)),
     "gqa16_decode": dict(num_seqs=4, lens=("uniform", 1, 1600)),
 }
 
