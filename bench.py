@@ -694,6 +694,73 @@ def run_copy_blocks(args):
     return 0
 
 
+def run_swap_blocks(args):
+    """Block swaps between the GPU cache and a pinned host cache ("paged_attn.py" swap_blocks):
+    fp16 blocks of 32 KiB (8 kv heads x head size 128 x block size 16), 512 random blocks out
+    (GPU -> host) and 512 in (host -> GPU) per step; bytes = every moved block once.  The
+    roofline's peak is the same bytes moved as one contiguous copy each way, timed in the same
+    run (the host link's rate for large copies)."""
+    import torch
+
+    import paged_kv_cache_v2_gb300 as pa
+
+    torch.cuda.set_device(0)
+    pa.load()
+    NB, pairs = 4096, 512
+    g = torch.Generator().manual_seed(12)
+    gpu = torch.empty((NB, 8, 128, 16), dtype=torch.float16, device="cuda").normal_()
+    host = torch.empty((NB, 8, 128, 16), dtype=torch.float16).pin_memory()
+    host.normal_()
+    block = gpu[0].numel() * 2
+    step_bytes = 2 * pairs * block
+    perms = [torch.randperm(NB, generator=g) for _ in range(2)]
+    outs = [torch.stack([p[:pairs], p[pairs:2 * pairs]], 1).contiguous() for p in perms]
+    ins = [torch.stack([p[2 * pairs:3 * pairs], p[3 * pairs:4 * pairs]], 1).contiguous() for p in perms]
+
+    def step(i):
+        pa.pa_swap_blocks(gpu, host, outs[i % 2])
+        pa.pa_swap_blocks(host, gpu, ins[i % 2])
+
+    dbig = torch.empty(pairs * block, dtype=torch.uint8, device="cuda")
+    hbig = torch.empty(pairs * block, dtype=torch.uint8).pin_memory()
+
+    def contiguous():
+        hbig.copy_(dbig, non_blocking=True)
+        dbig.copy_(hbig, non_blocking=True)
+
+    def timed(fn):
+        for i in range(args.warmup):
+            fn(i)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0 = time.perf_counter()
+        a.record()
+        for i in range(args.steps):
+            fn(i)
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / args.steps, (time.perf_counter() - t0) * 1e3 / args.steps
+
+    with ClockSampler(0) as clocks:
+        ms, host_ms = timed(step)
+        ref_ms, _ = timed(lambda i: contiguous())
+    gbs = step_bytes / (ms * 1e-3) / 1e9
+    ref = step_bytes / (ref_ms * 1e-3) / 1e9
+    print(json.dumps({
+        "metric": "swap_blocks achieved host-link GB/s (blocks out + blocks in), 1 GPU", "value": round(gbs, 1),
+        "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "host_ms_per_step": round(host_ms, 4), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16", "data": "synthetic",
+        "config": {"workload": "swap_blocks 512 blocks out + 512 in, 32 KiB blocks, pinned host cache",
+                   "bytes_per_step": step_bytes},
+        "roofline": {"bound": "host link", "achieved": round(gbs, 1), "peak": round(ref, 1), "unit": "GB/s",
+                     "frac": round(gbs / ref, 4), "traffic": None, "kernel": "pa_swap_blocks_kernel",
+                     "peak_source": "one contiguous copy of the same bytes each way, this run"},
+        # one launch per 480 pairs and direction (the library's kernel path for pinned memory)
+        "gpu_launches": 2 * -(-pairs // 480) * args.steps, "clocks": clocks.summary()}), flush=True)
+    return 0
+
+
 def _tensor_peak():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -881,14 +948,17 @@ def main():
                     help="prefix: most parts a long context is cut into (1: no split)")
     ap.add_argument("--min-split-keys", type=int, default=0,
                     help="prefix: shortest context (keys, a multiple of 64) that is cut (0: the library's 16384)")
-    ap.add_argument("--op", choices=["decode", "copy_blocks", "prefix"], default="decode",
+    ap.add_argument("--op", choices=["decode", "copy_blocks", "swap_blocks", "prefix"], default="decode",
                     help="decode: the decode step (default); copy_blocks: the block-copy kernel alone; "
+                         "swap_blocks: block moves between the GPU cache and a pinned host cache; "
                          "prefix: chunked-prefix attention (--workload prefix_long_gqa|prefix_llama_gqa)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.op == "swap_blocks":
+        return run_swap_blocks(args)
     if args.op == "copy_blocks":
         return run_copy_blocks(args)
     if args.op == "prefix":

@@ -364,8 +364,12 @@ PA_API pa_status pa_copy_blocks(void* const* key_caches, void* const* value_cach
  *   src_cache, dst_cache  device or pinned host memory (any pair the runtime can copy).
  *   block_mapping         HOST int64 [num_pairs][2] (src, dst), checked on the host.
  *   block_bytes > 0; src_num_blocks / dst_num_blocks: blocks in each cache.
- * One cudaMemcpyAsync per pair on `stream`.  Errors: PA_ERR_INVALID_ARG (nothing enqueued)
- * for a bad size or an id out of range; PA_ERR_CUDA if a copy cannot be enqueued.
+ * Where both caches are reachable from the current device (its own memory, managed memory,
+ * or pinned/registered host memory through its device mapping), block_bytes is a multiple of
+ * 16 and both caches are 16-byte aligned, a kernel on `stream` moves the blocks (one launch
+ * per 480 pairs, the pairs in its parameters); otherwise one cudaMemcpyAsync per pair.
+ * Errors: PA_ERR_INVALID_ARG (nothing enqueued) for a bad size or an id out of range;
+ * PA_ERR_CUDA if a copy or launch cannot be enqueued.
  */
 PA_API pa_status pa_swap_blocks(const void* src_cache, void* dst_cache, const int64_t* block_mapping,
                                 int num_pairs, int64_t block_bytes, int src_num_blocks,

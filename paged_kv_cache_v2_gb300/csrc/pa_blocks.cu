@@ -6,8 +6,10 @@
 // copy_blocks: one CTA per (pair, layer); its 256 threads stream the K block and then the V
 // block with 16-byte loads and stores, eight in flight per thread.  Block ids are checked on
 // the device (out-of-range pairs are skipped and flagged) because the mapping lives there.
-// swap_blocks: the mapping is on the host, so each pair becomes one cudaMemcpyAsync of one
-// contiguous block (no batched-copy API is used).
+// swap_blocks: the mapping is on the host.  Where both caches are addressable from the
+// device (device memory, pinned host memory) a kernel moves the blocks with the pairs in its
+// launch parameters; otherwise each pair becomes one cudaMemcpyAsync of one contiguous block
+// (no batched-copy API is used).
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -52,6 +54,54 @@ __global__ void __launch_bounds__(kCopyThreads) pa_copy_blocks_kernel(const Copy
         }
         for (; i < n16; i += kCopyThreads) d[i] = s[i];
     }
+}
+
+// swap_blocks by a kernel: one CTA per pair streams the block with 16-byte loads and stores,
+// eight in flight per thread, reading and writing pinned host memory through its device
+// mapping.  The pairs travel in the launch's parameters (the mapping is on the host).
+constexpr int kSwapPairsPerLaunch = 480;  // 3840 bytes of pairs: within the 4 KiB of parameters
+
+struct SwapParams {
+    const uint8_t* src;
+    uint8_t* dst;
+    int64_t block_bytes;
+    int2 pairs[kSwapPairsPerLaunch];
+};
+
+__global__ void __launch_bounds__(kCopyThreads) pa_swap_blocks_kernel(const SwapParams p) {
+    const int2 pr = p.pairs[blockIdx.x];
+    const int64_t n16 = p.block_bytes / 16;
+    const uint4* s = reinterpret_cast<const uint4*>(p.src) + pr.x * n16;
+    uint4* d = reinterpret_cast<uint4*>(p.dst) + pr.y * n16;
+    int64_t i = threadIdx.x;
+    for (; i + 7 * kCopyThreads < n16; i += 8 * kCopyThreads) {
+        uint4 r[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) r[u] = s[i + u * kCopyThreads];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) d[i + u * kCopyThreads] = r[u];
+    }
+    for (; i < n16; i += kCopyThreads) d[i] = s[i];
+}
+
+// The address under which the current device reaches `ptr`: device memory of the current
+// device (or managed memory) as is, registered or pinned host memory through its device
+// mapping; null for anything else (pageable host memory, another device's memory).
+static const void* device_view(const void* ptr) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, ptr) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    if (at.type == cudaMemoryTypeManaged) return ptr;
+    if (at.type == cudaMemoryTypeDevice) return at.device == dev ? ptr : nullptr;
+    if (at.type == cudaMemoryTypeHost) return at.devicePointer;
+    return nullptr;
 }
 
 }  // namespace pa
@@ -104,6 +154,29 @@ extern "C" pa_status pa_swap_blocks(const void* src_cache, void* dst_cache, cons
     for (int i = 0; i < num_pairs; ++i) {
         const int64_t s = block_mapping[2 * (int64_t)i], d = block_mapping[2 * (int64_t)i + 1];
         if (s < 0 || s >= src_num_blocks || d < 0 || d >= dst_num_blocks) return PA_ERR_INVALID_ARG;
+    }
+    // Both caches addressable from this device and blocks of whole 16-byte chunks: a kernel
+    // moves every block of a launch (one launch per 480 pairs); else one copy per pair, which
+    // costs a couple of microseconds of host time each (512 blocks out and 512 in of 32 KiB:
+    // 16.3 GB/s against 186 GB/s for the same bytes as one copy each way).
+    const void* src_dev = device_view(src_cache);
+    const void* dst_dev = device_view(dst_cache);
+    if (src_dev != nullptr && dst_dev != nullptr && block_bytes % 16 == 0 &&
+        ((reinterpret_cast<uintptr_t>(src_dev) | reinterpret_cast<uintptr_t>(dst_dev)) & 15) == 0 &&
+        src_num_blocks <= 2147483647 && dst_num_blocks <= 2147483647) {
+        SwapParams p;
+        p.src = static_cast<const uint8_t*>(src_dev);
+        p.dst = static_cast<uint8_t*>(const_cast<void*>(dst_dev));
+        p.block_bytes = block_bytes;
+        for (int i0 = 0; i0 < num_pairs; i0 += kSwapPairsPerLaunch) {
+            const int n = num_pairs - i0 < kSwapPairsPerLaunch ? num_pairs - i0 : kSwapPairsPerLaunch;
+            for (int i = 0; i < n; ++i)
+                p.pairs[i] = make_int2((int)block_mapping[2 * (int64_t)(i0 + i)],
+                                       (int)block_mapping[2 * (int64_t)(i0 + i) + 1]);
+            pa_swap_blocks_kernel<<<(unsigned)n, kCopyThreads, 0, stream>>>(p);
+            if (cudaGetLastError() != cudaSuccess) return PA_ERR_CUDA;
+        }
+        return PA_OK;
     }
     const char* src = static_cast<const char*>(src_cache);
     char* dst = static_cast<char*>(dst_cache);

@@ -77,3 +77,41 @@ def test_swap_blocks_rejects_out_of_range_on_host():
     dst = torch.zeros((4, 256), dtype=torch.uint8).pin_memory()
     with pytest.raises(pa.PagedAttentionError):
         pa.pa_swap_blocks(src, dst, torch.tensor([[0, 4]], dtype=torch.int64))
+
+
+@pytest.mark.parametrize("direction", ["h2d", "d2h"])
+def test_swap_blocks_with_pageable_host_memory(direction):
+    # host memory the device cannot address (not pinned): one copy per pair, same result
+    g = torch.Generator().manual_seed(4)
+    shape = (24, 2, 64, 16)
+    src = torch.randint(0, 255, shape, generator=g, dtype=torch.uint8)
+    dst = torch.randint(0, 255, (16,) + shape[1:], generator=g, dtype=torch.uint8)
+    m = torch.tensor([[5, 1], [23, 15], [0, 0]], dtype=torch.int64)
+    want = dst.numpy().copy()
+    oracle.copy_blocks(want, src.numpy(), m)
+    s_dev = src if direction == "h2d" else src.cuda()
+    d_dev = dst.cuda() if direction == "h2d" else dst
+    pa.pa_swap_blocks(s_dev, d_dev, m)
+    torch.cuda.synchronize()
+    assert np.array_equal(d_dev.cpu().numpy(), want)
+
+
+def test_swap_blocks_many_pairs_over_several_launches():
+    # more pairs than one launch carries (480): every block moved, in both directions
+    g = torch.Generator().manual_seed(5)
+    NB = 1200
+    src = torch.randint(0, 255, (NB, 2, 16, 16), generator=g, dtype=torch.uint8).cuda()
+    host = torch.zeros((NB, 2, 16, 16), dtype=torch.uint8).pin_memory()
+    perm = torch.randperm(NB, generator=g)
+    m = torch.stack([perm[:1000], perm[200:1200]], 1).contiguous()
+    want = host.numpy().copy()
+    oracle.copy_blocks(want, src.cpu().numpy(), m)
+    pa.pa_swap_blocks(src, host, m)
+    torch.cuda.synchronize()
+    assert np.array_equal(host.numpy(), want)
+    back = torch.zeros_like(src)
+    pa.pa_swap_blocks(host, back, m[:, [1, 0]].contiguous())
+    torch.cuda.synchronize()
+    want2 = np.zeros_like(want)
+    oracle.copy_blocks(want2, host.numpy(), m[:, [1, 0]].contiguous())
+    assert np.array_equal(back.cpu().numpy(), want2)
