@@ -403,7 +403,14 @@ def run_ours(args):
     nk, nv, slots = wl.new_key.to(dev), wl.new_value.to(dev), wl.slot_mapping.to(dev)
     slopes = None if wl.alibi_slopes is None else wl.alibi_slopes.to(dev)
     out = torch.empty_like(q)
-    es, ml, tmp = pa.workspace(S, H, d, wl.max_seq_len, dev)
+    tmp_dtype = q.dtype if args.tmp_dtype == "q" else torch.float32
+    es, ml, tmp = pa.workspace(S, H, d, wl.max_seq_len, dev, tmp_dtype)
+    # per-tensor scales, or (--head-scales) the same values as one scale per kv head, which
+    # takes the per-head entry points
+    ks, vs = wl.k_scale, wl.v_scale
+    if args.head_scales:
+        ks = torch.full((wl.num_kv_heads,), wl.k_scale, dtype=torch.float32, device=dev)
+        vs = torch.full((wl.num_kv_heads,), wl.v_scale, dtype=torch.float32, device=dev)
     # the fused entry point's arrival counters: zeroed once, left at zero by every call
     ctr = pa.decode_counters(S, H, wl.num_kv_heads, dev) if args.decode == "fused" else None
     # scratch for the append entry's grid order (longest sequences first where CTAs stride);
@@ -419,12 +426,12 @@ def run_ours(args):
         if args.decode == "append":
             # the writer of the newest token fused into the decode
             pa.pa_v2_decode_append(o_, es, ml, tmp, q_, nk_, nv_, kc, vc, wl.num_kv_heads, wl.scale, bt_, sl_,
-                                   wl.block_size, wl.max_seq_len, slopes, wl.kv_cache_dtype, wl.k_scale, wl.v_scale,
+                                   wl.block_size, wl.max_seq_len, slopes, wl.kv_cache_dtype, ks, vs,
                                    order=order)
             return
-        pa.pa_reshape_and_cache(nk_, nv_, kc, vc, slots_, wl.kv_cache_dtype, wl.k_scale, wl.v_scale)
+        pa.pa_reshape_and_cache(nk_, nv_, kc, vc, slots_, wl.kv_cache_dtype, ks, vs)
         pa.pa_v2_decode(o_, es, ml, tmp, q_, kc, vc, wl.num_kv_heads, wl.scale, bt_, sl_, wl.block_size,
-                        wl.max_seq_len, slopes, wl.kv_cache_dtype, wl.k_scale, wl.v_scale, counters=ctr)
+                        wl.max_seq_len, slopes, wl.kv_cache_dtype, ks, vs, counters=ctr)
 
     decode_bytes = wl.algorithmic_bytes()
     step_bytes = decode_bytes + wl.writer_bytes()
@@ -621,6 +628,9 @@ def run_ours(args):
         "dtype": wl.q_dtype if wl.kv_cache_dtype == "auto" else f"{wl.q_dtype}+fp8_e4m3",
         "data": "synthetic (seeded N(0, sigma) values, random block tables)",
         "config": workload_config(args.workload, wl, ws),
+        "scales": "one k_scale / v_scale per kv head (the head-scales entry points)" if args.head_scales
+                  else "per tensor",
+        "tmp_output": "query dtype" if args.tmp_dtype == "q" else "float32",
         "decode_entry": {"append": "pa_v2_decode_append", "fused": "pa_v2_decode_fused"}.get(args.decode,
                                                                                                "pa_v2_decode"),
         "grid_order": "longest-first (pa_v2_decode_order inside the call)" if ordered else "index order",
@@ -939,6 +949,10 @@ def main():
                          "1, the default), pa_v2_decode after pa_reshape_and_cache (two-kernel), or "
                          "pa_v2_decode_fused (the combine by the last CTA inside phase 1 on grids of at most "
                          "two waves; measured slower on every workload here)")
+    ap.add_argument("--head-scales", action="store_true",
+                    help="decode: pass the scales as one per kv head (the head-scales entry points)")
+    ap.add_argument("--tmp-dtype", choices=["f32", "q"], default="f32",
+                    help="decode: tmp_output in float32 (default) or in the query dtype")
     ap.add_argument("--no-order", dest="order", action="store_false",
                     help="decode (append): no grid-order scratch, so the grid serves sequences in index order")
     ap.add_argument("--cache-copies", type=int, default=0,
