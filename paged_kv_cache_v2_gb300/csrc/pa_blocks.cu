@@ -85,8 +85,9 @@ __global__ void __launch_bounds__(kCopyThreads) pa_swap_blocks_kernel(const Swap
 }
 
 // The address under which the current device reaches `ptr`: device memory of the current
-// device (or managed memory) as is, registered or pinned host memory through its device
-// mapping; null for anything else (pageable host memory, another device's memory).
+// device (or managed memory) as is, host memory pinned or registered while the current
+// device was active through its device mapping; null for anything else (pageable host
+// memory, another device's memory, host memory pinned for another device's context).
 static const void* device_view(const void* ptr) {
     cudaPointerAttributes at;
     if (cudaPointerGetAttributes(&at, ptr) != cudaSuccess) {
@@ -100,7 +101,7 @@ static const void* device_view(const void* ptr) {
     }
     if (at.type == cudaMemoryTypeManaged) return ptr;
     if (at.type == cudaMemoryTypeDevice) return at.device == dev ? ptr : nullptr;
-    if (at.type == cudaMemoryTypeHost) return at.devicePointer;
+    if (at.type == cudaMemoryTypeHost) return at.device == dev ? at.devicePointer : nullptr;
     return nullptr;
 }
 
