@@ -366,9 +366,9 @@ PA_API pa_status pa_copy_blocks(void* const* key_caches, void* const* value_cach
  *   block_bytes > 0; src_num_blocks / dst_num_blocks: blocks in each cache.
  * Where both caches are reachable from the current device (its own memory, managed memory,
  * or host memory pinned or registered while it was current, through its device mapping),
- * block_bytes is a multiple of
- * 16 and both caches are 16-byte aligned, a kernel on `stream` moves the blocks (one launch
- * per 480 pairs, the pairs in its parameters); otherwise one cudaMemcpyAsync per pair.
+ * block_bytes is a multiple of 16 and both caches are 16-byte aligned, a kernel on `stream`
+ * moves the blocks (one launch per 480 pairs, the pairs in its parameters); otherwise one
+ * cudaMemcpyAsync per pair.
  * Errors: PA_ERR_INVALID_ARG (nothing enqueued) for a bad size or an id out of range;
  * PA_ERR_CUDA if a copy or launch cannot be enqueued.
  */
