@@ -296,3 +296,47 @@ def test_prefix_num_parts_host_plan():
     assert lib.pa_prefix_num_parts(32, 8, 128, F16, 512, 1024, 16, 3, 4096, 1, ctypes.byref(n)) == 0 and n.value == 3
     # tables no longer than the split size: never cut
     assert lib.pa_prefix_num_parts(32, 8, 128, F16, 512, 256, 16, 8, 4096, 1, ctypes.byref(n)) == 0 and n.value == 1
+
+
+def test_binding_checks_arguments_before_any_device_call():
+    # the ctypes binding rejects what the C ABI cannot take, with CPU tensors, on a machine
+    # without a GPU: nothing reaches the library
+    import torch
+    q = torch.zeros(2, 4, 64, dtype=torch.float16)
+    kc = torch.zeros(8, 2, 8, 16, 8, dtype=torch.float16)
+    vc = torch.zeros(8, 2, 64, 16, dtype=torch.float16)
+    bt = torch.zeros(2, 4, dtype=torch.int32)
+    sl = torch.ones(2, dtype=torch.int32)
+    out = torch.zeros_like(q)
+    es = ml = torch.zeros(2, 4, 1)
+    tmp = torch.zeros(2, 4, 1, 64)
+    # decode: device tensors
+    with pytest.raises(ValueError):
+        pa.pa_v2_decode(out, es, ml, tmp, q, kc, vc, 2, 0.125, bt, sl, 16, 64)
+    # scales: both floats or both per-kv-head float32 CUDA tensors of num_kv_heads values
+    assert pa._head_scales(0.5, 0.25, 2) is None
+    with pytest.raises(TypeError):
+        pa._head_scales(torch.ones(2), 1.0, 2)
+    with pytest.raises(TypeError):
+        pa._head_scales(torch.ones(2), torch.ones(2), 2)    # CPU tensors
+    # block swaps: the mapping is an int64 host tensor [n, 2]
+    src = torch.zeros(4, 256, dtype=torch.uint8)
+    dst = torch.zeros(4, 256, dtype=torch.uint8)
+    with pytest.raises(TypeError):
+        pa.pa_swap_blocks(src, dst, torch.zeros(1, 2, dtype=torch.int32))
+    with pytest.raises(TypeError):
+        pa.pa_swap_blocks(src, dst, torch.zeros(2, dtype=torch.int64))
+    with pytest.raises(ValueError):
+        pa.pa_swap_blocks(src, torch.zeros(4, 128, dtype=torch.uint8), torch.zeros(1, 2, dtype=torch.int64))
+    # prefix: device tensors with dense heads
+    with pytest.raises(ValueError):
+        pa.pa_prefix(out, q, q[:, :2], q[:, :2], kc, vc, bt, torch.zeros(3, dtype=torch.int32),
+                     torch.zeros(2, dtype=torch.int32), 1)
+    # the parts query reports the library's own argument checks
+    with pytest.raises(pa.PagedAttentionError) as e:
+        pa.prefix_num_parts(30, 8, 128, torch.float16, 512, 1024, 16)
+    assert e.value.status == 1
+    with pytest.raises(pa.PagedAttentionError) as e:
+        pa.prefix_num_parts(32, 8, 100, torch.float16, 512, 1024, 16)
+    assert e.value.status == 2
+    assert pa.prefix_num_parts(32, 8, 128, torch.float16, 512, 1024, 16, 8, 4096) == 4
